@@ -1,0 +1,219 @@
+/*
+ * pkv.h -- C ABI of the paged KV-cache library for sm_103a (GB300).
+ *
+ * What the library computes is the decode step of a KV-cached transformer layer over a
+ * paged cache, as the KV-cache pages describe it:
+ *  - "KV cache and PagedAttention", section 1 (The setup): at each generation step the new
+ *    token's K and V are appended to the cache and attention of the new token's query reads
+ *    the whole cached K and V. The "KV Cache" glossary calls these the write phase and the
+ *    read phase.
+ *  - Same page, section 4 (PagedAttention): the cache is a pool of fixed-size pages (16
+ *    tokens); each request has a page table listing its page indices; the attention kernel
+ *    gathers K/V through that table; the allocator is O(1); requests with a common prefix
+ *    share pages.
+ *  - "KV Cache" glossary, GQA and MQA paragraphs: a group of query heads shares one KV head.
+ *  - Section 7 (KV cache quantisation): an FP8 (E4M3) cache at half the memory.
+ *
+ * Conventions for every entry point
+ *  - Return value: PKV_OK (0) or a negative pkv_status. No exception or abort crosses the
+ *    ABI. pkv_last_error() gives a message for the calling thread's last failure.
+ *  - "device" pointers are CUDA device (or managed) memory owned by the caller; "host"
+ *    pointers are ordinary host memory owned by the caller. The library never keeps a
+ *    pointer after a call returns and never allocates device memory.
+ *  - stream is a cudaStream_t (NULL = the legacy default stream). GPU work is enqueued
+ *    asynchronously on it; argument errors are detected on the host before anything is
+ *    launched and nothing is launched then.
+ *  - Device-side faults of the data (a page id or slot outside the pool) never trap: the
+ *    kernel skips the access and sets a bit in the device error word of the current device,
+ *    which pkv_device_error() reads and clears.
+ *
+ * Pool layout (reading: the pages fix none): k_cache and v_cache are each
+ *   [num_pages][num_kv_heads][page_size][head_dim]
+ * elements of cache_dtype, so the 16 rows of one (page, KV head) form one contiguous tile.
+ * Token position p of a request lives in page block_table[p / page_size], row
+ * p % page_size; its slot is page * page_size + row.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_EINVAL = -1,   /* bad argument value (null pointer, negative size, unsupported option) */
+  PKV_ESHAPE = -2,   /* inconsistent sizes (head counts, head_dim, page size) */
+  PKV_EDTYPE = -3,   /* unsupported dtype or dtype combination */
+  PKV_EALIGN = -4,   /* a device pointer is not 16-byte aligned */
+  PKV_ENOPAGES = -5, /* allocator: not enough free pages (nothing was allocated) */
+  PKV_EREFCNT = -6,  /* allocator: page id out of range or reference count would underflow */
+  PKV_ECUDA = -7,    /* a CUDA runtime call failed (message has the CUDA error string) */
+  PKV_EDEVICE = -8,  /* the device error word was non-zero (see pkv_device_error) */
+  PKV_ETIMEOUT = -9  /* reserved: a kernel wait timed out (reported in the error word) */
+} pkv_status;
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
+
+/* Bits of the device error word. */
+enum {
+  PKV_DEVERR_BAD_PAGE = 1, /* a block-table entry outside [0, num_pages), or a context longer
+                              than its block-table row: the page is skipped */
+  PKV_DEVERR_BAD_SLOT = 2, /* a slot outside [0, num_pages * page_size): token not written */
+  PKV_DEVERR_TIMEOUT = 4   /* a bounded wait on a shared-memory barrier gave up */
+};
+
+/* Description of one layer's pair of pools. page_size must be 16; head_dim 64 or 128. */
+typedef struct {
+  int32_t num_pages;
+  int32_t page_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t cache_dtype; /* pkv_dtype */
+} pkv_cache_desc;
+
+/* Message for the calling thread's last failed call ("" if none). Owned by the library. */
+const char* pkv_last_error(void);
+
+/* ABI version of this header: 1. */
+int pkv_version(void);
+
+/*
+ * Write phase ("KV Cache" glossary: new K and V are appended to the cache; PagedAttention
+ * section 4: they land in the request's page). For i < num_tokens and every KV head h:
+ *   k_cache[slot / P][h][slot % P][:] = k_new[i][h][:]   (likewise v), slot = slot_mapping[i]
+ * A negative slot skips token i (padding). A slot >= num_pages * P sets
+ * PKV_DEVERR_BAD_SLOT and skips the token.
+ *  k_new, v_new   device, [num_tokens][num_kv_heads][head_dim] of dtype_new, contiguous,
+ *                 16-byte aligned.
+ *  dtype_new      must equal cache_dtype for F32/BF16 caches; F32 or BF16 for an FP8 cache.
+ *  slot_mapping   device int64 [num_tokens].
+ *  k_cache,v_cache device pools (layout above), 16-byte aligned.
+ *  k_scales, v_scales  device float [num_kv_heads], FP8 cache only (else ignored, may be NULL):
+ *                 the stored code is round-to-nearest-even, saturating to +-448, of the
+ *                 fp32 quotient x / scale[h] (section 7, "fp8 KV (E4M3)"; the rounding and
+ *                 saturation are this library's reading).
+ */
+int pkv_kv_append(const void* k_new, const void* v_new, int32_t dtype_new, int32_t num_tokens,
+                  const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                  const pkv_cache_desc* desc, const float* k_scales, const float* v_scales,
+                  void* stream);
+
+/*
+ * Bytes of device workspace pkv_paged_decode_attention needs for these sizes (0 when the
+ * whole of every sequence is handled in one pass). max_pages_per_seq is the block-table
+ * width. The result depends on the chunk size in force (pkv_decode_set_chunk_pages).
+ */
+size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t max_pages_per_seq);
+
+/*
+ * Read phase: single-token decode attention over the paged cache (section 1: only the new
+ * token's query; attention over all cached K, V -- "cached + new", so context_lens counts
+ * the token appended this step). For request b and query head h, with G = num_q_heads /
+ * num_kv_heads and KV head j = h / G (consecutive groups; reading, the pages give none):
+ *   s_t   = scale * <q[b][h], K_t>            for t < context_lens[b]
+ *   out[b][h] = sum_t softmax(s)_t * V_t
+ * where K_t, V_t are row t % P of page block_tables[b][t / P] (times k_scales[j] /
+ * v_scales[j] for an FP8 cache). Accumulation is fp32. context_lens[b] == 0 gives out = 0.
+ *  q            device [batch][num_q_heads][head_dim] of dtype_q (F32 or BF16).
+ *               F32 q needs an F32 or FP8 cache; BF16 q a BF16 or FP8 cache.
+ *  block_tables device int32 [batch][max_pages_per_seq]; entries past a request's last page
+ *               are not read.
+ *  context_lens device int32 [batch], each <= max_pages_per_seq * 16 (longer ones are cut
+ *               to that and flagged with PKV_DEVERR_BAD_PAGE).
+ *  out          device [batch][num_q_heads][head_dim] of dtype_q.
+ *  workspace    device, >= pkv_decode_workspace_size(...) bytes, 16-byte aligned, or NULL
+ *               when that size is 0. Long contexts are split into chunks of pages whose
+ *               partial results (running max, sum, weighted values) are merged by a second
+ *               kernel in chunk order, so results do not depend on physical page placement.
+ * Requires num_q_heads % num_kv_heads == 0 and G in {1, 2, 4, 8, 16}.
+ */
+int pkv_paged_decode_attention(const void* q, int32_t dtype_q, int32_t batch,
+                               int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                               const pkv_cache_desc* desc, const int32_t* block_tables,
+                               int32_t max_pages_per_seq, const int32_t* context_lens,
+                               float scale, const float* k_scales, const float* v_scales,
+                               void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Per-KV-head scales for an FP8 cache (section 7; granularity is this library's reading):
+ *   scales_out[h] = fp32(max |x[:, h, :]| / 448), or 1 if that maximum is 0.
+ *  x           device [n_tokens][num_kv_heads][head_dim] of dtype (F32 or BF16), 16-byte
+ *              aligned.
+ *  scales_out  device float [num_kv_heads]; overwritten.
+ */
+int pkv_kv_absmax_scales(const void* x, int32_t dtype, int64_t n_tokens, int32_t num_kv_heads,
+                         int32_t head_dim, float* scales_out, void* stream);
+
+/*
+ * Synchronises stream, then reads and clears the current device's error word into
+ * *code_out (host). Returns PKV_OK, or PKV_EDEVICE when the word was non-zero. The word is
+ * shared by every stream of the device in this process.
+ */
+int pkv_device_error(void* stream, int32_t* code_out);
+
+/* Chunk size of the split over pages, in pages (1..4096); 0 restores the automatic choice.
+ * Process-wide; affects calls made after it returns. */
+int pkv_decode_set_chunk_pages(int32_t pages);
+
+/* Chunk size (pages) the decode uses for these sizes under the current setting. */
+int32_t pkv_decode_chunk_pages(int32_t batch, int32_t num_kv_heads, int32_t max_pages_per_seq);
+
+/* ---- host page accounting (no GPU needed) ------------------------------------------------ */
+
+/* Pages a request of n_tokens occupies: the smallest count whose capacity holds it (section 4:
+ * a 17-token request uses 2 pages of 16). */
+int pkv_pages_needed(int64_t n_tokens, int32_t page_size, int64_t* pages_out);
+
+/*
+ * Slots of n tokens: token i is position positions[i] of request requests[i] (requests may be
+ * NULL, meaning request i). slots_out[i] = block_tables[r][p / P] * P + p % P, or -1 when
+ * p < 0. All host arrays. Fails with PKV_EINVAL (slots_out unspecified) when p / P >=
+ * max_pages_per_seq or the table entry is outside [0, num_pages).
+ */
+int pkv_slot_mapping(const int32_t* block_tables, int32_t max_pages_per_seq,
+                     const int32_t* requests, const int64_t* positions, int64_t n,
+                     int32_t page_size, int32_t num_pages, int64_t* slots_out);
+
+/*
+ * Page allocator (section 4: uniform pages, O(1) allocator; shared pages for prefixes).
+ * A LIFO free list plus one reference count per page; every operation is O(1) per page and
+ * all-or-nothing. Not thread-safe: one handle per thread or external locking.
+ */
+typedef struct pkv_allocator pkv_allocator;
+
+/* initial_free_order (host, may be NULL = 0..num_pages-1) lists the pages in the order the
+ * first allocations hand them out. */
+int pkv_allocator_create(int32_t num_pages, const int32_t* initial_free_order,
+                         pkv_allocator** out);
+void pkv_allocator_destroy(pkv_allocator* a);
+/* n pages with reference count 1 into page_ids_out (host); PKV_ENOPAGES if fewer are free. */
+int pkv_alloc(pkv_allocator* a, int32_t n, int32_t* page_ids_out);
+/* One more reference to each listed (allocated) page: sharing a prefix. */
+int pkv_incref(pkv_allocator* a, const int32_t* ids, int32_t n);
+/* One reference less to each listed page; a page reaching 0 returns to the free list.
+ * PKV_EREFCNT (nothing changed) if an id is out of range or would drop below 0. */
+int pkv_decref(pkv_allocator* a, const int32_t* ids, int32_t n);
+int32_t pkv_num_free(const pkv_allocator* a);
+/* Reference count of a page, or -1 for an id out of range. */
+int32_t pkv_refcount(const pkv_allocator* a, int32_t id);
+
+/* ---- tracing --------------------------------------------------------------------------------- */
+
+/* When on, every kernel the library launches is bracketed by a pair of CUDA events on its
+ * stream. pkv_trace_read() synchronises those events and reports, for the kernel family
+ * named ("paged_decode", "decode_combine", "kv_append", "kv_absmax"), the number of launches
+ * and their summed device time in milliseconds since the last reset. pkv_trace_reset() drops
+ * all records. */
+int pkv_trace_enable(int on);
+int pkv_trace_reset(void);
+int pkv_trace_read(const char* kernel, int32_t* launches_out, double* total_ms_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H */

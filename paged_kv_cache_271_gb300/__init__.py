@@ -1,0 +1,294 @@
+"""Paged KV cache for single-token decode attention on GB300 (sm_103a).
+
+A thin ctypes binding over ``libpkv.so`` (C ABI declared in ``include/pkv.h``): argument
+marshalling only, every step of the decode path runs in the library's CUDA kernels. torch
+supplies device memory and streams. The library must have been built (``python -m
+paged_kv_cache_271_gb300.build``); calls fail loudly otherwise -- there is no fallback.
+
+Entry points (same names as the C ABI, without the ``pkv_`` prefix):
+``kv_append``, ``paged_decode_attention``, ``decode_workspace_size``, ``kv_absmax_scales``,
+``device_error``, ``pages_needed``, ``slot_mapping``, ``PageAllocator`` (``pkv_alloc``,
+``pkv_incref``, ``pkv_decref``, ...), ``decode_set_chunk_pages``, ``trace_*``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+__all__ = [
+    "PkvError", "F32", "BF16", "FP8_E4M3", "lib", "library_path", "cache_desc", "kv_append",
+    "decode_workspace_size", "paged_decode_attention", "kv_absmax_scales", "device_error",
+    "decode_set_chunk_pages", "decode_chunk_pages", "pages_needed", "slot_mapping",
+    "PageAllocator", "trace_enable", "trace_reset", "trace_read",
+]
+
+F32, BF16, FP8_E4M3 = 0, 1, 2
+DEVERR_BAD_PAGE, DEVERR_BAD_SLOT, DEVERR_TIMEOUT = 1, 2, 4
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libpkv.so")
+_lib = None
+
+
+class PkvError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__("pkv error %d: %s" % (code, msg))
+        self.code = code
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("cache_dtype", ctypes.c_int32)]
+
+
+def lib():
+    """The loaded C library. Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(library_path):
+        raise RuntimeError("libpkv.so is not built (run `python -m paged_kv_cache_271_gb300.build`"
+                           " or __graft_entry__.build()); there is no fallback path")
+    L = ctypes.CDLL(library_path)
+    vp, i32, i64, f32, dbl, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                  ctypes.c_float, ctypes.c_double, ctypes.c_size_t)
+    D = ctypes.POINTER(_Desc)
+    sig = {
+        "pkv_last_error": (ctypes.c_char_p, []),
+        "pkv_version": (ctypes.c_int, []),
+        "pkv_kv_append": (ctypes.c_int, [vp, vp, i32, i32, vp, vp, vp, D, vp, vp, vp]),
+        "pkv_decode_workspace_size": (sz, [i32, i32, i32, i32, i32]),
+        "pkv_paged_decode_attention": (ctypes.c_int, [vp, i32, i32, i32, vp, vp, D, vp, i32, vp,
+                                                      f32, vp, vp, vp, vp, sz, vp]),
+        "pkv_kv_absmax_scales": (ctypes.c_int, [vp, i32, i64, i32, i32, vp, vp]),
+        "pkv_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32)]),
+        "pkv_decode_set_chunk_pages": (ctypes.c_int, [i32]),
+        "pkv_decode_chunk_pages": (i32, [i32, i32, i32]),
+        "pkv_pages_needed": (ctypes.c_int, [i64, i32, ctypes.POINTER(i64)]),
+        "pkv_slot_mapping": (ctypes.c_int, [vp, i32, vp, vp, i64, i32, i32, vp]),
+        "pkv_allocator_create": (ctypes.c_int, [i32, vp, ctypes.POINTER(vp)]),
+        "pkv_allocator_destroy": (None, [vp]),
+        "pkv_alloc": (ctypes.c_int, [vp, i32, vp]),
+        "pkv_incref": (ctypes.c_int, [vp, vp, i32]),
+        "pkv_decref": (ctypes.c_int, [vp, vp, i32]),
+        "pkv_num_free": (i32, [vp]),
+        "pkv_refcount": (i32, [vp, i32]),
+        "pkv_trace_enable": (ctypes.c_int, [ctypes.c_int]),
+        "pkv_trace_reset": (ctypes.c_int, []),
+        "pkv_trace_read": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(i32),
+                                          ctypes.POINTER(dbl)]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def _check(st: int):
+    if st != 0:
+        raise PkvError(st, lib().pkv_last_error().decode())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return FP8_E4M3
+    raise PkvError(-3, "unsupported dtype %s" % t.dtype)
+
+
+def _dev(t: torch.Tensor, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise PkvError(-1, "%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise PkvError(-1, "%s must be contiguous" % name)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _opt(t, name):
+    return None if t is None else _dev(t, name)
+
+
+def cache_desc(k_cache: torch.Tensor) -> _Desc:
+    """Descriptor of a pool [num_pages, num_kv_heads, page_size, head_dim]; uint8 or
+    float8_e4m3fn pools are FP8 E4M3 caches."""
+    if k_cache.dim() != 4:
+        raise PkvError(-2, "pool must be [num_pages, num_kv_heads, page_size, head_dim]")
+    n, h, p, d = k_cache.shape
+    return _Desc(n, p, h, d, _dtype_code(k_cache))
+
+
+def kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, k_scales=None, v_scales=None,
+              stream=None):
+    """Write phase: k_new/v_new [N, h_kv, d] into the pools at slot_mapping (int64 [N])."""
+    if slot_mapping.dtype != torch.int64:
+        raise PkvError(-3, "slot_mapping must be int64")
+    if k_new.shape != v_new.shape or k_new.dim() != 3:
+        raise PkvError(-2, "k_new and v_new must both be [N, h_kv, d]")
+    if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
+        raise PkvError(-2, "k_cache and v_cache differ")
+    if slot_mapping.numel() != k_new.shape[0]:
+        raise PkvError(-2, "slot_mapping length != number of tokens")
+    desc = cache_desc(k_cache)
+    if k_new.shape[1] != desc.num_kv_heads or k_new.shape[2] != desc.head_dim:
+        raise PkvError(-2, "k_new heads/dims do not match the pool")
+    _check(lib().pkv_kv_append(_dev(k_new, "k_new"), _dev(v_new, "v_new"), _dtype_code(k_new),
+                               k_new.shape[0], _dev(slot_mapping, "slot_mapping"),
+                               _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                               ctypes.byref(desc), _opt(k_scales, "k_scales"),
+                               _opt(v_scales, "v_scales"), _stream(stream)))
+
+
+def decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_pages_per_seq) -> int:
+    return int(lib().pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                               max_pages_per_seq))
+
+
+def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
+                           k_scales=None, v_scales=None, workspace=None, stream=None):
+    """Read phase: decode attention of q [B, h_q, d] over the paged pools; returns out."""
+    if q.dim() != 3:
+        raise PkvError(-2, "q must be [batch, num_q_heads, head_dim]")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise PkvError(-3, "block_tables and context_lens must be int32")
+    B, h_q, d = q.shape
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.numel() != B:
+        raise PkvError(-2, "block_tables must be [batch, max_pages], context_lens [batch]")
+    desc = cache_desc(k_cache)
+    if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
+        raise PkvError(-2, "k_cache and v_cache differ")
+    if d != desc.head_dim:
+        raise PkvError(-2, "q head_dim does not match the pool")
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype:
+        raise PkvError(-2, "out must match q in shape and dtype")
+    maxp = block_tables.shape[1]
+    need = decode_workspace_size(B, h_q, desc.num_kv_heads, d, maxp)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws = _opt(workspace, "workspace")
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().pkv_paged_decode_attention(
+        _dev(q, "q"), _dtype_code(q), B, h_q, _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        ctypes.byref(desc), _dev(block_tables, "block_tables"), maxp,
+        _dev(context_lens, "context_lens"), float(scale), _opt(k_scales, "k_scales"),
+        _opt(v_scales, "v_scales"), _dev(out, "out"), ws, wsb, _stream(stream)))
+    return out
+
+
+def kv_absmax_scales(x, scales_out=None, stream=None):
+    """FP8 scales per KV head: fp32(max|x[:, h, :]| / 448) (1 for an all-zero head)."""
+    if x.dim() != 3:
+        raise PkvError(-2, "x must be [tokens, h_kv, d]")
+    n, h, d = x.shape
+    if scales_out is None:
+        scales_out = torch.empty(h, dtype=torch.float32, device=x.device)
+    _check(lib().pkv_kv_absmax_scales(_dev(x, "x"), _dtype_code(x), n, h, d,
+                                      _dev(scales_out, "scales_out"), _stream(stream)))
+    return scales_out
+
+
+def device_error(stream=None) -> int:
+    """Synchronise, then read and clear the device error word (0 when clean)."""
+    code = ctypes.c_int32(0)
+    st = lib().pkv_device_error(_stream(stream), ctypes.byref(code))
+    if st not in (0, -8):
+        _check(st)
+    return int(code.value)
+
+
+def decode_set_chunk_pages(pages: int):
+    _check(lib().pkv_decode_set_chunk_pages(int(pages)))
+
+
+def decode_chunk_pages(batch, num_kv_heads, max_pages_per_seq) -> int:
+    return int(lib().pkv_decode_chunk_pages(batch, num_kv_heads, max_pages_per_seq))
+
+
+def pages_needed(n_tokens: int, page_size: int = 16) -> int:
+    out = ctypes.c_int64(0)
+    _check(lib().pkv_pages_needed(int(n_tokens), int(page_size), ctypes.byref(out)))
+    return int(out.value)
+
+
+def slot_mapping(block_tables, positions, num_pages, requests=None, page_size=16) -> np.ndarray:
+    """Host slot mapping: int64 slots of (request, position) pairs through host page tables."""
+    bt = np.ascontiguousarray(np.asarray(block_tables, dtype=np.int32))
+    pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64))
+    req = None if requests is None else np.ascontiguousarray(np.asarray(requests, dtype=np.int32))
+    out = np.empty(len(pos), dtype=np.int64)
+    _check(lib().pkv_slot_mapping(bt.ctypes.data, bt.shape[1],
+                                  None if req is None else req.ctypes.data, pos.ctypes.data,
+                                  len(pos), page_size, int(num_pages), out.ctypes.data))
+    return out
+
+
+class PageAllocator:
+    """Host page allocator: O(1) LIFO free list with reference counts (pkv_allocator_*)."""
+
+    def __init__(self, num_pages: int, initial_free_order=None):
+        self._h = ctypes.c_void_p()
+        order = None
+        if initial_free_order is not None:
+            order = np.ascontiguousarray(np.asarray(initial_free_order, dtype=np.int32))
+        _check(lib().pkv_allocator_create(int(num_pages),
+                                          None if order is None else order.ctypes.data,
+                                          ctypes.byref(self._h)))
+        self.num_pages = int(num_pages)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.pkv_allocator_destroy(h)
+            self._h = None
+
+    def alloc(self, n: int) -> np.ndarray:
+        out = np.empty(max(n, 0), dtype=np.int32)
+        _check(lib().pkv_alloc(self._h, int(n), out.ctypes.data if n > 0 else None))
+        return out
+
+    def incref(self, ids):
+        a = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+        _check(lib().pkv_incref(self._h, a.ctypes.data if a.size else None, a.size))
+
+    def decref(self, ids):
+        a = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+        _check(lib().pkv_decref(self._h, a.ctypes.data if a.size else None, a.size))
+
+    def num_free(self) -> int:
+        return int(lib().pkv_num_free(self._h))
+
+    def refcount(self, page_id: int) -> int:
+        return int(lib().pkv_refcount(self._h, int(page_id)))
+
+
+def trace_enable(on: bool = True):
+    _check(lib().pkv_trace_enable(1 if on else 0))
+
+
+def trace_reset():
+    _check(lib().pkv_trace_reset())
+
+
+def trace_read(kernel: str):
+    """(launches, total device ms) for a kernel family since the last reset."""
+    n = ctypes.c_int32(0)
+    ms = ctypes.c_double(0.0)
+    _check(lib().pkv_trace_read(kernel.encode(), ctypes.byref(n), ctypes.byref(ms)))
+    return int(n.value), float(ms.value)

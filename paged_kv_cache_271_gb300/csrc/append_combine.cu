@@ -1,0 +1,250 @@
+// Write phase (KV append, with optional FP8 quantisation), FP8 scale computation, and the
+// split-K combine of decode partials.
+//
+// kv_append: "KV Cache" glossary, write phase -- the new token's K and V are appended to the
+// cache; "KV cache and PagedAttention", section 4 -- they land in a slot of the request's
+// page. One thread moves one 16-byte vector of K and the same vector of V; consecutive
+// threads cover consecutive dims of one (token, KV head) row, so loads and stores are
+// coalesced. FP8: code = cvt.rn.satfinite.e4m3(fp32(x / s)) (section 7, "fp8 KV (E4M3)";
+// per-head scale, round-to-nearest-even and saturation are this library's reading).
+#include <math.h>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+
+template <typename TIN>
+struct Vec16;  // one 16-byte vector of input elements, widened to float
+template <>
+struct Vec16<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void load(const void* p, float (&o)[4]) {
+    float4 v = *reinterpret_cast<const float4*>(p);
+    o[0] = v.x;
+    o[1] = v.y;
+    o[2] = v.z;
+    o[3] = v.w;
+  }
+};
+template <>
+struct Vec16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void load(const void* p, float (&o)[8]) {
+    uint4 v = *reinterpret_cast<const uint4*>(p);
+    o[0] = bf16lo(v.x);
+    o[1] = bf16hi(v.x);
+    o[2] = bf16lo(v.y);
+    o[3] = bf16hi(v.y);
+    o[4] = bf16lo(v.z);
+    o[5] = bf16hi(v.z);
+    o[6] = bf16lo(v.w);
+    o[7] = bf16hi(v.w);
+  }
+};
+
+// Same-type append: a straight 16-byte copy per thread.
+template <typename T>
+__global__ void kv_append_copy_kernel(const AppendArgs a) {
+  constexpr int VEC = 16 / sizeof(T);
+  const int vpr = a.head_dim / VEC;
+  const int64_t total = (int64_t)a.num_tokens * a.h_kv * vpr;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int v = (int)(idx % vpr);
+    const int64_t r = idx / vpr;
+    const int h = (int)(r % a.h_kv);
+    const int64_t i = r / a.h_kv;
+    const int64_t slot = a.slots[i];
+    if (slot < 0) continue;
+    if (slot >= a.num_slots) {
+      atomicOr(a.err, PKV_DEVERR_BAD_SLOT);
+      continue;
+    }
+    const int64_t page = slot / kPageSize, row = slot % kPageSize;
+    const int64_t src = (i * a.h_kv + h) * a.head_dim + (int64_t)v * VEC;
+    const int64_t dst = ((page * a.h_kv + h) * kPageSize + row) * a.head_dim + (int64_t)v * VEC;
+    const uint4 kx = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.k_new) + src);
+    const uint4 vx = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.v_new) + src);
+    *reinterpret_cast<uint4*>(static_cast<T*>(a.k_cache) + dst) = kx;
+    *reinterpret_cast<uint4*>(static_cast<T*>(a.v_cache) + dst) = vx;
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void quantize_store(const float (&x)[N], float s, uint8_t* dst) {
+  uint16_t codes[N / 2];
+#pragma unroll
+  for (int k = 0; k < N / 2; ++k) {
+    const float2 y = make_float2(__fdiv_rn(x[2 * k], s), __fdiv_rn(x[2 * k + 1], s));
+    codes[k] = static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3));
+  }
+  if constexpr (N == 8) {
+    uint2 w;
+    w.x = (uint32_t)codes[0] | ((uint32_t)codes[1] << 16);
+    w.y = (uint32_t)codes[2] | ((uint32_t)codes[3] << 16);
+    *reinterpret_cast<uint2*>(dst) = w;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = (uint32_t)codes[0] | ((uint32_t)codes[1] << 16);
+  }
+}
+
+// FP8 append: read a 16-byte vector of fp32/bf16, quantise with the head's scale, store codes.
+template <typename TIN>
+__global__ void kv_append_fp8_kernel(const AppendArgs a) {
+  constexpr int VEC = Vec16<TIN>::N;
+  const int vpr = a.head_dim / VEC;
+  const int64_t total = (int64_t)a.num_tokens * a.h_kv * vpr;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int v = (int)(idx % vpr);
+    const int64_t r = idx / vpr;
+    const int h = (int)(r % a.h_kv);
+    const int64_t i = r / a.h_kv;
+    const int64_t slot = a.slots[i];
+    if (slot < 0) continue;
+    if (slot >= a.num_slots) {
+      atomicOr(a.err, PKV_DEVERR_BAD_SLOT);
+      continue;
+    }
+    const int64_t page = slot / kPageSize, row = slot % kPageSize;
+    const int64_t src = (i * a.h_kv + h) * a.head_dim + (int64_t)v * VEC;
+    const int64_t dst = ((page * a.h_kv + h) * kPageSize + row) * a.head_dim + (int64_t)v * VEC;
+    float x[VEC];
+    Vec16<TIN>::load(static_cast<const TIN*>(a.k_new) + src, x);
+    quantize_store<VEC>(x, a.k_scales[h], static_cast<uint8_t*>(a.k_cache) + dst);
+    Vec16<TIN>::load(static_cast<const TIN*>(a.v_new) + src, x);
+    quantize_store<VEC>(x, a.v_scales[h], static_cast<uint8_t*>(a.v_cache) + dst);
+  }
+}
+
+// max |x| per KV head: grid.y = head; bits of the non-negative float maximum are combined with
+// an integer atomicMax (order-preserving for non-negative floats).
+template <typename TIN>
+__global__ void kv_absmax_kernel(const TIN* x, int64_t n_tokens, int h_kv, int head_dim,
+                                 unsigned int* bits) {
+  constexpr int VEC = Vec16<TIN>::N;
+  const int h = blockIdx.y;
+  const int vpr = head_dim / VEC;
+  const int64_t total = n_tokens * vpr;
+  float m = 0.f;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = e / vpr;
+    const int v = (int)(e % vpr);
+    float xs[VEC];
+    Vec16<TIN>::load(x + (t * h_kv + h) * head_dim + (int64_t)v * VEC, xs);
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) m = fmaxf(m, fabsf(xs[k]));
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o /= 2) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ float wmax[32];
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float bm = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) bm = fmaxf(bm, wmax[w]);
+    atomicMax(bits + h, __float_as_uint(bm));
+  }
+}
+
+__global__ void kv_scale_finalize_kernel(float* scales, int h_kv) {
+  const int h = blockIdx.x * blockDim.x + threadIdx.x;
+  if (h >= h_kv) return;
+  const float amax = __uint_as_float(reinterpret_cast<unsigned int*>(scales)[h]);
+  scales[h] = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+}
+
+// Merge of the chunk partials of one (b, h): M = max_c m_c, w_c = 2^(m_c - M),
+// out = sum_c w_c acc_c / sum_c w_c l_c, chunks in ascending order.
+template <typename TQ>
+__global__ void decode_combine_kernel(const DecodeArgs a, int head_dim) {
+  const int h = blockIdx.x, b = blockIdx.y, i = threadIdx.x;
+  const int ctx = min(max(0, a.context_lens[b]), a.max_pages * kPageSize);
+  const int pages_seq = (ctx + kPageSize - 1) / kPageSize;
+  const int n_chunks = (pages_seq + a.chunk_pages - 1) / a.chunk_pages;
+  if (n_chunks <= 1 || i >= head_dim) return;
+  const size_t bh = (size_t)b * a.h_q + h;
+  const float* ml = a.ws_ml + bh * a.n_chunk_slots * 2;
+  const float* acc = a.ws_acc + bh * a.n_chunk_slots * head_dim;
+  float M = -INFINITY;
+  for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, ml[2 * c]);
+  float L = 0.f, A = 0.f;
+  if (M != -INFINITY) {
+    for (int c = 0; c < n_chunks; ++c) {
+      const float w = exp2f(ml[2 * c] - M);
+      L = fmaf(w, ml[2 * c + 1], L);
+      A = fmaf(w, acc[(size_t)c * head_dim + i], A);
+    }
+  }
+  store_from_float(static_cast<TQ*>(a.out), bh * head_dim + i, L > 0.f ? A / L : 0.f);
+}
+
+inline int grid_for(int64_t work, int threads) {
+  int64_t blocks = (work + threads - 1) / threads;
+  if (blocks > 152 * 32) blocks = 152 * 32;
+  return (int)(blocks < 1 ? 1 : blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append(const AppendArgs& a, int in_dtype, int cache_dtype, cudaStream_t s) {
+  if (a.num_tokens == 0) return cudaSuccess;
+  const int threads = 256;
+  if (cache_dtype == PKV_FP8_E4M3) {
+    if (in_dtype == PKV_BF16) {
+      const int64_t work = (int64_t)a.num_tokens * a.h_kv * (a.head_dim / 8);
+      kv_append_fp8_kernel<__nv_bfloat16><<<grid_for(work, threads), threads, 0, s>>>(a);
+    } else {
+      const int64_t work = (int64_t)a.num_tokens * a.h_kv * (a.head_dim / 4);
+      kv_append_fp8_kernel<float><<<grid_for(work, threads), threads, 0, s>>>(a);
+    }
+  } else if (cache_dtype == PKV_BF16) {
+    const int64_t work = (int64_t)a.num_tokens * a.h_kv * (a.head_dim / 8);
+    kv_append_copy_kernel<__nv_bfloat16><<<grid_for(work, threads), threads, 0, s>>>(a);
+  } else {
+    const int64_t work = (int64_t)a.num_tokens * a.h_kv * (a.head_dim / 4);
+    kv_append_copy_kernel<float><<<grid_for(work, threads), threads, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_absmax(const void* x, int dtype, int64_t n_tokens, int h_kv, int head_dim,
+                             float* scales_out, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(scales_out, 0, sizeof(float) * h_kv, s);
+  if (e != cudaSuccess) return e;
+  if (n_tokens > 0) {
+    const int threads = 256;
+    const int vec = dtype == PKV_BF16 ? 8 : 4;
+    const int64_t work = n_tokens * (head_dim / vec);
+    int bx = grid_for(work, threads);
+    const int cap = (152 * 8 + h_kv - 1) / h_kv;
+    if (bx > cap) bx = cap < 1 ? 1 : cap;
+    dim3 grid(bx, h_kv);
+    unsigned int* bits = reinterpret_cast<unsigned int*>(scales_out);
+    if (dtype == PKV_BF16)
+      kv_absmax_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(
+          static_cast<const __nv_bfloat16*>(x), n_tokens, h_kv, head_dim, bits);
+    else
+      kv_absmax_kernel<float><<<grid, threads, 0, s>>>(static_cast<const float*>(x), n_tokens,
+                                                       h_kv, head_dim, bits);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  kv_scale_finalize_kernel<<<(h_kv + 127) / 128, 128, 0, s>>>(scales_out, h_kv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_combine(const DecodeArgs& a, int q_dtype, int head_dim, cudaStream_t s) {
+  dim3 grid(a.h_q, a.batch);
+  if (q_dtype == PKV_BF16)
+    decode_combine_kernel<__nv_bfloat16><<<grid, head_dim, 0, s>>>(a, head_dim);
+  else
+    decode_combine_kernel<float><<<grid, head_dim, 0, s>>>(a, head_dim);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,334 @@
+// C ABI of the library: argument checks, the split-over-pages policy, kernel dispatch, the
+// device error word and launch tracing. Every function here returns a pkv_status; argument
+// errors are found on the host before anything is launched.
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "pkv.h"
+#include "pkv_host.h"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+// One word per device: kernels OR PKV_DEVERR_* bits into it instead of trapping.
+__device__ int g_device_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_err_mu;
+int* g_err_ptr[kMaxDevices] = {};
+
+int current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return set_error(PKV_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (*dev < 0 || *dev >= kMaxDevices) return set_error(PKV_ECUDA, "device index %d", *dev);
+  return PKV_OK;
+}
+
+// Device address of the current device's error word (looked up once per device).
+int error_word(int** out) {
+  int dev = 0;
+  int st = current_device(&dev);
+  if (st != PKV_OK) return st;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_device_error);
+    if (e != cudaSuccess)
+      return set_error(PKV_ECUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return PKV_OK;
+}
+
+// ---- tracing --------------------------------------------------------------------------------
+
+struct TraceRec {
+  std::string name;
+  cudaEvent_t begin, end;
+};
+std::atomic<bool> g_trace_on{false};
+std::mutex g_trace_mu;
+std::vector<TraceRec> g_trace;
+
+template <class F>
+cudaError_t traced(const char* name, cudaStream_t s, F&& launch) {
+  if (!g_trace_on.load(std::memory_order_relaxed)) return launch();
+  TraceRec r{name, nullptr, nullptr};
+  cudaError_t e = cudaEventCreate(&r.begin);
+  if (e == cudaSuccess) e = cudaEventCreate(&r.end);
+  if (e != cudaSuccess) return e;
+  cudaEventRecord(r.begin, s);
+  e = launch();
+  cudaEventRecord(r.end, s);
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace.push_back(r);
+  return e;
+}
+
+int cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return PKV_OK;
+  return set_error(PKV_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+std::atomic<int> g_chunk_override{0};
+
+// Pages per chunk (one CTA each). 32 pages (512 tokens) keeps the partials to ~1% of the KV
+// bytes; smaller chunks when batch * kv_heads is too small to give ~1024 CTAs; one chunk when
+// every sequence fits in one.
+int chunk_pages_for(int batch, int h_kv, int max_pages) {
+  const int ov = g_chunk_override.load();
+  if (ov > 0) return ov;
+  int chunk = 32;
+  const long long units = (long long)batch * h_kv;
+  while (chunk > 8 && units * ((max_pages + chunk - 1) / chunk) < 1024) chunk /= 2;
+  if (max_pages <= chunk) chunk = max_pages < 1 ? 1 : max_pages;
+  return chunk;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int check_desc(const pkv_cache_desc* d, const char* who) {
+  if (!d) return set_error(PKV_EINVAL, "%s: desc is NULL", who);
+  if (d->page_size != 16) return set_error(PKV_EINVAL, "%s: page_size must be 16", who);
+  if (d->head_dim != 64 && d->head_dim != 128)
+    return set_error(PKV_ESHAPE, "%s: head_dim must be 64 or 128", who);
+  if (d->num_pages <= 0 || d->num_kv_heads <= 0)
+    return set_error(PKV_ESHAPE, "%s: num_pages and num_kv_heads must be positive", who);
+  if (d->cache_dtype != PKV_F32 && d->cache_dtype != PKV_BF16 && d->cache_dtype != PKV_FP8_E4M3)
+    return set_error(PKV_EDTYPE, "%s: unknown cache dtype %d", who, d->cache_dtype);
+  if ((long long)d->num_pages * d->num_kv_heads * d->page_size >= (1ll << 40))
+    return set_error(PKV_ESHAPE, "%s: pool too large", who);
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+int pkv_decode_set_chunk_pages(int32_t pages) {
+  if (pages < 0 || pages > 4096)
+    return set_error(PKV_EINVAL, "pkv_decode_set_chunk_pages: %d outside [0, 4096]", pages);
+  g_chunk_override.store(pages);
+  return PKV_OK;
+}
+
+int32_t pkv_decode_chunk_pages(int32_t batch, int32_t num_kv_heads, int32_t max_pages_per_seq) {
+  return chunk_pages_for(batch, num_kv_heads, max_pages_per_seq);
+}
+
+size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t max_pages_per_seq) {
+  if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      max_pages_per_seq <= 0)
+    return 0;
+  const int chunk = chunk_pages_for(batch, num_kv_heads, max_pages_per_seq);
+  const size_t slots = (size_t)((max_pages_per_seq + chunk - 1) / chunk);
+  if (slots <= 1) return 0;
+  const size_t rows = (size_t)batch * num_q_heads * slots;
+  return align256(rows * head_dim * sizeof(float)) + align256(rows * 2 * sizeof(float));
+}
+
+int pkv_paged_decode_attention(const void* q, int32_t dtype_q, int32_t batch,
+                               int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                               const pkv_cache_desc* desc, const int32_t* block_tables,
+                               int32_t max_pages_per_seq, const int32_t* context_lens,
+                               float scale, const float* k_scales, const float* v_scales,
+                               void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  const char* who = "pkv_paged_decode_attention";
+  int st = check_desc(desc, who);
+  if (st != PKV_OK) return st;
+  if (batch < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0)
+    return set_error(PKV_EINVAL, "%s: bad batch, head count or table width", who);
+  if (batch == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return set_error(PKV_EINVAL, "%s: null pointer", who);
+  const int h_kv = desc->num_kv_heads, D = desc->head_dim;
+  if (num_q_heads % h_kv != 0)
+    return set_error(PKV_ESHAPE, "%s: num_q_heads %% num_kv_heads != 0", who);
+  const int G = num_q_heads / h_kv;
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)
+    return set_error(PKV_ESHAPE, "%s: group size %d not in {1,2,4,8,16}", who, G);
+  const int kv = desc->cache_dtype;
+  if (dtype_q != PKV_F32 && dtype_q != PKV_BF16)
+    return set_error(PKV_EDTYPE, "%s: q dtype must be F32 or BF16", who);
+  if ((kv == PKV_F32 && dtype_q != PKV_F32) || (kv == PKV_BF16 && dtype_q != PKV_BF16))
+    return set_error(PKV_EDTYPE, "%s: q dtype must match an F32/BF16 cache", who);
+  if (kv == PKV_FP8_E4M3 && (!k_scales || !v_scales))
+    return set_error(PKV_EINVAL, "%s: FP8 cache needs k_scales and v_scales", who);
+  if (!aligned16(k_cache) || !aligned16(v_cache))
+    return set_error(PKV_EALIGN, "%s: pools must be 16-byte aligned", who);
+  if (!(scale == scale)) return set_error(PKV_EINVAL, "%s: scale is NaN", who);
+  if (h_kv > 65535 || batch > 65535)
+    return set_error(PKV_ESHAPE, "%s: batch and kv heads must be <= 65535", who);
+
+  DecodeArgs a{};
+  a.q = q;
+  a.out = out;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.k_scales = k_scales;
+  a.v_scales = v_scales;
+  a.batch = batch;
+  a.h_q = num_q_heads;
+  a.h_kv = h_kv;
+  a.num_pages = desc->num_pages;
+  a.max_pages = max_pages_per_seq;
+  a.chunk_pages = chunk_pages_for(batch, h_kv, max_pages_per_seq);
+  a.n_chunk_slots = (max_pages_per_seq + a.chunk_pages - 1) / a.chunk_pages;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  if (a.n_chunk_slots > 65535) return set_error(PKV_ESHAPE, "%s: too many chunks", who);
+  if (a.n_chunk_slots > 1) {
+    const size_t need = pkv_decode_workspace_size(batch, num_q_heads, h_kv, D, max_pages_per_seq);
+    if (!workspace || workspace_bytes < need)
+      return set_error(PKV_EINVAL, "%s: workspace of %zu bytes needed, %zu given", who, need,
+                       workspace_bytes);
+    if (!aligned16(workspace)) return set_error(PKV_EALIGN, "%s: workspace alignment", who);
+    const size_t rows = (size_t)batch * num_q_heads * a.n_chunk_slots;
+    a.ws_acc = static_cast<float*>(workspace);
+    a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                       align256(rows * D * sizeof(float)));
+  }
+  st = error_word(&a.err);
+  if (st != PKV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = traced("paged_decode", s, [&] {
+    if (kv == PKV_F32) return launch_decode_f32(a, dtype_q, D, G, s);
+    if (kv == PKV_BF16) return launch_decode_bf16(a, dtype_q, D, G, s);
+    return launch_decode_fp8(a, dtype_q, D, G, s);
+  });
+  st = cuda_status(e, "paged_decode launch");
+  if (st != PKV_OK) return st;
+  if (a.n_chunk_slots > 1) {
+    e = traced("decode_combine", s, [&] { return launch_decode_combine(a, dtype_q, D, s); });
+    st = cuda_status(e, "decode_combine launch");
+  }
+  return st;
+}
+
+int pkv_kv_append(const void* k_new, const void* v_new, int32_t dtype_new, int32_t num_tokens,
+                  const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                  const pkv_cache_desc* desc, const float* k_scales, const float* v_scales,
+                  void* stream) {
+  const char* who = "pkv_kv_append";
+  int st = check_desc(desc, who);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return set_error(PKV_EINVAL, "%s: num_tokens < 0", who);
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache)
+    return set_error(PKV_EINVAL, "%s: null pointer", who);
+  const int kv = desc->cache_dtype;
+  if (kv == PKV_FP8_E4M3) {
+    if (dtype_new != PKV_F32 && dtype_new != PKV_BF16)
+      return set_error(PKV_EDTYPE, "%s: FP8 cache takes F32 or BF16 input", who);
+    if (!k_scales || !v_scales) return set_error(PKV_EINVAL, "%s: FP8 cache needs scales", who);
+  } else if (dtype_new != kv) {
+    return set_error(PKV_EDTYPE, "%s: input dtype must equal the cache dtype", who);
+  }
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return set_error(PKV_EALIGN, "%s: inputs and pools must be 16-byte aligned", who);
+  AppendArgs a{};
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.slots = slot_mapping;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.k_scales = k_scales;
+  a.v_scales = v_scales;
+  a.num_tokens = num_tokens;
+  a.h_kv = desc->num_kv_heads;
+  a.head_dim = desc->head_dim;
+  a.num_slots = (int64_t)desc->num_pages * desc->page_size;
+  st = error_word(&a.err);
+  if (st != PKV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = traced("kv_append", s, [&] { return launch_kv_append(a, dtype_new, kv, s); });
+  return cuda_status(e, "kv_append launch");
+}
+
+int pkv_kv_absmax_scales(const void* x, int32_t dtype, int64_t n_tokens, int32_t num_kv_heads,
+                         int32_t head_dim, float* scales_out, void* stream) {
+  const char* who = "pkv_kv_absmax_scales";
+  if (n_tokens < 0 || num_kv_heads <= 0 || (head_dim != 64 && head_dim != 128) || !scales_out ||
+      (n_tokens > 0 && !x))
+    return set_error(PKV_EINVAL, "%s: bad argument", who);
+  if (dtype != PKV_F32 && dtype != PKV_BF16)
+    return set_error(PKV_EDTYPE, "%s: x must be F32 or BF16", who);
+  if (n_tokens > 0 && !aligned16(x)) return set_error(PKV_EALIGN, "%s: x alignment", who);
+  if (reinterpret_cast<uintptr_t>(scales_out) & 3u)
+    return set_error(PKV_EALIGN, "%s: scales_out alignment", who);
+  if (num_kv_heads > 65535) return set_error(PKV_ESHAPE, "%s: too many heads", who);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = traced("kv_absmax", s, [&] {
+    return launch_kv_absmax(x, dtype, n_tokens, num_kv_heads, head_dim, scales_out, s);
+  });
+  return cuda_status(e, "kv_absmax launch");
+}
+
+int pkv_device_error(void* stream, int32_t* code_out) {
+  if (!code_out) return set_error(PKV_EINVAL, "pkv_device_error: code_out is NULL");
+  int* w = nullptr;
+  int st = error_word(&w);
+  if (st != PKV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&v, w, sizeof v, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(w, 0, sizeof v, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  st = cuda_status(e, "pkv_device_error");
+  if (st != PKV_OK) return st;
+  *code_out = v;
+  if (v != 0) return set_error(PKV_EDEVICE, "device error word 0x%x", v);
+  return PKV_OK;
+}
+
+int pkv_trace_enable(int on) {
+  g_trace_on.store(on != 0);
+  return PKV_OK;
+}
+
+int pkv_trace_reset(void) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  for (auto& r : g_trace) {
+    cudaEventSynchronize(r.end);
+    cudaEventDestroy(r.begin);
+    cudaEventDestroy(r.end);
+  }
+  g_trace.clear();
+  return PKV_OK;
+}
+
+int pkv_trace_read(const char* kernel, int32_t* launches_out, double* total_ms_out) {
+  if (!kernel || !launches_out || !total_ms_out)
+    return set_error(PKV_EINVAL, "pkv_trace_read: null pointer");
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  int32_t n = 0;
+  double total = 0.0;
+  for (auto& r : g_trace) {
+    if (r.name != kernel) continue;
+    cudaError_t e = cudaEventSynchronize(r.end);
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.begin, r.end);
+    if (e != cudaSuccess) return cuda_status(e, "pkv_trace_read");
+    ++n;
+    total += ms;
+  }
+  *launches_out = n;
+  *total_ms_out = total;
+  return PKV_OK;
+}
+
+}  // extern "C"

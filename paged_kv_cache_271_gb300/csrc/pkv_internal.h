@@ -1,0 +1,60 @@
+// Internal interface between the C-ABI layer (capi.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct DecodeArgs {
+  const void* q;
+  void* out;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const float* k_scales;  // FP8 cache only
+  const float* v_scales;
+  float* ws_acc;  // [batch][h_q][n_chunk_slots][D] partial weighted values (split only)
+  float* ws_ml;   // [batch][h_q][n_chunk_slots][2] partial (max, sum), log2 domain
+  int* err;       // device error word
+  int batch;
+  int h_q;
+  int h_kv;
+  int num_pages;
+  int max_pages;      // block-table width
+  int chunk_pages;    // pages per chunk (one CTA)
+  int n_chunk_slots;  // grid.x = ceil(max_pages / chunk_pages)
+  float scale_log2;   // softmax scale * log2(e)
+};
+
+struct AppendArgs {
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slots;
+  void* k_cache;
+  void* v_cache;
+  const float* k_scales;
+  const float* v_scales;
+  int* err;
+  int num_tokens;
+  int h_kv;
+  int head_dim;
+  int64_t num_slots;  // num_pages * page_size
+};
+
+// Each returns the launch status. dtype codes are pkv_dtype values.
+cudaError_t launch_decode_f32(const DecodeArgs& a, int q_dtype, int head_dim, int group,
+                              cudaStream_t s);
+cudaError_t launch_decode_bf16(const DecodeArgs& a, int q_dtype, int head_dim, int group,
+                               cudaStream_t s);
+cudaError_t launch_decode_fp8(const DecodeArgs& a, int q_dtype, int head_dim, int group,
+                              cudaStream_t s);
+cudaError_t launch_decode_combine(const DecodeArgs& a, int q_dtype, int head_dim,
+                                  cudaStream_t s);
+cudaError_t launch_kv_append(const AppendArgs& a, int in_dtype, int cache_dtype, cudaStream_t s);
+cudaError_t launch_kv_absmax(const void* x, int dtype, int64_t n_tokens, int h_kv, int head_dim,
+                             float* scales_out, cudaStream_t s);
+
+}  // namespace pkv

@@ -1,0 +1,133 @@
+"""Drives the CUDA library through its public API for a ``workloads.DecodeInputs`` case and
+computes the oracle's answer for the same inputs. Used by the GPU tests and the benchmark."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_cache_271_gb300 as pkv
+from paged_kv_cache_271_gb300.cache import PagedKVCache
+
+POOL_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8}
+
+
+def fill_junk(t: torch.Tensor, seed: int):
+    """Unused pool slots hold random bytes (NaN and Inf patterns included): stale pages."""
+    g = torch.Generator(device=t.device)
+    g.manual_seed(seed)
+    raw = t.view(torch.uint8)
+    raw.copy_(torch.randint(0, 256, raw.shape, dtype=torch.uint8, device=t.device, generator=g))
+
+
+class Scenario:
+    """A decode step set up through the library: pools filled by kv_append via the host
+    allocator and slot mapping, then this step's token appended."""
+
+    def __init__(self, w, device="cuda", share_prefix=True, page_order=None, junk=True):
+        self.w = w
+        self.device = torch.device(device)
+        order = w.page_order if page_order is None else page_order
+        self.scales = None
+        ks = vs = None
+        if w.kv_dtype == "fp8_e4m3":
+            k_all, v_all = self.all_token_rows()
+            ks = pkv.kv_absmax_scales(k_all.to(self.device))
+            vs = pkv.kv_absmax_scales(v_all.to(self.device))
+            self.scales = (ks, vs)
+        self.cache = PagedKVCache(w.num_pages, w.num_kv_heads, w.head_dim,
+                                  POOL_DTYPE[w.kv_dtype], self.device,
+                                  initial_free_order=order, k_scales=ks, v_scales=vs)
+        if junk:
+            fill_junk(self.cache.k, w.fill_seed)
+            fill_junk(self.cache.v, w.fill_seed + 1)
+        self.rids = list(range(w.batch))
+        P = w.page_size
+        shared = bool(w.prefix_len and share_prefix)
+        if shared:
+            owner = -1
+            self.cache.add_request(owner)
+            s = self.cache.reserve([owner], [w.prefix_len])
+            self.cache.write(s, w.prefix_k.to(self.device), w.prefix_v.to(self.device))
+            pages = self.cache.pages[owner][:w.prefix_len // P]
+            for b in self.rids:
+                self.cache.add_request(b, shared_pages=pages, shared_len=w.prefix_len)
+            self.cache.free_request(owner)
+            self.shared_pages = list(pages)
+        else:
+            for b in self.rids:
+                self.cache.add_request(b)
+            self.shared_pages = []
+        # prefill everything except each request's last token
+        skip = w.prefix_len if shared else 0
+        counts = [int(n) - 1 - skip for n in w.context_lens]
+        rows_k, rows_v = [], []
+        for b in self.rids:
+            k, v = w.request_tokens(b)
+            rows_k.append(k[skip:skip + counts[b]])
+            rows_v.append(v[skip:skip + counts[b]])
+        if sum(counts):
+            s = self.cache.reserve(self.rids, counts)
+            self.cache.write(s, torch.cat(rows_k, 0).to(self.device),
+                             torch.cat(rows_v, 0).to(self.device))
+        # this step: append the newest token of every request
+        self.step_slots = self.cache.reserve(self.rids, [1] * w.batch)
+        self.k_new = torch.stack([w.request_tokens(b)[0][-1] for b in self.rids]).to(self.device)
+        self.v_new = torch.stack([w.request_tokens(b)[1][-1] for b in self.rids]).to(self.device)
+        self.slots_dev = torch.from_numpy(self.step_slots).to(self.device)
+        self.q = w.q.to(self.device)
+        self.block_tables = torch.from_numpy(self.cache.block_table_array(self.rids)).to(self.device)
+        self.context_lens = torch.from_numpy(self.cache.context_lens_array(self.rids)).to(self.device)
+        self.out = torch.empty_like(self.q)
+        maxp = self.block_tables.shape[1]
+        need = pkv.decode_workspace_size(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, maxp)
+        self.workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=self.device)
+
+    def all_token_rows(self):
+        """Every K and V row of the workload (prefix once), the set the FP8 scales cover."""
+        w = self.w
+        ks, vs = [w.k_tokens], [w.v_tokens]
+        if w.prefix_len:
+            ks.insert(0, w.prefix_k)
+            vs.insert(0, w.prefix_v)
+        return torch.cat(ks, 0), torch.cat(vs, 0)
+
+    def append(self, stream=None):
+        self.cache.write(self.slots_dev, self.k_new, self.v_new, stream)
+
+    def decode(self, stream=None):
+        ks, vs = self.scales if self.scales else (None, None)
+        return pkv.paged_decode_attention(self.q, self.cache.k, self.cache.v, self.block_tables,
+                                          self.context_lens, self.w.scale, out=self.out,
+                                          k_scales=ks, v_scales=vs, workspace=self.workspace,
+                                          stream=stream)
+
+    def step(self, stream=None):
+        self.append(stream)
+        return self.decode(stream)
+
+
+def oracle_fp8_codes(w):
+    """The oracle's own per-head scales and E4M3 codes for an FP8 workload's tokens."""
+    kf = w.k_tokens.float().numpy()
+    vf = w.v_tokens.float().numpy()
+    ks = oracle.absmax_scales_per_head(kf)
+    vs = oracle.absmax_scales_per_head(vf)
+    kc = np.stack([oracle.quantize_e4m3(kf[:, j], ks[j]) for j in range(kf.shape[1])], 1)
+    vc = np.stack([oracle.quantize_e4m3(vf[:, j], vs[j]) for j in range(vf.shape[1])], 1)
+    return ks, vs, kc, vc
+
+
+def oracle_expected(w, pairs=None, n_threads=0):
+    """The oracle's decode output for w, from its own contiguous tokens (and, for FP8, its own
+    scales and quantiser). float64 [B, h_q, d] or [n_pairs, d]."""
+    if w.kv_dtype != "fp8_e4m3":
+        return oracle.decode_inputs(w, pairs=pairs, n_threads=n_threads)
+    ks, vs, kc, vc = oracle_fp8_codes(w)
+    return oracle.decode_inputs(w, pairs=pairs, n_threads=n_threads, k_scales=ks, v_scales=vs,
+                                k_codes=kc, v_codes=vc)
+
+
+def tolerance(w) -> float:
+    """Max-abs bound for the attention output: 1e-5 for fp32 inputs, 1e-2 otherwise."""
+    return 1e-5 if w.kv_dtype == "f32" and w.q_dtype == "f32" else 1e-2

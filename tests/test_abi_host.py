@@ -1,0 +1,217 @@
+"""The C-ABI library without a GPU: it loads, exports every declared entry point, and its host
+logic (page accounting, slot mapping, allocator, argument checks) agrees with the oracle."""
+import ctypes
+import os
+import re
+import time
+
+import numpy as np
+import pytest
+
+import oracle
+import paged_kv_cache_271_gb300 as pkv
+from paged_kv_cache_271_gb300.cache import PagedKVCache
+
+HEADER_DIR = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_271_gb300 import build
+    build.build()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(HEADER_DIR):
+        if fn.endswith(".h"):
+            src = open(os.path.join(HEADER_DIR, fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names.update(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_entry_point():
+    names = _declared()
+    assert len(names) >= 20
+    L = ctypes.CDLL(pkv.library_path)
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+    assert pkv.lib().pkv_version() == 1
+
+
+@pytest.mark.parametrize("P", [1, 16, 32])
+def test_pages_needed_matches_oracle(P):
+    for n in range(0, 300):
+        assert pkv.pages_needed(n, P) == oracle.pages_needed(n, P)
+
+
+def test_slot_mapping_matches_oracle_bit_exact():
+    rng = np.random.default_rng(0)
+    for _ in range(20):
+        B, W, num_pages, P = rng.integers(1, 9), rng.integers(1, 12), 200, 16
+        bt = rng.integers(0, num_pages, (B, W)).astype(np.int32)
+        n = 100
+        req = rng.integers(0, B, n).astype(np.int32)
+        pos = rng.integers(-2, W * P, n).astype(np.int64)
+        got = pkv.slot_mapping(bt, pos, num_pages, requests=req, page_size=P)
+        ref = oracle.slot_mapping(bt, pos, P, requests=req)
+        np.testing.assert_array_equal(got, ref)
+
+
+def test_slot_mapping_rejects_bad_tables():
+    bt = np.array([[3, 4]], dtype=np.int32)
+    with pytest.raises(pkv.PkvError):
+        pkv.slot_mapping(bt, [32], 10)  # position beyond the table width
+    with pytest.raises(pkv.PkvError):
+        pkv.slot_mapping(np.array([[11]], dtype=np.int32), [0], 10)  # page id outside the pool
+
+
+def test_allocator_fuzz_against_model():
+    rng = np.random.default_rng(1)
+    for trial in range(5):
+        n = int(rng.integers(1, 64))
+        order = rng.permutation(n)
+        a = pkv.PageAllocator(n, order)
+        m = oracle.AllocatorModel(n, order)
+        live = []
+        for _ in range(400):
+            op = rng.integers(0, 3)
+            if op == 0:
+                k = int(rng.integers(0, 8))
+                try:
+                    ref = m.alloc(k)
+                except MemoryError:
+                    with pytest.raises(pkv.PkvError) as e:
+                        a.alloc(k)
+                    assert e.value.code == -5
+                    continue
+                got = a.alloc(k)
+                assert list(got) == ref
+                live.extend(ref)
+            elif op == 1 and live:
+                ids = list(rng.choice(live, size=int(rng.integers(1, 4))))
+                m.incref(ids)
+                a.incref(ids)
+                live.extend(ids)
+            else:
+                ids = list(rng.choice(np.arange(n), size=int(rng.integers(1, 3))))
+                try:
+                    m.decref(ids)
+                except (ValueError, IndexError):
+                    with pytest.raises(pkv.PkvError) as e:
+                        a.decref(ids)
+                    assert e.value.code == -6
+                    continue
+                a.decref(ids)
+                for i in ids:
+                    live.remove(i)
+            assert a.num_free() == m.num_free()
+            for p in range(n):
+                assert a.refcount(p) == m.ref[p]
+            assert a.num_free() + sum(1 for p in range(n) if a.refcount(p) > 0) == n
+
+
+def test_allocator_is_constant_time_per_page():
+    n = 1 << 20
+    a = pkv.PageAllocator(n)
+    t0 = time.perf_counter()
+    ids = a.alloc(n)
+    a.decref(ids)
+    t_big = time.perf_counter() - t0
+    assert a.num_free() == n
+    # one million pages allocated and freed well inside a second: no per-page scans
+    assert t_big < 1.0, t_big
+    with pytest.raises(pkv.PkvError):
+        a.alloc(n + 1)
+    assert a.num_free() == n
+
+
+def test_allocator_rejects_bad_initial_order():
+    with pytest.raises(pkv.PkvError):
+        pkv.PageAllocator(4, [0, 1, 1, 3])
+
+
+def _desc(**kw):
+    d = dict(num_pages=8, page_size=16, num_kv_heads=2, head_dim=64, cache_dtype=pkv.F32)
+    d.update(kw)
+    return pkv._Desc(d["num_pages"], d["page_size"], d["num_kv_heads"], d["head_dim"],
+                     d["cache_dtype"])
+
+
+def _decode_status(desc, dtype_q=pkv.F32, h_q=4, ws=None, wsb=0):
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: every case fails its host checks
+    return pkv.lib().pkv_paged_decode_attention(fake, dtype_q, 2, h_q, fake, fake,
+                                                ctypes.byref(desc), fake, 600, fake, 0.125,
+                                                None, None, fake, ws, wsb, None)
+
+
+def test_decode_argument_errors_are_caught_on_the_host():
+    assert _decode_status(_desc(page_size=8)) == -1
+    assert _decode_status(_desc(head_dim=96)) == -2
+    assert _decode_status(_desc(), h_q=6) == -2  # group 3
+    assert _decode_status(_desc(), dtype_q=pkv.BF16) == -3  # bf16 q on an fp32 cache
+    assert _decode_status(_desc(cache_dtype=pkv.FP8_E4M3)) == -1  # FP8 without scales
+    assert _decode_status(_desc(cache_dtype=7)) == -3
+    # 600 pages per row with batch 2 needs the split, and no workspace was given
+    assert _decode_status(_desc()) == -1
+    assert "workspace" in pkv.lib().pkv_last_error().decode()
+
+
+def test_append_argument_errors_are_caught_on_the_host():
+    fake = ctypes.c_void_p(1 << 20)
+    L = pkv.lib()
+    d = _desc(cache_dtype=pkv.BF16)
+    assert L.pkv_kv_append(fake, fake, pkv.F32, 4, fake, fake, fake, ctypes.byref(d), None, None,
+                           None) == -3
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    assert L.pkv_kv_append(odd, fake, pkv.BF16, 4, fake, fake, fake, ctypes.byref(d), None,
+                           None, None) == -4
+    assert L.pkv_kv_append(fake, fake, pkv.BF16, 0, fake, fake, fake, ctypes.byref(d), None,
+                           None, None) == 0  # nothing to do
+
+
+def test_workspace_size_and_chunk_policy():
+    pkv.decode_set_chunk_pages(0)
+    # Llama-3-8B-shaped batch 64: 32-page chunks over a 256-page table
+    assert pkv.decode_chunk_pages(64, 8, 256) == 32
+    rows = 64 * 32 * 8
+    assert pkv.decode_workspace_size(64, 32, 8, 128, 256) == rows * 128 * 4 + rows * 2 * 4
+    # everything fits one chunk: no workspace
+    assert pkv.decode_workspace_size(2, 4, 2, 64, 3) == 0
+    pkv.decode_set_chunk_pages(2)
+    try:
+        assert pkv.decode_chunk_pages(2, 2, 3) == 2
+        assert pkv.decode_workspace_size(2, 4, 2, 64, 3) > 0
+    finally:
+        pkv.decode_set_chunk_pages(0)
+    with pytest.raises(pkv.PkvError):
+        pkv.decode_set_chunk_pages(-1)
+
+
+def test_cache_bookkeeping_matches_oracle_without_gpu():
+    import torch
+    order = np.random.default_rng(3).permutation(40)
+    c = PagedKVCache(40, 2, 64, torch.float32, device="cpu", initial_free_order=order)
+    m = oracle.AllocatorModel(40, order)
+    c.add_request(0)
+    slots = c.reserve([0], [17])
+    pages = m.alloc(2)
+    assert c.pages[0] == pages
+    np.testing.assert_array_equal(
+        slots, oracle.slot_mapping(np.array([pages]), np.arange(17), requests=np.zeros(17, int)))
+    # a prefix of two full pages shared by two more requests
+    c.add_request(1)
+    c.reserve([1], [32])
+    shared = list(c.pages[1])
+    c.add_request(2, shared_pages=shared, shared_len=32)
+    c.add_request(3, shared_pages=shared, shared_len=32)
+    assert [c.allocator.refcount(p) for p in shared] == [3, 3]
+    s2 = c.reserve([2, 3], [1, 1])
+    assert s2[0] // 16 not in shared and s2[1] // 16 not in shared and s2[0] != s2[1]
+    c.free_request(1)
+    c.free_request(2)
+    assert [c.allocator.refcount(p) for p in shared] == [1, 1]
+    c.free_request(3)
+    c.free_request(0)
+    assert c.allocator.num_free() == 40

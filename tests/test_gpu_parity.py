@@ -1,0 +1,239 @@
+"""CUDA library vs the fp64 CPU oracle, through the C ABI, on seeded synthetic inputs.
+
+Bit-exact for the append (bf16/fp32 copies and FP8 codes), slot mapping and FP8 scales;
+attention output within 1e-5 max-abs for fp32 inputs and 1e-2 for bf16/FP8 inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_271_gb300 as pkv
+import workloads
+from gpu_harness import Scenario, fill_junk, oracle_expected, tolerance
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from paged_kv_cache_271_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+    yield
+    pkv.decode_set_chunk_pages(0)
+
+
+@pytest.fixture(autouse=True)
+def _clean_error_word():
+    pkv.decode_set_chunk_pages(0)
+    pkv.device_error()
+    yield
+    pkv.decode_set_chunk_pages(0)
+
+
+def _max_err(out, ref):
+    return float(np.abs(out.double().cpu().numpy() - ref).max()) if ref.size else 0.0
+
+
+def _run(w, chunk=0, **kw):
+    pkv.decode_set_chunk_pages(chunk)
+    sc = Scenario(w, **kw)
+    out = sc.step().clone()
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    return sc, out
+
+
+# ---- the workloads ------------------------------------------------------------------------------
+
+def test_tiny_ref_parity():
+    w = workloads.tiny_ref()
+    sc, out = _run(w)
+    assert list(sc.context_lens.cpu().numpy()) == [18, 34]
+    assert _max_err(out, oracle_expected(w)) <= 1e-5
+
+
+def test_llama3_8b_batch64_parity_full():
+    w = workloads.llama3_8b_batch64()
+    sc, out = _run(w)
+    err = _max_err(out, oracle_expected(w))
+    assert err <= 1e-2, err
+
+
+def test_llama3_70b_long_context_parity_sampled():
+    w = workloads.llama3_70b_long()
+    sc, out = _run(w)
+    rng = np.random.default_rng(0)
+    pairs = [(b, int(h)) for b in range(w.batch)
+             for h in rng.choice(w.num_q_heads, 6, replace=False)]
+    ref = oracle_expected(w, pairs=pairs)
+    got = np.stack([out[b, h].double().cpu().numpy() for b, h in pairs])
+    assert float(np.abs(got - ref).max()) <= 1e-2
+    # every output is a convex combination of value rows
+    vmax = float(w.v_tokens.float().abs().max())
+    assert bool(torch.isfinite(out).all()) and float(out.float().abs().max()) <= vmax
+
+
+def test_prefix_sharing_parity_and_shared_equals_copied():
+    w = workloads.prefix_sharing()
+    sc, shared = _run(w, share_prefix=True)
+    assert [sc.cache.allocator.refcount(p) for p in sc.shared_pages] == [w.batch] * 125
+    err = _max_err(shared, oracle_expected(w))
+    assert err <= 1e-2, err
+    del sc
+    torch.cuda.empty_cache()
+    _, copied = _run(w, share_prefix=False)
+    assert torch.equal(shared, copied)
+
+
+# ---- shapes, dtypes, split-K and ragged tails ---------------------------------------------------
+
+SHAPES = [
+    # kv dtype, q dtype, h_q, h_kv, d, context lengths
+    ("f32", "f32", 4, 2, 64, [18, 34]),
+    ("f32", "f32", 8, 8, 128, [1, 15, 16, 17, 100]),
+    ("f32", "f32", 16, 1, 64, [33, 200, 7]),
+    ("bf16", "bf16", 32, 8, 128, [1, 16, 17, 31, 32, 33, 511, 512, 513, 1000]),
+    ("bf16", "bf16", 64, 8, 128, [300, 2049, 17]),
+    ("bf16", "bf16", 16, 16, 64, [45, 800]),
+    ("bf16", "bf16", 32, 2, 64, [129, 3]),
+    ("fp8_e4m3", "bf16", 32, 8, 128, [40, 700, 1]),
+    ("fp8_e4m3", "f32", 8, 4, 64, [77, 260]),
+    ("fp8_e4m3", "bf16", 16, 1, 128, [500, 19]),
+]
+
+
+@pytest.mark.parametrize("kv,qd,h_q,h_kv,d,lens", SHAPES)
+@pytest.mark.parametrize("chunk", [0, 1, 3])
+def test_decode_parity_shapes(kv, qd, h_q, h_kv, d, lens, chunk):
+    w = workloads.custom("shape", 9000 + h_q + d + len(lens), len(lens), h_q, h_kv, d, kv, qd,
+                         lens)
+    _, out = _run(w, chunk=chunk)
+    err = _max_err(out, oracle_expected(w))
+    assert err <= tolerance(w), err
+
+
+def test_split_results_do_not_depend_on_physical_pages():
+    w = workloads.llama3_8b_batch64(batch=8)
+    _, a = _run(w)
+    order2 = np.random.default_rng(5).permutation(w.num_pages).astype(np.int32)
+    _, b = _run(w, page_order=order2)
+    assert torch.equal(a, b)
+
+
+def test_zero_length_context_gives_zero_output():
+    w = workloads.custom("zero", 77, 3, 8, 2, 64, "bf16", "bf16", [5, 40, 3])
+    sc = Scenario(w)
+    sc.append()
+    cl = sc.context_lens.clone()
+    cl[1] = 0
+    out = pkv.paged_decode_attention(sc.q, sc.cache.k, sc.cache.v, sc.block_tables, cl, w.scale,
+                                     workspace=sc.workspace)
+    assert pkv.device_error() == 0
+    assert int(torch.count_nonzero(out[1])) == 0
+    ref = oracle_expected(w, pairs=[(0, h) for h in range(8)])
+    assert _max_err(out[0], ref) <= 1e-2
+
+
+# ---- append, scales -------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kv,src", [("f32", "f32"), ("bf16", "bf16"), ("fp8_e4m3", "bf16"),
+                                     ("fp8_e4m3", "f32")])
+def test_append_bit_exact(kv, src):
+    torch.manual_seed(0)
+    num_pages, h_kv, d, N = 24, 4, 128, 150
+    pool_dt = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8}[kv]
+    src_dt = {"f32": torch.float32, "bf16": torch.bfloat16}[src]
+    kc = torch.empty(num_pages, h_kv, 16, d, dtype=pool_dt, device="cuda")
+    vc = torch.empty_like(kc)
+    fill_junk(kc, 1)
+    fill_junk(vc, 2)
+    rng = np.random.default_rng(1)
+    slots = rng.permutation(num_pages * 16)[:N].astype(np.int64)
+    slots[::17] = -1  # padding rows are skipped
+    kn = (torch.randn(N, h_kv, d) * 3).to(src_dt)
+    vn = (torch.randn(N, h_kv, d) * 0.01).to(src_dt)
+    raw = (lambda t: t.view(torch.uint8).cpu().numpy().copy())
+    exp_k, exp_v = raw(kc), raw(vc)
+    ks = vs = None
+    if kv == "fp8_e4m3":
+        ks = torch.tensor([0.01, 0.02, 0.003, 1.0], device="cuda")
+        vs = torch.tensor([1e-4, 2e-5, 3e-5, 0.5], device="cuda")
+        kq = np.stack([oracle.quantize_e4m3(kn.float().numpy()[:, j], ks[j].item())
+                       for j in range(h_kv)], 1)
+        vq = np.stack([oracle.quantize_e4m3(vn.float().numpy()[:, j], vs[j].item())
+                       for j in range(h_kv)], 1)
+    else:
+        kq, vq = kn.view(torch.uint8).numpy(), vn.view(torch.uint8).numpy()
+    # pools viewed as raw bytes: [num_pages, h_kv, 16, d * element bytes]
+    oracle.scatter_append(exp_k, slots, kq)
+    oracle.scatter_append(exp_v, slots, vq)
+    pkv.kv_append(kn.cuda(), vn.cuda(), torch.from_numpy(slots).cuda(), kc, vc, ks, vs)
+    assert pkv.device_error() == 0
+    np.testing.assert_array_equal(raw(kc), exp_k)
+    np.testing.assert_array_equal(raw(vc), exp_v)
+
+
+def test_fp8_quantiser_matches_oracle_on_every_bf16_pattern():
+    bits = torch.arange(0, 65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+    x = bits[~torch.isnan(bits)]
+    n = (x.numel() // 128) * 128
+    x = x[:n].reshape(-1, 1, 128).contiguous()
+    kc = torch.zeros(x.shape[0] // 16 + 1, 1, 16, 128, dtype=torch.uint8, device="cuda")
+    vc = torch.zeros_like(kc)
+    slots = torch.arange(x.shape[0], dtype=torch.int64, device="cuda")
+    for s in (1.0, 0.0123, 9.5):
+        sc = torch.tensor([s], device="cuda")
+        pkv.kv_append(x.cuda(), x.cuda(), slots, kc, vc, sc, sc)
+        got = kc.reshape(-1, 128)[:x.shape[0]].cpu().numpy()
+        ref = oracle.quantize_e4m3(x.float().numpy().reshape(-1, 128), s)
+        np.testing.assert_array_equal(got, ref)
+    assert pkv.device_error() == 0
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_absmax_scales_bit_exact(dt):
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(3000, 8, 128, generator=g) * torch.linspace(0.1, 50, 8)[None, :, None]
+    x[:, 5] = 0  # an all-zero head gets scale 1
+    x = x.to(torch.bfloat16 if dt == "bf16" else torch.float32)
+    got = pkv.kv_absmax_scales(x.cuda()).cpu().numpy()
+    ref = oracle.absmax_scales_per_head(x.float().numpy())
+    np.testing.assert_array_equal(got, ref)
+
+
+# ---- device error word: bad inputs are skipped, never faulted on ---------------------------------
+
+def test_bad_page_id_sets_error_word():
+    w = workloads.custom("badpage", 31, 2, 8, 2, 64, "bf16", "bf16", [40, 20])
+    sc = Scenario(w)
+    sc.append()
+    bt = sc.block_tables.clone()
+    bt[0, 1] = w.num_pages + 5
+    pkv.paged_decode_attention(sc.q, sc.cache.k, sc.cache.v, bt, sc.context_lens, w.scale,
+                               workspace=sc.workspace)
+    assert pkv.device_error() & pkv.DEVERR_BAD_PAGE
+    assert pkv.device_error() == 0  # reading clears it
+
+
+def test_context_longer_than_table_is_cut_and_flagged():
+    w = workloads.custom("longctx", 32, 2, 8, 2, 64, "bf16", "bf16", [40, 20])
+    sc = Scenario(w)
+    sc.append()
+    cl = sc.context_lens.clone()
+    cl[1] = 16 * sc.block_tables.shape[1] + 100
+    pkv.paged_decode_attention(sc.q, sc.cache.k, sc.cache.v, sc.block_tables, cl, w.scale,
+                               workspace=sc.workspace)
+    assert pkv.device_error() & pkv.DEVERR_BAD_PAGE
+
+
+def test_bad_slot_sets_error_word():
+    kc = torch.zeros(4, 2, 16, 64, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    kn = torch.ones(3, 2, 64, dtype=torch.bfloat16, device="cuda")
+    slots = torch.tensor([0, 4 * 16, 5], dtype=torch.int64, device="cuda")
+    pkv.kv_append(kn, kn, slots, kc, vc)
+    assert pkv.device_error() & pkv.DEVERR_BAD_SLOT
+    assert float(kc[0, 0, 0, 0]) == 1.0 and float(kc[0, 0, 5, 0]) == 1.0
