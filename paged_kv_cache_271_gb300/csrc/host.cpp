@@ -10,7 +10,6 @@
 #include <cstdio>
 #include <cstring>
 #include <new>
-#include <unordered_map>
 #include <vector>
 
 #include "pkv.h"
@@ -117,37 +116,42 @@ int pkv_alloc(pkv_allocator* a, int32_t n, int32_t* page_ids_out) {
   return PKV_OK;
 }
 
-static int check_ids(const pkv_allocator* a, const int32_t* ids, int32_t n, bool need_all,
-                     const char* who) {
+static int check_range(const pkv_allocator* a, const int32_t* ids, int32_t n, const char* who) {
   if (!a || n < 0 || (n > 0 && !ids)) return pkv::set_error(PKV_EINVAL, "%s: bad argument", who);
-  std::unordered_map<int32_t, int32_t> count;
-  for (int32_t k = 0; k < n; ++k) {
-    const int32_t id = ids[k];
-    if (id < 0 || id >= a->num_pages)
-      return pkv::set_error(PKV_EREFCNT, "%s: page id %d out of range", who, id);
-    ++count[id];
-  }
-  for (const auto& kv : count) {
-    const int32_t have = a->ref[kv.first];
-    if (have <= 0 || (need_all && have < kv.second))
-      return pkv::set_error(PKV_EREFCNT, "%s: page %d has reference count %d", who, kv.first,
-                            have);
-  }
+  for (int32_t k = 0; k < n; ++k)
+    if (ids[k] < 0 || ids[k] >= a->num_pages)
+      return pkv::set_error(PKV_EREFCNT, "%s: page id %d out of range", who, ids[k]);
   return PKV_OK;
 }
 
 int pkv_incref(pkv_allocator* a, const int32_t* ids, int32_t n) {
-  const int st = check_ids(a, ids, n, false, "pkv_incref");
+  const int st = check_range(a, ids, n, "pkv_incref");
   if (st != PKV_OK) return st;
+  for (int32_t k = 0; k < n; ++k)
+    if (a->ref[ids[k]] <= 0)
+      return pkv::set_error(PKV_EREFCNT, "pkv_incref: page %d is not allocated", ids[k]);
   for (int32_t k = 0; k < n; ++k) ++a->ref[ids[k]];
   return PKV_OK;
 }
 
 int pkv_decref(pkv_allocator* a, const int32_t* ids, int32_t n) {
-  const int st = check_ids(a, ids, n, true, "pkv_decref");
+  const int st = check_range(a, ids, n, "pkv_decref");
   if (st != PKV_OK) return st;
+  // Decrement in place; a page reaching 0 goes back on the free stack. If any count would
+  // drop below 0 (a free page, or an id listed more often than it is referenced), undo the
+  // decrements and pushes made so far, so the call has no effect.
+  size_t pushed = 0;
   for (int32_t k = 0; k < n; ++k) {
-    if (--a->ref[ids[k]] == 0) a->stack.push_back(ids[k]);
+    const int32_t id = ids[k];
+    if (a->ref[id] <= 0) {
+      for (int32_t u = k - 1; u >= 0; --u) ++a->ref[ids[u]];
+      a->stack.resize(a->stack.size() - pushed);
+      return pkv::set_error(PKV_EREFCNT, "pkv_decref: page %d has reference count 0", id);
+    }
+    if (--a->ref[id] == 0) {
+      a->stack.push_back(id);
+      ++pushed;
+    }
   }
   return PKV_OK;
 }
