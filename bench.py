@@ -1,0 +1,450 @@
+"""Benchmark: one decode step of a Llama-3-8B-shaped layer at batch 64 over a paged KV cache.
+
+A step is the whole hot path for one batch: the host computes this step's slots (page
+accounting, slot mapping), ``kv_append`` writes the new token of each request into its page,
+and ``paged_decode_attention`` attends each request's query over its whole cached context
+(decode kernel plus, for split sequences, the combine kernel). Inputs are seeded synthetic
+tensors (N(0, 1) bf16, context lengths U[512, 4096]) already resident in HBM; the L2 is flushed
+(a 256 MiB write) before every timed step, outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0. ``value`` is algorithmic HBM bytes per step (K and V of every
+attended token, the queries, the outputs, and the appended rows) over the step time, summed
+over ranks (replicas: every rank runs its own batch; no collective on the data path).
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+METRIC = ("paged-decode achieved HBM GB/s (% of GB300 peak) and decode tokens/s at batch 64")
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload():
+    import workloads
+    return workloads.llama3_8b_batch64()
+
+
+def config_of(w):
+    return {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
+            "kv_dtype": w.kv_dtype, "context_lens": "U[512,4096] seeded, sum %d"
+            % int(np.sum(w.context_lens)), "pool_pages": w.num_pages,
+            "l2": "flushed with a 256 MiB write before every timed step",
+            "step": "slot mapping (host) + kv_append + paged_decode_attention"}
+
+
+def decode_bytes(w):
+    """KV of every attended token + queries + outputs (bytes)."""
+    kvb = {"f32": 4, "bf16": 2, "fp8_e4m3": 1}[w.kv_dtype]
+    qb = {"f32": 4, "bf16": 2}[w.q_dtype]
+    kv = int(np.sum(w.context_lens.astype(np.int64))) * w.num_kv_heads * w.head_dim * kvb * 2
+    return kv + 2 * w.batch * w.num_q_heads * w.head_dim * qb
+
+
+def append_bytes(w):
+    kvb = {"f32": 4, "bf16": 2, "fp8_e4m3": 1}[w.kv_dtype]
+    inb = 4 if w.kv_dtype == "f32" else 2
+    return 2 * w.batch * w.num_kv_heads * w.head_dim * (inb + kvb)
+
+
+# ---- ranks -------------------------------------------------------------------------------------
+
+def rank_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(world_size, backend):
+    import torch.distributed as dist
+    if world_size > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The maximum of x over all ranks (x itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(bytes_per_rank_step: float, max_ms_per_step: float, world_size: int) -> float:
+    """Whole-job GB/s: every rank's bytes over the slowest rank's step time."""
+    return bytes_per_rank_step * world_size / (max_ms_per_step * 1e-3) / 1e9
+
+
+# ---- clocks --------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---- CPU baseline (the oracle, as it stands) ----------------------------------------------------
+
+def oracle_sample(w, n_seq: int, n_threads: int = 0):
+    """Time the fp64 oracle's paged decode on the first n_seq requests of w (all heads), with a
+    host pool laid out by the oracle's own allocator model, slot mapping and scatter."""
+    import oracle
+    P = w.page_size
+    alloc = oracle.AllocatorModel(w.num_pages, w.page_order)
+    tables, lens = [], []
+    for b in range(n_seq):
+        tables.append(alloc.alloc(oracle.pages_needed(int(w.context_lens[b]), P)))
+        lens.append(int(w.context_lens[b]))
+    width = max(len(t) for t in tables)
+    bt = np.zeros((n_seq, width), dtype=np.int32)
+    for b, t in enumerate(tables):
+        bt[b, :len(t)] = t
+    used = sorted({p for t in tables for p in t})
+    remap = {p: i for i, p in enumerate(used)}  # compact host pool holding only these pages
+    bt_c = np.vectorize(lambda p: remap.get(int(p), 0))(bt).astype(np.int32)
+    dt = np.uint16 if w.kv_dtype == "bf16" else np.float32
+    kp = np.zeros((len(used), w.num_kv_heads, P, w.head_dim), dtype=dt)
+    vp = np.zeros_like(kp)
+    for b in range(n_seq):
+        k, v = w.request_tokens(b)
+        slots = oracle.slot_mapping(bt_c, np.arange(lens[b]), P, requests=np.full(lens[b], b))
+        oracle.scatter_append(kp, slots, oracle.as_raw(k, w.kv_dtype))
+        oracle.scatter_append(vp, slots, oracle.as_raw(v, w.kv_dtype))
+    q = oracle.as_raw(w.q[:n_seq], w.q_dtype)
+    t0 = time.perf_counter()
+    oracle.paged_decode(q, w.q_dtype, kp, vp, w.kv_dtype, bt_c, np.array(lens, dtype=np.int32),
+                        w.scale, n_threads=n_threads)
+    dt_s = time.perf_counter() - t0
+    kvb = {"f32": 4, "bf16": 2}[w.kv_dtype]
+    qb = {"f32": 4, "bf16": 2}[w.q_dtype]
+    byts = (sum(lens) * w.num_kv_heads * w.head_dim * kvb * 2
+            + 2 * n_seq * w.num_q_heads * w.head_dim * qb)
+    return byts, dt_s
+
+
+def cpu_baseline(w, budget_s=12.0):
+    import oracle
+    threads = oracle.max_threads()
+    b1, t1 = oracle_sample(w, 1)
+    n = int(min(w.batch, max(1, budget_s / max(t1, 1e-3))))
+    byts, t = oracle_sample(w, n) if n > 1 else (b1, t1)
+    return {"value": byts / t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "fp64 C oracle (gather through page tables + textbook softmax), first %d "
+                      "of %d requests, all 32 heads, %.1f s" % (n, w.batch, t),
+            "cpu": _cpu_model()}
+
+
+def _cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
+# ---- our arm ------------------------------------------------------------------------------------
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_271_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """dram bytes per launch of the decode kernel from the committed ncu summary, if it was
+    taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "paged_decode_llama3_8b_b64.traffic.txt")
+    try:
+        with open(path) as f:
+            rec = dict(tok.split("=", 1) for tok in f.read().split())
+        if rec.get("source_sha") == source_sha():
+            return float(rec["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+def run_ours(args):
+    import torch
+    import paged_kv_cache_271_gb300 as pkv
+    from gpu_harness import Scenario
+
+    ws, rank, local = rank_info()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(ws, "nccl")
+    pkv.lib()  # fail loudly if the library is missing
+
+    w = workload()
+    sc = Scenario(w, device=dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    per_step_bytes = decode_bytes(w) + append_bytes(w)
+
+    def step_host():
+        # host part of the hot path: this step's slots from the page tables
+        slots = pkv.slot_mapping(sc.cache.block_table_array(sc.rids),
+                                 sc.cache.context_lens_array(sc.rids) - 1, w.num_pages)
+        assert np.array_equal(slots, sc.step_slots)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step_host()
+        sc.step()
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    pkv.trace_reset()
+    pkv.trace_enable(True)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        step_host()
+        starts[i].record(stream)
+        sc.step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    pkv.trace_enable(False)
+    clk = clocks.stop()
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_step = float(np.mean(ms))
+    launches = {}
+    for k in ("kv_append", "paged_decode", "decode_combine"):
+        launches[k] = pkv.trace_read(k)
+    pkv.trace_reset()
+    assert pkv.device_error() == 0
+
+    max_ms = max_over_ranks(ms_step, dev)
+    value = aggregate(per_step_bytes, max_ms, ws)
+    hbm_peak, peak_kind = peaks()
+
+    n_dec, t_dec = launches["paged_decode"]
+    dec_ms = t_dec / max(n_dec, 1)
+    dec_achieved = decode_bytes(w) / (dec_ms * 1e-3) / 1e9
+    traffic = recorded_traffic()
+    roofline = {"bound": "hbm", "kernel": "paged_decode_kernel<bf16, d=128, G=4>",
+                "achieved": round(dec_achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(dec_achieved / hbm_peak, 4), "peak_kind": peak_kind,
+                "frac_of_nominal_8TBs": round(dec_achieved / NOMINAL_HBM_GBS, 4),
+                "traffic": traffic, "algorithmic_bytes_per_launch": decode_bytes(w),
+                "launch_ms": round(dec_ms, 5)}
+
+    e2e = run_e2e(sc, w, args, dev, stream, flush)
+    max_e2e = max_over_ranks(e2e["ms_per_step"], dev)
+    e2e_value = aggregate(per_step_bytes, max_e2e, ws)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": dict(config_of(w), parallelism="replicas x%d" % ws),
+            "decode_tokens_per_s": round(ws * w.batch / (max_ms * 1e-3), 1),
+            "pct_of_peak": {"measured_copy_%s" % peak_kind: round(100 * value / ws / hbm_peak, 2),
+                            "nominal_8TBs": round(100 * value / ws / NOMINAL_HBM_GBS, 2)},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
+                    "ms_per_step": round(max_e2e, 5),
+                    "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+            "gpu_launches": int(sum(n for n, _ in launches.values())),
+            "launches_per_kernel": {k: n for k, (n, _) in launches.items()},
+            "kernel_ms": {k: round(t / max(n, 1), 5) for k, (n, t) in launches.items()},
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(sc, w, args, dev, stream, flush):
+    """Same step through the public API from pinned host buffers: per step the host->device
+    copies of the step's inputs (queries, new K/V rows, slots, page tables, context lengths) and
+    the device->host read of the outputs sit inside the timed region."""
+    import torch
+    import paged_kv_cache_271_gb300 as pkv
+    host = {
+        "q": sc.q.cpu().pin_memory(), "k_new": sc.k_new.cpu().pin_memory(),
+        "v_new": sc.v_new.cpu().pin_memory(), "slots": sc.slots_dev.cpu().pin_memory(),
+        "bt": sc.block_tables.cpu().pin_memory(), "cl": sc.context_lens.cpu().pin_memory(),
+    }
+    dev_t = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    out_host = torch.empty(sc.out.shape, dtype=sc.out.dtype).pin_memory()
+    h2d = int(sum(v.numel() * v.element_size() for v in host.values()))
+    d2h = int(out_host.numel() * out_host.element_size())
+    ks, vs = sc.scales if sc.scales else (None, None)
+
+    def one():
+        for k in host:
+            dev_t[k].copy_(host[k], non_blocking=True)
+        pkv.kv_append(dev_t["k_new"], dev_t["v_new"], dev_t["slots"], sc.cache.k, sc.cache.v,
+                      ks, vs)
+        pkv.paged_decode_attention(dev_t["q"], sc.cache.k, sc.cache.v, dev_t["bt"], dev_t["cl"],
+                                   w.scale, out=sc.out, k_scales=ks, v_scales=vs,
+                                   workspace=sc.workspace)
+        out_host.copy_(sc.out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        one()
+    torch.cuda.synchronize()
+    n = max(1, args.steps)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(n):
+        flush.zero_()
+        starts[i].record(stream)
+        one()
+        ends[i].record(stream)
+        ends[i].synchronize()  # the result is on the host before the next step starts
+    barrier()
+    ms = float(np.mean([s.elapsed_time(e) for s, e in zip(starts, ends)]))
+    return {"ms_per_step": ms, "h2d": h2d, "d2h": d2h}
+
+
+# ---- reference arm: the oracle as it stands --------------------------------------------------
+
+def run_reference(args):
+    ws, rank, _ = rank_info()
+    if rank != 0:
+        return
+    import oracle
+    w = workload()
+    threads = oracle.max_threads()
+    n_seq = 2
+    for _ in range(args.warmup):
+        oracle_sample(w, n_seq)
+    times, byts = [], 0
+    for _ in range(args.steps):
+        byts, t = oracle_sample(w, n_seq)
+        times.append(t)
+    ms = float(np.mean(times)) * 1e3
+    value = byts / (ms * 1e-3) / 1e9
+    sample = ("fp64 C oracle paged decode of the first %d of %d requests (all heads) per step"
+              % (n_seq, w.batch))
+    line = {"metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": dict(config_of(w), parallelism="host cores"),
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": sample, "cpu": _cpu_model()},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("bench.py: at least 3 warm-up steps")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

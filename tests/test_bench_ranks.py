@@ -1,0 +1,50 @@
+"""The benchmark's multi-rank logic on CPU: two gloo ranks, replicas with a max-over-ranks
+step time and a whole-job aggregate. No GPU and no data-path collective."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    bench.init_dist(world, "gloo")
+    ws, r, _ = bench.rank_info()
+    local_ms = 1.0 + r  # rank 1 is the slow one
+    m = bench.max_over_ranks(local_ms)
+    bench.barrier()
+    q.put((r, ws, m, bench.aggregate(1e9, m, ws)))
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_max_step_time():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r, ws, m, agg in res:
+        assert ws == 2 and m == 2.0
+        # 2 ranks x 1 GB each over the slowest rank's 2 ms = 1000 GB/s
+        assert agg == pytest.approx(1000.0)
+
+
+def test_single_process_needs_no_process_group():
+    assert bench.max_over_ranks(3.5) == 3.5
+    assert bench.aggregate(2e9, 2.0, 1) == pytest.approx(1000.0)
