@@ -140,6 +140,34 @@ int pkv_paged_decode_attention(const void* q, int32_t dtype_q, int32_t batch,
                                void* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The same decode attention as pkv_paged_decode_attention, for callers that cannot allocate
+ * device memory (a plugin whose host application owns all device memory and gives it no
+ * allocation hook; a server that reserved all free HBM for its KV pools at start-up; a
+ * latency-critical loop that must not risk cudaMalloc's device-wide synchronisation). It takes
+ * no workspace: the split partials go to a 16 MiB scratch array built into the library, held in
+ * device memory on every GPU that loads the library until the process exits. The pages have no
+ * counterpart to this entry point; it is a deployment convenience of this library.
+ *  - Arguments, layouts and results are those of pkv_paged_decode_attention.
+ *  - Sizes whose split would need more than the scratch (pkv_decode_workspace_size(...) >
+ *    pkv_decode_noalloc_scratch_bytes()) are rejected with PKV_EINVAL before anything runs.
+ *  - Calls no cudaMalloc or cudaFree. The first call on a device looks up the scratch's device
+ *    address for that device (with it current); make that call before any stream capture.
+ *  - All calls on a device share the scratch and it keeps the last call's contents (nothing in
+ *    it has to start at zero). Calls whose kernels may overlap on the GPU, e.g. on two streams
+ *    without ordering between them, race on it; calls on one stream are safe.
+ */
+int pkv_paged_decode_attention_noalloc(const void* q, int32_t dtype_q, int32_t batch,
+                                       int32_t num_q_heads, const void* k_cache,
+                                       const void* v_cache, const pkv_cache_desc* desc,
+                                       const int32_t* block_tables, int32_t max_pages_per_seq,
+                                       const int32_t* context_lens, float scale,
+                                       const float* k_scales, const float* v_scales, void* out,
+                                       void* stream);
+
+/* Bytes of the scratch pkv_paged_decode_attention_noalloc uses (16 MiB). */
+size_t pkv_decode_noalloc_scratch_bytes(void);
+
+/*
  * Per-KV-head scales for an FP8 cache (section 7; granularity is this library's reading):
  *   scales_out[h] = fp32(max |x[:, h, :]| / 448), or 1 if that maximum is 0.
  *  x           device [n_tokens][num_kv_heads][head_dim] of dtype (F32 or BF16), 16-byte

@@ -63,6 +63,9 @@ def lib():
         "pkv_decode_workspace_size": (sz, [i32, i32, i32, i32, i32]),
         "pkv_paged_decode_attention": (ctypes.c_int, [vp, i32, i32, i32, vp, vp, D, vp, i32, vp,
                                                       f32, vp, vp, vp, vp, sz, vp]),
+        "pkv_paged_decode_attention_noalloc": (ctypes.c_int, [vp, i32, i32, i32, vp, vp, D, vp,
+                                                              i32, vp, f32, vp, vp, vp, vp]),
+        "pkv_decode_noalloc_scratch_bytes": (sz, []),
         "pkv_kv_absmax_scales": (ctypes.c_int, [vp, i32, i64, i32, i32, vp, vp]),
         "pkv_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32)]),
         "pkv_decode_set_chunk_pages": (ctypes.c_int, [i32]),
@@ -189,6 +192,27 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
         ctypes.byref(desc), _dev(block_tables, "block_tables"), maxp,
         _dev(context_lens, "context_lens"), float(scale), _opt(k_scales, "k_scales"),
         _opt(v_scales, "v_scales"), _dev(out, "out"), ws, wsb, _stream(stream)))
+    return out
+
+
+def paged_decode_attention_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale,
+                                   out=None, k_scales=None, v_scales=None, stream=None):
+    """paged_decode_attention without a workspace: for callers that cannot allocate device
+    memory, the split partials go to the library's built-in 16 MiB scratch (shared by all calls
+    on a device; calls that overlap on the GPU race)."""
+    if q.dim() != 3 or block_tables.dim() != 2:
+        raise PkvError(-2, "q must be [batch, heads, dim], block_tables [batch, max_pages]")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise PkvError(-3, "block_tables and context_lens must be int32")
+    B, h_q, _ = q.shape
+    desc = cache_desc(k_cache)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(lib().pkv_paged_decode_attention_noalloc(
+        _dev(q, "q"), _dtype_code(q), B, h_q, _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        ctypes.byref(desc), _dev(block_tables, "block_tables"), block_tables.shape[1],
+        _dev(context_lens, "context_lens"), float(scale), _opt(k_scales, "k_scales"),
+        _opt(v_scales, "v_scales"), _dev(out, "out"), _stream(stream)))
     return out
 
 
