@@ -279,31 +279,61 @@ def run_ours(args):
     torch.cuda.synchronize()
     assert pkv.device_error() == 0
 
+    # The step's device work (append, decode, combine) is captured once as a CUDA graph and
+    # replayed every step, as a serving loop would; the host slot mapping runs outside it.
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            sc.step()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        sc.step()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        flush.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    pkv.trace_reset()
-    pkv.trace_enable(True)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    host_s = 0.0
     barrier()
     torch.cuda.synchronize()
     for i in range(args.steps):
         flush.zero_()
+        t0 = time.perf_counter()
         step_host()
+        host_s += time.perf_counter() - t0
         starts[i].record(stream)
-        sc.step()
+        graph.replay()
         ends[i].record(stream)
     torch.cuda.synchronize()
     barrier()
-    pkv.trace_enable(False)
     clk = clocks.stop()
     ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_step = float(np.mean(ms))
+    assert pkv.device_error() == 0
+
+    # Per-kernel durations: the same steps launched directly with the library's tracing on
+    # (events on the launching stream around every kernel).
+    pkv.trace_reset()
+    pkv.trace_enable(True)
+    for i in range(args.steps):
+        flush.zero_()
+        sc.step()
+    torch.cuda.synchronize()
+    pkv.trace_enable(False)
     launches = {}
     for k in ("kv_append", "paged_decode", "decode_combine"):
         launches[k] = pkv.trace_read(k)
     pkv.trace_reset()
+    per_step_launches = sum(n for n, _ in launches.values()) / max(args.steps, 1)
     assert pkv.device_error() == 0
 
     max_ms = max_over_ranks(ms_step, dev)
@@ -314,7 +344,7 @@ def run_ours(args):
     dec_ms = t_dec / max(n_dec, 1)
     dec_achieved = decode_bytes(w) / (dec_ms * 1e-3) / 1e9
     traffic = recorded_traffic()
-    roofline = {"bound": "hbm", "kernel": "paged_decode_kernel<bf16, d=128, G=4>",
+    roofline = {"bound": "hbm", "kernel": "paged_decode_kernel (bf16 cache, d=128, G=4)",
                 "achieved": round(dec_achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(dec_achieved / hbm_peak, 4), "peak_kind": peak_kind,
                 "frac_of_nominal_8TBs": round(dec_achieved / NOMINAL_HBM_GBS, 4),
@@ -343,7 +373,9 @@ def run_ours(args):
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
                     "ms_per_step": round(max_e2e, 5),
                     "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
-            "gpu_launches": int(sum(n for n, _ in launches.values())),
+            "gpu_launches": int(round(per_step_launches * args.steps)),
+            "graph": "append + decode + combine captured once, replayed per step",
+            "host_slot_mapping_us": round(1e6 * host_s / max(args.steps, 1), 1),
             "launches_per_kernel": {k: n for k, (n, _) in launches.items()},
             "kernel_ms": {k: round(t / max(n, 1), 5) for k, (n, t) in launches.items()},
             "clocks": clk,

@@ -129,7 +129,7 @@ size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num
  *  workspace    device, >= pkv_decode_workspace_size(...) bytes, 16-byte aligned, or NULL
  *               when that size is 0. Long contexts are split into chunks of pages whose
  *               partial results (running max, sum, weighted values) are merged by a second
- *               kernel in chunk order, so results do not depend on physical page placement.
+ *               kernel in a fixed order, so results do not depend on physical page placement.
  * Requires num_q_heads % num_kv_heads == 0 and G in {1, 2, 4, 8, 16}.
  */
 int pkv_paged_decode_attention(const void* q, int32_t dtype_q, int32_t batch,

@@ -159,28 +159,82 @@ __global__ void kv_scale_finalize_kernel(float* scales, int h_kv) {
 }
 
 // Merge of the chunk partials of one (b, h): M = max_c m_c, w_c = 2^(m_c - M),
-// out = sum_c w_c acc_c / sum_c w_c l_c, chunks in ascending order.
-template <typename TQ>
-__global__ void decode_combine_kernel(const DecodeArgs a, int head_dim) {
-  const int h = blockIdx.x, b = blockIdx.y, i = threadIdx.x;
+// out = sum_c w_c acc_c / sum_c w_c l_c. One CTA of 4 warps per (h, b): the threads find M
+// together; warp w then accumulates chunks w, w+4, w+8, ... with vector loads (lane = DL dims)
+// and the warps' sums are added in warp order, so the result depends only on the number of
+// chunks. Launched as a programmatic dependent of the decode kernel: it is scheduled while the
+// decode drains and waits for the decode's results before reading them.
+template <typename TQ, int D>
+__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a) {
+  constexpr int DL = D / 32;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ctx = min(max(0, a.context_lens[b]), a.max_pages * kPageSize);
   const int pages_seq = (ctx + kPageSize - 1) / kPageSize;
   const int n_chunks = (pages_seq + a.chunk_pages - 1) / a.chunk_pages;
-  if (n_chunks <= 1 || i >= head_dim) return;
+  if (n_chunks <= 1) return;
   const size_t bh = (size_t)b * a.h_q + h;
   const float* ml = a.ws_ml + bh * a.n_chunk_slots * 2;
-  const float* acc = a.ws_acc + bh * a.n_chunk_slots * head_dim;
+  const float* acc = a.ws_acc + bh * a.n_chunk_slots * D;
+  __shared__ float s_max[4];
+  __shared__ float s_l[4];
+  __shared__ float s_acc[4][D];
+
   float M = -INFINITY;
-  for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, ml[2 * c]);
-  float L = 0.f, A = 0.f;
+  for (int c = threadIdx.x; c < n_chunks; c += 128) M = fmaxf(M, ml[2 * c]);
+#pragma unroll
+  for (int o = 16; o >= 1; o /= 2) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) s_max[warp] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(s_max[0], s_max[1]), fmaxf(s_max[2], s_max[3]));
+
+  float L = 0.f, A[DL];
+#pragma unroll
+  for (int k = 0; k < DL; ++k) A[k] = 0.f;
   if (M != -INFINITY) {
-    for (int c = 0; c < n_chunks; ++c) {
+#pragma unroll 4
+    for (int c = warp; c < n_chunks; c += 4) {
       const float w = exp2f(ml[2 * c] - M);
       L = fmaf(w, ml[2 * c + 1], L);
-      A = fmaf(w, acc[(size_t)c * head_dim + i], A);
+      const float* src = acc + (size_t)c * D + lane * DL;
+      if constexpr (DL == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        A[0] = fmaf(w, v.x, A[0]);
+        A[1] = fmaf(w, v.y, A[1]);
+        A[2] = fmaf(w, v.z, A[2]);
+        A[3] = fmaf(w, v.w, A[3]);
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        A[0] = fmaf(w, v.x, A[0]);
+        A[1] = fmaf(w, v.y, A[1]);
+      }
     }
   }
-  store_from_float(static_cast<TQ*>(a.out), bh * head_dim + i, L > 0.f ? A / L : 0.f);
+  if (lane == 0) s_l[warp] = L;
+#pragma unroll
+  for (int k = 0; k < DL; ++k) s_acc[warp][lane * DL + k] = A[k];
+  __syncthreads();
+  const float Lt = ((s_l[0] + s_l[1]) + s_l[2]) + s_l[3];
+  for (int i = threadIdx.x; i < D; i += 128) {
+    const float At = ((s_acc[0][i] + s_acc[1][i]) + s_acc[2][i]) + s_acc[3][i];
+    store_from_float(static_cast<TQ*>(a.out), bh * D + i, Lt > 0.f ? At / Lt : 0.f);
+  }
+}
+
+template <typename TQ, int D>
+cudaError_t launch_combine_t(const DecodeArgs& a, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.h_q, a.batch);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<TQ, D>, a);
 }
 
 inline int grid_for(int64_t work, int threads) {
@@ -239,12 +293,10 @@ cudaError_t launch_kv_absmax(const void* x, int dtype, int64_t n_tokens, int h_k
 }
 
 cudaError_t launch_decode_combine(const DecodeArgs& a, int q_dtype, int head_dim, cudaStream_t s) {
-  dim3 grid(a.h_q, a.batch);
   if (q_dtype == PKV_BF16)
-    decode_combine_kernel<__nv_bfloat16><<<grid, head_dim, 0, s>>>(a, head_dim);
-  else
-    decode_combine_kernel<float><<<grid, head_dim, 0, s>>>(a, head_dim);
-  return cudaGetLastError();
+    return head_dim == 64 ? launch_combine_t<__nv_bfloat16, 64>(a, s)
+                          : launch_combine_t<__nv_bfloat16, 128>(a, s);
+  return head_dim == 64 ? launch_combine_t<float, 64>(a, s) : launch_combine_t<float, 128>(a, s);
 }
 
 }  // namespace pkv

@@ -21,7 +21,7 @@
 //    lane then accumulates p * V over its DL dims for all G heads.
 //  * Merge: the 4 warps' (m, l, acc) are combined in shared memory. A single-chunk request
 //    writes out = acc / l; otherwise the CTA writes its chunk's (m, l, acc) and the combine
-//    kernel merges the chunks of each (b, h) in chunk order. Chunk boundaries are logical
+//    kernel merges the chunks of each (b, h) in a fixed order. Chunk boundaries are logical
 //    positions, so results do not depend on which physical pages hold the tokens.
 #pragma once
 

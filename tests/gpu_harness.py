@@ -131,3 +131,102 @@ def oracle_expected(w, pairs=None, n_threads=0):
 def tolerance(w) -> float:
     """Max-abs bound for the attention output: 1e-5 for fp32 inputs, 1e-2 otherwise."""
     return 1e-5 if w.kv_dtype == "f32" and w.q_dtype == "f32" else 1e-2
+
+
+class ContinuousBatchingRun:
+    """Drives a ``workloads.ContinuousBatchingTrace`` through the library on an FP8 cache:
+    absmax scales over the initial cache, quantising prefill of every prompt, one appended
+    token per live request per step, finished requests freed and replaced (continuous
+    batching), paged decode every step."""
+
+    def __init__(self, trace, device="cuda"):
+        self.t = trace
+        self.device = torch.device(device)
+        B = trace.batch
+        self.tokens = {}  # rid -> (k, v) bf16 CPU rows
+        for b in range(B):
+            self.tokens[b] = trace.request_tokens(b)
+        init = [int(n) for n in trace.initial_lens]
+        k0 = torch.cat([self.tokens[b][0][:init[b]] for b in range(B)], 0).to(self.device)
+        v0 = torch.cat([self.tokens[b][1][:init[b]] for b in range(B)], 0).to(self.device)
+        self.k_scales = pkv.kv_absmax_scales(k0)
+        self.v_scales = pkv.kv_absmax_scales(v0)
+        self.cache = PagedKVCache(trace.num_pages, trace.num_kv_heads, trace.head_dim,
+                                  torch.uint8, self.device, initial_free_order=trace.page_order,
+                                  k_scales=self.k_scales, v_scales=self.v_scales)
+        fill_junk(self.cache.k, trace.seed + 11)
+        fill_junk(self.cache.v, trace.seed + 12)
+        self.slot_rid = list(range(B))
+        for b in range(B):
+            self.cache.add_request(b)
+        slots = self.cache.reserve(self.slot_rid, init)
+        self.cache.write(slots, k0, v0)
+        del k0, v0
+        self.step_index = 0
+        self.last_slots = None
+
+    def initial_rows(self):
+        """float32 [sum initial, h_kv, d] K and V rows the scales cover (for the oracle)."""
+        B = self.t.batch
+        init = [int(n) for n in self.t.initial_lens]
+        k = torch.cat([self.tokens[b][0][:init[b]] for b in range(B)], 0).float().numpy()
+        v = torch.cat([self.tokens[b][1][:init[b]] for b in range(B)], 0).float().numpy()
+        return k, v
+
+    def step(self):
+        """One continuous-batching step; returns the decode output [B, h_q, d] (bf16)."""
+        t, s = self.t, self.step_index
+        if s > 0:
+            new_rids, counts = [], []
+            for b in range(t.batch):
+                if t.finish[s - 1, b]:
+                    old = self.slot_rid[b]
+                    self.cache.free_request(old)
+                    del self.tokens[old]
+                    rid = int(t.rid_table[s, b])
+                    self.slot_rid[b] = rid
+                    self.tokens[rid] = t.request_tokens(rid)
+                    self.cache.add_request(rid)
+                    new_rids.append(rid)
+                    counts.append(int(t.prompt_lens[rid]))
+            if new_rids:
+                slots = self.cache.reserve(new_rids, counts)
+                k = torch.cat([self.tokens[r][0][:n] for r, n in zip(new_rids, counts)], 0)
+                v = torch.cat([self.tokens[r][1][:n] for r, n in zip(new_rids, counts)], 0)
+                self.cache.write(slots, k.to(self.device), v.to(self.device))
+        rids = self.slot_rid
+        pos = [self.cache.lens[r] for r in rids]
+        k_new = torch.stack([self.tokens[r][0][p] for r, p in zip(rids, pos)]).to(self.device)
+        v_new = torch.stack([self.tokens[r][1][p] for r, p in zip(rids, pos)]).to(self.device)
+        self.last_slots = self.cache.reserve(rids, [1] * len(rids))
+        self.cache.write(self.last_slots, k_new, v_new)
+        self.q = t.step_q(s).to(self.device)
+        self.block_tables = torch.from_numpy(self.cache.block_table_array(rids)).to(self.device)
+        self.context_lens = torch.from_numpy(self.cache.context_lens_array(rids)).to(self.device)
+        out = pkv.paged_decode_attention(self.q, self.cache.k, self.cache.v, self.block_tables,
+                                         self.context_lens, t.scale, k_scales=self.k_scales,
+                                         v_scales=self.v_scales)
+        self.step_index += 1
+        return out
+
+    def oracle_pairs(self, pairs, k_scales, v_scales):
+        """Oracle output for (slot, head) pairs of the step just run, from the requests' own
+        bf16 rows quantised by the oracle with the given (oracle-computed) scales."""
+        t = self.t
+        G = t.num_q_heads // t.num_kv_heads
+        q = self.q.cpu()
+        rows = []
+        for b, h in pairs:
+            rid = self.slot_rid[b]
+            T = self.cache.lens[rid]
+            j = h // G
+            k = self.tokens[rid][0][:T, j].float().numpy()
+            v = self.tokens[rid][1][:T, j].float().numpy()
+            kc = oracle.quantize_e4m3(k, k_scales[j])[:, None, :]
+            vc = oracle.quantize_e4m3(v, v_scales[j])[:, None, :]
+            out = oracle.contiguous_decode(oracle.as_raw(q[b:b + 1, h:h + 1], "bf16"), "bf16",
+                                           kc, vc, "fp8_e4m3", [0], [T], t.scale,
+                                           k_scales=k_scales[j:j + 1],
+                                           v_scales=v_scales[j:j + 1])
+            rows.append(out[0, 0])
+        return np.stack(rows)

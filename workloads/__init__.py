@@ -169,9 +169,9 @@ class ContinuousBatchingTrace:
 
     Slot b starts with request b holding ``initial_lens[b]`` cached tokens. Every step
     appends one token to each live request and decodes. ``finish[s, b]`` says the request in
-    slot b finishes after step s; it is replaced before step s+1 by a new request of
-    ``replacement_lens[s, b]`` prompt tokens. Request ids: 0..B-1 for the initial ones, then
-    B, B+1, ... in (step, slot) order of replacement.
+    slot b finishes after step s; before step s+1 it is replaced by a new request whose prompt
+    has ``replacement_lens[s, b]`` tokens. ``rid_table[s, b]`` is the id of the request in slot
+    b during step s (0..B-1 for the initial ones, then B, B+1, ... in (step, slot) order).
     """
 
     name: str
@@ -188,17 +188,34 @@ class ContinuousBatchingTrace:
     page_order: np.ndarray
     scale: float
     seed: int
+    rid_table: np.ndarray = None  # int64 [steps, B]
+    prompt_lens: np.ndarray = None  # int32 [number of requests]
 
-    def request_tokens(self, request_id: int, n: int):
-        """The first n key and value rows of a request, bf16 [n, h_kv, d]; same on every call."""
-        g = _gen(self.seed * 1000003 + 17 + request_id)
-        k = _normal((n, self.num_kv_heads, self.head_dim), "bf16", g)
-        v = _normal((n, self.num_kv_heads, self.head_dim), "bf16", g)
+    def __post_init__(self):
+        B, S = self.batch, self.steps
+        table = np.zeros((S, B), dtype=np.int64)
+        table[0] = np.arange(B)
+        prompts = list(self.initial_lens.astype(np.int64))
+        for s in range(1, S):
+            table[s] = table[s - 1]
+            for b in range(B):
+                if self.finish[s - 1, b]:
+                    table[s, b] = len(prompts)
+                    prompts.append(int(self.replacement_lens[s - 1, b]))
+        self.rid_table = table
+        self.prompt_lens = np.array(prompts, dtype=np.int32)
+
+    def max_rows(self, request_id: int) -> int:
+        """Rows a request can ever hold: its prompt plus one appended token per step."""
+        return int(self.prompt_lens[request_id]) + self.steps
+
+    def request_tokens(self, request_id: int):
+        """Keys and values of a request, bf16 [max_rows, h_kv, d]; the same on every call."""
+        n = self.max_rows(request_id)
+        shape = (n, self.num_kv_heads, self.head_dim)
+        k = _normal(shape, "bf16", _gen(self.seed * 1000003 + 2 * request_id + 17))
+        v = _normal(shape, "bf16", _gen(self.seed * 1000003 + 2 * request_id + 18))
         return k, v
-
-    def request_token_rows(self, request_id: int, start: int, n: int):
-        k, v = self.request_tokens(request_id, start + n)
-        return k[start:], v[start:]
 
     def step_q(self, step: int) -> torch.Tensor:
         g = _gen(self.seed * 7919 + step)
@@ -207,6 +224,8 @@ class ContinuousBatchingTrace:
 
 def fp8_continuous_batching(batch=256, steps=32, lo=128, hi=8192, rep_lo=128, rep_hi=2048,
                             p_finish=0.05, h_q=32, h_kv=8, d=128) -> ContinuousBatchingTrace:
+    """FP8 E4M3 cache with continuous batching: 256 slots, 32 steps, initial contexts
+    U[128, 8192], finish probability 0.05 per step, replacements of U[128, 2048] tokens."""
     seed = BASE_SEED + 5
     g = _gen(seed)
     init = torch.randint(lo, hi + 1, (batch,), generator=g).numpy().astype(np.int32)
