@@ -188,6 +188,13 @@ int pkv_device_error(void* stream, int32_t* code_out);
  * Process-wide; affects calls made after it returns. */
 int pkv_decode_set_chunk_pages(int32_t pages);
 
+/* Which decode kernel pkv_paged_decode_attention uses: 0 = automatic (tensor cores for a bf16
+ * or FP8 cache with head_dim 128, CUDA cores otherwise), 1 = always the CUDA-core kernel,
+ * 2 = always the tensor-core kernel (calls it cannot serve then fail with PKV_EINVAL).
+ * Process-wide; affects calls made after it returns. Both kernels compute the same result
+ * within the documented tolerances; each is deterministic for a given choice. */
+int pkv_decode_set_kernel(int32_t which);
+
 /* Chunk size (pages) the decode uses for these sizes under the current setting. */
 int32_t pkv_decode_chunk_pages(int32_t batch, int32_t num_kv_heads, int32_t max_pages_per_seq);
 

@@ -70,6 +70,7 @@ def lib():
         "pkv_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32)]),
         "pkv_decode_set_chunk_pages": (ctypes.c_int, [i32]),
         "pkv_decode_chunk_pages": (i32, [i32, i32, i32]),
+        "pkv_decode_set_kernel": (ctypes.c_int, [i32]),
         "pkv_pages_needed": (ctypes.c_int, [i64, i32, ctypes.POINTER(i64)]),
         "pkv_slot_mapping": (ctypes.c_int, [vp, i32, vp, vp, i64, i32, i32, vp]),
         "pkv_allocator_create": (ctypes.c_int, [i32, vp, ctypes.POINTER(vp)]),
@@ -239,6 +240,11 @@ def device_error(stream=None) -> int:
 
 def decode_set_chunk_pages(pages: int):
     _check(lib().pkv_decode_set_chunk_pages(int(pages)))
+
+
+def decode_set_kernel(which: int):
+    """0 automatic, 1 CUDA-core decode kernel, 2 tensor-core decode kernel."""
+    _check(lib().pkv_decode_set_kernel(int(which)))
 
 
 def decode_chunk_pages(batch, num_kv_heads, max_pages_per_seq) -> int:

@@ -1,6 +1,8 @@
 // C ABI of the library: argument checks, the split-over-pages policy, kernel dispatch, the
 // device error word and launch tracing. Every function here returns a pkv_status; argument
 // errors are found on the host before anything is launched.
+#include <cuda.h>
+
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -79,6 +81,72 @@ int cuda_status(cudaError_t e, const char* what) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 std::atomic<int> g_chunk_override{0};
+std::atomic<int> g_kernel_choice{0};  // 0 automatic, 1 CUDA cores, 2 tensor cores
+
+// ---- TMA tensor maps of the pools (for the tensor-core decode) -------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct MapEntry {
+  int dev;
+  const void* base;
+  long long rows;
+  int head_dim;
+  int dtype;
+  CUtensorMap map;
+};
+std::mutex g_map_mu;
+std::vector<MapEntry> g_maps;
+EncodeTiledFn g_encode = nullptr;
+
+// A pool seen as a 2-D tensor [num_pages * h_kv * 16 rows][head_dim], loaded in boxes of 16
+// rows x 128 bytes with the 128-byte swizzle. Encoded once per (device, pool, shape).
+int pool_tensor_map(const void* base, const pkv_cache_desc* d, CUtensorMap* out) {
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return set_error(PKV_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
+  const long long rows = (long long)d->num_pages * d->num_kv_heads * d->page_size;
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  for (auto& e : g_maps)
+    if (e.dev == dev && e.base == base && e.rows == rows && e.head_dim == d->head_dim &&
+        e.dtype == d->cache_dtype) {
+      *out = e.map;
+      return PKV_OK;
+    }
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    ce = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                          &q);
+    if (ce != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+      return set_error(PKV_ECUDA, "cuTensorMapEncodeTiled is not available");
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  const int eb = d->cache_dtype == PKV_BF16 ? 2 : 1;
+  MapEntry e{};
+  e.dev = dev;
+  e.base = base;
+  e.rows = rows;
+  e.head_dim = d->head_dim;
+  e.dtype = d->cache_dtype;
+  const cuuint64_t dims[2] = {(cuuint64_t)d->head_dim, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d->head_dim * eb};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / eb), (cuuint32_t)d->page_size};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(&e.map,
+                        eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                        2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(PKV_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  if (g_maps.size() >= 256) g_maps.clear();  // callers keep few pools; drop stale entries
+  g_maps.push_back(e);
+  *out = e.map;
+  return PKV_OK;
+}
 
 // Pages per chunk (one CTA each). 32 pages (512 tokens) keeps the partials to ~1% of the KV
 // bytes; smaller chunks when batch * kv_heads is too small to give ~1024 CTAs; one chunk when
@@ -120,6 +188,13 @@ int pkv_decode_set_chunk_pages(int32_t pages) {
   if (pages < 0 || pages > 4096)
     return set_error(PKV_EINVAL, "pkv_decode_set_chunk_pages: %d outside [0, 4096]", pages);
   g_chunk_override.store(pages);
+  return PKV_OK;
+}
+
+int pkv_decode_set_kernel(int32_t which) {
+  if (which < 0 || which > 2)
+    return set_error(PKV_EINVAL, "pkv_decode_set_kernel: %d is not 0, 1 or 2", which);
+  g_kernel_choice.store(which);
   return PKV_OK;
 }
 
@@ -201,10 +276,24 @@ int pkv_paged_decode_attention(const void* q, int32_t dtype_q, int32_t batch,
     a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                        align256(rows * D * sizeof(float)));
   }
+  const int choice = g_kernel_choice.load();
+  const bool mma_ok = kv != PKV_F32 && D == 128 &&
+                      (long long)desc->num_pages * h_kv * desc->page_size < (1ll << 31);
+  if (choice == 2 && !mma_ok)
+    return set_error(PKV_EINVAL, "%s: the tensor-core decode needs a bf16 or FP8 cache, head_dim "
+                     "128 and fewer than 2^31 pool rows", who);
+  const bool use_mma = mma_ok && choice != 1;
+  CUtensorMap tk, tv;
+  if (use_mma) {
+    st = pool_tensor_map(k_cache, desc, &tk);
+    if (st == PKV_OK) st = pool_tensor_map(v_cache, desc, &tv);
+    if (st != PKV_OK) return st;
+  }
   st = error_word(&a.err);
   if (st != PKV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = traced("paged_decode", s, [&] {
+    if (use_mma) return launch_decode_mma(a, kv, dtype_q, G, &tk, &tv, s);
     if (kv == PKV_F32) return launch_decode_f32(a, dtype_q, D, G, s);
     if (kv == PKV_BF16) return launch_decode_bf16(a, dtype_q, D, G, s);
     return launch_decode_fp8(a, dtype_q, D, G, s);

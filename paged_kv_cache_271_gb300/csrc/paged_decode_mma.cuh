@@ -1,0 +1,512 @@
+// Single-token paged decode attention on tensor cores (bf16 or FP8 E4M3 cache, head_dim 128).
+//
+// Same computation, work split and results contract as paged_decode.cuh (the read phase of the
+// KV-cache pages, "KV cache and PagedAttention" sections 1 and 4, GQA per the "KV Cache"
+// glossary); what changes is how a warp turns one 16-token page into scores and weighted
+// values. On CUDA cores that takes ~1260 instructions per 8 KiB page (shuffle reductions,
+// per-element widening and FMAs) and the kernel is issue-bound; here it is ~16 tensor-core
+// MMAs plus a few dozen other instructions per page.
+//
+//  * Staging: a 2-D TMA tensor copy (128-byte swizzle) moves each (page, KV head) tile of K
+//    and of V into a warp-owned ring stage, completing on the stage's mbarrier. The swizzle
+//    makes the fragment loads below free of shared-memory bank conflicts.
+//  * Scores: S^T = K Q^T with mma.m16n8k16 -- the page's 16 tokens are M, the group's query
+//    heads (padded to 8 per n-tile) are N, head_dim is K. The k order inside each 16-wide
+//    k-step is permuted so a lane's A fragment for two k-steps is one 16-byte load of its row;
+//    the query fragments (held in registers for the whole CTA) use the same permutation.
+//  * Online softmax (base 2) on the accumulator fragment: a lane holds 2 tokens x 2 heads;
+//    the page max per head needs 3 shuffles.
+//  * Values: O^T = V^T P^T with mma.m16n8k16 -- head_dim is M (8 m-tiles), heads are N, the
+//    page's tokens are K. V^T fragments come from ldmatrix.trans on the swizzled tile; P is
+//    rounded to the MMA input type and transposed through a 256-byte per-warp buffer.
+//  * FP8: codes are widened exactly to f16 (K in registers, V into a per-warp f16 staging
+//    tile), the query is used in f16, and the MMAs run in f16 with fp32 accumulation; the K
+//    scale multiplies the scores and the V scale the output.
+//  * Rows of the last page past the context may hold stale bytes (even NaN): their scores are
+//    set to -inf and their V rows to zero before the P.V product.
+#pragma once
+
+#include <cuda.h>
+#include <math.h>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+template <typename KV, int D, int G>
+struct MmaShape {
+  static_assert(D == 128, "tensor-core decode supports head_dim 128");
+  static constexpr bool kFp8 = KV::bytes == 1;
+  static constexpr int kWarps = 4;
+  static constexpr int kThreads = 32 * kWarps;
+  static constexpr int NT = (G + 7) / 8;                 // n-tiles of 8 query heads
+  static constexpr int KP = D / 32;                      // pairs of 16-wide k-steps
+  static constexpr int MT = D / 16;                      // m-tiles of the P.V product
+  static constexpr int SPW = 2;                          // ring stages per warp
+  static constexpr int STAGES = kWarps * SPW;
+  static constexpr int ROW_BYTES = D * KV::bytes;        // 256 (bf16) or 128 (fp8)
+  static constexpr int BOXES = ROW_BYTES / 128;          // 128-byte swizzle boxes per row
+  static constexpr int BOX_ELEMS = 128 / KV::bytes;
+  static constexpr int TILE_BYTES = kPageSize * ROW_BYTES;
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int VDEQ_BYTES = kFp8 ? kWarps * kPageSize * D * 2 : 0;  // f16 V tiles
+  static constexpr int PT_BYTES = kWarps * NT * 8 * kPageSize * 2;          // P^T buffers
+  static constexpr int MERGE_BYTES = kWarps * G * (D + 2) * 4;
+  static constexpr int BIG_BYTES =
+      ((RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES) + 1023) / 1024 * 1024;
+  static constexpr int SMEM_BYTES =
+      1024 + BIG_BYTES + VDEQ_BYTES + PT_BYTES + STAGES * 8 + STAGES * 4;
+};
+
+__device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma16816_f16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                             uint32_t a2, uint32_t a3, uint32_t b0,
+                                             uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (F16)
+    mma16816_f16(d, a0, a1, a2, a3, b0, b1);
+  else
+    mma16816_bf16(d, a0, a1, a2, a3, b0, b1);
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// 2-D tiled TMA load of one box into shared memory, completing on `bar`; L2 evict-first.
+__device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const CUtensorMap* map, int x,
+                                            int y, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// Byte offset of 16-byte chunk `chunk` (0 .. ROW_BYTES/16) of row `row` in a tile stored as
+// 128-byte-swizzled boxes of 16 rows (box b at b*2048).
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return (uint32_t)((chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  __half2_raw h =
+      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+template <typename KV, typename TQ, int D, int G>
+__global__ void __launch_bounds__(128) paged_decode_mma_kernel(
+    const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v) {
+  using S = MmaShape<KV, D, G>;
+  constexpr bool F8 = S::kFp8;
+  constexpr int NW = S::kWarps, SPW = S::SPW, NT = S::NT, KP = S::KP, MT = S::MT;
+  const int c = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  int ctx = max(0, a.context_lens[b]);
+  if (ctx > a.max_pages * kPageSize) {
+    if (c == 0 && threadIdx.x == 0) atomicOr(a.err, PKV_DEVERR_BAD_PAGE);
+    ctx = a.max_pages * kPageSize;
+  }
+  const int pages_seq = (ctx + kPageSize - 1) / kPageSize;
+  const int n_chunks = (pages_seq + a.chunk_pages - 1) / a.chunk_pages;
+  if (c > 0 && c >= n_chunks) return;
+  const int page0 = c * a.chunk_pages;
+  const int n_pages = max(0, min(a.chunk_pages, pages_seq - page0));
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint8_t* vdeq = smem + S::BIG_BYTES;                    // FP8 only
+  uint16_t* pt = reinterpret_cast<uint16_t*>(vdeq + S::VDEQ_BYTES) + warp * NT * 8 * kPageSize;
+  uint64_t* full = reinterpret_cast<uint64_t*>(vdeq + S::VDEQ_BYTES + S::PT_BYTES);
+  int* page_ok = reinterpret_cast<int*>(full + S::STAGES);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S::STAGES; ++s) mbar_init(&full[s], 1);
+    mbar_fence_init();
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
+  }
+  __syncthreads();
+
+  // Query fragments (MMA B operand of S^T = K Q^T), k order permuted as described above:
+  // lane (gid, tig) holds Q[g = 8 nt + gid][32 kp + 8 tig + 0..7] for every kp (bf16 path) or
+  // Q[g][16 (4 h + tig) + 4 ks + 0..3] for h = 0, 1 and ks = 0..3 (FP8 path).
+  uint32_t qf[NT][KP][4];
+  {
+    const TQ* q = static_cast<const TQ*>(a.q);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int g = nt * 8 + gid;
+      const bool live = g < G;
+      const size_t base = ((size_t)b * a.h_q + j * G + (live ? g : 0)) * D;
+#pragma unroll
+      for (int kp = 0; kp < KP; ++kp) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          int d0;
+          if constexpr (F8)
+            d0 = 16 * (4 * (kp >> 1) + tig) + 4 * (2 * (kp & 1) + (e >> 1)) + 2 * (e & 1);
+          else
+            d0 = 32 * kp + 8 * tig + 2 * e;
+          const float x0 = live ? load_as_float(q, base + d0) : 0.f;
+          const float x1 = live ? load_as_float(q, base + d0 + 1) : 0.f;
+          qf[nt][kp][e] = F8 ? pack_f16(x0, x1) : pack_bf16(x0, x1);
+        }
+      }
+    }
+  }
+  const float sc = a.scale_log2 * (F8 ? a.k_scales[j] : 1.f);
+
+  const int32_t* bt = a.block_tables + (size_t)b * a.max_pages + page0;
+  const uint64_t pol = l2_evict_first_policy();
+  const uint32_t ring_u32 = smem_u32(ring);
+
+  auto issue = [&](int i, int stg) {  // lane 0: fetch page i of the chunk into stage stg
+    const int pid = bt[i];
+    if (pid < 0 || pid >= a.num_pages) {
+      page_ok[stg] = 0;
+      atomicOr(a.err, PKV_DEVERR_BAD_PAGE);
+      mbar_arrive(&full[stg]);
+    } else {
+      page_ok[stg] = 1;
+      mbar_arrive_expect_tx(&full[stg], S::STAGE_BYTES);
+      const int row = (pid * a.h_kv + j) * kPageSize;
+      const uint32_t dst = ring_u32 + stg * S::STAGE_BYTES;
+#pragma unroll
+      for (int bx = 0; bx < S::BOXES; ++bx) {
+        tma_load_2d(dst + bx * 2048, &tm_k, bx * S::BOX_ELEMS, row, &full[stg], pol);
+        tma_load_2d(dst + S::TILE_BYTES + bx * 2048, &tm_v, bx * S::BOX_ELEMS, row, &full[stg],
+                    pol);
+      }
+    }
+  };
+
+  const int n_mine = n_pages > warp ? (n_pages - warp + NW - 1) / NW : 0;
+  if (lane == 0) {
+    for (int m = 0; m < SPW && m < n_mine; ++m) issue(warp + NW * m, warp * SPW + m);
+  }
+
+  float m_run[NT][2], l_run[NT][2];
+  float acc[MT][NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m_run[nt][0] = m_run[nt][1] = -INFINITY;
+    l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+    for (int mi = 0; mi < MT; ++mi)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mi][nt][e] = 0.f;
+  }
+  const uint32_t pt_u32 = smem_u32(pt);
+  const uint32_t vdeq_u32 = smem_u32(vdeq) + warp * (kPageSize * D * 2);
+
+  int m = 0;
+  bool ok = true;
+  for (; m < n_mine; ++m) {
+    const int i = warp + NW * m;
+    const int stg = warp * SPW + (m % SPW);
+    const bool got = mbar_wait(&full[stg], (m / SPW) & 1, a.err);
+    if (!__all_sync(0xffffffffu, got)) {
+      ok = false;
+      break;
+    }
+    if (page_ok[stg]) {
+      const int nvalid = min(kPageSize, ctx - (page0 + i) * kPageSize);
+      const uint32_t kt = ring_u32 + stg * S::STAGE_BYTES;
+      const uint32_t vt = kt + S::TILE_BYTES;
+
+      // ---- scores S^T[16 tokens][8 heads per n-tile] ----
+      float s[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      if constexpr (!F8) {
+#pragma unroll
+        for (int kp = 0; kp < KP; ++kp) {
+          const uint4 r0 = lds128(kt + swz(gid, 4 * kp + tig));
+          const uint4 r8 = lds128(kt + swz(gid + 8, 4 * kp + tig));
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma16816<false>(s[nt], r0.x, r8.x, r0.y, r8.y, qf[nt][kp][0], qf[nt][kp][1]);
+            mma16816<false>(s[nt], r0.z, r8.z, r0.w, r8.w, qf[nt][kp][2], qf[nt][kp][3]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // 16-byte chunk 4h+tig of a row = 4 k-steps x 4 codes
+          const uint4 r0 = lds128(kt + swz(gid, 4 * h + tig));
+          const uint4 r8 = lds128(kt + swz(gid + 8, 4 * h + tig));
+          const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w};
+          const uint32_t w8[4] = {r8.x, r8.y, r8.z, r8.w};
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t a0 = e4m3x2_to_f16x2(w0[ks]);
+            const uint32_t a2 = e4m3x2_to_f16x2(w0[ks] >> 16);
+            const uint32_t a1 = e4m3x2_to_f16x2(w8[ks]);
+            const uint32_t a3 = e4m3x2_to_f16x2(w8[ks] >> 16);
+            const int kp = 2 * h + (ks >> 1), half = ks & 1;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma16816<true>(s[nt], a0, a1, a2, a3, qf[nt][kp][2 * half],
+                             qf[nt][kp][2 * half + 1]);
+          }
+        }
+      }
+
+      // ---- online softmax: lane holds tokens gid, gid+8 of heads 8nt+2tig, 8nt+2tig+1 ----
+      const bool v0 = gid < nvalid, v8 = gid + 8 < nvalid;
+      float alpha[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        s[nt][0] = v0 ? s[nt][0] * sc : -INFINITY;
+        s[nt][1] = v0 ? s[nt][1] * sc : -INFINITY;
+        s[nt][2] = v8 ? s[nt][2] * sc : -INFINITY;
+        s[nt][3] = v8 ? s[nt][3] * sc : -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          float mx = fmaxf(s[nt][k], s[nt][k + 2]);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float m_new = fmaxf(m_run[nt][k], mx);
+          const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+          alpha[nt][k] = exp2f(m_run[nt][k] - m_use);
+          s[nt][k] = exp2f(s[nt][k] - m_use);
+          s[nt][k + 2] = exp2f(s[nt][k + 2] - m_use);
+          l_run[nt][k] = l_run[nt][k] * alpha[nt][k] + s[nt][k] + s[nt][k + 2];
+          m_run[nt][k] = m_new;
+        }
+        // P^T into the warp buffer: pt[g][t], g = 8nt + 2tig (+1), t = gid (+8)
+        uint16_t* row0 = pt + (nt * 8 + 2 * tig) * kPageSize;
+        uint16_t* row1 = row0 + kPageSize;
+        if constexpr (F8) {
+          const __half h0 = __float2half_rn(s[nt][0]), h1 = __float2half_rn(s[nt][1]);
+          const __half h2 = __float2half_rn(s[nt][2]), h3 = __float2half_rn(s[nt][3]);
+          row0[gid] = __half_as_ushort(h0);
+          row1[gid] = __half_as_ushort(h1);
+          row0[gid + 8] = __half_as_ushort(h2);
+          row1[gid + 8] = __half_as_ushort(h3);
+        } else {
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(s[nt][0]);
+          const __nv_bfloat16 h1 = __float2bfloat16_rn(s[nt][1]);
+          const __nv_bfloat16 h2 = __float2bfloat16_rn(s[nt][2]);
+          const __nv_bfloat16 h3 = __float2bfloat16_rn(s[nt][3]);
+          row0[gid] = __bfloat16_as_ushort(h0);
+          row1[gid] = __bfloat16_as_ushort(h1);
+          row0[gid + 8] = __bfloat16_as_ushort(h2);
+          row1[gid + 8] = __bfloat16_as_ushort(h3);
+        }
+#pragma unroll
+        for (int mi = 0; mi < MT; ++mi) {
+          acc[mi][nt][0] *= alpha[nt][0];
+          acc[mi][nt][1] *= alpha[nt][1];
+          acc[mi][nt][2] *= alpha[nt][0];
+          acc[mi][nt][3] *= alpha[nt][1];
+        }
+      }
+
+      // ---- V tile as 16-bit rows in the swizzled layout (FP8: widened into vdeq) ----
+      uint32_t vsrc = vt;
+      if constexpr (F8) {
+        // lane: row lane/2, dims 64*(lane%2) .. +64 = fp8 chunks 4*(lane%2) .. +4
+        const int r = lane >> 1, hb = lane & 1;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint4 w = lds128(vt + swz(r, 4 * hb + q4));
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+          uint4 o0, o1;
+          o0.x = e4m3x2_to_f16x2(ws[0]);
+          o0.y = e4m3x2_to_f16x2(ws[0] >> 16);
+          o0.z = e4m3x2_to_f16x2(ws[1]);
+          o0.w = e4m3x2_to_f16x2(ws[1] >> 16);
+          o1.x = e4m3x2_to_f16x2(ws[2]);
+          o1.y = e4m3x2_to_f16x2(ws[2] >> 16);
+          o1.z = e4m3x2_to_f16x2(ws[3]);
+          o1.w = e4m3x2_to_f16x2(ws[3] >> 16);
+          if (r >= nvalid) o0 = o1 = make_uint4(0, 0, 0, 0);
+          sts128(vdeq_u32 + swz(r, 8 * hb + 2 * q4), o0);
+          sts128(vdeq_u32 + swz(r, 8 * hb + 2 * q4 + 1), o1);
+        }
+        vsrc = vdeq_u32;
+      } else if (nvalid < kPageSize) {
+        // zero the stale rows of the last page (16 chunks of 16 bytes per row)
+        for (int e = lane; e < (kPageSize - nvalid) * 16; e += 32) {
+          const int r = nvalid + (e >> 4), ch = e & 15;
+          sts128(vt + swz(r, ch), make_uint4(0, 0, 0, 0));
+        }
+      }
+      __syncwarp();
+
+      // ---- O^T[dims][heads] += V^T P^T ----
+      uint32_t pb[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint32_t rowg = pt_u32 + (nt * 8 + gid) * kPageSize * 2;
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(pb[nt][0]) : "r"(rowg + 4 * tig));
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(pb[nt][1]) : "r"(rowg + 16 + 4 * tig));
+      }
+      {
+        const int q = lane >> 3, rr = lane & 7;
+        const int t = (q >> 1) * 8 + rr;
+#pragma unroll
+        for (int mi = 0; mi < MT; ++mi) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_trans(vsrc + swz(t, 2 * mi + (q & 1)), a0, a1, a2, a3);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma16816<F8>(acc[mi][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && m + SPW < n_mine) {
+      fence_proxy_async_smem();
+      issue(i + NW * SPW, stg);
+    }
+  }
+  if (!ok && lane == 0) {
+    for (int mm = m; mm < n_mine && mm < m + SPW; ++mm)
+      mbar_wait(&full[warp * SPW + (mm % SPW)], (mm / SPW) & 1, a.err);
+  }
+  __syncthreads();  // every copy has landed: the ring is free for the merge
+
+  float* red_acc = reinterpret_cast<float*>(ring);  // [NW][G][D]
+  float* red_m = red_acc + NW * G * D;              // [NW][G]
+  float* red_l = red_m + NW * G;                    // [NW][G]
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      float l = l_run[nt][k];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      const int g = nt * 8 + 2 * tig + k;
+      if (gid == 0 && g < G) {
+        red_m[warp * G + g] = m_run[nt][k];
+        red_l[warp * G + g] = l;
+      }
+#pragma unroll
+      for (int mi = 0; mi < MT; ++mi) {
+        if (g < G) {
+          red_acc[(warp * G + g) * D + mi * 16 + gid] = acc[mi][nt][k];
+          red_acc[(warp * G + g) * D + mi * 16 + gid + 8] = acc[mi][nt][k + 2];
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  const float vs = F8 ? a.v_scales[j] : 1.f;
+  for (int e = threadIdx.x; e < G * D; e += S::kThreads) {
+    const int g = e / D, i = e % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * G + g]);
+    float L = 0.f, A = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float wt = exp2f(red_m[w * G + g] - M);
+        L = fmaf(wt, red_l[w * G + g], L);
+        A = fmaf(wt, red_acc[(w * G + g) * D + i], A);
+      }
+    }
+    A *= vs;
+    const size_t bh = (size_t)b * a.h_q + j * G + g;
+    if (n_chunks <= 1) {
+      store_from_float(static_cast<TQ*>(a.out), bh * D + i, L > 0.f ? A / L : 0.f);
+    } else {
+      a.ws_acc[(bh * a.n_chunk_slots + c) * D + i] = A;
+      if (i == 0) {
+        a.ws_ml[(bh * a.n_chunk_slots + c) * 2 + 0] = M;
+        a.ws_ml[(bh * a.n_chunk_slots + c) * 2 + 1] = L;
+      }
+    }
+  }
+}
+
+template <typename KV, typename TQ, int D, int G>
+cudaError_t launch_decode_mma_t(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                                cudaStream_t s) {
+  using S = MmaShape<KV, D, G>;
+  auto kern = paged_decode_mma_kernel<KV, TQ, D, G>;
+  static unsigned long long attr_done = 0;  // one bit per device, per instantiation
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !((attr_done >> dev) & 1ull)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_done |= 1ull << dev;
+  }
+  dim3 grid(a.n_chunk_slots, a.h_kv, a.batch);
+  kern<<<grid, S::kThreads, S::SMEM_BYTES, s>>>(a, tk, tv);
+  return cudaGetLastError();
+}
+
+template <typename KV, typename TQ>
+cudaError_t launch_decode_mma_g(const DecodeArgs& a, int group, const CUtensorMap& tk,
+                                const CUtensorMap& tv, cudaStream_t s) {
+  switch (group) {
+    case 1: return launch_decode_mma_t<KV, TQ, 128, 1>(a, tk, tv, s);
+    case 2: return launch_decode_mma_t<KV, TQ, 128, 2>(a, tk, tv, s);
+    case 4: return launch_decode_mma_t<KV, TQ, 128, 4>(a, tk, tv, s);
+    case 8: return launch_decode_mma_t<KV, TQ, 128, 8>(a, tk, tv, s);
+    case 16: return launch_decode_mma_t<KV, TQ, 128, 16>(a, tk, tv, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pkv

@@ -51,6 +51,10 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, int q_dtype, int head_dim, i
                                cudaStream_t s);
 cudaError_t launch_decode_fp8(const DecodeArgs& a, int q_dtype, int head_dim, int group,
                               cudaStream_t s);
+// Tensor-core decode (bf16 or FP8 cache, head_dim 128); tk/tv are CUtensorMap objects
+// describing the K and V pools as 2-D [rows][head_dim] tensors (see capi.cu).
+cudaError_t launch_decode_mma(const DecodeArgs& a, int kv_dtype, int q_dtype, int group,
+                              const void* tk, const void* tv, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeArgs& a, int q_dtype, int head_dim,
                                   cudaStream_t s);
 cudaError_t launch_kv_append(const AppendArgs& a, int in_dtype, int cache_dtype, cudaStream_t s);

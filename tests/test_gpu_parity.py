@@ -28,17 +28,20 @@ def _gpu():
 @pytest.fixture(autouse=True)
 def _clean_error_word():
     pkv.decode_set_chunk_pages(0)
+    pkv.decode_set_kernel(0)
     pkv.device_error()
     yield
     pkv.decode_set_chunk_pages(0)
+    pkv.decode_set_kernel(0)
 
 
 def _max_err(out, ref):
     return float(np.abs(out.double().cpu().numpy() - ref).max()) if ref.size else 0.0
 
 
-def _run(w, chunk=0, **kw):
+def _run(w, chunk=0, kernel=0, **kw):
     pkv.decode_set_chunk_pages(chunk)
+    pkv.decode_set_kernel(kernel)
     sc = Scenario(w, **kw)
     out = sc.step().clone()
     torch.cuda.synchronize()
@@ -107,20 +110,41 @@ SHAPES = [
 
 @pytest.mark.parametrize("kv,qd,h_q,h_kv,d,lens", SHAPES)
 @pytest.mark.parametrize("chunk", [0, 1, 3])
-def test_decode_parity_shapes(kv, qd, h_q, h_kv, d, lens, chunk):
+@pytest.mark.parametrize("kernel", [1, 2])  # CUDA-core, tensor-core
+def test_decode_parity_shapes(kv, qd, h_q, h_kv, d, lens, chunk, kernel):
+    if kernel == 2 and (kv == "f32" or d != 128):
+        pytest.skip("the tensor-core decode serves bf16/FP8 caches with head_dim 128")
     w = workloads.custom("shape", 9000 + h_q + d + len(lens), len(lens), h_q, h_kv, d, kv, qd,
                          lens)
-    _, out = _run(w, chunk=chunk)
+    _, out = _run(w, chunk=chunk, kernel=kernel)
     err = _max_err(out, oracle_expected(w))
     assert err <= tolerance(w), err
 
 
-def test_split_results_do_not_depend_on_physical_pages():
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_split_results_do_not_depend_on_physical_pages(kernel):
     w = workloads.llama3_8b_batch64(batch=8)
-    _, a = _run(w)
+    _, a = _run(w, kernel=kernel)
     order2 = np.random.default_rng(5).permutation(w.num_pages).astype(np.int32)
-    _, b = _run(w, page_order=order2)
+    _, b = _run(w, kernel=kernel, page_order=order2)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_llama3_8b_batch64_both_kernels(kernel):
+    w = workloads.llama3_8b_batch64(batch=16)
+    _, out = _run(w, kernel=kernel)
+    err = _max_err(out, oracle_expected(w))
+    assert err <= 1e-2, err
+
+
+def test_tensor_core_kernel_rejects_what_it_cannot_serve():
+    w = workloads.custom("f32mma", 41, 2, 4, 2, 64, "f32", "f32", [20, 9])
+    sc = Scenario(w)
+    pkv.decode_set_kernel(2)
+    with pytest.raises(pkv.PkvError):
+        pkv.paged_decode_attention(sc.q, sc.cache.k, sc.cache.v, sc.block_tables,
+                                   sc.context_lens, w.scale, workspace=sc.workspace)
 
 
 def test_zero_length_context_gives_zero_output():
