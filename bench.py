@@ -1,9 +1,9 @@
 """Benchmark: one decode step of a Llama-3-8B-shaped layer at batch 64 over a paged KV cache.
 
 A step is the whole hot path for one batch: the host computes this step's slots (page
-accounting, slot mapping), ``kv_append`` writes the new token of each request into its page,
-and ``paged_decode_attention`` attends each request's query over its whole cached context
-(decode kernel plus, for split sequences, the combine kernel). Inputs are seeded synthetic
+accounting, slot mapping), then one ``paged_decode_step`` launch writes the new token of each
+request into its page (the append) and attends each request's query over its whole cached
+context, merging split sequences in place. Inputs are seeded synthetic
 tensors (N(0, 1) bf16, context lengths U[512, 4096]) already resident in HBM; the L2 is flushed
 (a 256 MiB write) before every timed step, outside the timed events.
 
@@ -58,7 +58,7 @@ def config_of(w):
             "kv_dtype": w.kv_dtype, "context_lens": "U[512,4096] seeded, sum %d"
             % int(np.sum(w.context_lens)), "pool_pages": w.num_pages,
             "l2": "flushed with a 256 MiB write before every timed step",
-            "step": "slot mapping (host) + kv_append + paged_decode_attention"}
+            "step": "slot mapping (host) + paged_decode_step (append + attention, one launch)"}
 
 
 def decode_bytes(w):
@@ -275,7 +275,7 @@ def run_ours(args):
     for _ in range(args.warmup):
         flush.zero_()
         step_host()
-        sc.step()
+        sc.fused_step()
     torch.cuda.synchronize()
     assert pkv.device_error() == 0
 
@@ -286,11 +286,11 @@ def run_ours(args):
     side.wait_stream(stream)
     with torch.cuda.stream(side):
         for _ in range(3):
-            sc.step()
+            sc.fused_step()
     stream.wait_stream(side)
     torch.cuda.synchronize()
     with torch.cuda.graph(graph):
-        sc.step()
+        sc.fused_step()
     torch.cuda.synchronize()
     for _ in range(args.warmup):
         flush.zero_()
@@ -326,7 +326,7 @@ def run_ours(args):
     pkv.trace_enable(True)
     for i in range(args.steps):
         flush.zero_()
-        sc.step()
+        sc.fused_step()
     torch.cuda.synchronize()
     pkv.trace_enable(False)
     launches = {}
@@ -342,13 +342,15 @@ def run_ours(args):
 
     n_dec, t_dec = launches["paged_decode"]
     dec_ms = t_dec / max(n_dec, 1)
-    dec_achieved = decode_bytes(w) / (dec_ms * 1e-3) / 1e9
+    kernel_bytes = decode_bytes(w) + append_bytes(w)  # the launch also appends the new rows
+    dec_achieved = kernel_bytes / (dec_ms * 1e-3) / 1e9
     traffic = recorded_traffic()
-    roofline = {"bound": "hbm", "kernel": "paged_decode_kernel (bf16 cache, d=128, G=4)",
+    roofline = {"bound": "hbm",
+                "kernel": "paged_decode_mma_kernel (bf16 cache, d=128, G=4, append fused)",
                 "achieved": round(dec_achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(dec_achieved / hbm_peak, 4), "peak_kind": peak_kind,
                 "frac_of_nominal_8TBs": round(dec_achieved / NOMINAL_HBM_GBS, 4),
-                "traffic": traffic, "algorithmic_bytes_per_launch": decode_bytes(w),
+                "traffic": traffic, "algorithmic_bytes_per_launch": kernel_bytes,
                 "launch_ms": round(dec_ms, 5)}
 
     e2e = run_e2e(sc, w, args, dev, stream, flush)
@@ -374,7 +376,7 @@ def run_ours(args):
                     "ms_per_step": round(max_e2e, 5),
                     "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
             "gpu_launches": int(round(per_step_launches * args.steps)),
-            "graph": "append + decode + combine captured once, replayed per step",
+            "graph": "the step's launches captured once as a CUDA graph, replayed per step",
             "host_slot_mapping_us": round(1e6 * host_s / max(args.steps, 1), 1),
             "launches_per_kernel": {k: n for k, (n, _) in launches.items()},
             "kernel_ms": {k: round(t / max(n, 1), 5) for k, (n, t) in launches.items()},
@@ -385,14 +387,14 @@ def run_ours(args):
 
 def run_e2e(sc, w, args, dev, stream, flush):
     """Same step through the public API from pinned host buffers: per step the host->device
-    copies of the step's inputs (queries, new K/V rows, slots, page tables, context lengths) and
-    the device->host read of the outputs sit inside the timed region."""
+    copies of the step's inputs (queries, new K/V rows, page tables, context lengths) and the
+    device->host read of the outputs sit inside the timed region."""
     import torch
     import paged_kv_cache_271_gb300 as pkv
     host = {
         "q": sc.q.cpu().pin_memory(), "k_new": sc.k_new.cpu().pin_memory(),
-        "v_new": sc.v_new.cpu().pin_memory(), "slots": sc.slots_dev.cpu().pin_memory(),
-        "bt": sc.block_tables.cpu().pin_memory(), "cl": sc.context_lens.cpu().pin_memory(),
+        "v_new": sc.v_new.cpu().pin_memory(), "bt": sc.block_tables.cpu().pin_memory(),
+        "cl": sc.context_lens.cpu().pin_memory(),
     }
     dev_t = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
     out_host = torch.empty(sc.out.shape, dtype=sc.out.dtype).pin_memory()
@@ -403,11 +405,9 @@ def run_e2e(sc, w, args, dev, stream, flush):
     def one():
         for k in host:
             dev_t[k].copy_(host[k], non_blocking=True)
-        pkv.kv_append(dev_t["k_new"], dev_t["v_new"], dev_t["slots"], sc.cache.k, sc.cache.v,
-                      ks, vs)
-        pkv.paged_decode_attention(dev_t["q"], sc.cache.k, sc.cache.v, dev_t["bt"], dev_t["cl"],
-                                   w.scale, out=sc.out, k_scales=ks, v_scales=vs,
-                                   workspace=sc.workspace)
+        pkv.paged_decode_step(dev_t["q"], dev_t["k_new"], dev_t["v_new"], sc.cache.k,
+                              sc.cache.v, dev_t["bt"], dev_t["cl"], w.scale, out=sc.out,
+                              k_scales=ks, v_scales=vs, workspace=sc.workspace)
         out_host.copy_(sc.out, non_blocking=True)
 
     for _ in range(max(3, args.warmup)):

@@ -127,9 +127,13 @@ size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num
  *               to that and flagged with PKV_DEVERR_BAD_PAGE).
  *  out          device [batch][num_q_heads][head_dim] of dtype_q.
  *  workspace    device, >= pkv_decode_workspace_size(...) bytes, 16-byte aligned, or NULL
- *               when that size is 0. Long contexts are split into chunks of pages whose
- *               partial results (running max, sum, weighted values) are merged by a second
- *               kernel in a fixed order, so results do not depend on physical page placement.
+ *               when that size is 0. It must be zero-filled before its first use; every call
+ *               that completes leaves it zero-filled where that matters (reuse it freely on
+ *               one stream; re-zero it after a call that reported a device error; one workspace
+ *               per stream). Long contexts are split into chunks of pages whose partial results
+ *               (running max, sum, weighted values) are merged in a fixed order -- by the last
+ *               CTA of each group when there are at most 16 chunks per sequence, else by a
+ *               second kernel -- so results do not depend on physical page placement.
  * Requires num_q_heads % num_kv_heads == 0 and G in {1, 2, 4, 8, 16}.
  */
 int pkv_paged_decode_attention(const void* q, int32_t dtype_q, int32_t batch,
@@ -138,6 +142,27 @@ int pkv_paged_decode_attention(const void* q, int32_t dtype_q, int32_t batch,
                                int32_t max_pages_per_seq, const int32_t* context_lens,
                                float scale, const float* k_scales, const float* v_scales,
                                void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * One decode step, append and attention fused in one launch (write phase + read phase of
+ * "KV cache and PagedAttention" section 1): for every request b with context_lens[b] >= 1,
+ * the row k_new[b] / v_new[b] is written at position context_lens[b] - 1 (page
+ * block_tables[b][p / 16], row p % 16), then attention runs over positions
+ * 0 .. context_lens[b] - 1 exactly as pkv_paged_decode_attention. The pool bytes and the
+ * output equal those of pkv_kv_append (with that position's slot) followed by
+ * pkv_paged_decode_attention.
+ *  k_new, v_new  device [batch][num_kv_heads][head_dim] of dtype_new, 16-byte aligned;
+ *                dtype_new as for pkv_kv_append.
+ * The page holding the new position must belong to request b alone (not a shared prefix page).
+ * Other arguments as pkv_paged_decode_attention.
+ */
+int pkv_paged_decode_step(const void* q, int32_t dtype_q, int32_t batch, int32_t num_q_heads,
+                          const void* k_new, const void* v_new, int32_t dtype_new,
+                          void* k_cache, void* v_cache, const pkv_cache_desc* desc,
+                          const int32_t* block_tables, int32_t max_pages_per_seq,
+                          const int32_t* context_lens, float scale, const float* k_scales,
+                          const float* v_scales, void* out, void* workspace,
+                          size_t workspace_bytes, void* stream);
 
 /*
  * The same decode attention as pkv_paged_decode_attention, for callers that cannot allocate
@@ -152,9 +177,10 @@ int pkv_paged_decode_attention(const void* q, int32_t dtype_q, int32_t batch,
  *    pkv_decode_noalloc_scratch_bytes()) are rejected with PKV_EINVAL before anything runs.
  *  - Calls no cudaMalloc or cudaFree. The first call on a device looks up the scratch's device
  *    address for that device (with it current); make that call before any stream capture.
- *  - All calls on a device share the scratch and it keeps the last call's contents (nothing in
- *    it has to start at zero). Calls whose kernels may overlap on the GPU, e.g. on two streams
- *    without ordering between them, race on it; calls on one stream are safe.
+ *  - All calls on a device share the scratch and it keeps the last call's contents; each call
+ *    zeroes the small part that must start at zero. Calls whose kernels may overlap on the GPU,
+ *    e.g. on two streams without ordering between them, race on it; calls on one stream are
+ *    safe.
  */
 int pkv_paged_decode_attention_noalloc(const void* q, int32_t dtype_q, int32_t batch,
                                        int32_t num_q_heads, const void* k_cache,
@@ -184,7 +210,8 @@ int pkv_kv_absmax_scales(const void* x, int32_t dtype, int64_t n_tokens, int32_t
  */
 int pkv_device_error(void* stream, int32_t* code_out);
 
-/* Chunk size of the split over pages, in pages (1..4096); 0 restores the automatic choice.
+/* Largest chunk of the split over pages, in pages (1..4096); each sequence is cut into the
+ * fewest near-equal chunks no larger than this. 0 restores the automatic choice.
  * Process-wide; affects calls made after it returns. */
 int pkv_decode_set_chunk_pages(int32_t pages);
 
@@ -195,7 +222,7 @@ int pkv_decode_set_chunk_pages(int32_t pages);
  * within the documented tolerances; each is deterministic for a given choice. */
 int pkv_decode_set_kernel(int32_t which);
 
-/* Chunk size (pages) the decode uses for these sizes under the current setting. */
+/* Largest chunk (pages) the decode uses for these sizes under the current setting. */
 int32_t pkv_decode_chunk_pages(int32_t batch, int32_t num_kv_heads, int32_t max_pages_per_seq);
 
 /* ---- host page accounting (no GPU needed) ------------------------------------------------ */

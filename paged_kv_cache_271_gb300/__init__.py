@@ -63,6 +63,8 @@ def lib():
         "pkv_decode_workspace_size": (sz, [i32, i32, i32, i32, i32]),
         "pkv_paged_decode_attention": (ctypes.c_int, [vp, i32, i32, i32, vp, vp, D, vp, i32, vp,
                                                       f32, vp, vp, vp, vp, sz, vp]),
+        "pkv_paged_decode_step": (ctypes.c_int, [vp, i32, i32, i32, vp, vp, i32, vp, vp, D, vp,
+                                                 i32, vp, f32, vp, vp, vp, vp, sz, vp]),
         "pkv_paged_decode_attention_noalloc": (ctypes.c_int, [vp, i32, i32, i32, vp, vp, D, vp,
                                                               i32, vp, f32, vp, vp, vp, vp]),
         "pkv_decode_noalloc_scratch_bytes": (sz, []),
@@ -185,7 +187,7 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
     maxp = block_tables.shape[1]
     need = decode_workspace_size(B, h_q, desc.num_kv_heads, d, maxp)
     if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     ws = _opt(workspace, "workspace")
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().pkv_paged_decode_attention(
@@ -193,6 +195,36 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
         ctypes.byref(desc), _dev(block_tables, "block_tables"), maxp,
         _dev(context_lens, "context_lens"), float(scale), _opt(k_scales, "k_scales"),
         _opt(v_scales, "v_scales"), _dev(out, "out"), ws, wsb, _stream(stream)))
+    return out
+
+
+def paged_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale,
+                      out=None, k_scales=None, v_scales=None, workspace=None, stream=None):
+    """Append + decode in one launch: k_new/v_new [B, h_kv, d] go to position
+    context_lens[b] - 1 of each request, then attention over positions 0 .. context_lens[b]-1.
+    A workspace, when needed, must be zero-filled before its first use (allocated zeroed here
+    when not given)."""
+    if q.dim() != 3 or k_new.dim() != 3 or k_new.shape != v_new.shape:
+        raise PkvError(-2, "q must be [B, h_q, d], k_new and v_new [B, h_kv, d]")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise PkvError(-3, "block_tables and context_lens must be int32")
+    B, h_q, d = q.shape
+    desc = cache_desc(k_cache)
+    if k_new.shape[0] != B or k_new.shape[1] != desc.num_kv_heads or k_new.shape[2] != d:
+        raise PkvError(-2, "k_new must be [batch, num_kv_heads, head_dim]")
+    if out is None:
+        out = torch.empty_like(q)
+    maxp = block_tables.shape[1]
+    need = decode_workspace_size(B, h_q, desc.num_kv_heads, d, maxp)
+    if need and workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().pkv_paged_decode_step(
+        _dev(q, "q"), _dtype_code(q), B, h_q, _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+        _dtype_code(k_new), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(desc),
+        _dev(block_tables, "block_tables"), maxp, _dev(context_lens, "context_lens"),
+        float(scale), _opt(k_scales, "k_scales"), _opt(v_scales, "v_scales"), _dev(out, "out"),
+        _opt(workspace, "workspace"), wsb, _stream(stream)))
     return out
 
 

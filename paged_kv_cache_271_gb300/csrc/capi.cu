@@ -81,6 +81,8 @@ int cuda_status(cudaError_t e, const char* what) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 std::atomic<int> g_chunk_override{0};
+// Calls whose sequences split into at most this many chunks merge them in the decode kernel.
+constexpr int kMergeInPlaceMaxChunks = 16;
 std::atomic<int> g_kernel_choice{0};  // 0 automatic, 1 CUDA cores, 2 tensor cores
 
 // ---- TMA tensor maps of the pools (for the tensor-core decode) -------------------------------
@@ -148,13 +150,14 @@ int pool_tensor_map(const void* base, const pkv_cache_desc* d, CUtensorMap* out)
   return PKV_OK;
 }
 
-// Pages per chunk (one CTA each). 32 pages (512 tokens) keeps the partials to ~1% of the KV
-// bytes; smaller chunks when batch * kv_heads is too small to give ~1024 CTAs; one chunk when
-// every sequence fits in one.
+// Largest chunk (pages per CTA); each sequence is split into the fewest near-equal chunks no
+// larger than this. 64 pages (1024 tokens) keeps the partials under 1 % of the KV bytes;
+// smaller when batch * kv_heads is too small to give ~1024 CTAs; one chunk when every sequence
+// fits in one.
 int chunk_pages_for(int batch, int h_kv, int max_pages) {
   const int ov = g_chunk_override.load();
   if (ov > 0) return ov;
-  int chunk = 32;
+  int chunk = 64;
   const long long units = (long long)batch * h_kv;
   while (chunk > 8 && units * ((max_pages + chunk - 1) / chunk) < 1024) chunk /= 2;
   if (max_pages <= chunk) chunk = max_pages < 1 ? 1 : max_pages;
@@ -211,16 +214,17 @@ size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num
   const size_t slots = (size_t)((max_pages_per_seq + chunk - 1) / chunk);
   if (slots <= 1) return 0;
   const size_t rows = (size_t)batch * num_q_heads * slots;
-  return align256(rows * head_dim * sizeof(float)) + align256(rows * 2 * sizeof(float));
+  return align256(rows * head_dim * sizeof(float)) + align256(rows * 2 * sizeof(float)) +
+         align256((size_t)batch * num_kv_heads * sizeof(int));
 }
 
-int pkv_paged_decode_attention(const void* q, int32_t dtype_q, int32_t batch,
-                               int32_t num_q_heads, const void* k_cache, const void* v_cache,
-                               const pkv_cache_desc* desc, const int32_t* block_tables,
-                               int32_t max_pages_per_seq, const int32_t* context_lens,
-                               float scale, const float* k_scales, const float* v_scales,
-                               void* out, void* workspace, size_t workspace_bytes, void* stream) {
-  const char* who = "pkv_paged_decode_attention";
+static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t batch,
+                       int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                       const pkv_cache_desc* desc, const int32_t* block_tables,
+                       int32_t max_pages_per_seq, const int32_t* context_lens, float scale,
+                       const float* k_scales, const float* v_scales, void* out, void* workspace,
+                       size_t workspace_bytes, const void* k_new, const void* v_new,
+                       int32_t dtype_new, void* stream) {
   int st = check_desc(desc, who);
   if (st != PKV_OK) return st;
   if (batch < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0)
@@ -272,16 +276,34 @@ int pkv_paged_decode_attention(const void* q, int32_t dtype_q, int32_t batch,
                        workspace_bytes);
     if (!aligned16(workspace)) return set_error(PKV_EALIGN, "%s: workspace alignment", who);
     const size_t rows = (size_t)batch * num_q_heads * a.n_chunk_slots;
-    a.ws_acc = static_cast<float*>(workspace);
-    a.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                       align256(rows * D * sizeof(float)));
+    char* ws = static_cast<char*>(workspace);
+    a.ws_acc = reinterpret_cast<float*>(ws);
+    a.ws_ml = reinterpret_cast<float*>(ws + align256(rows * D * sizeof(float)));
+    a.counters = reinterpret_cast<int*>(ws + align256(rows * D * sizeof(float)) +
+                                        align256(rows * 2 * sizeof(float)));
+    // few chunks per sequence: the last CTA of each group merges them (no combine kernel)
+    a.merge_in_place = a.n_chunk_slots <= kMergeInPlaceMaxChunks ? 1 : 0;
+  }
+  if (k_new) {
+    if (!v_new) return set_error(PKV_EINVAL, "%s: v_new is NULL", who);
+    if (kv == PKV_FP8_E4M3) {
+      if (dtype_new != PKV_F32 && dtype_new != PKV_BF16)
+        return set_error(PKV_EDTYPE, "%s: FP8 cache takes F32 or BF16 new rows", who);
+    } else if (dtype_new != kv) {
+      return set_error(PKV_EDTYPE, "%s: new rows must have the cache dtype", who);
+    }
+    if (!aligned16(k_new) || !aligned16(v_new))
+      return set_error(PKV_EALIGN, "%s: new rows must be 16-byte aligned", who);
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.new_dtype = dtype_new;
   }
   const int choice = g_kernel_choice.load();
-  const bool mma_ok = kv != PKV_F32 && D == 128 &&
+  const bool mma_ok = kv != PKV_F32 && D == 128 && aligned16(q) &&
                       (long long)desc->num_pages * h_kv * desc->page_size < (1ll << 31);
   if (choice == 2 && !mma_ok)
     return set_error(PKV_EINVAL, "%s: the tensor-core decode needs a bf16 or FP8 cache, head_dim "
-                     "128 and fewer than 2^31 pool rows", who);
+                     "128, a 16-byte aligned q and fewer than 2^31 pool rows", who);
   const bool use_mma = mma_ok && choice != 1;
   CUtensorMap tk, tv;
   if (use_mma) {
@@ -300,12 +322,39 @@ int pkv_paged_decode_attention(const void* q, int32_t dtype_q, int32_t batch,
   });
   st = cuda_status(e, "paged_decode launch");
   if (st != PKV_OK) return st;
-  if (a.n_chunk_slots > 1) {
+  if (a.n_chunk_slots > 1 && !a.merge_in_place) {
     e = traced("decode_combine", s, [&] { return launch_decode_combine(a, dtype_q, D, s); });
     st = cuda_status(e, "decode_combine launch");
   }
   return st;
 }
+
+int pkv_paged_decode_attention(const void* q, int32_t dtype_q, int32_t batch,
+                               int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                               const pkv_cache_desc* desc, const int32_t* block_tables,
+                               int32_t max_pages_per_seq, const int32_t* context_lens,
+                               float scale, const float* k_scales, const float* v_scales,
+                               void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl("pkv_paged_decode_attention", q, dtype_q, batch, num_q_heads, k_cache,
+                     v_cache, desc, block_tables, max_pages_per_seq, context_lens, scale,
+                     k_scales, v_scales, out, workspace, workspace_bytes, nullptr, nullptr, 0,
+                     stream);
+}
+
+int pkv_paged_decode_step(const void* q, int32_t dtype_q, int32_t batch, int32_t num_q_heads,
+                          const void* k_new, const void* v_new, int32_t dtype_new,
+                          void* k_cache, void* v_cache, const pkv_cache_desc* desc,
+                          const int32_t* block_tables, int32_t max_pages_per_seq,
+                          const int32_t* context_lens, float scale, const float* k_scales,
+                          const float* v_scales, void* out, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  if (!k_new) return set_error(PKV_EINVAL, "pkv_paged_decode_step: k_new is NULL");
+  return decode_impl("pkv_paged_decode_step", q, dtype_q, batch, num_q_heads, k_cache, v_cache,
+                     desc, block_tables, max_pages_per_seq, context_lens, scale, k_scales,
+                     v_scales, out, workspace, workspace_bytes, k_new, v_new, dtype_new, stream);
+}
+
+
 
 int pkv_kv_append(const void* k_new, const void* v_new, int32_t dtype_new, int32_t num_tokens,
                   const int64_t* slot_mapping, void* k_cache, void* v_cache,

@@ -1,0 +1,154 @@
+// End of a decode CTA, shared by the CUDA-core and tensor-core kernels: the CTA's warps have
+// left their (running max, sum, weighted values) per head in shared memory; merge them, then
+//  * one chunk: write out = acc / l;
+//  * several chunks: write this chunk's partial (m, l, acc) to the workspace; when the call
+//    merges in place (few chunks per sequence), the last CTA of the (request, KV head) to
+//    finish -- found with a counter in the workspace -- merges every chunk of the group in
+//    chunk order and writes out, then resets the counter to 0 for the next call. Otherwise a
+//    separate combine kernel merges the partials.
+#pragma once
+
+#include <math.h>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+template <typename TQ, int D, int G, int NW, int NTHR>
+__device__ __forceinline__ void decode_epilogue(const DecodeArgs& a, int b, int j, int c,
+                                                int n_chunks, const float* red_acc,
+                                                const float* red_m, const float* red_l,
+                                                float vs) {
+  __shared__ int s_last;
+  for (int e = threadIdx.x; e < G * D; e += NTHR) {
+    const int g = e / D, i = e % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * G + g]);
+    float L = 0.f, A = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float wt = exp2f(red_m[w * G + g] - M);
+        L = fmaf(wt, red_l[w * G + g], L);
+        A = fmaf(wt, red_acc[(w * G + g) * D + i], A);
+      }
+    }
+    A *= vs;
+    const size_t bh = (size_t)b * a.h_q + j * G + g;
+    if (n_chunks <= 1) {
+      store_from_float(static_cast<TQ*>(a.out), bh * D + i, L > 0.f ? A / L : 0.f);
+    } else {
+      a.ws_acc[(bh * a.n_chunk_slots + c) * D + i] = A;
+      if (i == 0) {
+        a.ws_ml[(bh * a.n_chunk_slots + c) * 2 + 0] = M;
+        a.ws_ml[(bh * a.n_chunk_slots + c) * 2 + 1] = L;
+      }
+    }
+  }
+  if (n_chunks <= 1 || !a.merge_in_place) return;
+
+  // Publish this chunk's partial, then count it; the CTA that brings the count to n_chunks
+  // sees every other chunk's partial (each was fenced before its count).
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(a.counters + (size_t)b * a.h_kv + j, 1);
+    s_last = (prev == n_chunks - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int e = threadIdx.x; e < G * D; e += NTHR) {
+    const int g = e / D, i = e % D;
+    const size_t bh = (size_t)b * a.h_q + j * G + g;
+    const float* ml = a.ws_ml + bh * a.n_chunk_slots * 2;
+    const float* acc = a.ws_acc + bh * a.n_chunk_slots * D + i;
+    float M = -INFINITY;
+    for (int k = 0; k < n_chunks; ++k) M = fmaxf(M, __ldcg(ml + 2 * k));
+    float L = 0.f, A = 0.f;
+    if (M != -INFINITY) {
+      for (int k = 0; k < n_chunks; ++k) {
+        const float w = exp2f(__ldcg(ml + 2 * k) - M);
+        L = fmaf(w, __ldcg(ml + 2 * k + 1), L);
+        A = fmaf(w, __ldcg(acc + (size_t)k * D), A);
+      }
+    }
+    store_from_float(static_cast<TQ*>(a.out), bh * D + i, L > 0.f ? A / L : 0.f);
+  }
+  if (threadIdx.x == 0) a.counters[(size_t)b * a.h_kv + j] = 0;
+}
+
+}  // namespace pkv
+
+namespace pkv {
+
+// Decode step with the append fused in: the CTA that reads the page holding position ctx-1 of
+// request b (KV head j) writes this step's K and V rows there -- into the pools and into its
+// shared-memory copy of the page -- before using the page. Same bytes as kv_append: a copy
+// for bf16/fp32 caches, cvt.rn.satfinite.e4m3(fp32(x / s)) for FP8. off(r, ch) is the byte
+// offset of 16-byte chunk ch of row r in a shared-memory tile.
+template <typename KV, int D, typename OffFn>
+__device__ __forceinline__ void fused_append_row(const DecodeArgs& a, int b, int j, int pid,
+                                                 int r, uint8_t* k_tile, uint8_t* v_tile,
+                                                 int lane, OffFn off) {
+  constexpr int NCH = D * KV::bytes / 16;  // 16-byte chunks per row
+  const size_t row_byte = ((((size_t)pid * a.h_kv + j) * kPageSize + r) * D) * KV::bytes;
+  const size_t src_elem = ((size_t)b * a.h_kv + j) * D;
+  for (int e = lane; e < 2 * NCH; e += 32) {
+    const bool isv = e >= NCH;
+    const int ch = isv ? e - NCH : e;
+    const void* src = isv ? a.v_new : a.k_new;
+    uint4 val;
+    if constexpr (KV::bytes == 1) {
+      float x[16];
+      if (a.new_dtype == PKV_BF16) {
+        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src) +
+                                                        src_elem + 16 * ch);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint4 u = p[h];
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            x[8 * h + 2 * t] = bf16lo(w[t]);
+            x[8 * h + 2 * t + 1] = bf16hi(w[t]);
+          }
+        }
+      } else {
+        const float4* p =
+            reinterpret_cast<const float4*>(static_cast<const float*>(src) + src_elem + 16 * ch);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float4 f = p[h];
+          x[4 * h] = f.x;
+          x[4 * h + 1] = f.y;
+          x[4 * h + 2] = f.z;
+          x[4 * h + 3] = f.w;
+        }
+      }
+      const float s = isv ? a.v_scales[j] : a.k_scales[j];
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint16_t lo = static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(x[4 * q], s), __fdiv_rn(x[4 * q + 1], s)), __NV_SATFINITE,
+            __NV_E4M3));
+        const uint16_t hi = static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(x[4 * q + 2], s), __fdiv_rn(x[4 * q + 3], s)), __NV_SATFINITE,
+            __NV_E4M3));
+        w[q] = (uint32_t)lo | ((uint32_t)hi << 16);
+      }
+      val = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      val = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(src) +
+                                            src_elem * KV::bytes + 16 * ch);
+    }
+    *reinterpret_cast<uint4*>((isv ? v_tile : k_tile) + off(r, ch)) = val;
+    uint8_t* pool = static_cast<uint8_t*>(const_cast<void*>(isv ? a.v_cache : a.k_cache));
+    *reinterpret_cast<uint4*>(pool + row_byte + 16 * ch) = val;
+  }
+}
+
+}  // namespace pkv

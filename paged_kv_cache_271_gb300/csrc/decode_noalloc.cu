@@ -13,9 +13,9 @@
 // library's device code has been loaded and stays there until the process exits. Its device
 // address is looked up once per device, on the first call made with that device current; make
 // that first call before starting any stream capture on that device. All calls on a device share
-// the one array and it keeps whatever the last call left in it. Nothing in it needs to start at
-// zero: the decode kernel writes every chunk's partial result before the combine kernel reads
-// it. Two calls whose kernels can overlap on the GPU (different streams without ordering
+// the one array and it keeps whatever the last call left in it. Each call zeroes the small
+// region of per-group chunk counters that must start at zero; the partial results are written
+// before they are read. Two calls whose kernels can overlap on the GPU (different streams without ordering
 // between them) race on the array and produce wrong results; calls on one stream are safe.
 #include <mutex>
 
@@ -82,6 +82,15 @@ extern "C" int pkv_paged_decode_attention_noalloc(
   if (need > 0) {
     const int st = pkv::scratch_address(&ws);
     if (st != PKV_OK) return st;
+    // the per-group chunk counters at the end of the layout must read zero when the decode
+    // starts; every call clears them (the rest of the scratch is written before it is read)
+    const size_t counters = (size_t)batch * desc->num_kv_heads * sizeof(int);
+    const size_t at = need - ((counters + 255) & ~size_t(255));
+    const cudaError_t e =
+        cudaMemsetAsync(static_cast<char*>(ws) + at, 0, counters, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+      return pkv::set_error(PKV_ECUDA, "pkv_paged_decode_attention_noalloc: %s",
+                            cudaGetErrorString(e));
   }
   return pkv_paged_decode_attention(q, dtype_q, batch, num_q_heads, k_cache, v_cache, desc,
                                     block_tables, max_pages_per_seq, context_lens, scale, k_scales,

@@ -28,6 +28,7 @@
 #include <math.h>
 
 #include "pkv_device.cuh"
+#include "decode_epilogue.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -188,15 +189,18 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const DecodeArgs a) {
   const int c = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int ctx = max(0, a.context_lens[b]);
-  if (ctx > a.max_pages * kPageSize) {  // longer than its page table: read what the table holds
+  const bool cut = ctx > a.max_pages * kPageSize;
+  if (cut) {  // longer than its page table: read what the table holds, append nothing
     if (c == 0 && threadIdx.x == 0) atomicOr(a.err, PKV_DEVERR_BAD_PAGE);
     ctx = a.max_pages * kPageSize;
   }
   const int pages_seq = (ctx + kPageSize - 1) / kPageSize;
+  // the sequence's pages split into n_chunks near-equal chunks of at most chunk_pages pages
   const int n_chunks = (pages_seq + a.chunk_pages - 1) / a.chunk_pages;
   if (c > 0 && c >= n_chunks) return;
-  const int page0 = c * a.chunk_pages;
-  const int n_pages = max(0, min(a.chunk_pages, pages_seq - page0));
+  const int per_chunk = n_chunks > 0 ? (pages_seq + n_chunks - 1) / n_chunks : 0;
+  const int page0 = c * per_chunk;
+  const int n_pages = max(0, min(per_chunk, pages_seq - page0));
 
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
@@ -267,7 +271,12 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const DecodeArgs a) {
     }
     if (page_ok[stg]) {
       const int nvalid = min(kPageSize, ctx - (page0 + i) * kPageSize);
-      const uint8_t* kt = ring + stg * 2 * TILE;
+      uint8_t* kt = ring + stg * 2 * TILE;
+      if (a.k_new != nullptr && page0 + i == pages_seq - 1 && !cut) {
+        fused_append_row<KV, D>(a, b, j, bt[i], nvalid - 1, kt, kt + TILE, lane,
+                                [](int r, int ch) { return r * S::ROW_BYTES + 16 * ch; });
+        __syncwarp();
+      }
 #pragma unroll 1
       for (int r = 0; r < S::ROUNDS; ++r)
         decode_round<KV, D, G>(st, qf, kt, kt + TILE, r, nvalid, pbuf, lane);
@@ -305,32 +314,7 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const DecodeArgs a) {
   __syncthreads();
 
   const float vs = KV::bytes == 1 ? a.v_scales[j] : 1.f;
-  for (int e = threadIdx.x; e < G * D; e += S::kThreads) {
-    const int g = e / D, i = e % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * G + g]);
-    float L = 0.f, A = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float wt = exp2f(red_m[w * G + g] - M);
-        L = fmaf(wt, red_l[w * G + g], L);
-        A = fmaf(wt, red_acc[(w * G + g) * D + i], A);
-      }
-    }
-    A *= vs;
-    const size_t bh = (size_t)b * a.h_q + j * G + g;
-    if (n_chunks <= 1) {
-      store_from_float(static_cast<TQ*>(a.out), bh * D + i, L > 0.f ? A / L : 0.f);
-    } else {
-      a.ws_acc[(bh * a.n_chunk_slots + c) * D + i] = A;
-      if (i == 0) {
-        a.ws_ml[(bh * a.n_chunk_slots + c) * 2 + 0] = M;
-        a.ws_ml[(bh * a.n_chunk_slots + c) * 2 + 1] = L;
-      }
-    }
-  }
+  decode_epilogue<TQ, D, G, NW, S::kThreads>(a, b, j, c, n_chunks, red_acc, red_m, red_l, vs);
 }
 
 template <typename KV, typename TQ, int D, int G>

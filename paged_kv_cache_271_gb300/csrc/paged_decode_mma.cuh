@@ -30,6 +30,7 @@
 #include <math.h>
 
 #include "pkv_device.cuh"
+#include "decode_epilogue.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -153,15 +154,18 @@ __global__ void __launch_bounds__(128) paged_decode_mma_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
   int ctx = max(0, a.context_lens[b]);
-  if (ctx > a.max_pages * kPageSize) {
+  const bool cut = ctx > a.max_pages * kPageSize;
+  if (cut) {  // longer than its page table: read what the table holds, append nothing
     if (c == 0 && threadIdx.x == 0) atomicOr(a.err, PKV_DEVERR_BAD_PAGE);
     ctx = a.max_pages * kPageSize;
   }
   const int pages_seq = (ctx + kPageSize - 1) / kPageSize;
+  // the sequence's pages split into n_chunks near-equal chunks of at most chunk_pages pages
   const int n_chunks = (pages_seq + a.chunk_pages - 1) / a.chunk_pages;
   if (c > 0 && c >= n_chunks) return;
-  const int page0 = c * a.chunk_pages;
-  const int n_pages = max(0, min(a.chunk_pages, pages_seq - page0));
+  const int per_chunk = n_chunks > 0 ? (pages_seq + n_chunks - 1) / n_chunks : 0;
+  const int page0 = c * per_chunk;
+  const int n_pages = max(0, min(per_chunk, pages_seq - page0));
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -179,35 +183,6 @@ __global__ void __launch_bounds__(128) paged_decode_mma_kernel(
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
   }
   __syncthreads();
-
-  // Query fragments (MMA B operand of S^T = K Q^T), k order permuted as described above:
-  // lane (gid, tig) holds Q[g = 8 nt + gid][32 kp + 8 tig + 0..7] for every kp (bf16 path) or
-  // Q[g][16 (4 h + tig) + 4 ks + 0..3] for h = 0, 1 and ks = 0..3 (FP8 path).
-  uint32_t qf[NT][KP][4];
-  {
-    const TQ* q = static_cast<const TQ*>(a.q);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int g = nt * 8 + gid;
-      const bool live = g < G;
-      const size_t base = ((size_t)b * a.h_q + j * G + (live ? g : 0)) * D;
-#pragma unroll
-      for (int kp = 0; kp < KP; ++kp) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          int d0;
-          if constexpr (F8)
-            d0 = 16 * (4 * (kp >> 1) + tig) + 4 * (2 * (kp & 1) + (e >> 1)) + 2 * (e & 1);
-          else
-            d0 = 32 * kp + 8 * tig + 2 * e;
-          const float x0 = live ? load_as_float(q, base + d0) : 0.f;
-          const float x1 = live ? load_as_float(q, base + d0 + 1) : 0.f;
-          qf[nt][kp][e] = F8 ? pack_f16(x0, x1) : pack_bf16(x0, x1);
-        }
-      }
-    }
-  }
-  const float sc = a.scale_log2 * (F8 ? a.k_scales[j] : 1.f);
 
   const int32_t* bt = a.block_tables + (size_t)b * a.max_pages + page0;
   const uint64_t pol = l2_evict_first_policy();
@@ -238,6 +213,62 @@ __global__ void __launch_bounds__(128) paged_decode_mma_kernel(
     for (int m = 0; m < SPW && m < n_mine; ++m) issue(warp + NW * m, warp * SPW + m);
   }
 
+  // Query fragments (MMA B operand of S^T = K Q^T), k order permuted as described above:
+  // lane (gid, tig) holds Q[g = 8 nt + gid][32 kp + 8 tig + 0..7] for every kp (bf16 path) or
+  // Q[g][16 (4 h + tig) + 0..15] for h = 0, 1 (FP8 path), read with 16-byte loads.
+  uint32_t qf[NT][KP][4];
+  {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int g = nt * 8 + gid;
+      const bool live = g < G;
+      const TQ* qrow = static_cast<const TQ*>(a.q) + ((size_t)b * a.h_q + j * G + (live ? g : 0)) * D;
+      if constexpr (!F8) {
+#pragma unroll
+        for (int kp = 0; kp < KP; ++kp) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (live) v = *reinterpret_cast<const uint4*>(qrow + 32 * kp + 8 * tig);
+          qf[nt][kp][0] = v.x;
+          qf[nt][kp][1] = v.y;
+          qf[nt][kp][2] = v.z;
+          qf[nt][kp][3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float x[16];
+          const TQ* src = qrow + 16 * (4 * h + tig);
+#pragma unroll
+          for (int k = 0; k < 16; k += (int)(16 / sizeof(TQ))) {
+            if constexpr (sizeof(TQ) == 4) {
+              float4 f = live ? *reinterpret_cast<const float4*>(src + k) : make_float4(0, 0, 0, 0);
+              x[k] = f.x;
+              x[k + 1] = f.y;
+              x[k + 2] = f.z;
+              x[k + 3] = f.w;
+            } else {
+              uint4 u = live ? *reinterpret_cast<const uint4*>(src + k) : make_uint4(0, 0, 0, 0);
+              const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                x[k + 2 * t] = bf16lo(w[t]);
+                x[k + 2 * t + 1] = bf16hi(w[t]);
+              }
+            }
+          }
+          // chunk 4h+tig of a K row holds k-steps 4h .. 4h+3, four values each
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const int kp = 2 * h + (ks >> 1), half = ks & 1;
+            qf[nt][kp][2 * half] = pack_f16(x[4 * ks], x[4 * ks + 1]);
+            qf[nt][kp][2 * half + 1] = pack_f16(x[4 * ks + 2], x[4 * ks + 3]);
+          }
+        }
+      }
+    }
+  }
+  const float sc = a.scale_log2 * (F8 ? a.k_scales[j] : 1.f);
+
   float m_run[NT][2], l_run[NT][2];
   float acc[MT][NT][4];
 #pragma unroll
@@ -266,6 +297,12 @@ __global__ void __launch_bounds__(128) paged_decode_mma_kernel(
       const int nvalid = min(kPageSize, ctx - (page0 + i) * kPageSize);
       const uint32_t kt = ring_u32 + stg * S::STAGE_BYTES;
       const uint32_t vt = kt + S::TILE_BYTES;
+      if (a.k_new != nullptr && page0 + i == pages_seq - 1 && !cut) {
+        uint8_t* ktp = ring + stg * S::STAGE_BYTES;
+        fused_append_row<KV, D>(a, b, j, bt[i], nvalid - 1, ktp, ktp + S::TILE_BYTES, lane,
+                                [](int r, int ch) { return (int)swz(r, ch); });
+        __syncwarp();
+      }
 
       // ---- scores S^T[16 tokens][8 heads per n-tile] ----
       float s[NT][4];
@@ -449,32 +486,7 @@ __global__ void __launch_bounds__(128) paged_decode_mma_kernel(
   __syncthreads();
 
   const float vs = F8 ? a.v_scales[j] : 1.f;
-  for (int e = threadIdx.x; e < G * D; e += S::kThreads) {
-    const int g = e / D, i = e % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w * G + g]);
-    float L = 0.f, A = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float wt = exp2f(red_m[w * G + g] - M);
-        L = fmaf(wt, red_l[w * G + g], L);
-        A = fmaf(wt, red_acc[(w * G + g) * D + i], A);
-      }
-    }
-    A *= vs;
-    const size_t bh = (size_t)b * a.h_q + j * G + g;
-    if (n_chunks <= 1) {
-      store_from_float(static_cast<TQ*>(a.out), bh * D + i, L > 0.f ? A / L : 0.f);
-    } else {
-      a.ws_acc[(bh * a.n_chunk_slots + c) * D + i] = A;
-      if (i == 0) {
-        a.ws_ml[(bh * a.n_chunk_slots + c) * 2 + 0] = M;
-        a.ws_ml[(bh * a.n_chunk_slots + c) * 2 + 1] = L;
-      }
-    }
-  }
+  decode_epilogue<TQ, D, G, NW, S::kThreads>(a, b, j, c, n_chunks, red_acc, red_m, red_l, vs);
 }
 
 template <typename KV, typename TQ, int D, int G>

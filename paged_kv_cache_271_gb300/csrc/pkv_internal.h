@@ -18,7 +18,12 @@ struct DecodeArgs {
   const float* v_scales;
   float* ws_acc;  // [batch][h_q][n_chunk_slots][D] partial weighted values (split only)
   float* ws_ml;   // [batch][h_q][n_chunk_slots][2] partial (max, sum), log2 domain
+  int* counters;  // [batch][h_kv] finished-chunk counts (merge in place); zero between calls
   int* err;       // device error word
+  const void* k_new;  // decode step only: this step's K/V rows [batch][h_kv][D], else null
+  const void* v_new;
+  int new_dtype;      // pkv_dtype of k_new / v_new
+  int merge_in_place; // 1: the last CTA of each (request, kv head) merges the chunks
   int batch;
   int h_q;
   int h_kv;

@@ -81,7 +81,7 @@ class Scenario:
         self.out = torch.empty_like(self.q)
         maxp = self.block_tables.shape[1]
         need = pkv.decode_workspace_size(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, maxp)
-        self.workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=self.device)
+        self.workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=self.device)
 
     def all_token_rows(self):
         """Every K and V row of the workload (prefix once), the set the FP8 scales cover."""
@@ -105,6 +105,14 @@ class Scenario:
     def step(self, stream=None):
         self.append(stream)
         return self.decode(stream)
+
+    def fused_step(self, stream=None):
+        """Append + decode in one launch (pkv_paged_decode_step)."""
+        ks, vs = self.scales if self.scales else (None, None)
+        return pkv.paged_decode_step(self.q, self.k_new, self.v_new, self.cache.k, self.cache.v,
+                                     self.block_tables, self.context_lens, self.w.scale,
+                                     out=self.out, k_scales=ks, v_scales=vs,
+                                     workspace=self.workspace, stream=stream)
 
 
 def oracle_fp8_codes(w):
