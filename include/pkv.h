@@ -131,9 +131,10 @@ size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num
  *               that completes leaves it zero-filled where that matters (reuse it freely on
  *               one stream; re-zero it after a call that reported a device error; one workspace
  *               per stream). Long contexts are split into chunks of pages whose partial results
- *               (running max, sum, weighted values) are merged in a fixed order -- by the last
- *               CTA of each group when there are at most 16 chunks per sequence, else by a
- *               second kernel -- so results do not depend on physical page placement.
+ *               (running max, sum, weighted values) are merged in a fixed order -- by a
+ *               second kernel, or by the last CTA of each group when chosen with
+ *               pkv_decode_set_merge_in_place -- so results do not depend on physical page
+ *               placement.
  * Requires num_q_heads % num_kv_heads == 0 and G in {1, 2, 4, 8, 16}.
  */
 int pkv_paged_decode_attention(const void* q, int32_t dtype_q, int32_t batch,
@@ -214,6 +215,12 @@ int pkv_device_error(void* stream, int32_t* code_out);
  * fewest near-equal chunks no larger than this. 0 restores the automatic choice.
  * Process-wide; affects calls made after it returns. */
 int pkv_decode_set_chunk_pages(int32_t pages);
+
+/* Merge the chunks of a split sequence inside the decode kernel (the last CTA of each
+ * (request, KV head) to finish merges them, using a counter in the workspace) when the call has
+ * at most max_chunks chunks per sequence; 0 (the default) always uses the separate combine
+ * kernel, which measured faster on every workload tried. Process-wide. */
+int pkv_decode_set_merge_in_place(int32_t max_chunks);
 
 /* Which decode kernel pkv_paged_decode_attention uses: 0 = automatic (tensor cores for a bf16
  * or FP8 cache with head_dim 128, CUDA cores otherwise), 1 = always the CUDA-core kernel,

@@ -73,6 +73,7 @@ def lib():
         "pkv_decode_set_chunk_pages": (ctypes.c_int, [i32]),
         "pkv_decode_chunk_pages": (i32, [i32, i32, i32]),
         "pkv_decode_set_kernel": (ctypes.c_int, [i32]),
+        "pkv_decode_set_merge_in_place": (ctypes.c_int, [i32]),
         "pkv_pages_needed": (ctypes.c_int, [i64, i32, ctypes.POINTER(i64)]),
         "pkv_slot_mapping": (ctypes.c_int, [vp, i32, vp, vp, i64, i32, i32, vp]),
         "pkv_allocator_create": (ctypes.c_int, [i32, vp, ctypes.POINTER(vp)]),
@@ -272,6 +273,12 @@ def device_error(stream=None) -> int:
 
 def decode_set_chunk_pages(pages: int):
     _check(lib().pkv_decode_set_chunk_pages(int(pages)))
+
+
+def decode_set_merge_in_place(max_chunks: int):
+    """Merge split sequences inside the decode kernel when they have at most max_chunks chunks
+    (0: always the separate combine kernel)."""
+    _check(lib().pkv_decode_set_merge_in_place(int(max_chunks)))
 
 
 def decode_set_kernel(which: int):

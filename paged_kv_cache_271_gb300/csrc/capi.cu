@@ -81,8 +81,9 @@ int cuda_status(cudaError_t e, const char* what) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 std::atomic<int> g_chunk_override{0};
-// Calls whose sequences split into at most this many chunks merge them in the decode kernel.
-constexpr int kMergeInPlaceMaxChunks = 16;
+// Calls whose sequences split into at most this many chunks merge them in the decode kernel
+// (0: always the combine kernel, the default -- measured faster on every workload tried).
+std::atomic<int> g_merge_in_place_max{0};
 std::atomic<int> g_kernel_choice{0};  // 0 automatic, 1 CUDA cores, 2 tensor cores
 
 // ---- TMA tensor maps of the pools (for the tensor-core decode) -------------------------------
@@ -151,14 +152,16 @@ int pool_tensor_map(const void* base, const pkv_cache_desc* d, CUtensorMap* out)
 }
 
 // Largest chunk (pages per CTA); each sequence is split into the fewest near-equal chunks no
-// larger than this. 64 pages (1024 tokens) keeps the partials under 1 % of the KV bytes;
-// smaller when batch * kv_heads is too small to give ~1024 CTAs; one chunk when every sequence
-// fits in one.
+// larger than this (64 or 32 pages keep the partials near 1 % of the KV bytes); one chunk
+// when every sequence fits in one.
 int chunk_pages_for(int batch, int h_kv, int max_pages) {
   const int ov = g_chunk_override.load();
   if (ov > 0) return ov;
-  int chunk = 64;
+  // 64-page chunks when they still give ~3000 CTA slots, else 32 (measured on the
+  // Llama-3-8B batch-64, 70B long-context, prefix-sharing and FP8 batch-256 workloads);
+  // smaller while there would be fewer than ~1024 slots.
   const long long units = (long long)batch * h_kv;
+  int chunk = units * ((max_pages + 63) / 64) >= 3000 ? 64 : 32;
   while (chunk > 8 && units * ((max_pages + chunk - 1) / chunk) < 1024) chunk /= 2;
   if (max_pages <= chunk) chunk = max_pages < 1 ? 1 : max_pages;
   return chunk;
@@ -191,6 +194,13 @@ int pkv_decode_set_chunk_pages(int32_t pages) {
   if (pages < 0 || pages > 4096)
     return set_error(PKV_EINVAL, "pkv_decode_set_chunk_pages: %d outside [0, 4096]", pages);
   g_chunk_override.store(pages);
+  return PKV_OK;
+}
+
+int pkv_decode_set_merge_in_place(int32_t max_chunks) {
+  if (max_chunks < 0 || max_chunks > 4096)
+    return set_error(PKV_EINVAL, "pkv_decode_set_merge_in_place: %d outside [0, 4096]", max_chunks);
+  g_merge_in_place_max.store(max_chunks);
   return PKV_OK;
 }
 
@@ -282,7 +292,7 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
     a.counters = reinterpret_cast<int*>(ws + align256(rows * D * sizeof(float)) +
                                         align256(rows * 2 * sizeof(float)));
     // few chunks per sequence: the last CTA of each group merges them (no combine kernel)
-    a.merge_in_place = a.n_chunk_slots <= kMergeInPlaceMaxChunks ? 1 : 0;
+    a.merge_in_place = a.n_chunk_slots <= g_merge_in_place_max.load() ? 1 : 0;
   }
   if (k_new) {
     if (!v_new) return set_error(PKV_EINVAL, "%s: v_new is NULL", who);

@@ -35,16 +35,23 @@
 
 namespace pkv {
 
+#ifndef PKV_MMA_WARPS
+#define PKV_MMA_WARPS 4  // warps per CTA
+#endif
+#ifndef PKV_MMA_SPW
+#define PKV_MMA_SPW 2  // ring stages per warp
+#endif
+
 template <typename KV, int D, int G>
 struct MmaShape {
   static_assert(D == 128, "tensor-core decode supports head_dim 128");
   static constexpr bool kFp8 = KV::bytes == 1;
-  static constexpr int kWarps = 4;
+  static constexpr int kWarps = PKV_MMA_WARPS;
   static constexpr int kThreads = 32 * kWarps;
   static constexpr int NT = (G + 7) / 8;                 // n-tiles of 8 query heads
   static constexpr int KP = D / 32;                      // pairs of 16-wide k-steps
   static constexpr int MT = D / 16;                      // m-tiles of the P.V product
-  static constexpr int SPW = 2;                          // ring stages per warp
+  static constexpr int SPW = PKV_MMA_SPW;
   static constexpr int STAGES = kWarps * SPW;
   static constexpr int ROW_BYTES = D * KV::bytes;        // 256 (bf16) or 128 (fp8)
   static constexpr int BOXES = ROW_BYTES / 128;          // 128-byte swizzle boxes per row
@@ -144,7 +151,7 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
 }
 
 template <typename KV, typename TQ, int D, int G>
-__global__ void __launch_bounds__(128) paged_decode_mma_kernel(
+__global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
     const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v) {
   using S = MmaShape<KV, D, G>;

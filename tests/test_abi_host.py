@@ -173,9 +173,11 @@ def test_append_argument_errors_are_caught_on_the_host():
 
 def test_workspace_size_and_chunk_policy():
     pkv.decode_set_chunk_pages(0)
-    # Llama-3-8B-shaped batch 64: chunks of at most 64 pages over a 256-page table
-    assert pkv.decode_chunk_pages(64, 8, 256) == 64
-    rows = 64 * 32 * 4
+    # Llama-3-8B-shaped batch 64: chunks of at most 32 pages over a 256-page table
+    assert pkv.decode_chunk_pages(64, 8, 256) == 32
+    # Llama-3-70B-shaped long contexts (4 x 8 units over 8192 pages): 64-page chunks
+    assert pkv.decode_chunk_pages(4, 8, 8192) == 64
+    rows = 64 * 32 * 8
     # partial values, partial (max, sum), then one counter per (request, kv head)
     assert pkv.decode_workspace_size(64, 32, 8, 128, 256) == rows * 128 * 4 + rows * 2 * 4 + 256 * 8
     # everything fits one chunk: no workspace

@@ -29,10 +29,12 @@ def _gpu():
 def _clean_error_word():
     pkv.decode_set_chunk_pages(0)
     pkv.decode_set_kernel(0)
+    pkv.decode_set_merge_in_place(0)
     pkv.device_error()
     yield
     pkv.decode_set_chunk_pages(0)
     pkv.decode_set_kernel(0)
+    pkv.decode_set_merge_in_place(0)
 
 
 def _max_err(out, ref):
@@ -112,6 +114,7 @@ SHAPES = [
 @pytest.mark.parametrize("chunk", [0, 1, 3])
 @pytest.mark.parametrize("kernel", [1, 2])  # CUDA-core, tensor-core
 def test_decode_parity_shapes(kv, qd, h_q, h_kv, d, lens, chunk, kernel):
+    pkv.decode_set_merge_in_place(16 if chunk == 3 else 0)
     if kernel == 2 and (kv == "f32" or d != 128):
         pytest.skip("the tensor-core decode serves bf16/FP8 caches with head_dim 128")
     w = workloads.custom("shape", 9000 + h_q + d + len(lens), len(lens), h_q, h_kv, d, kv, qd,
@@ -147,14 +150,15 @@ STEP_SHAPES = [
 
 
 @pytest.mark.parametrize("kv,qd,h_q,h_kv,d,lens", STEP_SHAPES)
-@pytest.mark.parametrize("chunk", [0, 1])  # merge in place / separate combine kernel
+@pytest.mark.parametrize("chunk,merge", [(0, 0), (0, 16), (5, 16), (1, 0)])
 @pytest.mark.parametrize("kernel", [1, 2])
-def test_fused_step_equals_append_then_decode(kv, qd, h_q, h_kv, d, lens, chunk, kernel):
+def test_fused_step_equals_append_then_decode(kv, qd, h_q, h_kv, d, lens, chunk, merge, kernel):
     if kernel == 2 and (kv == "f32" or d != 128):
         pytest.skip("the tensor-core decode serves bf16/FP8 caches with head_dim 128")
     w = workloads.custom("step", 7000 + h_q + len(lens), len(lens), h_q, h_kv, d, kv, qd, lens)
     pkv.decode_set_chunk_pages(chunk)
     pkv.decode_set_kernel(kernel)
+    pkv.decode_set_merge_in_place(merge)
     a = Scenario(w)
     out_a = a.step().clone()
     b = Scenario(w)
