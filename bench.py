@@ -47,32 +47,89 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def workload():
+WORKLOADS = ("llama3_8b_b64", "llama3_70b_long", "prefix_sharing", "fp8_cb_b256", "fp8_cb_b64")
+
+
+def workload(name="llama3_8b_b64"):
     import workloads
-    return workloads.llama3_8b_batch64()
+    return {"llama3_8b_b64": workloads.llama3_8b_batch64,
+            "llama3_70b_long": workloads.llama3_70b_long,
+            "prefix_sharing": workloads.prefix_sharing}[name]()
 
 
-def config_of(w):
-    return {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
-            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
-            "kv_dtype": w.kv_dtype, "context_lens": "U[512,4096] seeded, sum %d"
-            % int(np.sum(w.context_lens)), "pool_pages": w.num_pages,
-            "l2": "flushed with a 256 MiB write before every timed step",
-            "step": "slot mapping (host) + paged_decode_step (append + attention, one launch)"}
+class StepState:
+    """Device state of one decode step of a workload, built through the library: the pools
+    filled by kv_append, this step's queries and new K/V rows, page tables, context lengths."""
 
+    def __init__(self, name, dev):
+        import torch
+        import paged_kv_cache_271_gb300 as pkv
+        from gpu_harness import ContinuousBatchingRun, Scenario
+        self.name = name
+        if name.startswith("fp8_cb"):
+            import workloads
+            batch = 64 if name == "fp8_cb_b64" else 256
+            tr = workloads.fp8_continuous_batching(batch=batch, steps=4)
+            run = ContinuousBatchingRun(tr, device=dev)
+            run.step()
+            self.run = run
+            self.q, self.k_new, self.v_new = run.q, run.k_new, run.v_new
+            self.k, self.v = run.cache.k, run.cache.v
+            self.bt, self.cl = run.block_tables, run.context_lens
+            self.scales = (run.k_scales, run.v_scales)
+            self.scale = tr.scale
+            self.batch, self.h_q, self.h_kv, self.d = tr.batch, tr.num_q_heads, tr.num_kv_heads, 128
+            self.kv_bytes, self.in_bytes = 1, 2
+            self.ctx_sum = int(self.cl.sum())
+            self.config = {"workload": tr.name + "_state_after_1_step", "batch": tr.batch,
+                           "num_q_heads": tr.num_q_heads, "num_kv_heads": tr.num_kv_heads,
+                           "head_dim": 128, "page_size": 16, "kv_dtype": "fp8_e4m3",
+                           "context_lens": "U[128,8192] seeded, sum %d" % self.ctx_sum}
+            self.cache = run.cache
+            self.slots = run.last_slots
+        else:
+            w = workload(name)
+            sc = Scenario(w, device=dev)
+            self.sc = sc
+            self.q, self.k_new, self.v_new = sc.q, sc.k_new, sc.v_new
+            self.k, self.v = sc.cache.k, sc.cache.v
+            self.bt, self.cl = sc.block_tables, sc.context_lens
+            self.scales = sc.scales
+            self.scale = w.scale
+            self.batch, self.h_q, self.h_kv, self.d = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+            self.kv_bytes = {"f32": 4, "bf16": 2, "fp8_e4m3": 1}[w.kv_dtype]
+            self.in_bytes = 4 if w.kv_dtype == "f32" else 2
+            self.ctx_sum = int(np.sum(w.context_lens))
+            self.config = config_of(w)
+            self.cache = sc.cache
+            self.slots = sc.step_slots
+        self.out = torch.empty_like(self.q)
+        need = pkv.decode_workspace_size(self.batch, self.h_q, self.h_kv, self.d, self.bt.shape[1])
+        self.workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
 
-def decode_bytes(w):
-    """KV of every attended token + queries + outputs (bytes)."""
-    kvb = {"f32": 4, "bf16": 2, "fp8_e4m3": 1}[w.kv_dtype]
-    qb = {"f32": 4, "bf16": 2}[w.q_dtype]
-    kv = int(np.sum(w.context_lens.astype(np.int64))) * w.num_kv_heads * w.head_dim * kvb * 2
-    return kv + 2 * w.batch * w.num_q_heads * w.head_dim * qb
+    def decode_bytes(self):
+        """K and V of every attended token + queries + outputs."""
+        return self.ctx_sum * self.h_kv * self.d * self.kv_bytes * 2 + 2 * self.batch * self.h_q * self.d * 2
 
+    def append_bytes(self):
+        return 2 * self.batch * self.h_kv * self.d * (self.in_bytes + self.kv_bytes)
 
-def append_bytes(w):
-    kvb = {"f32": 4, "bf16": 2, "fp8_e4m3": 1}[w.kv_dtype]
-    inb = 4 if w.kv_dtype == "f32" else 2
-    return 2 * w.batch * w.num_kv_heads * w.head_dim * (inb + kvb)
+    def host_step(self):
+        """Host part of the step: this step's slots from the page tables (checked)."""
+        import paged_kv_cache_271_gb300 as pkv
+        bt = self.bt.cpu().numpy() if not hasattr(self, "_bt_host") else self._bt_host
+        self._bt_host = bt
+        cl = self.cl.cpu().numpy() if not hasattr(self, "_cl_host") else self._cl_host
+        self._cl_host = cl
+        slots = pkv.slot_mapping(bt, cl.astype(np.int64) - 1, self.cache.num_pages)
+        assert np.array_equal(slots, self.slots)
+
+    def fused_step(self, stream=None):
+        import paged_kv_cache_271_gb300 as pkv
+        ks, vs = self.scales if self.scales else (None, None)
+        return pkv.paged_decode_step(self.q, self.k_new, self.v_new, self.k, self.v, self.bt,
+                                     self.cl, self.scale, out=self.out, k_scales=ks, v_scales=vs,
+                                     workspace=self.workspace, stream=stream)
 
 
 # ---- ranks -------------------------------------------------------------------------------------
@@ -250,7 +307,6 @@ def recorded_traffic():
 def run_ours(args):
     import torch
     import paged_kv_cache_271_gb300 as pkv
-    from gpu_harness import Scenario
 
     ws, rank, local = rank_info()
     if not torch.cuda.is_available():
@@ -260,17 +316,11 @@ def run_ours(args):
     init_dist(ws, "nccl")
     pkv.lib()  # fail loudly if the library is missing
 
-    w = workload()
-    sc = Scenario(w, device=dev)
+    sc = StepState(args.workload, dev)
     stream = torch.cuda.current_stream()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    per_step_bytes = decode_bytes(w) + append_bytes(w)
-
-    def step_host():
-        # host part of the hot path: this step's slots from the page tables
-        slots = pkv.slot_mapping(sc.cache.block_table_array(sc.rids),
-                                 sc.cache.context_lens_array(sc.rids) - 1, w.num_pages)
-        assert np.array_equal(slots, sc.step_slots)
+    per_step_bytes = sc.decode_bytes() + sc.append_bytes()
+    step_host = sc.host_step
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -342,32 +392,34 @@ def run_ours(args):
 
     n_dec, t_dec = launches["paged_decode"]
     dec_ms = t_dec / max(n_dec, 1)
-    kernel_bytes = decode_bytes(w) + append_bytes(w)  # the launch also appends the new rows
+    kernel_bytes = per_step_bytes  # the launch also appends the new rows
     dec_achieved = kernel_bytes / (dec_ms * 1e-3) / 1e9
-    traffic = recorded_traffic()
+    traffic = recorded_traffic() if args.workload == "llama3_8b_b64" else None
     roofline = {"bound": "hbm",
-                "kernel": "paged_decode_mma_kernel (bf16 cache, d=128, G=4, append fused)",
+                "kernel": "paged_decode kernel (%s cache, d=%d, G=%d, append fused)"
+                          % (sc.config["kv_dtype"], sc.d, sc.h_q // sc.h_kv),
                 "achieved": round(dec_achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(dec_achieved / hbm_peak, 4), "peak_kind": peak_kind,
                 "frac_of_nominal_8TBs": round(dec_achieved / NOMINAL_HBM_GBS, 4),
                 "traffic": traffic, "algorithmic_bytes_per_launch": kernel_bytes,
                 "launch_ms": round(dec_ms, 5)}
 
-    e2e = run_e2e(sc, w, args, dev, stream, flush)
+    e2e = run_e2e(sc, args, dev, stream, flush)
     max_e2e = max_over_ranks(e2e["ms_per_step"], dev)
     e2e_value = aggregate(per_step_bytes, max_e2e, ws)
 
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and args.workload == "llama3_8b_b64":
+        cpu = cpu_baseline(workload())
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": dict(config_of(w), parallelism="replicas x%d" % ws),
-            "decode_tokens_per_s": round(ws * w.batch / (max_ms * 1e-3), 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if sc.kv_bytes == 2 else ("fp8_e4m3/f16" if sc.kv_bytes == 1 else "f32"),
+            "data": "synthetic", "config": dict(sc.config, parallelism="replicas x%d" % ws),
+            "decode_tokens_per_s": round(ws * sc.batch / (max_ms * 1e-3), 1),
             "pct_of_peak": {"measured_copy_%s" % peak_kind: round(100 * value / ws / hbm_peak, 2),
                             "nominal_8TBs": round(100 * value / ws / NOMINAL_HBM_GBS, 2)},
             "roofline": roofline,
@@ -385,7 +437,7 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(sc, w, args, dev, stream, flush):
+def run_e2e(sc, args, dev, stream, flush):
     """Same step through the public API from pinned host buffers: per step the host->device
     copies of the step's inputs (queries, new K/V rows, page tables, context lengths) and the
     device->host read of the outputs sit inside the timed region."""
@@ -405,9 +457,9 @@ def run_e2e(sc, w, args, dev, stream, flush):
     def one():
         for k in host:
             dev_t[k].copy_(host[k], non_blocking=True)
-        pkv.paged_decode_step(dev_t["q"], dev_t["k_new"], dev_t["v_new"], sc.cache.k,
-                              sc.cache.v, dev_t["bt"], dev_t["cl"], w.scale, out=sc.out,
-                              k_scales=ks, v_scales=vs, workspace=sc.workspace)
+        pkv.paged_decode_step(dev_t["q"], dev_t["k_new"], dev_t["v_new"], sc.k, sc.v,
+                              dev_t["bt"], dev_t["cl"], sc.scale, out=sc.out, k_scales=ks,
+                              v_scales=vs, workspace=sc.workspace)
         out_host.copy_(sc.out, non_blocking=True)
 
     for _ in range(max(3, args.warmup)):
@@ -437,7 +489,7 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    w = workload()
+    w = workload("llama3_8b_b64")
     threads = oracle.max_threads()
     n_seq = 2
     for _ in range(args.warmup):
@@ -469,6 +521,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=WORKLOADS, default="llama3_8b_b64",
+                    help="the default is the headline layer; the others are for measurement")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("bench.py: at least 3 warm-up steps")

@@ -19,9 +19,10 @@
 //  * Values: O^T = V^T P^T with mma.m16n8k16 -- head_dim is M (8 m-tiles), heads are N, the
 //    page's tokens are K. V^T fragments come from ldmatrix.trans on the swizzled tile; P is
 //    rounded to the MMA input type and transposed through a 256-byte per-warp buffer.
-//  * FP8: codes are widened exactly to f16 (K in registers, V into a per-warp f16 staging
-//    tile), the query is used in f16, and the MMAs run in f16 with fp32 accumulation; the K
-//    scale multiplies the scores and the V scale the output.
+//  * FP8: codes are widened exactly to f16 in registers (K fragments from 16-byte loads; V^T
+//    fragments by pairing the codes of consecutive tokens with byte permutes), the query is
+//    used in f16, and the MMAs run in f16 with fp32 accumulation; the K scale multiplies the
+//    scores and the V scale the output.
 //  * Rows of the last page past the context may hold stale bytes (even NaN): their scores are
 //    set to -inf and their V rows to zero before the P.V product.
 #pragma once
@@ -59,13 +60,12 @@ struct MmaShape {
   static constexpr int TILE_BYTES = kPageSize * ROW_BYTES;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
   static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-  static constexpr int VDEQ_BYTES = kFp8 ? kWarps * kPageSize * D * 2 : 0;  // f16 V tiles
   static constexpr int PT_BYTES = kWarps * NT * 8 * kPageSize * 2;          // P^T buffers
   static constexpr int MERGE_BYTES = kWarps * G * (D + 2) * 4;
   static constexpr int BIG_BYTES =
       ((RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES) + 1023) / 1024 * 1024;
   static constexpr int SMEM_BYTES =
-      1024 + BIG_BYTES + VDEQ_BYTES + PT_BYTES + STAGES * 8 + STAGES * 4;
+      1024 + BIG_BYTES + PT_BYTES + STAGES * 8 + STAGES * 4;
 };
 
 __device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1,
@@ -178,9 +178,8 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint8_t* vdeq = smem + S::BIG_BYTES;                    // FP8 only
-  uint16_t* pt = reinterpret_cast<uint16_t*>(vdeq + S::VDEQ_BYTES) + warp * NT * 8 * kPageSize;
-  uint64_t* full = reinterpret_cast<uint64_t*>(vdeq + S::VDEQ_BYTES + S::PT_BYTES);
+  uint16_t* pt = reinterpret_cast<uint16_t*>(smem + S::BIG_BYTES) + warp * NT * 8 * kPageSize;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::BIG_BYTES + S::PT_BYTES);
   int* page_ok = reinterpret_cast<int*>(full + S::STAGES);
 
   if (threadIdx.x == 0) {
@@ -288,7 +287,6 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
       for (int e = 0; e < 4; ++e) acc[mi][nt][e] = 0.f;
   }
   const uint32_t pt_u32 = smem_u32(pt);
-  const uint32_t vdeq_u32 = smem_u32(vdeq) + warp * (kPageSize * D * 2);
 
   int m = 0;
   bool ok = true;
@@ -400,39 +398,17 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
         }
       }
 
-      // ---- V tile as 16-bit rows in the swizzled layout (FP8: widened into vdeq) ----
-      uint32_t vsrc = vt;
-      if constexpr (F8) {
-        // lane: row lane/2, dims 64*(lane%2) .. +64 = fp8 chunks 4*(lane%2) .. +4
-        const int r = lane >> 1, hb = lane & 1;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint4 w = lds128(vt + swz(r, 4 * hb + q4));
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-          uint4 o0, o1;
-          o0.x = e4m3x2_to_f16x2(ws[0]);
-          o0.y = e4m3x2_to_f16x2(ws[0] >> 16);
-          o0.z = e4m3x2_to_f16x2(ws[1]);
-          o0.w = e4m3x2_to_f16x2(ws[1] >> 16);
-          o1.x = e4m3x2_to_f16x2(ws[2]);
-          o1.y = e4m3x2_to_f16x2(ws[2] >> 16);
-          o1.z = e4m3x2_to_f16x2(ws[3]);
-          o1.w = e4m3x2_to_f16x2(ws[3] >> 16);
-          if (r >= nvalid) o0 = o1 = make_uint4(0, 0, 0, 0);
-          sts128(vdeq_u32 + swz(r, 8 * hb + 2 * q4), o0);
-          sts128(vdeq_u32 + swz(r, 8 * hb + 2 * q4 + 1), o1);
-        }
-        vsrc = vdeq_u32;
-      } else if (nvalid < kPageSize) {
-        // zero the stale rows of the last page (16 chunks of 16 bytes per row)
-        for (int e = lane; e < (kPageSize - nvalid) * 16; e += 32) {
-          const int r = nvalid + (e >> 4), ch = e & 15;
-          sts128(vt + swz(r, ch), make_uint4(0, 0, 0, 0));
+      // ---- O^T[dims][heads] += V^T P^T ----
+      if constexpr (!F8) {
+        if (nvalid < kPageSize) {
+          // zero the stale rows of the last page (16 chunks of 16 bytes per row)
+          for (int e = lane; e < (kPageSize - nvalid) * 16; e += 32) {
+            const int r = nvalid + (e >> 4), ch = e & 15;
+            sts128(vt + swz(r, ch), make_uint4(0, 0, 0, 0));
+          }
         }
       }
       __syncwarp();
-
-      // ---- O^T[dims][heads] += V^T P^T ----
       uint32_t pb[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -440,16 +416,45 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
         asm volatile("ld.shared.b32 %0, [%1];" : "=r"(pb[nt][0]) : "r"(rowg + 4 * tig));
         asm volatile("ld.shared.b32 %0, [%1];" : "=r"(pb[nt][1]) : "r"(rowg + 16 + 4 * tig));
       }
-      {
+      if constexpr (!F8) {
+        // V^T fragments straight from the swizzled bf16 tile: m-tile mi covers dims 16 mi ..
         const int q = lane >> 3, rr = lane & 7;
         const int t = (q >> 1) * 8 + rr;
 #pragma unroll
         for (int mi = 0; mi < MT; ++mi) {
           uint32_t a0, a1, a2, a3;
-          ldsm_x4_trans(vsrc + swz(t, 2 * mi + (q & 1)), a0, a1, a2, a3);
+          ldsm_x4_trans(vt + swz(t, 2 * mi + (q & 1)), a0, a1, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
-            mma16816<F8>(acc[mi][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+            mma16816<false>(acc[mi][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+        }
+      } else {
+        // V^T fragments built in registers from the FP8 tile. The lane reads 16 codes (dims
+        // 16 gid .. 16 gid + 15) of tokens 2tig, 2tig+1, 2tig+8, 2tig+9; byte permutes pair
+        // each dim's codes of consecutive tokens, which widen exactly to f16. Row gid of m-tile
+        // mi is dim 16 gid + 2 mi and row gid + 8 is dim 16 gid + 2 mi + 1 (undone in the merge).
+        uint4 vr[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int r = 2 * tig + (k & 1) + 8 * (k >> 1);
+          vr[k] = lds128(vt + swz(r, gid));
+          if (r >= nvalid) vr[k] = make_uint4(0, 0, 0, 0);  // stale rows of the last page
+        }
+#pragma unroll
+        for (int mi = 0; mi < MT; ++mi) {
+          const int wi = mi >> 1;
+          const uint32_t sel = (mi & 1) ? 0x7362u : 0x5140u;
+          const uint32_t w0 = wi == 0 ? vr[0].x : wi == 1 ? vr[0].y : wi == 2 ? vr[0].z : vr[0].w;
+          const uint32_t w1 = wi == 0 ? vr[1].x : wi == 1 ? vr[1].y : wi == 2 ? vr[1].z : vr[1].w;
+          const uint32_t w2 = wi == 0 ? vr[2].x : wi == 1 ? vr[2].y : wi == 2 ? vr[2].z : vr[2].w;
+          const uint32_t w3 = wi == 0 ? vr[3].x : wi == 1 ? vr[3].y : wi == 2 ? vr[3].z : vr[3].w;
+          const uint32_t lo = __byte_perm(w0, w1, sel);  // tokens 2tig, 2tig+1
+          const uint32_t hi = __byte_perm(w2, w3, sel);  // tokens 2tig+8, 2tig+9
+          const uint32_t a0 = e4m3x2_to_f16x2(lo), a1 = e4m3x2_to_f16x2(lo >> 16);
+          const uint32_t a2 = e4m3x2_to_f16x2(hi), a3 = e4m3x2_to_f16x2(hi >> 16);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma16816<true>(acc[mi][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
         }
       }
     }
@@ -484,8 +489,11 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
 #pragma unroll
       for (int mi = 0; mi < MT; ++mi) {
         if (g < G) {
-          red_acc[(warp * G + g) * D + mi * 16 + gid] = acc[mi][nt][k];
-          red_acc[(warp * G + g) * D + mi * 16 + gid + 8] = acc[mi][nt][k + 2];
+          // dims of rows gid and gid+8 of m-tile mi (see the two V^T fragment layouts)
+          const int i0 = F8 ? 16 * gid + 2 * mi : 16 * mi + gid;
+          const int i1 = F8 ? i0 + 1 : i0 + 8;
+          red_acc[(warp * G + g) * D + i0] = acc[mi][nt][k];
+          red_acc[(warp * G + g) * D + i1] = acc[mi][nt][k + 2];
         }
       }
     }

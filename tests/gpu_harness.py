@@ -208,6 +208,7 @@ class ContinuousBatchingRun:
         v_new = torch.stack([self.tokens[r][1][p] for r, p in zip(rids, pos)]).to(self.device)
         self.last_slots = self.cache.reserve(rids, [1] * len(rids))
         self.cache.write(self.last_slots, k_new, v_new)
+        self.k_new, self.v_new = k_new, v_new
         self.q = t.step_q(s).to(self.device)
         self.block_tables = torch.from_numpy(self.cache.block_table_array(rids)).to(self.device)
         self.context_lens = torch.from_numpy(self.cache.context_lens_array(rids)).to(self.device)
