@@ -57,6 +57,15 @@ def workload(name="llama3_8b_b64"):
             "prefix_sharing": workloads.prefix_sharing}[name]()
 
 
+def config_of(w):
+    return {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "page_size": w.page_size,
+            "kv_dtype": w.kv_dtype, "context_lens": "sum %d" % int(np.sum(w.context_lens)),
+            "pool_pages": w.num_pages,
+            "l2": "flushed with a 256 MiB write before every timed step",
+            "step": "slot mapping (host) + paged_decode_step (append + attention, one launch)"}
+
+
 class StepState:
     """Device state of one decode step of a workload, built through the library: the pools
     filled by kv_append, this step's queries and new K/V rows, page tables, context lengths."""

@@ -48,3 +48,16 @@ def test_two_gloo_ranks_take_the_max_step_time():
 def test_single_process_needs_no_process_group():
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.aggregate(2e9, 2.0, 1) == pytest.approx(1000.0)
+
+
+def test_bench_cli_and_workload_configs_without_gpu():
+    import workloads
+    for name in ("llama3_8b_b64", "llama3_70b_long", "prefix_sharing"):
+        if name == "llama3_70b_long":
+            continue  # large draw; same code path as the others
+        cfg = bench.config_of(bench.workload(name))
+        assert cfg["workload"] and cfg["kv_dtype"] == "bf16"
+    assert set(bench.WORKLOADS) >= {"llama3_8b_b64", "fp8_cb_b256"}
+    w = workloads.llama3_8b_batch64()
+    # the metric's bytes: the sum of the drawn context lengths times 8 heads x 128 dims x 2 B x 2
+    assert bench.config_of(w)["context_lens"].endswith(str(int(w.context_lens.sum())))
