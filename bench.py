@@ -454,8 +454,8 @@ def run_e2e(sc, args, dev, stream, flush):
     import paged_kv_cache_271_gb300 as pkv
     host = {
         "q": sc.q.cpu().pin_memory(), "k_new": sc.k_new.cpu().pin_memory(),
-        "v_new": sc.v_new.cpu().pin_memory(), "bt": sc.block_tables.cpu().pin_memory(),
-        "cl": sc.context_lens.cpu().pin_memory(),
+        "v_new": sc.v_new.cpu().pin_memory(), "bt": sc.bt.cpu().pin_memory(),
+        "cl": sc.cl.cpu().pin_memory(),
     }
     dev_t = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
     out_host = torch.empty(sc.out.shape, dtype=sc.out.dtype).pin_memory()
