@@ -24,7 +24,9 @@ append scatter, the page allocator model):
   reference-counted (reading: the counting scheme is not on the pages). Free list is LIFO.
 * ``decode_*`` -- section 1 (The setup) and the "Memoizing Context" page: softmax attention
   of the new token's query over all cached keys and values. GQA grouping reading: query head
-  h uses KV head h // (h_q // h_kv).
+  h uses KV head h // (h_q // h_kv). Section 8 (sliding-window cache and attention sinks):
+  with a window of W tokens only the last W are attended, plus the first S "sink" tokens when
+  S > 0 (reading: the pages give W and S as counts of positions; W = 0 means no window).
 * ``e4m3_*`` / ``quantize_e4m3`` / ``absmax_scale`` -- section 7 (KV cache quantisation,
   "fp8 KV (E4M3)"): code values per the OCP FP8 E4M3 format; readings: per-(layer, kv head)
   scale s = fp32(absmax / 448) (1 when absmax is 0), code = RNE-with-saturation of
@@ -63,10 +65,11 @@ def lib():
         L.oracle_attend.argtypes = [vp, vp, vp, i64, i32, dbl, vp]
         L.oracle_paged_decode.restype = i32
         L.oracle_paged_decode.argtypes = [vp, i32, i32, i32, i32, vp, vp, i32, i32, i32, i32,
-                                          vp, i32, vp, dbl, vp, vp, vp, i32, vp, i32]
+                                          vp, i32, vp, dbl, vp, vp, vp, i32, vp, i32, i32, i32]
         L.oracle_contiguous_decode.restype = i32
         L.oracle_contiguous_decode.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, i32, i32,
-                                               i32, vp, vp, dbl, vp, vp, vp, i32, vp, i32]
+                                               i32, vp, vp, dbl, vp, vp, vp, i32, vp, i32, i32,
+                                               i32]
         L.oracle_max_threads.restype = i32
         L.oracle_max_threads.argtypes = []
         _lib = L
@@ -258,8 +261,9 @@ def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.ndar
 
 
 def paged_decode(q_raw, q_dtype, k_pool_raw, v_pool_raw, kv_dtype, block_tables, context_lens,
-                 scale, k_scales=None, v_scales=None, pairs=None, n_threads=0):
+                 scale, k_scales=None, v_scales=None, pairs=None, n_threads=0, sink=0, window=0):
     """Decode attention through page tables. Pools: [num_pages, h_kv, P, d] raw arrays.
+    window > 0 keeps only the last ``window`` tokens plus the first ``sink`` ones.
 
     Returns float64 [B, h_q, d], or [n_pairs, d] when ``pairs`` ((b, h) rows) is given."""
     q_raw = np.ascontiguousarray(q_raw)
@@ -277,7 +281,8 @@ def paged_decode(q_raw, q_dtype, k_pool_raw, v_pool_raw, kv_dtype, block_tables,
     st = lib().oracle_paged_decode(q_raw.ctypes.data, _DT[q_dtype], B, h_q, d, kp.ctypes.data,
                                    vp.ctypes.data, _DT[kv_dtype], num_pages, h_kv, P,
                                    bt.ctypes.data, bt.shape[1], cl.ctypes.data, float(scale),
-                                   _ptr(ks), _ptr(vs), _ptr(p), n, out.ctypes.data, n_threads)
+                                   _ptr(ks), _ptr(vs), _ptr(p), n, out.ctypes.data, n_threads,
+                                   int(sink), int(window))
     if st != 0:
         raise IndexError("page id out of range in a block table")
     return out
@@ -285,7 +290,7 @@ def paged_decode(q_raw, q_dtype, k_pool_raw, v_pool_raw, kv_dtype, block_tables,
 
 def contiguous_decode(q_raw, q_dtype, k_rows_raw, v_rows_raw, kv_dtype, offsets, context_lens,
                       scale, k_scales=None, v_scales=None, prefix_k_raw=None, prefix_v_raw=None,
-                      prefix_len=0, pairs=None, n_threads=0):
+                      prefix_len=0, pairs=None, n_threads=0, sink=0, window=0):
     """Decode attention over contiguous per-request rows (the naive cache).
 
     k_rows_raw: [rows, h_kv, d]; request b's own tokens start at row offsets[b]; with a
@@ -307,12 +312,20 @@ def contiguous_decode(q_raw, q_dtype, k_rows_raw, v_rows_raw, kv_dtype, offsets,
                                    vr.ctypes.data, _ptr(pk), _ptr(pv), int(prefix_len),
                                    _DT[kv_dtype], h_kv, off.ctypes.data, cl.ctypes.data,
                                    float(scale), _ptr(ks), _ptr(vs), _ptr(p), n,
-                                   out.ctypes.data, n_threads)
+                                   out.ctypes.data, n_threads, int(sink), int(window))
     return out
 
 
+def attended_tokens(T: int, sink: int = 0, window: int = 0):
+    """Token positions a request of T tokens attends: all when window is 0, else the last
+    ``window`` plus the first ``sink`` ("KV cache and PagedAttention", section 8)."""
+    if window <= 0:
+        return list(range(T))
+    return [t for t in range(T) if t >= T - window or t < sink]
+
+
 def decode_inputs(w, pairs=None, n_threads=0, k_scales=None, v_scales=None, k_codes=None,
-                  v_codes=None):
+                  v_codes=None, sink=0, window=0):
     """Expected decode output for a ``workloads.DecodeInputs`` from its contiguous tokens.
 
     For an FP8 cache pass the per-head scales and the codes (uint8, same layout as
@@ -330,4 +343,5 @@ def decode_inputs(w, pairs=None, n_threads=0, k_scales=None, v_scales=None, k_co
         pk = as_raw(w.prefix_k, kvd) if w.prefix_len else None
         pv = as_raw(w.prefix_v, kvd) if w.prefix_len else None
     return contiguous_decode(q_raw, qd, kr, vr, kvd, w.offsets, w.context_lens, w.scale,
-                             k_scales, v_scales, pk, pv, w.prefix_len, pairs, n_threads)
+                             k_scales, v_scales, pk, pv, w.prefix_len, pairs, n_threads, sink,
+                             window)

@@ -109,6 +109,14 @@ static double read_elem(const void* base, int dtype, int64_t idx, double code_sc
 
 /* ---- attention -------------------------------------------------------------------------- */
 
+/* Tokens attended by a request of T tokens ("KV cache and PagedAttention", section 8): with a
+ * sliding window of W tokens only the last W are kept; with S attention sinks the first S are
+ * kept as well. W == 0 means no window (every token). */
+static int attended(int64_t t, int64_t T, int sink, int window) {
+  if (window <= 0) return 1;
+  return t >= T - window || t < sink;
+}
+
 /* Textbook softmax attention of one query over T keys/values, all in double:
  *   x_t = scale * <q, K_t>,  p_t = exp(x_t - max x) / sum_u exp(x_u - max x),
  *   out = sum_t p_t V_t.
@@ -139,27 +147,33 @@ void oracle_attend(const double* q, const double* K, const double* V, int64_t T,
  * token t is row t % P of page block_tables[b][t / P]. Returns -1 on an out-of-range page. */
 static int gather_paged(const void* k_pool, const void* v_pool, int kv_dtype, int num_pages,
                         int h_kv, int P, int d, const int32_t* bt_row, int64_t T, int j,
-                        double ks, double vs, double* K, double* V) {
+                        double ks, double vs, double* K, double* V, int sink, int window) {
+  int64_t n = 0;
   for (int64_t t = 0; t < T; ++t) {
+    if (!attended(t, T, sink, window)) continue; /* its page need not exist any more */
     int32_t page = bt_row[t / P];
     if (page < 0 || page >= num_pages) return -1;
     int64_t row = ((int64_t)page * h_kv + j) * P + (t % P);
     for (int i = 0; i < d; ++i) {
-      K[t * d + i] = read_elem(k_pool, kv_dtype, row * d + i, ks);
-      V[t * d + i] = read_elem(v_pool, kv_dtype, row * d + i, vs);
+      K[n * d + i] = read_elem(k_pool, kv_dtype, row * d + i, ks);
+      V[n * d + i] = read_elem(v_pool, kv_dtype, row * d + i, vs);
     }
+    ++n;
   }
   return 0;
 }
 
 /* Decode attention over a paged pool for the listed (b, h) pairs (all pairs when pairs is
  * NULL). out rows follow the pair order: out[k][d] for pair k, or out[b][h][d] for all.
- * Returns 0, or -1 if a page id is out of range (that pair's output is left at 0). */
+ * sink/window select the attended tokens as in attended() (window 0: all); pages holding no
+ * attended token are not read. Returns 0, or -1 if a page id it reads is out of range (that
+ * pair's output is left at 0). */
 int oracle_paged_decode(const void* q, int q_dtype, int B, int h_q, int d, const void* k_pool,
                         const void* v_pool, int kv_dtype, int num_pages, int h_kv, int P,
                         const int32_t* block_tables, int max_pages, const int32_t* context_lens,
                         double scale, const float* k_scales, const float* v_scales,
-                        const int32_t* pairs, int n_pairs, double* out, int n_threads) {
+                        const int32_t* pairs, int n_pairs, double* out, int n_threads,
+                        int sink, int window) {
   int G = h_q / h_kv;
   int total = pairs ? n_pairs : B * h_q;
   int status = 0;
@@ -180,11 +194,14 @@ int oracle_paged_decode(const void* q, int q_dtype, int B, int h_q, int d, const
     for (int i = 0; i < d; ++i)
       qd[i] = read_elem(q, q_dtype, ((int64_t)b * h_q + h) * d + i, 1.0);
     if (gather_paged(k_pool, v_pool, kv_dtype, num_pages, h_kv, P, d,
-                     block_tables + (int64_t)b * max_pages, T, j, ks, vs, K, V) != 0) {
+                     block_tables + (int64_t)b * max_pages, T, j, ks, vs, K, V, sink,
+                     window) != 0) {
       for (int i = 0; i < d; ++i) out[(int64_t)k * d + i] = 0.0;
       status = -1;
     } else {
-      oracle_attend(qd, K, V, T, d, scale, out + (int64_t)k * d);
+      int64_t n = 0; /* attended tokens, packed to the front by the gather */
+      for (int64_t t = 0; t < T; ++t) n += attended(t, T, sink, window);
+      oracle_attend(qd, K, V, n, d, scale, out + (int64_t)k * d);
     }
     free(qd);
     free(K);
@@ -197,13 +214,14 @@ int oracle_paged_decode(const void* q, int q_dtype, int B, int h_q, int d, const
  * t, KV head j, is row (offsets[b] + t) of kv[rows][h_kv][d]. When prefix_len > 0, tokens
  * t < prefix_len come from prefix_k/prefix_v[prefix_len][h_kv][d] instead and the request's
  * own rows start at offsets[b] for t = prefix_len. This is the naive cache ("KV cache and
- * PagedAttention", section 3) that the paged layout must reproduce. */
+ * PagedAttention", section 3) that the paged layout must reproduce. sink/window select the
+ * attended tokens as in attended() (window 0: all). */
 int oracle_contiguous_decode(const void* q, int q_dtype, int B, int h_q, int d, const void* k_rows,
                              const void* v_rows, const void* prefix_k, const void* prefix_v,
                              int prefix_len, int kv_dtype, int h_kv, const int64_t* offsets,
                              const int32_t* context_lens, double scale, const float* k_scales,
                              const float* v_scales, const int32_t* pairs, int n_pairs,
-                             double* out, int n_threads) {
+                             double* out, int n_threads, int sink, int window) {
   int G = h_q / h_kv;
   int total = pairs ? n_pairs : B * h_q;
 #ifdef _OPENMP
@@ -222,20 +240,23 @@ int oracle_contiguous_decode(const void* q, int q_dtype, int B, int h_q, int d, 
     double* V = (double*)malloc((size_t)(T > 0 ? T : 1) * d * sizeof(double));
     for (int i = 0; i < d; ++i)
       qd[i] = read_elem(q, q_dtype, ((int64_t)b * h_q + h) * d + i, 1.0);
+    int64_t n = 0; /* attended tokens, in order */
     for (int64_t t = 0; t < T; ++t) {
+      if (!attended(t, T, sink, window)) continue;
       for (int i = 0; i < d; ++i) {
         if (t < prefix_len) {
           int64_t idx = (t * h_kv + j) * d + i;
-          K[t * d + i] = read_elem(prefix_k, kv_dtype, idx, ks);
-          V[t * d + i] = read_elem(prefix_v, kv_dtype, idx, vs);
+          K[n * d + i] = read_elem(prefix_k, kv_dtype, idx, ks);
+          V[n * d + i] = read_elem(prefix_v, kv_dtype, idx, vs);
         } else {
           int64_t idx = ((offsets[b] + t - prefix_len) * h_kv + j) * d + i;
-          K[t * d + i] = read_elem(k_rows, kv_dtype, idx, ks);
-          V[t * d + i] = read_elem(v_rows, kv_dtype, idx, vs);
+          K[n * d + i] = read_elem(k_rows, kv_dtype, idx, ks);
+          V[n * d + i] = read_elem(v_rows, kv_dtype, idx, vs);
         }
       }
+      ++n;
     }
-    oracle_attend(qd, K, V, T, d, scale, out + (int64_t)k * d);
+    oracle_attend(qd, K, V, n, d, scale, out + (int64_t)k * d);
     free(qd);
     free(K);
     free(V);

@@ -411,3 +411,71 @@ def test_allocator_model_invariants():
     with pytest.raises(ValueError):
         a.decref([4, 4])  # would go below zero
     assert sum(1 for r in a.ref if r > 0) + a.num_free() == a.num_pages
+
+
+# ---- sliding window and attention sinks ("KV cache and PagedAttention", section 8) -------------
+
+def _window_case(seed, T=40, d=8, h_q=4, h_kv=2):
+    rng = np.random.default_rng(seed)
+    K = rng.standard_normal((T, h_kv, d)).astype(np.float32)
+    V = rng.standard_normal((T, h_kv, d)).astype(np.float32)
+    q = rng.standard_normal((1, h_q, d)).astype(np.float32)
+    return q, K, V
+
+
+def test_attended_token_sets():
+    assert oracle.attended_tokens(10) == list(range(10))
+    assert oracle.attended_tokens(10, window=3) == [7, 8, 9]
+    assert oracle.attended_tokens(10, sink=2, window=3) == [0, 1, 7, 8, 9]
+    assert oracle.attended_tokens(4, sink=2, window=3) == [0, 1, 2, 3]  # overlap
+    assert oracle.attended_tokens(10, sink=4, window=0) == list(range(10))  # no window
+
+
+def test_window_covering_everything_is_full_attention():
+    q, K, V = _window_case(20)
+    full = oracle.contiguous_decode(q, "f32", K, V, "f32", [0], [40], 0.4)
+    wide = oracle.contiguous_decode(q, "f32", K, V, "f32", [0], [40], 0.4, window=40)
+    wider = oracle.contiguous_decode(q, "f32", K, V, "f32", [0], [40], 0.4, sink=5, window=100)
+    np.testing.assert_array_equal(full, wide)
+    np.testing.assert_array_equal(full, wider)
+
+
+def test_window_of_one_returns_the_newest_value():
+    q, K, V = _window_case(21)
+    out = oracle.contiguous_decode(q, "f32", K, V, "f32", [0], [40], 0.4, window=1)
+    for h in range(4):
+        np.testing.assert_array_equal(out[0, h], V[39, h // 2].astype(np.float64))
+
+
+def test_window_and_sinks_match_sdpa_with_a_boolean_mask():
+    q, K, V = _window_case(22)
+    T, sink, window = 40, 3, 9
+    got = oracle.contiguous_decode(q, "f32", K, V, "f32", [0], [T], 0.4, sink=sink, window=window)
+    mask = torch.zeros(1, 1, 1, T, dtype=torch.bool)
+    for t in range(T):
+        mask[..., t] = t < sink or t >= T - window
+    qt = torch.from_numpy(q.astype(np.float64))[:, :, None, :]
+    kt = torch.from_numpy(np.ascontiguousarray(K.astype(np.float64).transpose(1, 0, 2)))[None]
+    vt = torch.from_numpy(np.ascontiguousarray(V.astype(np.float64).transpose(1, 0, 2)))[None]
+    ref = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=0.4,
+                                         enable_gqa=True)[0, :, 0, :].numpy()
+    np.testing.assert_allclose(got[0], ref, rtol=0, atol=1e-12)
+
+
+def test_paged_window_reads_only_attended_pages():
+    # pages holding no attended token may be gone (page id -1): the window never reads them
+    q, K, V = _window_case(23, T=70)
+    P = 16
+    kp = np.full((8, 2, P, 8), np.nan, dtype=np.float32)
+    vp = kp.copy()
+    table = np.array([[4, 6, 1, 3, 0]], dtype=np.int32)
+    s = oracle.slot_mapping(table, np.arange(70), P, requests=np.zeros(70, int))
+    oracle.scatter_append(kp, s, K, P)
+    oracle.scatter_append(vp, s, V, P)
+    ref = oracle.paged_decode(q, "f32", kp, vp, "f32", table, [70], 0.4, sink=4, window=20)
+    table[0, 1] = -1  # tokens 16..31: outside both the 4 sinks and the last 20
+    table[0, 2] = -1  # tokens 32..47: likewise
+    got = oracle.paged_decode(q, "f32", kp, vp, "f32", table, [70], 0.4, sink=4, window=20)
+    np.testing.assert_array_equal(got, ref)
+    cont = oracle.contiguous_decode(q, "f32", K, V, "f32", [0], [70], 0.4, sink=4, window=20)
+    np.testing.assert_array_equal(got, cont)
