@@ -166,6 +166,31 @@ int pkv_paged_decode_step(const void* q, int32_t dtype_q, int32_t batch, int32_t
                           size_t workspace_bytes, void* stream);
 
 /*
+ * Sliding-window decode with attention sinks ("KV cache and PagedAttention", section 8: keep
+ * only the last W tokens; attention sinks also keep the first few). With window > 0 a request
+ * of ctx = context_lens[b] tokens attends positions t >= ctx - window and t < sink_tokens only;
+ * pages holding no attended position are never read, so the caller may release them (their
+ * block-table entries are then ignored). window == 0 is full attention (sink_tokens must then
+ * be 0). Otherwise as pkv_paged_decode_attention / pkv_paged_decode_step.
+ */
+int pkv_paged_decode_attention_window(const void* q, int32_t dtype_q, int32_t batch,
+                                      int32_t num_q_heads, const void* k_cache,
+                                      const void* v_cache, const pkv_cache_desc* desc,
+                                      const int32_t* block_tables, int32_t max_pages_per_seq,
+                                      const int32_t* context_lens, float scale,
+                                      const float* k_scales, const float* v_scales,
+                                      int32_t sink_tokens, int32_t window, void* out,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+int pkv_paged_decode_step_window(const void* q, int32_t dtype_q, int32_t batch,
+                                 int32_t num_q_heads, const void* k_new, const void* v_new,
+                                 int32_t dtype_new, void* k_cache, void* v_cache,
+                                 const pkv_cache_desc* desc, const int32_t* block_tables,
+                                 int32_t max_pages_per_seq, const int32_t* context_lens,
+                                 float scale, const float* k_scales, const float* v_scales,
+                                 int32_t sink_tokens, int32_t window, void* out, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
  * The same decode attention as pkv_paged_decode_attention, for callers that cannot allocate
  * device memory (a plugin whose host application owns all device memory and gives it no
  * allocation hook; a server that reserved all free HBM for its KV pools at start-up; a

@@ -65,6 +65,12 @@ def lib():
                                                       f32, vp, vp, vp, vp, sz, vp]),
         "pkv_paged_decode_step": (ctypes.c_int, [vp, i32, i32, i32, vp, vp, i32, vp, vp, D, vp,
                                                  i32, vp, f32, vp, vp, vp, vp, sz, vp]),
+        "pkv_paged_decode_attention_window": (ctypes.c_int, [vp, i32, i32, i32, vp, vp, D, vp,
+                                                             i32, vp, f32, vp, vp, i32, i32, vp,
+                                                             vp, sz, vp]),
+        "pkv_paged_decode_step_window": (ctypes.c_int, [vp, i32, i32, i32, vp, vp, i32, vp, vp, D,
+                                                        vp, i32, vp, f32, vp, vp, i32, i32, vp,
+                                                        vp, sz, vp]),
         "pkv_paged_decode_attention_noalloc": (ctypes.c_int, [vp, i32, i32, i32, vp, vp, D, vp,
                                                               i32, vp, f32, vp, vp, vp, vp]),
         "pkv_decode_noalloc_scratch_bytes": (sz, []),
@@ -167,8 +173,11 @@ def decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_pages_
 
 
 def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
-                           k_scales=None, v_scales=None, workspace=None, stream=None):
-    """Read phase: decode attention of q [B, h_q, d] over the paged pools; returns out."""
+                           k_scales=None, v_scales=None, workspace=None, stream=None, window=0,
+                           sink_tokens=0):
+    """Read phase: decode attention of q [B, h_q, d] over the paged pools; returns out.
+    window > 0: attend only the last ``window`` positions plus the first ``sink_tokens``
+    (pkv_paged_decode_attention_window)."""
     if q.dim() != 3:
         raise PkvError(-2, "q must be [batch, num_q_heads, head_dim]")
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
@@ -191,16 +200,22 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
         workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     ws = _opt(workspace, "workspace")
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib().pkv_paged_decode_attention(
-        _dev(q, "q"), _dtype_code(q), B, h_q, _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
-        ctypes.byref(desc), _dev(block_tables, "block_tables"), maxp,
-        _dev(context_lens, "context_lens"), float(scale), _opt(k_scales, "k_scales"),
-        _opt(v_scales, "v_scales"), _dev(out, "out"), ws, wsb, _stream(stream)))
+    args = [_dev(q, "q"), _dtype_code(q), B, h_q, _dev(k_cache, "k_cache"),
+            _dev(v_cache, "v_cache"), ctypes.byref(desc), _dev(block_tables, "block_tables"), maxp,
+            _dev(context_lens, "context_lens"), float(scale), _opt(k_scales, "k_scales"),
+            _opt(v_scales, "v_scales")]
+    tail = [_dev(out, "out"), ws, wsb, _stream(stream)]
+    if window or sink_tokens:
+        _check(lib().pkv_paged_decode_attention_window(*args, int(sink_tokens), int(window),
+                                                       *tail))
+    else:
+        _check(lib().pkv_paged_decode_attention(*args, *tail))
     return out
 
 
 def paged_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale,
-                      out=None, k_scales=None, v_scales=None, workspace=None, stream=None):
+                      out=None, k_scales=None, v_scales=None, workspace=None, stream=None,
+                      window=0, sink_tokens=0):
     """Append + decode in one launch: k_new/v_new [B, h_kv, d] go to position
     context_lens[b] - 1 of each request, then attention over positions 0 .. context_lens[b]-1.
     A workspace, when needed, must be zero-filled before its first use (allocated zeroed here
@@ -220,12 +235,16 @@ def paged_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_l
     if need and workspace is None:
         workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib().pkv_paged_decode_step(
-        _dev(q, "q"), _dtype_code(q), B, h_q, _dev(k_new, "k_new"), _dev(v_new, "v_new"),
-        _dtype_code(k_new), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(desc),
-        _dev(block_tables, "block_tables"), maxp, _dev(context_lens, "context_lens"),
-        float(scale), _opt(k_scales, "k_scales"), _opt(v_scales, "v_scales"), _dev(out, "out"),
-        _opt(workspace, "workspace"), wsb, _stream(stream)))
+    args = [_dev(q, "q"), _dtype_code(q), B, h_q, _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+            _dtype_code(k_new), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+            ctypes.byref(desc), _dev(block_tables, "block_tables"), maxp,
+            _dev(context_lens, "context_lens"), float(scale), _opt(k_scales, "k_scales"),
+            _opt(v_scales, "v_scales")]
+    tail = [_dev(out, "out"), _opt(workspace, "workspace"), wsb, _stream(stream)]
+    if window or sink_tokens:
+        _check(lib().pkv_paged_decode_step_window(*args, int(sink_tokens), int(window), *tail))
+    else:
+        _check(lib().pkv_paged_decode_step(*args, *tail))
     return out
 
 

@@ -54,8 +54,29 @@ class PagedKVCache:
         self.lens[rid] = int(shared_len)
 
     def free_request(self, rid: int):
-        self.allocator.decref(self.pages.pop(rid))
+        self.allocator.decref([p for p in self.pages.pop(rid) if p >= 0])
         del self.lens[rid]
+
+    def release_outside_window(self, rid: int, window: int, sink_tokens: int = 0) -> int:
+        """Sliding window ("KV cache and PagedAttention", section 8): return to the allocator
+        every page of the request whose positions all lie outside the first ``sink_tokens``
+        and the last ``window`` positions (the window only moves forward, so they are never
+        read again). Their table entries become -1. Returns the number of pages released."""
+        if window <= 0:
+            return 0
+        n, P = self.lens[rid], self.page_size
+        pages = self.pages[rid]
+        released = []
+        for lp, pid in enumerate(pages):
+            if pid < 0:
+                continue
+            first, last = lp * P, min(lp * P + P, n) - 1
+            if last < n - 1 and first >= sink_tokens and last < n - window:
+                released.append(pid)
+                pages[lp] = -1
+        if released:
+            self.allocator.decref(released)
+        return len(released)
 
     def reserve(self, rids, counts) -> np.ndarray:
         """Grow each request by counts[i] tokens (allocating pages on page boundaries) and
@@ -94,7 +115,7 @@ class PagedKVCache:
         bt = np.zeros((len(rids), width), dtype=np.int32)
         for i, r in enumerate(rids):
             p = self.pages[r]
-            bt[i, :len(p)] = p
+            bt[i, :len(p)] = p  # released pages stay as -1
         return bt
 
     def context_lens_array(self, rids) -> np.ndarray:

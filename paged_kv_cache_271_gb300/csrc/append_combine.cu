@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a)
   const int h = blockIdx.x, b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ctx = min(max(0, a.context_lens[b]), a.max_pages * kPageSize);
-  const int pages_seq = (ctx + kPageSize - 1) / kPageSize;
+  const int pages_seq = seq_pages(ctx, a.sink, a.window).n;
   const int n_chunks = (pages_seq + a.chunk_pages - 1) / a.chunk_pages;
   if (n_chunks <= 1) return;
   const size_t bh = (size_t)b * a.h_q + h;

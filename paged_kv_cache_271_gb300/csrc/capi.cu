@@ -234,7 +234,7 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
                        int32_t max_pages_per_seq, const int32_t* context_lens, float scale,
                        const float* k_scales, const float* v_scales, void* out, void* workspace,
                        size_t workspace_bytes, const void* k_new, const void* v_new,
-                       int32_t dtype_new, void* stream) {
+                       int32_t dtype_new, int32_t sink_tokens, int32_t window, void* stream) {
   int st = check_desc(desc, who);
   if (st != PKV_OK) return st;
   if (batch < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0)
@@ -258,6 +258,9 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
   if (!aligned16(k_cache) || !aligned16(v_cache))
     return set_error(PKV_EALIGN, "%s: pools must be 16-byte aligned", who);
   if (!(scale == scale)) return set_error(PKV_EINVAL, "%s: scale is NaN", who);
+  if (window < 0 || sink_tokens < 0 || (window == 0 && sink_tokens != 0))
+    return set_error(PKV_EINVAL, "%s: window and sink_tokens must be >= 0; sinks need a window",
+                     who);
   if (h_kv > 65535 || batch > 65535)
     return set_error(PKV_ESHAPE, "%s: batch and kv heads must be <= 65535", who);
 
@@ -278,6 +281,8 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
   a.chunk_pages = chunk_pages_for(batch, h_kv, max_pages_per_seq);
   a.n_chunk_slots = (max_pages_per_seq + a.chunk_pages - 1) / a.chunk_pages;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.window = window;
+  a.sink = window > 0 ? sink_tokens : 0;
   if (a.n_chunk_slots > 65535) return set_error(PKV_ESHAPE, "%s: too many chunks", who);
   if (a.n_chunk_slots > 1) {
     const size_t need = pkv_decode_workspace_size(batch, num_q_heads, h_kv, D, max_pages_per_seq);
@@ -347,8 +352,22 @@ int pkv_paged_decode_attention(const void* q, int32_t dtype_q, int32_t batch,
                                void* out, void* workspace, size_t workspace_bytes, void* stream) {
   return decode_impl("pkv_paged_decode_attention", q, dtype_q, batch, num_q_heads, k_cache,
                      v_cache, desc, block_tables, max_pages_per_seq, context_lens, scale,
+                     k_scales, v_scales, out, workspace, workspace_bytes, nullptr, nullptr, 0, 0,
+                     0, stream);
+}
+
+int pkv_paged_decode_attention_window(const void* q, int32_t dtype_q, int32_t batch,
+                                      int32_t num_q_heads, const void* k_cache,
+                                      const void* v_cache, const pkv_cache_desc* desc,
+                                      const int32_t* block_tables, int32_t max_pages_per_seq,
+                                      const int32_t* context_lens, float scale,
+                                      const float* k_scales, const float* v_scales,
+                                      int32_t sink_tokens, int32_t window, void* out,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl("pkv_paged_decode_attention_window", q, dtype_q, batch, num_q_heads,
+                     k_cache, v_cache, desc, block_tables, max_pages_per_seq, context_lens, scale,
                      k_scales, v_scales, out, workspace, workspace_bytes, nullptr, nullptr, 0,
-                     stream);
+                     sink_tokens, window, stream);
 }
 
 int pkv_paged_decode_step(const void* q, int32_t dtype_q, int32_t batch, int32_t num_q_heads,
@@ -361,7 +380,23 @@ int pkv_paged_decode_step(const void* q, int32_t dtype_q, int32_t batch, int32_t
   if (!k_new) return set_error(PKV_EINVAL, "pkv_paged_decode_step: k_new is NULL");
   return decode_impl("pkv_paged_decode_step", q, dtype_q, batch, num_q_heads, k_cache, v_cache,
                      desc, block_tables, max_pages_per_seq, context_lens, scale, k_scales,
-                     v_scales, out, workspace, workspace_bytes, k_new, v_new, dtype_new, stream);
+                     v_scales, out, workspace, workspace_bytes, k_new, v_new, dtype_new, 0, 0,
+                     stream);
+}
+
+int pkv_paged_decode_step_window(const void* q, int32_t dtype_q, int32_t batch,
+                                 int32_t num_q_heads, const void* k_new, const void* v_new,
+                                 int32_t dtype_new, void* k_cache, void* v_cache,
+                                 const pkv_cache_desc* desc, const int32_t* block_tables,
+                                 int32_t max_pages_per_seq, const int32_t* context_lens,
+                                 float scale, const float* k_scales, const float* v_scales,
+                                 int32_t sink_tokens, int32_t window, void* out, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (!k_new) return set_error(PKV_EINVAL, "pkv_paged_decode_step_window: k_new is NULL");
+  return decode_impl("pkv_paged_decode_step_window", q, dtype_q, batch, num_q_heads, k_cache,
+                     v_cache, desc, block_tables, max_pages_per_seq, context_lens, scale,
+                     k_scales, v_scales, out, workspace, workspace_bytes, k_new, v_new,
+                     dtype_new, sink_tokens, window, stream);
 }
 
 

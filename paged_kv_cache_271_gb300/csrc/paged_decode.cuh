@@ -107,11 +107,14 @@ struct WarpState {
 };
 
 // One round of TOKR tokens of the page in shared memory (rows round*TOKR ..).
+// Tokens: row r of the page is position tok0 + r; rows at or past nvalid lie beyond the
+// context; win is (ctx, sink, window) for the attended-position test.
 template <typename KV, int D, int G>
 __device__ __forceinline__ void decode_round(WarpState<KV, D, G>& st,
                                              const float (&qf)[G][D / 32],
                                              const uint8_t* k_tile, const uint8_t* v_tile,
-                                             int round, int nvalid, float* pb, int lane) {
+                                             int round, int nvalid, int tok0, int3 win, float* pb,
+                                             int lane) {
   using S = DecodeShape<KV, D, G>;
   constexpr int DL = S::DL, TOKR = S::TOKR, NV = S::NV, H = S::H;
   float part[NV];
@@ -135,7 +138,7 @@ __device__ __forceinline__ void decode_round(WarpState<KV, D, G>& st,
 #pragma unroll
   for (int r = 0; r < H; ++r) {
     const int tok = round * TOKR + (base % TOKR) + r;
-    s[r] = (tok < nvalid) ? part[r] : -INFINITY;
+    s[r] = attended(tok0 + tok, win.x, win.y, win.z) ? part[r] : -INFINITY;
     mx = fmaxf(mx, s[r]);
   }
   mx = run_max<S::RUN>(mx);
@@ -194,8 +197,9 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const DecodeArgs a) {
     if (c == 0 && threadIdx.x == 0) atomicOr(a.err, PKV_DEVERR_BAD_PAGE);
     ctx = a.max_pages * kPageSize;
   }
-  const int pages_seq = (ctx + kPageSize - 1) / kPageSize;
-  // the sequence's pages split into n_chunks near-equal chunks of at most chunk_pages pages
+  const SeqPages sp = seq_pages(ctx, a.sink, a.window);
+  const int pages_seq = sp.n;  // attended pages
+  // the attended pages split into n_chunks near-equal chunks of at most chunk_pages pages
   const int n_chunks = (pages_seq + a.chunk_pages - 1) / a.chunk_pages;
   if (c > 0 && c >= n_chunks) return;
   const int per_chunk = n_chunks > 0 ? (pages_seq + n_chunks - 1) / n_chunks : 0;
@@ -228,11 +232,11 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const DecodeArgs a) {
 
   const uint8_t* kc = static_cast<const uint8_t*>(a.k_cache);
   const uint8_t* vc = static_cast<const uint8_t*>(a.v_cache);
-  const int32_t* bt = a.block_tables + (size_t)b * a.max_pages + page0;
+  const int32_t* btrow = a.block_tables + (size_t)b * a.max_pages;
   const uint64_t pol = l2_evict_first_policy();
 
   auto issue = [&](int i, int stg) {  // lane 0: fetch page i of the chunk into stage stg
-    const int pid = bt[i];
+    const int pid = btrow[logical_page(sp, page0 + i)];
     if (pid < 0 || pid >= a.num_pages) {
       page_ok[stg] = 0;
       atomicOr(a.err, PKV_DEVERR_BAD_PAGE);
@@ -270,16 +274,18 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const DecodeArgs a) {
       break;
     }
     if (page_ok[stg]) {
-      const int nvalid = min(kPageSize, ctx - (page0 + i) * kPageSize);
+      const int lp = logical_page(sp, page0 + i);
+      const int nvalid = min(kPageSize, ctx - lp * kPageSize);
       uint8_t* kt = ring + stg * 2 * TILE;
       if (a.k_new != nullptr && page0 + i == pages_seq - 1 && !cut) {
-        fused_append_row<KV, D>(a, b, j, bt[i], nvalid - 1, kt, kt + TILE, lane,
+        fused_append_row<KV, D>(a, b, j, btrow[lp], nvalid - 1, kt, kt + TILE, lane,
                                 [](int r, int ch) { return r * S::ROW_BYTES + 16 * ch; });
         __syncwarp();
       }
 #pragma unroll 1
       for (int r = 0; r < S::ROUNDS; ++r)
-        decode_round<KV, D, G>(st, qf, kt, kt + TILE, r, nvalid, pbuf, lane);
+        decode_round<KV, D, G>(st, qf, kt, kt + TILE, r, nvalid, lp * kPageSize,
+                               make_int3(ctx, a.sink, a.window), pbuf, lane);
     }
     __syncwarp();
     if (lane == 0 && m + SPW < n_mine) {

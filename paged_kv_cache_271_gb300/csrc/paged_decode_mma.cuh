@@ -166,8 +166,9 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
     if (c == 0 && threadIdx.x == 0) atomicOr(a.err, PKV_DEVERR_BAD_PAGE);
     ctx = a.max_pages * kPageSize;
   }
-  const int pages_seq = (ctx + kPageSize - 1) / kPageSize;
-  // the sequence's pages split into n_chunks near-equal chunks of at most chunk_pages pages
+  const SeqPages sp = seq_pages(ctx, a.sink, a.window);
+  const int pages_seq = sp.n;  // attended pages
+  // the attended pages split into n_chunks near-equal chunks of at most chunk_pages pages
   const int n_chunks = (pages_seq + a.chunk_pages - 1) / a.chunk_pages;
   if (c > 0 && c >= n_chunks) return;
   const int per_chunk = n_chunks > 0 ? (pages_seq + n_chunks - 1) / n_chunks : 0;
@@ -190,12 +191,12 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
   }
   __syncthreads();
 
-  const int32_t* bt = a.block_tables + (size_t)b * a.max_pages + page0;
+  const int32_t* btrow = a.block_tables + (size_t)b * a.max_pages;
   const uint64_t pol = l2_evict_first_policy();
   const uint32_t ring_u32 = smem_u32(ring);
 
   auto issue = [&](int i, int stg) {  // lane 0: fetch page i of the chunk into stage stg
-    const int pid = bt[i];
+    const int pid = btrow[logical_page(sp, page0 + i)];
     if (pid < 0 || pid >= a.num_pages) {
       page_ok[stg] = 0;
       atomicOr(a.err, PKV_DEVERR_BAD_PAGE);
@@ -299,12 +300,13 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
       break;
     }
     if (page_ok[stg]) {
-      const int nvalid = min(kPageSize, ctx - (page0 + i) * kPageSize);
+      const int lp = logical_page(sp, page0 + i);
+      const int nvalid = min(kPageSize, ctx - lp * kPageSize);  // rows before the context end
       const uint32_t kt = ring_u32 + stg * S::STAGE_BYTES;
       const uint32_t vt = kt + S::TILE_BYTES;
       if (a.k_new != nullptr && page0 + i == pages_seq - 1 && !cut) {
         uint8_t* ktp = ring + stg * S::STAGE_BYTES;
-        fused_append_row<KV, D>(a, b, j, bt[i], nvalid - 1, ktp, ktp + S::TILE_BYTES, lane,
+        fused_append_row<KV, D>(a, b, j, btrow[lp], nvalid - 1, ktp, ktp + S::TILE_BYTES, lane,
                                 [](int r, int ch) { return (int)swz(r, ch); });
         __syncwarp();
       }
@@ -347,7 +349,8 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
       }
 
       // ---- online softmax: lane holds tokens gid, gid+8 of heads 8nt+2tig, 8nt+2tig+1 ----
-      const bool v0 = gid < nvalid, v8 = gid + 8 < nvalid;
+      const bool v0 = attended(lp * kPageSize + gid, ctx, a.sink, a.window);
+      const bool v8 = attended(lp * kPageSize + gid + 8, ctx, a.sink, a.window);
       float alpha[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {

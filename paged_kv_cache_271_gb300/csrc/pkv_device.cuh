@@ -40,6 +40,38 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
+// ---- which pages a request attends ----------------------------------------------------------
+
+// With a sliding window of W positions (plus S attention sinks) a request of ctx tokens attends
+// positions t >= ctx - W and t < S; without a window (W = 0) every position. Its attended
+// pages, in logical order, are numbered 0 .. n-1: the first `sink_pages` are logical pages
+// 0 .. sink_pages-1, the rest logical pages win_first, win_first + 1, ... Pages holding no
+// attended position are not read (their table entries may be released).
+struct SeqPages {
+  int n;
+  int sink_pages;
+  int win_first;
+};
+
+__device__ __forceinline__ SeqPages seq_pages(int ctx, int sink, int window) {
+  const int pages = (ctx + kPageSize - 1) / kPageSize;
+  SeqPages r{pages, pages, pages};
+  if (window > 0) {
+    const int wp = max(0, ctx - window) / kPageSize;
+    const int sp = min((max(0, sink) + kPageSize - 1) / kPageSize, pages);
+    if (wp > sp) r = SeqPages{sp + (pages - wp), sp, wp};
+  }
+  return r;
+}
+
+__device__ __forceinline__ int logical_page(const SeqPages& s, int v) {
+  return v < s.sink_pages ? v : s.win_first + (v - s.sink_pages);
+}
+
+__device__ __forceinline__ bool attended(int t, int ctx, int sink, int window) {
+  return t < ctx && (window <= 0 || t >= ctx - window || t < sink);
+}
+
 // ---- mbarrier ------------------------------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -24,6 +24,8 @@ struct DecodeArgs {
   const void* v_new;
   int new_dtype;      // pkv_dtype of k_new / v_new
   int merge_in_place; // 1: the last CTA of each (request, kv head) merges the chunks
+  int window;         // > 0: attend only the last `window` positions (plus `sink` first ones)
+  int sink;
   int batch;
   int h_q;
   int h_kv;

@@ -106,13 +106,19 @@ class Scenario:
         self.append(stream)
         return self.decode(stream)
 
-    def fused_step(self, stream=None):
-        """Append + decode in one launch (pkv_paged_decode_step)."""
+    def fused_step(self, stream=None, window=0, sink_tokens=0):
+        """Append + decode in one launch (pkv_paged_decode_step[_window])."""
         ks, vs = self.scales if self.scales else (None, None)
         return pkv.paged_decode_step(self.q, self.k_new, self.v_new, self.cache.k, self.cache.v,
                                      self.block_tables, self.context_lens, self.w.scale,
                                      out=self.out, k_scales=ks, v_scales=vs,
-                                     workspace=self.workspace, stream=stream)
+                                     workspace=self.workspace, stream=stream, window=window,
+                                     sink_tokens=sink_tokens)
+
+    def refresh_tables(self):
+        """Re-upload the page tables (after pages were released)."""
+        self.block_tables = torch.from_numpy(
+            self.cache.block_table_array(self.rids, self.block_tables.shape[1])).to(self.device)
 
 
 def oracle_fp8_codes(w):
@@ -126,14 +132,14 @@ def oracle_fp8_codes(w):
     return ks, vs, kc, vc
 
 
-def oracle_expected(w, pairs=None, n_threads=0):
+def oracle_expected(w, pairs=None, n_threads=0, sink=0, window=0):
     """The oracle's decode output for w, from its own contiguous tokens (and, for FP8, its own
     scales and quantiser). float64 [B, h_q, d] or [n_pairs, d]."""
     if w.kv_dtype != "fp8_e4m3":
-        return oracle.decode_inputs(w, pairs=pairs, n_threads=n_threads)
+        return oracle.decode_inputs(w, pairs=pairs, n_threads=n_threads, sink=sink, window=window)
     ks, vs, kc, vc = oracle_fp8_codes(w)
     return oracle.decode_inputs(w, pairs=pairs, n_threads=n_threads, k_scales=ks, v_scales=vs,
-                                k_codes=kc, v_codes=vc)
+                                k_codes=kc, v_codes=vc, sink=sink, window=window)
 
 
 def tolerance(w) -> float:

@@ -218,3 +218,23 @@ def test_cache_bookkeeping_matches_oracle_without_gpu():
     c.free_request(3)
     c.free_request(0)
     assert c.allocator.num_free() == 40
+
+
+def test_release_outside_window_bookkeeping():
+    import torch
+    c = PagedKVCache(20, 2, 64, torch.float32, device="cpu")
+    c.add_request(0)
+    c.reserve([0], [100])  # 7 pages: positions 0..99
+    pages = list(c.pages[0])
+    # window of the last 20 positions (80..99) plus 4 sinks (0..3): pages 1..4 hold none
+    assert c.release_outside_window(0, 20, 4) == 4
+    assert c.pages[0] == [pages[0], -1, -1, -1, -1, pages[5], pages[6]]
+    assert c.allocator.num_free() == 20 - 3
+    assert c.release_outside_window(0, 20, 4) == 0  # idempotent
+    assert c.release_outside_window(0, 0) == 0  # no window: nothing to release
+    bt = c.block_table_array([0])
+    assert list(bt[0, :7]) == c.pages[0]
+    c.reserve([0], [20])  # the window moves on; new pages still map by position
+    assert len(c.pages[0]) == 8
+    c.free_request(0)
+    assert c.allocator.num_free() == 20
