@@ -220,6 +220,16 @@ int pkv_paged_decode_attention_noalloc(const void* q, int32_t dtype_q, int32_t b
 size_t pkv_decode_noalloc_scratch_bytes(void);
 
 /*
+ * Copy whole pages of both pools (every KV head): for p < n, page dst_pages[p] becomes a copy
+ * of page src_pages[p] (device int32 arrays). With pkv_cow_page this gives copy-on-write for
+ * pages shared across sequences ("KV Cache" glossary: blocks shared for parallel sampling and
+ * beam search; the copy rule is this library's reading). An id outside [0, num_pages) skips
+ * that page and sets PKV_DEVERR_BAD_PAGE. Source and destination pages must not overlap.
+ */
+int pkv_copy_pages(void* k_cache, void* v_cache, const pkv_cache_desc* desc,
+                   const int32_t* src_pages, const int32_t* dst_pages, int32_t n, void* stream);
+
+/*
  * Per-KV-head scales for an FP8 cache (section 7; granularity is this library's reading):
  *   scales_out[h] = fp32(max |x[:, h, :]| / 448), or 1 if that maximum is 0.
  *  x           device [n_tokens][num_kv_heads][head_dim] of dtype (F32 or BF16), 16-byte
@@ -292,6 +302,13 @@ int pkv_incref(pkv_allocator* a, const int32_t* ids, int32_t n);
 /* One reference less to each listed page; a page reaching 0 returns to the free list.
  * PKV_EREFCNT (nothing changed) if an id is out of range or would drop below 0. */
 int pkv_decref(pkv_allocator* a, const int32_t* ids, int32_t n);
+/* Copy-on-write before writing position `position` of a request whose pages are row[0..n)
+ * (host array): if the page holding it is shared (reference count > 1) it is replaced in row by
+ * a newly allocated page, the old page loses this request's reference, and *copy_src/*copy_dst
+ * name the page contents to copy (pkv_copy_pages) before the write; otherwise both are -1
+ * (also when the position starts a page the request does not have yet). */
+int pkv_cow_page(pkv_allocator* a, int32_t* row, int32_t n, int64_t position, int32_t page_size,
+                 int32_t* copy_src, int32_t* copy_dst);
 int32_t pkv_num_free(const pkv_allocator* a);
 /* Reference count of a page, or -1 for an id out of range. */
 int32_t pkv_refcount(const pkv_allocator* a, int32_t id);

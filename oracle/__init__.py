@@ -31,6 +31,9 @@ append scatter, the page allocator model):
   "fp8 KV (E4M3)"): code values per the OCP FP8 E4M3 format; readings: per-(layer, kv head)
   scale s = fp32(absmax / 448) (1 when absmax is 0), code = RNE-with-saturation of
   fp32(x / s).
+* ``quantize_int8`` -- section 7, "INT8 KV: similar" (no scheme given); reading: symmetric
+  codes in [-127, 127], s = fp32(absmax / 127), code = fp32(x / s) rounded half-to-even and
+  clamped.
 """
 from __future__ import annotations
 
@@ -42,8 +45,8 @@ import torch
 
 from . import build as _build
 
-F32, BF16, E4M3 = 0, 1, 2
-_DT = {"f32": F32, "bf16": BF16, "fp8_e4m3": E4M3}
+F32, BF16, E4M3, INT8 = 0, 1, 2, 3
+_DT = {"f32": F32, "bf16": BF16, "fp8_e4m3": E4M3, "int8": INT8}
 
 _lib = None
 
@@ -61,6 +64,8 @@ def lib():
         L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
         L.oracle_quantize_e4m3.restype = None
         L.oracle_quantize_e4m3.argtypes = [vp, i64, ctypes.c_float, vp]
+        L.oracle_quantize_int8.restype = None
+        L.oracle_quantize_int8.argtypes = [vp, i64, ctypes.c_float, vp]
         L.oracle_attend.restype = None
         L.oracle_attend.argtypes = [vp, vp, vp, i64, i32, dbl, vp]
         L.oracle_paged_decode.restype = i32
@@ -211,17 +216,27 @@ def quantize_e4m3(x: np.ndarray, s: float) -> np.ndarray:
     return out
 
 
-def absmax_scale(x: np.ndarray) -> np.float32:
-    """fp32(max |x| / 448), or 1 when every element is zero. x: float32 values."""
+def absmax_scale(x: np.ndarray, qmax: float = 448.0) -> np.float32:
+    """fp32(max |x| / qmax), or 1 when every element is zero. x: float32 values; qmax 448 for
+    E4M3 codes, 127 for INT8 codes."""
     a = np.float32(np.max(np.abs(np.asarray(x, dtype=np.float32)))) if np.size(x) else np.float32(0)
     if a == 0:
         return np.float32(1.0)
-    return np.float32(a) / np.float32(448.0)
+    return np.float32(a) / np.float32(qmax)
 
 
-def absmax_scales_per_head(x: np.ndarray) -> np.ndarray:
+def absmax_scales_per_head(x: np.ndarray, qmax: float = 448.0) -> np.ndarray:
     """x: [tokens, h_kv, d] float32 -> float32 [h_kv] scales, one per KV head."""
-    return np.array([absmax_scale(x[:, j, :]) for j in range(x.shape[1])], dtype=np.float32)
+    return np.array([absmax_scale(x[:, j, :], qmax) for j in range(x.shape[1])],
+                    dtype=np.float32)
+
+
+def quantize_int8(x: np.ndarray, s: float) -> np.ndarray:
+    """int8 codes: fp32(x / s) rounded to nearest (ties to even), clamped to [-127, 127]."""
+    xf = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(xf.shape, dtype=np.int8)
+    lib().oracle_quantize_int8(xf.ctypes.data, xf.size, ctypes.c_float(s), out.ctypes.data)
+    return out
 
 
 # ---- conversions of torch CPU tensors to what the C oracle reads ---------------------------
@@ -235,6 +250,8 @@ def as_raw(t: torch.Tensor, dtype: str) -> np.ndarray:
         if t.dtype == torch.uint8:
             return t.numpy()
         return t.view(torch.uint8).numpy()
+    if dtype == "int8":
+        return t.view(torch.int8).numpy()
     return t.to(torch.float32).numpy()
 
 
@@ -332,11 +349,11 @@ def decode_inputs(w, pairs=None, n_threads=0, k_scales=None, v_scales=None, k_co
     ``w.k_tokens``) the oracle's own quantiser produced."""
     qd = w.q_dtype
     q_raw = as_raw(w.q, qd)
-    if w.kv_dtype == "fp8_e4m3":
-        kr, vr, kvd = k_codes, v_codes, "fp8_e4m3"
+    if w.kv_dtype in ("fp8_e4m3", "int8"):
+        kr, vr, kvd = k_codes, v_codes, w.kv_dtype
         pk = pv = None
         if w.prefix_len:
-            raise NotImplementedError("fp8 with a shared prefix")
+            raise NotImplementedError("quantised cache with a shared prefix")
     else:
         kvd = w.kv_dtype
         kr, vr = as_raw(w.k_tokens, kvd), as_raw(w.v_tokens, kvd)

@@ -33,7 +33,7 @@
 #include <omp.h>
 #endif
 
-enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2, ORC_INT8 = 3 };
 
 /* ---- OCP FP8 E4M3 ------------------------------------------------------------------- */
 
@@ -90,6 +90,21 @@ void oracle_quantize_e4m3(const float* x, int64_t n, float s, uint8_t* out) {
   }
 }
 
+/* ---- INT8 ------------------------------------------------------------------------------- */
+
+/* "INT8 KV" ("KV cache and PagedAttention", section 7) with the reading taken here: a
+ * symmetric code c in [-127, 127], value = c * scale, code = fp32(x / scale) rounded to the
+ * nearest integer (ties to even) and clamped to [-127, 127]. Inputs are finite. */
+void oracle_quantize_int8(const float* x, int64_t n, float s, int8_t* out) {
+  for (int64_t i = 0; i < n; ++i) {
+    float y = x[i] / s;
+    double r = nearbyint((double)y); /* default rounding mode: to nearest, ties to even */
+    if (r > 127.0) r = 127.0;
+    if (r < -127.0) r = -127.0;
+    out[i] = (int8_t)r;
+  }
+}
+
 /* ---- exact element reads --------------------------------------------------------------- */
 
 static double bf16_value(uint16_t bits) {
@@ -103,6 +118,7 @@ static double read_elem(const void* base, int dtype, int64_t idx, double code_sc
   switch (dtype) {
     case ORC_F32: return (double)((const float*)base)[idx];
     case ORC_BF16: return bf16_value(((const uint16_t*)base)[idx]);
+    case ORC_INT8: return (double)((const int8_t*)base)[idx] * code_scale;
     default: return oracle_e4m3_value(((const uint8_t*)base)[idx]) * code_scale;
   }
 }
@@ -186,8 +202,8 @@ int oracle_paged_decode(const void* q, int q_dtype, int B, int h_q, int d, const
     int h = pairs ? pairs[2 * k + 1] : k % h_q;
     int j = h / G;
     int64_t T = context_lens[b];
-    double ks = (kv_dtype == ORC_E4M3) ? (double)k_scales[j] : 1.0;
-    double vs = (kv_dtype == ORC_E4M3) ? (double)v_scales[j] : 1.0;
+    double ks = (kv_dtype >= ORC_E4M3) ? (double)k_scales[j] : 1.0;
+    double vs = (kv_dtype >= ORC_E4M3) ? (double)v_scales[j] : 1.0;
     double* qd = (double*)malloc((size_t)d * sizeof(double));
     double* K = (double*)malloc((size_t)(T > 0 ? T : 1) * d * sizeof(double));
     double* V = (double*)malloc((size_t)(T > 0 ? T : 1) * d * sizeof(double));
@@ -233,8 +249,8 @@ int oracle_contiguous_decode(const void* q, int q_dtype, int B, int h_q, int d, 
     int h = pairs ? pairs[2 * k + 1] : k % h_q;
     int j = h / G;
     int64_t T = context_lens[b];
-    double ks = (kv_dtype == ORC_E4M3) ? (double)k_scales[j] : 1.0;
-    double vs = (kv_dtype == ORC_E4M3) ? (double)v_scales[j] : 1.0;
+    double ks = (kv_dtype >= ORC_E4M3) ? (double)k_scales[j] : 1.0;
+    double vs = (kv_dtype >= ORC_E4M3) ? (double)v_scales[j] : 1.0;
     double* qd = (double*)malloc((size_t)d * sizeof(double));
     double* K = (double*)malloc((size_t)(T > 0 ? T : 1) * d * sizeof(double));
     double* V = (double*)malloc((size_t)(T > 0 ? T : 1) * d * sizeof(double));

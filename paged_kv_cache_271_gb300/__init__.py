@@ -88,6 +88,9 @@ def lib():
         "pkv_incref": (ctypes.c_int, [vp, vp, i32]),
         "pkv_decref": (ctypes.c_int, [vp, vp, i32]),
         "pkv_num_free": (i32, [vp]),
+        "pkv_cow_page": (ctypes.c_int, [vp, vp, i32, i64, i32, ctypes.POINTER(i32),
+                                        ctypes.POINTER(i32)]),
+        "pkv_copy_pages": (ctypes.c_int, [vp, vp, D, vp, vp, i32, vp]),
         "pkv_refcount": (i32, [vp, i32]),
         "pkv_trace_enable": (ctypes.c_int, [ctypes.c_int]),
         "pkv_trace_reset": (ctypes.c_int, []),
@@ -269,6 +272,18 @@ def paged_decode_attention_noalloc(q, k_cache, v_cache, block_tables, context_le
     return out
 
 
+def copy_pages(k_cache, v_cache, src_pages, dst_pages, stream=None):
+    """pool[dst_pages[p]] = pool[src_pages[p]] for both pools (device int32 id tensors)."""
+    if src_pages.dtype != torch.int32 or dst_pages.dtype != torch.int32:
+        raise PkvError(-3, "page ids must be int32")
+    if src_pages.numel() != dst_pages.numel():
+        raise PkvError(-2, "src_pages and dst_pages differ in length")
+    desc = cache_desc(k_cache)
+    _check(lib().pkv_copy_pages(_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                                ctypes.byref(desc), _dev(src_pages, "src_pages"),
+                                _dev(dst_pages, "dst_pages"), src_pages.numel(), _stream(stream)))
+
+
 def kv_absmax_scales(x, scales_out=None, stream=None):
     """FP8 scales per KV head: fp32(max|x[:, h, :]| / 448) (1 for an all-zero head)."""
     if x.dim() != 3:
@@ -364,6 +379,17 @@ class PageAllocator:
 
     def refcount(self, page_id: int) -> int:
         return int(lib().pkv_refcount(self._h, int(page_id)))
+
+    def cow_page(self, row: list, position: int, page_size: int = 16):
+        """Copy-on-write for a write at ``position`` of a request with pages ``row`` (updated
+        in place). Returns (src, dst) to copy, or None when the page is private."""
+        a = np.ascontiguousarray(np.asarray(row, dtype=np.int32))
+        src, dst = ctypes.c_int32(-1), ctypes.c_int32(-1)
+        _check(lib().pkv_cow_page(self._h, a.ctypes.data if a.size else None, a.size,
+                                  int(position), int(page_size), ctypes.byref(src),
+                                  ctypes.byref(dst)))
+        row[:] = [int(x) for x in a]
+        return None if src.value < 0 else (int(src.value), int(dst.value))
 
 
 def trace_enable(on: bool = True):

@@ -14,7 +14,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import PageAllocator, PkvError, kv_append, pages_needed, slot_mapping
+from . import PageAllocator, PkvError, copy_pages, kv_append, pages_needed, slot_mapping
 
 
 class PagedKVCache:
@@ -53,6 +53,18 @@ class PagedKVCache:
         self.pages[rid] = pages
         self.lens[rid] = int(shared_len)
 
+    def fork(self, src_rid: int, new_rid: int):
+        """A new request sharing every page of ``src_rid`` (parallel sampling, beam search);
+        writes into a shared, partly filled page first copy it (``reserve`` does that)."""
+        if new_rid in self.pages:
+            raise PkvError(-1, "request %d exists" % new_rid)
+        pages = list(self.pages[src_rid])
+        live = [p for p in pages if p >= 0]
+        if live:
+            self.allocator.incref(live)
+        self.pages[new_rid] = pages
+        self.lens[new_rid] = self.lens[src_rid]
+
     def free_request(self, rid: int):
         self.allocator.decref([p for p in self.pages.pop(rid) if p >= 0])
         del self.lens[rid]
@@ -83,7 +95,12 @@ class PagedKVCache:
         return the int64 slots of the new positions, request by request."""
         rids = list(rids)
         counts = [int(c) for c in counts]
+        copies = []
         for rid, n in zip(rids, counts):
+            if n > 0:  # copy-on-write of a shared, partly filled page before writing into it
+                pair = self.allocator.cow_page(self.pages[rid], self.lens[rid], self.page_size)
+                if pair is not None:
+                    copies.append(pair)
             need = pages_needed(self.lens[rid] + n, self.page_size) - len(self.pages[rid])
             if need > 0:
                 self.pages[rid].extend(int(p) for p in self.allocator.alloc(need))
@@ -98,6 +115,10 @@ class PagedKVCache:
             pos[o:o + n] = np.arange(self.lens[rid], self.lens[rid] + n)
             o += n
             self.lens[rid] += n
+        if copies:
+            src = torch.tensor([c[0] for c in copies], dtype=torch.int32, device=self.k.device)
+            dst = torch.tensor([c[1] for c in copies], dtype=torch.int32, device=self.k.device)
+            copy_pages(self.k, self.v, src, dst)
         return slot_mapping(table, pos, self.num_pages, requests=req, page_size=self.page_size)
 
     def write(self, slots, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):

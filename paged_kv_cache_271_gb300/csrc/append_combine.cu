@@ -237,6 +237,29 @@ cudaError_t launch_combine_t(const DecodeArgs& a, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, decode_combine_kernel<TQ, D>, a);
 }
 
+// Copy whole pages (every KV head's tile) of both pools: pool[dst[p]] = pool[src[p]]. One
+// thread moves 16 bytes of K and the same 16 bytes of V. Out-of-range ids are skipped and
+// flagged as bad pages.
+__global__ void copy_pages_kernel(uint8_t* k, uint8_t* v, const int32_t* src, const int32_t* dst,
+                                  int n, int64_t page_bytes, int num_pages, int* err) {
+  const int64_t vecs = page_bytes / 16;
+  const int64_t total = (int64_t)n * vecs;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int p = (int)(idx / vecs);
+    const int64_t off = (idx % vecs) * 16;
+    const int s = src[p], d = dst[p];
+    if (s < 0 || s >= num_pages || d < 0 || d >= num_pages) {
+      atomicOr(err, PKV_DEVERR_BAD_PAGE);
+      continue;
+    }
+    *reinterpret_cast<uint4*>(k + d * page_bytes + off) =
+        *reinterpret_cast<const uint4*>(k + s * page_bytes + off);
+    *reinterpret_cast<uint4*>(v + d * page_bytes + off) =
+        *reinterpret_cast<const uint4*>(v + s * page_bytes + off);
+  }
+}
+
 inline int grid_for(int64_t work, int threads) {
   int64_t blocks = (work + threads - 1) / threads;
   if (blocks > 152 * 32) blocks = 152 * 32;
@@ -289,6 +312,16 @@ cudaError_t launch_kv_absmax(const void* x, int dtype, int64_t n_tokens, int h_k
     if (e != cudaSuccess) return e;
   }
   kv_scale_finalize_kernel<<<(h_kv + 127) / 128, 128, 0, s>>>(scales_out, h_kv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_pages(void* k, void* v, const int32_t* src, const int32_t* dst, int n,
+                              int64_t page_bytes, int num_pages, int* err, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const int threads = 256;
+  copy_pages_kernel<<<grid_for((int64_t)n * (page_bytes / 16), threads), threads, 0, s>>>(
+      static_cast<uint8_t*>(k), static_cast<uint8_t*>(v), src, dst, n, page_bytes, num_pages,
+      err);
   return cudaGetLastError();
 }
 

@@ -460,6 +460,30 @@ int pkv_kv_absmax_scales(const void* x, int32_t dtype, int64_t n_tokens, int32_t
   return cuda_status(e, "kv_absmax launch");
 }
 
+int pkv_copy_pages(void* k_cache, void* v_cache, const pkv_cache_desc* desc,
+                   const int32_t* src_pages, const int32_t* dst_pages, int32_t n, void* stream) {
+  const char* who = "pkv_copy_pages";
+  int st = check_desc(desc, who);
+  if (st != PKV_OK) return st;
+  if (n < 0) return set_error(PKV_EINVAL, "%s: n < 0", who);
+  if (n == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !src_pages || !dst_pages)
+    return set_error(PKV_EINVAL, "%s: null pointer", who);
+  if (!aligned16(k_cache) || !aligned16(v_cache))
+    return set_error(PKV_EALIGN, "%s: pools must be 16-byte aligned", who);
+  const int eb = desc->cache_dtype == PKV_F32 ? 4 : desc->cache_dtype == PKV_BF16 ? 2 : 1;
+  const int64_t page_bytes = (int64_t)desc->num_kv_heads * desc->page_size * desc->head_dim * eb;
+  int* err = nullptr;
+  st = error_word(&err);
+  if (st != PKV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = traced("copy_pages", s, [&] {
+    return launch_copy_pages(k_cache, v_cache, src_pages, dst_pages, n, page_bytes,
+                             desc->num_pages, err, s);
+  });
+  return cuda_status(e, "copy_pages launch");
+}
+
 int pkv_device_error(void* stream, int32_t* code_out) {
   if (!code_out) return set_error(PKV_EINVAL, "pkv_device_error: code_out is NULL");
   int* w = nullptr;

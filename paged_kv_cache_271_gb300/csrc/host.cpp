@@ -156,6 +156,27 @@ int pkv_decref(pkv_allocator* a, const int32_t* ids, int32_t n) {
   return PKV_OK;
 }
 
+int pkv_cow_page(pkv_allocator* a, int32_t* row, int32_t n, int64_t position,
+                 int32_t page_size, int32_t* copy_src, int32_t* copy_dst) {
+  if (!a || (n > 0 && !row) || n < 0 || position < 0 || page_size <= 0 || !copy_src || !copy_dst)
+    return pkv::set_error(PKV_EINVAL, "pkv_cow_page: bad argument");
+  *copy_src = *copy_dst = -1;
+  const int64_t lp = position / page_size;
+  if (lp >= n) return PKV_OK;  // the write starts a page the request does not have yet
+  const int32_t page = row[lp];
+  if (page < 0 || page >= a->num_pages || a->ref[page] <= 0)
+    return pkv::set_error(PKV_EREFCNT, "pkv_cow_page: page %d is not allocated", page);
+  if (a->ref[page] == 1) return PKV_OK;  // private already: write in place
+  int32_t fresh = -1;
+  const int st = pkv_alloc(a, 1, &fresh);
+  if (st != PKV_OK) return st;
+  --a->ref[page];  // still referenced by the other sharers (count was > 1)
+  row[lp] = fresh;
+  *copy_src = page;
+  *copy_dst = fresh;
+  return PKV_OK;
+}
+
 int32_t pkv_num_free(const pkv_allocator* a) { return a ? (int32_t)a->stack.size() : -1; }
 
 int32_t pkv_refcount(const pkv_allocator* a, int32_t id) {

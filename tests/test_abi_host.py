@@ -238,3 +238,23 @@ def test_release_outside_window_bookkeeping():
     assert len(c.pages[0]) == 8
     c.free_request(0)
     assert c.allocator.num_free() == 20
+
+
+def test_copy_on_write_page_logic():
+    a = pkv.PageAllocator(10)
+    row = list(a.alloc(3))  # positions 0..47 on three private pages
+    assert a.cow_page(row, 40) is None  # private: write in place
+    a.incref(row)  # a fork shares all three
+    shared = list(row)
+    pair = a.cow_page(row, 40)  # write into the shared, partly filled third page
+    assert pair == (shared[2], row[2]) and row[2] != shared[2]
+    assert a.refcount(shared[2]) == 1 and a.refcount(row[2]) == 1
+    assert row[:2] == shared[:2] and a.refcount(shared[0]) == 2
+    assert a.cow_page(row, 48) is None  # a new page, nothing to copy
+    assert a.num_free() + sum(1 for p in range(10) if a.refcount(p) > 0) == 10
+    small = pkv.PageAllocator(1)
+    r = list(small.alloc(1))
+    small.incref(r)
+    with pytest.raises(pkv.PkvError):
+        small.cow_page(r, 3)  # no free page for the copy: nothing changes
+    assert small.refcount(r[0]) == 2

@@ -479,3 +479,38 @@ def test_paged_window_reads_only_attended_pages():
     np.testing.assert_array_equal(got, ref)
     cont = oracle.contiguous_decode(q, "f32", K, V, "f32", [0], [70], 0.4, sink=4, window=20)
     np.testing.assert_array_equal(got, cont)
+
+
+# ---- INT8 ("KV cache and PagedAttention", section 7: "INT8 KV: similar") -------------------------
+
+def test_int8_quantiser_closed_forms():
+    x = np.array([0.0, 0.5, 1.5, 2.5, -0.5, -1.5, 126.5, 127.4, 200.0, -1e9, 3.49], np.float32)
+    np.testing.assert_array_equal(oracle.quantize_int8(x, 1.0),
+                                  np.array([0, 0, 2, 2, 0, -2, 126, 127, 127, -127, 3], np.int8))
+    s = oracle.absmax_scale(np.array([-6.35, 2.0], np.float32), 127.0)
+    assert s == np.float32(6.35) / np.float32(127.0)
+    assert oracle.quantize_int8(np.array([-6.35], np.float32), s)[0] == -127
+
+
+def test_int8_quantiser_matches_torch_on_every_bf16_pattern():
+    bits = torch.arange(0, 65536, dtype=torch.int32).to(torch.int16)
+    x = bits.view(torch.bfloat16).float()
+    x = x[torch.isfinite(x)]
+    for s in (1.0, 0.0123, 37.0):
+        y = x / torch.tensor(s, dtype=torch.float32)
+        ref = torch.round(y).clamp(-127, 127).to(torch.int8).numpy()  # round half to even
+        np.testing.assert_array_equal(oracle.quantize_int8(x.numpy(), s), ref)
+
+
+def test_int8_decode_uses_code_times_scale():
+    rng = np.random.default_rng(30)
+    T, h_kv, d = 11, 2, 8
+    kc = rng.integers(-127, 128, (T, h_kv, d)).astype(np.int8)
+    vc = rng.integers(-127, 128, (T, h_kv, d)).astype(np.int8)
+    ks = np.array([0.01, 0.2], np.float32)
+    vs = np.array([0.05, 0.003], np.float32)
+    q = rng.standard_normal((1, 4, d)).astype(np.float32)
+    got = oracle.contiguous_decode(q, "f32", kc, vc, "int8", [0], [T], 0.3, ks, vs)
+    ref = _sdpa(q[0].astype(np.float64), kc * ks[None, :, None].astype(np.float64),
+                vc * vs[None, :, None].astype(np.float64), 0.3)
+    np.testing.assert_allclose(got[0], ref, rtol=0, atol=1e-12)
