@@ -56,7 +56,7 @@ typedef enum {
   PKV_ETIMEOUT = -9  /* reserved: a kernel wait timed out (reported in the error word) */
 } pkv_status;
 
-typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2, PKV_INT8 = 3 } pkv_dtype;
 
 /* Bits of the device error word. */
 enum {
@@ -89,13 +89,16 @@ int pkv_version(void);
  * PKV_DEVERR_BAD_SLOT and skips the token.
  *  k_new, v_new   device, [num_tokens][num_kv_heads][head_dim] of dtype_new, contiguous,
  *                 16-byte aligned.
- *  dtype_new      must equal cache_dtype for F32/BF16 caches; F32 or BF16 for an FP8 cache.
+ *  dtype_new      must equal cache_dtype for F32/BF16 caches; F32 or BF16 for an FP8/INT8
+ *                 cache.
  *  slot_mapping   device int64 [num_tokens].
  *  k_cache,v_cache device pools (layout above), 16-byte aligned.
- *  k_scales, v_scales  device float [num_kv_heads], FP8 cache only (else ignored, may be NULL):
- *                 the stored code is round-to-nearest-even, saturating to +-448, of the
- *                 fp32 quotient x / scale[h] (section 7, "fp8 KV (E4M3)"; the rounding and
- *                 saturation are this library's reading).
+ *  k_scales, v_scales  device float [num_kv_heads], FP8/INT8 cache only (else ignored, may
+ *                 be NULL). FP8: the stored code is round-to-nearest-even, saturating to
+ *                 +-448, of the fp32 quotient x / scale[h] (section 7, "fp8 KV (E4M3)").
+ *                 INT8 (section 7, "INT8 KV: similar"): the nearest integer (ties to even) of
+ *                 the fp32 quotient, clamped to [-127, 127]. Rounding, saturation and the
+ *                 symmetric INT8 range are this library's reading.
  */
 int pkv_kv_append(const void* k_new, const void* v_new, int32_t dtype_new, int32_t num_tokens,
                   const int64_t* slot_mapping, void* k_cache, void* v_cache,
@@ -118,9 +121,9 @@ size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num
  *   s_t   = scale * <q[b][h], K_t>            for t < context_lens[b]
  *   out[b][h] = sum_t softmax(s)_t * V_t
  * where K_t, V_t are row t % P of page block_tables[b][t / P] (times k_scales[j] /
- * v_scales[j] for an FP8 cache). Accumulation is fp32. context_lens[b] == 0 gives out = 0.
+ * v_scales[j] for an FP8/INT8 cache). Accumulation is fp32. context_lens[b] == 0 gives out = 0.
  *  q            device [batch][num_q_heads][head_dim] of dtype_q (F32 or BF16).
- *               F32 q needs an F32 or FP8 cache; BF16 q a BF16 or FP8 cache.
+ *               F32 q needs an F32, FP8 or INT8 cache; BF16 q a BF16, FP8 or INT8 cache.
  *  block_tables device int32 [batch][max_pages_per_seq]; entries past a request's last page
  *               are not read.
  *  context_lens device int32 [batch], each <= max_pages_per_seq * 16 (longer ones are cut
@@ -238,6 +241,10 @@ int pkv_copy_pages(void* k_cache, void* v_cache, const pkv_cache_desc* desc,
  */
 int pkv_kv_absmax_scales(const void* x, int32_t dtype, int64_t n_tokens, int32_t num_kv_heads,
                          int32_t head_dim, float* scales_out, void* stream);
+/* The same for an INT8 cache: scales_out[h] = fp32(max |x[:, h, :]| / 127), or 1. */
+int pkv_kv_absmax_scales_int8(const void* x, int32_t dtype, int64_t n_tokens,
+                              int32_t num_kv_heads, int32_t head_dim, float* scales_out,
+                              void* stream);
 
 /*
  * Synchronises stream, then reads and clears the current device's error word into
@@ -257,8 +264,8 @@ int pkv_decode_set_chunk_pages(int32_t pages);
  * kernel, which measured faster on every workload tried. Process-wide. */
 int pkv_decode_set_merge_in_place(int32_t max_chunks);
 
-/* Which decode kernel pkv_paged_decode_attention uses: 0 = automatic (tensor cores for a bf16
- * or FP8 cache with head_dim 128, CUDA cores otherwise), 1 = always the CUDA-core kernel,
+/* Which decode kernel pkv_paged_decode_attention uses: 0 = automatic (tensor cores for a bf16,
+ * FP8 or INT8 cache with head_dim 128, CUDA cores otherwise), 1 = always the CUDA-core kernel,
  * 2 = always the tensor-core kernel (calls it cannot serve then fail with PKV_EINVAL).
  * Process-wide; affects calls made after it returns. Both kernels compute the same result
  * within the documented tolerances; each is deterministic for a given choice. */

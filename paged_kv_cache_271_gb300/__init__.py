@@ -25,7 +25,7 @@ __all__ = [
     "PageAllocator", "trace_enable", "trace_reset", "trace_read",
 ]
 
-F32, BF16, FP8_E4M3 = 0, 1, 2
+F32, BF16, FP8_E4M3, INT8 = 0, 1, 2, 3
 DEVERR_BAD_PAGE, DEVERR_BAD_SLOT, DEVERR_TIMEOUT = 1, 2, 4
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libpkv.so")
@@ -75,6 +75,7 @@ def lib():
                                                               i32, vp, f32, vp, vp, vp, vp]),
         "pkv_decode_noalloc_scratch_bytes": (sz, []),
         "pkv_kv_absmax_scales": (ctypes.c_int, [vp, i32, i64, i32, i32, vp, vp]),
+        "pkv_kv_absmax_scales_int8": (ctypes.c_int, [vp, i32, i64, i32, i32, vp, vp]),
         "pkv_device_error": (ctypes.c_int, [vp, ctypes.POINTER(i32)]),
         "pkv_decode_set_chunk_pages": (ctypes.c_int, [i32]),
         "pkv_decode_chunk_pages": (i32, [i32, i32, i32]),
@@ -125,6 +126,8 @@ def _dtype_code(t: torch.Tensor) -> int:
         return BF16
     if t.dtype in (torch.uint8, torch.float8_e4m3fn):
         return FP8_E4M3
+    if t.dtype == torch.int8:
+        return INT8
     raise PkvError(-3, "unsupported dtype %s" % t.dtype)
 
 
@@ -142,7 +145,7 @@ def _opt(t, name):
 
 def cache_desc(k_cache: torch.Tensor) -> _Desc:
     """Descriptor of a pool [num_pages, num_kv_heads, page_size, head_dim]; uint8 or
-    float8_e4m3fn pools are FP8 E4M3 caches."""
+    float8_e4m3fn pools are FP8 E4M3 caches, int8 pools INT8 caches."""
     if k_cache.dim() != 4:
         raise PkvError(-2, "pool must be [num_pages, num_kv_heads, page_size, head_dim]")
     n, h, p, d = k_cache.shape
@@ -284,15 +287,17 @@ def copy_pages(k_cache, v_cache, src_pages, dst_pages, stream=None):
                                 _dev(dst_pages, "dst_pages"), src_pages.numel(), _stream(stream)))
 
 
-def kv_absmax_scales(x, scales_out=None, stream=None):
-    """FP8 scales per KV head: fp32(max|x[:, h, :]| / 448) (1 for an all-zero head)."""
+def kv_absmax_scales(x, scales_out=None, stream=None, int8=False):
+    """Scales per KV head: fp32(max|x[:, h, :]| / 448) for an FP8 cache, / 127 for an INT8
+    cache (int8=True); 1 for an all-zero head."""
     if x.dim() != 3:
         raise PkvError(-2, "x must be [tokens, h_kv, d]")
     n, h, d = x.shape
     if scales_out is None:
         scales_out = torch.empty(h, dtype=torch.float32, device=x.device)
-    _check(lib().pkv_kv_absmax_scales(_dev(x, "x"), _dtype_code(x), n, h, d,
-                                      _dev(scales_out, "scales_out"), _stream(stream)))
+    fn = lib().pkv_kv_absmax_scales_int8 if int8 else lib().pkv_kv_absmax_scales
+    _check(fn(_dev(x, "x"), _dtype_code(x), n, h, d, _dev(scales_out, "scales_out"),
+              _stream(stream)))
     return scales_out
 
 

@@ -22,7 +22,7 @@ class PagedKVCache:
                  device="cuda", page_size: int = 16, initial_free_order=None,
                  k_scales: torch.Tensor | None = None, v_scales: torch.Tensor | None = None):
         if dtype == torch.float8_e4m3fn:
-            dtype = torch.uint8
+            dtype = torch.uint8  # FP8 E4M3 codes; torch.int8 pools hold INT8 codes
         self.k = torch.empty(num_pages, num_kv_heads, page_size, head_dim, dtype=dtype,
                              device=device)
         self.v = torch.empty_like(self.k)
@@ -37,6 +37,10 @@ class PagedKVCache:
     @property
     def is_fp8(self) -> bool:
         return self.k.dtype == torch.uint8
+
+    @property
+    def is_int8(self) -> bool:
+        return self.k.dtype == torch.int8
 
     # ---- requests ---------------------------------------------------------------------------
 

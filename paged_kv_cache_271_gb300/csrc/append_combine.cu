@@ -91,8 +91,30 @@ __device__ __forceinline__ void quantize_store(const float (&x)[N], float s, uin
   }
 }
 
-// FP8 append: read a 16-byte vector of fp32/bf16, quantise with the head's scale, store codes.
-template <typename TIN>
+// INT8 codes of N values: fp32(x / s) rounded to nearest even, clamped to [-127, 127].
+template <int N>
+__device__ __forceinline__ void quantize_store_int8(const float (&x)[N], float s, uint8_t* dst) {
+  uint32_t w[N / 4];
+#pragma unroll
+  for (int k = 0; k < N / 4; ++k) {
+    uint32_t acc = 0;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int c = min(127, max(-127, __float2int_rn(__fdiv_rn(x[4 * k + t], s))));
+      acc |= ((uint32_t)(c & 0xff)) << (8 * t);
+    }
+    w[k] = acc;
+  }
+  if constexpr (N == 8) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = w[0];
+  }
+}
+
+// FP8 / INT8 append: read a 16-byte vector of fp32/bf16, quantise with the head's scale, store
+// the codes.
+template <typename TIN, bool INT8_CODES>
 __global__ void kv_append_fp8_kernel(const AppendArgs a) {
   constexpr int VEC = Vec16<TIN>::N;
   const int vpr = a.head_dim / VEC;
@@ -114,9 +136,15 @@ __global__ void kv_append_fp8_kernel(const AppendArgs a) {
     const int64_t dst = ((page * a.h_kv + h) * kPageSize + row) * a.head_dim + (int64_t)v * VEC;
     float x[VEC];
     Vec16<TIN>::load(static_cast<const TIN*>(a.k_new) + src, x);
-    quantize_store<VEC>(x, a.k_scales[h], static_cast<uint8_t*>(a.k_cache) + dst);
+    if constexpr (INT8_CODES)
+      quantize_store_int8<VEC>(x, a.k_scales[h], static_cast<uint8_t*>(a.k_cache) + dst);
+    else
+      quantize_store<VEC>(x, a.k_scales[h], static_cast<uint8_t*>(a.k_cache) + dst);
     Vec16<TIN>::load(static_cast<const TIN*>(a.v_new) + src, x);
-    quantize_store<VEC>(x, a.v_scales[h], static_cast<uint8_t*>(a.v_cache) + dst);
+    if constexpr (INT8_CODES)
+      quantize_store_int8<VEC>(x, a.v_scales[h], static_cast<uint8_t*>(a.v_cache) + dst);
+    else
+      quantize_store<VEC>(x, a.v_scales[h], static_cast<uint8_t*>(a.v_cache) + dst);
   }
 }
 
@@ -151,11 +179,11 @@ __global__ void kv_absmax_kernel(const TIN* x, int64_t n_tokens, int h_kv, int h
   }
 }
 
-__global__ void kv_scale_finalize_kernel(float* scales, int h_kv) {
+__global__ void kv_scale_finalize_kernel(float* scales, int h_kv, float code_max) {
   const int h = blockIdx.x * blockDim.x + threadIdx.x;
   if (h >= h_kv) return;
   const float amax = __uint_as_float(reinterpret_cast<unsigned int*>(scales)[h]);
-  scales[h] = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+  scales[h] = (amax == 0.f) ? 1.f : __fdiv_rn(amax, code_max);
 }
 
 // Merge of the chunk partials of one (b, h): M = max_c m_c, w_c = 2^(m_c - M),
@@ -271,13 +299,20 @@ inline int grid_for(int64_t work, int threads) {
 cudaError_t launch_kv_append(const AppendArgs& a, int in_dtype, int cache_dtype, cudaStream_t s) {
   if (a.num_tokens == 0) return cudaSuccess;
   const int threads = 256;
-  if (cache_dtype == PKV_FP8_E4M3) {
+  if (cache_dtype == PKV_FP8_E4M3 || cache_dtype == PKV_INT8) {
+    const bool i8 = cache_dtype == PKV_INT8;
     if (in_dtype == PKV_BF16) {
       const int64_t work = (int64_t)a.num_tokens * a.h_kv * (a.head_dim / 8);
-      kv_append_fp8_kernel<__nv_bfloat16><<<grid_for(work, threads), threads, 0, s>>>(a);
+      if (i8)
+        kv_append_fp8_kernel<__nv_bfloat16, true><<<grid_for(work, threads), threads, 0, s>>>(a);
+      else
+        kv_append_fp8_kernel<__nv_bfloat16, false><<<grid_for(work, threads), threads, 0, s>>>(a);
     } else {
       const int64_t work = (int64_t)a.num_tokens * a.h_kv * (a.head_dim / 4);
-      kv_append_fp8_kernel<float><<<grid_for(work, threads), threads, 0, s>>>(a);
+      if (i8)
+        kv_append_fp8_kernel<float, true><<<grid_for(work, threads), threads, 0, s>>>(a);
+      else
+        kv_append_fp8_kernel<float, false><<<grid_for(work, threads), threads, 0, s>>>(a);
     }
   } else if (cache_dtype == PKV_BF16) {
     const int64_t work = (int64_t)a.num_tokens * a.h_kv * (a.head_dim / 8);
@@ -290,7 +325,7 @@ cudaError_t launch_kv_append(const AppendArgs& a, int in_dtype, int cache_dtype,
 }
 
 cudaError_t launch_kv_absmax(const void* x, int dtype, int64_t n_tokens, int h_kv, int head_dim,
-                             float* scales_out, cudaStream_t s) {
+                             float code_max, float* scales_out, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(scales_out, 0, sizeof(float) * h_kv, s);
   if (e != cudaSuccess) return e;
   if (n_tokens > 0) {
@@ -311,7 +346,7 @@ cudaError_t launch_kv_absmax(const void* x, int dtype, int64_t n_tokens, int h_k
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  kv_scale_finalize_kernel<<<(h_kv + 127) / 128, 128, 0, s>>>(scales_out, h_kv);
+  kv_scale_finalize_kernel<<<(h_kv + 127) / 128, 128, 0, s>>>(scales_out, h_kv, code_max);
   return cudaGetLastError();
 }
 

@@ -176,7 +176,8 @@ int check_desc(const pkv_cache_desc* d, const char* who) {
     return set_error(PKV_ESHAPE, "%s: head_dim must be 64 or 128", who);
   if (d->num_pages <= 0 || d->num_kv_heads <= 0)
     return set_error(PKV_ESHAPE, "%s: num_pages and num_kv_heads must be positive", who);
-  if (d->cache_dtype != PKV_F32 && d->cache_dtype != PKV_BF16 && d->cache_dtype != PKV_FP8_E4M3)
+  if (d->cache_dtype != PKV_F32 && d->cache_dtype != PKV_BF16 && d->cache_dtype != PKV_FP8_E4M3 &&
+      d->cache_dtype != PKV_INT8)
     return set_error(PKV_EDTYPE, "%s: unknown cache dtype %d", who, d->cache_dtype);
   if ((long long)d->num_pages * d->num_kv_heads * d->page_size >= (1ll << 40))
     return set_error(PKV_ESHAPE, "%s: pool too large", who);
@@ -253,8 +254,9 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
     return set_error(PKV_EDTYPE, "%s: q dtype must be F32 or BF16", who);
   if ((kv == PKV_F32 && dtype_q != PKV_F32) || (kv == PKV_BF16 && dtype_q != PKV_BF16))
     return set_error(PKV_EDTYPE, "%s: q dtype must match an F32/BF16 cache", who);
-  if (kv == PKV_FP8_E4M3 && (!k_scales || !v_scales))
-    return set_error(PKV_EINVAL, "%s: FP8 cache needs k_scales and v_scales", who);
+  const bool coded = kv == PKV_FP8_E4M3 || kv == PKV_INT8;
+  if (coded && (!k_scales || !v_scales))
+    return set_error(PKV_EINVAL, "%s: FP8/INT8 cache needs k_scales and v_scales", who);
   if (!aligned16(k_cache) || !aligned16(v_cache))
     return set_error(PKV_EALIGN, "%s: pools must be 16-byte aligned", who);
   if (!(scale == scale)) return set_error(PKV_EINVAL, "%s: scale is NaN", who);
@@ -301,9 +303,9 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
   }
   if (k_new) {
     if (!v_new) return set_error(PKV_EINVAL, "%s: v_new is NULL", who);
-    if (kv == PKV_FP8_E4M3) {
+    if (coded) {
       if (dtype_new != PKV_F32 && dtype_new != PKV_BF16)
-        return set_error(PKV_EDTYPE, "%s: FP8 cache takes F32 or BF16 new rows", who);
+        return set_error(PKV_EDTYPE, "%s: FP8/INT8 cache takes F32 or BF16 new rows", who);
     } else if (dtype_new != kv) {
       return set_error(PKV_EDTYPE, "%s: new rows must have the cache dtype", who);
     }
@@ -333,6 +335,7 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
     if (use_mma) return launch_decode_mma(a, kv, dtype_q, G, &tk, &tv, s);
     if (kv == PKV_F32) return launch_decode_f32(a, dtype_q, D, G, s);
     if (kv == PKV_BF16) return launch_decode_bf16(a, dtype_q, D, G, s);
+    if (kv == PKV_INT8) return launch_decode_int8(a, dtype_q, D, G, s);
     return launch_decode_fp8(a, dtype_q, D, G, s);
   });
   st = cuda_status(e, "paged_decode launch");
@@ -413,10 +416,11 @@ int pkv_kv_append(const void* k_new, const void* v_new, int32_t dtype_new, int32
   if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache)
     return set_error(PKV_EINVAL, "%s: null pointer", who);
   const int kv = desc->cache_dtype;
-  if (kv == PKV_FP8_E4M3) {
+  if (kv == PKV_FP8_E4M3 || kv == PKV_INT8) {
     if (dtype_new != PKV_F32 && dtype_new != PKV_BF16)
-      return set_error(PKV_EDTYPE, "%s: FP8 cache takes F32 or BF16 input", who);
-    if (!k_scales || !v_scales) return set_error(PKV_EINVAL, "%s: FP8 cache needs scales", who);
+      return set_error(PKV_EDTYPE, "%s: FP8/INT8 cache takes F32 or BF16 input", who);
+    if (!k_scales || !v_scales)
+      return set_error(PKV_EINVAL, "%s: FP8/INT8 cache needs scales", who);
   } else if (dtype_new != kv) {
     return set_error(PKV_EDTYPE, "%s: input dtype must equal the cache dtype", who);
   }
@@ -441,9 +445,9 @@ int pkv_kv_append(const void* k_new, const void* v_new, int32_t dtype_new, int32
   return cuda_status(e, "kv_append launch");
 }
 
-int pkv_kv_absmax_scales(const void* x, int32_t dtype, int64_t n_tokens, int32_t num_kv_heads,
-                         int32_t head_dim, float* scales_out, void* stream) {
-  const char* who = "pkv_kv_absmax_scales";
+static int absmax_scales(const char* who, const void* x, int32_t dtype, int64_t n_tokens,
+                         int32_t num_kv_heads, int32_t head_dim, float code_max,
+                         float* scales_out, void* stream) {
   if (n_tokens < 0 || num_kv_heads <= 0 || (head_dim != 64 && head_dim != 128) || !scales_out ||
       (n_tokens > 0 && !x))
     return set_error(PKV_EINVAL, "%s: bad argument", who);
@@ -455,9 +459,22 @@ int pkv_kv_absmax_scales(const void* x, int32_t dtype, int64_t n_tokens, int32_t
   if (num_kv_heads > 65535) return set_error(PKV_ESHAPE, "%s: too many heads", who);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = traced("kv_absmax", s, [&] {
-    return launch_kv_absmax(x, dtype, n_tokens, num_kv_heads, head_dim, scales_out, s);
+    return launch_kv_absmax(x, dtype, n_tokens, num_kv_heads, head_dim, code_max, scales_out, s);
   });
   return cuda_status(e, "kv_absmax launch");
+}
+
+int pkv_kv_absmax_scales(const void* x, int32_t dtype, int64_t n_tokens, int32_t num_kv_heads,
+                         int32_t head_dim, float* scales_out, void* stream) {
+  return absmax_scales("pkv_kv_absmax_scales", x, dtype, n_tokens, num_kv_heads, head_dim, 448.f,
+                       scales_out, stream);
+}
+
+int pkv_kv_absmax_scales_int8(const void* x, int32_t dtype, int64_t n_tokens,
+                              int32_t num_kv_heads, int32_t head_dim, float* scales_out,
+                              void* stream) {
+  return absmax_scales("pkv_kv_absmax_scales_int8", x, dtype, n_tokens, num_kv_heads, head_dim,
+                       127.f, scales_out, stream);
 }
 
 int pkv_copy_pages(void* k_cache, void* v_cache, const pkv_cache_desc* desc,

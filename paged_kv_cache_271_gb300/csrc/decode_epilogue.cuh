@@ -87,7 +87,8 @@ namespace pkv {
 // Decode step with the append fused in: the CTA that reads the page holding position ctx-1 of
 // request b (KV head j) writes this step's K and V rows there -- into the pools and into its
 // shared-memory copy of the page -- before using the page. Same bytes as kv_append: a copy
-// for bf16/fp32 caches, cvt.rn.satfinite.e4m3(fp32(x / s)) for FP8. off(r, ch) is the byte
+// for bf16/fp32 caches, cvt.rn.satfinite.e4m3(fp32(x / s)) for FP8, the clamped nearest-even
+// integer of fp32(x / s) for INT8. off(r, ch) is the byte
 // offset of 16-byte chunk ch of row r in a shared-memory tile.
 template <typename KV, int D, typename OffFn>
 __device__ __forceinline__ void fused_append_row(const DecodeArgs& a, int b, int j, int pid,
@@ -132,13 +133,23 @@ __device__ __forceinline__ void fused_append_row(const DecodeArgs& a, int b, int
       uint32_t w[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint16_t lo = static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(
-            make_float2(__fdiv_rn(x[4 * q], s), __fdiv_rn(x[4 * q + 1], s)), __NV_SATFINITE,
-            __NV_E4M3));
-        const uint16_t hi = static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(
-            make_float2(__fdiv_rn(x[4 * q + 2], s), __fdiv_rn(x[4 * q + 3], s)), __NV_SATFINITE,
-            __NV_E4M3));
-        w[q] = (uint32_t)lo | ((uint32_t)hi << 16);
+        if constexpr (KV::code == PKV_INT8) {
+          uint32_t acc = 0;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int c = min(127, max(-127, __float2int_rn(__fdiv_rn(x[4 * q + t], s))));
+            acc |= ((uint32_t)(c & 0xff)) << (8 * t);
+          }
+          w[q] = acc;
+        } else {
+          const uint16_t lo = static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(
+              make_float2(__fdiv_rn(x[4 * q], s), __fdiv_rn(x[4 * q + 1], s)), __NV_SATFINITE,
+              __NV_E4M3));
+          const uint16_t hi = static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(
+              make_float2(__fdiv_rn(x[4 * q + 2], s), __fdiv_rn(x[4 * q + 3], s)),
+              __NV_SATFINITE, __NV_E4M3));
+          w[q] = (uint32_t)lo | ((uint32_t)hi << 16);
+        }
       }
       val = make_uint4(w[0], w[1], w[2], w[3]);
     } else {

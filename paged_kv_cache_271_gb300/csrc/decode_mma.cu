@@ -1,5 +1,5 @@
-// Tensor-core decode attention instantiations (bf16 cache with bf16 queries; FP8 cache with
-// bf16 or fp32 queries), head_dim 128, groups 1..16.
+// Tensor-core decode attention instantiations (bf16 cache with bf16 queries; FP8 or INT8 cache
+// with bf16 or fp32 queries), head_dim 128, groups 1..16.
 #include "paged_decode_mma.cuh"
 
 namespace pkv {
@@ -13,6 +13,10 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, int kv_dtype, int q_dtype, in
     return launch_decode_mma_g<FP8, __nv_bfloat16>(a, group, k, v, s);
   if (kv_dtype == PKV_FP8_E4M3 && q_dtype == PKV_F32)
     return launch_decode_mma_g<FP8, float>(a, group, k, v, s);
+  if (kv_dtype == PKV_INT8 && q_dtype == PKV_BF16)
+    return launch_decode_mma_g<INT8, __nv_bfloat16>(a, group, k, v, s);
+  if (kv_dtype == PKV_INT8 && q_dtype == PKV_F32)
+    return launch_decode_mma_g<INT8, float>(a, group, k, v, s);
   return cudaErrorInvalidValue;
 }
 }  // namespace pkv

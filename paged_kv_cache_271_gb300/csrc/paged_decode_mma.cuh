@@ -1,4 +1,5 @@
-// Single-token paged decode attention on tensor cores (bf16 or FP8 E4M3 cache, head_dim 128).
+// Single-token paged decode attention on tensor cores (bf16, FP8 E4M3 or INT8 cache,
+// head_dim 128).
 //
 // Same computation, work split and results contract as paged_decode.cuh (the read phase of the
 // KV-cache pages, "KV cache and PagedAttention" sections 1 and 4, GQA per the "KV Cache"
@@ -19,7 +20,7 @@
 //  * Values: O^T = V^T P^T with mma.m16n8k16 -- head_dim is M (8 m-tiles), heads are N, the
 //    page's tokens are K. V^T fragments come from ldmatrix.trans on the swizzled tile; P is
 //    rounded to the MMA input type and transposed through a 256-byte per-warp buffer.
-//  * FP8: codes are widened exactly to f16 in registers (K fragments from 16-byte loads; V^T
+//  * FP8 / INT8: codes are widened exactly to f16 in registers (K fragments from 16-byte loads; V^T
 //    fragments by pairing the codes of consecutive tokens with byte permutes), the query is
 //    used in f16, and the MMAs run in f16 with fp32 accumulation; the K scale multiplies the
 //    scores and the V scale the output.
@@ -148,6 +149,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   __half2_raw h =
       __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
   return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// Two one-byte codes (the low 16 bits) of a narrow cache -> two f16 values, exactly.
+template <typename KV>
+__device__ __forceinline__ uint32_t widen2(uint32_t two_codes) {
+  if constexpr (KV::code == PKV_INT8)
+    return int8x2_to_f16x2(two_codes & 0xffffu);
+  else
+    return e4m3x2_to_f16x2(two_codes);
 }
 
 template <typename KV, typename TQ, int D, int G>
@@ -335,10 +345,10 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
           const uint32_t w8[4] = {r8.x, r8.y, r8.z, r8.w};
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t a0 = e4m3x2_to_f16x2(w0[ks]);
-            const uint32_t a2 = e4m3x2_to_f16x2(w0[ks] >> 16);
-            const uint32_t a1 = e4m3x2_to_f16x2(w8[ks]);
-            const uint32_t a3 = e4m3x2_to_f16x2(w8[ks] >> 16);
+            const uint32_t a0 = widen2<KV>(w0[ks]);
+            const uint32_t a2 = widen2<KV>(w0[ks] >> 16);
+            const uint32_t a1 = widen2<KV>(w8[ks]);
+            const uint32_t a3 = widen2<KV>(w8[ks] >> 16);
             const int kp = 2 * h + (ks >> 1), half = ks & 1;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -453,8 +463,8 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
           const uint32_t w3 = wi == 0 ? vr[3].x : wi == 1 ? vr[3].y : wi == 2 ? vr[3].z : vr[3].w;
           const uint32_t lo = __byte_perm(w0, w1, sel);  // tokens 2tig, 2tig+1
           const uint32_t hi = __byte_perm(w2, w3, sel);  // tokens 2tig+8, 2tig+9
-          const uint32_t a0 = e4m3x2_to_f16x2(lo), a1 = e4m3x2_to_f16x2(lo >> 16);
-          const uint32_t a2 = e4m3x2_to_f16x2(hi), a3 = e4m3x2_to_f16x2(hi >> 16);
+          const uint32_t a0 = widen2<KV>(lo), a1 = widen2<KV>(lo >> 16);
+          const uint32_t a2 = widen2<KV>(hi), a3 = widen2<KV>(hi >> 16);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
             mma16816<true>(acc[mi][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);

@@ -20,14 +20,22 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 struct F32 {
   using storage = float;
   static constexpr int bytes = 4;
+  static constexpr int code = PKV_F32;
 };
 struct BF16 {
   using storage = __nv_bfloat16;
   static constexpr int bytes = 2;
+  static constexpr int code = PKV_BF16;
 };
 struct FP8 {
   using storage = uint8_t;
   static constexpr int bytes = 1;
+  static constexpr int code = PKV_FP8_E4M3;
+};
+struct INT8 {
+  using storage = int8_t;
+  static constexpr int bytes = 1;
+  static constexpr int code = PKV_INT8;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -156,6 +164,15 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t codes) {
   return __half22float2(__half2(h));
 }
 
+// Two INT8 codes (low byte first) -> two f16 (exact): biasing the byte by 128 and placing it
+// under the f16 exponent of 1024 gives 1024 + (c + 128); subtracting 1152 leaves c.
+__device__ __forceinline__ uint32_t int8x2_to_f16x2(uint32_t two_codes) {
+  const uint32_t u = __byte_perm(two_codes ^ 0x8080u, 0x6464u, 0x5140u);
+  __half2 h = *reinterpret_cast<const __half2*>(&u);
+  h = __hsub2(h, __half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u)));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // Loads DL consecutive elements of a shared-memory row and widens them to float.
 template <typename T, int DL>
 struct RowLoad;
@@ -214,6 +231,23 @@ struct RowLoad<FP8, 4> {
     o[1] = a.y;
     o[2] = b.x;
     o[3] = b.y;
+  }
+};
+
+template <>
+struct RowLoad<INT8, 2> {
+  __device__ __forceinline__ static void run(const uint8_t* p, float (&o)[2]) {
+    const int8_t* c = reinterpret_cast<const int8_t*>(p);
+    o[0] = (float)c[0];
+    o[1] = (float)c[1];
+  }
+};
+template <>
+struct RowLoad<INT8, 4> {
+  __device__ __forceinline__ static void run(const uint8_t* p, float (&o)[4]) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = (float)(int8_t)(w >> (8 * k));
   }
 };
 

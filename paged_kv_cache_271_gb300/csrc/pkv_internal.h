@@ -68,6 +68,8 @@ cudaError_t launch_kv_append(const AppendArgs& a, int in_dtype, int cache_dtype,
 cudaError_t launch_copy_pages(void* k, void* v, const int32_t* src, const int32_t* dst, int n,
                               int64_t page_bytes, int num_pages, int* err, cudaStream_t s);
 cudaError_t launch_kv_absmax(const void* x, int dtype, int64_t n_tokens, int h_kv, int head_dim,
-                             float* scales_out, cudaStream_t s);
+                             float code_max, float* scales_out, cudaStream_t s);
+cudaError_t launch_decode_int8(const DecodeArgs& a, int q_dtype, int head_dim, int group,
+                               cudaStream_t s);
 
 }  // namespace pkv

@@ -9,7 +9,9 @@ import oracle
 import paged_kv_cache_271_gb300 as pkv
 from paged_kv_cache_271_gb300.cache import PagedKVCache
 
-POOL_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8}
+POOL_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8,
+              "int8": torch.int8}
+CODED = ("fp8_e4m3", "int8")
 
 
 def fill_junk(t: torch.Tensor, seed: int):
@@ -30,10 +32,11 @@ class Scenario:
         order = w.page_order if page_order is None else page_order
         self.scales = None
         ks = vs = None
-        if w.kv_dtype == "fp8_e4m3":
+        if w.kv_dtype in CODED:
             k_all, v_all = self.all_token_rows()
-            ks = pkv.kv_absmax_scales(k_all.to(self.device))
-            vs = pkv.kv_absmax_scales(v_all.to(self.device))
+            i8 = w.kv_dtype == "int8"
+            ks = pkv.kv_absmax_scales(k_all.to(self.device), int8=i8)
+            vs = pkv.kv_absmax_scales(v_all.to(self.device), int8=i8)
             self.scales = (ks, vs)
         self.cache = PagedKVCache(w.num_pages, w.num_kv_heads, w.head_dim,
                                   POOL_DTYPE[w.kv_dtype], self.device,
@@ -122,20 +125,22 @@ class Scenario:
 
 
 def oracle_fp8_codes(w):
-    """The oracle's own per-head scales and E4M3 codes for an FP8 workload's tokens."""
+    """The oracle's own per-head scales and codes (E4M3 or INT8) for a quantised workload."""
     kf = w.k_tokens.float().numpy()
     vf = w.v_tokens.float().numpy()
-    ks = oracle.absmax_scales_per_head(kf)
-    vs = oracle.absmax_scales_per_head(vf)
-    kc = np.stack([oracle.quantize_e4m3(kf[:, j], ks[j]) for j in range(kf.shape[1])], 1)
-    vc = np.stack([oracle.quantize_e4m3(vf[:, j], vs[j]) for j in range(vf.shape[1])], 1)
+    qmax, quant = (127.0, oracle.quantize_int8) if w.kv_dtype == "int8" else \
+        (448.0, oracle.quantize_e4m3)
+    ks = oracle.absmax_scales_per_head(kf, qmax)
+    vs = oracle.absmax_scales_per_head(vf, qmax)
+    kc = np.stack([quant(kf[:, j], ks[j]) for j in range(kf.shape[1])], 1)
+    vc = np.stack([quant(vf[:, j], vs[j]) for j in range(vf.shape[1])], 1)
     return ks, vs, kc, vc
 
 
 def oracle_expected(w, pairs=None, n_threads=0, sink=0, window=0):
     """The oracle's decode output for w, from its own contiguous tokens (and, for FP8, its own
     scales and quantiser). float64 [B, h_q, d] or [n_pairs, d]."""
-    if w.kv_dtype != "fp8_e4m3":
+    if w.kv_dtype not in CODED:
         return oracle.decode_inputs(w, pairs=pairs, n_threads=n_threads, sink=sink, window=window)
     ks, vs, kc, vc = oracle_fp8_codes(w)
     return oracle.decode_inputs(w, pairs=pairs, n_threads=n_threads, k_scales=ks, v_scales=vs,

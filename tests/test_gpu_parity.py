@@ -107,6 +107,8 @@ SHAPES = [
     ("fp8_e4m3", "bf16", 32, 8, 128, [40, 700, 1]),
     ("fp8_e4m3", "f32", 8, 4, 64, [77, 260]),
     ("fp8_e4m3", "bf16", 16, 1, 128, [500, 19]),
+    ("int8", "bf16", 32, 8, 128, [40, 700, 1, 1100]),
+    ("int8", "f32", 16, 2, 64, [77, 260]),
 ]
 
 
@@ -143,6 +145,7 @@ def test_llama3_8b_batch64_both_kernels(kernel):
 
 STEP_SHAPES = [
     ("bf16", "bf16", 32, 8, 128, [1, 16, 17, 500, 1100, 2049]),
+    ("int8", "bf16", 32, 8, 128, [3, 600, 16]),
     ("f32", "f32", 4, 2, 64, [18, 34, 1]),
     ("fp8_e4m3", "bf16", 32, 8, 128, [40, 700, 1, 1000]),
     ("fp8_e4m3", "f32", 16, 8, 128, [33, 129]),
@@ -201,11 +204,12 @@ def test_zero_length_context_gives_zero_output():
 # ---- append, scales -------------------------------------------------------------------------------
 
 @pytest.mark.parametrize("kv,src", [("f32", "f32"), ("bf16", "bf16"), ("fp8_e4m3", "bf16"),
-                                     ("fp8_e4m3", "f32")])
+                                     ("fp8_e4m3", "f32"), ("int8", "bf16"), ("int8", "f32")])
 def test_append_bit_exact(kv, src):
     torch.manual_seed(0)
     num_pages, h_kv, d, N = 24, 4, 128, 150
-    pool_dt = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8}[kv]
+    pool_dt = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8,
+               "int8": torch.int8}[kv]
     src_dt = {"f32": torch.float32, "bf16": torch.bfloat16}[src]
     kc = torch.empty(num_pages, h_kv, 16, d, dtype=pool_dt, device="cuda")
     vc = torch.empty_like(kc)
@@ -219,13 +223,13 @@ def test_append_bit_exact(kv, src):
     raw = (lambda t: t.view(torch.uint8).cpu().numpy().copy())
     exp_k, exp_v = raw(kc), raw(vc)
     ks = vs = None
-    if kv == "fp8_e4m3":
+    if kv in ("fp8_e4m3", "int8"):
+        quant = oracle.quantize_int8 if kv == "int8" else oracle.quantize_e4m3
         ks = torch.tensor([0.01, 0.02, 0.003, 1.0], device="cuda")
         vs = torch.tensor([1e-4, 2e-5, 3e-5, 0.5], device="cuda")
-        kq = np.stack([oracle.quantize_e4m3(kn.float().numpy()[:, j], ks[j].item())
-                       for j in range(h_kv)], 1)
-        vq = np.stack([oracle.quantize_e4m3(vn.float().numpy()[:, j], vs[j].item())
-                       for j in range(h_kv)], 1)
+        kq = np.stack([quant(kn.float().numpy()[:, j], ks[j].item()) for j in range(h_kv)], 1)
+        vq = np.stack([quant(vn.float().numpy()[:, j], vs[j].item()) for j in range(h_kv)], 1)
+        kq, vq = kq.view(np.uint8), vq.view(np.uint8)
     else:
         kq, vq = kn.view(torch.uint8).numpy(), vn.view(torch.uint8).numpy()
     # pools viewed as raw bytes: [num_pages, h_kv, 16, d * element bytes]
@@ -255,14 +259,32 @@ def test_fp8_quantiser_matches_oracle_on_every_bf16_pattern():
 
 
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
-def test_absmax_scales_bit_exact(dt):
+@pytest.mark.parametrize("int8", [False, True])
+def test_absmax_scales_bit_exact(dt, int8):
     g = torch.Generator().manual_seed(3)
     x = torch.randn(3000, 8, 128, generator=g) * torch.linspace(0.1, 50, 8)[None, :, None]
     x[:, 5] = 0  # an all-zero head gets scale 1
     x = x.to(torch.bfloat16 if dt == "bf16" else torch.float32)
-    got = pkv.kv_absmax_scales(x.cuda()).cpu().numpy()
-    ref = oracle.absmax_scales_per_head(x.float().numpy())
+    got = pkv.kv_absmax_scales(x.cuda(), int8=int8).cpu().numpy()
+    ref = oracle.absmax_scales_per_head(x.float().numpy(), 127.0 if int8 else 448.0)
     np.testing.assert_array_equal(got, ref)
+
+
+def test_int8_quantiser_matches_oracle_on_every_bf16_pattern():
+    bits = torch.arange(0, 65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+    x = bits[torch.isfinite(bits)]
+    n = (x.numel() // 128) * 128
+    x = x[:n].reshape(-1, 1, 128).contiguous()
+    kc = torch.zeros(x.shape[0] // 16 + 1, 1, 16, 128, dtype=torch.int8, device="cuda")
+    vc = torch.zeros_like(kc)
+    slots = torch.arange(x.shape[0], dtype=torch.int64, device="cuda")
+    for s in (1.0, 0.0123, 37.0):
+        sc = torch.tensor([s], device="cuda")
+        pkv.kv_append(x.cuda(), x.cuda(), slots, kc, vc, sc, sc)
+        got = kc.reshape(-1, 128)[:x.shape[0]].cpu().numpy()
+        ref = oracle.quantize_int8(x.float().numpy().reshape(-1, 128), s)
+        np.testing.assert_array_equal(got, ref)
+    assert pkv.device_error() == 0
 
 
 # ---- device error word: bad inputs are skipped, never faulted on ---------------------------------

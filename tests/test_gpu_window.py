@@ -35,6 +35,7 @@ CASES = [
     ("bf16", "bf16", 32, 8, 128, [1, 17, 300, 1200, 2049]),
     ("f32", "f32", 4, 2, 64, [18, 34, 100]),
     ("fp8_e4m3", "bf16", 32, 8, 128, [40, 700, 1, 1000]),
+    ("int8", "bf16", 32, 8, 128, [40, 700, 1, 1000]),
 ]
 WINDOWS = [(0, 1), (0, 16), (4, 64), (16, 100), (3, 500), (0, 4096)]
 
