@@ -320,6 +320,34 @@ int32_t pkv_num_free(const pkv_allocator* a);
 /* Reference count of a page, or -1 for an id out of range. */
 int32_t pkv_refcount(const pkv_allocator* a, int32_t id);
 
+/* ---- prefix cache (host) ----------------------------------------------------------------- */
+
+/*
+ * Reuse of the KV pages of a prompt prefix ("KV cache and PagedAttention", section 6: hash the
+ * prefix tokens, store its pages keyed by the hash, reuse them on a match; "KV Cache" glossary:
+ * longest common prefix; pitfall 5: include the tenant in the key). Whole pages only: entry i
+ * of a prompt is keyed by a chained hash of (tenant, tokens of pages 0..i) and stores its
+ * tokens, so a match is exact (collisions never share pages). The cache holds one reference on
+ * each listed page (through the allocator it was created with). Not thread-safe.
+ */
+typedef struct pkv_prefix_cache pkv_prefix_cache;
+int pkv_prefix_cache_create(pkv_allocator* a, int32_t page_size, pkv_prefix_cache** out);
+/* Drops the cache's page references. */
+void pkv_prefix_cache_destroy(pkv_prefix_cache* c);
+/* Longest cached prefix of tokens[0..n) in whole pages, at most max_pages: its page ids go to
+ * pages_out (host) and *n_pages_out; the caller receives one reference on each. */
+int pkv_prefix_lookup(pkv_prefix_cache* c, int64_t tenant, const int32_t* tokens, int64_t n,
+                      int32_t* pages_out, int32_t max_pages, int32_t* n_pages_out);
+/* Registers the full pages of a prompt: pages[i] holds tokens [i*P, (i+1)*P). Pages already
+ * cached for the same prefix are kept (the caller's copies are not taken). */
+int pkv_prefix_insert(pkv_prefix_cache* c, int64_t tenant, const int32_t* tokens, int64_t n,
+                      const int32_t* pages, int32_t n_pages);
+/* Releases up to max_pages least recently used entries that end a cached chain and whose page
+ * only the cache references; *n_evicted receives the count. */
+int pkv_prefix_evict(pkv_prefix_cache* c, int32_t max_pages, int32_t* n_evicted);
+/* Number of cached pages (-1 for NULL). */
+int32_t pkv_prefix_size(const pkv_prefix_cache* c);
+
 /* ---- tracing --------------------------------------------------------------------------------- */
 
 /* When on, every kernel the library launches is bracketed by a pair of CUDA events on its

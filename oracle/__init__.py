@@ -193,6 +193,73 @@ class AllocatorModel:
         return len(self.free)
 
 
+class PrefixCacheModel:
+    """Prompt-prefix page cache model ("KV cache and PagedAttention", section 6; tenant in the
+    key per pitfall 5): entry i of a prompt is the exact (tenant, tokens of pages 0..i); a
+    lookup returns the pages of the longest cached prefix in whole pages and references them;
+    the cache holds one reference per entry; eviction removes, in passes over least-recently-
+    used order, entries with no cached continuation whose page only the cache references."""
+
+    def __init__(self, allocator: AllocatorModel, page_size: int = 16):
+        self.a = allocator
+        self.P = page_size
+        self.entries = {}  # key -> page
+        self.lru = []  # keys, least recently used first
+
+    def _touch(self, key):
+        self.lru.remove(key)
+        self.lru.append(key)
+
+    def _key(self, tenant, tokens, i):
+        return (tenant, tuple(int(t) for t in tokens[:(i + 1) * self.P]))
+
+    def lookup(self, tenant, tokens, max_pages=1 << 20):
+        hits = []
+        for i in range(min(len(tokens) // self.P, max_pages)):
+            key = self._key(tenant, tokens, i)
+            if key not in self.entries:
+                break
+            hits.append(key)
+        pages = [self.entries[k] for k in hits]
+        if pages:
+            self.a.incref(pages)
+        for k in hits:
+            self._touch(k)
+        return pages
+
+    def insert(self, tenant, tokens, pages):
+        for i in range(min(len(tokens) // self.P, len(pages))):
+            key = self._key(tenant, tokens, i)
+            if key in self.entries:
+                self._touch(key)
+                continue
+            self.a.incref([pages[i]])
+            self.entries[key] = pages[i]
+            self.lru.append(key)
+
+    def _children(self, key):
+        return sum(1 for k in self.entries
+                   if k[0] == key[0] and len(k[1]) == len(key[1]) + self.P and k[1][:len(key[1])] == key[1])
+
+    def evict(self, max_pages):
+        done, progress = 0, True
+        while done < max_pages and progress:
+            progress = False
+            for key in list(self.lru):
+                if done >= max_pages:
+                    break
+                if key not in self.entries:
+                    continue
+                page = self.entries[key]
+                if self._children(key) == 0 and self.a.ref[page] == 1:
+                    self.a.decref([page])
+                    del self.entries[key]
+                    self.lru.remove(key)
+                    done += 1
+                    progress = True
+        return done
+
+
 # ---- FP8 E4M3 -------------------------------------------------------------------------------
 
 def e4m3_value(code: int) -> float:

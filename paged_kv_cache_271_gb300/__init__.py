@@ -93,6 +93,12 @@ def lib():
                                         ctypes.POINTER(i32)]),
         "pkv_copy_pages": (ctypes.c_int, [vp, vp, D, vp, vp, i32, vp]),
         "pkv_refcount": (i32, [vp, i32]),
+        "pkv_prefix_cache_create": (ctypes.c_int, [vp, i32, ctypes.POINTER(vp)]),
+        "pkv_prefix_cache_destroy": (None, [vp]),
+        "pkv_prefix_lookup": (ctypes.c_int, [vp, i64, vp, i64, vp, i32, ctypes.POINTER(i32)]),
+        "pkv_prefix_insert": (ctypes.c_int, [vp, i64, vp, i64, vp, i32]),
+        "pkv_prefix_evict": (ctypes.c_int, [vp, i32, ctypes.POINTER(i32)]),
+        "pkv_prefix_size": (i32, [vp]),
         "pkv_trace_enable": (ctypes.c_int, [ctypes.c_int]),
         "pkv_trace_reset": (ctypes.c_int, []),
         "pkv_trace_read": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(i32),
@@ -395,6 +401,47 @@ class PageAllocator:
                                   ctypes.byref(dst)))
         row[:] = [int(x) for x in a]
         return None if src.value < 0 else (int(src.value), int(dst.value))
+
+
+class PrefixCache:
+    """Prompt-prefix page cache over a PageAllocator (pkv_prefix_*): whole pages, keyed by
+    tenant and tokens, exact matches only."""
+
+    def __init__(self, allocator: PageAllocator, page_size: int = 16):
+        self._alloc = allocator  # keeps the allocator alive while the cache exists
+        self._h = ctypes.c_void_p()
+        _check(lib().pkv_prefix_cache_create(allocator._h, int(page_size), ctypes.byref(self._h)))
+        self.page_size = page_size
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.pkv_prefix_cache_destroy(h)
+            self._h = None
+
+    def lookup(self, tenant: int, tokens, max_pages: int = 1 << 20) -> list:
+        """Pages of the longest cached prefix (the caller gets a reference on each)."""
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        cap = min(max_pages, len(t) // self.page_size)
+        out = np.empty(max(cap, 1), dtype=np.int32)
+        n = ctypes.c_int32(0)
+        _check(lib().pkv_prefix_lookup(self._h, int(tenant), t.ctypes.data if t.size else None,
+                                       t.size, out.ctypes.data, cap, ctypes.byref(n)))
+        return [int(x) for x in out[:n.value]]
+
+    def insert(self, tenant: int, tokens, pages):
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        p = np.ascontiguousarray(np.asarray(pages, dtype=np.int32))
+        _check(lib().pkv_prefix_insert(self._h, int(tenant), t.ctypes.data if t.size else None,
+                                       t.size, p.ctypes.data if p.size else None, p.size))
+
+    def evict(self, max_pages: int) -> int:
+        n = ctypes.c_int32(0)
+        _check(lib().pkv_prefix_evict(self._h, int(max_pages), ctypes.byref(n)))
+        return int(n.value)
+
+    def size(self) -> int:
+        return int(lib().pkv_prefix_size(self._h))
 
 
 def trace_enable(on: bool = True):

@@ -258,3 +258,61 @@ def test_copy_on_write_page_logic():
     with pytest.raises(pkv.PkvError):
         small.cow_page(r, 3)  # no free page for the copy: nothing changes
     assert small.refcount(r[0]) == 2
+
+
+def test_prefix_cache_against_model():
+    rng = np.random.default_rng(7)
+    P = 16
+    for trial in range(3):
+        n = 64
+        a, am = pkv.PageAllocator(n), oracle.AllocatorModel(n)
+        c, cm = pkv.PrefixCache(a, P), oracle.PrefixCacheModel(am, P)
+        vocab = [rng.integers(0, 50, 80).tolist() for _ in range(4)]  # a few shared prompts
+        held = []  # (pages) referenced by "requests"
+        for _ in range(150):
+            op = rng.integers(0, 4)
+            tenant = int(rng.integers(0, 2))
+            base = vocab[int(rng.integers(0, len(vocab)))]
+            cut = int(rng.integers(0, len(base) + 1))
+            tokens = base[:cut] + rng.integers(0, 50, int(rng.integers(0, 20))).tolist()
+            if op <= 1:  # a request arrives: reuse the cached prefix, allocate the rest, cache it
+                got, ref = c.lookup(tenant, tokens), cm.lookup(tenant, tokens)
+                assert got == ref
+                need = -(-len(tokens) // P) - len(got)
+                if need > am.num_free():
+                    for p in got:
+                        a.decref([p]), am.decref([p])
+                    continue
+                fresh, fresh_m = list(a.alloc(need)), am.alloc(need)
+                assert fresh == fresh_m
+                pages = got + fresh
+                c.insert(tenant, tokens, pages)
+                cm.insert(tenant, tokens, pages)
+                held.append(pages)
+            elif op == 2 and held:  # a request finishes
+                pages = held.pop(int(rng.integers(0, len(held))))
+                a.decref(pages), am.decref(pages)
+            else:
+                k = int(rng.integers(0, 8))
+                assert c.evict(k) == cm.evict(k)
+            assert c.size() == len(cm.entries)
+            assert a.num_free() == am.num_free()
+            for p in range(n):
+                assert a.refcount(p) == am.ref[p]
+        for pages in held:
+            a.decref(pages)
+        del c
+        assert a.num_free() == n  # destroying the cache releases its references
+
+
+def test_prefix_cache_separates_tenants():
+    a = pkv.PageAllocator(8)
+    c = pkv.PrefixCache(a, 16)
+    toks = list(range(40))
+    pages = list(a.alloc(3))
+    c.insert(tenant=1, tokens=toks, pages=pages)
+    assert c.size() == 2  # two full pages
+    assert c.lookup(tenant=2, tokens=toks) == []  # another tenant: no reuse
+    hit = c.lookup(tenant=1, tokens=toks[:35] + [99])
+    assert hit == pages[:2] and a.refcount(pages[0]) == 3
+    assert c.lookup(tenant=1, tokens=[7] + toks[1:]) == []  # first page differs
