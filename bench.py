@@ -3,9 +3,11 @@
 A step is the whole hot path for one batch: the host computes this step's slots (page
 accounting, slot mapping), then one ``paged_decode_step`` launch writes the new token of each
 request into its page (the append) and attends each request's query over its whole cached
-context, merging split sequences in place. Inputs are seeded synthetic
-tensors (N(0, 1) bf16, context lengths U[512, 4096]) already resident in HBM; the L2 is flushed
-(a 256 MiB write) before every timed step, outside the timed events.
+context; a combine launch merges the sequences split over several CTAs. Inputs are seeded
+synthetic tensors (N(0, 1) bf16, context lengths U[512, 4096]) already resident in HBM. No
+step finds its inputs in the L2: identical copies of the KV pools are used in turn (``--l2
+rotate``, the default), or the L2 is flushed with a 256 MiB write before every timed step
+(``--l2 flush``).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -19,6 +21,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -33,28 +36,32 @@ sys.path.insert(0, os.path.join(ROOT, "tests"))
 
 METRIC = ("paged-decode achieved HBM GB/s (% of GB300 peak) and decode tokens/s at batch 64")
 NOMINAL_HBM_GBS = 8000.0
-FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 256 << 20
 
 
-def peaks():
+def peaks(kind="hbm_gbs"):
+    """A measured peak from MEASURED_PEAKS.json (hbm_gbs, bf16_tflops, ...), else the fallback."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
+        return float(p[kind]), "measured"
     except (OSError, KeyError, ValueError):
-        return FALLBACK_HBM_GBS, "fallback"
+        return FALLBACK_PEAKS[kind], "fallback"
 
 
-WORKLOADS = ("llama3_8b_b64", "llama3_70b_long", "prefix_sharing", "fp8_cb_b256", "fp8_cb_b64")
+WORKLOADS = ("llama3_8b_b64", "llama3_70b_long", "prefix_sharing", "prefix_sharing_cascade",
+             "fp8_cb_b256", "fp8_cb_b64")
 
 
 def workload(name="llama3_8b_b64"):
     import workloads
     return {"llama3_8b_b64": workloads.llama3_8b_batch64,
             "llama3_70b_long": workloads.llama3_70b_long,
-            "prefix_sharing": workloads.prefix_sharing}[name]()
+            "prefix_sharing": workloads.prefix_sharing,
+            "prefix_sharing_cascade": workloads.prefix_sharing}[name]()
 
 
 def config_of(w):
@@ -113,7 +120,21 @@ class StepState:
             self.cache = sc.cache
             self.slots = sc.step_slots
         self.out = torch.empty_like(self.q)
-        need = pkv.decode_workspace_size(self.batch, self.h_q, self.h_kv, self.d, self.bt.shape[1])
+        self.groups = None
+        if name.endswith("_cascade"):
+            # the shared prompt's pages computed once per group (pkv_cascade_decode_step)
+            self.groups = pkv.cascade_groups(self.bt.cpu().numpy(), self.cl.cpu().numpy())
+            self.groups.to(dev)
+            g = self.groups
+            self.config["step"] = ("slot mapping (host) + cascade_decode_step (shared-prefix "
+                                   "kernel, append + own-page attention, combine)")
+            self.config["cascade"] = "%d group(s), %s shared pages, %d members max" % (
+                g.n_groups, "/".join(str(int(x)) for x in g.prefix_pages), g.max_members)
+            need = pkv.cascade_workspace_size(self.batch, self.h_q, self.h_kv, self.d,
+                                              self.bt.shape[1], g)
+        else:
+            need = pkv.decode_workspace_size(self.batch, self.h_q, self.h_kv, self.d,
+                                             self.bt.shape[1])
         self.workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
 
     def decode_bytes(self):
@@ -132,13 +153,58 @@ class StepState:
         self._cl_host = cl
         slots = pkv.slot_mapping(bt, cl.astype(np.int64) - 1, self.cache.num_pages)
         assert np.array_equal(slots, self.slots)
+        if self.groups is not None:  # the cascade's groups come from the same host tables
+            g = pkv.cascade_groups(bt, cl)
+            assert g.n_groups == self.groups.n_groups
 
-    def fused_step(self, stream=None):
+    def shared_rows_tokens(self):
+        """(query rows, shared tokens) pairs of the cascade groups: every member's query heads
+        attend over its group's shared tokens in the prefix kernel."""
+        g = self.groups
+        return [((int(g.group_offsets[i + 1]) - int(g.group_offsets[i])) * self.h_q,
+                 16 * int(g.prefix_pages[i])) for i in range(g.n_groups)]
+
+    def kernel_work(self):
+        """Algorithmic work per launch of the step's main kernels: name -> (bound, amount)
+        with bytes for HBM-bound kernels and FLOPs for tensor-core ones."""
+        if self.groups is None:  # the decode kernel, which also appends the new rows
+            return {"paged_decode": ("hbm", self.decode_bytes() + self.append_bytes())}
+        row_bytes = self.h_kv * self.d * self.kv_bytes * 2  # K and V of one token
+        shared = self.shared_rows_tokens()
+        g = self.groups
+        # the prefix kernel reads each group's shared pages once and every member's queries
+        pre_bytes = (sum(16 * int(p) for p in g.prefix_pages) * row_bytes
+                     + sum(r for r, _ in shared) * self.d * 2)
+        pre_flops = sum(4.0 * r * t * self.d for r, t in shared)  # Q.K^T and P.V
+        own_tokens = self.ctx_sum - sum(t * r // self.h_q for r, t in shared)
+        own = own_tokens * row_bytes + 2 * self.batch * self.h_q * self.d * 2 + self.append_bytes()
+        return {"cascade_prefix": ("tensor", pre_flops, pre_bytes), "paged_decode": ("hbm", own)}
+
+    def used_kv_bytes(self):
+        """Bytes of the pool pages that hold tokens (K and V)."""
+        a = self.cache.allocator
+        used = self.cache.num_pages - a.num_free()
+        return used * 2 * self.h_kv * 16 * self.d * self.kv_bytes
+
+    def make_copies(self, n):
+        """n identical copies of the K/V pools for steps to use in turn."""
+        self.pools = [(self.k, self.v)] + [(self.k.clone(), self.v.clone()) for _ in range(n - 1)]
+
+    def step_call(self, q, k_new, v_new, bt, cl, groups=None, stream=None, pool=0):
         import paged_kv_cache_271_gb300 as pkv
         ks, vs = self.scales if self.scales else (None, None)
-        return pkv.paged_decode_step(self.q, self.k_new, self.v_new, self.k, self.v, self.bt,
-                                     self.cl, self.scale, out=self.out, k_scales=ks, v_scales=vs,
+        k, v = self.pools[pool] if hasattr(self, "pools") else (self.k, self.v)
+        if self.groups is not None:
+            return pkv.cascade_decode_step(q, k_new, v_new, k, v, bt, cl, self.scale,
+                                           groups or self.groups, out=self.out,
+                                           workspace=self.workspace, stream=stream)
+        return pkv.paged_decode_step(q, k_new, v_new, k, v, bt, cl, self.scale,
+                                     out=self.out, k_scales=ks, v_scales=vs,
                                      workspace=self.workspace, stream=stream)
+
+    def fused_step(self, stream=None, pool=0):
+        return self.step_call(self.q, self.k_new, self.v_new, self.bt, self.cl, stream=stream,
+                              pool=pool)
 
 
 # ---- ranks -------------------------------------------------------------------------------------
@@ -327,33 +393,50 @@ def run_ours(args):
 
     sc = StepState(args.workload, dev)
     stream = torch.cuda.current_stream()
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(FLUSH_BYTES if args.l2 == "flush" else 0, dev)
+    n_sets = 1
+    sc.config["l2"] = "flushed with a 256 MiB write before every timed step"
+    if args.l2 == "rotate":
+        # Inputs larger than the L2 instead of a flush (whose dirty lines would be written back
+        # inside the timed step): identical copies of the pools, used in turn, so that a copy
+        # is read again only after at least 3 x L2 bytes of other copies.
+        used = sc.used_kv_bytes()
+        n_sets = max(2, int(math.ceil(3 * L2_BYTES / used)))
+        sc.make_copies(n_sets)
+        sc.config["l2"] = ("not flushed: %d copies of the KV pools (%.0f MB of pages in use "
+                           "each) used in turn, %.0f MB of other copies read between two reads "
+                           "of one copy (L2: 129 MB)" % (n_sets, used / 1e6,
+                                                           (n_sets - 1) * used / 1e6))
     per_step_bytes = sc.decode_bytes() + sc.append_bytes()
     step_host = sc.host_step
 
-    for _ in range(args.warmup):
+    for i in range(args.warmup):
         flush.zero_()
         step_host()
-        sc.fused_step()
+        sc.fused_step(pool=i % n_sets)
     torch.cuda.synchronize()
     assert pkv.device_error() == 0
 
-    # The step's device work (append, decode, combine) is captured once as a CUDA graph and
-    # replayed every step, as a serving loop would; the host slot mapping runs outside it.
-    graph = torch.cuda.CUDAGraph()
+    # The step's device work (append, decode, combine) is captured once as a CUDA graph (one
+    # per pool copy) and replayed every step, as a serving loop would; the host slot mapping
+    # runs outside it.
+    graphs = []
     side = torch.cuda.Stream(device=dev)
     side.wait_stream(stream)
     with torch.cuda.stream(side):
-        for _ in range(3):
-            sc.fused_step()
+        for i in range(3):
+            sc.fused_step(pool=i % n_sets)
     stream.wait_stream(side)
     torch.cuda.synchronize()
-    with torch.cuda.graph(graph):
-        sc.fused_step()
+    for p in range(n_sets):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            sc.fused_step(pool=p)
+        graphs.append(g)
     torch.cuda.synchronize()
-    for _ in range(args.warmup):
+    for i in range(args.warmup):
         flush.zero_()
-        graph.replay()
+        graphs[i % n_sets].replay()
     torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
@@ -370,7 +453,7 @@ def run_ours(args):
         step_host()
         host_s += time.perf_counter() - t0
         starts[i].record(stream)
-        graph.replay()
+        graphs[i % n_sets].replay()
         ends[i].record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -385,11 +468,11 @@ def run_ours(args):
     pkv.trace_enable(True)
     for i in range(args.steps):
         flush.zero_()
-        sc.fused_step()
+        sc.fused_step(pool=i % n_sets)
     torch.cuda.synchronize()
     pkv.trace_enable(False)
     launches = {}
-    for k in ("kv_append", "paged_decode", "decode_combine"):
+    for k in ("kv_append", "cascade_prefix", "paged_decode", "decode_combine"):
         launches[k] = pkv.trace_read(k)
     pkv.trace_reset()
     per_step_launches = sum(n for n, _ in launches.values()) / max(args.steps, 1)
@@ -399,21 +482,41 @@ def run_ours(args):
     value = aggregate(per_step_bytes, max_ms, ws)
     hbm_peak, peak_kind = peaks()
 
-    n_dec, t_dec = launches["paged_decode"]
-    dec_ms = t_dec / max(n_dec, 1)
-    kernel_bytes = per_step_bytes  # the launch also appends the new rows
-    dec_achieved = kernel_bytes / (dec_ms * 1e-3) / 1e9
-    traffic = recorded_traffic() if args.workload == "llama3_8b_b64" else None
-    roofline = {"bound": "hbm",
-                "kernel": "paged_decode kernel (%s cache, d=%d, G=%d, append fused)"
-                          % (sc.config["kv_dtype"], sc.d, sc.h_q // sc.h_kv),
-                "achieved": round(dec_achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                "frac": round(dec_achieved / hbm_peak, 4), "peak_kind": peak_kind,
-                "frac_of_nominal_8TBs": round(dec_achieved / NOMINAL_HBM_GBS, 4),
-                "traffic": traffic, "algorithmic_bytes_per_launch": kernel_bytes,
-                "launch_ms": round(dec_ms, 5)}
+    # the roofline of the kernel that takes the most time in the step
+    work = sc.kernel_work()
+    top = max(work, key=lambda k: launches[k][1])
+    n_top, t_top = launches[top]
+    top_ms = t_top / max(n_top, 1)
+    if work[top][0] == "hbm":
+        kernel_bytes = work[top][1]
+        achieved = kernel_bytes / (top_ms * 1e-3) / 1e9
+        traffic = recorded_traffic() if args.workload == "llama3_8b_b64" else None
+        roofline = {"bound": "hbm",
+                    "kernel": "paged_decode kernel (%s cache, d=%d, G=%d, append fused)"
+                              % (sc.config["kv_dtype"], sc.d, sc.h_q // sc.h_kv),
+                    "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
+                    "frac_of_nominal_8TBs": round(achieved / NOMINAL_HBM_GBS, 4),
+                    "traffic": traffic, "algorithmic_bytes_per_launch": kernel_bytes,
+                    "launch_ms": round(top_ms, 5)}
+    else:
+        flops, byts = work[top][1], work[top][2]
+        tf_peak, tf_kind = peaks("bf16_tflops")
+        achieved = flops / (top_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": "cascade_prefix kernel (bf16 mma.sync, d=%d)" % sc.d,
+                    "achieved": round(achieved, 2), "peak": tf_peak, "unit": "TFLOP/s",
+                    "frac": round(achieved / tf_peak, 4), "peak_kind": tf_kind + " cuBLAS bf16",
+                    "traffic": None, "algorithmic_flops_per_launch": flops,
+                    "algorithmic_bytes_per_launch": byts,
+                    "bytes_GBs": round(byts / (top_ms * 1e-3) / 1e9, 1),
+                    "launch_ms": round(top_ms, 5)}
+    roofline["other_kernels"] = {
+        k: {"bound": v[0], "ms": round(launches[k][1] / max(launches[k][0], 1), 5),
+            ("GB/s" if v[0] == "hbm" else "TFLOP/s"): round(
+                v[1] / (launches[k][1] / max(launches[k][0], 1) * 1e-3) / (1e9 if v[0] == "hbm" else 1e12), 2)}
+        for k, v in work.items() if k != top and launches[k][0]}
 
-    e2e = run_e2e(sc, args, dev, stream, flush)
+    e2e = run_e2e(sc, args, dev, stream, flush, n_sets)
     max_e2e = max_over_ranks(e2e["ms_per_step"], dev)
     e2e_value = aggregate(per_step_bytes, max_e2e, ws)
 
@@ -439,6 +542,7 @@ def run_ours(args):
             "gpu_launches": int(round(per_step_launches * args.steps)),
             "graph": "the step's launches captured once as a CUDA graph, replayed per step",
             "host_slot_mapping_us": round(1e6 * host_s / max(args.steps, 1), 1),
+            "host_step": "slot mapping" + (" + cascade grouping" if sc.groups is not None else ""),
             "launches_per_kernel": {k: n for k, (n, _) in launches.items()},
             "kernel_ms": {k: round(t / max(n, 1), 5) for k, (n, t) in launches.items()},
             "clocks": clk,
@@ -446,7 +550,19 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(sc, args, dev, stream, flush):
+class L2Flush:
+    """zero_() writes a buffer larger than the L2 (nothing when size is 0)."""
+
+    def __init__(self, size, dev):
+        import torch
+        self.buf = torch.empty(size, dtype=torch.uint8, device=dev) if size else None
+
+    def zero_(self):
+        if self.buf is not None:
+            self.buf.zero_()
+
+
+def run_e2e(sc, args, dev, stream, flush, n_sets=1):
     """Same step through the public API from pinned host buffers: per step the host->device
     copies of the step's inputs (queries, new K/V rows, page tables, context lengths) and the
     device->host read of the outputs sit inside the timed region."""
@@ -461,19 +577,26 @@ def run_e2e(sc, args, dev, stream, flush):
     out_host = torch.empty(sc.out.shape, dtype=sc.out.dtype).pin_memory()
     h2d = int(sum(v.numel() * v.element_size() for v in host.values()))
     d2h = int(out_host.numel() * out_host.element_size())
-    ks, vs = sc.scales if sc.scales else (None, None)
 
-    def one():
+    bt_np, cl_np = host["bt"].numpy(), host["cl"].numpy()
+    groups_h2d = [0]
+    g_stage = torch.empty(3 * sc.batch + 2, dtype=torch.int32).pin_memory()
+    g_buf = torch.empty(3 * sc.batch + 2, dtype=torch.int32, device=dev)
+
+    def one(i):
         for k in host:
             dev_t[k].copy_(host[k], non_blocking=True)
-        pkv.paged_decode_step(dev_t["q"], dev_t["k_new"], dev_t["v_new"], sc.k, sc.v,
-                              dev_t["bt"], dev_t["cl"], sc.scale, out=sc.out, k_scales=ks,
-                              v_scales=vs, workspace=sc.workspace)
+        groups = None
+        if sc.groups is not None:  # this step's groups from its host tables, one H2D copy
+            groups = pkv.cascade_groups(bt_np, cl_np).to(dev, buffer=g_buf, staging=g_stage)
+            groups_h2d[0] = groups.nbytes
+        sc.step_call(dev_t["q"], dev_t["k_new"], dev_t["v_new"], dev_t["bt"], dev_t["cl"],
+                     groups=groups, pool=i % n_sets)
         out_host.copy_(sc.out, non_blocking=True)
 
-    for _ in range(max(3, args.warmup)):
+    for i in range(max(3, args.warmup)):
         flush.zero_()
-        one()
+        one(i)
     torch.cuda.synchronize()
     n = max(1, args.steps)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -483,12 +606,12 @@ def run_e2e(sc, args, dev, stream, flush):
     for i in range(n):
         flush.zero_()
         starts[i].record(stream)
-        one()
+        one(i)
         ends[i].record(stream)
         ends[i].synchronize()  # the result is on the host before the next step starts
     barrier()
     ms = float(np.mean([s.elapsed_time(e) for s, e in zip(starts, ends)]))
-    return {"ms_per_step": ms, "h2d": h2d, "d2h": d2h}
+    return {"ms_per_step": ms, "h2d": h2d + groups_h2d[0], "d2h": d2h}
 
 
 # ---- reference arm: the oracle as it stands --------------------------------------------------
@@ -530,6 +653,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate",
+                    help="rotate: copies of the pools used in turn (at least 3 x L2 of other "
+                         "copies between two reads of one); flush: write 256 MiB before every "
+                         "timed step")
     ap.add_argument("--workload", choices=WORKLOADS, default="llama3_8b_b64",
                     help="the default is the headline layer; the others are for measurement")
     args = ap.parse_args(argv)

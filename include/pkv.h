@@ -63,7 +63,10 @@ enum {
   PKV_DEVERR_BAD_PAGE = 1, /* a block-table entry outside [0, num_pages), or a context longer
                               than its block-table row: the page is skipped */
   PKV_DEVERR_BAD_SLOT = 2, /* a slot outside [0, num_pages * page_size): token not written */
-  PKV_DEVERR_TIMEOUT = 4   /* a bounded wait on a shared-memory barrier gave up */
+  PKV_DEVERR_TIMEOUT = 4,  /* a bounded wait on a shared-memory barrier gave up */
+  PKV_DEVERR_BAD_GROUP = 8 /* cascade decode: inconsistent groups (a member whose context does
+                              not extend past the shared prefix, a member index outside the
+                              batch, more members or prefix pages than declared) */
 };
 
 /* Description of one layer's pair of pools. page_size must be 16; head_dim 64 or 128. */
@@ -319,6 +322,91 @@ int pkv_cow_page(pkv_allocator* a, int32_t* row, int32_t n, int64_t position, in
 int32_t pkv_num_free(const pkv_allocator* a);
 /* Reference count of a page, or -1 for an id out of range. */
 int32_t pkv_refcount(const pkv_allocator* a, int32_t id);
+
+/* ---- cascade decode (shared prompt prefixes) ---------------------------------------------- */
+
+/*
+ * Requests whose page tables start with the same physical pages (a shared prompt prefix,
+ * "KV cache and PagedAttention" section 6; "KV Cache" glossary, prefix caching) form groups.
+ * The cascade decode computes the attention of every member's query heads over the group's
+ * shared pages once per group -- the pages are read once for all members, and the members'
+ * queries form a dense tensor-core contraction -- then over each member's own pages, and
+ * merges the two (in the second kernel: a cascade decode launches no combine kernel) with the
+ * split-decode rule (a softmax over a union of disjoint key sets from
+ * the per-set maxima, sums and weighted values). The result is the same attention as
+ * pkv_paged_decode_attention over the same tables (rounding aside).
+ *
+ * Arrays are device memory unless noted; the bounds are host values that the arrays must
+ * respect (the kernels clamp to them and flag PKV_DEVERR_BAD_GROUP otherwise).
+ */
+typedef struct {
+  const int32_t* group_of;       /* [batch]: group of request b, or -1 */
+  const int32_t* prefix_pages;   /* [n_groups]: leading pages shared by every member of g */
+  const int32_t* group_offsets;  /* [n_groups + 1]: members of g are ... */
+  const int32_t* group_members;  /* ... group_members[group_offsets[g] .. group_offsets[g+1]) */
+  int32_t n_groups;              /* 0: a plain decode */
+  int32_t max_members;           /* host: most members of any group, in [1, batch] */
+  int32_t max_prefix_pages;      /* host: most shared pages of any group, in [1, table width] */
+  int32_t max_own_pages;         /* host hint: most pages any request reads past its group's
+                                    shared pages (all its pages outside a group); sizes the
+                                    split of those pages. 0: the table width. A request with
+                                    more pages still gets a correct result, in larger chunks. */
+} pkv_cascade_desc;
+
+/*
+ * Host. Groups of a batch from its HOST page tables [batch][max_pages_per_seq] and context
+ * lengths: requests are bucketed by their first page id (batch order); a bucket of at least
+ * min_members (>= 2) requests shares the longest run of leading page ids common to all its
+ * members, cut to the full pages before each member's position ctx - 1; fewer than
+ * min_prefix_pages (>= 1) shared pages: no group. Outputs (host, caller-sized): group_of
+ * [batch], prefix_pages [batch], group_offsets [batch + 1], group_members [batch], and the
+ * counts and bounds of a pkv_cascade_desc (*n_groups may be 0; *max_own_pages counts the pages
+ * of a context cut to the table width).
+ */
+int pkv_cascade_groups(const int32_t* block_tables, const int32_t* context_lens, int32_t batch,
+                       int32_t max_pages_per_seq, int32_t min_members, int32_t min_prefix_pages,
+                       int32_t* group_of, int32_t* prefix_pages, int32_t* group_offsets,
+                       int32_t* group_members, int32_t* n_groups, int32_t* max_members,
+                       int32_t* max_prefix_pages, int32_t* max_own_pages);
+
+/* Workspace bytes of a cascade decode (its partials: the prefix chunks, then the members' own
+ * chunks, for every request); pkv_decode_workspace_size when groups has no group. Zero-fill it
+ * before first use. */
+size_t pkv_cascade_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_pages_per_seq,
+                                  const pkv_cascade_desc* groups);
+
+/* Pages per CTA of the prefix pass for these groups (0 without groups). */
+int32_t pkv_cascade_prefix_chunk_pages(int32_t num_kv_heads, int32_t num_q_heads,
+                                       const pkv_cascade_desc* groups);
+
+/*
+ * Cascade decode attention: the arguments of pkv_paged_decode_attention (bf16 cache and
+ * queries, head_dim 128; no window) plus the groups. Every member's table must list its
+ * group's shared pages first and its context must cover them. Launches the prefix kernel,
+ * then the decode kernel over the members' own pages (and the other requests' pages), which
+ * merges.
+ * groups == NULL or n_groups == 0: exactly pkv_paged_decode_attention.
+ */
+int pkv_cascade_decode_attention(const void* q, int32_t dtype_q, int32_t batch,
+                                 int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                 const pkv_cache_desc* desc, const int32_t* block_tables,
+                                 int32_t max_pages_per_seq, const int32_t* context_lens,
+                                 float scale, const pkv_cascade_desc* groups, void* out,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Cascade decode step: as pkv_paged_decode_step (the append of this step's K/V rows is fused
+ * into the decode), with the groups; each member's context must extend past its shared pages. */
+int pkv_cascade_decode_step(const void* q, int32_t dtype_q, int32_t batch, int32_t num_q_heads,
+                            const void* k_new, const void* v_new, int32_t dtype_new,
+                            void* k_cache, void* v_cache, const pkv_cache_desc* desc,
+                            const int32_t* block_tables, int32_t max_pages_per_seq,
+                            const int32_t* context_lens, float scale,
+                            const pkv_cascade_desc* groups, void* out, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Tuning: pages per CTA of the prefix pass (0 = automatic). */
+int pkv_cascade_set_prefix_chunk_pages(int32_t pages);
 
 /* ---- prefix cache (host) ----------------------------------------------------------------- */
 

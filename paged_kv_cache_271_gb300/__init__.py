@@ -8,7 +8,8 @@ paged_kv_cache_271_gb300.build``); calls fail loudly otherwise -- there is no fa
 Entry points (same names as the C ABI, without the ``pkv_`` prefix):
 ``kv_append``, ``paged_decode_attention``, ``decode_workspace_size``, ``kv_absmax_scales``,
 ``device_error``, ``pages_needed``, ``slot_mapping``, ``PageAllocator`` (``pkv_alloc``,
-``pkv_incref``, ``pkv_decref``, ...), ``decode_set_chunk_pages``, ``trace_*``.
+``pkv_incref``, ``pkv_decref``, ...), ``PrefixCache`` (``pkv_prefix_*``), ``cascade_groups``,
+``cascade_decode_attention``, ``cascade_decode_step``, ``decode_set_chunk_pages``, ``trace_*``.
 """
 from __future__ import annotations
 
@@ -22,11 +23,12 @@ __all__ = [
     "PkvError", "F32", "BF16", "FP8_E4M3", "lib", "library_path", "cache_desc", "kv_append",
     "decode_workspace_size", "paged_decode_attention", "kv_absmax_scales", "device_error",
     "decode_set_chunk_pages", "decode_chunk_pages", "pages_needed", "slot_mapping",
-    "PageAllocator", "trace_enable", "trace_reset", "trace_read",
+    "PageAllocator", "PrefixCache", "CascadeGroups", "cascade_groups", "cascade_decode_attention",
+    "cascade_decode_step", "cascade_workspace_size", "trace_enable", "trace_reset", "trace_read",
 ]
 
 F32, BF16, FP8_E4M3, INT8 = 0, 1, 2, 3
-DEVERR_BAD_PAGE, DEVERR_BAD_SLOT, DEVERR_TIMEOUT = 1, 2, 4
+DEVERR_BAD_PAGE, DEVERR_BAD_SLOT, DEVERR_TIMEOUT, DEVERR_BAD_GROUP = 1, 2, 4, 8
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libpkv.so")
 _lib = None
@@ -44,6 +46,13 @@ class _Desc(ctypes.Structure):
                 ("cache_dtype", ctypes.c_int32)]
 
 
+class _CascadeDesc(ctypes.Structure):
+    _fields_ = [("group_of", ctypes.c_void_p), ("prefix_pages", ctypes.c_void_p),
+                ("group_offsets", ctypes.c_void_p), ("group_members", ctypes.c_void_p),
+                ("n_groups", ctypes.c_int32), ("max_members", ctypes.c_int32),
+                ("max_prefix_pages", ctypes.c_int32), ("max_own_pages", ctypes.c_int32)]
+
+
 def lib():
     """The loaded C library. Raises if it has not been built."""
     global _lib
@@ -56,6 +65,7 @@ def lib():
     vp, i32, i64, f32, dbl, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                                   ctypes.c_float, ctypes.c_double, ctypes.c_size_t)
     D = ctypes.POINTER(_Desc)
+    C = ctypes.POINTER(_CascadeDesc)
     sig = {
         "pkv_last_error": (ctypes.c_char_p, []),
         "pkv_version": (ctypes.c_int, []),
@@ -99,6 +109,16 @@ def lib():
         "pkv_prefix_insert": (ctypes.c_int, [vp, i64, vp, i64, vp, i32]),
         "pkv_prefix_evict": (ctypes.c_int, [vp, i32, ctypes.POINTER(i32)]),
         "pkv_prefix_size": (i32, [vp]),
+        "pkv_cascade_groups": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp,
+                                              ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                              ctypes.POINTER(i32), ctypes.POINTER(i32)]),
+        "pkv_cascade_workspace_size": (sz, [i32, i32, i32, i32, i32, C]),
+        "pkv_cascade_prefix_chunk_pages": (i32, [i32, i32, C]),
+        "pkv_cascade_decode_attention": (ctypes.c_int, [vp, i32, i32, i32, vp, vp, D, vp, i32,
+                                                        vp, f32, C, vp, vp, sz, vp]),
+        "pkv_cascade_decode_step": (ctypes.c_int, [vp, i32, i32, i32, vp, vp, i32, vp, vp, D, vp,
+                                                   i32, vp, f32, C, vp, vp, sz, vp]),
+        "pkv_cascade_set_prefix_chunk_pages": (ctypes.c_int, [i32]),
         "pkv_trace_enable": (ctypes.c_int, [ctypes.c_int]),
         "pkv_trace_reset": (ctypes.c_int, []),
         "pkv_trace_read": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(i32),
@@ -257,6 +277,147 @@ def paged_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_l
         _check(lib().pkv_paged_decode_step_window(*args, int(sink_tokens), int(window), *tail))
     else:
         _check(lib().pkv_paged_decode_step(*args, *tail))
+    return out
+
+
+class CascadeGroups:
+    """Groups of a batch that share leading pages (pkv_cascade_groups), as host arrays; call
+    ``to(device)`` once to place them for the cascade decode."""
+
+    def __init__(self, group_of, prefix_pages, group_offsets, group_members, max_members,
+                 max_prefix_pages, max_own_pages=0):
+        self.group_of = group_of
+        self.prefix_pages = prefix_pages
+        self.group_offsets = group_offsets
+        self.group_members = group_members
+        self.n_groups = len(prefix_pages)
+        self.max_members = int(max_members)
+        self.max_prefix_pages = int(max_prefix_pages)
+        self.max_own_pages = int(max_own_pages)
+        self._dev = None
+
+    def packed(self) -> np.ndarray:
+        """The four arrays back to back (int32), as ``to`` places them."""
+        return np.concatenate([self.group_of, self.prefix_pages, self.group_offsets,
+                               self.group_members]).astype(np.int32)
+
+    def to(self, device, buffer=None, staging=None):
+        """Place the arrays on the device in one copy: into a new tensor, or into ``buffer``
+        (int32 device tensor) through ``staging`` (pinned int32 host tensor), asynchronously."""
+        p = self.packed()
+        if buffer is None:
+            buffer = torch.from_numpy(p).to(device)
+        else:
+            if buffer.numel() < p.size or staging is None or staging.numel() < p.size:
+                raise PkvError(-1, "cascade group buffers are too small")
+            staging[:p.size].copy_(torch.from_numpy(p))
+            buffer[:p.size].copy_(staging[:p.size], non_blocking=True)
+        self._dev = buffer
+        self.nbytes = 4 * p.size
+        B, ng = len(self.group_of), self.n_groups
+        base = buffer.data_ptr()
+        self._ptrs = [base, base + 4 * B, base + 4 * (B + ng), base + 4 * (B + 2 * ng + 1)]
+        return self
+
+    def desc(self) -> _CascadeDesc:
+        if self.n_groups == 0:
+            return _CascadeDesc(None, None, None, None, 0, 0, 0)
+        if self._dev is None:
+            raise PkvError(-1, "CascadeGroups.to(device) has not been called")
+        g, p, o, m = self._ptrs
+        return _CascadeDesc(g, p, o, m, self.n_groups, self.max_members, self.max_prefix_pages,
+                            self.max_own_pages)
+
+
+def cascade_groups(block_tables, context_lens, min_members=2, min_prefix_pages=1) -> CascadeGroups:
+    """Requests whose tables start with the same pages (host arrays; pkv_cascade_groups)."""
+    bt = np.ascontiguousarray(np.asarray(block_tables, dtype=np.int32))
+    cl = np.ascontiguousarray(np.asarray(context_lens, dtype=np.int32))
+    B, W = bt.shape
+    if cl.shape != (B,):
+        raise PkvError(-2, "context_lens must be [batch]")
+    group_of = np.empty(B, np.int32)
+    prefix = np.empty(max(B, 1), np.int32)
+    offs = np.empty(B + 1, np.int32)
+    members = np.empty(max(B, 1), np.int32)
+    n, mm, mp, mo = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().pkv_cascade_groups(bt.ctypes.data if B else None, cl.ctypes.data if B else None,
+                                    B, W, int(min_members), int(min_prefix_pages),
+                                    group_of.ctypes.data, prefix.ctypes.data, offs.ctypes.data,
+                                    members.ctypes.data, ctypes.byref(n), ctypes.byref(mm),
+                                    ctypes.byref(mp), ctypes.byref(mo)))
+    ng = n.value
+    return CascadeGroups(group_of, prefix[:ng].copy(), offs[:ng + 1].copy(),
+                         members[:offs[ng]].copy(), mm.value, mp.value, mo.value)
+
+
+def cascade_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_pages_per_seq,
+                           groups: CascadeGroups) -> int:
+    d = groups.desc() if groups.n_groups == 0 or groups._dev is not None else _CascadeDesc(
+        None, None, None, None, groups.n_groups, groups.max_members, groups.max_prefix_pages,
+        groups.max_own_pages)
+    return int(lib().pkv_cascade_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                                max_pages_per_seq, ctypes.byref(d)))
+
+
+def cascade_prefix_chunk_pages(num_kv_heads, num_q_heads, groups: CascadeGroups) -> int:
+    d = _CascadeDesc(None, None, None, None, groups.n_groups, groups.max_members,
+                     groups.max_prefix_pages)
+    return int(lib().pkv_cascade_prefix_chunk_pages(num_kv_heads, num_q_heads, ctypes.byref(d)))
+
+
+def cascade_set_prefix_chunk_pages(pages: int):
+    _check(lib().pkv_cascade_set_prefix_chunk_pages(int(pages)))
+
+
+def _cascade_common(q, k_cache, block_tables, context_lens, groups, workspace):
+    if q.dim() != 3 or block_tables.dim() != 2:
+        raise PkvError(-2, "q must be [batch, heads, dim], block_tables [batch, max_pages]")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise PkvError(-3, "block_tables and context_lens must be int32")
+    B, h_q, d = q.shape
+    desc = cache_desc(k_cache)
+    maxp = block_tables.shape[1]
+    need = cascade_workspace_size(B, h_q, desc.num_kv_heads, d, maxp, groups)
+    if need and workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return B, h_q, desc, maxp, workspace, wsb
+
+
+def cascade_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale,
+                             groups: CascadeGroups, out=None, workspace=None, stream=None):
+    """Decode attention with each group's shared pages computed once for all its members
+    (pkv_cascade_decode_attention); same result as paged_decode_attention."""
+    B, h_q, desc, maxp, workspace, wsb = _cascade_common(q, k_cache, block_tables, context_lens,
+                                                         groups, workspace)
+    if out is None:
+        out = torch.empty_like(q)
+    gd = groups.desc()
+    _check(lib().pkv_cascade_decode_attention(
+        _dev(q, "q"), _dtype_code(q), B, h_q, _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        ctypes.byref(desc), _dev(block_tables, "block_tables"), maxp,
+        _dev(context_lens, "context_lens"), float(scale), ctypes.byref(gd), _dev(out, "out"),
+        _opt(workspace, "workspace"), wsb, _stream(stream)))
+    return out
+
+
+def cascade_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale,
+                        groups: CascadeGroups, out=None, workspace=None, stream=None):
+    """paged_decode_step with each group's shared pages computed once (pkv_cascade_decode_step)."""
+    B, h_q, desc, maxp, workspace, wsb = _cascade_common(q, k_cache, block_tables, context_lens,
+                                                         groups, workspace)
+    if k_new.shape != v_new.shape or k_new.dim() != 3 or k_new.shape[0] != B:
+        raise PkvError(-2, "k_new and v_new must both be [batch, h_kv, d]")
+    if out is None:
+        out = torch.empty_like(q)
+    gd = groups.desc()
+    _check(lib().pkv_cascade_decode_step(
+        _dev(q, "q"), _dtype_code(q), B, h_q, _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+        _dtype_code(k_new), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        ctypes.byref(desc), _dev(block_tables, "block_tables"), maxp,
+        _dev(context_lens, "context_lens"), float(scale), ctypes.byref(gd), _dev(out, "out"),
+        _opt(workspace, "workspace"), wsb, _stream(stream)))
     return out
 
 

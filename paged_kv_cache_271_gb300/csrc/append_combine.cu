@@ -9,6 +9,7 @@
 // per-head scale, round-to-nearest-even and saturation are this library's reading).
 #include <math.h>
 
+#include "decode_plan.cuh"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -199,8 +200,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a)
   const int h = blockIdx.x, b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ctx = min(max(0, a.context_lens[b]), a.max_pages * kPageSize);
-  const int pages_seq = seq_pages(ctx, a.sink, a.window).n;
-  const int n_chunks = (pages_seq + a.chunk_pages - 1) / a.chunk_pages;
+  const int n_chunks = seq_plan(a, b, ctx).n_total;  // partials of the request
   if (n_chunks <= 1) return;
   const size_t bh = (size_t)b * a.h_q + h;
   const float* ml = a.ws_ml + bh * a.n_chunk_slots * 2;

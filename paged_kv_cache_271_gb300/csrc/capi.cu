@@ -3,6 +3,7 @@
 // errors are found on the host before anything is launched.
 #include <cuda.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -169,6 +170,47 @@ int chunk_pages_for(int batch, int h_kv, int max_pages) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Workspace: acc [batch][h_q][slots][d] and (max, sum) [batch][h_q][slots][2] floats, then one
+// counter per (request, KV head) for the in-place merge; 256-byte aligned regions.
+size_t workspace_bytes_for(int batch, int h_q, int h_kv, int head_dim, int slots) {
+  const size_t rows = (size_t)batch * h_q * slots;
+  return align256(rows * head_dim * sizeof(float)) + align256(rows * 2 * sizeof(float)) +
+         align256((size_t)batch * h_kv * sizeof(int));
+}
+
+std::atomic<int> g_prefix_chunk_override{0};
+
+// Pages per CTA of the cascade prefix kernel: the shared pages of each (group, KV head, row
+// tile) are cut into as many chunks (of at least 2 pages) as keep the launch within one wave
+// of resident CTAs (kCascadeWaveCtas); a chunk of at most the whole prefix.
+int prefix_chunk_pages_for(int n_groups, int h_kv, int group, int max_members, int max_prefix) {
+  const int ov = g_prefix_chunk_override.load();
+  if (ov > 0) return ov;
+  if (max_prefix < 1) return 1;
+  const long long tiles = ((long long)max_members * group + kCascadeRows - 1) / kCascadeRows;
+  const long long units = (long long)n_groups * h_kv * tiles;
+  long long chunks = kCascadeWaveCtas / (units > 0 ? units : 1);
+  chunks = std::max(1ll, std::min(chunks, (long long)(max_prefix + 1) / 2));
+  return (int)((max_prefix + chunks - 1) / chunks);
+}
+
+// Pages any request of a cascade decode reads itself (the hint, else the table width).
+int cascade_own_pages(int max_pages, const pkv_cascade_desc* g) {
+  return g->max_own_pages > 0 && g->max_own_pages < max_pages ? g->max_own_pages : max_pages;
+}
+
+// Chunk columns of the decode grid and chunk slots of a cascade decode: the prefix chunks
+// first, then the requests' own chunks.
+void cascade_split(int batch, int h_kv, int h_q, int max_pages, const pkv_cascade_desc* g,
+                   int* chunk_pages, int* chunk_grid, int* prefix_chunk_pages, int* slots) {
+  const int own = cascade_own_pages(max_pages, g);
+  *chunk_pages = chunk_pages_for(batch, h_kv, own);
+  *chunk_grid = (own + *chunk_pages - 1) / *chunk_pages;
+  *prefix_chunk_pages =
+      prefix_chunk_pages_for(g->n_groups, h_kv, h_q / h_kv, g->max_members, g->max_prefix_pages);
+  *slots = *chunk_grid + (g->max_prefix_pages + *prefix_chunk_pages - 1) / *prefix_chunk_pages;
+}
+
 int check_desc(const pkv_cache_desc* d, const char* who) {
   if (!d) return set_error(PKV_EINVAL, "%s: desc is NULL", who);
   if (d->page_size != 16) return set_error(PKV_EINVAL, "%s: page_size must be 16", who);
@@ -222,11 +264,32 @@ size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num
       max_pages_per_seq <= 0)
     return 0;
   const int chunk = chunk_pages_for(batch, num_kv_heads, max_pages_per_seq);
-  const size_t slots = (size_t)((max_pages_per_seq + chunk - 1) / chunk);
-  if (slots <= 1) return 0;
-  const size_t rows = (size_t)batch * num_q_heads * slots;
-  return align256(rows * head_dim * sizeof(float)) + align256(rows * 2 * sizeof(float)) +
-         align256((size_t)batch * num_kv_heads * sizeof(int));
+  const int slots = (max_pages_per_seq + chunk - 1) / chunk;
+  return slots <= 1 ? 0 : workspace_bytes_for(batch, num_q_heads, num_kv_heads, head_dim, slots);
+}
+
+int32_t pkv_cascade_prefix_chunk_pages(int32_t num_kv_heads, int32_t num_q_heads,
+                                       const pkv_cascade_desc* groups) {
+  if (!groups || groups->n_groups <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 ||
+      groups->max_prefix_pages <= 0 || groups->max_members <= 0)
+    return 0;
+  return prefix_chunk_pages_for(groups->n_groups, num_kv_heads, num_q_heads / num_kv_heads,
+                                groups->max_members, groups->max_prefix_pages);
+}
+
+size_t pkv_cascade_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_pages_per_seq,
+                                  const pkv_cascade_desc* groups) {
+  if (!groups || groups->n_groups <= 0)
+    return pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                     max_pages_per_seq);
+  if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      max_pages_per_seq <= 0 || groups->max_prefix_pages <= 0 || groups->max_members <= 0)
+    return 0;
+  int chunk, grid, pchunk, slots;
+  cascade_split(batch, num_kv_heads, num_q_heads, max_pages_per_seq, groups, &chunk, &grid,
+                &pchunk, &slots);
+  return workspace_bytes_for(batch, num_q_heads, num_kv_heads, head_dim, slots);
 }
 
 static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t batch,
@@ -235,7 +298,8 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
                        int32_t max_pages_per_seq, const int32_t* context_lens, float scale,
                        const float* k_scales, const float* v_scales, void* out, void* workspace,
                        size_t workspace_bytes, const void* k_new, const void* v_new,
-                       int32_t dtype_new, int32_t sink_tokens, int32_t window, void* stream) {
+                       int32_t dtype_new, int32_t sink_tokens, int32_t window,
+                       const pkv_cascade_desc* groups, void* stream) {
   int st = check_desc(desc, who);
   if (st != PKV_OK) return st;
   if (batch < 0 || num_q_heads <= 0 || max_pages_per_seq <= 0)
@@ -282,12 +346,41 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
   a.max_pages = max_pages_per_seq;
   a.chunk_pages = chunk_pages_for(batch, h_kv, max_pages_per_seq);
   a.n_chunk_slots = (max_pages_per_seq + a.chunk_pages - 1) / a.chunk_pages;
+  a.chunk_grid = a.n_chunk_slots;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.window = window;
   a.sink = window > 0 ? sink_tokens : 0;
+  const bool cascade = groups != nullptr && groups->n_groups > 0;
+  CascadeArgs ca{};
+  if (cascade) {
+    if (!groups->group_of || !groups->prefix_pages || !groups->group_offsets ||
+        !groups->group_members)
+      return set_error(PKV_EINVAL, "%s: cascade groups with a null array", who);
+    if (groups->max_members < 1 || groups->max_members > batch || groups->max_prefix_pages < 1 ||
+        groups->max_prefix_pages > max_pages_per_seq || groups->n_groups > batch)
+      return set_error(PKV_EINVAL, "%s: cascade bounds outside [1, batch] members, [1, table "
+                       "width] prefix pages, <= batch groups", who);
+    if (window != 0)
+      return set_error(PKV_EINVAL, "%s: a cascade decode takes no window", who);
+    if (kv != PKV_BF16 || D != 128 || !aligned16(q) ||
+        (long long)desc->num_pages * h_kv * desc->page_size >= (1ll << 31))
+      return set_error(PKV_EDTYPE, "%s: the cascade decode needs a bf16 cache and queries, "
+                       "head_dim 128, a 16-byte aligned q and fewer than 2^31 pool rows", who);
+    if ((long long)groups->n_groups * h_kv > 65535)
+      return set_error(PKV_ESHAPE, "%s: groups * kv heads must be <= 65535", who);
+    a.group_of = groups->group_of;
+    a.prefix_pages = groups->prefix_pages;
+    a.n_groups = groups->n_groups;
+    a.max_prefix_pages = groups->max_prefix_pages;
+    cascade_split(batch, h_kv, num_q_heads, max_pages_per_seq, groups, &a.chunk_pages,
+                  &a.chunk_grid, &a.prefix_chunk_pages, &a.n_chunk_slots);
+    ca.group_offsets = groups->group_offsets;
+    ca.group_members = groups->group_members;
+    ca.max_members = groups->max_members;
+  }
   if (a.n_chunk_slots > 65535) return set_error(PKV_ESHAPE, "%s: too many chunks", who);
   if (a.n_chunk_slots > 1) {
-    const size_t need = pkv_decode_workspace_size(batch, num_q_heads, h_kv, D, max_pages_per_seq);
+    const size_t need = workspace_bytes_for(batch, num_q_heads, h_kv, D, a.n_chunk_slots);
     if (!workspace || workspace_bytes < need)
       return set_error(PKV_EINVAL, "%s: workspace of %zu bytes needed, %zu given", who, need,
                        workspace_bytes);
@@ -299,7 +392,9 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
     a.counters = reinterpret_cast<int*>(ws + align256(rows * D * sizeof(float)) +
                                         align256(rows * 2 * sizeof(float)));
     // few chunks per sequence: the last CTA of each group merges them (no combine kernel)
-    a.merge_in_place = a.n_chunk_slots <= g_merge_in_place_max.load() ? 1 : 0;
+    // A cascade decode always merges in the decode kernel: a request's one own chunk folds in
+    // its prefix partials, several own chunks merge in place.
+    a.merge_in_place = cascade || a.n_chunk_slots <= g_merge_in_place_max.load() ? 1 : 0;
   }
   if (k_new) {
     if (!v_new) return set_error(PKV_EINVAL, "%s: v_new is NULL", who);
@@ -323,7 +418,7 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
                      "128, a 16-byte aligned q and fewer than 2^31 pool rows", who);
   const bool use_mma = mma_ok && choice != 1;
   CUtensorMap tk, tv;
-  if (use_mma) {
+  if (use_mma || cascade) {
     st = pool_tensor_map(k_cache, desc, &tk);
     if (st == PKV_OK) st = pool_tensor_map(v_cache, desc, &tv);
     if (st != PKV_OK) return st;
@@ -331,7 +426,13 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
   st = error_word(&a.err);
   if (st != PKV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = traced("paged_decode", s, [&] {
+  cudaError_t e;
+  if (cascade) {
+    e = traced("cascade_prefix", s, [&] { return launch_cascade_prefix(a, ca, G, &tk, &tv, s); });
+    st = cuda_status(e, "cascade_prefix launch");
+    if (st != PKV_OK) return st;
+  }
+  e = traced("paged_decode", s, [&] {
     if (use_mma) return launch_decode_mma(a, kv, dtype_q, G, &tk, &tv, s);
     if (kv == PKV_F32) return launch_decode_f32(a, dtype_q, D, G, s);
     if (kv == PKV_BF16) return launch_decode_bf16(a, dtype_q, D, G, s);
@@ -356,7 +457,7 @@ int pkv_paged_decode_attention(const void* q, int32_t dtype_q, int32_t batch,
   return decode_impl("pkv_paged_decode_attention", q, dtype_q, batch, num_q_heads, k_cache,
                      v_cache, desc, block_tables, max_pages_per_seq, context_lens, scale,
                      k_scales, v_scales, out, workspace, workspace_bytes, nullptr, nullptr, 0, 0,
-                     0, stream);
+                     0, nullptr, stream);
 }
 
 int pkv_paged_decode_attention_window(const void* q, int32_t dtype_q, int32_t batch,
@@ -370,7 +471,7 @@ int pkv_paged_decode_attention_window(const void* q, int32_t dtype_q, int32_t ba
   return decode_impl("pkv_paged_decode_attention_window", q, dtype_q, batch, num_q_heads,
                      k_cache, v_cache, desc, block_tables, max_pages_per_seq, context_lens, scale,
                      k_scales, v_scales, out, workspace, workspace_bytes, nullptr, nullptr, 0,
-                     sink_tokens, window, stream);
+                     sink_tokens, window, nullptr, stream);
 }
 
 int pkv_paged_decode_step(const void* q, int32_t dtype_q, int32_t batch, int32_t num_q_heads,
@@ -384,7 +485,7 @@ int pkv_paged_decode_step(const void* q, int32_t dtype_q, int32_t batch, int32_t
   return decode_impl("pkv_paged_decode_step", q, dtype_q, batch, num_q_heads, k_cache, v_cache,
                      desc, block_tables, max_pages_per_seq, context_lens, scale, k_scales,
                      v_scales, out, workspace, workspace_bytes, k_new, v_new, dtype_new, 0, 0,
-                     stream);
+                     nullptr, stream);
 }
 
 int pkv_paged_decode_step_window(const void* q, int32_t dtype_q, int32_t batch,
@@ -399,10 +500,44 @@ int pkv_paged_decode_step_window(const void* q, int32_t dtype_q, int32_t batch,
   return decode_impl("pkv_paged_decode_step_window", q, dtype_q, batch, num_q_heads, k_cache,
                      v_cache, desc, block_tables, max_pages_per_seq, context_lens, scale,
                      k_scales, v_scales, out, workspace, workspace_bytes, k_new, v_new,
-                     dtype_new, sink_tokens, window, stream);
+                     dtype_new, sink_tokens, window, nullptr, stream);
 }
 
 
+
+int pkv_cascade_decode_attention(const void* q, int32_t dtype_q, int32_t batch,
+                                 int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                 const pkv_cache_desc* desc, const int32_t* block_tables,
+                                 int32_t max_pages_per_seq, const int32_t* context_lens,
+                                 float scale, const pkv_cascade_desc* groups, void* out,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl("pkv_cascade_decode_attention", q, dtype_q, batch, num_q_heads, k_cache,
+                     v_cache, desc, block_tables, max_pages_per_seq, context_lens, scale, nullptr,
+                     nullptr, out, workspace, workspace_bytes, nullptr, nullptr, 0, 0, 0, groups,
+                     stream);
+}
+
+int pkv_cascade_decode_step(const void* q, int32_t dtype_q, int32_t batch, int32_t num_q_heads,
+                            const void* k_new, const void* v_new, int32_t dtype_new,
+                            void* k_cache, void* v_cache, const pkv_cache_desc* desc,
+                            const int32_t* block_tables, int32_t max_pages_per_seq,
+                            const int32_t* context_lens, float scale,
+                            const pkv_cascade_desc* groups, void* out, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (!k_new) return set_error(PKV_EINVAL, "pkv_cascade_decode_step: k_new is NULL");
+  return decode_impl("pkv_cascade_decode_step", q, dtype_q, batch, num_q_heads, k_cache,
+                     v_cache, desc, block_tables, max_pages_per_seq, context_lens, scale, nullptr,
+                     nullptr, out, workspace, workspace_bytes, k_new, v_new, dtype_new, 0, 0,
+                     groups, stream);
+}
+
+int pkv_cascade_set_prefix_chunk_pages(int32_t pages) {
+  if (pages < 0 || pages > 4096)
+    return set_error(PKV_EINVAL, "pkv_cascade_set_prefix_chunk_pages: %d outside [0, 4096]",
+                     pages);
+  g_prefix_chunk_override.store(pages);
+  return PKV_OK;
+}
 
 int pkv_kv_append(const void* k_new, const void* v_new, int32_t dtype_new, int32_t num_tokens,
                   const int64_t* slot_mapping, void* k_cache, void* v_cache,

@@ -1,11 +1,13 @@
 // End of a decode CTA, shared by the CUDA-core and tensor-core kernels: the CTA's warps have
 // left their (running max, sum, weighted values) per head in shared memory; merge them, then
-//  * one chunk: write out = acc / l;
-//  * several chunks: write this chunk's partial (m, l, acc) to the workspace; when the call
-//    merges in place (few chunks per sequence), the last CTA of the (request, KV head) to
-//    finish -- found with a counter in the workspace -- merges every chunk of the group in
-//    chunk order and writes out, then resets the counter to 0 for the next call. Otherwise a
-//    separate combine kernel merges the partials.
+//  * the request's only chunk: write out = acc / l -- in a cascade decode after merging in the
+//    partials of the request's shared prefix (chunk slots 0 .. slot0 - 1, written by the
+//    prefix kernel before this launch);
+//  * one of several chunks: write this chunk's partial (m, l, acc) to chunk slot slot0 + c;
+//    when the call merges in place, the last CTA of the (request, KV head) to finish -- found
+//    with a counter in the workspace -- merges every slot of the group in slot order and
+//    writes out, then resets the counter to 0 for the next call. Otherwise a separate combine
+//    kernel merges the partials.
 #pragma once
 
 #include <math.h>
@@ -17,10 +19,11 @@ namespace pkv {
 
 template <typename TQ, int D, int G, int NW, int NTHR>
 __device__ __forceinline__ void decode_epilogue(const DecodeArgs& a, int b, int j, int c,
-                                                int n_chunks, const float* red_acc,
+                                                int n_chunks, int slot0, const float* red_acc,
                                                 const float* red_m, const float* red_l,
                                                 float vs) {
   __shared__ int s_last;
+  const bool direct = n_chunks <= 1;  // this CTA finishes the request
   for (int e = threadIdx.x; e < G * D; e += NTHR) {
     const int g = e / D, i = e % D;
     float M = -INFINITY;
@@ -37,17 +40,46 @@ __device__ __forceinline__ void decode_epilogue(const DecodeArgs& a, int b, int 
     }
     A *= vs;
     const size_t bh = (size_t)b * a.h_q + j * G + g;
-    if (n_chunks <= 1) {
+    if (direct) {
+      if (slot0 > 0) {  // fold in the shared prefix's partials, 8 slots per batch of loads
+        const float* ml = a.ws_ml + bh * a.n_chunk_slots * 2;
+        const float* acc = a.ws_acc + bh * a.n_chunk_slots * D + i;
+        for (int k0 = 0; k0 < slot0; k0 += 8) {
+          float mv[8], lv[8], av[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const bool in = k0 + u < slot0;
+            mv[u] = in ? ml[2 * (k0 + u)] : -INFINITY;
+            lv[u] = in ? ml[2 * (k0 + u) + 1] : 0.f;
+            av[u] = in ? acc[(size_t)(k0 + u) * D] : 0.f;
+          }
+          float Mb = M;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) Mb = fmaxf(Mb, mv[u]);
+          if (Mb == -INFINITY) continue;
+          const float w0 = exp2f(M - Mb);
+          L *= w0;
+          A *= w0;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float w = exp2f(mv[u] - Mb);
+            L = fmaf(w, lv[u], L);
+            A = fmaf(w, av[u], A);
+          }
+          M = Mb;
+        }
+      }
       store_from_float(static_cast<TQ*>(a.out), bh * D + i, L > 0.f ? A / L : 0.f);
     } else {
-      a.ws_acc[(bh * a.n_chunk_slots + c) * D + i] = A;
+      const size_t part = bh * a.n_chunk_slots + slot0 + c;
+      a.ws_acc[part * D + i] = A;
       if (i == 0) {
-        a.ws_ml[(bh * a.n_chunk_slots + c) * 2 + 0] = M;
-        a.ws_ml[(bh * a.n_chunk_slots + c) * 2 + 1] = L;
+        a.ws_ml[part * 2 + 0] = M;
+        a.ws_ml[part * 2 + 1] = L;
       }
     }
   }
-  if (n_chunks <= 1 || !a.merge_in_place) return;
+  if (direct || !a.merge_in_place) return;
 
   // Publish this chunk's partial, then count it; the CTA that brings the count to n_chunks
   // sees every other chunk's partial (each was fenced before its count).
@@ -60,16 +92,17 @@ __device__ __forceinline__ void decode_epilogue(const DecodeArgs& a, int b, int 
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  const int n_total = slot0 + n_chunks;
   for (int e = threadIdx.x; e < G * D; e += NTHR) {
     const int g = e / D, i = e % D;
     const size_t bh = (size_t)b * a.h_q + j * G + g;
     const float* ml = a.ws_ml + bh * a.n_chunk_slots * 2;
     const float* acc = a.ws_acc + bh * a.n_chunk_slots * D + i;
     float M = -INFINITY;
-    for (int k = 0; k < n_chunks; ++k) M = fmaxf(M, __ldcg(ml + 2 * k));
+    for (int k = 0; k < n_total; ++k) M = fmaxf(M, __ldcg(ml + 2 * k));
     float L = 0.f, A = 0.f;
     if (M != -INFINITY) {
-      for (int k = 0; k < n_chunks; ++k) {
+      for (int k = 0; k < n_total; ++k) {
         const float w = exp2f(__ldcg(ml + 2 * k) - M);
         L = fmaf(w, __ldcg(ml + 2 * k + 1), L);
         A = fmaf(w, __ldcg(acc + (size_t)k * D), A);

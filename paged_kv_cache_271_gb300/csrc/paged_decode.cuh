@@ -29,6 +29,7 @@
 
 #include "pkv_device.cuh"
 #include "decode_epilogue.cuh"
+#include "decode_plan.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -197,10 +198,14 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const DecodeArgs a) {
     if (c == 0 && threadIdx.x == 0) atomicOr(a.err, PKV_DEVERR_BAD_PAGE);
     ctx = a.max_pages * kPageSize;
   }
-  const SeqPages sp = seq_pages(ctx, a.sink, a.window);
-  const int pages_seq = sp.n;  // attended pages
-  // the attended pages split into n_chunks near-equal chunks of at most chunk_pages pages
-  const int n_chunks = (pages_seq + a.chunk_pages - 1) / a.chunk_pages;
+  const SeqPlan plan = seq_plan(a, b, ctx);
+  if (plan.prefix > 0 && ctx < plan.prefix * kPageSize + (a.k_new != nullptr ? 1 : 0)) {
+    // a cascade member's context must reach past its group's shared pages
+    if (c == 0 && threadIdx.x == 0) atomicOr(a.err, PKV_DEVERR_BAD_GROUP);
+  }
+  const SeqPages sp = plan.sp;
+  const int pages_seq = sp.n;  // the pages read here, split into n_chunks near-equal chunks
+  const int n_chunks = plan.n_chunks;
   if (c > 0 && c >= n_chunks) return;
   const int per_chunk = n_chunks > 0 ? (pages_seq + n_chunks - 1) / n_chunks : 0;
   const int page0 = c * per_chunk;
@@ -235,8 +240,7 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const DecodeArgs a) {
   const int32_t* btrow = a.block_tables + (size_t)b * a.max_pages;
   const uint64_t pol = l2_evict_first_policy();
 
-  auto issue = [&](int i, int stg) {  // lane 0: fetch page i of the chunk into stage stg
-    const int pid = btrow[logical_page(sp, page0 + i)];
+  auto issue = [&](int i, int stg, int pid) {  // lane 0: page i of the chunk (id pid) -> stage stg
     if (pid < 0 || pid >= a.num_pages) {
       page_ok[stg] = 0;
       atomicOr(a.err, PKV_DEVERR_BAD_PAGE);
@@ -251,8 +255,23 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const DecodeArgs a) {
   };
 
   const int n_mine = n_pages > warp ? (n_pages - warp + NW - 1) / NW : 0;
-  if (lane == 0) {
-    for (int m = 0; m < SPW && m < n_mine; ++m) issue(warp + NW * m, warp * SPW + m);
+  // Page ids of the warp's pages, read 32 at a time ahead of their copies so that no copy waits
+  // on a table read: lane L holds the id of the warp's page 32 t + L (chunk page warp + NW m).
+  int ids = -1;
+  auto load_ids = [&](int t) {
+    const int mm = 32 * t + lane;
+    ids = mm < n_mine ? btrow[logical_page(sp, page0 + warp + NW * mm)] : -1;
+  };
+  load_ids(0);
+  {
+    int first[SPW];
+#pragma unroll
+    for (int m = 0; m < SPW; ++m) first[m] = __shfl_sync(0xffffffffu, ids, m);
+    if (lane == 0) {
+#pragma unroll
+      for (int m = 0; m < SPW; ++m)
+        if (m < n_mine) issue(warp + NW * m, warp * SPW + m, first[m]);
+    }
   }
 
   WarpState<KV, D, G> st;
@@ -288,9 +307,14 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const DecodeArgs a) {
                                make_int3(ctx, a.sink, a.window), pbuf, lane);
     }
     __syncwarp();
-    if (lane == 0 && m + SPW < n_mine) {
-      fence_proxy_async_smem();
-      issue(i + NW * SPW, stg);
+    if (m + SPW < n_mine) {  // warp-uniform
+      const int mn = m + SPW;
+      if ((mn & 31) == 0) load_ids(mn >> 5);
+      const int pid = __shfl_sync(0xffffffffu, ids, mn & 31);
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        issue(i + NW * SPW, stg, pid);
+      }
     }
   }
   if (!ok && lane == 0) {
@@ -320,7 +344,8 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const DecodeArgs a) {
   __syncthreads();
 
   const float vs = KV::bytes == 1 ? a.v_scales[j] : 1.f;
-  decode_epilogue<TQ, D, G, NW, S::kThreads>(a, b, j, c, n_chunks, red_acc, red_m, red_l, vs);
+  decode_epilogue<TQ, D, G, NW, S::kThreads>(a, b, j, c, n_chunks, plan.slot0, red_acc,
+                                             red_m, red_l, vs);
 }
 
 template <typename KV, typename TQ, int D, int G>
@@ -336,7 +361,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_done |= 1ull << dev;
   }
-  dim3 grid(a.n_chunk_slots, a.h_kv, a.batch);
+  dim3 grid(a.chunk_grid, a.h_kv, a.batch);
   kern<<<grid, S::kThreads, S::SMEM_BYTES, s>>>(a);
   return cudaGetLastError();
 }

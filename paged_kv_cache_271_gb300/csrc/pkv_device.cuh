@@ -142,6 +142,12 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return pol;
 }
 
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // Global -> shared bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned),
 // completing as transaction bytes on `bar`. The source is streamed (L2 evict-first).
 __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint32_t bytes,

@@ -32,8 +32,31 @@ struct DecodeArgs {
   int num_pages;
   int max_pages;      // block-table width
   int chunk_pages;    // pages per chunk (one CTA)
-  int n_chunk_slots;  // grid.x = ceil(max_pages / chunk_pages)
+  int n_chunk_slots;  // partial slots per (request, query head)
+  int chunk_grid;     // decode grid.x = ceil(max_pages / chunk_pages) (n_chunk_slots without
+                      // the cascade prefix slots)
   float scale_log2;   // softmax scale * log2(e)
+  // Cascade decode (null group_of otherwise): request b belongs to group group_of[b] (-1:
+  // none), whose first prefix_pages[g] logical pages are shared by every member and handled
+  // by the prefix kernel in chunks of prefix_chunk_pages; their partials take chunk slots
+  // 0 .. ceil(prefix_pages[g] / prefix_chunk_pages) - 1 and the request's own pages follow.
+  const int32_t* group_of;
+  const int32_t* prefix_pages;
+  int n_groups;
+  int max_prefix_pages;
+  int prefix_chunk_pages;
+};
+
+// Query rows ((member, query head) pairs) per CTA of the cascade prefix kernel, and the CTAs
+// of it that run at once on a GB300 (152 SMs x 3 resident CTAs).
+constexpr int kCascadeRows = 64;
+constexpr int kCascadeWaveCtas = 152 * 3;
+
+// Members of the cascade groups (prefix kernel only).
+struct CascadeArgs {
+  const int32_t* group_offsets;  // [n_groups + 1]: members of g are group_members[off[g] .. off[g+1])
+  const int32_t* group_members;  // request indices
+  int max_members;               // rows per group = members * group size; larger groups are cut
 };
 
 struct AppendArgs {
@@ -69,6 +92,9 @@ cudaError_t launch_copy_pages(void* k, void* v, const int32_t* src, const int32_
                               int64_t page_bytes, int num_pages, int* err, cudaStream_t s);
 cudaError_t launch_kv_absmax(const void* x, int dtype, int64_t n_tokens, int h_kv, int head_dim,
                              float code_max, float* scales_out, cudaStream_t s);
+// Shared-prefix pass of the cascade decode (bf16 cache and queries, head_dim 128).
+cudaError_t launch_cascade_prefix(const DecodeArgs& a, const CascadeArgs& ca, int group,
+                                  const void* tk, const void* tv, cudaStream_t s);
 cudaError_t launch_decode_int8(const DecodeArgs& a, int q_dtype, int head_dim, int group,
                                cudaStream_t s);
 

@@ -250,3 +250,75 @@ class ContinuousBatchingRun:
                                            v_scales=v_scales[j:j + 1])
             rows.append(out[0, 0])
         return np.stack(rows)
+
+
+class GroupScenario:
+    """A decode step over a ``workloads.PrefixGroupsInputs`` batch set up through the library:
+    each prefix written once and shared (reference counts) by its members' page tables, every
+    request's own tokens but the last prefilled, then the step's slots reserved."""
+
+    def __init__(self, w, device="cuda"):
+        self.w = w
+        self.device = torch.device(device)
+        P = w.page_size
+        self.cache = PagedKVCache(w.num_pages, w.num_kv_heads, w.head_dim, torch.bfloat16,
+                                  self.device, initial_free_order=w.page_order)
+        fill_junk(self.cache.k, w.fill_seed)
+        fill_junk(self.cache.v, w.fill_seed + 1)
+        self.rids = list(range(w.batch))
+        shared = []
+        for g, n in enumerate(w.prefix_lens):
+            owner = -1 - g
+            self.cache.add_request(owner)
+            s = self.cache.reserve([owner], [int(n)])
+            self.cache.write(s, w.prefix_k[g].to(self.device), w.prefix_v[g].to(self.device))
+            shared.append(list(self.cache.pages[owner][:int(n) // P]))
+        for b in self.rids:
+            g = int(w.group_of[b])
+            if g >= 0:
+                self.cache.add_request(b, shared_pages=shared[g], shared_len=int(w.prefix_lens[g]))
+            else:
+                self.cache.add_request(b)
+        for g in range(len(w.prefix_lens)):
+            self.cache.free_request(-1 - g)
+        self.shared_pages = shared
+        pre = [int(w.prefix_lens[w.group_of[b]]) if w.group_of[b] >= 0 else 0 for b in self.rids]
+        counts = [int(w.context_lens[b]) - 1 - pre[b] for b in self.rids]
+        if sum(counts):
+            ks, vs = [], []
+            for b in self.rids:
+                k, v = w.request_tokens(b)
+                ks.append(k[pre[b]:pre[b] + counts[b]])
+                vs.append(v[pre[b]:pre[b] + counts[b]])
+            s = self.cache.reserve(self.rids, counts)
+            self.cache.write(s, torch.cat(ks, 0).to(self.device), torch.cat(vs, 0).to(self.device))
+        self.step_slots = self.cache.reserve(self.rids, [1] * w.batch)
+        self.slots_dev = torch.from_numpy(self.step_slots).to(self.device)
+        self.k_new = torch.stack([w.request_tokens(b)[0][-1] for b in self.rids]).to(self.device)
+        self.v_new = torch.stack([w.request_tokens(b)[1][-1] for b in self.rids]).to(self.device)
+        self.q = w.q.to(self.device)
+        self.bt_host = self.cache.block_table_array(self.rids)
+        self.cl_host = self.cache.context_lens_array(self.rids)
+        self.block_tables = torch.from_numpy(self.bt_host).to(self.device)
+        self.context_lens = torch.from_numpy(self.cl_host).to(self.device)
+
+    def append(self):
+        self.cache.write(self.slots_dev, self.k_new, self.v_new)
+
+
+def oracle_groups_expected(w, pairs=None, n_threads=0):
+    """The oracle's decode output for a ``PrefixGroupsInputs`` batch, from each request's own
+    contiguous tokens (its prefix followed by its own rows)."""
+    ks, vs, offs = [], [], []
+    o = 0
+    for b in range(w.batch):
+        k, v = w.request_tokens(b)
+        ks.append(k)
+        vs.append(v)
+        offs.append(o)
+        o += k.shape[0]
+    kr = oracle.as_raw(torch.cat(ks, 0), "bf16")
+    vr = oracle.as_raw(torch.cat(vs, 0), "bf16")
+    return oracle.contiguous_decode(oracle.as_raw(w.q, "bf16"), "bf16", kr, vr, "bf16",
+                                    np.array(offs, dtype=np.int64), w.context_lens, w.scale,
+                                    pairs=pairs, n_threads=n_threads)

@@ -316,3 +316,85 @@ def test_prefix_cache_separates_tenants():
     hit = c.lookup(tenant=1, tokens=toks[:35] + [99])
     assert hit == pages[:2] and a.refcount(pages[0]) == 3
     assert c.lookup(tenant=1, tokens=[7] + toks[1:]) == []  # first page differs
+
+
+def _groups_model(bt, cl, min_members=2, min_prefix=1):
+    """Plain restatement of the grouping rule: bucket by first page in batch order, share the
+    longest common run of leading page ids, cut to the full pages before position ctx - 1."""
+    B = bt.shape[0]
+    cap = [min(max(int(c) - 1, 0) // 16, bt.shape[1]) for c in cl]
+    buckets = {}
+    for b in range(B):
+        if cap[b] >= min_prefix:
+            buckets.setdefault(int(bt[b, 0]), []).append(b)
+    out = []
+    for mem in buckets.values():  # dicts keep insertion (first appearance) order
+        if len(mem) < min_members:
+            continue
+        n = min(cap[b] for b in mem)
+        for b in mem[1:]:
+            k = 0
+            while k < n and bt[b, k] == bt[mem[0], k]:
+                k += 1
+            n = k
+        if n >= min_prefix:
+            out.append((mem, n))
+    return out
+
+
+def test_cascade_groups_against_model():
+    rng = np.random.default_rng(3)
+    for trial in range(200):
+        B, W = int(rng.integers(1, 24)), int(rng.integers(1, 12))
+        prompts = rng.integers(0, 6, (4, W))  # a few shared page runs
+        bt = np.empty((B, W), np.int32)
+        for b in range(B):
+            p = prompts[rng.integers(0, 4)].copy()
+            cut = int(rng.integers(0, W + 1))
+            p[cut:] = rng.integers(100, 1000, W - cut)
+            bt[b] = p
+        cl = rng.integers(0, 16 * W + 1, B).astype(np.int32)
+        mm, mp = int(rng.integers(1, 4)), int(rng.integers(0, 3))
+        g = pkv.cascade_groups(bt, cl, min_members=mm, min_prefix_pages=mp)
+        ref = _groups_model(bt, cl, max(mm, 2), max(mp, 1))
+        assert g.n_groups == len(ref)
+        got = [(g.group_members[g.group_offsets[i]:g.group_offsets[i + 1]].tolist(),
+                int(g.prefix_pages[i])) for i in range(g.n_groups)]
+        assert got == ref
+        of = np.full(B, -1)
+        for i, (mem, _) in enumerate(ref):
+            of[mem] = i
+        assert np.array_equal(g.group_of, of)
+        assert g.max_members == max([len(m) for m, _ in ref], default=0)
+        assert g.max_prefix_pages == max([n for _, n in ref], default=0)
+        pre = {b: n for mem, n in ref for b in mem}
+        own = [-(-min(max(int(cl[b]), 0), 16 * W) // 16) - pre.get(b, 0) for b in range(B)]
+        assert g.max_own_pages == max(own, default=0)
+
+
+def test_cascade_argument_errors_are_caught_on_the_host():
+    L = pkv.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    d = _desc(cache_dtype=pkv.BF16)
+    d.head_dim = 128
+    good = pkv._CascadeDesc(fake, fake, fake, fake, 1, 2, 3)
+
+    def call(gd, dtype_q=pkv.BF16, desc=d, maxp=600):
+        return L.pkv_cascade_decode_attention(fake, dtype_q, 2, 8, fake, fake, ctypes.byref(desc),
+                                              fake, maxp, fake, 0.1, ctypes.byref(gd), fake, None,
+                                              0, None)
+    assert call(pkv._CascadeDesc(None, fake, fake, fake, 1, 2, 3)) == -1  # null array
+    assert call(pkv._CascadeDesc(fake, fake, fake, fake, 1, 3, 3)) == -1  # members > batch
+    assert call(pkv._CascadeDesc(fake, fake, fake, fake, 1, 2, 601)) == -1  # prefix > table
+    f32 = _desc(cache_dtype=pkv.F32)
+    f32.head_dim = 128
+    assert call(good, dtype_q=pkv.F32, desc=f32) == -3  # the prefix pass is bf16 only
+    assert call(good) == -1  # needs a workspace
+    assert "workspace" in L.pkv_last_error().decode()
+    g = pkv.CascadeGroups(np.zeros(2, np.int32), np.array([3], np.int32), np.array([0, 2], np.int32),
+                          np.array([0, 1], np.int32), 2, 3)
+    plain = pkv.decode_workspace_size(2, 8, 4, 128, 600)
+    assert pkv.cascade_workspace_size(2, 8, 4, 128, 600, g) > plain
+    none = pkv.CascadeGroups(np.full(2, -1, np.int32), np.zeros(0, np.int32), np.zeros(1, np.int32),
+                             np.zeros(0, np.int32), 0, 0)
+    assert pkv.cascade_workspace_size(2, 8, 4, 128, 600, none) == plain

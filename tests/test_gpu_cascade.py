@@ -1,0 +1,188 @@
+"""Cascade decode (shared prompt prefixes computed once per group) against the oracle.
+
+The cascade splits each member's attention into its group's shared pages (prefix kernel,
+once for all members) and its own pages (decode kernel), merged by the combine kernel; the
+result must be the attention over all of the request's tokens, as the oracle computes it from
+the request's contiguous tokens."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_271_gb300 as pkv
+import workloads
+from gpu_harness import GroupScenario, oracle_groups_expected
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2  # bf16 inputs and P rounded to bf16 in both tensor-core products
+
+
+def _cascade(sc, groups, step=False, out=None, workspace=None):
+    w = sc.w
+    if step:
+        return pkv.cascade_decode_step(sc.q, sc.k_new, sc.v_new, sc.cache.k, sc.cache.v,
+                                       sc.block_tables, sc.context_lens, w.scale, groups,
+                                       out=out, workspace=workspace)
+    return pkv.cascade_decode_attention(sc.q, sc.cache.k, sc.cache.v, sc.block_tables,
+                                        sc.context_lens, w.scale, groups, out=out,
+                                        workspace=workspace)
+
+
+def _check_no_error():
+    assert pkv.device_error() == 0
+
+
+def _case(G, h_kv=2, seed=11, groups=((5, 7, 1, 40), (2, 3, 1, 20)), singles=((1, 60),) * 3):
+    return workloads.prefix_groups("cascade_g%d" % G, workloads.BASE_SEED + 500 + seed, G * h_kv,
+                                   h_kv, 128, list(groups), list(singles))
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_cascade_matches_oracle(G, kernel):
+    w = _case(G)
+    sc = GroupScenario(w)
+    sc.append()
+    groups = pkv.cascade_groups(sc.bt_host, sc.cl_host).to(sc.q.device)
+    assert groups.n_groups == 2 and sorted(groups.prefix_pages.tolist()) == [2, 5]
+    pkv.device_error()
+    pkv.decode_set_kernel(kernel)
+    try:
+        out = _cascade(sc, groups)
+    finally:
+        pkv.decode_set_kernel(0)
+    torch.cuda.synchronize()
+    _check_no_error()
+    ref = oracle_groups_expected(w)
+    err = np.abs(out.float().cpu().numpy() - ref).max()
+    assert err < TOL, err
+
+
+def test_cascade_step_equals_append_then_cascade_and_oracle():
+    w = _case(4, h_kv=4, seed=12)
+    sc = GroupScenario(w)
+    groups = pkv.cascade_groups(sc.bt_host, sc.cl_host).to(sc.q.device)
+    k0, v0 = sc.cache.k.clone(), sc.cache.v.clone()
+    pkv.device_error()
+    fused = _cascade(sc, groups, step=True).clone()
+    k1, v1 = sc.cache.k.clone(), sc.cache.v.clone()
+    sc.cache.k.copy_(k0)
+    sc.cache.v.copy_(v0)
+    sc.append()
+    split = _cascade(sc, groups)
+    torch.cuda.synchronize()
+    _check_no_error()
+    assert torch.equal(sc.cache.k.view(torch.uint8), k1.view(torch.uint8))
+    assert torch.equal(sc.cache.v.view(torch.uint8), v1.view(torch.uint8))
+    assert torch.equal(fused, split)
+    err = np.abs(fused.float().cpu().numpy() - oracle_groups_expected(w)).max()
+    assert err < TOL, err
+
+
+@pytest.mark.parametrize("chunk", [1, 3, 8, 32])
+def test_cascade_prefix_chunking_and_ragged_row_tiles(chunk):
+    # 70 shared pages split into several chunks; 17 members x 4 heads = 68 rows: a ragged
+    # second row tile; singles long enough to need the split decode too
+    w = _case(4, h_kv=2, seed=13, groups=((70, 17, 1, 90),), singles=((700, 1400),) * 2)
+    sc = GroupScenario(w)
+    sc.append()
+    groups = pkv.cascade_groups(sc.bt_host, sc.cl_host).to(sc.q.device)
+    pkv.cascade_set_prefix_chunk_pages(chunk)
+    pkv.device_error()
+    try:
+        assert pkv.cascade_prefix_chunk_pages(2, 8, groups) == chunk
+        out = _cascade(sc, groups)
+        torch.cuda.synchronize()
+    finally:
+        pkv.cascade_set_prefix_chunk_pages(0)
+    _check_no_error()
+    err = np.abs(out.float().cpu().numpy() - oracle_groups_expected(w)).max()
+    assert err < TOL, err
+
+
+def test_cascade_with_empty_suffix_and_no_groups():
+    # a member whose context ends exactly at the end of the shared pages (attention only):
+    # its own part is empty and the merge takes the prefix partials alone
+    w = _case(4, h_kv=2, seed=14, groups=((3, 4, 1, 30),), singles=((1, 9),))
+    sc = GroupScenario(w)
+    sc.append()
+    ref = oracle_groups_expected(w)
+    groups = pkv.cascade_groups(sc.bt_host, sc.cl_host)
+    # trim one member's context to the shared pages: still a valid cascade for attention
+    b = int(groups.group_members[0])
+    cl = sc.cl_host.copy()
+    cl[b] = 16 * int(groups.prefix_pages[0])
+    sc.context_lens.copy_(torch.from_numpy(cl))
+    groups.to(sc.q.device)
+    pkv.device_error()
+    out = _cascade(sc, groups)
+    plain = pkv.paged_decode_attention(sc.q, sc.cache.k, sc.cache.v, sc.block_tables,
+                                       sc.context_lens, w.scale)
+    torch.cuda.synchronize()
+    _check_no_error()
+    assert (out.float() - plain.float()).abs().max().item() < TOL
+    others = [i for i in range(w.batch) if i != b]
+    err = np.abs(out.float().cpu().numpy()[others] - ref[others]).max()
+    assert err < TOL, err
+    # no group at all: exactly the plain decode
+    none = pkv.cascade_groups(sc.bt_host, sc.cl_host, min_members=w.batch + 1).to(sc.q.device)
+    assert none.n_groups == 0
+    assert torch.equal(_cascade(sc, none), plain)
+
+
+def test_cascade_flags_members_that_do_not_cover_the_prefix():
+    w = _case(4, h_kv=2, seed=15, groups=((3, 4, 5, 30),), singles=())
+    sc = GroupScenario(w)
+    sc.append()
+    groups = pkv.cascade_groups(sc.bt_host, sc.cl_host)
+    cl = sc.cl_host.copy()
+    cl[int(groups.group_members[1])] = 20  # shorter than the 48 shared positions
+    sc.context_lens.copy_(torch.from_numpy(cl))
+    groups.to(sc.q.device)
+    pkv.device_error()
+    _cascade(sc, groups)
+    assert pkv.device_error() & pkv.DEVERR_BAD_GROUP
+
+
+def test_cascade_prefix_sharing_full_size_sampled():
+    # 128 requests on one 2000-token prefix (125 pages), own suffixes U[5, 200]
+    w = workloads.prefix_sharing()
+    from gpu_harness import Scenario, oracle_expected
+    sc = Scenario(w)
+    sc.append()
+    bt = sc.block_tables.cpu().numpy()
+    groups = pkv.cascade_groups(bt, sc.context_lens.cpu().numpy()).to(sc.q.device)
+    assert groups.n_groups == 1 and int(groups.prefix_pages[0]) == 125
+    pkv.device_error()
+    out = pkv.cascade_decode_attention(sc.q, sc.cache.k, sc.cache.v, sc.block_tables,
+                                       sc.context_lens, w.scale, groups)
+    plain = sc.decode()
+    torch.cuda.synchronize()
+    _check_no_error()
+    assert (out.float() - plain.float()).abs().max().item() < TOL
+    rng = np.random.default_rng(5)
+    pairs = np.stack([rng.integers(0, w.batch, 48), rng.integers(0, w.num_q_heads, 48)], 1)
+    ref = oracle_expected(w, pairs=pairs)
+    got = out.float().cpu().numpy()[pairs[:, 0], pairs[:, 1]]
+    assert np.abs(got - ref).max() < TOL
+
+
+@pytest.mark.parametrize("own_chunk", [1, 2])
+def test_cascade_members_with_several_own_chunks(own_chunk):
+    # own pages split into chunks of 1-2 pages: every member's chunks write partials after its
+    # prefix partials and the last chunk to finish merges them all (in place)
+    w = _case(8, h_kv=2, seed=16, groups=((4, 5, 20, 70), (9, 3, 40, 90)), singles=((30, 200),))
+    sc = GroupScenario(w)
+    sc.append()
+    groups = pkv.cascade_groups(sc.bt_host, sc.cl_host).to(sc.q.device)
+    pkv.decode_set_chunk_pages(own_chunk)
+    pkv.device_error()
+    try:
+        outs = [_cascade(sc, groups).clone() for _ in range(2)]  # counters reset between calls
+        torch.cuda.synchronize()
+    finally:
+        pkv.decode_set_chunk_pages(0)
+    _check_no_error()
+    assert torch.equal(outs[0], outs[1])
+    err = np.abs(outs[0].float().cpu().numpy() - oracle_groups_expected(w)).max()
+    assert err < TOL, err

@@ -155,6 +155,82 @@ def prefix_sharing(batch: int = 128, prefix_len: int = 2000) -> DecodeInputs:
                      pages, prefix_len=prefix_len)
 
 
+@dataclasses.dataclass
+class PrefixGroupsInputs:
+    """A batch where several prompt prefixes are each shared by a set of requests and the
+    other requests share nothing ("Prefix caching" section: requests with a common system
+    prompt). Request b belongs to prefix ``group_of[b]`` (-1: none); its tokens are the
+    ``prefix_lens[g]`` rows of ``prefix_k[g]``/``prefix_v[g]`` followed by rows
+    ``offsets[b] ..`` of ``k_tokens``/``v_tokens``; ``context_lens[b]`` counts both. The last
+    token of every request is the one the step appends. bf16 values, bf16 queries."""
+
+    name: str
+    batch: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    group_of: np.ndarray  # int32 [B]
+    prefix_lens: np.ndarray  # int32 [n_prefixes], whole pages
+    prefix_k: list
+    prefix_v: list
+    context_lens: np.ndarray  # int32 [B]
+    offsets: np.ndarray  # int64 [B]
+    k_tokens: torch.Tensor
+    v_tokens: torch.Tensor
+    q: torch.Tensor
+    num_pages: int
+    page_order: np.ndarray
+    scale: float
+    fill_seed: int
+    kv_dtype: str = "bf16"
+    q_dtype: str = "bf16"
+
+    def request_tokens(self, b: int):
+        g = int(self.group_of[b])
+        n_pre = int(self.prefix_lens[g]) if g >= 0 else 0
+        o, n_own = int(self.offsets[b]), int(self.context_lens[b]) - n_pre
+        k, v = self.k_tokens[o:o + n_own], self.v_tokens[o:o + n_own]
+        if g >= 0:
+            k = torch.cat([self.prefix_k[g][:n_pre], k], 0)
+            v = torch.cat([self.prefix_v[g][:n_pre], v], 0)
+        return k, v
+
+
+def prefix_groups(name, seed, h_q, h_kv, d, groups, singles=(), slack=0.10):
+    """``groups``: (prefix pages, members, lowest, highest own length) per prefix; own lengths
+    are U[lowest, highest] (>= 1: the step's token); ``singles``: (lowest, highest) length
+    ranges of requests with no shared prefix. Batch order is a seeded shuffle of them all."""
+    g = _gen(seed)
+    kinds = []
+    for gi, (_, members, lo, hi) in enumerate(groups):
+        kinds += [(gi, lo, hi)] * int(members)
+    kinds += [(-1, lo, hi) for lo, hi in singles]
+    perm = torch.randperm(len(kinds), generator=g).tolist()
+    kinds = [kinds[i] for i in perm]
+    B = len(kinds)
+    prefix_lens = np.array([int(p) * PAGE_SIZE for p, _, _, _ in groups], dtype=np.int32)
+    group_of = np.array([k[0] for k in kinds], dtype=np.int32)
+    own = np.array([int(torch.randint(lo, hi + 1, (1,), generator=g)) for _, lo, hi in kinds],
+                   dtype=np.int64)
+    lens = own + np.array([prefix_lens[k[0]] if k[0] >= 0 else 0 for k in kinds], dtype=np.int64)
+    offsets = np.zeros(B, dtype=np.int64)
+    if B > 1:
+        offsets[1:] = np.cumsum(own)[:-1]
+    pk = [_normal((int(n), h_kv, d), "bf16", g) for n in prefix_lens]
+    pv = [_normal((int(n), h_kv, d), "bf16", g) for n in prefix_lens]
+    k = _normal((int(own.sum()), h_kv, d), "bf16", g)
+    v = _normal((int(own.sum()), h_kv, d), "bf16", g)
+    q = _normal((B, h_q, d), "bf16", g)
+    pages = _pool_pages(list(own + PAGE_SIZE), PAGE_SIZE, slack) + int(sum(p for p, *_ in groups))
+    order = torch.randperm(pages, generator=g).numpy().astype(np.int32)
+    return PrefixGroupsInputs(name=name, batch=B, num_q_heads=h_q, num_kv_heads=h_kv, head_dim=d,
+                              page_size=PAGE_SIZE, group_of=group_of, prefix_lens=prefix_lens,
+                              prefix_k=pk, prefix_v=pv, context_lens=lens.astype(np.int32),
+                              offsets=offsets, k_tokens=k, v_tokens=v, q=q, num_pages=int(pages),
+                              page_order=order, scale=1.0 / math.sqrt(d), fill_seed=seed + 7)
+
+
 def custom(name, seed, batch, h_q, h_kv, d, kv_dtype, q_dtype, lens, slack=0.10,
            prefix_len=0) -> DecodeInputs:
     """Any shape, for parity sweeps and edge cases."""
