@@ -180,6 +180,16 @@ class StepState:
         own = own_tokens * row_bytes + 2 * self.batch * self.h_q * self.d * 2 + self.append_bytes()
         return {"cascade_prefix": ("tensor", pre_flops, pre_bytes), "paged_decode": ("hbm", own)}
 
+    def unique_bytes(self):
+        """Bytes of distinct pages the step reads (shared pages once) + queries + outputs."""
+        bt = self.bt.cpu().numpy()
+        cl = self.cl.cpu().numpy()
+        pages = set()
+        for b in range(self.batch):
+            pages.update(int(p) for p in bt[b, :(int(cl[b]) + 15) // 16])
+        tile = 2 * self.h_kv * 16 * self.d * self.kv_bytes
+        return len(pages) * tile + 2 * self.batch * self.h_q * self.d * 2
+
     def used_kv_bytes(self):
         """Bytes of the pool pages that hold tokens (K and V)."""
         a = self.cache.allocator
@@ -462,6 +472,21 @@ def run_ours(args):
     ms_step = float(np.mean(ms))
     assert pkv.device_error() == 0
 
+    # The other L2 treatment, for comparison: a 256 MiB write before every step (rotate mode),
+    # or no flush and one pool copy (flush mode).
+    alt = L2Flush(FLUSH_BYTES if args.l2 == "rotate" else 0, dev)
+    a_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    a_ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        alt.zero_()
+        a_starts[i].record(stream)
+        graphs[0].replay()
+        a_ends[i].record(stream)
+    torch.cuda.synchronize()
+    alt_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(a_starts, a_ends)]))
+    del alt
+
     # Per-kernel durations: the same steps launched directly with the library's tracing on
     # (events on the launching stream around every kernel).
     pkv.trace_reset()
@@ -532,6 +557,12 @@ def run_ours(args):
             "dtype": "bf16" if sc.kv_bytes == 2 else ("fp8_e4m3/f16" if sc.kv_bytes == 1 else "f32"),
             "data": "synthetic", "config": dict(sc.config, parallelism="replicas x%d" % ws),
             "decode_tokens_per_s": round(ws * sc.batch / (max_ms * 1e-3), 1),
+            "tokens_per_s_32_layer_projection": round(ws * sc.batch / (32 * max_ms * 1e-3), 1),
+            "steps_per_s": round(1e3 / max_ms, 1),
+            "unique_bytes_GBs": round(ws * sc.unique_bytes() / (max_ms * 1e-3) / 1e9, 1),
+            ("l2_flushed" if args.l2 == "rotate" else "l2_not_flushed"): {
+                "ms_per_step": round(alt_ms, 5),
+                "value": round(aggregate(per_step_bytes, alt_ms, 1) * ws, 1)},
             "pct_of_peak": {"measured_copy_%s" % peak_kind: round(100 * value / ws / hbm_peak, 2),
                             "nominal_8TBs": round(100 * value / ws / NOMINAL_HBM_GBS, 2)},
             "roofline": roofline,

@@ -408,6 +408,10 @@ int pkv_cascade_decode_step(const void* q, int32_t dtype_q, int32_t batch, int32
 /* Tuning: pages per CTA of the prefix pass (0 = automatic). */
 int pkv_cascade_set_prefix_chunk_pages(int32_t pages);
 
+/* Tuning: the prefix pass on tcgen05 (tensor memory accumulators, 128 rows per CTA; 0 =
+ * automatic, 2) or on mma.sync (64 rows per CTA; 1). Same results up to rounding. */
+int pkv_cascade_set_prefix_kernel(int32_t which);
+
 /* ---- prefix cache (host) ----------------------------------------------------------------- */
 
 /*

@@ -119,6 +119,7 @@ def lib():
         "pkv_cascade_decode_step": (ctypes.c_int, [vp, i32, i32, i32, vp, vp, i32, vp, vp, D, vp,
                                                    i32, vp, f32, C, vp, vp, sz, vp]),
         "pkv_cascade_set_prefix_chunk_pages": (ctypes.c_int, [i32]),
+        "pkv_cascade_set_prefix_kernel": (ctypes.c_int, [i32]),
         "pkv_trace_enable": (ctypes.c_int, [ctypes.c_int]),
         "pkv_trace_reset": (ctypes.c_int, []),
         "pkv_trace_read": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(i32),
@@ -368,6 +369,11 @@ def cascade_prefix_chunk_pages(num_kv_heads, num_q_heads, groups: CascadeGroups)
 
 def cascade_set_prefix_chunk_pages(pages: int):
     _check(lib().pkv_cascade_set_prefix_chunk_pages(int(pages)))
+
+
+def cascade_set_prefix_kernel(which: int):
+    """0 automatic (tcgen05), 1 mma.sync, 2 tcgen05."""
+    _check(lib().pkv_cascade_set_prefix_kernel(int(which)))
 
 
 def _cascade_common(q, k_cache, block_tables, context_lens, groups, workspace):

@@ -100,24 +100,33 @@ struct MapEntry {
   long long rows;
   int head_dim;
   int dtype;
+  int rank;
   CUtensorMap map;
 };
 std::mutex g_map_mu;
 std::vector<MapEntry> g_maps;
 EncodeTiledFn g_encode = nullptr;
 
-// A pool seen as a 2-D tensor [num_pages * h_kv * 16 rows][head_dim], loaded in boxes of 16
-// rows x 128 bytes with the 128-byte swizzle. Encoded once per (device, pool, shape).
-int pool_tensor_map(const void* base, const pkv_cache_desc* d, CUtensorMap* out) {
+// The TMA view of a pool, encoded once per (device, pool, shape). A row of 128 bytes (FP8,
+// INT8 at head_dim 128) is a 2-D tensor [num_pages * h_kv * 16 rows][128 bytes], one
+// (page, KV head) tile per box of 16 rows. A bf16 row of 256 bytes is a 3-D tensor
+// [2 halves][rows][64 elements] (halves 128 bytes apart, rows 256 bytes apart), so that one box
+// of 2 x 16 x 64 moves a whole (page, KV head) tile into shared memory as two 128-byte-swizzled
+// blocks of 16 rows, the first half of every row before the second (the layout the kernels
+// read); *rank receives 2 or 3.
+int pool_tensor_map(const void* base, const pkv_cache_desc* d, CUtensorMap* out, int* rank) {
   int dev = 0;
   cudaError_t ce = cudaGetDevice(&dev);
   if (ce != cudaSuccess) return set_error(PKV_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
   const long long rows = (long long)d->num_pages * d->num_kv_heads * d->page_size;
+  const int eb = d->cache_dtype == PKV_BF16 ? 2 : 1;
+  const int want_rank = d->head_dim * eb == 256 ? 3 : 2;
   std::lock_guard<std::mutex> lk(g_map_mu);
   for (auto& e : g_maps)
     if (e.dev == dev && e.base == base && e.rows == rows && e.head_dim == d->head_dim &&
         e.dtype == d->cache_dtype) {
       *out = e.map;
+      *rank = e.rank;
       return PKV_OK;
     }
   if (!g_encode) {
@@ -129,26 +138,41 @@ int pool_tensor_map(const void* base, const pkv_cache_desc* d, CUtensorMap* out)
       return set_error(PKV_ECUDA, "cuTensorMapEncodeTiled is not available");
     g_encode = reinterpret_cast<EncodeTiledFn>(fn);
   }
-  const int eb = d->cache_dtype == PKV_BF16 ? 2 : 1;
   MapEntry e{};
   e.dev = dev;
   e.base = base;
   e.rows = rows;
   e.head_dim = d->head_dim;
   e.dtype = d->cache_dtype;
-  const cuuint64_t dims[2] = {(cuuint64_t)d->head_dim, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)d->head_dim * eb};
-  const cuuint32_t box[2] = {(cuuint32_t)(128 / eb), (cuuint32_t)d->page_size};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(&e.map,
-                        eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                        2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUtensorMapDataType dt =
+      eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUresult r;
+  if (want_rank == 3) {
+    const cuuint64_t dims[3] = {64, (cuuint64_t)rows, 2};
+    const cuuint64_t strides[2] = {256, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)d->page_size, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    r = g_encode(&e.map, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    e.rank = 3;
+    if (r != CUDA_SUCCESS) e.rank = 2;  // not accepted: two 2-D boxes per tile instead
+  }
+  if (want_rank == 2 || e.rank == 2) {
+    const cuuint64_t dims[2] = {(cuuint64_t)d->head_dim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)d->head_dim * eb};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / eb), (cuuint32_t)d->page_size};
+    const cuuint32_t estr[2] = {1, 1};
+    r = g_encode(&e.map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    e.rank = 2;
+  }
   if (r != CUDA_SUCCESS) return set_error(PKV_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   if (g_maps.size() >= 256) g_maps.clear();  // callers keep few pools; drop stale entries
   g_maps.push_back(e);
   *out = e.map;
+  *rank = e.rank;
   return PKV_OK;
 }
 
@@ -180,17 +204,25 @@ size_t workspace_bytes_for(int batch, int h_q, int h_kv, int head_dim, int slots
 
 std::atomic<int> g_prefix_chunk_override{0};
 
+std::atomic<int> g_prefix_kernel{0};  // 0 automatic (tcgen05), 1 mma.sync, 2 tcgen05
+bool prefix_on_tcgen05() { return g_prefix_kernel.load() != 1; }
+
 // Pages per CTA of the cascade prefix kernel: the shared pages of each (group, KV head, row
-// tile) are cut into as many chunks (of at least 2 pages) as keep the launch within one wave
-// of resident CTAs (kCascadeWaveCtas); a chunk of at most the whole prefix.
+// tile) are cut into as many chunks as keep the launch within one wave of resident CTAs
+// (tcgen05: 128 rows per CTA, one CTA per SM, chunks of at least one 4-page tile; mma.sync:
+// 64 rows, three CTAs per SM, at least 2 pages); a chunk of at most the whole prefix.
 int prefix_chunk_pages_for(int n_groups, int h_kv, int group, int max_members, int max_prefix) {
   const int ov = g_prefix_chunk_override.load();
   if (ov > 0) return ov;
   if (max_prefix < 1) return 1;
-  const long long tiles = ((long long)max_members * group + kCascadeRows - 1) / kCascadeRows;
+  const bool tc = prefix_on_tcgen05();
+  const int rows = tc ? kCascadeTcRows : kCascadeRows;
+  const int wave = tc ? kCascadeTcWaveCtas : kCascadeWaveCtas;
+  const int min_pages = tc ? 4 : 2;
+  const long long tiles = ((long long)max_members * group + rows - 1) / rows;
   const long long units = (long long)n_groups * h_kv * tiles;
-  long long chunks = kCascadeWaveCtas / (units > 0 ? units : 1);
-  chunks = std::max(1ll, std::min(chunks, (long long)(max_prefix + 1) / 2));
+  long long chunks = wave / (units > 0 ? units : 1);
+  chunks = std::max(1ll, std::min(chunks, (long long)(max_prefix + min_pages - 1) / min_pages));
   return (int)((max_prefix + chunks - 1) / chunks);
 }
 
@@ -419,8 +451,11 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
   const bool use_mma = mma_ok && choice != 1;
   CUtensorMap tk, tv;
   if (use_mma || cascade) {
-    st = pool_tensor_map(k_cache, desc, &tk);
-    if (st == PKV_OK) st = pool_tensor_map(v_cache, desc, &tv);
+    int rk = 2, rv = 2;
+    st = pool_tensor_map(k_cache, desc, &tk, &rk);
+    if (st == PKV_OK) st = pool_tensor_map(v_cache, desc, &tv, &rv);
+    if (st == PKV_OK && rk != rv) st = set_error(PKV_ECUDA, "%s: pool tensor maps differ", who);
+    a.tma_rank = rk;
     if (st != PKV_OK) return st;
   }
   st = error_word(&a.err);
@@ -428,7 +463,10 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (cascade) {
-    e = traced("cascade_prefix", s, [&] { return launch_cascade_prefix(a, ca, G, &tk, &tv, s); });
+    e = traced("cascade_prefix", s, [&] {
+      return prefix_on_tcgen05() ? launch_cascade_prefix_tc(a, ca, G, &tk, &tv, s)
+                                 : launch_cascade_prefix(a, ca, G, &tk, &tv, s);
+    });
     st = cuda_status(e, "cascade_prefix launch");
     if (st != PKV_OK) return st;
   }
@@ -529,6 +567,13 @@ int pkv_cascade_decode_step(const void* q, int32_t dtype_q, int32_t batch, int32
                      v_cache, desc, block_tables, max_pages_per_seq, context_lens, scale, nullptr,
                      nullptr, out, workspace, workspace_bytes, k_new, v_new, dtype_new, 0, 0,
                      groups, stream);
+}
+
+int pkv_cascade_set_prefix_kernel(int32_t which) {
+  if (which < 0 || which > 2)
+    return set_error(PKV_EINVAL, "pkv_cascade_set_prefix_kernel: %d is not 0, 1 or 2", which);
+  g_prefix_kernel.store(which);
+  return PKV_OK;
 }
 
 int pkv_cascade_set_prefix_chunk_pages(int32_t pages) {

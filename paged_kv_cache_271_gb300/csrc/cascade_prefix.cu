@@ -121,11 +121,8 @@ __global__ void __launch_bounds__(32 * kCpWarps, 3) cascade_prefix_kernel(
     for (int k = 0; k < 2; ++k) {
       if (pid[k] < 0) continue;
       const int row = (pid[k] * a.h_kv + j) * kPageSize;
-#pragma unroll
-      for (int bx = 0; bx < 2; ++bx) {
-        tma_load_2d(dst + k * kCpTile + bx * 2048, &tm_k, bx * 64, row, &full[stg], pol);
-        tma_load_2d(dst + (2 + k) * kCpTile + bx * 2048, &tm_v, bx * 64, row, &full[stg], pol);
-      }
+      tma_tile<2, 64>(dst + k * kCpTile, &tm_k, a.tma_rank, row, &full[stg], pol);
+      tma_tile<2, 64>(dst + (2 + k) * kCpTile, &tm_v, a.tma_rank, row, &full[stg], pol);
     }
   };
   if (threadIdx.x == 0)

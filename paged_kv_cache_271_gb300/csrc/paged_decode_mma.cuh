@@ -130,6 +130,31 @@ __device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const CUtensorMap
       : "memory");
 }
 
+// 3-D tiled TMA load of one box (a whole (page, KV head) tile of a bf16 pool, as two
+// swizzled 2 KB blocks: the first 64 dims of its 16 rows, then the last 64).
+__device__ __forceinline__ void tma_load_3d(uint32_t smem_dst, const CUtensorMap* map, int y,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(0), "r"(smem_u32(bar)),
+      "l"(policy)
+      : "memory");
+}
+
+// One (page, KV head) tile of K or V into shared memory: one 3-D box for a bf16 pool whose
+// tensor map has rank 3, else one 2-D box per 128 bytes of row.
+template <int BOXES, int BOX_ELEMS>
+__device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap* map, int rank, int row,
+                                         uint64_t* bar, uint64_t policy) {
+  if (BOXES == 2 && rank == 3) {
+    tma_load_3d(dst, map, row, bar, policy);
+  } else {
+#pragma unroll
+    for (int bx = 0; bx < BOXES; ++bx) tma_load_2d(dst + bx * 2048, map, bx * BOX_ELEMS, row, bar, policy);
+  }
+}
+
 // Byte offset of 16-byte chunk `chunk` (0 .. ROW_BYTES/16) of row `row` in a tile stored as
 // 128-byte-swizzled boxes of 16 rows (box b at b*2048).
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
@@ -220,12 +245,9 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
       mbar_arrive_expect_tx(&full[stg], S::STAGE_BYTES);
       const int row = (pid * a.h_kv + j) * kPageSize;
       const uint32_t dst = ring_u32 + stg * S::STAGE_BYTES;
-#pragma unroll
-      for (int bx = 0; bx < S::BOXES; ++bx) {
-        tma_load_2d(dst + bx * 2048, &tm_k, bx * S::BOX_ELEMS, row, &full[stg], pol);
-        tma_load_2d(dst + S::TILE_BYTES + bx * 2048, &tm_v, bx * S::BOX_ELEMS, row, &full[stg],
-                    pol);
-      }
+      tma_tile<S::BOXES, S::BOX_ELEMS>(dst, &tm_k, a.tma_rank, row, &full[stg], pol);
+      tma_tile<S::BOXES, S::BOX_ELEMS>(dst + S::TILE_BYTES, &tm_v, a.tma_rank, row, &full[stg],
+                                       pol);
     }
   };
 

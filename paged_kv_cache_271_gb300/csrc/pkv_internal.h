@@ -36,6 +36,7 @@ struct DecodeArgs {
   int chunk_grid;     // decode grid.x = ceil(max_pages / chunk_pages) (n_chunk_slots without
                       // the cascade prefix slots)
   float scale_log2;   // softmax scale * log2(e)
+  int tma_rank;       // tensor maps of a 256-byte-row pool: 3 (one box per tile) or 2
   // Cascade decode (null group_of otherwise): request b belongs to group group_of[b] (-1:
   // none), whose first prefix_pages[g] logical pages are shared by every member and handled
   // by the prefix kernel in chunks of prefix_chunk_pages; their partials take chunk slots
@@ -51,6 +52,9 @@ struct DecodeArgs {
 // of it that run at once on a GB300 (152 SMs x 3 resident CTAs).
 constexpr int kCascadeRows = 64;
 constexpr int kCascadeWaveCtas = 152 * 3;
+// The same for the tcgen05 prefix kernel (M = 128 rows per CTA, one CTA per SM).
+constexpr int kCascadeTcRows = 128;
+constexpr int kCascadeTcWaveCtas = 152;
 
 // Members of the cascade groups (prefix kernel only).
 struct CascadeArgs {
@@ -95,6 +99,9 @@ cudaError_t launch_kv_absmax(const void* x, int dtype, int64_t n_tokens, int h_k
 // Shared-prefix pass of the cascade decode (bf16 cache and queries, head_dim 128).
 cudaError_t launch_cascade_prefix(const DecodeArgs& a, const CascadeArgs& ca, int group,
                                   const void* tk, const void* tv, cudaStream_t s);
+// The same pass on tcgen05 (accumulators in tensor memory).
+cudaError_t launch_cascade_prefix_tc(const DecodeArgs& a, const CascadeArgs& ca, int group,
+                                     const void* tk, const void* tv, cudaStream_t s);
 cudaError_t launch_decode_int8(const DecodeArgs& a, int q_dtype, int head_dim, int group,
                                cudaStream_t s);
 

@@ -37,9 +37,16 @@ def _case(G, h_kv=2, seed=11, groups=((5, 7, 1, 40), (2, 3, 1, 20)), singles=((1
                                    h_kv, 128, list(groups), list(singles))
 
 
+@pytest.fixture(params=[1, 2], ids=["prefix_mma_sync", "prefix_tcgen05"])
+def prefix_kernel(request):
+    pkv.cascade_set_prefix_kernel(request.param)
+    yield request.param
+    pkv.cascade_set_prefix_kernel(0)
+
+
 @pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
 @pytest.mark.parametrize("kernel", [1, 2])
-def test_cascade_matches_oracle(G, kernel):
+def test_cascade_matches_oracle(G, kernel, prefix_kernel):
     w = _case(G)
     sc = GroupScenario(w)
     sc.append()
@@ -58,7 +65,7 @@ def test_cascade_matches_oracle(G, kernel):
     assert err < TOL, err
 
 
-def test_cascade_step_equals_append_then_cascade_and_oracle():
+def test_cascade_step_equals_append_then_cascade_and_oracle(prefix_kernel):
     w = _case(4, h_kv=4, seed=12)
     sc = GroupScenario(w)
     groups = pkv.cascade_groups(sc.bt_host, sc.cl_host).to(sc.q.device)
@@ -80,7 +87,7 @@ def test_cascade_step_equals_append_then_cascade_and_oracle():
 
 
 @pytest.mark.parametrize("chunk", [1, 3, 8, 32])
-def test_cascade_prefix_chunking_and_ragged_row_tiles(chunk):
+def test_cascade_prefix_chunking_and_ragged_row_tiles(chunk, prefix_kernel):
     # 70 shared pages split into several chunks; 17 members x 4 heads = 68 rows: a ragged
     # second row tile; singles long enough to need the split decode too
     w = _case(4, h_kv=2, seed=13, groups=((70, 17, 1, 90),), singles=((700, 1400),) * 2)
@@ -100,7 +107,7 @@ def test_cascade_prefix_chunking_and_ragged_row_tiles(chunk):
     assert err < TOL, err
 
 
-def test_cascade_with_empty_suffix_and_no_groups():
+def test_cascade_with_empty_suffix_and_no_groups(prefix_kernel):
     # a member whose context ends exactly at the end of the shared pages (attention only):
     # its own part is empty and the merge takes the prefix partials alone
     w = _case(4, h_kv=2, seed=14, groups=((3, 4, 1, 30),), singles=((1, 9),))
@@ -130,7 +137,7 @@ def test_cascade_with_empty_suffix_and_no_groups():
     assert torch.equal(_cascade(sc, none), plain)
 
 
-def test_cascade_flags_members_that_do_not_cover_the_prefix():
+def test_cascade_flags_members_that_do_not_cover_the_prefix(prefix_kernel):
     w = _case(4, h_kv=2, seed=15, groups=((3, 4, 5, 30),), singles=())
     sc = GroupScenario(w)
     sc.append()
@@ -144,7 +151,7 @@ def test_cascade_flags_members_that_do_not_cover_the_prefix():
     assert pkv.device_error() & pkv.DEVERR_BAD_GROUP
 
 
-def test_cascade_prefix_sharing_full_size_sampled():
+def test_cascade_prefix_sharing_full_size_sampled(prefix_kernel):
     # 128 requests on one 2000-token prefix (125 pages), own suffixes U[5, 200]
     w = workloads.prefix_sharing()
     from gpu_harness import Scenario, oracle_expected
@@ -168,7 +175,7 @@ def test_cascade_prefix_sharing_full_size_sampled():
 
 
 @pytest.mark.parametrize("own_chunk", [1, 2])
-def test_cascade_members_with_several_own_chunks(own_chunk):
+def test_cascade_members_with_several_own_chunks(own_chunk, prefix_kernel):
     # own pages split into chunks of 1-2 pages: every member's chunks write partials after its
     # prefix partials and the last chunk to finish merges them all (in place)
     w = _case(8, h_kv=2, seed=16, groups=((4, 5, 20, 70), (9, 3, 40, 90)), singles=((30, 200),))
