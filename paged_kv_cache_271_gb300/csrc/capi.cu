@@ -100,7 +100,8 @@ struct MapEntry {
   long long rows;
   int head_dim;
   int dtype;
-  int rank;
+  int want;  // the rank asked for
+  int rank;  // the rank encoded
   CUtensorMap map;
 };
 std::mutex g_map_mu;
@@ -113,18 +114,20 @@ EncodeTiledFn g_encode = nullptr;
 // [2 halves][rows][64 elements] (halves 128 bytes apart, rows 256 bytes apart), so that one box
 // of 2 x 16 x 64 moves a whole (page, KV head) tile into shared memory as two 128-byte-swizzled
 // blocks of 16 rows, the first half of every row before the second (the layout the kernels
-// read); *rank receives 2 or 3.
-int pool_tensor_map(const void* base, const pkv_cache_desc* d, CUtensorMap* out, int* rank) {
+// read); *rank receives 2 or 3. force_2d asks for the 2-D view of a bf16 pool too (two boxes
+// of 16 rows x 64 elements per tile).
+int pool_tensor_map(const void* base, const pkv_cache_desc* d, CUtensorMap* out, int* rank,
+                    bool force_2d = false) {
   int dev = 0;
   cudaError_t ce = cudaGetDevice(&dev);
   if (ce != cudaSuccess) return set_error(PKV_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
   const long long rows = (long long)d->num_pages * d->num_kv_heads * d->page_size;
   const int eb = d->cache_dtype == PKV_BF16 ? 2 : 1;
-  const int want_rank = d->head_dim * eb == 256 ? 3 : 2;
+  const int want_rank = d->head_dim * eb == 256 && !force_2d ? 3 : 2;
   std::lock_guard<std::mutex> lk(g_map_mu);
   for (auto& e : g_maps)
     if (e.dev == dev && e.base == base && e.rows == rows && e.head_dim == d->head_dim &&
-        e.dtype == d->cache_dtype) {
+        e.dtype == d->cache_dtype && e.want == want_rank) {
       *out = e.map;
       *rank = e.rank;
       return PKV_OK;
@@ -144,6 +147,7 @@ int pool_tensor_map(const void* base, const pkv_cache_desc* d, CUtensorMap* out,
   e.rows = rows;
   e.head_dim = d->head_dim;
   e.dtype = d->cache_dtype;
+  e.want = want_rank;
   const CUtensorMapDataType dt =
       eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   CUresult r;
@@ -463,8 +467,14 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (cascade) {
+    CUtensorMap tk2;
+    if (prefix_on_tcgen05()) {  // its K operand needs 2-D boxes (see cascade_prefix_tc.cu)
+      int r2 = 0;
+      st = pool_tensor_map(k_cache, desc, &tk2, &r2, true);
+      if (st != PKV_OK) return st;
+    }
     e = traced("cascade_prefix", s, [&] {
-      return prefix_on_tcgen05() ? launch_cascade_prefix_tc(a, ca, G, &tk, &tv, s)
+      return prefix_on_tcgen05() ? launch_cascade_prefix_tc(a, ca, G, &tk2, &tv, s)
                                  : launch_cascade_prefix(a, ca, G, &tk, &tv, s);
     });
     st = cuda_status(e, "cascade_prefix launch");

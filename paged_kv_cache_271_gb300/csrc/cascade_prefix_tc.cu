@@ -9,10 +9,10 @@
 //  * a copy warp (lane 0) streams 64-token tiles (4 pages) of K and V into a 4-stage ring with
 //    2-D TMA copies (128-byte swizzle), refilling a stage as soon as the P V of its tile is
 //    done; an MMA warp (lane 0) issues the MMAs:
-//      S = Q K^T   M = 128 rows, N = 16 tokens (a page), K = 128 dims: 8 MMAs of K = 16 per
-//                  page into its 16 columns of S (TMEM);
+//      S = Q K^T   M = 128 rows, N = 64 tokens, K = 128 dims  (8 MMAs of K = 16), S in TMEM;
 //      O += P V    M = 128 rows, N = 128 dims, K = 16 tokens (a page): 4 MMAs, O in TMEM;
-//    each page of a stage is one 4 KB block (its 16 rows' first 64 dims, then the last 64);
+//    K arrives as two swizzled [64 rows][64 dims] blocks (2-D boxes, two per page), V as one
+//    4 KB block per page (a 3-D box);
 //    Q, K and P are K-major operands and V an MN-major one, all in the canonical 128-byte
 //    swizzled layout that the TMA copies (and the threads' swizzled stores) produce;
 //  * four softmax warps, one per TMEM lane quarter, so thread r owns row r: it zeroes its row
@@ -66,7 +66,7 @@ constexpr uint32_t tc_idesc(int M, int N, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-constexpr uint32_t kIdescS = tc_idesc(kTcRows, kPageSize, false);  // one page of S
+constexpr uint32_t kIdescS = tc_idesc(kTcRows, kTcTok, false);
 constexpr uint32_t kIdescPV = tc_idesc(kTcRows, 128, true);
 
 // Shared-memory matrix descriptor, 128-byte swizzle: start address, leading-dimension byte
@@ -124,7 +124,7 @@ __device__ __forceinline__ uint32_t sw128(int r, int ch) {
 
 template <int G>
 __global__ void __launch_bounds__(kTcThreads, 1) cascade_prefix_tc_kernel(
-    const DecodeArgs a, const CascadeArgs ca, const __grid_constant__ CUtensorMap tm_k,
+    const DecodeArgs a, const CascadeArgs ca, const __grid_constant__ CUtensorMap tm_k2,
     const __grid_constant__ CUtensorMap tm_v) {
   constexpr int D = 128;
   const int c = blockIdx.x, rt = blockIdx.y;
@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) cascade_prefix_tc_kernel(
     mbar_init(q_ready, kTcRows);
     mbar_init(mma_idle, 1);
     mbar_fence_init();
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k2)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
   }
   const int32_t* btrow = a.block_tables + (size_t)b_first * a.max_pages;
@@ -251,8 +251,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) cascade_prefix_tc_kernel(
     page_mask[st] = mask;
     mbar_arrive_expect_tx(&full[st], kTcStageBytes);  // releases page_mask
     const uint32_t dst = stage_u + st * kTcStageBytes;
-    for (int p = 0; p < kTcPages; ++p) {  // page p: 4 KB at p * 4096 (two 2 KB halves)
-      tma_tile<2, 64>(dst + p * 4096, &tm_k, a.tma_rank, rows[p], &full[st], pol);
+    for (int p = 0; p < kTcPages; ++p) {
+      // K: the tile's 64 rows as two swizzled blocks of [64 rows][64 dims] (page p's rows at
+      // p * 2048 in each), the layout of one N = 64 operand
+      for (int bx = 0; bx < 2; ++bx)
+        tma_load_2d(dst + bx * (kTcKV / 2) + p * 2048, &tm_k2, bx * 64, rows[p], &full[st], pol);
+      // V: page p as one 4 KB block (two [16 rows][64 dims] halves), one K = 16 step of P V
       tma_tile<2, 64>(dst + kTcKV + p * 4096, &tm_v, a.tma_rank, rows[p], &full[st], pol);
     }
   };
@@ -306,14 +310,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) cascade_prefix_tc_kernel(
         const uint32_t kb = stage_u + st * kTcStageBytes;
         const uint32_t s_tmem = tmem + 128 + 64 * (t % kTcSBufs);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t qd = tc_desc(q_u + (kk >> 2) * (kTcQBytes / 2) + (kk & 3) * 32, 16, 1024);
-#pragma unroll
-          for (int p = 0; p < kTcPages; ++p)  // the page's 16 tokens are S columns 16p ..
-            tc_mma(s_tmem + 16 * p, qd,
-                   tc_desc(kb + p * 4096 + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024), kIdescS,
-                   kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma(s_tmem, tc_desc(q_u + (kk >> 2) * (kTcQBytes / 2) + (kk & 3) * 32, 16, 1024),
+                 tc_desc(kb + (kk >> 2) * (kTcKV / 2) + (kk & 3) * 32, 16, 1024), kIdescS,
+                 kk > 0 ? 1u : 0u);
         tc_commit(&s_done[t % kTcSBufs]);
         return true;
       };
