@@ -121,29 +121,73 @@ namespace pkv {
 // request b (KV head j) writes this step's K and V rows there -- into the pools and into its
 // shared-memory copy of the page -- before using the page. Same bytes as kv_append: a copy
 // for bf16/fp32 caches, cvt.rn.satfinite.e4m3(fp32(x / s)) for FP8, the clamped nearest-even
-// integer of fp32(x / s) for INT8. off(r, ch) is the byte
-// offset of 16-byte chunk ch of row r in a shared-memory tile.
-template <typename KV, int D, typename OffFn>
-__device__ __forceinline__ void fused_append_row(const DecodeArgs& a, int b, int j, int pid,
-                                                 int r, uint8_t* k_tile, uint8_t* v_tile,
-                                                 int lane, OffFn off) {
-  constexpr int NCH = D * KV::bytes / 16;  // 16-byte chunks per row
-  const size_t row_byte = ((((size_t)pid * a.h_kv + j) * kPageSize + r) * D) * KV::bytes;
+// integer of fp32(x / s) for INT8.
+//
+// The appending warp prefetches its share of the new rows into L1 as soon as the kernel starts
+// (append_prefetch), so that the reads at the page hit.
+template <typename KV, int D>
+struct AppendRow {
+  static constexpr int NCH = D * KV::bytes / 16;  // 16-byte chunks per output row
+  static constexpr int PER = (2 * NCH + 31) / 32;  // chunks per lane
+  uint4 raw[PER][4];  // the chunk's inputs: up to 16 fp32 values
+};
+
+template <typename KV, int D>
+__device__ __forceinline__ void append_prefetch(const DecodeArgs& a, int b, int j, int lane) {
+  const int in_bytes = a.new_dtype == PKV_F32 ? 4 : 2;
+  const int row = D * in_bytes;  // bytes of one new row (K or V)
+  const size_t off = ((size_t)b * a.h_kv + j) * row;
+  for (int e = lane; e < 2 * row / 128; e += 32) {
+    const char* base = static_cast<const char*>(e < row / 128 ? a.k_new : a.v_new);
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(base + off + 128 * (e % (row / 128))));
+  }
+}
+
+template <typename KV, int D>
+__device__ __forceinline__ void append_load(const DecodeArgs& a, int b, int j, int lane,
+                                            AppendRow<KV, D>& ar) {
+  constexpr int NCH = AppendRow<KV, D>::NCH;
   const size_t src_elem = ((size_t)b * a.h_kv + j) * D;
-  for (int e = lane; e < 2 * NCH; e += 32) {
+#pragma unroll
+  for (int k = 0; k < AppendRow<KV, D>::PER; ++k) {
+    const int e = lane + 32 * k;
+    if (e >= 2 * NCH) continue;
     const bool isv = e >= NCH;
     const int ch = isv ? e - NCH : e;
     const void* src = isv ? a.v_new : a.k_new;
+    if constexpr (KV::bytes == 1) {
+      const int n16 = a.new_dtype == PKV_BF16 ? 2 : 4;  // 16 inputs in 2 or 4 vectors
+      const uint4* p = reinterpret_cast<const uint4*>(
+          static_cast<const uint8_t*>(src) + (src_elem + 16 * ch) * (n16 == 2 ? 2 : 4));
+#pragma unroll
+      for (int h = 0; h < 4; ++h) ar.raw[k][h] = h < n16 ? p[h] : make_uint4(0, 0, 0, 0);
+    } else {
+      ar.raw[k][0] = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(src) +
+                                                      src_elem * KV::bytes + 16 * ch);
+    }
+  }
+}
+
+// off(r, ch) is the byte offset of 16-byte chunk ch of row r in a shared-memory tile.
+template <typename KV, int D, typename OffFn>
+__device__ __forceinline__ void append_store(const DecodeArgs& a, int j, int pid, int r,
+                                             uint8_t* k_tile, uint8_t* v_tile, int lane,
+                                             OffFn off, const AppendRow<KV, D>& ar) {
+  constexpr int NCH = AppendRow<KV, D>::NCH;
+  const size_t row_byte = ((((size_t)pid * a.h_kv + j) * kPageSize + r) * D) * KV::bytes;
+#pragma unroll
+  for (int k = 0; k < AppendRow<KV, D>::PER; ++k) {
+    const int e = lane + 32 * k;
+    if (e >= 2 * NCH) continue;
+    const bool isv = e >= NCH;
+    const int ch = isv ? e - NCH : e;
     uint4 val;
     if constexpr (KV::bytes == 1) {
       float x[16];
       if (a.new_dtype == PKV_BF16) {
-        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src) +
-                                                        src_elem + 16 * ch);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const uint4 u = p[h];
-          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+          const uint32_t w[4] = {ar.raw[k][h].x, ar.raw[k][h].y, ar.raw[k][h].z, ar.raw[k][h].w};
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             x[8 * h + 2 * t] = bf16lo(w[t]);
@@ -151,15 +195,12 @@ __device__ __forceinline__ void fused_append_row(const DecodeArgs& a, int b, int
           }
         }
       } else {
-        const float4* p =
-            reinterpret_cast<const float4*>(static_cast<const float*>(src) + src_elem + 16 * ch);
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          const float4 f = p[h];
-          x[4 * h] = f.x;
-          x[4 * h + 1] = f.y;
-          x[4 * h + 2] = f.z;
-          x[4 * h + 3] = f.w;
+          x[4 * h] = __uint_as_float(ar.raw[k][h].x);
+          x[4 * h + 1] = __uint_as_float(ar.raw[k][h].y);
+          x[4 * h + 2] = __uint_as_float(ar.raw[k][h].z);
+          x[4 * h + 3] = __uint_as_float(ar.raw[k][h].w);
         }
       }
       const float s = isv ? a.v_scales[j] : a.k_scales[j];
@@ -186,12 +227,38 @@ __device__ __forceinline__ void fused_append_row(const DecodeArgs& a, int b, int
       }
       val = make_uint4(w[0], w[1], w[2], w[3]);
     } else {
-      val = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(src) +
-                                            src_elem * KV::bytes + 16 * ch);
+      val = ar.raw[k][0];
     }
     *reinterpret_cast<uint4*>((isv ? v_tile : k_tile) + off(r, ch)) = val;
     uint8_t* pool = static_cast<uint8_t*>(const_cast<void*>(isv ? a.v_cache : a.k_cache));
     *reinterpret_cast<uint4*>(pool + row_byte + 16 * ch) = val;
+  }
+}
+
+// Both steps at once (for callers that do not read ahead).
+template <typename KV, int D, typename OffFn>
+__device__ __forceinline__ void fused_append_row(const DecodeArgs& a, int b, int j, int pid,
+                                                 int r, uint8_t* k_tile, uint8_t* v_tile,
+                                                 int lane, OffFn off) {
+  AppendRow<KV, D> ar;
+  append_load<KV, D>(a, b, j, lane, ar);
+  append_store<KV, D>(a, j, pid, r, k_tile, v_tile, lane, off, ar);
+}
+
+// The partials of a cascade member's shared prefix that the epilogue will fold in: prefetched
+// into L1 when the CTA starts, one 128-byte line per thread.
+template <int D, int G, int NTHR>
+__device__ __forceinline__ void prefetch_prefix_partials(const DecodeArgs& a, int b, int j,
+                                                         int slot0) {
+  const int lines = slot0 * D * 4 / 128 + 2;  // weighted values, then the (max, sum) pairs
+  for (int e = threadIdx.x; e < G * lines; e += NTHR) {
+    const int g = e / lines, k = e % lines;
+    const size_t bh = (size_t)b * a.h_q + j * G + g;
+    const char* p =
+        k < lines - 2 ? reinterpret_cast<const char*>(a.ws_acc + bh * a.n_chunk_slots * D) + 128 * k
+                      : reinterpret_cast<const char*>(a.ws_ml + bh * a.n_chunk_slots * 2) +
+                            (k == lines - 1 ? 8 * slot0 - 4 : 0);
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
   }
 }
 

@@ -214,6 +214,14 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
   const int per_chunk = n_chunks > 0 ? (pages_seq + n_chunks - 1) / n_chunks : 0;
   const int page0 = c * per_chunk;
   const int n_pages = max(0, min(per_chunk, pages_seq - page0));
+  // the warp that will reach the page of position ctx-1 prefetches this step's rows now
+  const int append_warp =
+      a.k_new != nullptr && !cut && n_pages > 0 && page0 + n_pages == pages_seq
+          ? (n_pages - 1) % PKV_MMA_WARPS
+          : -1;
+  if (warp == append_warp) append_prefetch<KV, D>(a, b, j, lane);
+  if (plan.slot0 > 0 && n_chunks <= 1)
+    prefetch_prefix_partials<D, G, 32 * PKV_MMA_WARPS>(a, b, j, plan.slot0);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -355,7 +363,7 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
       const int nvalid = min(kPageSize, ctx - lp * kPageSize);  // rows before the context end
       const uint32_t kt = ring_u32 + stg * S::STAGE_BYTES;
       const uint32_t vt = kt + S::TILE_BYTES;
-      if (a.k_new != nullptr && page0 + i == pages_seq - 1 && !cut) {
+      if (warp == append_warp && i == n_pages - 1) {
         uint8_t* ktp = ring + stg * S::STAGE_BYTES;
         fused_append_row<KV, D>(a, b, j, btrow[lp], nvalid - 1, ktp, ktp + S::TILE_BYTES, lane,
                                 [](int r, int ch) { return (int)swz(r, ch); });
