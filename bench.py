@@ -594,36 +594,33 @@ class L2Flush:
 
 
 def run_e2e(sc, args, dev, stream, flush, n_sets=1):
-    """Same step through the public API from pinned host buffers: per step the host->device
-    copies of the step's inputs (queries, new K/V rows, page tables, context lengths) and the
-    device->host read of the outputs sit inside the timed region."""
+    """Same step through the public API from pinned host buffers (pkv.HostStep): per step one
+    host->device copy of the step's inputs (queries, new K/V rows, page tables, context
+    lengths; for the cascade also this step's groups, found on the host from the tables) and
+    the device->host copy of the outputs sit inside the timed region, and the host waits for
+    the outputs before the next step."""
     import torch
     import paged_kv_cache_271_gb300 as pkv
-    host = {
-        "q": sc.q.cpu().pin_memory(), "k_new": sc.k_new.cpu().pin_memory(),
-        "v_new": sc.v_new.cpu().pin_memory(), "bt": sc.bt.cpu().pin_memory(),
-        "cl": sc.cl.cpu().pin_memory(),
-    }
-    dev_t = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
-    out_host = torch.empty(sc.out.shape, dtype=sc.out.dtype).pin_memory()
-    h2d = int(sum(v.numel() * v.element_size() for v in host.values()))
-    d2h = int(out_host.numel() * out_host.element_size())
-
-    bt_np, cl_np = host["bt"].numpy(), host["cl"].numpy()
+    hs = pkv.HostStep(sc.batch, sc.h_q, sc.h_kv, sc.d, sc.bt.shape[1], q_dtype=sc.q.dtype,
+                      new_dtype=sc.k_new.dtype, device=dev)
+    hs.q_host.copy_(sc.q.cpu())
+    hs.k_new_host.copy_(sc.k_new.cpu())
+    hs.v_new_host.copy_(sc.v_new.cpu())
+    hs.block_tables_host.copy_(sc.bt.cpu())
+    hs.context_lens_host.copy_(sc.cl.cpu())
+    ks, vs = sc.scales if sc.scales else (None, None)
+    bt_np, cl_np = hs.block_tables_host.numpy(), hs.context_lens_host.numpy()
     groups_h2d = [0]
     g_stage = torch.empty(3 * sc.batch + 2, dtype=torch.int32).pin_memory()
     g_buf = torch.empty(3 * sc.batch + 2, dtype=torch.int32, device=dev)
 
     def one(i):
-        for k in host:
-            dev_t[k].copy_(host[k], non_blocking=True)
         groups = None
         if sc.groups is not None:  # this step's groups from its host tables, one H2D copy
             groups = pkv.cascade_groups(bt_np, cl_np).to(dev, buffer=g_buf, staging=g_stage)
             groups_h2d[0] = groups.nbytes
-        sc.step_call(dev_t["q"], dev_t["k_new"], dev_t["v_new"], dev_t["bt"], dev_t["cl"],
-                     groups=groups, pool=i % n_sets)
-        out_host.copy_(sc.out, non_blocking=True)
+        k, v = sc.pools[i % n_sets] if hasattr(sc, "pools") else (sc.k, sc.v)
+        hs.step(k, v, sc.scale, k_scales=ks, v_scales=vs, workspace=sc.workspace, groups=groups)
 
     for i in range(max(3, args.warmup)):
         flush.zero_()
@@ -642,7 +639,7 @@ def run_e2e(sc, args, dev, stream, flush, n_sets=1):
         ends[i].synchronize()  # the result is on the host before the next step starts
     barrier()
     ms = float(np.mean([s.elapsed_time(e) for s, e in zip(starts, ends)]))
-    return {"ms_per_step": ms, "h2d": h2d + groups_h2d[0], "d2h": d2h}
+    return {"ms_per_step": ms, "h2d": hs.h2d_bytes + groups_h2d[0], "d2h": hs.d2h_bytes}
 
 
 # ---- reference arm: the oracle as it stands --------------------------------------------------

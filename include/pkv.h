@@ -323,6 +323,32 @@ int32_t pkv_num_free(const pkv_allocator* a);
 /* Reference count of a page, or -1 for an id out of range. */
 int32_t pkv_refcount(const pkv_allocator* a, int32_t id);
 
+/* ---- decode step from host memory ---------------------------------------------------------- */
+
+/*
+ * Layout of the packed step inputs (host): q [batch][num_q_heads][head_dim] (dtype_q), k_new and
+ * v_new [batch][num_kv_heads][head_dim] (dtype_new), block_tables int32 [batch][max_pages],
+ * context_lens int32 [batch], each starting at offsets[0..4] (256-byte aligned, in this order);
+ * *total_bytes is the size of the block.
+ */
+int pkv_packed_step_layout(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t max_pages_per_seq, int32_t dtype_q,
+                           int32_t dtype_new, size_t* offsets, size_t* total_bytes);
+
+/*
+ * pkv_paged_decode_step with its inputs and output in host memory: one copy of the packed
+ * inputs (host_in, pinned, laid out as pkv_packed_step_layout says) into dev_in (device, the
+ * same size), the fused append + decode on the device copies, and one copy of the output
+ * (out_dev, device) into out_host (pinned), all on `stream` (the caller synchronises before
+ * reading out_host or rewriting host_in).
+ */
+int pkv_paged_decode_step_packed(const void* host_in, void* dev_in, int32_t batch,
+                                 int32_t num_q_heads, int32_t dtype_q, int32_t dtype_new,
+                                 void* k_cache, void* v_cache, const pkv_cache_desc* desc,
+                                 int32_t max_pages_per_seq, float scale, const float* k_scales,
+                                 const float* v_scales, void* out_dev, void* out_host,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- cascade decode (shared prompt prefixes) ---------------------------------------------- */
 
 /*

@@ -24,7 +24,8 @@ __all__ = [
     "decode_workspace_size", "paged_decode_attention", "kv_absmax_scales", "device_error",
     "decode_set_chunk_pages", "decode_chunk_pages", "pages_needed", "slot_mapping",
     "PageAllocator", "PrefixCache", "CascadeGroups", "cascade_groups", "cascade_decode_attention",
-    "cascade_decode_step", "cascade_workspace_size", "trace_enable", "trace_reset", "trace_read",
+    "cascade_decode_step", "cascade_workspace_size", "HostStep", "trace_enable", "trace_reset",
+    "trace_read",
 ]
 
 F32, BF16, FP8_E4M3, INT8 = 0, 1, 2, 3
@@ -109,6 +110,10 @@ def lib():
         "pkv_prefix_insert": (ctypes.c_int, [vp, i64, vp, i64, vp, i32]),
         "pkv_prefix_evict": (ctypes.c_int, [vp, i32, ctypes.POINTER(i32)]),
         "pkv_prefix_size": (i32, [vp]),
+        "pkv_packed_step_layout": (ctypes.c_int, [i32, i32, i32, i32, i32, i32, i32, vp,
+                                                  ctypes.POINTER(sz)]),
+        "pkv_paged_decode_step_packed": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, vp, vp, D, i32,
+                                                        f32, vp, vp, vp, vp, vp, sz, vp]),
         "pkv_cascade_groups": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp,
                                               ctypes.POINTER(i32), ctypes.POINTER(i32),
                                               ctypes.POINTER(i32), ctypes.POINTER(i32)]),
@@ -425,6 +430,75 @@ def cascade_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context
         _dev(context_lens, "context_lens"), float(scale), ctypes.byref(gd), _dev(out, "out"),
         _opt(workspace, "workspace"), wsb, _stream(stream)))
     return out
+
+
+class HostStep:
+    """A decode step whose inputs live in host memory: the step's queries, new K/V rows, page
+    tables and context lengths are packed into one pinned buffer (the ``*_host`` views, filled
+    by the caller, laid out by pkv_packed_step_layout); ``step`` makes one library call
+    (pkv_paged_decode_step_packed) that copies them to the device, runs the fused append +
+    decode and copies the output into ``out_host``. With cascade ``groups`` the copies are made
+    here and the step is cascade_decode_step."""
+
+    _CODE = {torch.float32: F32, torch.bfloat16: BF16}
+
+    def __init__(self, batch, num_q_heads, num_kv_heads, head_dim, max_pages,
+                 q_dtype=torch.bfloat16, new_dtype=torch.bfloat16, device="cuda"):
+        self.batch, self.h_q, self.max_pages = batch, num_q_heads, max_pages
+        self.q_code, self.new_code = self._CODE[q_dtype], self._CODE[new_dtype]
+        offs = (ctypes.c_size_t * 5)()
+        total = ctypes.c_size_t(0)
+        _check(lib().pkv_packed_step_layout(batch, num_q_heads, num_kv_heads, head_dim, max_pages,
+                                            self.q_code, self.new_code, offs, ctypes.byref(total)))
+        self.h2d_bytes = int(total.value)
+        self.host = torch.empty(self.h2d_bytes, dtype=torch.uint8).pin_memory()
+        self.dev = torch.empty(self.h2d_bytes, dtype=torch.uint8, device=device)
+        parts = [("q", (batch, num_q_heads, head_dim), q_dtype),
+                 ("k_new", (batch, num_kv_heads, head_dim), new_dtype),
+                 ("v_new", (batch, num_kv_heads, head_dim), new_dtype),
+                 ("block_tables", (batch, max_pages), torch.int32),
+                 ("context_lens", (batch,), torch.int32)]
+        for (name, shape, dt), o in zip(parts, offs):
+            n = int(np.prod(shape)) * torch.empty(0, dtype=dt).element_size()
+            setattr(self, name + "_host", self.host[o:o + n].view(dt).view(shape))
+            setattr(self, name, self.dev[o:o + n].view(dt).view(shape))
+        self.out = torch.empty((batch, num_q_heads, head_dim), dtype=q_dtype, device=device)
+        self.out_host = torch.empty(self.out.shape, dtype=q_dtype).pin_memory()
+        self.d2h_bytes = self.out.numel() * self.out.element_size()
+        self._key = None
+
+    def step(self, k_cache, v_cache, scale, k_scales=None, v_scales=None, workspace=None,
+             groups=None, stream=None):
+        """One step; returns ``out_host`` (valid once the stream has reached this point)."""
+        if groups is not None:
+            st = torch.cuda.current_stream() if stream is None else stream
+            with torch.cuda.stream(st):
+                self.dev.copy_(self.host, non_blocking=True)
+                cascade_decode_step(self.q, self.k_new, self.v_new, k_cache, v_cache,
+                                    self.block_tables, self.context_lens, scale, groups,
+                                    out=self.out, workspace=workspace, stream=st)
+                self.out_host.copy_(self.out, non_blocking=True)
+            return self.out_host
+        key = (k_cache.data_ptr(), v_cache.data_ptr(), float(scale),
+               None if k_scales is None else k_scales.data_ptr(),
+               None if workspace is None else workspace.data_ptr(), _stream(stream).value)
+        if key != self._key:  # the call's arguments, built once per pool / workspace / stream
+            if workspace is None:
+                need = decode_workspace_size(self.batch, self.h_q, k_cache.shape[1],
+                                             k_cache.shape[3], self.max_pages)
+                workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=self.dev.device)
+            self._ws = workspace
+            self._desc = cache_desc(k_cache)
+            self._args = (ctypes.c_void_p(self.host.data_ptr()), ctypes.c_void_p(self.dev.data_ptr()),
+                          self.batch, self.h_q, self.q_code, self.new_code, _dev(k_cache, "k_cache"),
+                          _dev(v_cache, "v_cache"), ctypes.byref(self._desc), self.max_pages,
+                          float(scale), _opt(k_scales, "k_scales"), _opt(v_scales, "v_scales"),
+                          ctypes.c_void_p(self.out.data_ptr()),
+                          ctypes.c_void_p(self.out_host.data_ptr()), _opt(workspace, "workspace"),
+                          workspace.numel() * workspace.element_size(), _stream(stream))
+            self._key = key
+        _check(lib().pkv_paged_decode_step_packed(*self._args))
+        return self.out_host
 
 
 def paged_decode_attention_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale,

@@ -553,6 +553,60 @@ int pkv_paged_decode_step_window(const void* q, int32_t dtype_q, int32_t batch,
 
 
 
+int pkv_packed_step_layout(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t max_pages_per_seq, int32_t dtype_q,
+                           int32_t dtype_new, size_t* offsets, size_t* total_bytes) {
+  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      max_pages_per_seq <= 0 || !offsets || !total_bytes)
+    return set_error(PKV_EINVAL, "pkv_packed_step_layout: bad argument");
+  auto esize = [](int dt) { return dt == PKV_F32 ? 4 : dt == PKV_BF16 ? 2 : 0; };
+  if (!esize(dtype_q) || !esize(dtype_new))
+    return set_error(PKV_EDTYPE, "pkv_packed_step_layout: q and new rows are F32 or BF16");
+  const size_t sz[5] = {(size_t)batch * num_q_heads * head_dim * esize(dtype_q),
+                        (size_t)batch * num_kv_heads * head_dim * esize(dtype_new),
+                        (size_t)batch * num_kv_heads * head_dim * esize(dtype_new),
+                        (size_t)batch * max_pages_per_seq * 4, (size_t)batch * 4};
+  size_t off = 0;
+  for (int i = 0; i < 5; ++i) {
+    offsets[i] = off;
+    off += align256(sz[i]);
+  }
+  *total_bytes = off;
+  return PKV_OK;
+}
+
+int pkv_paged_decode_step_packed(const void* host_in, void* dev_in, int32_t batch,
+                                 int32_t num_q_heads, int32_t dtype_q, int32_t dtype_new,
+                                 void* k_cache, void* v_cache, const pkv_cache_desc* desc,
+                                 int32_t max_pages_per_seq, float scale, const float* k_scales,
+                                 const float* v_scales, void* out_dev, void* out_host,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  const char* who = "pkv_paged_decode_step_packed";
+  int st = check_desc(desc, who);
+  if (st != PKV_OK) return st;
+  if (!host_in || !dev_in || !out_dev || !out_host)
+    return set_error(PKV_EINVAL, "%s: null pointer", who);
+  size_t off[5], total = 0;
+  st = pkv_packed_step_layout(batch, num_q_heads, desc->num_kv_heads, desc->head_dim,
+                              max_pages_per_seq, dtype_q, dtype_new, off, &total);
+  if (st != PKV_OK) return st;
+  if (batch == 0) return PKV_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(dev_in, host_in, total, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_status(e, "packed step inputs copy");
+  char* d = static_cast<char*>(dev_in);
+  st = decode_impl(who, d + off[0], dtype_q, batch, num_q_heads, k_cache, v_cache, desc,
+                   reinterpret_cast<const int32_t*>(d + off[3]), max_pages_per_seq,
+                   reinterpret_cast<const int32_t*>(d + off[4]), scale, k_scales, v_scales,
+                   out_dev, workspace, workspace_bytes, d + off[1], d + off[2], dtype_new, 0, 0,
+                   nullptr, stream);
+  if (st != PKV_OK) return st;
+  const size_t out_bytes =
+      (size_t)batch * num_q_heads * desc->head_dim * (dtype_q == PKV_F32 ? 4 : 2);
+  e = cudaMemcpyAsync(out_host, out_dev, out_bytes, cudaMemcpyDeviceToHost, s);
+  return cuda_status(e, "packed step output copy");
+}
+
 int pkv_cascade_decode_attention(const void* q, int32_t dtype_q, int32_t batch,
                                  int32_t num_q_heads, const void* k_cache, const void* v_cache,
                                  const pkv_cache_desc* desc, const int32_t* block_tables,

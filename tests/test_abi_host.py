@@ -398,3 +398,19 @@ def test_cascade_argument_errors_are_caught_on_the_host():
     none = pkv.CascadeGroups(np.full(2, -1, np.int32), np.zeros(0, np.int32), np.zeros(1, np.int32),
                              np.zeros(0, np.int32), 0, 0)
     assert pkv.cascade_workspace_size(2, 8, 4, 128, 600, none) == plain
+
+
+def test_packed_step_layout():
+    L = pkv.lib()
+    offs = (ctypes.c_size_t * 5)()
+    total = ctypes.c_size_t(0)
+    assert L.pkv_packed_step_layout(64, 32, 8, 128, 256, pkv.BF16, pkv.BF16, offs,
+                                    ctypes.byref(total)) == 0
+    sizes = [64 * 32 * 128 * 2, 64 * 8 * 128 * 2, 64 * 8 * 128 * 2, 64 * 256 * 4, 64 * 4]
+    expect, o = [], 0
+    for n in sizes:
+        expect.append(o)
+        o += (n + 255) // 256 * 256
+    assert list(offs) == expect and total.value == o
+    assert L.pkv_packed_step_layout(1, 4, 2, 64, 3, pkv.FP8_E4M3, pkv.BF16, offs,
+                                    ctypes.byref(total)) == -3  # q must be F32 or BF16

@@ -320,3 +320,28 @@ def test_bad_slot_sets_error_word():
     pkv.kv_append(kn, kn, slots, kc, vc)
     assert pkv.device_error() & pkv.DEVERR_BAD_SLOT
     assert float(kc[0, 0, 0, 0]) == 1.0 and float(kc[0, 0, 5, 0]) == 1.0
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_host_step_equals_device_step(kv):
+    # one packed host->device copy, the fused step, one device->host copy: same output and
+    # pool bytes as the fused step on device-resident inputs
+    w = workloads.custom("hoststep", 7300, 5, 8, 2, 128, kv, "bf16", [40, 3, 200, 17, 64])
+    a = Scenario(w)
+    out_a = a.fused_step().clone()
+    b = Scenario(w)
+    hs = pkv.HostStep(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                      b.block_tables.shape[1], q_dtype=b.q.dtype, new_dtype=b.k_new.dtype)
+    hs.q_host.copy_(b.q.cpu())
+    hs.k_new_host.copy_(b.k_new.cpu())
+    hs.v_new_host.copy_(b.v_new.cpu())
+    hs.block_tables_host.copy_(b.block_tables.cpu())
+    hs.context_lens_host.copy_(b.context_lens.cpu())
+    ks, vs = b.scales if b.scales else (None, None)
+    out_b = hs.step(b.cache.k, b.cache.v, w.scale, k_scales=ks, v_scales=vs,
+                    workspace=b.workspace)
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    assert torch.equal(out_a.cpu(), out_b)
+    assert torch.equal(a.cache.k.view(torch.uint8), b.cache.k.view(torch.uint8))
+    assert hs.h2d_bytes >= (b.q.numel() + 2 * b.k_new.numel()) * 2
