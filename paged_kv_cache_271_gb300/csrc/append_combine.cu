@@ -191,17 +191,19 @@ __global__ void kv_scale_finalize_kernel(float* scales, int h_kv, float code_max
 // out = sum_c w_c acc_c / sum_c w_c l_c. One CTA of 4 warps per (h, b): the threads find M
 // together; warp w then accumulates chunks w, w+4, w+8, ... with vector loads (lane = DL dims)
 // and the warps' sums are added in warp order, so the result depends only on the number of
-// chunks. Launched as a programmatic dependent of the decode kernel: it is scheduled while the
-// decode drains and waits for the decode's results before reading them.
+// chunks. Launched as a programmatic dependent of the decode kernel, whose CTAs allow it to be
+// scheduled as they start: its CTAs are placed while the decode's last CTAs run and wait for
+// the decode's results before reading them.
 template <typename TQ, int D>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a) {
   constexpr int DL = D / 32;
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int h = blockIdx.x, b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the chunk count depends on inputs only: known before the decode's results are
   const int ctx = min(max(0, a.context_lens[b]), a.max_pages * kPageSize);
   const int n_chunks = seq_plan(a, b, ctx).n_total;  // partials of the request
   if (n_chunks <= 1) return;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid is done, its writes seen
   const size_t bh = (size_t)b * a.h_q + h;
   const float* ml = a.ws_ml + bh * a.n_chunk_slots * 2;
   const float* acc = a.ws_acc + bh * a.n_chunk_slots * D;

@@ -81,17 +81,18 @@ __device__ __forceinline__ void decode_epilogue(const DecodeArgs& a, int b, int 
   }
   if (direct || !a.merge_in_place) return;
 
-  // Publish this chunk's partial, then count it; the CTA that brings the count to n_chunks
-  // sees every other chunk's partial (each was fenced before its count).
-  __threadfence();
+  // Publish this chunk's partial, then count it: after the barrier one thread's fence orders
+  // the whole CTA's partial before the count (fences are cumulative), and the CTA that brings
+  // the count to n_chunks fences again before reading the other chunks' partials from L2.
   __syncthreads();
   if (threadIdx.x == 0) {
+    __threadfence();
     const int prev = atomicAdd(a.counters + (size_t)b * a.h_kv + j, 1);
     s_last = (prev == n_chunks - 1);
+    if (s_last) __threadfence();
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   const int n_total = slot0 + n_chunks;
   for (int e = threadIdx.x; e < G * D; e += NTHR) {
     const int g = e / D, i = e % D;

@@ -210,6 +210,9 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
   const SeqPages sp = plan.sp;
   const int pages_seq = sp.n;  // the pages read here, split into n_chunks near-equal chunks
   const int n_chunks = plan.n_chunks;
+  // the combine kernel (a programmatic dependent launch) may be scheduled once every CTA of
+  // this grid has started; it waits for this grid's completion before reading its partials
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (c > 0 && c >= n_chunks) return;
   const int per_chunk = n_chunks > 0 ? (pages_seq + n_chunks - 1) / n_chunks : 0;
   const int page0 = c * per_chunk;
