@@ -186,6 +186,27 @@ __device__ __forceinline__ uint32_t widen2(uint32_t two_codes) {
     return e4m3x2_to_f16x2(two_codes);
 }
 
+// Four one-byte codes -> two f16x2 words, exactly: lo = codes 0, 1 and hi = codes 2, 3. E4M3:
+// the word's two 16-bit halves go straight to cvt.rn.f16x2.e4m3x2.
+template <typename KV>
+__device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  if constexpr (KV::code == PKV_INT8) {  // code + 128 under the exponent of 1024, minus 1152
+    const uint32_t x = w ^ 0x80808080u;
+    const __half2 bias = __half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));
+    uint32_t u = __byte_perm(x, 0x6464u, 0x5140u);
+    __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&u), bias);
+    lo = *reinterpret_cast<const uint32_t*>(&h);
+    u = __byte_perm(x, 0x6464u, 0x5342u);
+    h = __hsub2(*reinterpret_cast<const __half2*>(&u), bias);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    asm("{\n.reg .b16 a, b;\nmov.b32 {a, b}, %2;\ncvt.rn.f16x2.e4m3x2 %0, a;\n"
+        "cvt.rn.f16x2.e4m3x2 %1, b;\n}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+  }
+}
+
 template <typename KV, typename TQ, int D, int G>
 __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
     const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
@@ -397,10 +418,9 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
           const uint32_t w8[4] = {r8.x, r8.y, r8.z, r8.w};
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t a0 = widen2<KV>(w0[ks]);
-            const uint32_t a2 = widen2<KV>(w0[ks] >> 16);
-            const uint32_t a1 = widen2<KV>(w8[ks]);
-            const uint32_t a3 = widen2<KV>(w8[ks] >> 16);
+            uint32_t a0, a1, a2, a3;
+            widen4<KV>(w0[ks], a0, a2);
+            widen4<KV>(w8[ks], a1, a3);
             const int kp = 2 * h + (ks >> 1), half = ks & 1;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -515,8 +535,9 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
           const uint32_t w3 = wi == 0 ? vr[3].x : wi == 1 ? vr[3].y : wi == 2 ? vr[3].z : vr[3].w;
           const uint32_t lo = __byte_perm(w0, w1, sel);  // tokens 2tig, 2tig+1
           const uint32_t hi = __byte_perm(w2, w3, sel);  // tokens 2tig+8, 2tig+9
-          const uint32_t a0 = widen2<KV>(lo), a1 = widen2<KV>(lo >> 16);
-          const uint32_t a2 = widen2<KV>(hi), a3 = widen2<KV>(hi >> 16);
+          uint32_t a0, a1, a2, a3;
+          widen4<KV>(lo, a0, a1);
+          widen4<KV>(hi, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
             mma16816<true>(acc[mi][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
