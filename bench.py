@@ -53,7 +53,7 @@ def peaks(kind="hbm_gbs"):
 
 
 WORKLOADS = ("llama3_8b_b64", "llama3_70b_long", "prefix_sharing", "prefix_sharing_cascade",
-             "fp8_cb_b256", "fp8_cb_b64")
+             "fp8_cb_b256", "fp8_cb_b64", "int8_cb_b256", "llama3_8b_window")
 
 
 def workload(name="llama3_8b_b64"):
@@ -61,7 +61,8 @@ def workload(name="llama3_8b_b64"):
     return {"llama3_8b_b64": workloads.llama3_8b_batch64,
             "llama3_70b_long": workloads.llama3_70b_long,
             "prefix_sharing": workloads.prefix_sharing,
-            "prefix_sharing_cascade": workloads.prefix_sharing}[name]()
+            "prefix_sharing_cascade": workloads.prefix_sharing,
+            "llama3_8b_window": workloads.llama3_8b_window}[name]()
 
 
 def config_of(w):
@@ -82,11 +83,12 @@ class StepState:
         import paged_kv_cache_271_gb300 as pkv
         from gpu_harness import ContinuousBatchingRun, Scenario
         self.name = name
-        if name.startswith("fp8_cb"):
+        if name.startswith(("fp8_cb", "int8_cb")):
             import workloads
-            batch = 64 if name == "fp8_cb_b64" else 256
+            batch = 64 if name.endswith("_b64") else 256
+            coded = "int8" if name.startswith("int8") else "fp8_e4m3"
             tr = workloads.fp8_continuous_batching(batch=batch, steps=4)
-            run = ContinuousBatchingRun(tr, device=dev)
+            run = ContinuousBatchingRun(tr, device=dev, cache_dtype=coded)
             run.step()
             self.run = run
             self.q, self.k_new, self.v_new = run.q, run.k_new, run.v_new
@@ -97,9 +99,10 @@ class StepState:
             self.batch, self.h_q, self.h_kv, self.d = tr.batch, tr.num_q_heads, tr.num_kv_heads, 128
             self.kv_bytes, self.in_bytes = 1, 2
             self.ctx_sum = int(self.cl.sum())
-            self.config = {"workload": tr.name + "_state_after_1_step", "batch": tr.batch,
+            wname = tr.name if coded != "int8" else tr.name.replace("fp8", "int8")
+            self.config = {"workload": wname + "_state_after_1_step", "batch": tr.batch,
                            "num_q_heads": tr.num_q_heads, "num_kv_heads": tr.num_kv_heads,
-                           "head_dim": 128, "page_size": 16, "kv_dtype": "fp8_e4m3",
+                           "head_dim": 128, "page_size": 16, "kv_dtype": coded,
                            "context_lens": "U[128,8192] seeded, sum %d" % self.ctx_sum}
             self.cache = run.cache
             self.slots = run.last_slots
@@ -119,6 +122,19 @@ class StepState:
             self.config = config_of(w)
             self.cache = sc.cache
             self.slots = sc.step_slots
+            self.window, self.sink = w.window, w.sink
+            if w.window:
+                # pages wholly outside every request's window go back to the allocator (their
+                # table entries become -1): the step can only read attended pages
+                import oracle
+                for b in sc.rids:
+                    sc.cache.release_outside_window(b, w.window, w.sink)
+                sc.refresh_tables()
+                self.bt = sc.block_tables
+                self.ctx_sum = int(sum(len(oracle.attended_tokens(int(n), w.sink, w.window))
+                                       for n in w.context_lens))  # attended tokens
+                self.config.update({"window": w.window, "sink_tokens": w.sink,
+                                    "attended_tokens": self.ctx_sum})
         self.out = torch.empty_like(self.q)
         self.groups = None
         if name.endswith("_cascade"):
@@ -186,7 +202,7 @@ class StepState:
         cl = self.cl.cpu().numpy()
         pages = set()
         for b in range(self.batch):
-            pages.update(int(p) for p in bt[b, :(int(cl[b]) + 15) // 16])
+            pages.update(int(p) for p in bt[b, :(int(cl[b]) + 15) // 16] if p >= 0)
         tile = 2 * self.h_kv * 16 * self.d * self.kv_bytes
         return len(pages) * tile + 2 * self.batch * self.h_q * self.d * 2
 
@@ -210,7 +226,9 @@ class StepState:
                                            workspace=self.workspace, stream=stream)
         return pkv.paged_decode_step(q, k_new, v_new, k, v, bt, cl, self.scale,
                                      out=self.out, k_scales=ks, v_scales=vs,
-                                     workspace=self.workspace, stream=stream)
+                                     workspace=self.workspace, stream=stream,
+                                     window=getattr(self, "window", 0),
+                                     sink_tokens=getattr(self, "sink", 0))
 
     def fused_step(self, stream=None, pool=0):
         return self.step_call(self.q, self.k_new, self.v_new, self.bt, self.cl, stream=stream,
@@ -554,7 +572,7 @@ def run_ours(args):
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if sc.kv_bytes == 2 else ("fp8_e4m3/f16" if sc.kv_bytes == 1 else "f32"),
+            "dtype": "bf16" if sc.kv_bytes == 2 else (sc.config["kv_dtype"] + "/f16" if sc.kv_bytes == 1 else "f32"),
             "data": "synthetic", "config": dict(sc.config, parallelism="replicas x%d" % ws),
             "decode_tokens_per_s": round(ws * sc.batch / (max_ms * 1e-3), 1),
             "tokens_per_s_32_layer_projection": round(ws * sc.batch / (32 * max_ms * 1e-3), 1),
@@ -620,7 +638,8 @@ def run_e2e(sc, args, dev, stream, flush, n_sets=1):
             groups = pkv.cascade_groups(bt_np, cl_np).to(dev, buffer=g_buf, staging=g_stage)
             groups_h2d[0] = groups.nbytes
         k, v = sc.pools[i % n_sets] if hasattr(sc, "pools") else (sc.k, sc.v)
-        hs.step(k, v, sc.scale, k_scales=ks, v_scales=vs, workspace=sc.workspace, groups=groups)
+        hs.step(k, v, sc.scale, k_scales=ks, v_scales=vs, workspace=sc.workspace, groups=groups,
+                window=getattr(sc, "window", 0), sink_tokens=getattr(sc, "sink", 0))
 
     for i in range(max(3, args.warmup)):
         flush.zero_()

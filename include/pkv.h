@@ -336,18 +336,19 @@ int pkv_packed_step_layout(int32_t batch, int32_t num_q_heads, int32_t num_kv_he
                            int32_t dtype_new, size_t* offsets, size_t* total_bytes);
 
 /*
- * pkv_paged_decode_step with its inputs and output in host memory: one copy of the packed
- * inputs (host_in, pinned, laid out as pkv_packed_step_layout says) into dev_in (device, the
- * same size), the fused append + decode on the device copies, and one copy of the output
- * (out_dev, device) into out_host (pinned), all on `stream` (the caller synchronises before
- * reading out_host or rewriting host_in).
+ * pkv_paged_decode_step_window with its inputs and output in host memory (window = 0, sinks 0:
+ * pkv_paged_decode_step): one copy of the packed inputs (host_in, pinned, laid out as
+ * pkv_packed_step_layout says) into dev_in (device, the same size), the fused append + decode
+ * on the device copies, and one copy of the output (out_dev, device) into out_host (pinned),
+ * all on `stream` (the caller synchronises before reading out_host or rewriting host_in).
  */
 int pkv_paged_decode_step_packed(const void* host_in, void* dev_in, int32_t batch,
                                  int32_t num_q_heads, int32_t dtype_q, int32_t dtype_new,
                                  void* k_cache, void* v_cache, const pkv_cache_desc* desc,
                                  int32_t max_pages_per_seq, float scale, const float* k_scales,
-                                 const float* v_scales, void* out_dev, void* out_host,
-                                 void* workspace, size_t workspace_bytes, void* stream);
+                                 const float* v_scales, int32_t sink_tokens, int32_t window,
+                                 void* out_dev, void* out_host, void* workspace,
+                                 size_t workspace_bytes, void* stream);
 
 /* ---- cascade decode (shared prompt prefixes) ---------------------------------------------- */
 

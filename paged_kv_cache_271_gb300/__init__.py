@@ -113,7 +113,8 @@ def lib():
         "pkv_packed_step_layout": (ctypes.c_int, [i32, i32, i32, i32, i32, i32, i32, vp,
                                                   ctypes.POINTER(sz)]),
         "pkv_paged_decode_step_packed": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, vp, vp, D, i32,
-                                                        f32, vp, vp, vp, vp, vp, sz, vp]),
+                                                        f32, vp, vp, i32, i32, vp, vp, vp, sz,
+                                                        vp]),
         "pkv_cascade_groups": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp,
                                               ctypes.POINTER(i32), ctypes.POINTER(i32),
                                               ctypes.POINTER(i32), ctypes.POINTER(i32)]),
@@ -437,8 +438,8 @@ class HostStep:
     tables and context lengths are packed into one pinned buffer (the ``*_host`` views, filled
     by the caller, laid out by pkv_packed_step_layout); ``step`` makes one library call
     (pkv_paged_decode_step_packed) that copies them to the device, runs the fused append +
-    decode and copies the output into ``out_host``. With cascade ``groups`` the copies are made
-    here and the step is cascade_decode_step."""
+    decode (windowed when ``window`` > 0) and copies the output into ``out_host``. With cascade
+    ``groups`` the copies are made here and the step is cascade_decode_step."""
 
     _CODE = {torch.float32: F32, torch.bfloat16: BF16}
 
@@ -468,7 +469,7 @@ class HostStep:
         self._key = None
 
     def step(self, k_cache, v_cache, scale, k_scales=None, v_scales=None, workspace=None,
-             groups=None, stream=None):
+             groups=None, stream=None, window=0, sink_tokens=0):
         """One step; returns ``out_host`` (valid once the stream has reached this point)."""
         if groups is not None:
             st = torch.cuda.current_stream() if stream is None else stream
@@ -481,7 +482,8 @@ class HostStep:
             return self.out_host
         key = (k_cache.data_ptr(), v_cache.data_ptr(), float(scale),
                None if k_scales is None else k_scales.data_ptr(),
-               None if workspace is None else workspace.data_ptr(), _stream(stream).value)
+               None if workspace is None else workspace.data_ptr(), _stream(stream).value,
+               int(window), int(sink_tokens))
         if key != self._key:  # the call's arguments, built once per pool / workspace / stream
             if workspace is None:
                 need = decode_workspace_size(self.batch, self.h_q, k_cache.shape[1],
@@ -493,7 +495,7 @@ class HostStep:
                           self.batch, self.h_q, self.q_code, self.new_code, _dev(k_cache, "k_cache"),
                           _dev(v_cache, "v_cache"), ctypes.byref(self._desc), self.max_pages,
                           float(scale), _opt(k_scales, "k_scales"), _opt(v_scales, "v_scales"),
-                          ctypes.c_void_p(self.out.data_ptr()),
+                          int(sink_tokens), int(window), ctypes.c_void_p(self.out.data_ptr()),
                           ctypes.c_void_p(self.out_host.data_ptr()), _opt(workspace, "workspace"),
                           workspace.numel() * workspace.element_size(), _stream(stream))
             self._key = key

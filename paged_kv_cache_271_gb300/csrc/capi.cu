@@ -579,8 +579,9 @@ int pkv_paged_decode_step_packed(const void* host_in, void* dev_in, int32_t batc
                                  int32_t num_q_heads, int32_t dtype_q, int32_t dtype_new,
                                  void* k_cache, void* v_cache, const pkv_cache_desc* desc,
                                  int32_t max_pages_per_seq, float scale, const float* k_scales,
-                                 const float* v_scales, void* out_dev, void* out_host,
-                                 void* workspace, size_t workspace_bytes, void* stream) {
+                                 const float* v_scales, int32_t sink_tokens, int32_t window,
+                                 void* out_dev, void* out_host, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
   const char* who = "pkv_paged_decode_step_packed";
   int st = check_desc(desc, who);
   if (st != PKV_OK) return st;
@@ -598,8 +599,8 @@ int pkv_paged_decode_step_packed(const void* host_in, void* dev_in, int32_t batc
   st = decode_impl(who, d + off[0], dtype_q, batch, num_q_heads, k_cache, v_cache, desc,
                    reinterpret_cast<const int32_t*>(d + off[3]), max_pages_per_seq,
                    reinterpret_cast<const int32_t*>(d + off[4]), scale, k_scales, v_scales,
-                   out_dev, workspace, workspace_bytes, d + off[1], d + off[2], dtype_new, 0, 0,
-                   nullptr, stream);
+                   out_dev, workspace, workspace_bytes, d + off[1], d + off[2], dtype_new,
+                   sink_tokens, window, nullptr, stream);
   if (st != PKV_OK) return st;
   const size_t out_bytes =
       (size_t)batch * num_q_heads * desc->head_dim * (dtype_q == PKV_F32 ? 4 : 2);

@@ -153,14 +153,16 @@ def tolerance(w) -> float:
 
 
 class ContinuousBatchingRun:
-    """Drives a ``workloads.ContinuousBatchingTrace`` through the library on an FP8 cache:
-    absmax scales over the initial cache, quantising prefill of every prompt, one appended
-    token per live request per step, finished requests freed and replaced (continuous
-    batching), paged decode every step."""
+    """Drives a ``workloads.ContinuousBatchingTrace`` through the library on an FP8 (or, with
+    cache_dtype="int8", an INT8) cache: absmax scales over the initial cache, quantising
+    prefill of every prompt, one appended token per live request per step, finished requests
+    freed and replaced (continuous batching), paged decode every step."""
 
-    def __init__(self, trace, device="cuda"):
+    def __init__(self, trace, device="cuda", cache_dtype="fp8_e4m3"):
         self.t = trace
         self.device = torch.device(device)
+        self.cache_dtype = cache_dtype
+        i8 = cache_dtype == "int8"
         B = trace.batch
         self.tokens = {}  # rid -> (k, v) bf16 CPU rows
         for b in range(B):
@@ -168,10 +170,11 @@ class ContinuousBatchingRun:
         init = [int(n) for n in trace.initial_lens]
         k0 = torch.cat([self.tokens[b][0][:init[b]] for b in range(B)], 0).to(self.device)
         v0 = torch.cat([self.tokens[b][1][:init[b]] for b in range(B)], 0).to(self.device)
-        self.k_scales = pkv.kv_absmax_scales(k0)
-        self.v_scales = pkv.kv_absmax_scales(v0)
+        self.k_scales = pkv.kv_absmax_scales(k0, int8=i8)
+        self.v_scales = pkv.kv_absmax_scales(v0, int8=i8)
         self.cache = PagedKVCache(trace.num_pages, trace.num_kv_heads, trace.head_dim,
-                                  torch.uint8, self.device, initial_free_order=trace.page_order,
+                                  POOL_DTYPE[cache_dtype], self.device,
+                                  initial_free_order=trace.page_order,
                                   k_scales=self.k_scales, v_scales=self.v_scales)
         fill_junk(self.cache.k, trace.seed + 11)
         fill_junk(self.cache.v, trace.seed + 12)
@@ -242,10 +245,11 @@ class ContinuousBatchingRun:
             j = h // G
             k = self.tokens[rid][0][:T, j].float().numpy()
             v = self.tokens[rid][1][:T, j].float().numpy()
-            kc = oracle.quantize_e4m3(k, k_scales[j])[:, None, :]
-            vc = oracle.quantize_e4m3(v, v_scales[j])[:, None, :]
+            quant = oracle.quantize_int8 if self.cache_dtype == "int8" else oracle.quantize_e4m3
+            kc = quant(k, k_scales[j])[:, None, :]
+            vc = quant(v, v_scales[j])[:, None, :]
             out = oracle.contiguous_decode(oracle.as_raw(q[b:b + 1, h:h + 1], "bf16"), "bf16",
-                                           kc, vc, "fp8_e4m3", [0], [T], t.scale,
+                                           kc, vc, self.cache_dtype, [0], [T], t.scale,
                                            k_scales=k_scales[j:j + 1],
                                            v_scales=v_scales[j:j + 1])
             rows.append(out[0, 0])

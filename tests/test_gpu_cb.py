@@ -1,4 +1,4 @@
-"""FP8 E4M3 cache under continuous batching, against the oracle: per-head absmax scales,
+"""FP8 E4M3 (and INT8) cache under continuous batching, against the oracle: per-head absmax scales,
 quantising appends, requests finishing and being replaced (pages freed and reused through the
 allocator), paged decode each step. Bit-exact scales and appended codes; attention within
 1e-2 of the oracle's attention over its own dequantised codes."""
@@ -28,6 +28,7 @@ def _gpu():
 def _check_appended_codes(run, ks, vs):
     """The codes just written for each request's new token equal the oracle's quantiser."""
     t = run.t
+    quant = oracle.quantize_int8 if run.cache_dtype == "int8" else oracle.quantize_e4m3
     slots = run.last_slots
     kc = run.cache.k.view(-1, t.num_kv_heads, 16, t.head_dim)
     for b in range(0, t.batch, max(1, t.batch // 8)):
@@ -36,15 +37,16 @@ def _check_appended_codes(run, ks, vs):
         s = int(slots[b])
         got = kc[s // 16, :, s % 16, :].cpu().numpy()
         x = run.tokens[rid][0][p].float().numpy()
-        ref = np.stack([oracle.quantize_e4m3(x[j], ks[j]) for j in range(t.num_kv_heads)])
+        ref = np.stack([quant(x[j], ks[j]) for j in range(t.num_kv_heads)])
         np.testing.assert_array_equal(got, ref)
 
 
-def _run(trace, pairs_per_step, full_check):
-    run = ContinuousBatchingRun(trace)
+def _run(trace, pairs_per_step, full_check, cache_dtype="fp8_e4m3"):
+    run = ContinuousBatchingRun(trace, cache_dtype=cache_dtype)
     k0, v0 = run.initial_rows()
-    ks = oracle.absmax_scales_per_head(k0)
-    vs = oracle.absmax_scales_per_head(v0)
+    qmax = 127.0 if cache_dtype == "int8" else 448.0
+    ks = oracle.absmax_scales_per_head(k0, qmax)
+    vs = oracle.absmax_scales_per_head(v0, qmax)
     del k0, v0
     np.testing.assert_array_equal(run.k_scales.cpu().numpy(), ks)
     np.testing.assert_array_equal(run.v_scales.cpu().numpy(), vs)
@@ -81,3 +83,14 @@ def test_fp8_continuous_batching_small_full_check():
 def test_fp8_continuous_batching_full_size_sampled():
     tr = workloads.fp8_continuous_batching()
     assert _run(tr, 6, full_check=False) > 0
+
+
+def test_int8_continuous_batching_small_full_check():
+    tr = workloads.fp8_continuous_batching(batch=16, steps=8, lo=128, hi=512, rep_lo=16,
+                                           rep_hi=400, p_finish=0.3)
+    assert _run(tr, 0, full_check=True, cache_dtype="int8") > 0
+
+
+def test_int8_continuous_batching_full_size_sampled():
+    tr = workloads.fp8_continuous_batching(steps=6)
+    assert _run(tr, 6, full_check=False, cache_dtype="int8") > 0

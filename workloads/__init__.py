@@ -71,6 +71,8 @@ class DecodeInputs:
     prefix_len: int = 0
     prefix_k: torch.Tensor | None = None
     prefix_v: torch.Tensor | None = None
+    window: int = 0  # > 0: the decode attends the last `window` positions ...
+    sink: int = 0  # ... and the first `sink` ones ("Sliding window" section)
 
     def request_tokens(self, b: int):
         """Keys and values of request b in logical order, as [ctx, h_kv, d] CPU tensors."""
@@ -141,6 +143,19 @@ def llama3_70b_long() -> DecodeInputs:
     lens = [131072, 65536, 32768, 8191]
     return _assemble("llama3_70b_long_b4", seed, 4, 64, 8, 128, "bf16", "bf16", lens,
                      _pool_pages(lens, PAGE_SIZE))
+
+
+def llama3_8b_window(batch: int = 64, window: int = 1024, sink: int = 4) -> DecodeInputs:
+    """Llama-3-8B-shaped layer with a sliding window of 1024 positions plus 4 attention sinks
+    ("Sliding window" section: StreamingLLM keeps a few first tokens and the last W), contexts
+    U[2048, 6144], so a request attends about a quarter of its cache."""
+    seed = BASE_SEED + 6
+    g = _gen(seed - 1000)
+    lens = torch.randint(2048, 6145, (batch,), generator=g).numpy()
+    w = _assemble("llama3_8b_window%d_sink%d_b%d" % (window, sink, batch), seed, batch, 32, 8,
+                  128, "bf16", "bf16", lens, _pool_pages(lens, PAGE_SIZE))
+    w.window, w.sink = window, sink
+    return w
 
 
 def prefix_sharing(batch: int = 128, prefix_len: int = 2000) -> DecodeInputs:
