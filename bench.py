@@ -53,7 +53,8 @@ def peaks(kind="hbm_gbs"):
 
 
 WORKLOADS = ("llama3_8b_b64", "llama3_70b_long", "prefix_sharing", "prefix_sharing_cascade",
-             "fp8_cb_b256", "fp8_cb_b64", "int8_cb_b256", "llama3_8b_window")
+             "fp8_cb_b256", "fp8_cb_b64", "int8_cb_b256", "llama3_8b_window",
+             "parallel_sampling_fork")
 
 
 def workload(name="llama3_8b_b64"):
@@ -611,6 +612,146 @@ class L2Flush:
             self.buf.zero_()
 
 
+def run_fork(args):
+    """Copy-on-write fork (parallel sampling): per step, fork each of 16 prompts into 4 samples
+    (reference counts), reserve each sample's first slot -- the shared, partly filled last page
+    of its prompt is copied for every writer (pkv_cow_page on the host, pkv_copy_pages on the
+    device) --, run the fused append + decode over the 64 samples, and free the samples again,
+    so that every step starts from the same state. ``value`` counts the decode's bytes plus the
+    copied pages (read and written)."""
+    import torch
+    import paged_kv_cache_271_gb300 as pkv
+    from paged_kv_cache_271_gb300.cache import PagedKVCache
+    import workloads
+    ws, rank, local = rank_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(ws, "nccl")
+    pkv.lib()
+    ps = workloads.parallel_sampling()
+    w = ps.prompts
+    cache = PagedKVCache(w.num_pages, w.num_kv_heads, w.head_dim, torch.bfloat16, dev,
+                         initial_free_order=w.page_order)
+    P, S = w.batch, ps.samples
+    for p in range(P):
+        cache.add_request(p)
+    slots = cache.reserve(list(range(P)), [int(n) for n in w.context_lens])
+    cache.write(slots, w.k_tokens.to(dev), w.v_tokens.to(dev))
+    q, k_new, v_new = ps.q.to(dev), ps.k_new.to(dev), ps.v_new.to(dev)
+    rids = [1000 + i for i in range(P * S)]
+    out = torch.empty_like(q)
+    maxp = int(max(pkv.pages_needed(int(n) + 1) for n in w.context_lens))
+    need = pkv.decode_workspace_size(P * S, 32, 8, 128, maxp)
+    workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
+    bt_dev = torch.zeros((P * S, maxp), dtype=torch.int32, device=dev)
+    cl_dev = torch.zeros((P * S,), dtype=torch.int32, device=dev)
+    bt_pin = torch.zeros((P * S, maxp), dtype=torch.int32).pin_memory()
+    cl_pin = torch.zeros((P * S,), dtype=torch.int32).pin_memory()
+    out_pin = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+    copies = [0]
+    cp_pin = torch.zeros((2, P * S), dtype=torch.int32).pin_memory()
+    cp_dev = torch.zeros((2, P * S), dtype=torch.int32, device=dev)
+
+    def host_fork():
+        for i, r in enumerate(rids):
+            cache.fork(i // S, r)
+        pairs = []
+        cache.reserve(rids, [1] * len(rids), copies_out=pairs)  # copy-on-write decisions
+        copies[0] = len(pairs)
+        cp_pin[0, :len(pairs)] = torch.tensor([a for a, _ in pairs], dtype=torch.int32)
+        cp_pin[1, :len(pairs)] = torch.tensor([b for _, b in pairs], dtype=torch.int32)
+        bt_pin.copy_(torch.from_numpy(cache.block_table_array(rids, maxp)))
+        cl_pin.copy_(torch.from_numpy(cache.context_lens_array(rids)))
+
+    def device_step():
+        cp_dev.copy_(cp_pin, non_blocking=True)
+        bt_dev.copy_(bt_pin, non_blocking=True)
+        cl_dev.copy_(cl_pin, non_blocking=True)
+        n = copies[0]
+        if n:
+            pkv.copy_pages(cache.k, cache.v, cp_dev[0, :n], cp_dev[1, :n])
+        pkv.paged_decode_step(q, k_new, v_new, cache.k, cache.v, bt_dev, cl_dev, w.scale,
+                              out=out, workspace=workspace)
+
+    def host_free():
+        for r in rids:
+            cache.free_request(r)
+
+    for _ in range(args.warmup):
+        host_fork()
+        device_step()
+        torch.cuda.synchronize()
+        host_free()
+    assert pkv.device_error() == 0
+    n = args.steps
+    dev_ms, host_s, e2e_ms = [], 0.0, []
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    for i in range(n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2 = torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        host_fork()  # host: fork, copy-on-write decisions, tables (timed on the host)
+        th = time.perf_counter() - t0
+        host_s += th
+        e0.record(stream)
+        device_step()
+        e1.record(stream)
+        out_pin.copy_(out, non_blocking=True)
+        e2.record(stream)
+        e2.synchronize()
+        dev_ms.append(e0.elapsed_time(e1))
+        e2e_ms.append(1e3 * th + e0.elapsed_time(e2))  # host bookkeeping + copies + step + D2H
+        host_free()
+    barrier()
+    clk = clocks.stop()
+    assert pkv.device_error() == 0
+    ctx = [int(cache.lens[p]) + 1 for p in range(P) for _ in range(S)]
+    row = 8 * 128 * 2 * 2
+    decode_bytes = sum(ctx) * row + 2 * P * S * 32 * 128 * 2 + 2 * P * S * 8 * 128 * 4
+    copy_bytes = copies[0] * 8 * 16 * 128 * 2 * 2 * 2  # pages x (K and V) x (read and write)
+    ms = max_over_ranks(float(np.mean(dev_ms)), dev)
+    e2e = max_over_ranks(float(np.mean(e2e_ms)), dev)
+    peak, kind = peaks()
+    if rank == 0:
+        value = aggregate(decode_bytes + copy_bytes, ms, ws)
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+            "steps": n, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "prompts": P, "samples_per_prompt": S,
+                       "batch": P * S, "num_q_heads": 32, "num_kv_heads": 8, "head_dim": 128,
+                       "page_size": 16, "kv_dtype": "bf16",
+                       "prompt_lens": "U[1000, 3000], sum %d" % int(np.sum(w.context_lens)),
+                       "step": "device: copy-on-write page copies + fused append + decode "
+                               "(host fork, copy-on-write decisions and tables timed apart, "
+                               "host_fork_us); samples freed after each step",
+                       "l2": "not flushed: the step reads the prompts' pages (%.0f MB) once"
+                             % (sum(int(x) for x in w.context_lens) * row / 1e6),
+                       "parallelism": "replicas x%d" % ws},
+            "copied_pages_per_step": copies[0],
+            "decode_tokens_per_s": round(ws * P * S / (ms * 1e-3), 1),
+            "roofline": {"bound": "hbm", "kernel": "page copies + paged_decode step (device)",
+                         "achieved": round(value / ws, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(value / ws / peak, 4), "peak_kind": kind, "traffic": None,
+                         "algorithmic_bytes_per_launch": decode_bytes + copy_bytes,
+                         "launch_ms": round(ms, 5)},
+            "cpu_baseline": None,
+            "host_fork_us": round(1e6 * host_s / n, 1),
+            "host_fork": "Python cache manager (PagedKVCache) over the C++ allocator, 64 requests",
+            "e2e": {"value": round(aggregate(decode_bytes + copy_bytes, e2e, ws), 1), "unit": "GB/s",
+                    "ms_per_step": round(e2e, 5),
+                    "h2d_bytes_per_step": int(bt_pin.numel() * 4 + cl_pin.numel() * 4),
+                    "d2h_bytes_per_step": int(out.numel() * 2)},
+            "gpu_launches": int(3 * n), "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+
+
 def run_e2e(sc, args, dev, stream, flush, n_sets=1):
     """Same step through the public API from pinned host buffers (pkv.HostStep): per step one
     host->device copy of the step's inputs (queries, new K/V rows, page tables, context
@@ -711,6 +852,8 @@ def main(argv=None):
         raise SystemExit("bench.py: at least 3 warm-up steps")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "parallel_sampling_fork":
+        run_fork(args)
     else:
         run_ours(args)
 

@@ -637,12 +637,14 @@ class PageAllocator:
     def cow_page(self, row: list, position: int, page_size: int = 16):
         """Copy-on-write for a write at ``position`` of a request with pages ``row`` (updated
         in place). Returns (src, dst) to copy, or None when the page is private."""
-        a = np.ascontiguousarray(np.asarray(row, dtype=np.int32))
+        lp = int(position) // int(page_size)
+        if lp >= len(row):
+            return None  # the write starts a page the request does not have yet
+        one = (ctypes.c_int32 * 1)(int(row[lp]))  # only the written page matters
         src, dst = ctypes.c_int32(-1), ctypes.c_int32(-1)
-        _check(lib().pkv_cow_page(self._h, a.ctypes.data if a.size else None, a.size,
-                                  int(position), int(page_size), ctypes.byref(src),
-                                  ctypes.byref(dst)))
-        row[:] = [int(x) for x in a]
+        _check(lib().pkv_cow_page(self._h, one, 1, int(position) % int(page_size),
+                                  int(page_size), ctypes.byref(src), ctypes.byref(dst)))
+        row[lp] = int(one[0])
         return None if src.value < 0 else (int(src.value), int(dst.value))
 
 

@@ -94,9 +94,12 @@ class PagedKVCache:
             self.allocator.decref(released)
         return len(released)
 
-    def reserve(self, rids, counts) -> np.ndarray:
+    def reserve(self, rids, counts, copies_out=None) -> np.ndarray:
         """Grow each request by counts[i] tokens (allocating pages on page boundaries) and
-        return the int64 slots of the new positions, request by request."""
+        return the int64 slots of the new positions, request by request. Shared, partly filled
+        pages about to be written are copied first (copy-on-write): on the device here, or,
+        when ``copies_out`` is a list, appended to it as (source, destination) page pairs for
+        the caller to copy (``copy_pages``) before the writes."""
         rids = list(rids)
         counts = [int(c) for c in counts]
         copies = []
@@ -119,7 +122,9 @@ class PagedKVCache:
             pos[o:o + n] = np.arange(self.lens[rid], self.lens[rid] + n)
             o += n
             self.lens[rid] += n
-        if copies:
+        if copies_out is not None:
+            copies_out.extend(copies)
+        elif copies:
             src = torch.tensor([c[0] for c in copies], dtype=torch.int32, device=self.k.device)
             dst = torch.tensor([c[1] for c in copies], dtype=torch.int32, device=self.k.device)
             copy_pages(self.k, self.v, src, dst)

@@ -89,3 +89,25 @@ def test_window_argument_errors():
         sc.fused_step(window=-1)
     with pytest.raises(pkv.PkvError):
         sc.fused_step(window=0, sink_tokens=4)
+
+
+def test_windowed_host_step_equals_device_step():
+    # the packed host-memory step with a window: one copy in, the windowed fused step, one out
+    w = workloads.custom("hostwin", 7400, 4, 8, 2, 128, "bf16", "bf16", [300, 45, 1000, 17])
+    a = Scenario(w)
+    out_a = a.fused_step(window=64, sink_tokens=4).clone()
+    b = Scenario(w)
+    hs = pkv.HostStep(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                      b.block_tables.shape[1])
+    hs.q_host.copy_(b.q.cpu())
+    hs.k_new_host.copy_(b.k_new.cpu())
+    hs.v_new_host.copy_(b.v_new.cpu())
+    hs.block_tables_host.copy_(b.block_tables.cpu())
+    hs.context_lens_host.copy_(b.context_lens.cpu())
+    out_b = hs.step(b.cache.k, b.cache.v, w.scale, workspace=b.workspace, window=64,
+                    sink_tokens=4)
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    assert torch.equal(out_a.cpu(), out_b)
+    err = float(np.abs(out_b.double().numpy() - oracle_expected(w, sink=4, window=64)).max())
+    assert err <= tolerance(w), err

@@ -158,6 +158,34 @@ def llama3_8b_window(batch: int = 64, window: int = 1024, sink: int = 4) -> Deco
     return w
 
 
+@dataclasses.dataclass
+class ParallelSampling:
+    """Parallel sampling ("KV Cache" glossary: a prompt's blocks shared by the sequences sampled
+    from it): ``prompts`` holds the prompts' tokens (request p = prompt p); each prompt is
+    forked into ``samples`` sequences, sample s of prompt p being row p * samples + s of the
+    first decode step's ``q`` [P*S, h_q, d] and new rows ``k_new``/``v_new`` [P*S, h_kv, d]."""
+
+    prompts: DecodeInputs
+    samples: int
+    q: torch.Tensor
+    k_new: torch.Tensor
+    v_new: torch.Tensor
+
+
+def parallel_sampling(n_prompts: int = 16, samples: int = 4) -> ParallelSampling:
+    """16 Llama-3-8B-shaped prompts of U[1000, 3000] tokens (a partly filled last page each),
+    4 samples each (batch 64)."""
+    seed = BASE_SEED + 7
+    g = _gen(seed - 1000)
+    lens = torch.randint(1000, 3001, (n_prompts,), generator=g).numpy()
+    w = _assemble("parallel_sampling_p%d_s%d" % (n_prompts, samples), seed, n_prompts, 32, 8, 128,
+                  "bf16", "bf16", lens, _pool_pages(lens, PAGE_SIZE) + 2 * n_prompts * samples)
+    n = n_prompts * samples
+    return ParallelSampling(prompts=w, samples=samples, q=_normal((n, 32, 128), "bf16", g),
+                            k_new=_normal((n, 8, 128), "bf16", g),
+                            v_new=_normal((n, 8, 128), "bf16", g))
+
+
 def prefix_sharing(batch: int = 128, prefix_len: int = 2000) -> DecodeInputs:
     """128 requests sharing a 2000-token prompt prefix, then own suffixes of U[5, 200] tokens."""
     seed = BASE_SEED + 4
