@@ -770,8 +770,8 @@ def run_e2e(sc, args, dev, stream, flush, n_sets=1):
     ks, vs = sc.scales if sc.scales else (None, None)
     bt_np, cl_np = hs.block_tables_host.numpy(), hs.context_lens_host.numpy()
     groups_h2d = [0]
-    g_stage = torch.empty(3 * sc.batch + 2, dtype=torch.int32).pin_memory()
-    g_buf = torch.empty(3 * sc.batch + 2, dtype=torch.int32, device=dev)
+    g_stage = torch.empty(4 * sc.batch + 2, dtype=torch.int32).pin_memory()
+    g_buf = torch.empty(4 * sc.batch + 2, dtype=torch.int32, device=dev)
 
     def one(i):
         groups = None

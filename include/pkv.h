@@ -378,6 +378,9 @@ typedef struct {
                                     shared pages (all its pages outside a group); sizes the
                                     split of those pages. 0: the table width. A request with
                                     more pages still gets a correct result, in larger chunks. */
+  const int32_t* own_start;      /* [batch] or NULL: prefix_pages[group_of[b]] (0 outside a
+                                    group), read directly by the decode of the members' own
+                                    pages instead of through group_of (one read fewer) */
 } pkv_cascade_desc;
 
 /*
@@ -386,7 +389,8 @@ typedef struct {
  * min_members (>= 2) requests shares the longest run of leading page ids common to all its
  * members, cut to the full pages before each member's position ctx - 1; fewer than
  * min_prefix_pages (>= 1) shared pages: no group. Outputs (host, caller-sized): group_of
- * [batch], prefix_pages [batch], group_offsets [batch + 1], group_members [batch], and the
+ * [batch], prefix_pages [batch], group_offsets [batch + 1], group_members [batch], own_start
+ * [batch] (may be NULL), and the
  * counts and bounds of a pkv_cascade_desc (*n_groups may be 0; *max_own_pages counts the pages
  * of a context cut to the table width).
  */
@@ -394,7 +398,7 @@ int pkv_cascade_groups(const int32_t* block_tables, const int32_t* context_lens,
                        int32_t max_pages_per_seq, int32_t min_members, int32_t min_prefix_pages,
                        int32_t* group_of, int32_t* prefix_pages, int32_t* group_offsets,
                        int32_t* group_members, int32_t* n_groups, int32_t* max_members,
-                       int32_t* max_prefix_pages, int32_t* max_own_pages);
+                       int32_t* max_prefix_pages, int32_t* max_own_pages, int32_t* own_start);
 
 /* Workspace bytes of a cascade decode (its partials: the prefix chunks, then the members' own
  * chunks, for every request); pkv_decode_workspace_size when groups has no group. Zero-fill it
@@ -431,6 +435,10 @@ int pkv_cascade_decode_step(const void* q, int32_t dtype_q, int32_t batch, int32
                             const int32_t* context_lens, float scale,
                             const pkv_cascade_desc* groups, void* out, void* workspace,
                             size_t workspace_bytes, void* stream);
+
+/* Tuning: when every request of a tensor-core decode fits one chunk of at most 16 pages,
+ * one warp serves each request (1, the default) or four warps share one (0). */
+int pkv_decode_set_warp_per_request(int32_t on);
 
 /* Tuning: pages per CTA of the prefix pass (0 = automatic). */
 int pkv_cascade_set_prefix_chunk_pages(int32_t pages);

@@ -51,7 +51,8 @@ class _CascadeDesc(ctypes.Structure):
     _fields_ = [("group_of", ctypes.c_void_p), ("prefix_pages", ctypes.c_void_p),
                 ("group_offsets", ctypes.c_void_p), ("group_members", ctypes.c_void_p),
                 ("n_groups", ctypes.c_int32), ("max_members", ctypes.c_int32),
-                ("max_prefix_pages", ctypes.c_int32), ("max_own_pages", ctypes.c_int32)]
+                ("max_prefix_pages", ctypes.c_int32), ("max_own_pages", ctypes.c_int32),
+                ("own_start", ctypes.c_void_p)]
 
 
 def lib():
@@ -92,6 +93,7 @@ def lib():
         "pkv_decode_chunk_pages": (i32, [i32, i32, i32]),
         "pkv_decode_set_kernel": (ctypes.c_int, [i32]),
         "pkv_decode_set_merge_in_place": (ctypes.c_int, [i32]),
+        "pkv_decode_set_warp_per_request": (ctypes.c_int, [i32]),
         "pkv_pages_needed": (ctypes.c_int, [i64, i32, ctypes.POINTER(i64)]),
         "pkv_slot_mapping": (ctypes.c_int, [vp, i32, vp, vp, i64, i32, i32, vp]),
         "pkv_allocator_create": (ctypes.c_int, [i32, vp, ctypes.POINTER(vp)]),
@@ -117,7 +119,7 @@ def lib():
                                                         vp]),
         "pkv_cascade_groups": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp,
                                               ctypes.POINTER(i32), ctypes.POINTER(i32),
-                                              ctypes.POINTER(i32), ctypes.POINTER(i32)]),
+                                              ctypes.POINTER(i32), ctypes.POINTER(i32), vp]),
         "pkv_cascade_workspace_size": (sz, [i32, i32, i32, i32, i32, C]),
         "pkv_cascade_prefix_chunk_pages": (i32, [i32, i32, C]),
         "pkv_cascade_decode_attention": (ctypes.c_int, [vp, i32, i32, i32, vp, vp, D, vp, i32,
@@ -292,7 +294,7 @@ class CascadeGroups:
     ``to(device)`` once to place them for the cascade decode."""
 
     def __init__(self, group_of, prefix_pages, group_offsets, group_members, max_members,
-                 max_prefix_pages, max_own_pages=0):
+                 max_prefix_pages, max_own_pages=0, own_start=None):
         self.group_of = group_of
         self.prefix_pages = prefix_pages
         self.group_offsets = group_offsets
@@ -301,12 +303,15 @@ class CascadeGroups:
         self.max_members = int(max_members)
         self.max_prefix_pages = int(max_prefix_pages)
         self.max_own_pages = int(max_own_pages)
+        if own_start is None:  # prefix_pages[group_of[b]], 0 outside a group
+            own_start = np.where(group_of >= 0, np.append(prefix_pages, 0)[group_of], 0)
+        self.own_start = np.asarray(own_start, dtype=np.int32)
         self._dev = None
 
     def packed(self) -> np.ndarray:
         """The four arrays back to back (int32), as ``to`` places them."""
         return np.concatenate([self.group_of, self.prefix_pages, self.group_offsets,
-                               self.group_members]).astype(np.int32)
+                               self.group_members, self.own_start]).astype(np.int32)
 
     def to(self, device, buffer=None, staging=None):
         """Place the arrays on the device in one copy: into a new tensor, or into ``buffer``
@@ -321,9 +326,10 @@ class CascadeGroups:
             buffer[:p.size].copy_(staging[:p.size], non_blocking=True)
         self._dev = buffer
         self.nbytes = 4 * p.size
-        B, ng = len(self.group_of), self.n_groups
+        B, ng, nm = len(self.group_of), self.n_groups, len(self.group_members)
         base = buffer.data_ptr()
-        self._ptrs = [base, base + 4 * B, base + 4 * (B + ng), base + 4 * (B + 2 * ng + 1)]
+        self._ptrs = [base, base + 4 * B, base + 4 * (B + ng), base + 4 * (B + 2 * ng + 1),
+                      base + 4 * (B + 2 * ng + 1 + nm)]
         return self
 
     def desc(self) -> _CascadeDesc:
@@ -331,9 +337,9 @@ class CascadeGroups:
             return _CascadeDesc(None, None, None, None, 0, 0, 0)
         if self._dev is None:
             raise PkvError(-1, "CascadeGroups.to(device) has not been called")
-        g, p, o, m = self._ptrs
+        g, p, o, m, st = self._ptrs
         return _CascadeDesc(g, p, o, m, self.n_groups, self.max_members, self.max_prefix_pages,
-                            self.max_own_pages)
+                            self.max_own_pages, st)
 
 
 def cascade_groups(block_tables, context_lens, min_members=2, min_prefix_pages=1) -> CascadeGroups:
@@ -348,14 +354,15 @@ def cascade_groups(block_tables, context_lens, min_members=2, min_prefix_pages=1
     offs = np.empty(B + 1, np.int32)
     members = np.empty(max(B, 1), np.int32)
     n, mm, mp, mo = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    start = np.empty(max(B, 1), np.int32)
     _check(lib().pkv_cascade_groups(bt.ctypes.data if B else None, cl.ctypes.data if B else None,
                                     B, W, int(min_members), int(min_prefix_pages),
                                     group_of.ctypes.data, prefix.ctypes.data, offs.ctypes.data,
                                     members.ctypes.data, ctypes.byref(n), ctypes.byref(mm),
-                                    ctypes.byref(mp), ctypes.byref(mo)))
+                                    ctypes.byref(mp), ctypes.byref(mo), start.ctypes.data))
     ng = n.value
     return CascadeGroups(group_of, prefix[:ng].copy(), offs[:ng + 1].copy(),
-                         members[:offs[ng]].copy(), mm.value, mp.value, mo.value)
+                         members[:offs[ng]].copy(), mm.value, mp.value, mo.value, start[:B].copy())
 
 
 def cascade_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_pages_per_seq,
@@ -557,6 +564,11 @@ def device_error(stream=None) -> int:
     if st not in (0, -8):
         _check(st)
     return int(code.value)
+
+
+def decode_set_warp_per_request(on: bool):
+    """One warp per request when every request fits one chunk of at most 16 pages (default)."""
+    _check(lib().pkv_decode_set_warp_per_request(1 if on else 0))
 
 
 def decode_set_chunk_pages(pages: int):

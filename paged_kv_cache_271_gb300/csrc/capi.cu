@@ -86,6 +86,7 @@ std::atomic<int> g_chunk_override{0};
 // (0: always the combine kernel, the default -- measured faster on every workload tried).
 std::atomic<int> g_merge_in_place_max{0};
 std::atomic<int> g_kernel_choice{0};  // 0 automatic, 1 CUDA cores, 2 tensor cores
+std::atomic<int> g_warp_units{1};     // 1: one warp per request for short single-chunk runs
 
 // ---- TMA tensor maps of the pools (for the tensor-core decode) -------------------------------
 
@@ -290,6 +291,13 @@ int pkv_decode_set_kernel(int32_t which) {
   return PKV_OK;
 }
 
+int pkv_decode_set_warp_per_request(int32_t on) {
+  if (on != 0 && on != 1)
+    return set_error(PKV_EINVAL, "pkv_decode_set_warp_per_request: %d is not 0 or 1", on);
+  g_warp_units.store(on);
+  return PKV_OK;
+}
+
 int32_t pkv_decode_chunk_pages(int32_t batch, int32_t num_kv_heads, int32_t max_pages_per_seq) {
   return chunk_pages_for(batch, num_kv_heads, max_pages_per_seq);
 }
@@ -406,6 +414,7 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
       return set_error(PKV_ESHAPE, "%s: groups * kv heads must be <= 65535", who);
     a.group_of = groups->group_of;
     a.prefix_pages = groups->prefix_pages;
+    a.own_start = groups->own_start;
     a.n_groups = groups->n_groups;
     a.max_prefix_pages = groups->max_prefix_pages;
     cascade_split(batch, h_kv, num_q_heads, max_pages_per_seq, groups, &a.chunk_pages,
@@ -453,6 +462,10 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
     return set_error(PKV_EINVAL, "%s: the tensor-core decode needs a bf16 or FP8 cache, head_dim "
                      "128, a 16-byte aligned q and fewer than 2^31 pool rows", who);
   const bool use_mma = mma_ok && choice != 1;
+  // every request in one chunk of at most 16 pages: one warp per request (short runs would
+  // leave a CTA's four warps with a page or two each)
+  // (one chunk column: no request splits, so no merge of chunk partials can arise)
+  a.warp_units = use_mma && a.chunk_grid == 1 && a.chunk_pages <= 16 && g_warp_units.load() != 0;
   CUtensorMap tk, tv;
   if (use_mma || cascade) {
     int rk = 2, rv = 2;

@@ -20,7 +20,7 @@ extern "C" int pkv_cascade_groups(const int32_t* block_tables, const int32_t* co
                                   int32_t* prefix_pages, int32_t* group_offsets,
                                   int32_t* group_members, int32_t* n_groups,
                                   int32_t* max_members, int32_t* max_prefix_pages,
-                                  int32_t* max_own_pages) {
+                                  int32_t* max_own_pages, int32_t* own_start) {
   if (batch < 0 || max_pages_per_seq <= 0 || (batch > 0 && (!block_tables || !context_lens ||
       !group_of || !prefix_pages || !group_members)) || !group_offsets || !n_groups ||
       !max_members || !max_prefix_pages || !max_own_pages)
@@ -76,7 +76,9 @@ extern "C" int pkv_cascade_groups(const int32_t* block_tables, const int32_t* co
   for (int32_t b = 0; b < batch; ++b) {
     const int64_t ctx = std::min<int64_t>(std::max(context_lens[b], 0), (int64_t)P * max_pages_per_seq);
     const int32_t pages = (int32_t)((ctx + P - 1) / P);
-    mo = std::max(mo, pages - (group_of[b] >= 0 ? prefix_pages[group_of[b]] : 0));
+    const int32_t start = group_of[b] >= 0 ? prefix_pages[group_of[b]] : 0;
+    mo = std::max(mo, pages - start);
+    if (own_start) own_start[b] = start;
   }
   *n_groups = ng;
   *max_members = mm;

@@ -114,6 +114,69 @@ __device__ __forceinline__ void decode_epilogue(const DecodeArgs& a, int b, int 
   if (threadIdx.x == 0) a.counters[(size_t)b * a.h_kv + j] = 0;
 }
 
+// The same for one warp that owns a whole (request, KV head) run of a launch in which every
+// request has a single chunk (warp-per-request decode): the warp's merged values are in its own
+// [G][D] area. Lane L owns dims 4L .. 4L+3 (D = 128) of every head, so a cascade member's prefix
+// partials come in with one 16-byte load per (head, slot), all heads' loads at once.
+template <typename TQ, int D, int G>
+__device__ __forceinline__ void decode_epilogue_warp(const DecodeArgs& a, int b, int j,
+                                                     int slot0, const float* red_acc,
+                                                     const float* red_m, const float* red_l,
+                                                     float vs, int lane) {
+  static_assert(D == 128, "four dims per lane");
+  const int i0 = 4 * lane;
+  float M[G], L[G], A[G][4];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    M[g] = red_m[g];
+    L[g] = M[g] != -INFINITY ? red_l[g] : 0.f;
+    const float4 v = *reinterpret_cast<const float4*>(red_acc + g * D + i0);
+    const bool live = M[g] != -INFINITY;
+    A[g][0] = live ? v.x * vs : 0.f;
+    A[g][1] = live ? v.y * vs : 0.f;
+    A[g][2] = live ? v.z * vs : 0.f;
+    A[g][3] = live ? v.w * vs : 0.f;
+  }
+  constexpr int KB = G <= 4 ? 4 : (G <= 8 ? 2 : 1);  // slots whose loads go out together
+  for (int k0 = 0; k0 < slot0; k0 += KB) {  // fold in the prefix partials
+    float mv[KB][G], lv[KB][G];
+    float4 av[KB][G];
+#pragma unroll
+    for (int u = 0; u < KB; ++u)
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const bool in = k0 + u < slot0;
+        const size_t part =
+            ((size_t)b * a.h_q + j * G + g) * a.n_chunk_slots + (in ? k0 + u : 0);
+        mv[u][g] = in ? a.ws_ml[part * 2] : -INFINITY;
+        lv[u][g] = in ? a.ws_ml[part * 2 + 1] : 0.f;
+        av[u][g] = in ? *reinterpret_cast<const float4*>(a.ws_acc + part * D + i0)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+    for (int u = 0; u < KB; ++u)
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float Mb = fmaxf(M[g], mv[u][g]);
+        if (Mb == -INFINITY) continue;
+        const float w0 = exp2f(M[g] - Mb), w = exp2f(mv[u][g] - Mb);
+        L[g] = fmaf(w, lv[u][g], L[g] * w0);
+        A[g][0] = fmaf(w, av[u][g].x, A[g][0] * w0);
+        A[g][1] = fmaf(w, av[u][g].y, A[g][1] * w0);
+        A[g][2] = fmaf(w, av[u][g].z, A[g][2] * w0);
+        A[g][3] = fmaf(w, av[u][g].w, A[g][3] * w0);
+        M[g] = Mb;
+      }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const size_t o = ((size_t)b * a.h_q + j * G + g) * D + i0;
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      store_from_float(static_cast<TQ*>(a.out), o + t, L[g] > 0.f ? A[g][t] / L[g] : 0.f);
+  }
+}
+
 }  // namespace pkv
 
 namespace pkv {
@@ -250,9 +313,9 @@ __device__ __forceinline__ void fused_append_row(const DecodeArgs& a, int b, int
 // into L1 when the CTA starts, one 128-byte line per thread.
 template <int D, int G, int NTHR>
 __device__ __forceinline__ void prefetch_prefix_partials(const DecodeArgs& a, int b, int j,
-                                                         int slot0) {
+                                                         int slot0, int tid) {
   const int lines = slot0 * D * 4 / 128 + 2;  // weighted values, then the (max, sum) pairs
-  for (int e = threadIdx.x; e < G * lines; e += NTHR) {
+  for (int e = tid; e < G * lines; e += NTHR) {
     const int g = e / lines, k = e % lines;
     const size_t bh = (size_t)b * a.h_q + j * G + g;
     const char* p =

@@ -42,14 +42,17 @@ __device__ __forceinline__ SeqPlan seq_plan(const DecodeArgs& a, int b, int ctx)
   p.slot0 = 0;
   p.prefix = 0;
   if (a.group_of != nullptr) {
-    const int g = a.group_of[b];
-    if (g >= 0 && g < a.n_groups) {
-      const int pp = cascade_group_pages(a, g);
-      if (pp > 0) {  // no window in a cascade decode: sp covers pages 0 .. n-1
-        p.prefix = pp;
-        p.sp = SeqPages{max(0, p.sp.n - pp), 0, pp};
-        p.slot0 = cascade_prefix_chunks(a, pp);
-      }
+    int pp = 0;
+    if (a.own_start != nullptr) {  // the member's shared pages, without the group lookup
+      pp = min(max(0, a.own_start[b]), a.max_prefix_pages);
+    } else {
+      const int g = a.group_of[b];
+      if (g >= 0 && g < a.n_groups) pp = cascade_group_pages(a, g);
+    }
+    if (pp > 0) {  // no window in a cascade decode: sp covers pages 0 .. n-1
+      p.prefix = pp;
+      p.sp = SeqPages{max(0, p.sp.n - pp), 0, pp};
+      p.slot0 = cascade_prefix_chunks(a, pp);
     }
   }
   // the grid has chunk_grid chunk columns: a longer run of pages takes larger chunks

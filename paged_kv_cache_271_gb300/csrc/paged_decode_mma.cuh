@@ -45,7 +45,7 @@ namespace pkv {
 #define PKV_MMA_SPW 2  // ring stages per warp
 #endif
 
-template <typename KV, int D, int G>
+template <typename KV, int D, int G, bool WU = false>
 struct MmaShape {
   static_assert(D == 128, "tensor-core decode supports head_dim 128");
   static constexpr bool kFp8 = KV::bytes == 1;
@@ -54,7 +54,9 @@ struct MmaShape {
   static constexpr int NT = (G + 7) / 8;                 // n-tiles of 8 query heads
   static constexpr int KP = D / 32;                      // pairs of 16-wide k-steps
   static constexpr int MT = D / 16;                      // m-tiles of the P.V product
-  static constexpr int SPW = PKV_MMA_SPW;
+  // ring stages per warp: a warp that streams a whole short request keeps three copies in
+  // flight (twelve stages per CTA, still one wave at two CTAs per SM)
+  static constexpr int SPW = WU ? 3 : PKV_MMA_SPW;
   static constexpr int STAGES = kWarps * SPW;
   static constexpr int ROW_BYTES = D * KV::bytes;        // 256 (bf16) or 128 (fp8)
   static constexpr int BOXES = ROW_BYTES / 128;          // 128-byte swizzle boxes per row
@@ -64,8 +66,10 @@ struct MmaShape {
   static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
   static constexpr int PT_BYTES = kWarps * NT * 8 * kPageSize * 2;          // P^T buffers
   static constexpr int MERGE_BYTES = kWarps * G * (D + 2) * 4;
+  // the merge area aliases the ring, except with one warp per request (warps finish apart)
   static constexpr int BIG_BYTES =
-      ((RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES) + 1023) / 1024 * 1024;
+      ((WU ? RING_BYTES + MERGE_BYTES : (RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES)) +
+       1023) / 1024 * 1024;
   static constexpr int SMEM_BYTES =
       1024 + BIG_BYTES + PT_BYTES + STAGES * 8 + STAGES * 4;
 };
@@ -207,26 +211,32 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
   }
 }
 
-template <typename KV, typename TQ, int D, int G>
+// WU (warp per request): every request has a single chunk; warp w of CTA z takes request
+// NW z + w whole (its pages 0, 1, 2, ... through its own two ring stages) and writes its output
+// itself; the warps of a CTA only share the barrier set-up.
+template <typename KV, typename TQ, int D, int G, bool WU>
 __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
     const DecodeArgs a, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v) {
-  using S = MmaShape<KV, D, G>;
+  using S = MmaShape<KV, D, G, WU>;
   constexpr bool F8 = S::kFp8;
   constexpr int NW = S::kWarps, SPW = S::SPW, NT = S::NT, KP = S::KP, MT = S::MT;
-  const int c = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
+  const int c = blockIdx.x, j = blockIdx.y;
+  const bool warp_live = !WU || (int)blockIdx.z * NW + warp < a.batch;
+  const int b = WU ? (warp_live ? (int)blockIdx.z * NW + warp : 0) : (int)blockIdx.z;
+  const bool reporter = c == 0 && (WU ? lane == 0 && warp_live : threadIdx.x == 0);
   int ctx = max(0, a.context_lens[b]);
   const bool cut = ctx > a.max_pages * kPageSize;
   if (cut) {  // longer than its page table: read what the table holds, append nothing
-    if (c == 0 && threadIdx.x == 0) atomicOr(a.err, PKV_DEVERR_BAD_PAGE);
+    if (reporter) atomicOr(a.err, PKV_DEVERR_BAD_PAGE);
     ctx = a.max_pages * kPageSize;
   }
   const SeqPlan plan = seq_plan(a, b, ctx);
   if (plan.prefix > 0 && ctx < plan.prefix * kPageSize + (a.k_new != nullptr ? 1 : 0)) {
     // a cascade member's context must reach past its group's shared pages
-    if (c == 0 && threadIdx.x == 0) atomicOr(a.err, PKV_DEVERR_BAD_GROUP);
+    if (reporter) atomicOr(a.err, PKV_DEVERR_BAD_GROUP);
   }
   const SeqPages sp = plan.sp;
   const int pages_seq = sp.n;  // the pages read here, split into n_chunks near-equal chunks
@@ -234,18 +244,23 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
   // the combine kernel (a programmatic dependent launch) may be scheduled once every CTA of
   // this grid has started; it waits for this grid's completion before reading its partials
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (c > 0 && c >= n_chunks) return;
+  if (!WU && c > 0 && c >= n_chunks) return;
+  const bool active = warp_live && !(c > 0 && c >= n_chunks);  // (WU: per warp)
   const int per_chunk = n_chunks > 0 ? (pages_seq + n_chunks - 1) / n_chunks : 0;
   const int page0 = c * per_chunk;
-  const int n_pages = max(0, min(per_chunk, pages_seq - page0));
+  const int n_pages = active ? max(0, min(per_chunk, pages_seq - page0)) : 0;
   // the warp that will reach the page of position ctx-1 prefetches this step's rows now
   const int append_warp =
-      a.k_new != nullptr && !cut && n_pages > 0 && page0 + n_pages == pages_seq
-          ? (n_pages - 1) % PKV_MMA_WARPS
+      active && a.k_new != nullptr && !cut && n_pages > 0 && page0 + n_pages == pages_seq
+          ? (WU ? warp : (n_pages - 1) % PKV_MMA_WARPS)
           : -1;
   if (warp == append_warp) append_prefetch<KV, D>(a, b, j, lane);
-  if (plan.slot0 > 0 && n_chunks <= 1)
-    prefetch_prefix_partials<D, G, 32 * PKV_MMA_WARPS>(a, b, j, plan.slot0);
+  if (active && plan.slot0 > 0 && n_chunks <= 1) {
+    if constexpr (WU)
+      prefetch_prefix_partials<D, G, 32>(a, b, j, plan.slot0, lane);
+    else
+      prefetch_prefix_partials<D, G, 32 * PKV_MMA_WARPS>(a, b, j, plan.slot0, threadIdx.x);
+  }
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -262,6 +277,7 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
   }
   __syncthreads();
+  if (WU && !active) return;  // (no CTA-wide barrier follows in this mode)
 
   const int32_t* btrow = a.block_tables + (size_t)b * a.max_pages;
   const uint64_t pol = l2_evict_first_policy();
@@ -283,23 +299,26 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
     }
   };
 
-  const int n_mine = n_pages > warp ? (n_pages - warp + NW - 1) / NW : 0;
+  // the warp's pages: chunk pages w, w + NW, ... (WU: all of them)
+  constexpr int STRIDE = WU ? 1 : NW;
+  const int first = WU ? 0 : warp;
+  const int n_mine = WU ? n_pages : (n_pages > warp ? (n_pages - warp + NW - 1) / NW : 0);
   // Page ids of the warp's pages, read 32 at a time ahead of their copies so that no copy waits
-  // on a table read: lane L holds the id of the warp's page 32 t + L (chunk page warp + NW m).
+  // on a table read: lane L holds the id of the warp's page 32 t + L.
   int ids = -1;
   auto load_ids = [&](int t) {
     const int mm = 32 * t + lane;
-    ids = mm < n_mine ? btrow[logical_page(sp, page0 + warp + NW * mm)] : -1;
+    ids = mm < n_mine ? btrow[logical_page(sp, page0 + first + STRIDE * mm)] : -1;
   };
   load_ids(0);
   {
-    int first[SPW];
+    int first_ids[SPW];
 #pragma unroll
-    for (int m = 0; m < SPW; ++m) first[m] = __shfl_sync(0xffffffffu, ids, m);
+    for (int m = 0; m < SPW; ++m) first_ids[m] = __shfl_sync(0xffffffffu, ids, m);
     if (lane == 0) {
 #pragma unroll
       for (int m = 0; m < SPW; ++m)
-        if (m < n_mine) issue(warp + NW * m, warp * SPW + m, first[m]);
+        if (m < n_mine) issue(first + STRIDE * m, warp * SPW + m, first_ids[m]);
     }
   }
 
@@ -375,7 +394,7 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
   int m = 0;
   bool ok = true;
   for (; m < n_mine; ++m) {
-    const int i = warp + NW * m;
+    const int i = first + STRIDE * m;
     const int stg = warp * SPW + (m % SPW);
     const bool got = mbar_wait(&full[stg], (m / SPW) & 1, a.err);
     if (!__all_sync(0xffffffffu, got)) {
@@ -551,7 +570,7 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
       const int pid = __shfl_sync(0xffffffffu, ids, mn & 31);
       if (lane == 0) {
         fence_proxy_async_smem();
-        issue(i + NW * SPW, stg, pid);
+        issue(i + STRIDE * SPW, stg, pid);
       }
     }
   }
@@ -559,11 +578,15 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
     for (int mm = m; mm < n_mine && mm < m + SPW; ++mm)
       mbar_wait(&full[warp * SPW + (mm % SPW)], (mm / SPW) & 1, a.err);
   }
-  __syncthreads();  // every copy has landed: the ring is free for the merge
+  if constexpr (WU)
+    __syncwarp();
+  else
+    __syncthreads();  // every copy has landed: the ring is free for the merge
 
-  float* red_acc = reinterpret_cast<float*>(ring);  // [NW][G][D]
-  float* red_m = red_acc + NW * G * D;              // [NW][G]
-  float* red_l = red_m + NW * G;                    // [NW][G]
+  // the merge area: [NW][G][D] values, [NW][G] maxima, [NW][G] sums (WU: past the ring)
+  float* red_acc = reinterpret_cast<float*>(ring + (WU ? S::RING_BYTES : 0));
+  float* red_m = red_acc + NW * G * D;
+  float* red_l = red_m + NW * G;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -589,18 +612,23 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
       }
     }
   }
-  __syncthreads();
-
   const float vs = F8 ? a.v_scales[j] : 1.f;
-  decode_epilogue<TQ, D, G, NW, S::kThreads>(a, b, j, c, n_chunks, plan.slot0, red_acc,
-                                             red_m, red_l, vs);
+  if constexpr (WU) {
+    __syncwarp();
+    decode_epilogue_warp<TQ, D, G>(a, b, j, plan.slot0, red_acc + warp * G * D, red_m + warp * G,
+                                   red_l + warp * G, vs, lane);
+  } else {
+    __syncthreads();
+    decode_epilogue<TQ, D, G, NW, S::kThreads>(a, b, j, c, n_chunks, plan.slot0, red_acc,
+                                               red_m, red_l, vs);
+  }
 }
 
-template <typename KV, typename TQ, int D, int G>
-cudaError_t launch_decode_mma_t(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                                cudaStream_t s) {
-  using S = MmaShape<KV, D, G>;
-  auto kern = paged_decode_mma_kernel<KV, TQ, D, G>;
+template <typename KV, typename TQ, int D, int G, bool WU>
+cudaError_t launch_decode_mma_w(const DecodeArgs& a, const CUtensorMap& tk,
+                                const CUtensorMap& tv, cudaStream_t s) {
+  using S = MmaShape<KV, D, G, WU>;
+  auto kern = paged_decode_mma_kernel<KV, TQ, D, G, WU>;
   static unsigned long long attr_done = 0;  // one bit per device, per instantiation
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -610,9 +638,16 @@ cudaError_t launch_decode_mma_t(const DecodeArgs& a, const CUtensorMap& tk, cons
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_done |= 1ull << dev;
   }
-  dim3 grid(a.chunk_grid, a.h_kv, a.batch);
+  dim3 grid(a.chunk_grid, a.h_kv, WU ? (a.batch + S::kWarps - 1) / S::kWarps : a.batch);
   kern<<<grid, S::kThreads, S::SMEM_BYTES, s>>>(a, tk, tv);
   return cudaGetLastError();
+}
+
+template <typename KV, typename TQ, int D, int G>
+cudaError_t launch_decode_mma_t(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                                cudaStream_t s) {
+  return a.warp_units ? launch_decode_mma_w<KV, TQ, D, G, true>(a, tk, tv, s)
+                      : launch_decode_mma_w<KV, TQ, D, G, false>(a, tk, tv, s);
 }
 
 template <typename KV, typename TQ>

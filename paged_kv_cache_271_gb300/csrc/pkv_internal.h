@@ -37,12 +37,14 @@ struct DecodeArgs {
                       // the cascade prefix slots)
   float scale_log2;   // softmax scale * log2(e)
   int tma_rank;       // tensor maps of a 256-byte-row pool: 3 (one box per tile) or 2
+  int warp_units;     // tensor-core decode: one warp per request (every request one chunk)
   // Cascade decode (null group_of otherwise): request b belongs to group group_of[b] (-1:
   // none), whose first prefix_pages[g] logical pages are shared by every member and handled
   // by the prefix kernel in chunks of prefix_chunk_pages; their partials take chunk slots
   // 0 .. ceil(prefix_pages[g] / prefix_chunk_pages) - 1 and the request's own pages follow.
   const int32_t* group_of;
   const int32_t* prefix_pages;
+  const int32_t* own_start;  // [batch] prefix_pages[group_of[b]] (0 outside groups), or null
   int n_groups;
   int max_prefix_pages;
   int prefix_chunk_pages;

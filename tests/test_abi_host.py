@@ -370,6 +370,7 @@ def test_cascade_groups_against_model():
         pre = {b: n for mem, n in ref for b in mem}
         own = [-(-min(max(int(cl[b]), 0), 16 * W) // 16) - pre.get(b, 0) for b in range(B)]
         assert g.max_own_pages == max(own, default=0)
+        assert g.own_start.tolist() == [pre.get(b, 0) for b in range(B)]
 
 
 def test_cascade_argument_errors_are_caught_on_the_host():

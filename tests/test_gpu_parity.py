@@ -345,3 +345,25 @@ def test_host_step_equals_device_step(kv):
     assert torch.equal(out_a.cpu(), out_b)
     assert torch.equal(a.cache.k.view(torch.uint8), b.cache.k.view(torch.uint8))
     assert hs.h2d_bytes >= (b.q.numel() + 2 * b.k_new.numel()) * 2
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3", "int8"])
+@pytest.mark.parametrize("wpr", [True, False])
+def test_short_single_chunk_batches_both_ways(kv, wpr):
+    # every request fits one chunk of <= 16 pages: one warp per request (default) or four warps
+    # per request; both match the oracle, the step and append-then-decode agree bitwise
+    lens = [1, 16, 17, 100, 255, 3, 64, 200, 33, 129]
+    w = workloads.custom("wpr", 7500, len(lens), 16, 4, 128, kv, "bf16", lens)
+    pkv.decode_set_warp_per_request(wpr)
+    try:
+        a = Scenario(w)
+        out_a = a.step().clone()
+        b = Scenario(w)
+        out_b = b.fused_step().clone()
+        torch.cuda.synchronize()
+    finally:
+        pkv.decode_set_warp_per_request(True)
+    assert pkv.device_error() == 0
+    assert torch.equal(out_a, out_b)
+    err = _max_err(out_b, oracle_expected(w))
+    assert err <= tolerance(w), err
