@@ -188,17 +188,20 @@ __global__ void kv_scale_finalize_kernel(float* scales, int h_kv, float code_max
 }
 
 // Merge of the chunk partials of one (b, h): M = max_c m_c, w_c = 2^(m_c - M),
-// out = sum_c w_c acc_c / sum_c w_c l_c. One CTA of 4 warps per (h, b): the threads find M
-// together; warp w then accumulates chunks w, w+4, w+8, ... with vector loads (lane = DL dims)
-// and the warps' sums are added in warp order, so the result depends only on the number of
-// chunks. Launched as a programmatic dependent of the decode kernel, whose CTAs allow it to be
-// scheduled as they start: its CTAs are placed while the decode's last CTAs run and wait for
-// the decode's results before reading them.
+// out = sum_c w_c acc_c / sum_c w_c l_c, the sums taken in chunk order. One warp per (h, b),
+// four per CTA: lane L owns dims DL L .. DL L + DL - 1; the partials of up to 32 chunks come in
+// at once (lane c reads chunk c's (max, sum), every lane its dims of every chunk), the maximum
+// and the weights go round by shuffles, and no block barrier is needed. Launched as a
+// programmatic dependent of the decode kernel, whose CTAs allow it to be scheduled as they
+// start: its CTAs are placed while the decode's last CTAs run and wait for the decode's results
+// before reading them.
 template <typename TQ, int D>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a) {
   constexpr int DL = D / 32;
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int CB = 8;  // chunks whose values are loaded together
+  const int h = blockIdx.x * 4 + (threadIdx.x >> 5), b = blockIdx.y;
+  const int lane = threadIdx.x & 31;
+  if (h >= a.h_q) return;
   // the chunk count depends on inputs only: known before the decode's results are
   const int ctx = min(max(0, a.context_lens[b]), a.max_pages * kPageSize);
   const int n_chunks = seq_plan(a, b, ctx).n_total;  // partials of the request
@@ -206,56 +209,70 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a)
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid is done, its writes seen
   const size_t bh = (size_t)b * a.h_q + h;
   const float* ml = a.ws_ml + bh * a.n_chunk_slots * 2;
-  const float* acc = a.ws_acc + bh * a.n_chunk_slots * D;
-  __shared__ float s_max[4];
-  __shared__ float s_l[4];
-  __shared__ float s_acc[4][D];
+  const float* acc = a.ws_acc + bh * a.n_chunk_slots * D + lane * DL;
 
-  float M = -INFINITY;
-  for (int c = threadIdx.x; c < n_chunks; c += 128) M = fmaxf(M, ml[2 * c]);
-#pragma unroll
-  for (int o = 16; o >= 1; o /= 2) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (lane == 0) s_max[warp] = M;
-  __syncthreads();
-  M = fmaxf(fmaxf(s_max[0], s_max[1]), fmaxf(s_max[2], s_max[3]));
-
-  float L = 0.f, A[DL];
+  float M = -INFINITY, Lw = 0.f, A[DL];
 #pragma unroll
   for (int k = 0; k < DL; ++k) A[k] = 0.f;
-  if (M != -INFINITY) {
-#pragma unroll 4
-    for (int c = warp; c < n_chunks; c += 4) {
-      const float w = exp2f(ml[2 * c] - M);
-      L = fmaf(w, ml[2 * c + 1], L);
-      const float* src = acc + (size_t)c * D + lane * DL;
-      if constexpr (DL == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        A[0] = fmaf(w, v.x, A[0]);
-        A[1] = fmaf(w, v.y, A[1]);
-        A[2] = fmaf(w, v.z, A[2]);
-        A[3] = fmaf(w, v.w, A[3]);
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        A[0] = fmaf(w, v.x, A[0]);
-        A[1] = fmaf(w, v.y, A[1]);
+  for (int c0 = 0; c0 < n_chunks; c0 += 32) {  // 32 chunks per round of (max, sum) pairs
+    const int nc = min(32, n_chunks - c0);
+    const float2 p = lane < nc ? *reinterpret_cast<const float2*>(ml + 2 * (c0 + lane))
+                               : make_float2(-INFINITY, 0.f);
+    float mr = p.x;
+#pragma unroll
+    for (int o = 16; o >= 1; o /= 2) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+    const float Mn = fmaxf(M, mr);
+    if (Mn == -INFINITY) continue;
+    const float rescale = exp2f(M - Mn);  // 0 on the first round with a finite maximum
+    const float w = p.x == -INFINITY ? 0.f : exp2f(p.x - Mn);
+    float lw = w * p.y;
+#pragma unroll
+    for (int o = 16; o >= 1; o /= 2) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+    Lw = fmaf(Lw, rescale, lw);
+#pragma unroll
+    for (int k = 0; k < DL; ++k) A[k] *= rescale;
+    M = Mn;
+    for (int cb = 0; cb < nc; cb += CB) {
+      float v[CB][DL];
+#pragma unroll
+      for (int u = 0; u < CB; ++u) {  // loads of CB chunks in flight together
+        const int c = c0 + cb + u;
+        if (cb + u < nc) {
+          if constexpr (DL == 4) {
+            const float4 x = *reinterpret_cast<const float4*>(acc + (size_t)c * D);
+            v[u][0] = x.x;
+            v[u][1] = x.y;
+            v[u][2] = x.z;
+            v[u][3] = x.w;
+          } else {
+            const float2 x = *reinterpret_cast<const float2*>(acc + (size_t)c * D);
+            v[u][0] = x.x;
+            v[u][1] = x.y;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < DL; ++k) v[u][k] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < CB; ++u) {
+        const float wu = __shfl_sync(0xffffffffu, w, (cb + u) & 31);
+        if (cb + u < nc) {
+#pragma unroll
+          for (int k = 0; k < DL; ++k) A[k] = fmaf(wu, v[u][k], A[k]);
+        }
       }
     }
   }
-  if (lane == 0) s_l[warp] = L;
 #pragma unroll
-  for (int k = 0; k < DL; ++k) s_acc[warp][lane * DL + k] = A[k];
-  __syncthreads();
-  const float Lt = ((s_l[0] + s_l[1]) + s_l[2]) + s_l[3];
-  for (int i = threadIdx.x; i < D; i += 128) {
-    const float At = ((s_acc[0][i] + s_acc[1][i]) + s_acc[2][i]) + s_acc[3][i];
-    store_from_float(static_cast<TQ*>(a.out), bh * D + i, Lt > 0.f ? At / Lt : 0.f);
-  }
+  for (int k = 0; k < DL; ++k)
+    store_from_float(static_cast<TQ*>(a.out), bh * D + lane * DL + k, Lw > 0.f ? A[k] / Lw : 0.f);
 }
 
 template <typename TQ, int D>
 cudaError_t launch_combine_t(const DecodeArgs& a, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.h_q, a.batch);
+  cfg.gridDim = dim3((a.h_q + 3) / 4, a.batch);
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
