@@ -440,6 +440,12 @@ int pkv_cascade_decode_step(const void* q, int32_t dtype_q, int32_t batch, int32
  * one warp serves each request (1, the default) or four warps share one (0). */
 int pkv_decode_set_warp_per_request(int32_t on);
 
+/* Tuning: in a cascade decode on the tensor-core path, the own-page decode is launched as a
+ * programmatic dependent of the prefix kernel (1, the default): it reads its own pages while
+ * the prefix kernel runs and waits for that kernel only before it folds in the prefix
+ * partials. 0 runs the two kernels one after the other. The results are the same. */
+int pkv_cascade_set_overlap(int32_t on);
+
 /* Tuning: pages per CTA of the prefix pass (0 = automatic). */
 int pkv_cascade_set_prefix_chunk_pages(int32_t pages);
 

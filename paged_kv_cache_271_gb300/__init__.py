@@ -94,6 +94,7 @@ def lib():
         "pkv_decode_set_kernel": (ctypes.c_int, [i32]),
         "pkv_decode_set_merge_in_place": (ctypes.c_int, [i32]),
         "pkv_decode_set_warp_per_request": (ctypes.c_int, [i32]),
+        "pkv_cascade_set_overlap": (ctypes.c_int, [i32]),
         "pkv_pages_needed": (ctypes.c_int, [i64, i32, ctypes.POINTER(i64)]),
         "pkv_slot_mapping": (ctypes.c_int, [vp, i32, vp, vp, i64, i32, i32, vp]),
         "pkv_allocator_create": (ctypes.c_int, [i32, vp, ctypes.POINTER(vp)]),
@@ -569,6 +570,11 @@ def device_error(stream=None) -> int:
 def decode_set_warp_per_request(on: bool):
     """One warp per request when every request fits one chunk of at most 16 pages (default)."""
     _check(lib().pkv_decode_set_warp_per_request(1 if on else 0))
+
+
+def cascade_set_overlap(on: bool):
+    """Cascade decode: run the own-page decode alongside the prefix kernel (default) or after it."""
+    _check(lib().pkv_cascade_set_overlap(1 if on else 0))
 
 
 def decode_set_chunk_pages(pages: int):

@@ -86,6 +86,7 @@ std::atomic<int> g_chunk_override{0};
 // (0: always the combine kernel, the default -- measured faster on every workload tried).
 std::atomic<int> g_merge_in_place_max{0};
 std::atomic<int> g_kernel_choice{0};  // 0 automatic, 1 CUDA cores, 2 tensor cores
+std::atomic<int> g_cascade_overlap{1};  // 1: own-page decode overlaps the prefix kernel
 std::atomic<int> g_warp_units{1};     // 1: one warp per request for short single-chunk runs
 
 // ---- TMA tensor maps of the pools (for the tensor-core decode) -------------------------------
@@ -298,6 +299,13 @@ int pkv_decode_set_warp_per_request(int32_t on) {
   return PKV_OK;
 }
 
+int pkv_cascade_set_overlap(int32_t on) {
+  if (on != 0 && on != 1)
+    return set_error(PKV_EINVAL, "pkv_cascade_set_overlap: %d is not 0 or 1", on);
+  g_cascade_overlap.store(on);
+  return PKV_OK;
+}
+
 int32_t pkv_decode_chunk_pages(int32_t batch, int32_t num_kv_heads, int32_t max_pages_per_seq) {
   return chunk_pages_for(batch, num_kv_heads, max_pages_per_seq);
 }
@@ -466,6 +474,7 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
   // leave a CTA's four warps with a page or two each)
   // (one chunk column: no request splits, so no merge of chunk partials can arise)
   a.warp_units = use_mma && a.chunk_grid == 1 && a.chunk_pages <= 16 && g_warp_units.load() != 0;
+  a.prefix_dep = cascade && use_mma && g_cascade_overlap.load() != 0 ? 1 : 0;
   CUtensorMap tk, tv;
   if (use_mma || cascade) {
     int rk = 2, rv = 2;

@@ -56,6 +56,9 @@ __global__ void __launch_bounds__(32 * kCpWarps, 3) cascade_prefix_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const bool reporter = c == 0 && rt == 0 && threadIdx.x == 0;
+  // the own-page decode (a programmatic dependent launch) may start on the SMs this grid leaves
+  // free; it waits for this grid's completion before it reads the partials written here
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int o0 = ca.group_offsets[g];
   int members = ca.group_offsets[g + 1] - o0;

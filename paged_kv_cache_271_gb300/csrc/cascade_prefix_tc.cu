@@ -131,6 +131,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) cascade_prefix_tc_kernel(
   const int g = blockIdx.z / a.h_kv, j = blockIdx.z % a.h_kv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool reporter = c == 0 && rt == 0 && threadIdx.x == 0;
+  // the own-page decode (a programmatic dependent launch) may start on the SMs this grid leaves
+  // free; it waits for this grid's completion before it reads the partials written here
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ---- the CTA's rows and pages (uniform exits before any barrier) ----
   const int o0 = ca.group_offsets[g];
@@ -459,7 +462,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) cascade_prefix_tc_kernel(
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         a.ws_ml[part * 2 + 0] = m_used;
         a.ws_ml[part * 2 + 1] = l;
-        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // written before exit
+        // the shared-memory source is read before the CTA exits (the global writes complete
+        // with the grid)
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
       }
     }
   }

@@ -255,7 +255,8 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
           ? (WU ? warp : (n_pages - 1) % PKV_MMA_WARPS)
           : -1;
   if (warp == append_warp) append_prefetch<KV, D>(a, b, j, lane);
-  if (active && plan.slot0 > 0 && n_chunks <= 1) {
+  // (as a dependent launch of the prefix kernel, its partials are not written yet)
+  if (active && plan.slot0 > 0 && n_chunks <= 1 && !a.prefix_dep) {
     if constexpr (WU)
       prefetch_prefix_partials<D, G, 32>(a, b, j, plan.slot0, lane);
     else
@@ -613,6 +614,8 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
     }
   }
   const float vs = F8 ? a.v_scales[j] : 1.f;
+  // a dependent launch of the prefix kernel: its partials are complete and visible past here
+  if (a.prefix_dep) asm volatile("griddepcontrol.wait;" ::: "memory");
   if constexpr (WU) {
     __syncwarp();
     decode_epilogue_warp<TQ, D, G>(a, b, j, plan.slot0, red_acc + warp * G * D, red_m + warp * G,
@@ -638,9 +641,17 @@ cudaError_t launch_decode_mma_w(const DecodeArgs& a, const CUtensorMap& tk,
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_done |= 1ull << dev;
   }
-  dim3 grid(a.chunk_grid, a.h_kv, WU ? (a.batch + S::kWarps - 1) / S::kWarps : a.batch);
-  kern<<<grid, S::kThreads, S::SMEM_BYTES, s>>>(a, tk, tv);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.chunk_grid, a.h_kv, WU ? (a.batch + S::kWarps - 1) / S::kWarps : a.batch);
+  cfg.blockDim = dim3(S::kThreads);
+  cfg.dynamicSmemBytes = S::SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.prefix_dep ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a, tk, tv);
 }
 
 template <typename KV, typename TQ, int D, int G>

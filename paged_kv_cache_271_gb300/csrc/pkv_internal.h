@@ -48,6 +48,10 @@ struct DecodeArgs {
   int n_groups;
   int max_prefix_pages;
   int prefix_chunk_pages;
+  // 1: the tensor-core decode is a programmatic dependent launch of the cascade prefix kernel:
+  // it reads its own pages while the prefix kernel runs and waits for that grid
+  // (griddepcontrol.wait) before it reads any prefix partial
+  int prefix_dep;
 };
 
 // Query rows ((member, query head) pairs) per CTA of the cascade prefix kernel, and the CTAs

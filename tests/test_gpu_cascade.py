@@ -86,10 +86,11 @@ def test_cascade_step_equals_append_then_cascade_and_oracle(prefix_kernel):
     assert err < TOL, err
 
 
-@pytest.mark.parametrize("chunk", [1, 3, 8, 32])
+@pytest.mark.parametrize("chunk", [1, 3, 8, 32, 70])
 def test_cascade_prefix_chunking_and_ragged_row_tiles(chunk, prefix_kernel):
-    # 70 shared pages split into several chunks; 17 members x 4 heads = 68 rows: a ragged
-    # second row tile; singles long enough to need the split decode too
+    # 70 shared pages split into several chunks (or one of 18 tiles: the copy ring and the
+    # page masks wrap several times); 17 members x 4 heads = 68 rows: a ragged second row
+    # tile; singles long enough to need the split decode too
     w = _case(4, h_kv=2, seed=13, groups=((70, 17, 1, 90),), singles=((700, 1400),) * 2)
     sc = GroupScenario(w)
     sc.append()
@@ -104,6 +105,31 @@ def test_cascade_prefix_chunking_and_ragged_row_tiles(chunk, prefix_kernel):
         pkv.cascade_set_prefix_chunk_pages(0)
     _check_no_error()
     err = np.abs(out.float().cpu().numpy() - oracle_groups_expected(w)).max()
+    assert err < TOL, err
+
+
+@pytest.mark.parametrize("own_pages", [(1, 90), (300, 700)], ids=["one_own_chunk", "own_chunks"])
+def test_cascade_overlap_on_and_off_agree(own_pages, prefix_kernel):
+    # the own-page decode as a dependent launch of the prefix kernel (waiting for it only
+    # before the fold) and after it: the same kernels, so the same bits
+    lo, hi = own_pages
+    w = _case(4, h_kv=4, seed=14, groups=((40, 9, lo, hi), (3, 5, lo, hi)),
+              singles=((lo, hi),) * 3)
+    sc = GroupScenario(w)
+    sc.append()
+    groups = pkv.cascade_groups(sc.bt_host, sc.cl_host).to(sc.q.device)
+    pkv.device_error()
+    outs = []
+    try:
+        for on in (False, True):
+            pkv.cascade_set_overlap(on)
+            outs.append(_cascade(sc, groups).clone())
+            torch.cuda.synchronize()
+            _check_no_error()
+    finally:
+        pkv.cascade_set_overlap(True)
+    assert torch.equal(outs[0], outs[1])
+    err = np.abs(outs[1].float().cpu().numpy() - oracle_groups_expected(w)).max()
     assert err < TOL, err
 
 
