@@ -188,34 +188,22 @@ __global__ void kv_scale_finalize_kernel(float* scales, int h_kv, float code_max
 }
 
 // Merge of the chunk partials of one (b, h): M = max_c m_c, w_c = 2^(m_c - M),
-// out = sum_c w_c acc_c / sum_c w_c l_c, the sums taken in chunk order. One warp per (h, b),
-// four per CTA: lane L owns dims DL L .. DL L + DL - 1; the partials of up to 32 chunks come in
-// at once (lane c reads chunk c's (max, sum), every lane its dims of every chunk), the maximum
-// and the weights go round by shuffles, and no block barrier is needed. Launched as a
-// programmatic dependent of the decode kernel, whose CTAs allow it to be scheduled as they
-// start: its CTAs are placed while the decode's last CTAs run and wait for the decode's results
-// before reading them.
-template <typename TQ, int D>
-__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a) {
+// out = sum_c w_c acc_c / sum_c w_c l_c. A warp merges a run of chunks in chunk order: lane L
+// owns dims DL L .. DL L + DL - 1; the (max, sum) pairs of up to 32 chunks come in at once (lane
+// c reads chunk c's), then the values of CB chunks at a time; the maximum and the weights go
+// round by shuffles. Launched as a programmatic dependent of the decode kernel, whose CTAs allow
+// it to be scheduled as they start: its CTAs are placed while the decode's last CTAs run and
+// wait for the decode's results before reading them.
+//  * few chunks (SPLIT false): one warp per (h, b), four per CTA, no block barrier;
+//  * many chunks (SPLIT true, a long context cut into up to hundreds of chunks): one CTA per
+//    (h, b) whose four warps each merge a quarter of the chunks (a run of consecutive chunks),
+//    then warp 0 merges the four results in warp order, so fewer loads wait on one another.
+template <int D, int CB>
+__device__ __forceinline__ void merge_run(const float* ml, const float* acc, int lo, int hi,
+                                          int lane, float& M, float& Lw, float (&A)[D / 32]) {
   constexpr int DL = D / 32;
-  constexpr int CB = 8;  // chunks whose values are loaded together
-  const int h = blockIdx.x * 4 + (threadIdx.x >> 5), b = blockIdx.y;
-  const int lane = threadIdx.x & 31;
-  if (h >= a.h_q) return;
-  // the chunk count depends on inputs only: known before the decode's results are
-  const int ctx = min(max(0, a.context_lens[b]), a.max_pages * kPageSize);
-  const int n_chunks = seq_plan(a, b, ctx).n_total;  // partials of the request
-  if (n_chunks <= 1) return;
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid is done, its writes seen
-  const size_t bh = (size_t)b * a.h_q + h;
-  const float* ml = a.ws_ml + bh * a.n_chunk_slots * 2;
-  const float* acc = a.ws_acc + bh * a.n_chunk_slots * D + lane * DL;
-
-  float M = -INFINITY, Lw = 0.f, A[DL];
-#pragma unroll
-  for (int k = 0; k < DL; ++k) A[k] = 0.f;
-  for (int c0 = 0; c0 < n_chunks; c0 += 32) {  // 32 chunks per round of (max, sum) pairs
-    const int nc = min(32, n_chunks - c0);
+  for (int c0 = lo; c0 < hi; c0 += 32) {  // 32 chunks per round of (max, sum) pairs
+    const int nc = min(32, hi - c0);
     const float2 p = lane < nc ? *reinterpret_cast<const float2*>(ml + 2 * (c0 + lane))
                                : make_float2(-INFINITY, 0.f);
     float mr = p.x;
@@ -264,15 +252,70 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a)
       }
     }
   }
+}
+
+template <typename TQ, int D, bool SPLIT>
+__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a) {
+  constexpr int DL = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = SPLIT ? blockIdx.x : blockIdx.x * 4 + warp, b = blockIdx.y;
+  if (h >= a.h_q) return;
+  // the chunk count depends on inputs only: known before the decode's results are
+  const int ctx = min(max(0, a.context_lens[b]), a.max_pages * kPageSize);
+  const int n_chunks = seq_plan(a, b, ctx).n_total;  // partials of the request
+  if (n_chunks <= 1) return;  // (uniform over the CTA when SPLIT)
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid is done, its writes seen
+  const size_t bh = (size_t)b * a.h_q + h;
+  const float* ml = a.ws_ml + bh * a.n_chunk_slots * 2;
+  const float* acc = a.ws_acc + bh * a.n_chunk_slots * D + lane * DL;
+
+  float M = -INFINITY, Lw = 0.f, A[DL];
+#pragma unroll
+  for (int k = 0; k < DL; ++k) A[k] = 0.f;
+  if constexpr (!SPLIT) {
+    merge_run<D, 8>(ml, acc, 0, n_chunks, lane, M, Lw, A);
+  } else {
+    const int q = (n_chunks + 3) / 4;
+    merge_run<D, 16>(ml, acc, min(n_chunks, warp * q), min(n_chunks, (warp + 1) * q), lane, M,
+                     Lw, A);
+    __shared__ float red_a[4][D];
+    __shared__ float red_ml[4][2];
+#pragma unroll
+    for (int k = 0; k < DL; ++k) red_a[warp][lane * DL + k] = A[k];
+    if (lane == 0) {
+      red_ml[warp][0] = M;
+      red_ml[warp][1] = Lw;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    float Mw[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) Mw[w] = red_ml[w][0];
+    M = fmaxf(fmaxf(Mw[0], Mw[1]), fmaxf(Mw[2], Mw[3]));
+    Lw = 0.f;
+#pragma unroll
+    for (int k = 0; k < DL; ++k) A[k] = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {  // an empty quarter (maximum -inf) has weight 0
+      const float sw = Mw[w] == -INFINITY ? 0.f : exp2f(Mw[w] - M);
+      Lw = fmaf(sw, red_ml[w][1], Lw);
+#pragma unroll
+      for (int k = 0; k < DL; ++k) A[k] = fmaf(sw, red_a[w][lane * DL + k], A[k]);
+    }
+  }
 #pragma unroll
   for (int k = 0; k < DL; ++k)
     store_from_float(static_cast<TQ*>(a.out), bh * D + lane * DL + k, Lw > 0.f ? A[k] / Lw : 0.f);
 }
 
+// Chunk slots above which one CTA (four warps) merges each (request, head)
+constexpr int kCombineSplitSlots = 16;
+
 template <typename TQ, int D>
 cudaError_t launch_combine_t(const DecodeArgs& a, cudaStream_t s) {
+  const bool split = a.n_chunk_slots > kCombineSplitSlots;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.h_q + 3) / 4, a.batch);
+  cfg.gridDim = dim3(split ? a.h_q : (a.h_q + 3) / 4, a.batch);
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
@@ -281,7 +324,8 @@ cudaError_t launch_combine_t(const DecodeArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<TQ, D>, a);
+  return split ? cudaLaunchKernelEx(&cfg, decode_combine_kernel<TQ, D, true>, a)
+               : cudaLaunchKernelEx(&cfg, decode_combine_kernel<TQ, D, false>, a);
 }
 
 // Copy whole pages (every KV head's tile) of both pools: pool[dst[p]] = pool[src[p]]. One

@@ -126,6 +126,18 @@ def test_decode_parity_shapes(kv, qd, h_q, h_kv, d, lens, chunk, kernel):
     assert err <= tolerance(w), err
 
 
+@pytest.mark.parametrize("chunk", [1, 2, 3])
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_combine_of_many_chunks(chunk, kernel):
+    # more than 16 chunk slots: each (request, head) is merged by four warps, each over a run
+    # of consecutive chunks; requests with 1, 2, 3, 5, 17 and 63+ chunks leave some warps an
+    # empty run
+    lens = [1000, 16, 17, 33, 70, 260, 1, 2, 1500]
+    w = workloads.custom("many_chunks", 9500 + chunk, len(lens), 16, 4, 128, "bf16", "bf16", lens)
+    sc, out = _run(w, chunk=chunk, kernel=kernel)
+    assert _max_err(out, oracle_expected(w)) <= tolerance(w)
+
+
 @pytest.mark.parametrize("kernel", [1, 2])
 def test_split_results_do_not_depend_on_physical_pages(kernel):
     w = workloads.llama3_8b_batch64(batch=8)
