@@ -398,6 +398,19 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
   a.max_pages = max_pages_per_seq;
   a.chunk_pages = chunk_pages_for(batch, h_kv, max_pages_per_seq);
   a.n_chunk_slots = (max_pages_per_seq + a.chunk_pages - 1) / a.chunk_pages;
+  if (window > 0) {
+    // a windowed request walks at most its sink pages, the window's pages and one boundary
+    // page: the chunks are sized for that run, not for the table width (while the partials
+    // still fit the workspace sized for the table width)
+    const long long run =
+        ((long long)sink_tokens + desc->page_size - 1) / desc->page_size +
+        ((long long)window + desc->page_size - 1) / desc->page_size + 1;
+    const int walk = (int)std::min<long long>(max_pages_per_seq, run);
+    int chunk = chunk_pages_for(batch, h_kv, walk);
+    while ((walk + chunk - 1) / chunk > a.n_chunk_slots) chunk *= 2;
+    a.chunk_pages = chunk;
+    a.n_chunk_slots = (walk + chunk - 1) / chunk;
+  }
   a.chunk_grid = a.n_chunk_slots;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.window = window;
