@@ -832,7 +832,10 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": dict(config_of(w), parallelism="host cores"),
+            "config": dict(config_of(w), parallelism="host cores",
+                           l2="not applicable: the oracle runs on the host cores",
+                           step="fp64 oracle paged decode over each sampled request's cached and "
+                                "new tokens (the append is its host scatter, untimed)"),
             "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": threads,
                              "kind": "oracle", "sample": sample, "cpu": _cpu_model()},
             "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
