@@ -314,7 +314,7 @@ int pkv_incref(pkv_allocator* a, const int32_t* ids, int32_t n);
 int pkv_decref(pkv_allocator* a, const int32_t* ids, int32_t n);
 /* Copy-on-write before writing position `position` of a request whose pages are row[0..n)
  * (host array): if the page holding it is shared (reference count > 1) it is replaced in row by
- * a newly allocated page, the old page loses this request's reference, and *copy_src/*copy_dst
+ * a newly allocated page, the old page loses this request's reference, and *copy_src and *copy_dst
  * name the page contents to copy (pkv_copy_pages) before the write; otherwise both are -1
  * (also when the position starts a page the request does not have yet). */
 int pkv_cow_page(pkv_allocator* a, int32_t* row, int32_t n, int64_t position, int32_t page_size,
@@ -322,6 +322,58 @@ int pkv_cow_page(pkv_allocator* a, int32_t* row, int32_t n, int64_t position, in
 int32_t pkv_num_free(const pkv_allocator* a);
 /* Reference count of a page, or -1 for an id out of range. */
 int32_t pkv_refcount(const pkv_allocator* a, int32_t id);
+
+/*
+ * Request page tables over an allocator (section 4: a page table per request; section 5:
+ * requests join and leave every step; section 6 and the "KV Cache" glossary: prefixes, parallel
+ * samples and beams share pages; section 8: pages outside a sliding window are released).
+ * A request (any int64 id) is a row of page ids (-1 where a page was released) and a token
+ * count; every page in a row holds one allocator reference. Host only; not thread-safe. The
+ * table does not own the allocator, which must outlive it; destroying the table drops its
+ * rows without touching the allocator (free the requests first to return their pages).
+ * Calls that fail with PKV_EINVAL or PKV_ENOPAGES change nothing.
+ */
+typedef struct pkv_seq_table pkv_seq_table;
+int pkv_seq_table_create(pkv_allocator* a, int32_t page_size, pkv_seq_table** out);
+void pkv_seq_table_destroy(pkv_seq_table* t);
+/* A new request, empty or starting on n_shared whole pages holding its first shared_len =
+ * n_shared * page_size tokens (a cached prefix; one more reference on each). */
+int pkv_seq_add(pkv_seq_table* t, int64_t rid, const int32_t* shared_pages, int32_t n_shared,
+                int64_t shared_len);
+/* new_rids[i] becomes a copy of src_rids[i] (same pages, one more reference on each, same
+ * length), in order: a parent may be a request forked earlier in the list. */
+int pkv_seq_fork(pkv_seq_table* t, const int64_t* src_rids, const int64_t* new_rids, int32_t n);
+/* Drops the listed requests and their page references. */
+int pkv_seq_free(pkv_seq_table* t, const int64_t* rids, int32_t n);
+/*
+ * Grows request rids[i] by counts[i] tokens, in order. For a request with counts[i] > 0 whose
+ * next position falls in a shared page, the page is first replaced by a fresh one
+ * (pkv_cow_page) and the pair (old, new) is appended to copy_src/copy_dst (host, room for n
+ * pairs; the caller copies the contents on the device, pkv_copy_pages, before the writes);
+ * *n_copies receives their number. Then the pages the new length needs are allocated. The
+ * slots of the new positions, request by request, go to slots_out (host, sum of counts):
+ * page * page_size + position % page_size. PKV_ENOPAGES (nothing changed) when the free pages
+ * cannot cover every copy and page of the batch; PKV_EINVAL for an unknown or repeated id, a
+ * negative count or a write into a released page.
+ */
+int pkv_seq_reserve(pkv_seq_table* t, const int64_t* rids, const int32_t* counts, int32_t n,
+                    int64_t* slots_out, int32_t* copy_src, int32_t* copy_dst, int32_t* n_copies);
+/* Block-table rows (int32 [n][width], unused columns 0) and token counts (int32 [n]) of the
+ * listed requests into host arrays (either may be NULL). PKV_EINVAL if a row does not fit. */
+int pkv_seq_tables(const pkv_seq_table* t, const int64_t* rids, int32_t n, int32_t width,
+                   int32_t* block_tables_out, int32_t* context_lens_out);
+/* Releases every page of the request whose positions all lie at or past sink_tokens, before
+ * the last `window` positions and before the newest token (window 0: none); their row entries
+ * become -1. *released (may be NULL) receives the count. */
+int pkv_seq_release_outside_window(pkv_seq_table* t, int64_t rid, int64_t window,
+                                   int64_t sink_tokens, int32_t* released);
+/* Token count of a request, or -1 if unknown. */
+int64_t pkv_seq_len(const pkv_seq_table* t, int64_t rid);
+/* Row length of a request (or -1 if unknown); copies up to cap entries into pages_out. */
+int32_t pkv_seq_pages(const pkv_seq_table* t, int64_t rid, int32_t* pages_out, int32_t cap);
+/* Number of requests; pkv_seq_ids copies up to cap ids (any order) and returns the number. */
+int32_t pkv_seq_count(const pkv_seq_table* t);
+int32_t pkv_seq_ids(const pkv_seq_table* t, int64_t* rids_out, int32_t cap);
 
 /* ---- decode step from host memory ---------------------------------------------------------- */
 

@@ -107,6 +107,19 @@ def lib():
                                         ctypes.POINTER(i32)]),
         "pkv_copy_pages": (ctypes.c_int, [vp, vp, D, vp, vp, i32, vp]),
         "pkv_refcount": (i32, [vp, i32]),
+        "pkv_seq_table_create": (ctypes.c_int, [vp, i32, ctypes.POINTER(vp)]),
+        "pkv_seq_table_destroy": (None, [vp]),
+        "pkv_seq_add": (ctypes.c_int, [vp, i64, vp, i32, i64]),
+        "pkv_seq_fork": (ctypes.c_int, [vp, vp, vp, i32]),
+        "pkv_seq_free": (ctypes.c_int, [vp, vp, i32]),
+        "pkv_seq_reserve": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, vp, ctypes.POINTER(i32)]),
+        "pkv_seq_tables": (ctypes.c_int, [vp, vp, i32, i32, vp, vp]),
+        "pkv_seq_release_outside_window": (ctypes.c_int, [vp, i64, i64, i64,
+                                                          ctypes.POINTER(i32)]),
+        "pkv_seq_len": (i64, [vp, i64]),
+        "pkv_seq_pages": (i32, [vp, i64, vp, i32]),
+        "pkv_seq_count": (i32, [vp]),
+        "pkv_seq_ids": (i32, [vp, vp, i32]),
         "pkv_prefix_cache_create": (ctypes.c_int, [vp, i32, ctypes.POINTER(vp)]),
         "pkv_prefix_cache_destroy": (None, [vp]),
         "pkv_prefix_lookup": (ctypes.c_int, [vp, i64, vp, i64, vp, i32, ctypes.POINTER(i32)]),
@@ -664,6 +677,111 @@ class PageAllocator:
                                   int(page_size), ctypes.byref(src), ctypes.byref(dst)))
         row[lp] = int(one[0])
         return None if src.value < 0 else (int(src.value), int(dst.value))
+
+
+def _ids(rids) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(list(rids) if not isinstance(rids, np.ndarray)
+                                           else rids, dtype=np.int64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data if a.size else None
+
+
+class SeqTable:
+    """Request page tables over a PageAllocator (pkv_seq_*): rows of page ids and token counts,
+    fork / free / reserve (with copy-on-write) / window release, all in the C library."""
+
+    def __init__(self, allocator: PageAllocator, page_size: int = 16):
+        self._alloc = allocator  # the allocator outlives the table
+        self._h = ctypes.c_void_p()
+        _check(lib().pkv_seq_table_create(allocator._h, int(page_size), ctypes.byref(self._h)))
+        self.page_size = int(page_size)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.pkv_seq_table_destroy(h)
+            self._h = None
+
+    def add(self, rid: int, shared_pages=None, shared_len: int = 0):
+        p = np.ascontiguousarray(np.asarray([] if shared_pages is None else list(shared_pages),
+                                            dtype=np.int32))
+        _check(lib().pkv_seq_add(self._h, int(rid), _ptr(p), p.size, int(shared_len)))
+
+    def fork(self, src_rids, new_rids):
+        s, n = _ids(src_rids), _ids(new_rids)
+        if s.size != n.size:
+            raise PkvError(-1, "src_rids and new_rids differ in length")
+        _check(lib().pkv_seq_fork(self._h, _ptr(s), _ptr(n), s.size))
+
+    def free(self, rids):
+        r = _ids(rids)
+        _check(lib().pkv_seq_free(self._h, _ptr(r), r.size))
+
+    def reserve(self, rids, counts):
+        """Returns (int64 slots of the new positions, list of (src, dst) pages to copy)."""
+        r = _ids(rids)
+        c = np.ascontiguousarray(np.asarray(list(counts), dtype=np.int32))
+        if r.size != c.size:
+            raise PkvError(-1, "rids and counts differ in length")
+        slots = np.empty(int(c.sum()) if c.size else 0, dtype=np.int64)
+        src = np.empty(max(r.size, 1), dtype=np.int32)
+        dst = np.empty_like(src)
+        nc = ctypes.c_int32(0)
+        _check(lib().pkv_seq_reserve(self._h, _ptr(r), _ptr(c), r.size, _ptr(slots),
+                                     src.ctypes.data, dst.ctypes.data, ctypes.byref(nc)))
+        return slots, [(int(src[i]), int(dst[i])) for i in range(nc.value)]
+
+    def tables(self, rids, width: int | None = None, out=None):
+        """Block-table rows int32 [n][width] of the requests (unused columns 0, released pages
+        -1); ``out`` (a contiguous int32 numpy array or CPU tensor) is filled in place."""
+        r = _ids(rids)
+        if width is None:
+            width = max([self.num_pages_of(x) for x in r.tolist()] + [1])
+        bt = np.empty((r.size, int(width)), dtype=np.int32) if out is None else out
+        bt_p = bt.data_ptr() if isinstance(bt, torch.Tensor) else bt.ctypes.data
+        _check(lib().pkv_seq_tables(self._h, _ptr(r), r.size, int(width),
+                                    bt_p if r.size else None, None))
+        return bt
+
+    def lengths(self, rids, out=None):
+        """Token counts (int32 [n]) of the requests; ``out`` is filled in place when given."""
+        r = _ids(rids)
+        cl = np.empty(r.size, dtype=np.int32) if out is None else out
+        cl_p = cl.data_ptr() if isinstance(cl, torch.Tensor) else cl.ctypes.data
+        _check(lib().pkv_seq_tables(self._h, _ptr(r), r.size, 0, None, cl_p if r.size else None))
+        return cl
+
+    def release_outside_window(self, rid: int, window: int, sink_tokens: int = 0) -> int:
+        n = ctypes.c_int32(0)
+        _check(lib().pkv_seq_release_outside_window(self._h, int(rid), int(window),
+                                                    int(sink_tokens), ctypes.byref(n)))
+        return int(n.value)
+
+    def length(self, rid: int) -> int:
+        n = int(lib().pkv_seq_len(self._h, int(rid)))
+        if n < 0:
+            raise KeyError(rid)
+        return n
+
+    def num_pages_of(self, rid: int) -> int:
+        n = int(lib().pkv_seq_pages(self._h, int(rid), None, 0))
+        if n < 0:
+            raise KeyError(rid)
+        return n
+
+    def pages(self, rid: int) -> list:
+        n = self.num_pages_of(rid)
+        out = np.empty(max(n, 1), dtype=np.int32)
+        lib().pkv_seq_pages(self._h, int(rid), out.ctypes.data, n)
+        return [int(x) for x in out[:n]]
+
+    def ids(self) -> list:
+        n = int(lib().pkv_seq_count(self._h))
+        out = np.empty(max(n, 1), dtype=np.int64)
+        m = int(lib().pkv_seq_ids(self._h, out.ctypes.data, n))
+        return [int(x) for x in out[:min(n, m)]]
 
 
 class PrefixCache:
