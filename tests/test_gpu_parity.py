@@ -359,6 +359,35 @@ def test_host_step_equals_device_step(kv):
     assert hs.h2d_bytes >= (b.q.numel() + 2 * b.k_new.numel()) * 2
 
 
+def test_host_step_graph_replays_each_steps_inputs():
+    # the captured host step re-reads the pinned inputs on every replay: new queries each
+    # step give the same bytes as the step made call by call, and differ between steps
+    w = workloads.custom("hoststep_graph", 7301, 5, 8, 2, 128, "bf16", "bf16",
+                         [40, 3, 700, 17, 64])
+    b = Scenario(w)
+    steps = [pkv.HostStep(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                          b.block_tables.shape[1], use_graph=g) for g in (True, False)]
+    for hs in steps:
+        hs.k_new_host.copy_(b.k_new.cpu())
+        hs.v_new_host.copy_(b.v_new.cpu())
+        hs.block_tables_host.copy_(b.block_tables.cpu())
+        hs.context_lens_host.copy_(b.context_lens.cpu())
+    prev = None
+    for it in range(3):
+        q = torch.randn(b.q.shape, generator=torch.Generator().manual_seed(it)).to(b.q.dtype)
+        outs = []
+        for hs in steps:
+            hs.q_host.copy_(q)
+            hs.step(b.cache.k, b.cache.v, w.scale, workspace=b.workspace)
+            torch.cuda.synchronize()
+            outs.append(hs.out_host.clone())
+        assert pkv.device_error() == 0
+        assert torch.equal(outs[0], outs[1])
+        if prev is not None:
+            assert not torch.equal(prev, outs[0])
+        prev = outs[0]
+
+
 @pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3", "int8"])
 @pytest.mark.parametrize("wpr", [True, False])
 def test_short_single_chunk_batches_both_ways(kv, wpr):
