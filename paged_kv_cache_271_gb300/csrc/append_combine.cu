@@ -202,10 +202,35 @@ template <int D, int CB>
 __device__ __forceinline__ void merge_run(const float* ml, const float* acc, int lo, int hi,
                                           int lane, float& M, float& Lw, float (&A)[D / 32]) {
   constexpr int DL = D / 32;
+  auto load_batch = [&](int c0, int nc, int cb, float (&v)[CB][DL]) {  // values of CB chunks
+#pragma unroll
+    for (int u = 0; u < CB; ++u) {
+      const int c = c0 + cb + u;
+      if (cb + u < nc) {
+        if constexpr (DL == 4) {
+          const float4 x = *reinterpret_cast<const float4*>(acc + (size_t)c * D);
+          v[u][0] = x.x;
+          v[u][1] = x.y;
+          v[u][2] = x.z;
+          v[u][3] = x.w;
+        } else {
+          const float2 x = *reinterpret_cast<const float2*>(acc + (size_t)c * D);
+          v[u][0] = x.x;
+          v[u][1] = x.y;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < DL; ++k) v[u][k] = 0.f;
+      }
+    }
+  };
   for (int c0 = lo; c0 < hi; c0 += 32) {  // 32 chunks per round of (max, sum) pairs
     const int nc = min(32, hi - c0);
     const float2 p = lane < nc ? *reinterpret_cast<const float2*>(ml + 2 * (c0 + lane))
                                : make_float2(-INFINITY, 0.f);
+    // the first CB chunks' values do not depend on the pairs: load them together
+    float v[CB][DL];
+    load_batch(c0, nc, 0, v);
     float mr = p.x;
 #pragma unroll
     for (int o = 16; o >= 1; o /= 2) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
@@ -221,27 +246,7 @@ __device__ __forceinline__ void merge_run(const float* ml, const float* acc, int
     for (int k = 0; k < DL; ++k) A[k] *= rescale;
     M = Mn;
     for (int cb = 0; cb < nc; cb += CB) {
-      float v[CB][DL];
-#pragma unroll
-      for (int u = 0; u < CB; ++u) {  // loads of CB chunks in flight together
-        const int c = c0 + cb + u;
-        if (cb + u < nc) {
-          if constexpr (DL == 4) {
-            const float4 x = *reinterpret_cast<const float4*>(acc + (size_t)c * D);
-            v[u][0] = x.x;
-            v[u][1] = x.y;
-            v[u][2] = x.z;
-            v[u][3] = x.w;
-          } else {
-            const float2 x = *reinterpret_cast<const float2*>(acc + (size_t)c * D);
-            v[u][0] = x.x;
-            v[u][1] = x.y;
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < DL; ++k) v[u][k] = 0.f;
-        }
-      }
+      if (cb > 0) load_batch(c0, nc, cb, v);  // CB chunks' loads in flight together
 #pragma unroll
       for (int u = 0; u < CB; ++u) {
         const float wu = __shfl_sync(0xffffffffu, w, (cb + u) & 31);
