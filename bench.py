@@ -366,13 +366,25 @@ def cpu_baseline(w, budget_s=12.0):
     b1, t1 = oracle_sample(w, 1)
     n = int(min(w.batch, max(1, budget_s / max(t1, 1e-3))))
     byts, t = oracle_sample(w, n) if n > 1 else (b1, t1)
+    bs, ts = oracle_sample(w, 1, n_threads=1)
     return {"value": byts / t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": "fp64 C oracle (gather through page tables + textbook softmax), first %d "
                       "of %d requests, all 32 heads, %.1f s" % (n, w.batch, t),
+            "single_thread": {"value": bs / ts / 1e9, "unit": "GB/s",
+                              "sample": "first request, all heads, 1 thread, %.2f s" % ts},
             "cpu": _cpu_model()}
 
 
 def _cpu_model():
+    """The host CPU's model name (lscpu), else what /proc/cpuinfo names."""
+    try:
+        import subprocess
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
