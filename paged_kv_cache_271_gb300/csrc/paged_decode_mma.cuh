@@ -211,6 +211,22 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
   }
 }
 
+// K codes for the scores: as widen4, except that an INT8 code comes out as code + 1152 (the
+// subtraction is left out). Every score of a (request, query head) then carries the same
+// extra term 1152 * k_scale * sum(q), which the softmax cancels (a common shift of one row's
+// scores; every chunk of the row gets the same one, so the split merge cancels it too). The
+// biased values 1025..1279 are exact in f16 and the fp32 products and sums add only rounding.
+template <typename KV>
+__device__ __forceinline__ void widen4_scores(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  if constexpr (KV::code == PKV_INT8) {
+    const uint32_t x = w ^ 0x80808080u;
+    lo = __byte_perm(x, 0x6464u, 0x5140u);
+    hi = __byte_perm(x, 0x6464u, 0x5342u);
+  } else {
+    widen4<KV>(w, lo, hi);
+  }
+}
+
 // WU (warp per request): every request has a single chunk; warp w of CTA z takes request
 // NW z + w whole (its pages 0, 1, 2, ... through its own two ring stages) and writes its output
 // itself; the warps of a CTA only share the barrier set-up.
@@ -439,8 +455,8 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             uint32_t a0, a1, a2, a3;
-            widen4<KV>(w0[ks], a0, a2);
-            widen4<KV>(w8[ks], a1, a3);
+            widen4_scores<KV>(w0[ks], a0, a2);
+            widen4_scores<KV>(w8[ks], a1, a3);
             const int kp = 2 * h + (ks >> 1), half = ks & 1;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
