@@ -410,9 +410,9 @@ int pkv_paged_decode_step_packed(const void* host_in, void* dev_in, int32_t batc
  * The cascade decode computes the attention of every member's query heads over the group's
  * shared pages once per group -- the pages are read once for all members, and the members'
  * queries form a dense tensor-core contraction -- then over each member's own pages, and
- * merges the two (in the second kernel: a cascade decode launches no combine kernel) with the
- * split-decode rule (a softmax over a union of disjoint key sets from
- * the per-set maxima, sums and weighted values). The result is the same attention as
+ * merges the two with the split-decode rule (a softmax over a union of disjoint key sets from
+ * the per-set maxima, sums and weighted values): in the combine kernel, or in the own-page
+ * kernel (see pkv_cascade_set_overlap). The result is the same attention as
  * pkv_paged_decode_attention over the same tables (rounding aside).
  *
  * Arrays are device memory unless noted; the bounds are host values that the arrays must
@@ -493,9 +493,13 @@ int pkv_cascade_decode_step(const void* q, int32_t dtype_q, int32_t batch, int32
 int pkv_decode_set_warp_per_request(int32_t on);
 
 /* Tuning: in a cascade decode on the tensor-core path, the own-page decode is launched as a
- * programmatic dependent of the prefix kernel (1, the default): it reads its own pages while
- * the prefix kernel runs and waits for that kernel only before it folds in the prefix
- * partials. 0 runs the two kernels one after the other. The results are the same. */
+ * programmatic dependent of the prefix kernel. 2 (the default): it writes each member's result
+ * as a partial and exits without waiting (one thread of its first CTA waits for the prefix
+ * kernel before exiting), the combine kernel merges prefix and own partials, and the tcgen05
+ * prefix kernel is sized for about half the SMs so that the two kernels share the GPU. 1: it
+ * waits for the prefix kernel before folding the prefix partials in itself (no combine).
+ * 0 runs the two kernels one after the other. The results agree within rounding (mode 2
+ * merges in another order). Process-wide; the workspace size depends on it. */
 int pkv_cascade_set_overlap(int32_t on);
 
 /* Tuning: pages per CTA of the prefix pass (0 = automatic). */

@@ -617,9 +617,11 @@ def decode_set_warp_per_request(on: bool):
     _check(lib().pkv_decode_set_warp_per_request(1 if on else 0))
 
 
-def cascade_set_overlap(on: bool):
-    """Cascade decode: run the own-page decode alongside the prefix kernel (default) or after it."""
-    _check(lib().pkv_cascade_set_overlap(1 if on else 0))
+def cascade_set_overlap(on):
+    """Cascade decode: run the own-page decode alongside the prefix kernel with the fold left
+    to the combine kernel (2, the default), alongside it folding itself (True or 1), or after
+    it (False or 0)."""
+    _check(lib().pkv_cascade_set_overlap(int(on)))
 
 
 def decode_set_chunk_pages(pages: int):

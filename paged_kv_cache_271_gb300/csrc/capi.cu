@@ -86,7 +86,9 @@ std::atomic<int> g_chunk_override{0};
 // (0: always the combine kernel, the default -- measured faster on every workload tried).
 std::atomic<int> g_merge_in_place_max{0};
 std::atomic<int> g_kernel_choice{0};  // 0 automatic, 1 CUDA cores, 2 tensor cores
-std::atomic<int> g_cascade_overlap{1};  // 1: own-page decode overlaps the prefix kernel
+// 0: prefix kernel, then own-page decode; 1: the own-page decode overlaps the prefix kernel and
+// folds its partials in; 2: overlaps it and leaves the fold to the combine kernel
+std::atomic<int> g_cascade_overlap{2};
 std::atomic<int> g_warp_units{1};     // 1: one warp per request for short single-chunk runs
 
 // ---- TMA tensor maps of the pools (for the tensor-core decode) -------------------------------
@@ -223,7 +225,11 @@ int prefix_chunk_pages_for(int n_groups, int h_kv, int group, int max_members, i
   if (max_prefix < 1) return 1;
   const bool tc = prefix_on_tcgen05();
   const int rows = tc ? kCascadeTcRows : kCascadeRows;
-  const int wave = tc ? kCascadeTcWaveCtas : kCascadeWaveCtas;
+  // with the fold left to the combine, the tcgen05 prefix kernel takes about half the SMs and
+  // the own-page decode runs on the rest meanwhile (prefix sharing, batch 128: two chunks,
+  // 38.1 us a step, against 41.1 us with the prefix kernel on every SM)
+  const int wave = tc ? (g_cascade_overlap.load() == 2 ? kCascadeTcWaveCtas / 2 : kCascadeTcWaveCtas)
+                      : kCascadeWaveCtas;
   const int min_pages = tc ? 4 : 2;
   const long long tiles = ((long long)max_members * group + rows - 1) / rows;
   const long long units = (long long)n_groups * h_kv * tiles;
@@ -300,8 +306,8 @@ int pkv_decode_set_warp_per_request(int32_t on) {
 }
 
 int pkv_cascade_set_overlap(int32_t on) {
-  if (on != 0 && on != 1)
-    return set_error(PKV_EINVAL, "pkv_cascade_set_overlap: %d is not 0 or 1", on);
+  if (on < 0 || on > 2)
+    return set_error(PKV_EINVAL, "pkv_cascade_set_overlap: %d is not 0, 1 or 2", on);
   g_cascade_overlap.store(on);
   return PKV_OK;
 }
@@ -457,9 +463,10 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
     a.ws_ml = reinterpret_cast<float*>(ws + align256(rows * D * sizeof(float)));
     a.counters = reinterpret_cast<int*>(ws + align256(rows * D * sizeof(float)) +
                                         align256(rows * 2 * sizeof(float)));
-    // few chunks per sequence: the last CTA of each group merges them (no combine kernel)
-    // A cascade decode always merges in the decode kernel: a request's one own chunk folds in
-    // its prefix partials, several own chunks merge in place.
+    // few chunks per sequence: the last CTA of each group merges them (no combine kernel).
+    // A cascade decode that folds in the own-page kernel (overlap modes 0 and 1) always merges
+    // there: a request's one own chunk folds in its prefix partials, several own chunks merge
+    // in place; with the fold left to the combine (mode 2) this is undone below.
     a.merge_in_place = cascade || a.n_chunk_slots <= g_merge_in_place_max.load() ? 1 : 0;
   }
   if (k_new) {
@@ -488,6 +495,8 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
   // (one chunk column: no request splits, so no merge of chunk partials can arise)
   a.warp_units = use_mma && a.chunk_grid == 1 && a.chunk_pages <= 16 && g_warp_units.load() != 0;
   a.prefix_dep = cascade && use_mma && g_cascade_overlap.load() != 0 ? 1 : 0;
+  a.defer_fold = a.prefix_dep && g_cascade_overlap.load() == 2 ? 1 : 0;
+  if (a.defer_fold) a.merge_in_place = 0;  // every member's chunks go to the combine
   CUtensorMap tk, tv;
   if (use_mma || cascade) {
     int rk = 2, rv = 2;

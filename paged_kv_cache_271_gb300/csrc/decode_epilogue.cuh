@@ -23,7 +23,9 @@ __device__ __forceinline__ void decode_epilogue(const DecodeArgs& a, int b, int 
                                                 const float* red_m, const float* red_l,
                                                 float vs) {
   __shared__ int s_last;
-  const bool direct = n_chunks <= 1;  // this CTA finishes the request
+  // this CTA finishes the request (with a deferred fold, a cascade member's prefix partials
+  // are merged by the combine kernel instead)
+  const bool direct = n_chunks <= 1 && !(a.defer_fold && slot0 > 0);
   for (int e = threadIdx.x; e < G * D; e += NTHR) {
     const int g = e / D, i = e % D;
     float M = -INFINITY;
@@ -136,6 +138,19 @@ __device__ __forceinline__ void decode_epilogue_warp(const DecodeArgs& a, int b,
     A[g][1] = live ? v.y * vs : 0.f;
     A[g][2] = live ? v.z * vs : 0.f;
     A[g][3] = live ? v.w * vs : 0.f;
+  }
+  if (a.defer_fold && slot0 > 0) {  // the own pages' partial, at slot slot0 (the combine merges)
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const size_t part = ((size_t)b * a.h_q + j * G + g) * a.n_chunk_slots + slot0;
+      *reinterpret_cast<float4*>(a.ws_acc + part * D + i0) =
+          make_float4(A[g][0], A[g][1], A[g][2], A[g][3]);
+      if (lane == 0) {
+        a.ws_ml[part * 2] = M[g];
+        a.ws_ml[part * 2 + 1] = L[g];
+      }
+    }
+    return;
   }
   constexpr int KB = G <= 4 ? 4 : (G <= 8 ? 2 : 1);  // slots whose loads go out together
   for (int k0 = 0; k0 < slot0; k0 += KB) {  // fold in the prefix partials

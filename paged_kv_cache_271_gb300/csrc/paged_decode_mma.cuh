@@ -631,7 +631,7 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
   }
   const float vs = F8 ? a.v_scales[j] : 1.f;
   // a dependent launch of the prefix kernel: its partials are complete and visible past here
-  if (a.prefix_dep) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (a.prefix_dep && !a.defer_fold) asm volatile("griddepcontrol.wait;" ::: "memory");
   if constexpr (WU) {
     __syncwarp();
     decode_epilogue_warp<TQ, D, G>(a, b, j, plan.slot0, red_acc + warp * G * D, red_m + warp * G,
@@ -641,6 +641,10 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
     decode_epilogue<TQ, D, G, NW, S::kThreads>(a, b, j, c, n_chunks, plan.slot0, red_acc,
                                                red_m, red_l, vs);
   }
+  // deferred fold: the combine waits for this grid only, so this grid must not complete before
+  // the prefix kernel; one thread of the first CTA (always active) waits for it, at its end
+  if (a.defer_fold && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <typename KV, typename TQ, int D, int G, bool WU>

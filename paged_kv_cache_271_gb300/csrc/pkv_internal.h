@@ -52,6 +52,11 @@ struct DecodeArgs {
   // it reads its own pages while the prefix kernel runs and waits for that grid
   // (griddepcontrol.wait) before it reads any prefix partial
   int prefix_dep;
+  // 1 (with prefix_dep): a cascade member's own chunks are written as partials (slots slot0 ..)
+  // and the combine kernel merges them with the prefix partials; one thread of the decode
+  // grid's first CTA waits for the prefix grid before it exits, so the decode grid -- which the
+  // combine waits for -- cannot complete before the prefix kernel
+  int defer_fold;
 };
 
 // Query rows ((member, query head) pairs) per CTA of the cascade prefix kernel, and the CTAs

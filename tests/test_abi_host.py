@@ -400,10 +400,10 @@ def test_cascade_argument_errors_are_caught_on_the_host():
                              np.zeros(0, np.int32), 0, 0)
     assert pkv.cascade_workspace_size(2, 8, 4, 128, 600, none) == plain
     # tuning switches reject values outside their range and keep their setting
-    assert L.pkv_cascade_set_overlap(2) == -1
+    assert L.pkv_cascade_set_overlap(3) == -1
     assert L.pkv_cascade_set_prefix_kernel(3) == -1
     assert L.pkv_decode_set_warp_per_request(-1) == -1
-    pkv.cascade_set_overlap(True)
+    pkv.cascade_set_overlap(2)
 
 
 def test_packed_step_layout():

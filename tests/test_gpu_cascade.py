@@ -37,6 +37,15 @@ def _case(G, h_kv=2, seed=11, groups=((5, 7, 1, 40), (2, 3, 1, 20)), singles=((1
                                    h_kv, 128, list(groups), list(singles))
 
 
+@pytest.fixture(autouse=True, params=[1, 2], ids=["fold_in_decode", "fold_in_combine"])
+def overlap_mode(request):
+    # the own-page decode alongside the prefix kernel, folding the prefix partials itself (1)
+    # or leaving them to the combine kernel (2)
+    pkv.cascade_set_overlap(request.param)
+    yield request.param
+    pkv.cascade_set_overlap(2)
+
+
 @pytest.fixture(params=[1, 2], ids=["prefix_mma_sync", "prefix_tcgen05"])
 def prefix_kernel(request):
     pkv.cascade_set_prefix_kernel(request.param)
@@ -121,16 +130,18 @@ def test_cascade_overlap_on_and_off_agree(own_pages, prefix_kernel):
     pkv.device_error()
     outs = []
     try:
-        for on in (False, True):
-            pkv.cascade_set_overlap(on)
+        for mode in (0, 1, 2):
+            pkv.cascade_set_overlap(mode)
             outs.append(_cascade(sc, groups).clone())
             torch.cuda.synchronize()
             _check_no_error()
     finally:
-        pkv.cascade_set_overlap(True)
-    assert torch.equal(outs[0], outs[1])
-    err = np.abs(outs[1].float().cpu().numpy() - oracle_groups_expected(w)).max()
-    assert err < TOL, err
+        pkv.cascade_set_overlap(2)
+    assert torch.equal(outs[0], outs[1])  # the same kernels in the same order
+    ref = oracle_groups_expected(w)
+    for o in outs[1:]:  # (mode 2 merges the same partials in another order)
+        err = np.abs(o.float().cpu().numpy() - ref).max()
+        assert err < TOL, err
 
 
 def test_cascade_with_empty_suffix_and_no_groups(prefix_kernel):
