@@ -6,7 +6,7 @@
 // softmax attention over those pages. Here the two contractions run as tcgen05 MMAs with the
 // accumulators in tensor memory:
 //
-//  * a copy warp (lane 0) streams 64-token tiles (4 pages) of K and V into a 4-stage ring with
+//  * a copy warp (lane 0) streams 64-token tiles (4 pages) of K and V into a 5-stage ring with
 //    2-D TMA copies (128-byte swizzle), refilling a stage as soon as the P V of its tile is
 //    done; an MMA warp (lane 0) issues the MMAs:
 //      S = Q K^T   M = 128 rows, N = 64 tokens, K = 128 dims  (8 MMAs of K = 16), S in TMEM;
@@ -47,7 +47,7 @@ constexpr int kTcCopyWarp = kTcSoftWarps + 1;            // issues the TMA copie
 constexpr int kTcThreads = 32 * (kTcSoftWarps + 2);
 constexpr int kTcTok = 64;                               // tokens per tile
 constexpr int kTcPages = kTcTok / kPageSize;             // pages per tile
-constexpr int kTcStages = 4;
+constexpr int kTcStages = 5;
 constexpr int kTcQBytes = kTcRows * 256;                 // Q: 128 rows x 128 bf16
 constexpr int kTcKV = kTcTok * 256;                      // K (or V) of one tile
 constexpr int kTcStageBytes = 2 * kTcKV;
@@ -56,6 +56,8 @@ constexpr int kTcOffStage = kTcQBytes;
 constexpr int kTcOffP = kTcOffStage + kTcStages * kTcStageBytes;
 constexpr int kTcOffBar = kTcOffP + 2 * kTcPBytes;
 constexpr int kTcSmem = 1024 + kTcOffBar + 256;
+static_assert(kTcSmem <= 227 * 1024, "shared memory of one CTA");
+static_assert(8 * (2 * kTcStages + 3 + 2 + 2) + 4 * kTcStages + 4 <= 256, "barrier area");
 constexpr int kTcSBufs = 3;                              // S buffers in TMEM
 constexpr uint32_t kTcTmemCols = 512;                    // O: 128 columns, S: 3 x 64
 constexpr float kTcLazyLog2 = 8.f;
