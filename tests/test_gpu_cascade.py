@@ -144,6 +144,35 @@ def test_cascade_overlap_on_and_off_agree(own_pages, prefix_kernel):
         assert err < TOL, err
 
 
+def test_cascade_host_step_equals_device_step():
+    # the step from host memory (queries, new rows, tables and lengths packed in one pinned
+    # buffer, the groups found on the host): same output and pool bytes as the device step
+    w = _case(4, h_kv=4, seed=15)
+    a = GroupScenario(w)
+    groups = pkv.cascade_groups(a.bt_host, a.cl_host).to(a.q.device)
+    pkv.device_error()
+    out_a = _cascade(a, groups, step=True).clone()
+    b = GroupScenario(w)
+    hs = pkv.HostStep(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, b.block_tables.shape[1])
+    hs.q_host.copy_(b.q.cpu())
+    hs.k_new_host.copy_(b.k_new.cpu())
+    hs.v_new_host.copy_(b.v_new.cpu())
+    hs.block_tables_host.copy_(b.block_tables.cpu())
+    hs.context_lens_host.copy_(b.context_lens.cpu())
+    g_host = pkv.cascade_groups(hs.block_tables_host.numpy(), hs.context_lens_host.numpy())
+    ws = torch.zeros(pkv.cascade_workspace_size(w.batch, w.num_q_heads, w.num_kv_heads,
+                                                w.head_dim, b.block_tables.shape[1], g_host),
+                     dtype=torch.uint8, device=b.q.device)
+    out_b = hs.step(b.cache.k, b.cache.v, w.scale, workspace=ws, groups=g_host.to(b.q.device))
+    torch.cuda.synchronize()
+    _check_no_error()
+    assert torch.equal(out_a.cpu(), out_b)
+    assert torch.equal(a.cache.k.view(torch.uint8), b.cache.k.view(torch.uint8))
+    assert torch.equal(a.cache.v.view(torch.uint8), b.cache.v.view(torch.uint8))
+    err = np.abs(out_b.float().numpy() - oracle_groups_expected(w)).max()
+    assert err < TOL, err
+
+
 def test_cascade_with_empty_suffix_and_no_groups(prefix_kernel):
     # a member whose context ends exactly at the end of the shared pages (attention only):
     # its own part is empty and the merge takes the prefix partials alone
