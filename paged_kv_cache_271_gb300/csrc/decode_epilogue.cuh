@@ -1,9 +1,10 @@
 // End of a decode CTA, shared by the CUDA-core and tensor-core kernels: the CTA's warps have
 // left their (running max, sum, weighted values) per head in shared memory; merge them, then
-//  * the request's only chunk: write out = acc / l -- in a cascade decode after merging in the
-//    partials of the request's shared prefix (chunk slots 0 .. slot0 - 1, written by the
-//    prefix kernel before this launch);
-//  * one of several chunks: write this chunk's partial (m, l, acc) to chunk slot slot0 + c;
+//  * the request's only chunk: write out = acc / l -- in a cascade decode that folds in the
+//    decode kernel, after merging in the partials of the request's shared prefix (chunk slots
+//    0 .. slot0 - 1, written by the prefix kernel);
+//  * one of several chunks, or a cascade member's chunk when the combine kernel folds: write
+//    this chunk's partial (m, l, acc) to chunk slot slot0 + c;
 //    when the call merges in place, the last CTA of the (request, KV head) to finish -- found
 //    with a counter in the workspace -- merges every slot of the group in slot order and
 //    writes out, then resets the counter to 0 for the next call. Otherwise a separate combine

@@ -8,10 +8,11 @@
 // Cascade decode (a request in a group that shares its first P logical pages with the other
 // members, "KV cache and PagedAttention" section 6): the prefix kernel covers those P pages
 // once for the whole group and writes its partials to slots 0 .. ceil(P / prefix_chunk_pages)
-// - 1 of every member; the decode kernel then reads pages P .. of the request only. With one
-// chunk of its own (possibly empty) its CTA merges the prefix partials in and writes the
-// output; with several, each chunk writes a partial after the prefix's and the last to finish
-// merges them all.
+// - 1 of every member; the decode kernel then reads pages P .. of the request only and its
+// chunks write their partials after the prefix's (slots slot0 ..). Who merges: by default the
+// combine kernel, which merges all of a request's slots; or (overlap modes 0 and 1) the decode
+// kernel itself -- a single own chunk (possibly empty) folds the prefix partials in and writes
+// the output, and with several the last chunk to finish merges them all.
 #pragma once
 
 #include "pkv_device.cuh"

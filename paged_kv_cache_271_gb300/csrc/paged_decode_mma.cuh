@@ -8,9 +8,12 @@
 // per-element widening and FMAs) and the kernel is issue-bound; here it is ~16 tensor-core
 // MMAs plus a few dozen other instructions per page.
 //
-//  * Staging: a 2-D TMA tensor copy (128-byte swizzle) moves each (page, KV head) tile of K
-//    and of V into a warp-owned ring stage, completing on the stage's mbarrier. The swizzle
-//    makes the fragment loads below free of shared-memory bank conflicts.
+//  * Staging: TMA tensor copies (128-byte swizzle) move each (page, KV head) tile of K and of
+//    V into a warp-owned ring stage, completing on the stage's mbarrier: a bf16 pool is viewed
+//    as a 3-D tensor [2 halves][rows][64 dims], so one box moves a whole 4 KiB tile as two
+//    swizzled blocks; FP8/INT8 rows of 128 bytes take one 2-D box. The swizzle makes the
+//    fragment loads below free of shared-memory bank conflicts. Each warp reads the page ids
+//    of its pages 32 at a time (one per lane) ahead of their copies.
 //  * Scores: S^T = K Q^T with mma.m16n8k16 -- the page's 16 tokens are M, the group's query
 //    heads (padded to 8 per n-tile) are N, head_dim is K. The k order inside each 16-wide
 //    k-step is permuted so a lane's A fragment for two k-steps is one 16-byte load of its row;
@@ -20,10 +23,13 @@
 //  * Values: O^T = V^T P^T with mma.m16n8k16 -- head_dim is M (8 m-tiles), heads are N, the
 //    page's tokens are K. V^T fragments come from ldmatrix.trans on the swizzled tile; P is
 //    rounded to the MMA input type and transposed through a 256-byte per-warp buffer.
-//  * FP8 / INT8: codes are widened exactly to f16 in registers (K fragments from 16-byte loads; V^T
-//    fragments by pairing the codes of consecutive tokens with byte permutes), the query is
-//    used in f16, and the MMAs run in f16 with fp32 accumulation; the K scale multiplies the
-//    scores and the V scale the output.
+//  * FP8 / INT8: codes are widened to f16 in registers, four per 32-bit word (K fragments
+//    from 16-byte loads; V^T fragments by pairing the codes of consecutive tokens with byte
+//    permutes), the query is used in f16, and the MMAs run in f16 with fp32 accumulation; the
+//    K scale multiplies the scores and the V scale the output. The widening is exact, except
+//    that INT8 K codes for the scores carry a bias that the softmax cancels (widen4_scores).
+//  * Fused append: the CTA that reads the page holding position ctx-1 writes this step's K/V
+//    row into the pool and into its staged copy of the page first (decode_epilogue.cuh).
 //  * Rows of the last page past the context may hold stale bytes (even NaN): their scores are
 //    set to -inf and their V rows to zero before the P.V product.
 #pragma once

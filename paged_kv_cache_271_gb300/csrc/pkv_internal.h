@@ -14,7 +14,7 @@ struct DecodeArgs {
   const void* v_cache;
   const int32_t* block_tables;
   const int32_t* context_lens;
-  const float* k_scales;  // FP8 cache only
+  const float* k_scales;  // FP8 or INT8 cache only
   const float* v_scales;
   float* ws_acc;  // [batch][h_q][n_chunk_slots][D] partial weighted values (split only)
   float* ws_ml;   // [batch][h_q][n_chunk_slots][2] partial (max, sum), log2 domain
@@ -33,8 +33,8 @@ struct DecodeArgs {
   int max_pages;      // block-table width
   int chunk_pages;    // pages per chunk (one CTA)
   int n_chunk_slots;  // partial slots per (request, query head)
-  int chunk_grid;     // decode grid.x = ceil(max_pages / chunk_pages) (n_chunk_slots without
-                      // the cascade prefix slots)
+  int chunk_grid;     // decode grid.x: chunk columns, ceil(pages a request can walk /
+                      // chunk_pages) (n_chunk_slots without the cascade prefix slots)
   float scale_log2;   // softmax scale * log2(e)
   int tma_rank;       // tensor maps of a 256-byte-row pool: 3 (one box per tile) or 2
   int warp_units;     // tensor-core decode: one warp per request (every request one chunk)
