@@ -809,32 +809,28 @@ def run_fork(args):
 def run_e2e(sc, args, dev, stream, flush, n_sets=1):
     """Same step through the public API from pinned host buffers (pkv.HostStep): per step one
     host->device copy of the step's inputs (queries, new K/V rows, page tables, context
-    lengths; for the cascade also this step's groups, found on the host from the tables) and
-    the device->host copy of the outputs sit inside the timed region, and the host waits for
-    the outputs before the next step."""
+    lengths; for the cascade also this step's groups, which the library finds on the host from
+    the tables inside the same call) and the device->host copy of the outputs sit inside the
+    timed region, and the host waits for the outputs before the next step."""
     import torch
     import paged_kv_cache_271_gb300 as pkv
+    cascade = sc.groups is not None
     hs = pkv.HostStep(sc.batch, sc.h_q, sc.h_kv, sc.d, sc.bt.shape[1], q_dtype=sc.q.dtype,
-                      new_dtype=sc.k_new.dtype, device=dev)
+                      new_dtype=sc.k_new.dtype, device=dev, cascade=cascade)
     hs.q_host.copy_(sc.q.cpu())
     hs.k_new_host.copy_(sc.k_new.cpu())
     hs.v_new_host.copy_(sc.v_new.cpu())
     hs.block_tables_host.copy_(sc.bt.cpu())
     hs.context_lens_host.copy_(sc.cl.cpu())
     ks, vs = sc.scales if sc.scales else (None, None)
-    bt_np, cl_np = hs.block_tables_host.numpy(), hs.context_lens_host.numpy()
-    groups_h2d = [0]
-    g_stage = torch.empty(4 * sc.batch + 2, dtype=torch.int32).pin_memory()
-    g_buf = torch.empty(4 * sc.batch + 2, dtype=torch.int32, device=dev)
 
     def one(i):
-        groups = None
-        if sc.groups is not None:  # this step's groups from its host tables, one H2D copy
-            groups = pkv.cascade_groups(bt_np, cl_np).to(dev, buffer=g_buf, staging=g_stage)
-            groups_h2d[0] = groups.nbytes
         k, v = sc.pools[i % n_sets] if hasattr(sc, "pools") else (sc.k, sc.v)
-        hs.step(k, v, sc.scale, k_scales=ks, v_scales=vs, workspace=sc.workspace, groups=groups,
-                window=getattr(sc, "window", 0), sink_tokens=getattr(sc, "sink", 0))
+        if cascade:  # this step's groups found by the library from the packed host tables
+            hs.cascade_step(k, v, sc.scale, sc.workspace)
+        else:
+            hs.step(k, v, sc.scale, k_scales=ks, v_scales=vs, workspace=sc.workspace,
+                    window=getattr(sc, "window", 0), sink_tokens=getattr(sc, "sink", 0))
 
     for i in range(max(3, args.warmup)):
         flush.zero_()
@@ -853,7 +849,7 @@ def run_e2e(sc, args, dev, stream, flush, n_sets=1):
         ends[i].synchronize()  # the result is on the host before the next step starts
     barrier()
     ms = float(np.mean([s.elapsed_time(e) for s, e in zip(starts, ends)]))
-    return {"ms_per_step": ms, "h2d": hs.h2d_bytes + groups_h2d[0], "d2h": hs.d2h_bytes}
+    return {"ms_per_step": ms, "h2d": hs.h2d_bytes, "d2h": hs.d2h_bytes}
 
 
 # ---- reference arm: the oracle as it stands --------------------------------------------------

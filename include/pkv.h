@@ -488,6 +488,36 @@ int pkv_cascade_decode_step(const void* q, int32_t dtype_q, int32_t batch, int32
                             const pkv_cascade_desc* groups, void* out, void* workspace,
                             size_t workspace_bytes, void* stream);
 
+/*
+ * The cascade decode step from host memory. Layout of the block (host_in, pinned, and its
+ * device twin dev_in, the same size): the five regions of pkv_packed_step_layout (offsets[0..4])
+ * filled by the caller, then five int32 regions this call fills (offsets[5..9]): group_of
+ * [batch], prefix_pages [batch], group_offsets [batch + 1], group_members [batch], own_start
+ * [batch], each 256-byte aligned; *total_bytes is the size of the block.
+ */
+int pkv_packed_cascade_layout(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t max_pages_per_seq, int32_t dtype_q,
+                              int32_t dtype_new, size_t* offsets, size_t* total_bytes);
+
+/*
+ * One call per step: groups the batch on the host from the block's page tables and context
+ * lengths (pkv_cascade_groups, at least 2 members and 1 shared page per group) into the block's
+ * group regions, copies the whole block into dev_in, runs pkv_cascade_decode_step on the device
+ * copies (a plain fused decode step when no group forms) and copies the output (out_dev) into
+ * out_host, all on `stream`. host_in is written (the group regions), so the caller
+ * synchronises before rewriting it or reading out_host. The workspace must hold
+ * pkv_cascade_workspace_size for this step's groups: *workspace_needed (may be NULL) receives
+ * it, and a smaller workspace fails with PKV_EINVAL before anything is enqueued;
+ * *n_groups_out (may be NULL) receives the number of groups.
+ */
+int pkv_cascade_decode_step_packed(void* host_in, void* dev_in, int32_t batch,
+                                   int32_t num_q_heads, int32_t dtype_q, int32_t dtype_new,
+                                   void* k_cache, void* v_cache, const pkv_cache_desc* desc,
+                                   int32_t max_pages_per_seq, float scale, void* out_dev,
+                                   void* out_host, void* workspace, size_t workspace_bytes,
+                                   size_t* workspace_needed, int32_t* n_groups_out,
+                                   void* stream);
+
 /* Tuning: when every request of a tensor-core decode fits one chunk of at most 16 pages,
  * one warp serves each request (1, the default) or four warps share one (0). */
 int pkv_decode_set_warp_per_request(int32_t on);

@@ -131,6 +131,12 @@ def lib():
         "pkv_paged_decode_step_packed": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, vp, vp, D, i32,
                                                         f32, vp, vp, i32, i32, vp, vp, vp, sz,
                                                         vp]),
+        "pkv_packed_cascade_layout": (ctypes.c_int, [i32, i32, i32, i32, i32, i32, i32, vp,
+                                                     ctypes.POINTER(sz)]),
+        "pkv_cascade_decode_step_packed": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, vp, vp, D,
+                                                          i32, f32, vp, vp, vp, sz,
+                                                          ctypes.POINTER(sz), ctypes.POINTER(i32),
+                                                          vp]),
         "pkv_cascade_groups": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp,
                                               ctypes.POINTER(i32), ctypes.POINTER(i32),
                                               ctypes.POINTER(i32), ctypes.POINTER(i32), vp]),
@@ -473,15 +479,17 @@ class HostStep:
 
     def __init__(self, batch, num_q_heads, num_kv_heads, head_dim, max_pages,
                  q_dtype=torch.bfloat16, new_dtype=torch.bfloat16, device="cuda",
-                 use_graph=False):
+                 use_graph=False, cascade=False):
         self.use_graph = bool(use_graph)
+        self.cascade = bool(cascade)  # room for the groups (cascade_step)
         self._graphs = {}
         self.batch, self.h_q, self.max_pages = batch, num_q_heads, max_pages
         self.q_code, self.new_code = self._CODE[q_dtype], self._CODE[new_dtype]
-        offs = (ctypes.c_size_t * 5)()
+        offs = (ctypes.c_size_t * 10)()
         total = ctypes.c_size_t(0)
-        _check(lib().pkv_packed_step_layout(batch, num_q_heads, num_kv_heads, head_dim, max_pages,
-                                            self.q_code, self.new_code, offs, ctypes.byref(total)))
+        layout = lib().pkv_packed_cascade_layout if cascade else lib().pkv_packed_step_layout
+        _check(layout(batch, num_q_heads, num_kv_heads, head_dim, max_pages, self.q_code,
+                      self.new_code, offs, ctypes.byref(total)))
         self.h2d_bytes = int(total.value)
         self.host = torch.empty(self.h2d_bytes, dtype=torch.uint8).pin_memory()
         self.dev = torch.empty(self.h2d_bytes, dtype=torch.uint8, device=device)
@@ -498,6 +506,8 @@ class HostStep:
         self.out_host = torch.empty(self.out.shape, dtype=q_dtype).pin_memory()
         self.d2h_bytes = self.out.numel() * self.out.element_size()
         self._key = None
+        self.n_groups = 0
+        self.workspace_needed = 0
 
     def step(self, k_cache, v_cache, scale, k_scales=None, v_scales=None, workspace=None,
              groups=None, stream=None, window=0, sink_tokens=0):
@@ -555,6 +565,29 @@ class HostStep:
             g.replay()
         return self.out_host
 
+
+    def cascade_step(self, k_cache, v_cache, scale, workspace, stream=None):
+        """One cascade step from host memory (HostStep built with cascade=True): the library
+        groups the batch from ``block_tables_host``/``context_lens_host``, copies the block once,
+        runs the cascade (or, with no group, the plain) fused step and copies the output into
+        ``out_host``. The workspace must hold ``workspace_needed`` bytes (set by every call; a
+        first call with too small a workspace raises before anything is enqueued)."""
+        if not self.cascade:
+            raise PkvError(-1, "HostStep was built without cascade=True")
+        desc = cache_desc(k_cache)
+        need = ctypes.c_size_t(0)
+        ng = ctypes.c_int32(0)
+        wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        st = lib().pkv_cascade_decode_step_packed(
+            ctypes.c_void_p(self.host.data_ptr()), ctypes.c_void_p(self.dev.data_ptr()), self.batch,
+            self.h_q, self.q_code, self.new_code, _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+            ctypes.byref(desc), self.max_pages, float(scale), ctypes.c_void_p(self.out.data_ptr()),
+            ctypes.c_void_p(self.out_host.data_ptr()), _opt(workspace, "workspace"), wsb,
+            ctypes.byref(need), ctypes.byref(ng), _stream(stream))
+        self.workspace_needed = int(need.value)
+        self.n_groups = int(ng.value)
+        _check(st)
+        return self.out_host
 
 def paged_decode_attention_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale,
                                    out=None, k_scales=None, v_scales=None, stream=None):

@@ -420,3 +420,29 @@ def test_packed_step_layout():
     assert list(offs) == expect and total.value == o
     assert L.pkv_packed_step_layout(1, 4, 2, 64, 3, pkv.FP8_E4M3, pkv.BF16, offs,
                                     ctypes.byref(total)) == -3  # q must be F32 or BF16
+
+
+def test_packed_cascade_layout_and_argument_errors():
+    L = pkv.lib()
+    offs = (ctypes.c_size_t * 10)()
+    total = ctypes.c_size_t(0)
+    B = 100
+    assert L.pkv_packed_cascade_layout(B, 32, 8, 128, 256, pkv.BF16, pkv.BF16, offs,
+                                       ctypes.byref(total)) == 0
+    sizes = [B * 32 * 128 * 2, B * 8 * 128 * 2, B * 8 * 128 * 2, B * 256 * 4, B * 4,
+             B * 4, B * 4, (B + 1) * 4, B * 4, B * 4]  # the step's inputs, then the groups
+    expect, o = [], 0
+    for n in sizes:
+        expect.append(o)
+        o += (n + 255) // 256 * 256
+    assert list(offs) == expect and total.value == o
+    step = (ctypes.c_size_t * 5)()
+    t5 = ctypes.c_size_t(0)
+    L.pkv_packed_step_layout(B, 32, 8, 128, 256, pkv.BF16, pkv.BF16, step, ctypes.byref(t5))
+    assert list(step) == expect[:5]  # the step's regions sit where the plain step has them
+    d = _desc(cache_dtype=pkv.BF16)
+    d.head_dim = 128
+    fake = ctypes.c_void_p(1 << 20)
+    assert L.pkv_cascade_decode_step_packed(None, fake, 2, 8, pkv.BF16, pkv.BF16, fake, fake,
+                                            ctypes.byref(d), 4, 0.1, fake, fake, None, 0, None,
+                                            None, None) == -1  # null host block

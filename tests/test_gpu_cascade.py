@@ -173,6 +173,47 @@ def test_cascade_host_step_equals_device_step():
     assert err < TOL, err
 
 
+@pytest.mark.parametrize("grouped", [True, False], ids=["groups", "no_group"])
+def test_packed_cascade_step_equals_device_step(grouped):
+    # one library call from host memory: groups found on the host from the packed tables,
+    # one copy in, the cascade step, one copy out
+    w = _case(4, h_kv=4, seed=16, groups=((6, 9, 1, 60), (3, 4, 1, 30)) if grouped else (),
+              singles=((1, 60),) * (3 if grouped else 7))
+    a = GroupScenario(w)
+    g_a = pkv.cascade_groups(a.bt_host, a.cl_host)
+    assert (g_a.n_groups > 0) == grouped
+    pkv.device_error()
+    if grouped:
+        out_a = _cascade(a, g_a.to(a.q.device), step=True).clone()
+    else:
+        out_a = pkv.paged_decode_step(a.q, a.k_new, a.v_new, a.cache.k, a.cache.v,
+                                      a.block_tables, a.context_lens, w.scale).clone()
+    b = GroupScenario(w)
+    hs = pkv.HostStep(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                      b.block_tables.shape[1], cascade=True)
+    hs.q_host.copy_(b.q.cpu())
+    hs.k_new_host.copy_(b.k_new.cpu())
+    hs.v_new_host.copy_(b.v_new.cpu())
+    hs.block_tables_host.copy_(b.block_tables.cpu())
+    hs.context_lens_host.copy_(b.context_lens.cpu())
+    try:  # without a workspace: refused before anything runs, when the step needs one
+        hs.cascade_step(b.cache.k, b.cache.v, w.scale, None)
+        refused = False
+    except pkv.PkvError:
+        refused = True
+    assert refused == (hs.workspace_needed > 0)
+    ws = torch.zeros(max(hs.workspace_needed, 16), dtype=torch.uint8, device=b.q.device)
+    out_b = hs.cascade_step(b.cache.k, b.cache.v, w.scale, ws)
+    torch.cuda.synchronize()
+    _check_no_error()
+    assert hs.n_groups == g_a.n_groups
+    assert torch.equal(out_a.cpu(), out_b)
+    assert torch.equal(a.cache.k.view(torch.uint8), b.cache.k.view(torch.uint8))
+    assert torch.equal(a.cache.v.view(torch.uint8), b.cache.v.view(torch.uint8))
+    err = np.abs(out_b.float().numpy() - oracle_groups_expected(w)).max()
+    assert err < TOL, err
+
+
 def test_cascade_with_empty_suffix_and_no_groups(prefix_kernel):
     # a member whose context ends exactly at the end of the shared pages (attention only):
     # its own part is empty and the merge takes the prefix partials alone
