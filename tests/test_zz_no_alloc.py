@@ -6,7 +6,6 @@ owns all device memory, a server whose KV pools took all free HBM, a loop that m
 cudaMalloc's device-wide synchronisation). This file is collected last on purpose."""
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
