@@ -340,6 +340,10 @@ void pkv_seq_table_destroy(pkv_seq_table* t);
  * n_shared * page_size tokens (a cached prefix; one more reference on each). */
 int pkv_seq_add(pkv_seq_table* t, int64_t rid, const int32_t* shared_pages, int32_t n_shared,
                 int64_t shared_len);
+/* The same, but the request takes over references the caller already holds on the pages
+ * (for example those a prefix-cache lookup handed out) instead of taking new ones. */
+int pkv_seq_adopt(pkv_seq_table* t, int64_t rid, const int32_t* pages, int32_t n_pages,
+                  int64_t n_tokens);
 /* new_rids[i] becomes a copy of src_rids[i] (same pages, one more reference on each, same
  * length), in order: a parent may be a request forked earlier in the list. */
 int pkv_seq_fork(pkv_seq_table* t, const int64_t* src_rids, const int64_t* new_rids, int32_t n);

@@ -110,6 +110,7 @@ def lib():
         "pkv_seq_table_create": (ctypes.c_int, [vp, i32, ctypes.POINTER(vp)]),
         "pkv_seq_table_destroy": (None, [vp]),
         "pkv_seq_add": (ctypes.c_int, [vp, i64, vp, i32, i64]),
+        "pkv_seq_adopt": (ctypes.c_int, [vp, i64, vp, i32, i64]),
         "pkv_seq_fork": (ctypes.c_int, [vp, vp, vp, i32]),
         "pkv_seq_free": (ctypes.c_int, [vp, vp, i32]),
         "pkv_seq_reserve": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, vp, ctypes.POINTER(i32)]),
@@ -771,10 +772,13 @@ class SeqTable:
             _lib.pkv_seq_table_destroy(h)
             self._h = None
 
-    def add(self, rid: int, shared_pages=None, shared_len: int = 0):
+    def add(self, rid: int, shared_pages=None, shared_len: int = 0, adopt: bool = False):
+        """A new request, optionally on whole shared pages; ``adopt``: the request takes over
+        references the caller holds on them instead of taking new ones."""
         p = np.ascontiguousarray(np.asarray([] if shared_pages is None else list(shared_pages),
                                             dtype=np.int32))
-        _check(lib().pkv_seq_add(self._h, int(rid), _ptr(p), p.size, int(shared_len)))
+        fn = lib().pkv_seq_adopt if adopt else lib().pkv_seq_add
+        _check(fn(self._h, int(rid), _ptr(p), p.size, int(shared_len)))
 
     def fork(self, src_rids, new_rids):
         s, n = _ids(src_rids), _ids(new_rids)

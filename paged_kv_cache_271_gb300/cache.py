@@ -70,10 +70,28 @@ class PagedKVCache:
 
     # ---- requests ---------------------------------------------------------------------------
 
-    def add_request(self, rid: int, shared_pages=None, shared_len: int = 0):
+    def add_request(self, rid: int, shared_pages=None, shared_len: int = 0, adopt: bool = False):
         """New request; optionally starting on ``shared_pages`` that already hold its first
-        ``shared_len`` tokens (a prefix, whole pages only)."""
-        self.table.add(rid, shared_pages, shared_len)
+        ``shared_len`` tokens (a prefix, whole pages only). ``adopt``: the request takes over
+        references the caller holds on those pages instead of taking new ones."""
+        self.table.add(rid, shared_pages, shared_len, adopt)
+
+    def add_request_from_prefix_cache(self, rid: int, prefix_cache, tenant: int, tokens) -> int:
+        """New request whose prompt is ``tokens``: it starts on the longest prefix of whole
+        pages that ``prefix_cache`` holds for this tenant (the lookup's references become the
+        request's). Returns the number of prompt tokens already in the cache; the caller
+        reserves and writes the rest."""
+        pages = prefix_cache.lookup(tenant, tokens)
+        self.table.add(rid, pages, len(pages) * self.page_size, adopt=True)
+        return len(pages) * self.page_size
+
+    def register_prompt(self, rid: int, prefix_cache, tenant: int, tokens):
+        """Puts the full pages of request ``rid``'s prompt (``tokens``, already written) into
+        ``prefix_cache`` for later requests of the same tenant."""
+        n_full = min(len(tokens), self.table.length(rid)) // self.page_size
+        if n_full:
+            prefix_cache.insert(tenant, list(tokens)[:n_full * self.page_size],
+                                self.table.pages(rid)[:n_full])
 
     def fork(self, src_rid: int, new_rid: int):
         """A new request sharing every page of ``src_rid`` (parallel sampling, beam search);

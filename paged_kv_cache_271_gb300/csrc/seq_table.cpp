@@ -54,15 +54,25 @@ int pkv_seq_table_create(pkv_allocator* a, int32_t page_size, pkv_seq_table** ou
 
 void pkv_seq_table_destroy(pkv_seq_table* t) { delete t; }
 
-int pkv_seq_add(pkv_seq_table* t, int64_t rid, const int32_t* shared_pages, int32_t n_shared,
-                int64_t shared_len) {
+}  // extern "C"
+
+namespace {
+
+// A new request on n_shared whole pages; take_refs: one more reference on each (a shared
+// prefix), else the caller's references become the request's (pages it was handed, e.g. by a
+// prefix-cache lookup).
+int seq_add(pkv_seq_table* t, int64_t rid, const int32_t* shared_pages, int32_t n_shared,
+            int64_t shared_len, bool take_refs, const char* who) {
   if (!t || n_shared < 0 || (n_shared > 0 && !shared_pages))
-    return pkv::set_error(PKV_EINVAL, "pkv_seq_add: bad argument");
-  if (t->seqs.count(rid)) return pkv::set_error(PKV_EINVAL, "pkv_seq_add: request %lld exists",
-                                                (long long)rid);
+    return pkv::set_error(PKV_EINVAL, "%s: bad argument", who);
+  if (t->seqs.count(rid))
+    return pkv::set_error(PKV_EINVAL, "%s: request %lld exists", who, (long long)rid);
   if (shared_len != (int64_t)n_shared * t->page_size)
-    return pkv::set_error(PKV_EINVAL, "pkv_seq_add: a shared prefix must fill whole pages");
-  if (n_shared > 0) {
+    return pkv::set_error(PKV_EINVAL, "%s: a shared prefix must fill whole pages", who);
+  for (int32_t i = 0; i < n_shared; ++i)
+    if (pkv_refcount(t->alloc, shared_pages[i]) <= 0)
+      return pkv::set_error(PKV_EREFCNT, "%s: page %d is not allocated", who, shared_pages[i]);
+  if (take_refs && n_shared > 0) {
     const int st = pkv_incref(t->alloc, shared_pages, n_shared);
     if (st != PKV_OK) return st;
   }
@@ -71,6 +81,20 @@ int pkv_seq_add(pkv_seq_table* t, int64_t rid, const int32_t* shared_pages, int3
   s.len = shared_len;
   t->seqs.emplace(rid, std::move(s));
   return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_seq_add(pkv_seq_table* t, int64_t rid, const int32_t* shared_pages, int32_t n_shared,
+                int64_t shared_len) {
+  return seq_add(t, rid, shared_pages, n_shared, shared_len, true, "pkv_seq_add");
+}
+
+int pkv_seq_adopt(pkv_seq_table* t, int64_t rid, const int32_t* pages, int32_t n_pages,
+                  int64_t n_tokens) {
+  return seq_add(t, rid, pages, n_pages, n_tokens, false, "pkv_seq_adopt");
 }
 
 int pkv_seq_fork(pkv_seq_table* t, const int64_t* src_rids, const int64_t* new_rids, int32_t n) {

@@ -204,3 +204,29 @@ def test_seq_table_tables_and_errors():
     assert t.release_outside_window(8, 1, 0) == 0  # the newest token's page stays
     t.free([5, 7, 8])
     assert alloc.num_free() == 8
+
+
+def test_prefix_cache_and_request_tables_compose():
+    # a prompt's full pages go into the prefix cache; a later request of the same tenant starts
+    # on them (the lookup's references become the request's); freeing and evicting returns
+    # every page to the pool
+    import torch
+    from paged_kv_cache_271_gb300.cache import PagedKVCache
+    c = PagedKVCache(32, 2, 64, torch.float32, device="cpu")
+    pc = pkv.PrefixCache(c.allocator, P)
+    prompt = list(range(1000, 1050))  # 50 tokens: 3 full pages and 2 tokens
+    assert c.add_request_from_prefix_cache(0, pc, 7, prompt) == 0  # nothing cached yet
+    c.reserve([0], [len(prompt)])
+    c.register_prompt(0, pc, 7, prompt)
+    shared = c.pages[0][:3]
+    assert [c.allocator.refcount(p) for p in shared] == [2, 2, 2]  # request 0 and the cache
+    assert c.add_request_from_prefix_cache(1, pc, 7, prompt) == 48
+    assert c.pages[1] == shared and c.lens[1] == 48
+    assert [c.allocator.refcount(p) for p in shared] == [3, 3, 3]
+    slots = c.reserve([1], [len(prompt) - 48 + 1])  # the rest of the prompt and one new token
+    assert len(c.pages[1]) == 4 and c.pages[1][3] not in c.pages[0]
+    assert all(s // P == c.pages[1][3] for s in slots)
+    assert c.add_request_from_prefix_cache(2, pc, 8, prompt) == 0  # another tenant: no match
+    c.free_many([0, 1, 2])
+    assert [c.allocator.refcount(p) for p in shared] == [1, 1, 1]  # the cache's own
+    assert pc.evict(3) == 3 and c.allocator.num_free() == 32
