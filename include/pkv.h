@@ -304,6 +304,8 @@ typedef struct pkv_allocator pkv_allocator;
  * first allocations hand them out. */
 int pkv_allocator_create(int32_t num_pages, const int32_t* initial_free_order,
                          pkv_allocator** out);
+/* Frees the allocator's own bookkeeping (the pools are the caller's device memory). Objects
+ * built on it (request tables, prefix caches) must be destroyed first. */
 void pkv_allocator_destroy(pkv_allocator* a);
 /* n pages with reference count 1 into page_ids_out (host); PKV_ENOPAGES if fewer are free. */
 int pkv_alloc(pkv_allocator* a, int32_t n, int32_t* page_ids_out);
@@ -319,6 +321,7 @@ int pkv_decref(pkv_allocator* a, const int32_t* ids, int32_t n);
  * (also when the position starts a page the request does not have yet). */
 int pkv_cow_page(pkv_allocator* a, int32_t* row, int32_t n, int64_t position, int32_t page_size,
                  int32_t* copy_src, int32_t* copy_dst);
+/* Number of free pages (-1 for NULL). */
 int32_t pkv_num_free(const pkv_allocator* a);
 /* Reference count of a page, or -1 for an id out of range. */
 int32_t pkv_refcount(const pkv_allocator* a, int32_t id);
@@ -575,7 +578,8 @@ int32_t pkv_prefix_size(const pkv_prefix_cache* c);
 
 /* When on, every kernel the library launches is bracketed by a pair of CUDA events on its
  * stream. pkv_trace_read() synchronises those events and reports, for the kernel family
- * named ("paged_decode", "decode_combine", "kv_append", "kv_absmax"), the number of launches
+ * named ("paged_decode", "decode_combine", "cascade_prefix", "kv_append", "kv_absmax"), the
+ * number of launches
  * and their summed device time in milliseconds since the last reset. pkv_trace_reset() drops
  * all records. */
 int pkv_trace_enable(int on);
