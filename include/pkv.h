@@ -579,9 +579,8 @@ int32_t pkv_prefix_size(const pkv_prefix_cache* c);
 /* When on, every kernel the library launches is bracketed by a pair of CUDA events on its
  * stream. pkv_trace_read() synchronises those events and reports, for the kernel family
  * named ("paged_decode", "decode_combine", "cascade_prefix", "kv_append", "kv_absmax"), the
- * number of launches
- * and their summed device time in milliseconds since the last reset. pkv_trace_reset() drops
- * all records. */
+ * number of launches and their summed device time in milliseconds since the last reset.
+ * pkv_trace_reset() drops all records. */
 int pkv_trace_enable(int on);
 int pkv_trace_reset(void);
 int pkv_trace_read(const char* kernel, int32_t* launches_out, double* total_ms_out);
