@@ -570,7 +570,7 @@ def run_ours(args):
         flops, byts = work[top][1], work[top][2]
         tf_peak, tf_kind = peaks("bf16_tflops")
         achieved = flops / (top_ms * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "kernel": "cascade_prefix kernel (bf16 mma.sync, d=%d)" % sc.d,
+        roofline = {"bound": "tensor", "kernel": "cascade_prefix kernel (bf16 tcgen05, d=%d)" % sc.d,
                     "achieved": round(achieved, 2), "peak": tf_peak, "unit": "TFLOP/s",
                     "frac": round(achieved / tf_peak, 4), "peak_kind": tf_kind + " cuBLAS bf16",
                     "traffic": None, "algorithmic_flops_per_launch": flops,
