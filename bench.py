@@ -59,7 +59,7 @@ def peaks(kind="hbm_gbs"):
 
 WORKLOADS = ("llama3_8b_b64", "llama3_70b_long", "prefix_sharing", "prefix_sharing_cascade",
              "fp8_cb_b256", "fp8_cb_b64", "int8_cb_b256", "llama3_8b_window",
-             "parallel_sampling_fork")
+             "parallel_sampling_fork", "fp8_cb_trace", "int8_cb_trace")
 
 
 def workload(name="llama3_8b_b64"):
@@ -676,8 +676,9 @@ def run_fork(args):
     cp_pin = torch.zeros((2, P * S), dtype=torch.int32).pin_memory()
     cp_dev = torch.zeros((2, P * S), dtype=torch.int32, device=dev)
 
-    parents = [i // S for i in range(P * S)]
-    ones = [1] * (P * S)
+    parents = np.arange(P * S, dtype=np.int64) // S
+    rids = np.asarray(rids, dtype=np.int64)
+    ones = np.ones(P * S, dtype=np.int32)
     cp_np = cp_pin.numpy()
 
     def host_fork():
@@ -852,6 +853,207 @@ def run_e2e(sc, args, dev, stream, flush, n_sets=1):
     return {"ms_per_step": ms, "h2d": hs.h2d_bytes, "d2h": hs.d2h_bytes}
 
 
+def trace_joins(tr):
+    """Per step of a continuous-batching trace, the requests that join before it: (slot,
+    finished request, new request) triples, from the trace's finish flags and request table."""
+    return [[] if s == 0 else
+            [(b, int(tr.rid_table[s - 1, b]), int(tr.rid_table[s, b]))
+             for b in range(tr.batch) if tr.finish[s - 1, b]] for s in range(tr.steps)]
+
+
+def run_trace(args):
+    """FP8 (or INT8) continuous batching over the whole trace: 256 request slots, contexts
+    U[128, 8192] at the start; every step each live request gains one token, and a request
+    that finished (probability 0.05 per step) is freed and replaced by a new one whose prompt
+    (U[128, 2048] tokens) is prefilled through the quantising append. ``--warmup`` steps run
+    first, untimed; the trace is ``warmup + steps`` long.
+
+    A step is: the host bookkeeping (frees, new requests, the prompts' and the new tokens'
+    slots, page tables and context lengths into pinned buffers: native request tables, timed
+    on the host); the copies of the step's inputs from pinned host memory (queries, new K/V
+    rows, the prompts' K/V rows, tables, context lengths, prompt slots); the device work (the
+    prompts' quantising append, the fused append + decode of every live request, the combine);
+    the copy of the output to the host. ``value`` is the step's algorithmic bytes (K and V of
+    every attended token, queries, outputs, appended rows, prompt rows) over the device work
+    alone (its inputs resident by then); ``e2e`` over host bookkeeping + copies + device work."""
+    import torch
+    import paged_kv_cache_271_gb300 as pkv
+    import workloads
+    from gpu_harness import ContinuousBatchingRun
+    ws, rank, local = rank_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(ws, "nccl")
+    pkv.lib()
+    coded = "int8" if args.workload.startswith("int8") else "fp8_e4m3"
+    n_warm, n = max(3, args.warmup), max(1, args.steps)
+    tr = workloads.fp8_continuous_batching(steps=n_warm + n)
+    run = ContinuousBatchingRun(tr, device=dev, cache_dtype=coded)  # scales + initial prefill
+    cache, B, h_q, h_kv, d = run.cache, tr.batch, tr.num_q_heads, tr.num_kv_heads, tr.head_dim
+    joins_at = trace_joins(tr)
+    n_max = max(1, max(sum(int(tr.prompt_lens[r]) for _, _, r in j) for j in joins_at))
+    width = pkv.pages_needed(int(tr.prompt_lens.max()) + tr.steps)
+    need = pkv.decode_workspace_size(B, h_q, h_kv, d, width)
+    workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
+    bf = torch.bfloat16
+
+    def pair(shape, dtype):
+        return (torch.zeros(shape, dtype=dtype).pin_memory(),
+                torch.zeros(shape, dtype=dtype, device=dev))
+
+    bt = pair((B, width), torch.int32)
+    cl = pair((B,), torch.int32)
+    ps = pair((n_max,), torch.int64)
+    q = pair((B, h_q, d), bf)
+    kn, vn = pair((B, h_kv, d), bf), pair((B, h_kv, d), bf)
+    kp, vp = pair((n_max, h_kv, d), bf), pair((n_max, h_kv, d), bf)
+    out = torch.empty((B, h_q, d), dtype=bf, device=dev)
+    out_pin = torch.empty(out.shape, dtype=bf).pin_memory()
+    stream = torch.cuda.current_stream()
+    start_step = {b: 0 for b in range(B)}  # request -> the step it joined
+    expect = np.zeros(B, dtype=np.int32)
+    rid_arr = np.arange(B, dtype=np.int64)  # the live request of each slot
+    ones = np.ones(B, dtype=np.int32)
+
+    def stage(s):
+        """Step s's inputs into the pinned buffers (untimed): queries, every live request's
+        new K/V row and the prompts of the requests that join before it."""
+        o = 0
+        for _, old, rid in joins_at[s]:
+            del run.tokens[old]
+            run.tokens[rid] = tr.request_tokens(rid)
+            start_step[rid] = s
+            m = int(tr.prompt_lens[rid])
+            kp[0][o:o + m].copy_(run.tokens[rid][0][:m])
+            vp[0][o:o + m].copy_(run.tokens[rid][1][:m])
+            o += m
+        rids = [int(r) for r in tr.rid_table[s]]
+        pos = [int(tr.prompt_lens[r]) + s - start_step[r] for r in rids]
+        expect[:] = np.asarray(pos, dtype=np.int32) + 1  # the lengths the tables must give
+        kn[0].copy_(torch.stack([run.tokens[r][0][p] for r, p in zip(rids, pos)]))
+        vn[0].copy_(torch.stack([run.tokens[r][1][p] for r, p in zip(rids, pos)]))
+        q[0].copy_(tr.step_q(s))
+
+    def host(s):
+        """Frees, new requests, slots, tables: the bookkeeping a scheduler does per step."""
+        j, npr = joins_at[s], 0
+        if j:
+            cache.free_many(np.array([old for _, old, _ in j], dtype=np.int64))
+            new = np.array([rid for _, _, rid in j], dtype=np.int64)
+            for rid in new.tolist():
+                cache.add_request(rid)
+            slots = cache.reserve(new, tr.prompt_lens[new])
+            npr = len(slots)
+            ps[0].numpy()[:npr] = slots
+            for b, _, rid in j:
+                run.slot_rid[b] = rid
+                rid_arr[b] = rid
+        cache.reserve(rid_arr, ones)
+        cache.block_table_array(rid_arr, width, out=bt[0])
+        cache.context_lens_array(rid_arr, out=cl[0])
+        return npr
+
+    def copy_in(npr):
+        for h, dv in (q, kn, vn, bt, cl):
+            dv.copy_(h, non_blocking=True)
+        if npr:
+            for h, dv in (kp, vp, ps):
+                dv[:npr].copy_(h[:npr], non_blocking=True)
+
+    def device(npr):
+        if npr:
+            pkv.kv_append(kp[1][:npr], vp[1][:npr], ps[1][:npr], cache.k, cache.v,
+                          run.k_scales, run.v_scales)
+        pkv.paged_decode_step(q[1], kn[1], vn[1], cache.k, cache.v, bt[1], cl[1], tr.scale,
+                              out=out, k_scales=run.k_scales, v_scales=run.v_scales,
+                              workspace=workspace)
+        return 2 + (1 if npr else 0)  # the fused step, the combine, the prompts' append
+
+    for s in range(n_warm):
+        stage(s)
+        npr = host(s)
+        assert np.array_equal(cl[0].numpy(), expect), s
+        copy_in(npr)
+        device(npr)
+        torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    row = h_kv * d * 1 * 2  # K and V codes of one token
+    app = 2 * h_kv * d * (2 + 1)  # a bf16 row in and a code row out, K and V
+    dev_ms, e2e_ms, host_s, byts, h2d, launches, n_prompt_tok, n_joins = [], [], 0.0, 0, 0, 0, 0, 0
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    for s in range(n_warm, n_warm + n):
+        stage(s)
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        t0 = time.perf_counter()
+        npr = host(s)
+        th = time.perf_counter() - t0
+        ev[0].record(stream)
+        copy_in(npr)
+        ev[1].record(stream)
+        launches += device(npr)
+        ev[2].record(stream)
+        out_pin.copy_(out, non_blocking=True)
+        ev[3].record(stream)
+        ev[3].synchronize()
+        host_s += th
+        assert np.array_equal(cl[0].numpy(), expect), s  # tables agree with the trace
+        dev_ms.append(ev[1].elapsed_time(ev[2]))
+        e2e_ms.append(1e3 * th + ev[0].elapsed_time(ev[3]))
+        byts += int(cl[0].sum()) * row + 2 * B * h_q * d * 2 + B * app + npr * app
+        h2d += (q[0].numel() + kn[0].numel() + vn[0].numel()) * 2 + (bt[0].numel() + B) * 4 \
+            + npr * (2 * h_kv * d * 2 + 8)
+        n_prompt_tok += npr
+        n_joins += len(joins_at[s])
+    barrier()
+    clk = clocks.stop()
+    assert pkv.device_error() == 0
+    ms = max_over_ranks(float(np.mean(dev_ms)), dev)
+    e2e = max_over_ranks(float(np.mean(e2e_ms)), dev)
+    per_step = byts / n
+    peak, kind = peaks()
+    if rank == 0:
+        value = aggregate(per_step, ms, ws)
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+            "steps": n, "warmup": n_warm, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": coded + "/bf16", "data": "synthetic",
+            "config": {"workload": ("int8" if coded == "int8" else "fp8")
+                       + "_continuous_batching_b%d_trace" % B, "batch": B, "num_q_heads": h_q,
+                       "num_kv_heads": h_kv, "head_dim": d, "page_size": 16, "kv_dtype": coded,
+                       "trace_steps": tr.steps,
+                       "timed_steps": "%d..%d" % (n_warm, n_warm + n - 1),
+                       "context_lens": "initial U[128, 8192]; replacements U[128, 2048]; "
+                                       "finish p = 0.05 per step",
+                       "pool_pages": tr.num_pages,
+                       "step": "device: quantising prompt append + fused append + decode + "
+                               "combine (host bookkeeping and the copies in e2e only)",
+                       "l2": "not flushed: a step reads %.0f MB of pages (L2: 129 MB)"
+                             % (per_step / 1e6),
+                       "parallelism": "replicas x%d" % ws},
+            "steps_per_s": round(1e3 / ms, 1),
+            "decode_tokens_per_s": round(ws * B / (ms * 1e-3), 1),
+            "prompt_tokens_per_step": round(n_prompt_tok / n, 1),
+            "requests_replaced": n_joins,
+            "roofline": {"bound": "hbm", "kernel": "whole device step (append + decode + combine)",
+                         "achieved": round(value / ws, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(value / ws / peak, 4), "peak_kind": kind, "traffic": None,
+                         "algorithmic_bytes_per_launch": int(per_step), "launch_ms": round(ms, 5)},
+            "cpu_baseline": None,
+            "host_step_us": round(1e6 * host_s / n, 1),
+            "e2e": {"value": round(aggregate(per_step, e2e, ws), 1), "unit": "GB/s",
+                    "ms_per_step": round(e2e, 5), "h2d_bytes_per_step": int(h2d / n),
+                    "d2h_bytes_per_step": int(out.numel() * 2)},
+            "gpu_launches": int(launches), "clocks": clk,
+            "graph": "none: the step's shapes change along the trace (launched op by op)",
+        }
+        print(json.dumps(line), flush=True)
+
+
 # ---- reference arm: the oracle as it stands --------------------------------------------------
 
 def run_reference(args):
@@ -907,6 +1109,8 @@ def main(argv=None):
         run_reference(args)
     elif args.workload == "parallel_sampling_fork":
         run_fork(args)
+    elif args.workload in ("fp8_cb_trace", "int8_cb_trace"):
+        run_trace(args)
     else:
         run_ours(args)
 

@@ -748,8 +748,13 @@ class PageAllocator:
 
 
 def _ids(rids) -> np.ndarray:
-    return np.ascontiguousarray(np.asarray(list(rids) if not isinstance(rids, np.ndarray)
-                                           else rids, dtype=np.int64))
+    return np.ascontiguousarray(np.asarray(rids if isinstance(rids, np.ndarray) else list(rids),
+                                           dtype=np.int64))
+
+
+def _counts(counts) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(counts if isinstance(counts, np.ndarray)
+                                           else list(counts), dtype=np.int32))
 
 
 def _ptr(a: np.ndarray):
@@ -775,9 +780,11 @@ class SeqTable:
     def add(self, rid: int, shared_pages=None, shared_len: int = 0, adopt: bool = False):
         """A new request, optionally on whole shared pages; ``adopt``: the request takes over
         references the caller holds on them instead of taking new ones."""
-        p = np.ascontiguousarray(np.asarray([] if shared_pages is None else list(shared_pages),
-                                            dtype=np.int32))
         fn = lib().pkv_seq_adopt if adopt else lib().pkv_seq_add
+        if shared_pages is None:
+            _check(fn(self._h, int(rid), None, 0, int(shared_len)))
+            return
+        p = np.ascontiguousarray(np.asarray(list(shared_pages), dtype=np.int32))
         _check(fn(self._h, int(rid), _ptr(p), p.size, int(shared_len)))
 
     def fork(self, src_rids, new_rids):
@@ -792,8 +799,7 @@ class SeqTable:
 
     def reserve(self, rids, counts):
         """Returns (int64 slots of the new positions, list of (src, dst) pages to copy)."""
-        r = _ids(rids)
-        c = np.ascontiguousarray(np.asarray(list(counts), dtype=np.int32))
+        r, c = _ids(rids), _counts(counts)
         if r.size != c.size:
             raise PkvError(-1, "rids and counts differ in length")
         slots = np.empty(int(c.sum()) if c.size else 0, dtype=np.int64)

@@ -30,6 +30,7 @@ namespace {
 struct Seq {
   std::vector<int32_t> pages;  // -1: released (outside a window)
   int64_t len = 0;
+  uint64_t mark = 0;  // the table's epoch of the last batch call that listed it
 };
 
 int64_t pages_for(int64_t tokens, int32_t P) { return (tokens + P - 1) / P; }
@@ -39,7 +40,12 @@ int64_t pages_for(int64_t tokens, int32_t P) { return (tokens + P - 1) / P; }
 struct pkv_seq_table {
   pkv_allocator* alloc;
   int32_t page_size;
-  std::unordered_map<int64_t, Seq> seqs;
+  std::unordered_map<int64_t, Seq> seqs;  // (references to values stay valid across inserts)
+  // A batch call stamps each listed request with a fresh epoch: a request already stamped
+  // with it is listed twice. No per-call set to build.
+  uint64_t epoch = 0;
+  std::vector<Seq*> listed;     // the requests of the current batch call, in order
+  std::vector<int32_t> scratch;  // page lists of the current call
 };
 
 extern "C" {
@@ -47,7 +53,7 @@ extern "C" {
 int pkv_seq_table_create(pkv_allocator* a, int32_t page_size, pkv_seq_table** out) {
   if (!a || !out || page_size <= 0)
     return pkv::set_error(PKV_EINVAL, "pkv_seq_table_create: bad argument");
-  *out = new (std::nothrow) pkv_seq_table{a, page_size, {}};
+  *out = new (std::nothrow) pkv_seq_table{a, page_size, {}, 0, {}, {}};
   if (!*out) return pkv::set_error(PKV_EINVAL, "pkv_seq_table_create: out of host memory");
   return PKV_OK;
 }
@@ -130,15 +136,18 @@ int pkv_seq_fork(pkv_seq_table* t, const int64_t* src_rids, const int64_t* new_r
 
 int pkv_seq_free(pkv_seq_table* t, const int64_t* rids, int32_t n) {
   if (!t || n < 0 || (n > 0 && !rids)) return pkv::set_error(PKV_EINVAL, "pkv_seq_free: bad argument");
-  std::unordered_set<int64_t> seen;
-  for (int32_t i = 0; i < n; ++i)
-    if (!t->seqs.count(rids[i]) || !seen.insert(rids[i]).second)
-      return pkv::set_error(PKV_EINVAL, "pkv_seq_free: no request %lld (or listed twice)",
-                            (long long)rids[i]);
+  const uint64_t ep = ++t->epoch;
   for (int32_t i = 0; i < n; ++i) {
     auto it = t->seqs.find(rids[i]);
-    std::vector<int32_t> live;
-    live.reserve(it->second.pages.size());
+    if (it == t->seqs.end() || it->second.mark == ep)
+      return pkv::set_error(PKV_EINVAL, "pkv_seq_free: no request %lld (or listed twice)",
+                            (long long)rids[i]);
+    it->second.mark = ep;
+  }
+  std::vector<int32_t>& live = t->scratch;
+  for (int32_t i = 0; i < n; ++i) {
+    auto it = t->seqs.find(rids[i]);
+    live.clear();
     for (int32_t p : it->second.pages)
       if (p >= 0) live.push_back(p);
     if (!live.empty()) {
@@ -156,16 +165,20 @@ int pkv_seq_reserve(pkv_seq_table* t, const int64_t* rids, const int32_t* counts
     return pkv::set_error(PKV_EINVAL, "pkv_seq_reserve: bad argument");
   const int32_t P = t->page_size;
   // pass 1: checks, and the pages the batch will take (copies replay the reference counts)
-  std::unordered_set<int64_t> seen;
-  std::unordered_map<int32_t, int32_t> dropped;  // page -> references given up by copies
+  const uint64_t ep = ++t->epoch;
+  std::vector<Seq*>& listed = t->listed;
+  listed.clear();
+  std::unordered_map<int32_t, int32_t> dropped;  // shared page -> references given up by copies
   int64_t total = 0, need_pages = 0;
   bool any_copy = false;
   for (int32_t i = 0; i < n; ++i) {
     auto it = t->seqs.find(rids[i]);
-    if (it == t->seqs.end() || !seen.insert(rids[i]).second || counts[i] < 0)
+    if (it == t->seqs.end() || it->second.mark == ep || counts[i] < 0)
       return pkv::set_error(PKV_EINVAL, "pkv_seq_reserve: request %lld unknown, listed twice or "
                             "with a negative count", (long long)rids[i]);
-    const Seq& s = it->second;
+    Seq& s = it->second;
+    s.mark = ep;
+    listed.push_back(&s);
     total += counts[i];
     if (counts[i] > 0) {
       const int64_t lp = s.len / P;
@@ -177,10 +190,13 @@ int pkv_seq_reserve(pkv_seq_table* t, const int64_t* rids, const int32_t* counts
         const int32_t ref = pkv_refcount(t->alloc, page);
         if (ref <= 0)
           return pkv::set_error(PKV_EREFCNT, "pkv_seq_reserve: page %d is not allocated", page);
-        if (ref - dropped[page] > 1) {
-          ++dropped[page];
-          ++need_pages;
-          any_copy = true;
+        if (ref > 1) {  // shared: copied unless every other holder copied it first
+          int32_t& d = dropped[page];
+          if (ref - d > 1) {
+            ++d;
+            ++need_pages;
+            any_copy = true;
+          }
         }
       }
     }
@@ -198,7 +214,7 @@ int pkv_seq_reserve(pkv_seq_table* t, const int64_t* rids, const int32_t* counts
   int32_t nc = 0;
   int64_t o = 0;
   for (int32_t i = 0; i < n; ++i) {
-    Seq& s = t->seqs.at(rids[i]);
+    Seq& s = *listed[i];
     const int32_t c = counts[i];
     if (c > 0) {
       int32_t src = -1, dst = -1;
@@ -218,11 +234,15 @@ int pkv_seq_reserve(pkv_seq_table* t, const int64_t* rids, const int32_t* counts
       const int st = pkv_alloc(t->alloc, (int32_t)grow, s.pages.data() + old);
       if (st != PKV_OK) return st;
     }
-    for (int32_t k = 0; k < c; ++k, ++o) {
-      const int64_t pos = s.len + k;
-      slots_out[o] = (int64_t)s.pages[pos / P] * P + pos % P;
+    // slots page by page: page * P + offset, consecutive within a page
+    const int64_t end = s.len + c;
+    for (int64_t pos = s.len; pos < end;) {
+      const int64_t lp = pos / P;
+      const int64_t base = (int64_t)s.pages[lp] * P - lp * P;
+      const int64_t stop = std::min<int64_t>(end, (lp + 1) * P);
+      for (; pos < stop; ++pos) slots_out[o++] = base + pos;
     }
-    s.len += c;
+    s.len = end;
   }
   *n_copies = nc;
   return PKV_OK;

@@ -61,3 +61,19 @@ def test_bench_cli_and_workload_configs_without_gpu():
     w = workloads.llama3_8b_batch64()
     # the metric's bytes: the sum of the drawn context lengths times 8 heads x 128 dims x 2 B x 2
     assert bench.config_of(w)["context_lens"].endswith(str(int(w.context_lens.sum())))
+
+
+def test_trace_joins_follow_the_request_table():
+    import workloads
+    tr = workloads.fp8_continuous_batching(batch=32, steps=12, lo=128, hi=512, p_finish=0.2)
+    joins = bench.trace_joins(tr)
+    assert joins[0] == [] and sum(len(j) for j in joins) == int(tr.finish[:-1].sum()) > 0
+    seen = set(range(tr.batch))
+    for s in range(1, tr.steps):
+        live = list(tr.rid_table[s - 1])
+        for b, old, new in joins[s]:
+            assert tr.finish[s - 1, b] and old == live[b] and new not in seen
+            live[b] = new
+            seen.add(new)
+        assert live == list(tr.rid_table[s])  # every other slot keeps its request
+    assert sorted(seen) == list(range(len(tr.prompt_lens)))  # ids 0, 1, ... in join order
