@@ -13,8 +13,9 @@ rotate``, the default), or the L2 is flushed with a 256 MiB write before every t
                   [--workload NAME] [--l2 rotate|flush] [--no-cpu-baseline]
 
 The default workload is the layer above; the others (``--workload``) are the 70B long-context
-layer, prefix sharing (plain and cascade), FP8 and INT8 continuous batching, the sliding window
-with sinks and the copy-on-write fork of parallel sampling, each measured the same way.
+layer, prefix sharing (plain and cascade), FP8 and INT8 continuous batching (one step's state,
+or the whole trace step by step with its frees, replacements and prompt prefills), the sliding
+window with sinks and the copy-on-write fork of parallel sampling, each measured the same way.
 
 Prints one JSON line on rank 0. ``value`` is algorithmic HBM bytes per step (K and V of every
 attended token, the queries, the outputs, and the appended rows) over the step time, summed
