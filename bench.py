@@ -1011,6 +1011,22 @@ def run_trace(args):
         n_joins += len(joins_at[s])
     barrier()
     clk = clocks.stop()
+    # Per-kernel durations: the last step's device work again (it rewrites the same slots with
+    # the same values), with the library's tracing on and the L2 flushed before each repeat.
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    pkv.trace_reset()
+    pkv.trace_enable(True)
+    for _ in range(10):
+        flush.zero_()
+        device(npr)
+    torch.cuda.synchronize()
+    pkv.trace_enable(False)
+    kernel_ms = {}
+    for k in ("kv_append", "paged_decode", "decode_combine"):
+        c, t = pkv.trace_read(k)
+        kernel_ms[k] = round(t / max(c, 1), 5)
+    pkv.trace_reset()
+    del flush
     assert pkv.device_error() == 0
     ms = max_over_ranks(float(np.mean(dev_ms)), dev)
     e2e = max_over_ranks(float(np.mean(e2e_ms)), dev)
@@ -1046,6 +1062,9 @@ def run_trace(args):
                          "algorithmic_bytes_per_launch": int(per_step), "launch_ms": round(ms, 5)},
             "cpu_baseline": None,
             "host_step_us": round(1e6 * host_s / n, 1),
+            "kernel_ms": kernel_ms,
+            "kernel_ms_of": "the last timed step's device work run 10 more times, one event "
+                            "pair per kernel, L2 flushed before each (%d prompt tokens)" % npr,
             "e2e": {"value": round(aggregate(per_step, e2e, ws), 1), "unit": "GB/s",
                     "ms_per_step": round(e2e, 5), "h2d_bytes_per_step": int(h2d / n),
                     "d2h_bytes_per_step": int(out.numel() * 2)},

@@ -7,6 +7,7 @@
 // threads cover consecutive dims of one (token, KV head) row, so loads and stores are
 // coalesced. FP8: code = cvt.rn.satfinite.e4m3(fp32(x / s)) (section 7, "fp8 KV (E4M3)";
 // per-head scale, round-to-nearest-even and saturation are this library's reading).
+#include <algorithm>
 #include <math.h>
 
 #include "decode_plan.cuh"
@@ -113,39 +114,63 @@ __device__ __forceinline__ void quantize_store_int8(const float (&x)[N], float s
   }
 }
 
-// FP8 / INT8 append: read a 16-byte vector of fp32/bf16, quantise with the head's scale, store
-// the codes.
+template <typename TIN, bool INT8_CODES>
+__device__ __forceinline__ void quantize_vec(const uint4& raw, float s, uint8_t* dst) {
+  constexpr int VEC = Vec16<TIN>::N;
+  float x[VEC];
+  Vec16<TIN>::load(&raw, x);
+  if constexpr (INT8_CODES)
+    quantize_store_int8<VEC>(x, s, dst);
+  else
+    quantize_store<VEC>(x, s, dst);
+}
+
+// FP8 / INT8 append: each 16-byte vector of fp32/bf16 input is quantised with its head's scale
+// and its codes stored at the token's slot. A thread owns fixed (head, vector) columns of the
+// token rows -- their index arithmetic and scales are set once -- and walks the tokens
+// blockIdx.x, blockIdx.x + gridDim.x, ..., two at a time with both tokens' loads issued before
+// either store.
 template <typename TIN, bool INT8_CODES>
 __global__ void kv_append_fp8_kernel(const AppendArgs a) {
   constexpr int VEC = Vec16<TIN>::N;
   const int vpr = a.head_dim / VEC;
-  const int64_t total = (int64_t)a.num_tokens * a.h_kv * vpr;
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int v = (int)(idx % vpr);
-    const int64_t r = idx / vpr;
-    const int h = (int)(r % a.h_kv);
-    const int64_t i = r / a.h_kv;
-    const int64_t slot = a.slots[i];
-    if (slot < 0) continue;
-    if (slot >= a.num_slots) {
-      atomicOr(a.err, PKV_DEVERR_BAD_SLOT);
-      continue;
+  const int per_tok = a.h_kv * vpr;
+  const int64_t row_elems = (int64_t)a.h_kv * a.head_dim;  // one token's input row
+  const int64_t page_elems = row_elems * kPageSize;        // one pool page (every head)
+  const TIN* kin = static_cast<const TIN*>(a.k_new);
+  const TIN* vin = static_cast<const TIN*>(a.v_new);
+  uint8_t* kc = static_cast<uint8_t*>(a.k_cache);
+  uint8_t* vc = static_cast<uint8_t*>(a.v_cache);
+  const int n = a.num_tokens, step = gridDim.x;
+  for (int t = threadIdx.x; t < per_tok; t += blockDim.x) {
+    const int h = t / vpr, v = t - h * vpr;
+    const float ks = a.k_scales[h], vs = a.v_scales[h];
+    const int64_t src0 = (int64_t)h * a.head_dim + v * VEC;
+    const int64_t dst0 = (int64_t)h * kPageSize * a.head_dim + v * VEC;
+    for (int i = blockIdx.x; i < n; i += 2 * step) {
+      const int i2 = i + step;
+      const bool two = i2 < n;
+      const int64_t s1 = a.slots[i];
+      const int64_t s2 = two ? a.slots[i2] : -1;
+      const uint4 k1 = *reinterpret_cast<const uint4*>(kin + i * row_elems + src0);
+      const uint4 v1 = *reinterpret_cast<const uint4*>(vin + i * row_elems + src0);
+      uint4 k2 = make_uint4(0, 0, 0, 0), v2 = k2;
+      if (two) {
+        k2 = *reinterpret_cast<const uint4*>(kin + i2 * row_elems + src0);
+        v2 = *reinterpret_cast<const uint4*>(vin + i2 * row_elems + src0);
+      }
+      if (s1 >= a.num_slots || s2 >= a.num_slots) atomicOr(a.err, PKV_DEVERR_BAD_SLOT);
+      if (s1 >= 0 && s1 < a.num_slots) {
+        const int64_t d = (s1 / kPageSize) * page_elems + (s1 % kPageSize) * a.head_dim + dst0;
+        quantize_vec<TIN, INT8_CODES>(k1, ks, kc + d);
+        quantize_vec<TIN, INT8_CODES>(v1, vs, vc + d);
+      }
+      if (s2 >= 0 && s2 < a.num_slots) {
+        const int64_t d = (s2 / kPageSize) * page_elems + (s2 % kPageSize) * a.head_dim + dst0;
+        quantize_vec<TIN, INT8_CODES>(k2, ks, kc + d);
+        quantize_vec<TIN, INT8_CODES>(v2, vs, vc + d);
+      }
     }
-    const int64_t page = slot / kPageSize, row = slot % kPageSize;
-    const int64_t src = (i * a.h_kv + h) * a.head_dim + (int64_t)v * VEC;
-    const int64_t dst = ((page * a.h_kv + h) * kPageSize + row) * a.head_dim + (int64_t)v * VEC;
-    float x[VEC];
-    Vec16<TIN>::load(static_cast<const TIN*>(a.k_new) + src, x);
-    if constexpr (INT8_CODES)
-      quantize_store_int8<VEC>(x, a.k_scales[h], static_cast<uint8_t*>(a.k_cache) + dst);
-    else
-      quantize_store<VEC>(x, a.k_scales[h], static_cast<uint8_t*>(a.k_cache) + dst);
-    Vec16<TIN>::load(static_cast<const TIN*>(a.v_new) + src, x);
-    if constexpr (INT8_CODES)
-      quantize_store_int8<VEC>(x, a.v_scales[h], static_cast<uint8_t*>(a.v_cache) + dst);
-    else
-      quantize_store<VEC>(x, a.v_scales[h], static_cast<uint8_t*>(a.v_cache) + dst);
   }
 }
 
@@ -369,18 +394,34 @@ cudaError_t launch_kv_append(const AppendArgs& a, int in_dtype, int cache_dtype,
   const int threads = 256;
   if (cache_dtype == PKV_FP8_E4M3 || cache_dtype == PKV_INT8) {
     const bool i8 = cache_dtype == PKV_INT8;
+    // one wave of blocks, each taking a token pair at a time; threads cover a token row's
+    // (head, vector) columns
+    const int per_tok = a.h_kv * (a.head_dim / (in_dtype == PKV_BF16 ? 8 : 4));
+    const int qt = per_tok <= 128 ? 128 : 256;
+    const int64_t pairs = ((int64_t)a.num_tokens + 1) / 2;
+    auto go = [&](auto kern, int slot) {
+      static int wave[2] = {0, 0};  // resident blocks on the device, per block size
+      if (!wave[slot]) {
+        int per_sm = 0, dev = 0, sms = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, qt, 0);
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        wave[slot] = std::max(1, per_sm) * std::max(1, sms);
+      }
+      const int blocks = (int)std::min<int64_t>(pairs, wave[slot]);
+      kern<<<blocks, qt, 0, s>>>(a);
+    };
+    const int slot = qt == 128 ? 0 : 1;
     if (in_dtype == PKV_BF16) {
-      const int64_t work = (int64_t)a.num_tokens * a.h_kv * (a.head_dim / 8);
       if (i8)
-        kv_append_fp8_kernel<__nv_bfloat16, true><<<grid_for(work, threads), threads, 0, s>>>(a);
+        go(kv_append_fp8_kernel<__nv_bfloat16, true>, slot);
       else
-        kv_append_fp8_kernel<__nv_bfloat16, false><<<grid_for(work, threads), threads, 0, s>>>(a);
+        go(kv_append_fp8_kernel<__nv_bfloat16, false>, slot);
     } else {
-      const int64_t work = (int64_t)a.num_tokens * a.h_kv * (a.head_dim / 4);
       if (i8)
-        kv_append_fp8_kernel<float, true><<<grid_for(work, threads), threads, 0, s>>>(a);
+        go(kv_append_fp8_kernel<float, true>, slot);
       else
-        kv_append_fp8_kernel<float, false><<<grid_for(work, threads), threads, 0, s>>>(a);
+        go(kv_append_fp8_kernel<float, false>, slot);
     }
   } else if (cache_dtype == PKV_BF16) {
     const int64_t work = (int64_t)a.num_tokens * a.h_kv * (a.head_dim / 8);

@@ -324,14 +324,23 @@ def test_context_longer_than_table_is_cut_and_flagged():
     assert pkv.device_error() & pkv.DEVERR_BAD_PAGE
 
 
-def test_bad_slot_sets_error_word():
-    kc = torch.zeros(4, 2, 16, 64, dtype=torch.bfloat16, device="cuda")
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_bad_slot_sets_error_word(kv):
+    # three tokens (an odd count) with the out-of-range slot in the middle: it is reported and
+    # skipped, the other two are written
+    fp8 = kv == "fp8_e4m3"
+    kc = torch.zeros(4, 2, 16, 64, dtype=torch.uint8 if fp8 else torch.bfloat16, device="cuda")
     vc = torch.zeros_like(kc)
     kn = torch.ones(3, 2, 64, dtype=torch.bfloat16, device="cuda")
     slots = torch.tensor([0, 4 * 16, 5], dtype=torch.int64, device="cuda")
-    pkv.kv_append(kn, kn, slots, kc, vc)
+    one = torch.ones(2, device="cuda") if fp8 else None
+    pkv.device_error()
+    pkv.kv_append(kn, kn, slots, kc, vc, one, one)
     assert pkv.device_error() & pkv.DEVERR_BAD_SLOT
-    assert float(kc[0, 0, 0, 0]) == 1.0 and float(kc[0, 0, 5, 0]) == 1.0
+    want = int(oracle.quantize_e4m3(np.ones(1, np.float32), 1.0)[0]) if fp8 else 1.0
+    got = kc.float() if not fp8 else kc.to(torch.int32)
+    assert got[0, :, 0].eq(want).all() and got[0, :, 5].eq(want).all()
+    assert int(torch.count_nonzero(kc.view(torch.uint8))) == 2 * 2 * 64 * (1 if fp8 else 2)
 
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
