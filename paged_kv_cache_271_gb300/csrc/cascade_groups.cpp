@@ -8,6 +8,7 @@
 // position ctx - 1, which a decode step writes, is never shared). A group sharing fewer than
 // min_prefix_pages pages is dropped. Members keep batch order inside their group.
 #include <algorithm>
+#include <cstring>
 #include <unordered_map>
 #include <vector>
 
@@ -34,41 +35,55 @@ extern "C" int pkv_cascade_groups(const int32_t* block_tables, const int32_t* co
     const int64_t c = ctx >= 1 ? (ctx - 1) / P : 0;
     return (int32_t)std::min<int64_t>(c, max_pages_per_seq);
   };
+  // bucket of each request (by first page id, buckets numbered in order of first appearance),
+  // then the members of every bucket in batch order, in one flat array (a counting pass)
   std::unordered_map<int32_t, int32_t> bucket_of;  // first page id -> bucket
-  std::vector<std::vector<int32_t>> buckets;
+  bucket_of.reserve((size_t)batch * 2);
+  std::vector<int32_t> bucket(batch, -1), count, start;
   for (int32_t b = 0; b < batch; ++b) {
     group_of[b] = -1;
     if (cap(b) < min_prefix_pages) continue;
     const int32_t first = block_tables[(size_t)b * max_pages_per_seq];
-    auto it = bucket_of.find(first);
-    if (it == bucket_of.end()) {
-      bucket_of.emplace(first, (int32_t)buckets.size());
-      buckets.push_back({b});
-    } else {
-      buckets[it->second].push_back(b);
-    }
+    auto ins = bucket_of.emplace(first, (int32_t)count.size());
+    if (ins.second) count.push_back(0);
+    bucket[b] = ins.first->second;
+    ++count[bucket[b]];
+  }
+  const int32_t nb = (int32_t)count.size();
+  start.assign(nb + 1, 0);
+  for (int32_t k = 0; k < nb; ++k) start[k + 1] = start[k] + count[k];
+  std::vector<int32_t> flat(start[nb]);
+  {
+    std::vector<int32_t> fill(start.begin(), start.end() - 1);
+    for (int32_t b = 0; b < batch; ++b)
+      if (bucket[b] >= 0) flat[fill[bucket[b]]++] = b;
   }
   int32_t ng = 0, nm = 0, mm = 0, mp = 0;
   group_offsets[0] = 0;
-  for (const auto& mem : buckets) {
-    if ((int32_t)mem.size() < min_members) continue;
+  for (int32_t k = 0; k < nb; ++k) {
+    const int32_t* mem = flat.data() + start[k];
+    const int32_t size = count[k];
+    if (size < min_members) continue;
     const int32_t* r0 = block_tables + (size_t)mem[0] * max_pages_per_seq;
     int32_t shared = cap(mem[0]);
-    for (size_t k = 1; k < mem.size() && shared > 0; ++k) {
-      const int32_t* r = block_tables + (size_t)mem[k] * max_pages_per_seq;
-      int32_t n = 0;
-      const int32_t lim = std::min(shared, cap(mem[k]));
-      while (n < lim && r[n] == r0[n]) ++n;
+    for (int32_t m = 1; m < size && shared > 0; ++m) {
+      const int32_t* r = block_tables + (size_t)mem[m] * max_pages_per_seq;
+      const int32_t lim = std::min(shared, cap(mem[m]));
+      int32_t n = lim;
+      if (std::memcmp(r, r0, (size_t)lim * sizeof(int32_t)) != 0) {  // find where they part
+        n = 0;
+        while (r[n] == r0[n]) ++n;
+      }
       shared = n;
     }
     if (shared < min_prefix_pages) continue;
-    for (int32_t b : mem) {
-      group_of[b] = ng;
-      group_members[nm++] = b;
+    for (int32_t m = 0; m < size; ++m) {
+      group_of[mem[m]] = ng;
+      group_members[nm++] = mem[m];
     }
     prefix_pages[ng] = shared;
     group_offsets[ng + 1] = nm;
-    mm = std::max(mm, (int32_t)mem.size());
+    mm = std::max(mm, size);
     mp = std::max(mp, shared);
     ++ng;
   }
