@@ -522,7 +522,8 @@ class HostStep:
                                     out=self.out, workspace=workspace, stream=st)
                 self.out_host.copy_(self.out, non_blocking=True)
             return self.out_host
-        key = (k_cache.data_ptr(), v_cache.data_ptr(), float(scale),
+        key = (k_cache.data_ptr(), v_cache.data_ptr(), k_cache.shape, k_cache.stride(),
+               v_cache.stride(), k_cache.dtype, float(scale),
                None if k_scales is None else k_scales.data_ptr(),
                None if v_scales is None else v_scales.data_ptr(),
                None if workspace is None else workspace.data_ptr(), _stream(stream).value,
@@ -575,18 +576,25 @@ class HostStep:
         first call with too small a workspace raises before anything is enqueued)."""
         if not self.cascade:
             raise PkvError(-1, "HostStep was built without cascade=True")
-        desc = cache_desc(k_cache)
-        need = ctypes.c_size_t(0)
-        ng = ctypes.c_int32(0)
         wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
-        st = lib().pkv_cascade_decode_step_packed(
-            ctypes.c_void_p(self.host.data_ptr()), ctypes.c_void_p(self.dev.data_ptr()), self.batch,
-            self.h_q, self.q_code, self.new_code, _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
-            ctypes.byref(desc), self.max_pages, float(scale), ctypes.c_void_p(self.out.data_ptr()),
-            ctypes.c_void_p(self.out_host.data_ptr()), _opt(workspace, "workspace"), wsb,
-            ctypes.byref(need), ctypes.byref(ng), _stream(stream))
-        self.workspace_needed = int(need.value)
-        self.n_groups = int(ng.value)
+        key = (k_cache.data_ptr(), v_cache.data_ptr(), k_cache.shape, k_cache.stride(),
+               v_cache.stride(), k_cache.dtype, float(scale),
+               None if workspace is None else workspace.data_ptr(), wsb)
+        if key != getattr(self, "_ckey", None):  # the call's arguments, built once per set
+            self._cdesc = cache_desc(k_cache)
+            self._need, self._ng = ctypes.c_size_t(0), ctypes.c_int32(0)
+            self._cws = workspace
+            self._cpre = (ctypes.c_void_p(self.host.data_ptr()), ctypes.c_void_p(self.dev.data_ptr()),
+                          self.batch, self.h_q, self.q_code, self.new_code,
+                          _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                          ctypes.byref(self._cdesc), self.max_pages, float(scale),
+                          ctypes.c_void_p(self.out.data_ptr()),
+                          ctypes.c_void_p(self.out_host.data_ptr()), _opt(workspace, "workspace"),
+                          wsb, ctypes.byref(self._need), ctypes.byref(self._ng))
+            self._ckey = key
+        st = lib().pkv_cascade_decode_step_packed(*self._cpre, _stream(stream))
+        self.workspace_needed = int(self._need.value)
+        self.n_groups = int(self._ng.value)
         _check(st)
         return self.out_host
 
