@@ -526,7 +526,9 @@ class HostStep:
                v_cache.stride(), k_cache.dtype, float(scale),
                None if k_scales is None else k_scales.data_ptr(),
                None if v_scales is None else v_scales.data_ptr(),
-               None if workspace is None else workspace.data_ptr(), _stream(stream).value,
+               None if workspace is None else workspace.data_ptr(),
+               None if workspace is None else workspace.numel() * workspace.element_size(),
+               _stream(stream).value,
                int(window), int(sink_tokens))
         if key != self._key:  # the call's arguments, built once per pool / workspace / stream
             if workspace is None:
