@@ -522,14 +522,14 @@ class HostStep:
                                     out=self.out, workspace=workspace, stream=st)
                 self.out_host.copy_(self.out, non_blocking=True)
             return self.out_host
+        sp = _stream(stream)
         key = (k_cache.data_ptr(), v_cache.data_ptr(), k_cache.shape, k_cache.stride(),
                v_cache.stride(), k_cache.dtype, float(scale),
                None if k_scales is None else k_scales.data_ptr(),
                None if v_scales is None else v_scales.data_ptr(),
                None if workspace is None else workspace.data_ptr(),
                None if workspace is None else workspace.numel() * workspace.element_size(),
-               _stream(stream).value,
-               int(window), int(sink_tokens))
+               sp.value, int(window), int(sink_tokens))
         if key != self._key:  # the call's arguments, built once per pool / workspace / stream
             if workspace is None:
                 need = decode_workspace_size(self.batch, self.h_q, k_cache.shape[1],
@@ -546,7 +546,7 @@ class HostStep:
                          workspace.numel() * workspace.element_size())
             self._key = key
         if not self.use_graph:
-            _check(lib().pkv_paged_decode_step_packed(*self._pre, _stream(stream)))
+            _check(lib().pkv_paged_decode_step_packed(*self._pre, sp))
             return self.out_host
         g = self._graphs.get(key)
         if stream is None:
