@@ -914,7 +914,6 @@ def run_trace(args):
     start_step = {b: 0 for b in range(B)}  # request -> the step it joined
     expect = np.zeros(B, dtype=np.int32)
     rid_arr = np.arange(B, dtype=np.int64)  # the live request of each slot
-    ones = np.ones(B, dtype=np.int32)
 
     def stage(s):
         """Step s's inputs into the pinned buffers (untimed): queries, every live request's
@@ -936,22 +935,19 @@ def run_trace(args):
         q[0].copy_(tr.step_q(s))
 
     def host(s):
-        """Frees, new requests, slots, tables: the bookkeeping a scheduler does per step."""
-        j, npr = joins_at[s], 0
-        if j:
-            cache.free_many(np.array([old for _, old, _ in j], dtype=np.int64))
-            new = np.array([rid for _, _, rid in j], dtype=np.int64)
-            for rid in new.tolist():
-                cache.add_request(rid)
-            slots = cache.reserve(new, tr.prompt_lens[new])
-            npr = len(slots)
+        """Frees, new requests, slots, tables: the bookkeeping a scheduler does per step, in one
+        library call (pkv_seq_step; table rows patched in place where they keep a request)."""
+        j = joins_at[s]
+        old = np.array([o for _, o, _ in j], dtype=np.int64)
+        new = np.array([r for _, _, r in j], dtype=np.int64)
+        for b, _, rid in j:  # a new request takes the finished one's slot
+            run.slot_rid[b] = rid
+            rid_arr[b] = rid
+        slots, _, _ = cache.step(old, new, tr.prompt_lens[new], rid_arr, width,
+                                 tables_out=bt[0], lens_out=cl[0], incremental=True)
+        npr = len(slots)
+        if npr:
             ps[0].numpy()[:npr] = slots
-            for b, _, rid in j:
-                run.slot_rid[b] = rid
-                rid_arr[b] = rid
-        cache.reserve(rid_arr, ones)
-        cache.block_table_array(rid_arr, width, out=bt[0])
-        cache.context_lens_array(rid_arr, out=cl[0])
         return npr
 
     def copy_in(npr):

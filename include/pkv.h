@@ -369,6 +369,34 @@ int pkv_seq_reserve(pkv_seq_table* t, const int64_t* rids, const int32_t* counts
  * listed requests into host arrays (either may be NULL). PKV_EINVAL if a row does not fit. */
 int pkv_seq_tables(const pkv_seq_table* t, const int64_t* rids, int32_t n, int32_t width,
                    int32_t* block_tables_out, int32_t* context_lens_out);
+/*
+ * One scheduler step in one call ("KV cache and PagedAttention", section 5: requests leave and
+ * join the running batch every step). In order: the n_free finished requests are dropped
+ * (pkv_seq_free); the n_new new requests are added empty and grown by their prompt_counts
+ * tokens (their slots, request by request, to prompt_slots_out: host, sum of prompt_counts);
+ * every one of the n_live live requests -- which may include new ones -- is grown by one token
+ * (slots to live_slots_out, host [n_live], or NULL), with copy-on-write as in pkv_seq_reserve
+ * (copy_src/copy_dst: host, room for n_live pairs, or NULL when no live page is shared;
+ * *n_copies set); and their block-table rows and token counts are written as by
+ * pkv_seq_tables (block_tables_out [n_live][width] and context_lens_out [n_live], host,
+ * either may be NULL). With incremental != 0, a row that already holds the same request's
+ * row from the previous incremental step into the same buffer with the same width is
+ * written only from the first column that changed since (new pages, copies, released
+ * pages); every other row in full. The caller then must not change those rows in between
+ * (a pkv_seq_tables call into the same buffer pointer makes the next step write in full).
+ * Every argument is checked before anything changes (PKV_EINVAL: an
+ * unknown or repeated id, a new id that is live, a live id that is neither live nor new, a
+ * write into a released page, a row wider than the table). The frees then stand; if the pages
+ * cannot cover the prompts, the copies and the new tokens (PKV_ENOPAGES), the new requests
+ * are removed again and their pages returned (the free list's order may differ), so the
+ * table holds exactly the state after the frees. Not thread-safe.
+ */
+int pkv_seq_step(pkv_seq_table* t, const int64_t* free_rids, int32_t n_free,
+                 const int64_t* new_rids, const int32_t* prompt_counts, int32_t n_new,
+                 int64_t* prompt_slots_out, const int64_t* live_rids, int32_t n_live,
+                 int64_t* live_slots_out, int32_t width, int32_t* block_tables_out,
+                 int32_t* context_lens_out, int32_t incremental, int32_t* copy_src,
+                 int32_t* copy_dst, int32_t* n_copies);
 /* Releases every page of the request whose positions all lie at or past sink_tokens, before
  * the last `window` positions and before the newest token (window 0: none); their row entries
  * become -1. *released (may be NULL) receives the count. */

@@ -115,6 +115,8 @@ def lib():
         "pkv_seq_free": (ctypes.c_int, [vp, vp, i32]),
         "pkv_seq_reserve": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, vp, ctypes.POINTER(i32)]),
         "pkv_seq_tables": (ctypes.c_int, [vp, vp, i32, i32, vp, vp]),
+        "pkv_seq_step": (ctypes.c_int, [vp, vp, i32, vp, vp, i32, vp, vp, i32, vp, i32, vp, vp,
+                                        i32, vp, vp, ctypes.POINTER(i32)]),
         "pkv_seq_release_outside_window": (ctypes.c_int, [vp, i64, i64, i64,
                                                           ctypes.POINTER(i32)]),
         "pkv_seq_len": (i64, [vp, i64]),
@@ -839,6 +841,48 @@ class SeqTable:
         cl_p = cl.data_ptr() if isinstance(cl, torch.Tensor) else cl.ctypes.data
         _check(lib().pkv_seq_tables(self._h, _ptr(r), r.size, 0, None, cl_p if r.size else None))
         return cl
+
+    def step(self, free_rids, new_rids, prompt_counts, live_rids, width=None, tables_out=None,
+             lens_out=None, live_slots=False, incremental=False):
+        """One scheduler step (pkv_seq_step): drop ``free_rids``, add ``new_rids`` grown by their
+        ``prompt_counts``, grow every one of ``live_rids`` by one token and export their table
+        rows (``width`` columns; into ``tables_out`` when given, else a new array) and lengths
+        (into ``lens_out``). ``incremental``: rows still holding the same request from the
+        previous incremental step into the same ``tables_out`` are only patched (the caller
+        leaves them alone in between). Returns (prompt slots int64, tables, lengths, copy
+        pairs), plus the live requests' new slots when ``live_slots``."""
+        f, nw, c, lv = _ids(free_rids), _ids(new_rids), _counts(prompt_counts), _ids(live_rids)
+        if nw.size != c.size:
+            raise PkvError(-1, "new_rids and prompt_counts differ in length")
+        n = lv.size
+        if width is None:
+            width = self._step_width(lv, nw, c)
+        bt = np.empty((n, int(width)), dtype=np.int32) if tables_out is None else tables_out
+        cl = np.empty(n, dtype=np.int32) if lens_out is None else lens_out
+        ptr = (lambda a: a.data_ptr() if isinstance(a, torch.Tensor) else a.ctypes.data)
+        ps = np.empty(int(c.sum()) if c.size else 0, dtype=np.int64)
+        ls = np.empty(n, dtype=np.int64) if live_slots else None
+        src = np.empty(max(n, 1), dtype=np.int32)
+        dst = np.empty_like(src)
+        nc = ctypes.c_int32(0)
+        _check(lib().pkv_seq_step(self._h, _ptr(f), f.size, _ptr(nw), _ptr(c), nw.size, _ptr(ps),
+                                  _ptr(lv), n, None if ls is None else _ptr(ls), int(width),
+                                  ptr(bt) if n else None, ptr(cl) if n else None,
+                                  int(bool(incremental)), src.ctypes.data, dst.ctypes.data,
+                                  ctypes.byref(nc)))
+        copies = [(int(src[i]), int(dst[i])) for i in range(nc.value)]
+        return (ps, bt, cl, copies) + ((ls,) if live_slots else ())
+
+    def _step_width(self, live, new, prompts):
+        """Columns the live requests need after a step (at least 1)."""
+        pr = dict(zip(new.tolist(), prompts.tolist()))
+        P, w = self.page_size, 1
+        for r in live.tolist():
+            if r in pr:
+                w = max(w, -(-(pr[r] + 1) // P))
+            else:
+                w = max(w, self.num_pages_of(r), -(-(self.length(r) + 1) // P))
+        return w
 
     def release_outside_window(self, rid: int, window: int, sink_tokens: int = 0) -> int:
         n = ctypes.c_int32(0)

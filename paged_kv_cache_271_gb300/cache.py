@@ -130,6 +130,26 @@ class PagedKVCache:
             copy_pages(self.k, self.v, src, dst)
         return slots
 
+    def step(self, finished, joining, prompt_lens, live, width: int | None = None,
+             tables_out=None, lens_out=None, copies_out=None, incremental: bool = False):
+        """One continuous-batching step of bookkeeping in one library call: the ``finished``
+        requests are freed, the ``joining`` ones added and grown by their ``prompt_lens``, every
+        ``live`` request (joining ones included) gets room for one new token, and the live
+        requests' page-table rows and lengths are exported (into ``tables_out``/``lens_out``
+        when given). Returns (prompt slots, tables, lengths). Shared pages about to be written
+        are copied as in ``reserve``. If the pages run out, the frees stand and the joining
+        requests are not added (PkvError). ``incremental``: rows of ``tables_out`` that still
+        hold the same request as after the previous incremental step are only patched."""
+        slots, bt, cl, copies = self.table.step(finished, joining, prompt_lens, live, width,
+                                                tables_out, lens_out, incremental=incremental)
+        if copies_out is not None:
+            copies_out.extend(copies)
+        elif copies:
+            src = torch.tensor([c[0] for c in copies], dtype=torch.int32, device=self.k.device)
+            dst = torch.tensor([c[1] for c in copies], dtype=torch.int32, device=self.k.device)
+            copy_pages(self.k, self.v, src, dst)
+        return slots, bt, cl
+
     def write(self, slots, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
         """Append rows k_new/v_new [N, h_kv, d] at the given slots (host array or CUDA int64)."""
         if not isinstance(slots, torch.Tensor):

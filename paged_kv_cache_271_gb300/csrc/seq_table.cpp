@@ -31,6 +31,11 @@ struct Seq {
   std::vector<int32_t> pages;  // -1: released (outside a window)
   int64_t len = 0;
   uint64_t mark = 0;  // the table's epoch of the last batch call that listed it
+  // incremental table export: the row of the table's export buffer this request was last
+  // written to (-1: none), and the first column changed since
+  int64_t exp_row = -1;
+  int64_t dirty_from = 0;
+  void changed(int64_t col) { dirty_from = std::min(dirty_from, col); }
 };
 
 int64_t pages_for(int64_t tokens, int32_t P) { return (tokens + P - 1) / P; }
@@ -46,6 +51,13 @@ struct pkv_seq_table {
   uint64_t epoch = 0;
   std::vector<Seq*> listed;     // the requests of the current batch call, in order
   std::vector<int32_t> scratch;  // page lists of the current call
+  std::vector<int32_t> ones;     // per-request counts of 1 (pkv_seq_step)
+  std::vector<int64_t> slots;    // slots nobody asked for (pkv_seq_step)
+  // incremental table export (pkv_seq_step): the buffer and width it last wrote, and the
+  // request whose row each of its rows holds
+  mutable const int32_t* inc_buf = nullptr;  // (pkv_seq_tables into it forgets it)
+  int32_t inc_width = -1;
+  std::vector<int64_t> inc_owner;
 };
 
 extern "C" {
@@ -53,7 +65,7 @@ extern "C" {
 int pkv_seq_table_create(pkv_allocator* a, int32_t page_size, pkv_seq_table** out) {
   if (!a || !out || page_size <= 0)
     return pkv::set_error(PKV_EINVAL, "pkv_seq_table_create: bad argument");
-  *out = new (std::nothrow) pkv_seq_table{a, page_size, {}, 0, {}, {}};
+  *out = new (std::nothrow) pkv_seq_table{a, page_size, {}, 0, {}, {}, {}, {}, nullptr, -1, {}};
   if (!*out) return pkv::set_error(PKV_EINVAL, "pkv_seq_table_create: out of host memory");
   return PKV_OK;
 }
@@ -225,11 +237,13 @@ int pkv_seq_reserve(pkv_seq_table* t, const int64_t* rids, const int32_t* counts
         copy_src[nc] = src;
         copy_dst[nc] = dst;
         ++nc;
+        s.changed(s.len / P);
       }
     }
     const int64_t grow = pages_for(s.len + c, P) - (int64_t)s.pages.size();
     if (grow > 0) {
       const size_t old = s.pages.size();
+      s.changed((int64_t)old);
       s.pages.resize(old + grow);
       const int st = pkv_alloc(t->alloc, (int32_t)grow, s.pages.data() + old);
       if (st != PKV_OK) return st;
@@ -252,6 +266,7 @@ int pkv_seq_tables(const pkv_seq_table* t, const int64_t* rids, int32_t n, int32
                    int32_t* block_tables_out, int32_t* context_lens_out) {
   if (!t || n < 0 || (n > 0 && !rids) || width < 0)
     return pkv::set_error(PKV_EINVAL, "pkv_seq_tables: bad argument");
+  if (block_tables_out && block_tables_out == t->inc_buf) t->inc_buf = nullptr;
   for (int32_t i = 0; i < n; ++i) {
     auto it = t->seqs.find(rids[i]);
     if (it == t->seqs.end())
@@ -271,6 +286,148 @@ int pkv_seq_tables(const pkv_seq_table* t, const int64_t* rids, int32_t n, int32
                               (long long)rids[i]);
       context_lens_out[i] = (int32_t)s.len;
     }
+  }
+  return PKV_OK;
+}
+
+int pkv_seq_step(pkv_seq_table* t, const int64_t* free_rids, int32_t n_free,
+                 const int64_t* new_rids, const int32_t* prompt_counts, int32_t n_new,
+                 int64_t* prompt_slots_out, const int64_t* live_rids, int32_t n_live,
+                 int64_t* live_slots_out, int32_t width, int32_t* block_tables_out,
+                 int32_t* context_lens_out, int32_t incremental, int32_t* copy_src,
+                 int32_t* copy_dst, int32_t* n_copies) {
+  const char* who = "pkv_seq_step";
+  if (!t || n_free < 0 || n_new < 0 || n_live < 0 || width < 0 || !n_copies ||
+      (n_free > 0 && !free_rids) || (n_new > 0 && (!new_rids || !prompt_counts)) ||
+      (n_live > 0 && !live_rids))
+    return pkv::set_error(PKV_EINVAL, "%s: bad argument", who);
+  const int32_t P = t->page_size;
+  *n_copies = 0;
+  // ---- every check first: nothing has changed when one fails ----
+  const uint64_t ep_free = ++t->epoch;
+  for (int32_t i = 0; i < n_free; ++i) {
+    auto it = t->seqs.find(free_rids[i]);
+    if (it == t->seqs.end() || it->second.mark == ep_free)
+      return pkv::set_error(PKV_EINVAL, "%s: no request %lld to free (or listed twice)", who,
+                            (long long)free_rids[i]);
+    it->second.mark = ep_free;
+  }
+  // new requests: distinct, and not live unless freed by this call; value: prompt, listed live
+  std::unordered_map<int64_t, std::pair<int32_t, bool>> fresh;
+  int64_t prompt_total = 0;
+  for (int32_t i = 0; i < n_new; ++i) {
+    auto it = t->seqs.find(new_rids[i]);
+    if (prompt_counts[i] < 0 || (it != t->seqs.end() && it->second.mark != ep_free) ||
+        !fresh.emplace(new_rids[i], std::make_pair(prompt_counts[i], false)).second)
+      return pkv::set_error(PKV_EINVAL, "%s: new request %lld exists, is listed twice or has a "
+                            "negative prompt", who, (long long)new_rids[i]);
+    prompt_total += prompt_counts[i];
+  }
+  if (prompt_total > 0 && !prompt_slots_out)
+    return pkv::set_error(PKV_EINVAL, "%s: prompt_slots_out is NULL", who);
+  // live requests: distinct, live after the frees and adds, writable, and fitting the table
+  const uint64_t ep_live = ++t->epoch;
+  for (int32_t i = 0; i < n_live; ++i) {
+    int64_t len, pages;
+    auto f = fresh.find(live_rids[i]);
+    if (f != fresh.end()) {
+      if (f->second.second)
+        return pkv::set_error(PKV_EINVAL, "%s: request %lld listed twice", who,
+                              (long long)live_rids[i]);
+      f->second.second = true;
+      len = f->second.first;
+      pages = pages_for(len, P);
+    } else {
+      auto it = t->seqs.find(live_rids[i]);
+      if (it == t->seqs.end() || it->second.mark == ep_free || it->second.mark == ep_live)
+        return pkv::set_error(PKV_EINVAL, "%s: request %lld is not live (or listed twice)", who,
+                              (long long)live_rids[i]);
+      Seq& s = it->second;
+      s.mark = ep_live;
+      len = s.len;
+      pages = (int64_t)s.pages.size();
+      const int64_t lp = len / P;
+      if (lp < pages && s.pages[lp] < 0)
+        return pkv::set_error(PKV_EINVAL, "%s: request %lld writes into a released page", who,
+                              (long long)live_rids[i]);
+      if (lp < pages && (!copy_src || !copy_dst) && pkv_refcount(t->alloc, s.pages[lp]) > 1)
+        return pkv::set_error(PKV_EINVAL, "%s: request %lld writes into a shared page and the "
+                              "copy arrays are NULL", who, (long long)live_rids[i]);
+    }
+    if (len + 1 > INT32_MAX && context_lens_out)
+      return pkv::set_error(PKV_EINVAL, "%s: request %lld is longer than int32", who,
+                            (long long)live_rids[i]);
+    if (block_tables_out && std::max(pages, pages_for(len + 1, P)) > width)
+      return pkv::set_error(PKV_EINVAL, "%s: request %lld needs more than the table's %d "
+                            "columns", who, (long long)live_rids[i], width);
+  }
+  // ---- the finished requests go (this stands whatever follows) ----
+  int st = pkv_seq_free(t, free_rids, n_free);
+  if (st != PKV_OK) return st;
+  // ---- the new requests and their prompts, then one token for every live request; if the
+  // pages run out, the new requests are removed again (their prompt pages go back) ----
+  for (int32_t i = 0; i < n_new; ++i) t->seqs.emplace(new_rids[i], Seq{});
+  auto drop_new = [&]() {
+    std::vector<int32_t> live;
+    for (int32_t i = 0; i < n_new; ++i) {
+      auto it = t->seqs.find(new_rids[i]);
+      live.clear();
+      for (int32_t p : it->second.pages)
+        if (p >= 0) live.push_back(p);
+      if (!live.empty()) pkv_decref(t->alloc, live.data(), (int32_t)live.size());
+      t->seqs.erase(it);
+    }
+  };
+  int32_t none = 0;
+  st = pkv_seq_reserve(t, new_rids, prompt_counts, n_new, prompt_slots_out, nullptr, nullptr,
+                       &none);
+  if (st != PKV_OK) {
+    drop_new();
+    return st;
+  }
+  if (n_live > 0) {
+    t->ones.assign(n_live, 1);
+    int64_t* slots = live_slots_out;
+    if (!slots) {
+      t->slots.resize(n_live);
+      slots = t->slots.data();
+    }
+    st = pkv_seq_reserve(t, live_rids, t->ones.data(), n_live, slots, copy_src, copy_dst,
+                         n_copies);
+    if (st != PKV_OK) {
+      drop_new();
+      return st;
+    }
+  }
+  if (!incremental || !block_tables_out) {
+    if (block_tables_out) t->inc_buf = nullptr;  // (a full export may reuse that buffer)
+    return pkv_seq_tables(t, live_rids, n_live, width, block_tables_out, context_lens_out);
+  }
+  // incremental: a row that holds this request's row from the last export into this buffer
+  // (same width) is written only from the first column changed since; any other row in full
+  if (t->inc_buf != block_tables_out || t->inc_width != width) {
+    t->inc_buf = block_tables_out;
+    t->inc_width = width;
+    t->inc_owner.clear();
+  }
+  if ((int64_t)t->inc_owner.size() < n_live) t->inc_owner.resize(n_live, INT64_MIN);
+  for (int32_t i = 0; i < n_live; ++i) {
+    Seq& s = t->seqs.find(live_rids[i])->second;
+    int32_t* row = block_tables_out + (int64_t)i * width;
+    const int64_t np = (int64_t)s.pages.size();
+    if (t->inc_owner[i] == live_rids[i] && s.exp_row == i) {
+      for (int64_t c = s.dirty_from; c < np; ++c) row[c] = s.pages[c];
+    } else {
+      if (np) std::memcpy(row, s.pages.data(), np * sizeof(int32_t));
+      std::memset(row + np, 0, (width - np) * sizeof(int32_t));
+      if (s.exp_row >= 0 && s.exp_row < (int64_t)t->inc_owner.size() &&
+          t->inc_owner[s.exp_row] == live_rids[i])
+        t->inc_owner[s.exp_row] = INT64_MIN;  // that row is stale for this request now
+      t->inc_owner[i] = live_rids[i];
+      s.exp_row = i;
+    }
+    s.dirty_from = np;
+    if (context_lens_out) context_lens_out[i] = (int32_t)s.len;
   }
   return PKV_OK;
 }
@@ -295,6 +452,7 @@ int pkv_seq_release_outside_window(pkv_seq_table* t, int64_t rid, int64_t window
       if (last < s.len - 1 && first >= sink_tokens && last < s.len - window) {
         gone.push_back(s.pages[lp]);
         s.pages[lp] = -1;
+        s.changed((int64_t)lp);
       }
     }
   }

@@ -230,3 +230,200 @@ def test_prefix_cache_and_request_tables_compose():
     c.free_many([0, 1, 2])
     assert [c.allocator.refcount(p) for p in shared] == [1, 1, 1]  # the cache's own
     assert pc.evict(3) == 3 and c.allocator.num_free() == 32
+
+
+def _model_step(model, free, new, prompts, live):
+    """pkv_seq_step on the model: frees stand; if the pages run out, the new requests are
+    removed again (their pages returned in the library's order). Returns (prompt slots,
+    copies) or None when the pages ran out."""
+    model.free(free)
+    for r in new:
+        model.add(r)
+    before = copy.deepcopy(model)
+    out = None
+    try:
+        ps, c1 = model.reserve(new, prompts)
+    except MemoryError:
+        model.__dict__.update(before.__dict__)
+    else:
+        assert c1 == []
+        mid = copy.deepcopy(model)
+        try:
+            out = ps, model.reserve(live, [1] * len(live))[1]
+        except MemoryError:
+            model.__dict__.update(mid.__dict__)
+    if out is None:  # back to the state after the frees
+        for r in new:
+            model.a.decref([p for p in model.rows.pop(r) if p >= 0])
+            del model.lens[r]
+    return out
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_seq_step_against_model(seed):
+    rng = np.random.default_rng(100 + seed)
+    num_pages = 40
+    order = rng.permutation(num_pages)
+    alloc = pkv.PageAllocator(num_pages, order)
+    table = pkv.SeqTable(alloc, P)
+    model = SeqModel(num_pages, order)
+    next_id, seen = 0, {"ok": 0, "nopages": 0, "copies": 0, "reuse": 0}
+    for _ in range(300):
+        live = sorted(model.rows)
+        if live and rng.random() < 0.2:  # a fork between steps: shared pages, later copies
+            src = int(rng.choice(live))
+            model.fork([src], [next_id])
+            table.fork([src], [next_id])
+            next_id += 1
+            _same(model, table, alloc, num_pages)
+            continue
+        k = int(rng.integers(0, min(3, len(live)) + 1))
+        free = [int(x) for x in rng.choice(live, size=k, replace=False)] if k else []
+        new = []
+        if free and rng.random() < 0.2:  # a freed id comes back as a new request
+            new.append(free[0])
+            seen["reuse"] += 1
+        for _ in range(int(rng.integers(0, 3))):
+            new.append(next_id)
+            next_id += 1
+        prompts = [int(rng.choice([0, 1, 5, 16, 17, 40, 200, 400])) for _ in new]
+        rest = [r for r in live if r not in free]
+        keep = [r for r in rest if rng.random() < 0.85]
+        live_now = keep + [r for r in new if rng.random() < 0.9]
+        rng.shuffle(live_now)
+        live_now = [int(r) for r in live_now]
+        # a write into a released page is refused up front: keep such requests out
+        live_now = [r for r in live_now if r in new or model.lens[r] // P >= len(model.rows[r])
+                    or model.rows[r][model.lens[r] // P] >= 0]
+        width = num_pages
+        want = _model_step(model, free, new, prompts, live_now)
+        if want is None:
+            with pytest.raises(pkv.PkvError):
+                table.step(free, new, prompts, live_now, width)
+            seen["nopages"] += 1
+        else:
+            ps, bt, cl, copies = table.step(free, new, prompts, live_now, width)
+            assert ps.tolist() == want[0] and copies == want[1]
+            assert cl.tolist() == [model.lens[r] for r in live_now]
+            for i, r in enumerate(live_now):
+                row = model.rows[r]
+                assert bt[i].tolist() == row + [0] * (width - len(row))
+            seen["ok"] += 1
+            seen["copies"] += len(copies)
+        _same(model, table, alloc, num_pages)
+    assert all(v > 0 for v in seen.values()), seen
+    table.free(sorted(model.rows))
+    assert alloc.num_free() == num_pages
+
+
+def test_seq_step_checks_before_changing_anything():
+    alloc = pkv.PageAllocator(8)
+    t = pkv.SeqTable(alloc, P)
+    t.add(1)
+    t.add(2)
+    t.reserve([1, 2], [20, 3])
+    state = ([t.pages(r) for r in (1, 2)], t.lengths([1, 2]).tolist(), alloc.num_free())
+
+    def same():
+        assert ([t.pages(r) for r in (1, 2)], t.lengths([1, 2]).tolist(),
+                alloc.num_free()) == state and sorted(t.ids()) == [1, 2]
+
+    bad = [([9], [], [], [2]),            # unknown request to free
+           ([1, 1], [], [], [2]),         # freed twice
+           ([], [2], [4], [2]),           # a new id that is live
+           ([], [5, 5], [1, 1], [5]),     # a new id listed twice
+           ([1], [], [], [1]),            # a freed request decoded
+           ([], [], [], [2, 2]),          # decoded twice
+           ([], [], [], [7])]             # unknown live request
+    for free, new, prompts, live in bad:
+        with pytest.raises(pkv.PkvError):
+            t.step(free, new, prompts, live, 8)
+        same()
+    with pytest.raises(pkv.PkvError):
+        t.step([2], [], [], [1], 1)  # request 1 needs 2 columns: refused before the free
+    same()
+    # a freed id may come back as a new request in the same step
+    ps, bt, cl, cp = t.step([2], [2], [5], [1, 2], 4)
+    assert len(ps) == 5 and cl.tolist() == [21, 6] and cp == []
+    # out of pages: the frees stand, the new requests are gone again
+    free_before = alloc.num_free()
+    with pytest.raises(pkv.PkvError):
+        t.step([2], [3], [16 * 8], [1, 3], 16)
+    assert sorted(t.ids()) == [1] and alloc.num_free() == free_before + 1
+    t.free([1])
+    assert alloc.num_free() == 8
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_seq_step_incremental_tables_stay_exact(seed):
+    # one buffer across steps, rows patched in place: after every step it must equal the
+    # model's rows; slots keep their requests (a replacement takes a finished one's row),
+    # with shuffles, window releases, forks and a plain export into the same buffer mixed in
+    rng = np.random.default_rng(200 + seed)
+    num_pages = 48
+    order = rng.permutation(num_pages)
+    alloc = pkv.PageAllocator(num_pages, order)
+    table = pkv.SeqTable(alloc, P)
+    model = SeqModel(num_pages, order)
+    width = num_pages
+    buf = np.full((64, width), -7, dtype=np.int32)
+    lens = np.zeros(64, dtype=np.int32)
+    slots = []  # live request per row, in row order
+    next_id = 0
+    seen = {"patched": 0, "shuffle": 0, "release": 0, "plain": 0, "fork": 0, "nopages": 0}
+    for _ in range(250):
+        r = rng.random()
+        if slots and r < 0.1:
+            rid = int(rng.choice(slots))
+            window, sink = int(rng.choice([5, 20, 40])), int(rng.choice([0, 4]))
+            assert table.release_outside_window(rid, window, sink) == model.release(rid, window,
+                                                                                     sink)
+            seen["release"] += 1
+        elif slots and r < 0.15:
+            src = int(rng.choice(slots))
+            model.fork([src], [next_id])
+            table.fork([src], [next_id])
+            slots.append(next_id)
+            next_id += 1
+            seen["fork"] += 1
+        elif slots and r < 0.2:
+            table.tables(slots, width, out=buf[:len(slots)])  # forgets the incremental state
+            seen["plain"] += 1
+        elif slots and r < 0.3:
+            rng.shuffle(slots)
+            seen["shuffle"] += 1
+        k = int(rng.integers(0, min(2, len(slots)) + 1))
+        free = [int(x) for x in rng.choice(slots, size=k, replace=False)] if k else []
+        new = [next_id + i for i in range(int(rng.integers(0, 3)))]
+        next_id += len(new)
+        prompts = [int(rng.choice([0, 3, 16, 17, 40, 120, 400])) for _ in new]
+        live = list(slots)
+        for i, f in enumerate(free):  # a new request takes a finished one's row
+            j = live.index(f)
+            if i < len(new):
+                live[j] = new[i]
+            else:
+                live[j] = None
+        live = [x for x in live if x is not None] + new[len(free):]
+        live = [x for x in live if x in new or model.lens[x] // P >= len(model.rows[x])
+                or model.rows[x][model.lens[x] // P] >= 0]
+        want = _model_step(model, free, new, prompts, live)
+        if want is None:
+            with pytest.raises(pkv.PkvError):
+                table.step(free, new, prompts, live, width, buf[:len(live)], lens[:len(live)],
+                           incremental=True)
+            slots = [x for x in slots if x not in free]
+            seen["nopages"] += 1
+            _same(model, table, alloc, num_pages)
+            continue
+        ps, _, _, copies = table.step(free, new, prompts, live, width, buf[:len(live)],
+                                      lens[:len(live)], incremental=True)
+        assert ps.tolist() == want[0] and copies == want[1]
+        slots = live
+        for i, x in enumerate(slots):
+            row = model.rows[x]
+            assert buf[i].tolist() == row + [0] * (width - len(row)), (i, x)
+            assert lens[i] == model.lens[x]
+        seen["patched"] += 1
+        _same(model, table, alloc, num_pages)
+    assert all(v > 0 for v in seen.values()), seen
