@@ -613,6 +613,15 @@ int pkv_trace_enable(int on);
 int pkv_trace_reset(void);
 int pkv_trace_read(const char* kernel, int32_t* launches_out, double* total_ms_out);
 
+/*
+ * Self-test of the kernels' failure detection: one thread waits, with the same bounded wait
+ * every kernel uses on its copy barriers, on a barrier that nothing completes. After the wait's
+ * limit (2 s) it gives up: PKV_DEVERR_TIMEOUT is OR-ed into *err_dev and *done_dev is set to 1
+ * (2 would mean the wait completed). err_dev and done_dev are device int32 words owned by the
+ * caller; asynchronous on the stream. Nothing faults or hangs; the context stays usable.
+ */
+int pkv_selftest_wait_timeout(int32_t* err_dev, int32_t* done_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -153,6 +153,7 @@ def lib():
         "pkv_cascade_set_prefix_kernel": (ctypes.c_int, [i32]),
         "pkv_trace_enable": (ctypes.c_int, [ctypes.c_int]),
         "pkv_trace_reset": (ctypes.c_int, []),
+        "pkv_selftest_wait_timeout": (ctypes.c_int, [vp, vp, vp]),
         "pkv_trace_read": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(i32),
                                           ctypes.POINTER(dbl)]),
     }
@@ -661,6 +662,18 @@ def device_error(stream=None) -> int:
 def decode_set_warp_per_request(on: bool):
     """One warp per request when every request fits one chunk of at most 16 pages (default)."""
     _check(lib().pkv_decode_set_warp_per_request(1 if on else 0))
+
+
+def selftest_wait_timeout(stream=None):
+    """Makes one bounded kernel wait run out on purpose (pkv_selftest_wait_timeout: a barrier
+    nothing completes, given up after the kernels' 2 s limit) and returns (status bits, done):
+    DEVERR_TIMEOUT set and done == 1 when the wait gave up as it should."""
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    done = torch.zeros_like(err)
+    st = stream if stream is not None else torch.cuda.current_stream()
+    _check(lib().pkv_selftest_wait_timeout(_dev(err, "err"), _dev(done, "done"), _stream(st)))
+    st.synchronize()
+    return int(err.item()), int(done.item())
 
 
 def cascade_set_overlap(on):
