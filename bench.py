@@ -862,6 +862,22 @@ def trace_joins(tr):
              for b in range(tr.batch) if tr.finish[s - 1, b]] for s in range(tr.steps)]
 
 
+def trace_bookkeeping(cache, tr, joins, rid_arr, width, tables_out, lens_out):
+    """One step's scheduler bookkeeping for a continuous-batching trace, in one library call
+    (PagedKVCache.step -> pkv_seq_step): the finished requests of ``joins`` (slot, finished,
+    new) are freed, the new ones take their slots in ``rid_arr`` and get room for their
+    prompts, every live request gets room for one token, and the live requests' table rows
+    (patched in place where a slot keeps its request) and lengths go to ``tables_out`` /
+    ``lens_out``. Returns the prompts' slots, request by request in ``joins`` order."""
+    old = np.array([o for _, o, _ in joins], dtype=np.int64)
+    new = np.array([r for _, _, r in joins], dtype=np.int64)
+    for b, _, rid in joins:
+        rid_arr[b] = rid
+    slots, _, _ = cache.step(old, new, tr.prompt_lens[new], rid_arr, width,
+                             tables_out=tables_out, lens_out=lens_out, incremental=True)
+    return slots
+
+
 def run_trace(args):
     """FP8 (or INT8) continuous batching over the whole trace: 256 request slots, contexts
     U[128, 8192] at the start; every step each live request gains one token, and a request
@@ -935,16 +951,10 @@ def run_trace(args):
         q[0].copy_(tr.step_q(s))
 
     def host(s):
-        """Frees, new requests, slots, tables: the bookkeeping a scheduler does per step, in one
-        library call (pkv_seq_step; table rows patched in place where they keep a request)."""
-        j = joins_at[s]
-        old = np.array([o for _, o, _ in j], dtype=np.int64)
-        new = np.array([r for _, _, r in j], dtype=np.int64)
-        for b, _, rid in j:  # a new request takes the finished one's slot
+        """Frees, new requests, slots, tables: the bookkeeping a scheduler does per step."""
+        for b, _, rid in joins_at[s]:  # a new request takes the finished one's slot
             run.slot_rid[b] = rid
-            rid_arr[b] = rid
-        slots, _, _ = cache.step(old, new, tr.prompt_lens[new], rid_arr, width,
-                                 tables_out=bt[0], lens_out=cl[0], incremental=True)
+        slots = trace_bookkeeping(cache, tr, joins_at[s], rid_arr, width, bt[0], cl[0])
         npr = len(slots)
         if npr:
             ps[0].numpy()[:npr] = slots

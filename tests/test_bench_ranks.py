@@ -3,6 +3,7 @@ step time and a whole-job aggregate. No GPU and no data-path collective."""
 import os
 import socket
 
+import numpy as np
 import pytest
 import torch.multiprocessing as mp
 
@@ -77,3 +78,38 @@ def test_trace_joins_follow_the_request_table():
             seen.add(new)
         assert live == list(tr.rid_table[s])  # every other slot keeps its request
     assert sorted(seen) == list(range(len(tr.prompt_lens)))  # ids 0, 1, ... in join order
+
+
+def test_trace_bookkeeping_full_size_matches_the_trace():
+    # the bench's per-step bookkeeping over the whole 256-slot trace, host only: incrementally
+    # patched tables equal a full export, lengths equal each request's position + 1, and the
+    # prompts get exactly their token counts of distinct slots
+    import torch
+    import paged_kv_cache_271_gb300 as pkv
+    from paged_kv_cache_271_gb300.cache import PagedKVCache
+    import workloads
+    tr = workloads.fp8_continuous_batching(steps=35)
+    B = tr.batch
+    cache = PagedKVCache(tr.num_pages, 1, 16, torch.uint8, device="cpu",
+                         initial_free_order=tr.page_order)
+    for b in range(B):
+        cache.add_request(b)
+    cache.reserve(list(range(B)), [int(x) for x in tr.initial_lens])
+    joins = bench.trace_joins(tr)
+    width = pkv.pages_needed(int(tr.prompt_lens.max()) + tr.steps)
+    bt = torch.zeros((B, width), dtype=torch.int32)
+    cl = torch.zeros(B, dtype=torch.int32)
+    rid_arr = np.arange(B, dtype=np.int64)
+    start = {b: 0 for b in range(B)}
+    for s in range(tr.steps):
+        for _, _, r in joins[s]:
+            start[r] = s
+        slots = bench.trace_bookkeeping(cache, tr, joins[s], rid_arr, width, bt, cl)
+        assert rid_arr.tolist() == [int(r) for r in tr.rid_table[s]]
+        want = [int(tr.prompt_lens[r]) + s - start[r] + 1 for r in tr.rid_table[s]]
+        assert cl.tolist() == want
+        assert np.array_equal(bt.numpy(), cache.block_table_array(rid_arr, width))
+        n = sum(int(tr.prompt_lens[r]) for _, _, r in joins[s])
+        assert len(slots) == n and len(set(slots.tolist())) == n
+    assert cache.allocator.num_free() + sum(len(cache.pages[r]) for r in rid_arr.tolist()) \
+        == tr.num_pages
