@@ -51,33 +51,36 @@ _DT = {"f32": F32, "bf16": BF16, "fp8_e4m3": E4M3, "int8": INT8}
 _lib = None
 
 
+def bind(L):
+    """Declare the C oracle's entry points on a loaded library ``L`` and return it."""
+    vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+    L.oracle_e4m3_value.restype = ctypes.c_double
+    L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+    L.oracle_e4m3_encode.restype = ctypes.c_uint8
+    L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    L.oracle_quantize_e4m3.restype = None
+    L.oracle_quantize_e4m3.argtypes = [vp, i64, ctypes.c_float, vp]
+    L.oracle_quantize_int8.restype = None
+    L.oracle_quantize_int8.argtypes = [vp, i64, ctypes.c_float, vp]
+    L.oracle_attend.restype = None
+    L.oracle_attend.argtypes = [vp, vp, vp, i64, i32, dbl, vp]
+    L.oracle_paged_decode.restype = i32
+    L.oracle_paged_decode.argtypes = [vp, i32, i32, i32, i32, vp, vp, i32, i32, i32, i32,
+                                      vp, i32, vp, dbl, vp, vp, vp, i32, vp, i32, i32, i32]
+    L.oracle_contiguous_decode.restype = i32
+    L.oracle_contiguous_decode.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, i32, i32,
+                                           i32, vp, vp, dbl, vp, vp, vp, i32, vp, i32, i32,
+                                           i32]
+    L.oracle_max_threads.restype = i32
+    L.oracle_max_threads.argtypes = []
+    return L
+
+
 def lib():
     """The compiled C oracle (built on first use)."""
     global _lib
     if _lib is None:
-        path = _build.build()
-        L = ctypes.CDLL(path)
-        vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
-        L.oracle_e4m3_value.restype = ctypes.c_double
-        L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
-        L.oracle_e4m3_encode.restype = ctypes.c_uint8
-        L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
-        L.oracle_quantize_e4m3.restype = None
-        L.oracle_quantize_e4m3.argtypes = [vp, i64, ctypes.c_float, vp]
-        L.oracle_quantize_int8.restype = None
-        L.oracle_quantize_int8.argtypes = [vp, i64, ctypes.c_float, vp]
-        L.oracle_attend.restype = None
-        L.oracle_attend.argtypes = [vp, vp, vp, i64, i32, dbl, vp]
-        L.oracle_paged_decode.restype = i32
-        L.oracle_paged_decode.argtypes = [vp, i32, i32, i32, i32, vp, vp, i32, i32, i32, i32,
-                                          vp, i32, vp, dbl, vp, vp, vp, i32, vp, i32, i32, i32]
-        L.oracle_contiguous_decode.restype = i32
-        L.oracle_contiguous_decode.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, i32, i32,
-                                               i32, vp, vp, dbl, vp, vp, vp, i32, vp, i32, i32,
-                                               i32]
-        L.oracle_max_threads.restype = i32
-        L.oracle_max_threads.argtypes = []
-        _lib = L
+        _lib = bind(ctypes.CDLL(_build.build()))
     return _lib
 
 
