@@ -376,7 +376,8 @@ int pkv_seq_tables(const pkv_seq_table* t, const int64_t* rids, int32_t n, int32
  * tokens (their slots, request by request, to prompt_slots_out: host, sum of prompt_counts);
  * every one of the n_live live requests -- which may include new ones -- is grown by one token
  * (slots to live_slots_out, host [n_live], or NULL), with copy-on-write as in pkv_seq_reserve
- * (copy_src/copy_dst: host, room for n_live pairs, or NULL when no live page is shared;
+ * (copy_src/copy_dst: host, room for n_live pairs, or NULL when no live page is shared
+ * once the frees are done -- references held by the finished requests do not count;
  * *n_copies set); and their block-table rows and token counts are written as by
  * pkv_seq_tables (block_tables_out [n_live][width] and context_lens_out [n_live], host,
  * either may be NULL). With incremental != 0, a row that already holds the same request's
@@ -397,6 +398,14 @@ int pkv_seq_step(pkv_seq_table* t, const int64_t* free_rids, int32_t n_free,
                  int64_t* live_slots_out, int32_t width, int32_t* block_tables_out,
                  int32_t* context_lens_out, int32_t incremental, int32_t* copy_src,
                  int32_t* copy_dst, int32_t* n_copies);
+/* The table width (columns) a pkv_seq_step with these new requests, prompts and live requests
+ * needs: the most pages any live request holds after it grows by its prompt (a new request)
+ * and one token -- ceil((length + 1) / page_size), or more where it already holds more rows --
+ * and at least 1. Host arrays; PKV_EINVAL for an unknown live id that is not new, or a
+ * negative prompt. Changes nothing. */
+int pkv_seq_step_width(const pkv_seq_table* t, const int64_t* new_rids,
+                       const int32_t* prompt_counts, int32_t n_new, const int64_t* live_rids,
+                       int32_t n_live, int32_t* width_out);
 /* Releases every page of the request whose positions all lie at or past sink_tokens, before
  * the last `window` positions and before the newest token (window 0: none); their row entries
  * become -1. *released (may be NULL) receives the count. */
@@ -596,6 +605,16 @@ int pkv_prefix_lookup(pkv_prefix_cache* c, int64_t tenant, const int32_t* tokens
  * cached for the same prefix are kept (the caller's copies are not taken). */
 int pkv_prefix_insert(pkv_prefix_cache* c, int64_t tenant, const int32_t* tokens, int64_t n,
                       const int32_t* pages, int32_t n_pages);
+/* pkv_prefix_insert of request rid's own pages (a request table over the same allocator): the
+ * full pages among the first min(n, its length) tokens, tokens[0..n) being its prompt. */
+int pkv_prefix_insert_request(pkv_prefix_cache* c, int64_t tenant, const int32_t* tokens,
+                              int64_t n, const pkv_seq_table* t, int64_t rid);
+/* A new request rid in table t whose prompt is tokens[0..n): it starts on the pages of the
+ * longest prefix the cache holds for this tenant (a pkv_prefix_lookup whose references the
+ * request adopts, pkv_seq_adopt); *cached_tokens receives the prompt tokens already cached
+ * (whole pages). On an error nothing changes and no reference is kept. */
+int pkv_seq_add_cached_prefix(pkv_seq_table* t, int64_t rid, pkv_prefix_cache* c, int64_t tenant,
+                              const int32_t* tokens, int64_t n, int64_t* cached_tokens);
 /* Releases up to max_pages least recently used entries that end a cached chain and whose page
  * only the cache references; *n_evicted receives the count. */
 int pkv_prefix_evict(pkv_prefix_cache* c, int32_t max_pages, int32_t* n_evicted);

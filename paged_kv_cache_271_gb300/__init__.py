@@ -117,6 +117,10 @@ def lib():
         "pkv_seq_tables": (ctypes.c_int, [vp, vp, i32, i32, vp, vp]),
         "pkv_seq_step": (ctypes.c_int, [vp, vp, i32, vp, vp, i32, vp, vp, i32, vp, i32, vp, vp,
                                         i32, vp, vp, ctypes.POINTER(i32)]),
+        "pkv_seq_step_width": (ctypes.c_int, [vp, vp, vp, i32, vp, i32, ctypes.POINTER(i32)]),
+        "pkv_seq_add_cached_prefix": (ctypes.c_int, [vp, i64, vp, i64, vp, i64,
+                                                     ctypes.POINTER(i64)]),
+        "pkv_prefix_insert_request": (ctypes.c_int, [vp, i64, vp, i64, vp, i64]),
         "pkv_seq_release_outside_window": (ctypes.c_int, [vp, i64, i64, i64,
                                                           ctypes.POINTER(i32)]),
         "pkv_seq_len": (i64, [vp, i64]),
@@ -761,14 +765,11 @@ class PageAllocator:
     def cow_page(self, row: list, position: int, page_size: int = 16):
         """Copy-on-write for a write at ``position`` of a request with pages ``row`` (updated
         in place). Returns (src, dst) to copy, or None when the page is private."""
-        lp = int(position) // int(page_size)
-        if lp >= len(row):
-            return None  # the write starts a page the request does not have yet
-        one = (ctypes.c_int32 * 1)(int(row[lp]))  # only the written page matters
+        r = (ctypes.c_int32 * max(len(row), 1))(*[int(x) for x in row])
         src, dst = ctypes.c_int32(-1), ctypes.c_int32(-1)
-        _check(lib().pkv_cow_page(self._h, one, 1, int(position) % int(page_size),
-                                  int(page_size), ctypes.byref(src), ctypes.byref(dst)))
-        row[lp] = int(one[0])
+        _check(lib().pkv_cow_page(self._h, r, len(row), int(position), int(page_size),
+                                  ctypes.byref(src), ctypes.byref(dst)))
+        row[:] = list(r)[:len(row)]
         return None if src.value < 0 else (int(src.value), int(dst.value))
 
 
@@ -784,6 +785,21 @@ def _counts(counts) -> np.ndarray:
 
 def _ptr(a: np.ndarray):
     return a.ctypes.data if a.size else None
+
+
+def _host_int32(a, shape, name):
+    """``a`` if it is a C-contiguous int32 host array (numpy, or a CPU tensor) of ``shape``;
+    the library writes through its address."""
+    if isinstance(a, torch.Tensor):
+        ok = (a.device.type == "cpu" and a.dtype == torch.int32 and a.is_contiguous() and
+              tuple(a.shape) == tuple(shape))
+    else:
+        ok = (isinstance(a, np.ndarray) and a.dtype == np.int32 and a.flags.c_contiguous and
+              a.flags.writeable and a.shape == tuple(shape))
+    if not ok:
+        raise PkvError(-2, "%s must be a C-contiguous int32 host array of shape %s" %
+                       (name, tuple(shape)))
+    return a
 
 
 class SeqTable:
@@ -869,9 +885,18 @@ class SeqTable:
             raise PkvError(-1, "new_rids and prompt_counts differ in length")
         n = lv.size
         if width is None:
-            width = self._step_width(lv, nw, c)
-        bt = np.empty((n, int(width)), dtype=np.int32) if tables_out is None else tables_out
-        cl = np.empty(n, dtype=np.int32) if lens_out is None else lens_out
+            w = ctypes.c_int32(0)
+            _check(lib().pkv_seq_step_width(self._h, _ptr(nw), _ptr(c), nw.size, _ptr(lv), n,
+                                            ctypes.byref(w)))
+            width = w.value
+        if tables_out is None:
+            # a fresh array every call: the previous call's rows are not in it
+            incremental = False
+            bt = np.empty((n, int(width)), dtype=np.int32)
+        else:
+            bt = _host_int32(tables_out, (n, int(width)), "tables_out")
+        cl = np.empty(n, dtype=np.int32) if lens_out is None else _host_int32(lens_out, (n,),
+                                                                              "lens_out")
         ptr = (lambda a: a.data_ptr() if isinstance(a, torch.Tensor) else a.ctypes.data)
         ps = np.empty(int(c.sum()) if c.size else 0, dtype=np.int64)
         ls = np.empty(n, dtype=np.int64) if live_slots else None
@@ -885,17 +910,6 @@ class SeqTable:
                                   ctypes.byref(nc)))
         copies = [(int(src[i]), int(dst[i])) for i in range(nc.value)]
         return (ps, bt, cl, copies) + ((ls,) if live_slots else ())
-
-    def _step_width(self, live, new, prompts):
-        """Columns the live requests need after a step (at least 1)."""
-        pr = dict(zip(new.tolist(), prompts.tolist()))
-        P, w = self.page_size, 1
-        for r in live.tolist():
-            if r in pr:
-                w = max(w, -(-(pr[r] + 1) // P))
-            else:
-                w = max(w, self.num_pages_of(r), -(-(self.length(r) + 1) // P))
-        return w
 
     def release_outside_window(self, rid: int, window: int, sink_tokens: int = 0) -> int:
         n = ctypes.c_int32(0)
@@ -947,7 +961,7 @@ class PrefixCache:
     def lookup(self, tenant: int, tokens, max_pages: int = 1 << 20) -> list:
         """Pages of the longest cached prefix (the caller gets a reference on each)."""
         t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
-        cap = min(max_pages, len(t) // self.page_size)
+        cap = min(max_pages, t.size)  # room for any whole-page count; the library counts them
         out = np.empty(max(cap, 1), dtype=np.int32)
         n = ctypes.c_int32(0)
         _check(lib().pkv_prefix_lookup(self._h, int(tenant), t.ctypes.data if t.size else None,
@@ -967,6 +981,22 @@ class PrefixCache:
 
     def size(self) -> int:
         return int(lib().pkv_prefix_size(self._h))
+
+    def insert_request(self, tenant: int, tokens, table: SeqTable, rid: int):
+        """Caches the full pages of request ``rid``'s prompt ``tokens`` (already written)."""
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        _check(lib().pkv_prefix_insert_request(self._h, int(tenant), _ptr(t), t.size, table._h,
+                                               int(rid)))
+
+    def add_request(self, table: SeqTable, rid: int, tenant: int, tokens) -> int:
+        """New request ``rid`` in ``table`` starting on the longest cached prefix of its prompt
+        ``tokens`` (the lookup's references become the request's); returns the prompt tokens
+        already cached."""
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        n = ctypes.c_int64(0)
+        _check(lib().pkv_seq_add_cached_prefix(table._h, int(rid), self._h, int(tenant), _ptr(t),
+                                               t.size, ctypes.byref(n)))
+        return int(n.value)
 
 
 def trace_enable(on: bool = True):

@@ -81,17 +81,12 @@ class PagedKVCache:
         pages that ``prefix_cache`` holds for this tenant (the lookup's references become the
         request's). Returns the number of prompt tokens already in the cache; the caller
         reserves and writes the rest."""
-        pages = prefix_cache.lookup(tenant, tokens)
-        self.table.add(rid, pages, len(pages) * self.page_size, adopt=True)
-        return len(pages) * self.page_size
+        return prefix_cache.add_request(self.table, rid, tenant, tokens)
 
     def register_prompt(self, rid: int, prefix_cache, tenant: int, tokens):
         """Puts the full pages of request ``rid``'s prompt (``tokens``, already written) into
         ``prefix_cache`` for later requests of the same tenant."""
-        n_full = min(len(tokens), self.table.length(rid)) // self.page_size
-        if n_full:
-            prefix_cache.insert(tenant, list(tokens)[:n_full * self.page_size],
-                                self.table.pages(rid)[:n_full])
+        prefix_cache.insert_request(tenant, tokens, self.table, rid)
 
     def fork(self, src_rid: int, new_rid: int):
         """A new request sharing every page of ``src_rid`` (parallel sampling, beam search);

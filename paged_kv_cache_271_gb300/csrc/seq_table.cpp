@@ -350,9 +350,18 @@ int pkv_seq_step(pkv_seq_table* t, const int64_t* free_rids, int32_t n_free,
       if (lp < pages && s.pages[lp] < 0)
         return pkv::set_error(PKV_EINVAL, "%s: request %lld writes into a released page", who,
                               (long long)live_rids[i]);
-      if (lp < pages && (!copy_src || !copy_dst) && pkv_refcount(t->alloc, s.pages[lp]) > 1)
-        return pkv::set_error(PKV_EINVAL, "%s: request %lld writes into a shared page and the "
-                              "copy arrays are NULL", who, (long long)live_rids[i]);
+      if (lp < pages && (!copy_src || !copy_dst)) {
+        // shared once the frees are done: references held by finished requests do not count
+        const int32_t page = s.pages[lp];
+        int32_t ref = pkv_refcount(t->alloc, page);
+        for (int32_t k = 0; k < n_free && ref > 1; ++k) {
+          const std::vector<int32_t>& fp = t->seqs.find(free_rids[k])->second.pages;
+          ref -= (int32_t)std::count(fp.begin(), fp.end(), page);
+        }
+        if (ref > 1)
+          return pkv::set_error(PKV_EINVAL, "%s: request %lld writes into a shared page and the "
+                                "copy arrays are NULL", who, (long long)live_rids[i]);
+      }
     }
     if (len + 1 > INT32_MAX && context_lens_out)
       return pkv::set_error(PKV_EINVAL, "%s: request %lld is longer than int32", who,
@@ -430,6 +439,74 @@ int pkv_seq_step(pkv_seq_table* t, const int64_t* free_rids, int32_t n_free,
     if (context_lens_out) context_lens_out[i] = (int32_t)s.len;
   }
   return PKV_OK;
+}
+
+int pkv_seq_step_width(const pkv_seq_table* t, const int64_t* new_rids,
+                       const int32_t* prompt_counts, int32_t n_new, const int64_t* live_rids,
+                       int32_t n_live, int32_t* width_out) {
+  if (!t || n_new < 0 || n_live < 0 || (n_new > 0 && (!new_rids || !prompt_counts)) ||
+      (n_live > 0 && !live_rids) || !width_out)
+    return pkv::set_error(PKV_EINVAL, "pkv_seq_step_width: bad argument");
+  const int32_t P = t->page_size;
+  int64_t w = 1;
+  for (int32_t i = 0; i < n_live; ++i) {
+    const int64_t rid = live_rids[i];
+    int32_t k = 0;
+    while (k < n_new && new_rids[k] != rid) ++k;
+    if (k < n_new) {
+      if (prompt_counts[k] < 0)
+        return pkv::set_error(PKV_EINVAL, "pkv_seq_step_width: negative prompt");
+      w = std::max(w, pages_for((int64_t)prompt_counts[k] + 1, P));
+      continue;
+    }
+    auto it = t->seqs.find(rid);
+    if (it == t->seqs.end())
+      return pkv::set_error(PKV_EINVAL, "pkv_seq_step_width: no request %lld", (long long)rid);
+    w = std::max(w, std::max((int64_t)it->second.pages.size(), pages_for(it->second.len + 1, P)));
+  }
+  if (w > INT32_MAX) return pkv::set_error(PKV_EINVAL, "pkv_seq_step_width: row too wide");
+  *width_out = (int32_t)w;
+  return PKV_OK;
+}
+
+int pkv_seq_add_cached_prefix(pkv_seq_table* t, int64_t rid, pkv_prefix_cache* c, int64_t tenant,
+                              const int32_t* tokens, int64_t n_tokens, int64_t* cached_tokens) {
+  if (!t || !c || n_tokens < 0 || (n_tokens > 0 && !tokens) || !cached_tokens)
+    return pkv::set_error(PKV_EINVAL, "pkv_seq_add_cached_prefix: bad argument");
+  if (t->seqs.count(rid))
+    return pkv::set_error(PKV_EINVAL, "pkv_seq_add_cached_prefix: request %lld exists",
+                          (long long)rid);
+  const int64_t whole = n_tokens / t->page_size;
+  std::vector<int32_t>& pages = t->scratch;
+  pages.assign((size_t)std::max<int64_t>(whole, 1), -1);
+  int32_t n = 0;
+  int st = pkv_prefix_lookup(c, tenant, tokens, n_tokens, pages.data(),
+                             (int32_t)std::min<int64_t>(whole, INT32_MAX), &n);
+  if (st != PKV_OK) return st;
+  st = seq_add(t, rid, pages.data(), n, (int64_t)n * t->page_size, false,
+               "pkv_seq_add_cached_prefix");
+  if (st != PKV_OK) {
+    if (n > 0) pkv_decref(t->alloc, pages.data(), n);  // hand the lookup's references back
+    return st;
+  }
+  *cached_tokens = (int64_t)n * t->page_size;
+  return PKV_OK;
+}
+
+int pkv_prefix_insert_request(pkv_prefix_cache* c, int64_t tenant, const int32_t* tokens,
+                              int64_t n_tokens, const pkv_seq_table* t, int64_t rid) {
+  if (!c || !t || n_tokens < 0 || (n_tokens > 0 && !tokens))
+    return pkv::set_error(PKV_EINVAL, "pkv_prefix_insert_request: bad argument");
+  auto it = t->seqs.find(rid);
+  if (it == t->seqs.end())
+    return pkv::set_error(PKV_EINVAL, "pkv_prefix_insert_request: no request %lld",
+                          (long long)rid);
+  const Seq& s = it->second;
+  const int64_t n = std::min(n_tokens, s.len);  // tokens both written and given
+  const int64_t full = std::min<int64_t>(n / t->page_size, (int64_t)s.pages.size());
+  if (full == 0) return PKV_OK;
+  return pkv_prefix_insert(c, tenant, tokens, full * t->page_size, s.pages.data(),
+                           (int32_t)full);
 }
 
 int pkv_seq_release_outside_window(pkv_seq_table* t, int64_t rid, int64_t window,

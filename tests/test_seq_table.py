@@ -295,7 +295,7 @@ def test_seq_step_against_model(seed):
         # a write into a released page is refused up front: keep such requests out
         live_now = [r for r in live_now if r in new or model.lens[r] // P >= len(model.rows[r])
                     or model.rows[r][model.lens[r] // P] >= 0]
-        width = num_pages
+        width = num_pages if rng.random() < 0.5 else None  # None: the library sizes the rows
         want = _model_step(model, free, new, prompts, live_now)
         if want is None:
             with pytest.raises(pkv.PkvError):
@@ -303,6 +303,9 @@ def test_seq_step_against_model(seed):
             seen["nopages"] += 1
         else:
             ps, bt, cl, copies = table.step(free, new, prompts, live_now, width)
+            if width is None:  # the widest live row after the step, at least one column
+                width = max([len(model.rows[r]) for r in live_now] + [1])
+                assert bt.shape == (len(live_now), width)
             assert ps.tolist() == want[0] and copies == want[1]
             assert cl.tolist() == [model.lens[r] for r in live_now]
             for i, r in enumerate(live_now):
@@ -427,3 +430,83 @@ def test_seq_step_incremental_tables_stay_exact(seed):
         seen["patched"] += 1
         _same(model, table, alloc, num_pages)
     assert all(v > 0 for v in seen.values()), seen
+
+
+def test_seq_step_checks_its_host_buffers():
+    alloc = pkv.PageAllocator(16)
+    t = pkv.SeqTable(alloc, P)
+    t.step([], [1, 2], [20, 3], [1, 2], width=4)
+    for bad in (np.zeros((2, 3), np.int32), np.zeros((2, 4), np.int64),
+                np.zeros((4, 2), np.int32).T, np.zeros((3, 4), np.int32)):
+        with pytest.raises(pkv.PkvError):
+            t.step([], [], [], [1, 2], width=4, tables_out=bad)
+    with pytest.raises(pkv.PkvError):
+        t.step([], [], [], [1, 2], width=4, lens_out=np.zeros(3, np.int32))
+    assert t.lengths([1, 2]).tolist() == [21, 4]  # the refused calls changed nothing
+    # incremental without a buffer of the caller's: every row is written in full
+    for _ in range(3):
+        _, bt, cl, _ = t.step([], [], [], [1, 2], width=4, incremental=True)
+        assert bt.tolist() == [t.pages(1) + [0] * (4 - len(t.pages(1))),
+                               t.pages(2) + [0] * (4 - len(t.pages(2)))]
+    import torch
+    out = torch.zeros(2, 4, dtype=torch.int32)
+    _, bt, _, _ = t.step([], [], [], [1, 2], width=4, tables_out=out)
+    assert bt is out and out[0].tolist()[:2] == t.pages(1)
+
+
+def test_seq_step_judges_sharing_after_the_frees():
+    # a forked child writes into the partly filled page it shares with its parent; when the
+    # parent finishes in the same step, the page is the child's alone and needs no copy
+    import ctypes
+    alloc = pkv.PageAllocator(8)
+    t = pkv.SeqTable(alloc, P)
+    t.add(1)
+    t.reserve([1], [20])  # one full page and a partly filled one
+    L = pkv.lib()
+
+    def step(free, live):
+        f = np.array(free, np.int64)
+        lv = np.array(live, np.int64)
+        bt = np.zeros((len(live), 4), np.int32)
+        cl = np.zeros(len(live), np.int32)
+        nc = ctypes.c_int32(-1)
+        st = L.pkv_seq_step(t._h, f.ctypes.data if f.size else None, f.size, None, None, 0,
+                            None, lv.ctypes.data, lv.size, None, 4, bt.ctypes.data,
+                            cl.ctypes.data, 0, None, None, ctypes.byref(nc))
+        return st, nc.value
+
+    t.fork([1], [2])
+    before = (t.pages(2), alloc.num_free())
+    st, _ = step([], [2])  # the parent lives on: the page is shared and there are no copy arrays
+    assert st != 0 and (t.pages(2), alloc.num_free()) == before
+    st, nc = step([1], [2])
+    assert st == 0 and nc == 0 and t.pages(2) == before[0] and t.length(2) == 21
+    assert [alloc.refcount(p) for p in t.pages(2)] == [1, 1]
+
+
+def test_seq_step_width_query():
+    alloc = pkv.PageAllocator(64)
+    t = pkv.SeqTable(alloc, P)
+    t.add(1)
+    t.reserve([1], [31])  # 2 pages; one more token still fits
+    t.add(2)
+    t.reserve([2], [32])  # 2 full pages; one more token needs a third
+    L = pkv.lib()
+
+    def width(new, prompts, live):
+        import ctypes
+        n = np.array(new, np.int64)
+        c = np.array(prompts, np.int32)
+        lv = np.array(live, np.int64)
+        w = ctypes.c_int32(0)
+        st = L.pkv_seq_step_width(t._h, n.ctypes.data if n.size else None,
+                                  c.ctypes.data if c.size else None, n.size,
+                                  lv.ctypes.data if lv.size else None, lv.size, ctypes.byref(w))
+        return w.value if st == 0 else None
+
+    assert width([], [], []) == 1
+    assert width([], [], [1]) == 2
+    assert width([], [], [1, 2]) == 3
+    assert width([5], [47], [1, 5]) == 3  # 48 tokens after the step: 3 pages
+    assert width([5], [48], [5]) == 4     # 49 tokens: 4 pages
+    assert width([], [], [9]) is None     # unknown request
