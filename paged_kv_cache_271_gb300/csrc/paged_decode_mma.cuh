@@ -348,7 +348,16 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
   // Query fragments (MMA B operand of S^T = K Q^T), k order permuted as described above:
   // lane (gid, tig) holds Q[g = 8 nt + gid][32 kp + 8 tig + 0..7] for every kp (bf16 path) or
   // Q[g][16 (4 h + tig) + 0..15] for h = 0, 1 (FP8 path), read with 16-byte loads.
+  // FP8 / INT8 path: the MMAs take f16, whose range (max 65504, normal from 2^-14) is far
+  // narrower than bf16's or fp32's. Each query row is therefore multiplied by a power of two
+  // 2^e_g that puts its largest |q| in [2^14, 2^15) -- exact, so a bf16 q loses nothing -- and
+  // 2^-e_g goes into that head's score factor. An fp32 q is split into two f16 parts
+  // hi + lo (lo = the f16 rounding of q - hi), each contracted with K: 22 significant bits.
+  constexpr bool QLO = F8 && sizeof(TQ) == 4;
   uint32_t qf[NT][KP][4];
+  uint32_t qlo[QLO ? NT : 1][QLO ? KP : 1][4];
+  float sc_h[NT][2];  // score factor of heads 8 nt + 2 tig and 8 nt + 2 tig + 1 (log2 units)
+  const float sc = a.scale_log2 * (F8 ? a.k_scales[j] : 1.f);
   {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -365,41 +374,73 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
           qf[nt][kp][2] = v.z;
           qf[nt][kp][3] = v.w;
         }
+        sc_h[nt][0] = sc_h[nt][1] = sc;
       } else {
+        float x[2][16];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          float x[16];
           const TQ* src = qrow + 16 * (4 * h + tig);
 #pragma unroll
           for (int k = 0; k < 16; k += (int)(16 / sizeof(TQ))) {
             if constexpr (sizeof(TQ) == 4) {
               float4 f = live ? *reinterpret_cast<const float4*>(src + k) : make_float4(0, 0, 0, 0);
-              x[k] = f.x;
-              x[k + 1] = f.y;
-              x[k + 2] = f.z;
-              x[k + 3] = f.w;
+              x[h][k] = f.x;
+              x[h][k + 1] = f.y;
+              x[h][k + 2] = f.z;
+              x[h][k + 3] = f.w;
             } else {
               uint4 u = live ? *reinterpret_cast<const uint4*>(src + k) : make_uint4(0, 0, 0, 0);
               const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
               for (int t = 0; t < 4; ++t) {
-                x[k + 2 * t] = bf16lo(w[t]);
-                x[k + 2 * t + 1] = bf16hi(w[t]);
+                x[h][k + 2 * t] = bf16lo(w[t]);
+                x[h][k + 2 * t + 1] = bf16hi(w[t]);
               }
             }
           }
-          // chunk 4h+tig of a K row holds k-steps 4h .. 4h+3, four values each
+        }
+        // largest |q| of head g: this lane's 32 values, then the 4 lanes (tig) sharing g
+        float mx = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int k = 0; k < 16; ++k) mx = fmaxf(mx, fabsf(x[h][k]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const int ex = (__float_as_int(mx) >> 23) & 0xff;  // biased exponent of the maximum
+        // mx * 2^e in [2^14, 2^15) for a normal mx: e = 14 - (ex - 127); none for 0, inf, NaN
+        const int e = (mx > 0.f && ex < 255) ? min(126, max(-126, 141 - ex)) : 0;
+        const float up = __int_as_float((127 + e) << 23);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int k = 0; k < 16; ++k) x[h][k] *= up;
+        // chunk 4h+tig of a K row holds k-steps 4h .. 4h+3, four values each
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             const int kp = 2 * h + (ks >> 1), half = ks & 1;
-            qf[nt][kp][2 * half] = pack_f16(x[4 * ks], x[4 * ks + 1]);
-            qf[nt][kp][2 * half + 1] = pack_f16(x[4 * ks + 2], x[4 * ks + 3]);
+            const float* v = &x[h][4 * ks];
+            qf[nt][kp][2 * half] = pack_f16(v[0], v[1]);
+            qf[nt][kp][2 * half + 1] = pack_f16(v[2], v[3]);
+            if constexpr (QLO) {
+              const __half2 h01 = *reinterpret_cast<const __half2*>(&qf[nt][kp][2 * half]);
+              const __half2 h23 = *reinterpret_cast<const __half2*>(&qf[nt][kp][2 * half + 1]);
+              qlo[nt][kp][2 * half] = pack_f16(v[0] - __low2float(h01), v[1] - __high2float(h01));
+              qlo[nt][kp][2 * half + 1] =
+                  pack_f16(v[2] - __low2float(h23), v[3] - __high2float(h23));
+            }
           }
-        }
+        // this lane's scores belong to heads 8 nt + 2 tig (+1): their exponents come from the
+        // lanes holding those query rows (gid = 2 tig, 2 tig + 1)
+        const int e0 = __shfl_sync(0xffffffffu, e, (2 * tig) * 4);
+        const int e1 = __shfl_sync(0xffffffffu, e, (2 * tig + 1) * 4);
+        sc_h[nt][0] = sc * __int_as_float((127 - e0) << 23);
+        sc_h[nt][1] = sc * __int_as_float((127 - e1) << 23);
       }
     }
   }
-  const float sc = a.scale_log2 * (F8 ? a.k_scales[j] : 1.f);
 
   float m_run[NT][2], l_run[NT][2];
   float acc[MT][NT][4];
@@ -465,9 +506,13 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
             widen4_scores<KV>(w8[ks], a1, a3);
             const int kp = 2 * h + (ks >> 1), half = ks & 1;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt) {
               mma16816<true>(s[nt], a0, a1, a2, a3, qf[nt][kp][2 * half],
                              qf[nt][kp][2 * half + 1]);
+              if constexpr (QLO)
+                mma16816<true>(s[nt], a0, a1, a2, a3, qlo[nt][kp][2 * half],
+                               qlo[nt][kp][2 * half + 1]);
+            }
           }
         }
       }
@@ -478,10 +523,10 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
       float alpha[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        s[nt][0] = v0 ? s[nt][0] * sc : -INFINITY;
-        s[nt][1] = v0 ? s[nt][1] * sc : -INFINITY;
-        s[nt][2] = v8 ? s[nt][2] * sc : -INFINITY;
-        s[nt][3] = v8 ? s[nt][3] * sc : -INFINITY;
+        s[nt][0] = v0 ? s[nt][0] * sc_h[nt][0] : -INFINITY;
+        s[nt][1] = v0 ? s[nt][1] * sc_h[nt][1] : -INFINITY;
+        s[nt][2] = v8 ? s[nt][2] * sc_h[nt][0] : -INFINITY;
+        s[nt][3] = v8 ? s[nt][3] * sc_h[nt][1] : -INFINITY;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           float mx = fmaxf(s[nt][k], s[nt][k + 2]);

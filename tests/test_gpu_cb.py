@@ -60,8 +60,12 @@ def _run(trace, pairs_per_step, full_check, cache_dtype="fp8_e4m3"):
         if full_check:
             pairs = [(b, h) for b in range(trace.batch) for h in range(trace.num_q_heads)]
         else:
-            pairs = [(int(rng.integers(trace.batch)), int(rng.integers(trace.num_q_heads)))
-                     for _ in range(pairs_per_step)]
+            # every head of the longest live request, plus random (request, head) pairs
+            lens = [run.cache.lens[r] for r in run.slot_rid]
+            longest = int(np.argmax(lens))
+            pairs = [(longest, h) for h in range(trace.num_q_heads)]
+            pairs += [(int(rng.integers(trace.batch)), int(rng.integers(trace.num_q_heads)))
+                      for _ in range(pairs_per_step)]
         ref = run.oracle_pairs(pairs, ks, vs)
         got = np.stack([out[b, h].double().cpu().numpy() for b, h in pairs])
         worst = max(worst, float(np.abs(got - ref).max()))
