@@ -75,14 +75,60 @@ __global__ void kv_append_copy_kernel(const AppendArgs a) {
   }
 }
 
-template <int N>
-__device__ __forceinline__ void quantize_store(const float (&x)[N], float s, uint8_t* dst) {
+// x / s, correctly rounded to fp32, for a divisor known in advance (the head's scale): with
+// r = RN(1/s) computed once, q0 = RN(x r) and one FMA correction q = RN(q0 + r RN(x - q0 s))
+// (Markstein's correction step; Brisebarre, Muller and Raina, "Accelerating correctly rounded
+// floating-point division when the divisor is known in advance", IEEE Trans. Computers 53(8),
+// 2004, study exactly this case). For x with at most 8 significant bits -- every bf16 value --
+// and any fp32 s, q equals the IEEE quotient: checked exhaustively over the 2^7 bf16
+// significands and the 2^23 fp32 significands of s, which covers every exponent as long as
+// no intermediate is subnormal or overflows. That holds for s in [2^-80, 2^80] whenever the
+// quotient matters (|q| >= 2^-13; smaller quotients give the code 0 either way). The sign is
+// copied from x (so -0 / s = -0). Anything else -- s outside that range, an infinite or NaN x
+// or an overflow, which all leave a NaN in q -- takes the IEEE division for the whole vector.
+// fp32 inputs (24-bit significands) always take the IEEE division.
+struct KnownDivisor {
+  float s, r;
+  bool fast;
+};
+
+__device__ __forceinline__ KnownDivisor known_divisor(float scale) {
+  KnownDivisor d;
+  d.s = scale;
+  d.r = __fdiv_rn(1.f, scale);
+  d.fast = scale >= 0x1p-80f && scale <= 0x1p80f;  // (false for NaN)
+  return d;
+}
+
+template <typename TIN, int N>
+__device__ __forceinline__ void divide_vec(const float (&x)[N], const KnownDivisor& d,
+                                           float (&q)[N]) {
+  bool slow = sizeof(TIN) == 4 || !d.fast;
+  if (!slow) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const float q0 = __fmul_rn(x[k], d.r);
+      const float qq = __fmaf_rn(__fmaf_rn(-q0, d.s, x[k]), d.r, q0);
+      slow |= qq != qq;  // NaN: infinite or NaN x, or an overflow
+      q[k] = copysignf(qq, x[k]);
+    }
+  }
+  if (slow) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) q[k] = __fdiv_rn(x[k], d.s);
+  }
+}
+
+template <typename TIN, int N>
+__device__ __forceinline__ void quantize_store(const float (&x)[N], const KnownDivisor& d,
+                                               uint8_t* dst) {
+  float y[N];
+  divide_vec<TIN, N>(x, d, y);
   uint16_t codes[N / 2];
 #pragma unroll
-  for (int k = 0; k < N / 2; ++k) {
-    const float2 y = make_float2(__fdiv_rn(x[2 * k], s), __fdiv_rn(x[2 * k + 1], s));
-    codes[k] = static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3));
-  }
+  for (int k = 0; k < N / 2; ++k)
+    codes[k] = static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(y[2 * k], y[2 * k + 1]),
+                                                              __NV_SATFINITE, __NV_E4M3));
   if constexpr (N == 8) {
     uint2 w;
     w.x = (uint32_t)codes[0] | ((uint32_t)codes[1] << 16);
@@ -94,15 +140,18 @@ __device__ __forceinline__ void quantize_store(const float (&x)[N], float s, uin
 }
 
 // INT8 codes of N values: fp32(x / s) rounded to nearest even, clamped to [-127, 127].
-template <int N>
-__device__ __forceinline__ void quantize_store_int8(const float (&x)[N], float s, uint8_t* dst) {
+template <typename TIN, int N>
+__device__ __forceinline__ void quantize_store_int8(const float (&x)[N], const KnownDivisor& d,
+                                                    uint8_t* dst) {
+  float y[N];
+  divide_vec<TIN, N>(x, d, y);
   uint32_t w[N / 4];
 #pragma unroll
   for (int k = 0; k < N / 4; ++k) {
     uint32_t acc = 0;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      const int c = min(127, max(-127, __float2int_rn(__fdiv_rn(x[4 * k + t], s))));
+      const int c = min(127, max(-127, __float2int_rn(y[4 * k + t])));
       acc |= ((uint32_t)(c & 0xff)) << (8 * t);
     }
     w[k] = acc;
@@ -115,14 +164,15 @@ __device__ __forceinline__ void quantize_store_int8(const float (&x)[N], float s
 }
 
 template <typename TIN, bool INT8_CODES>
-__device__ __forceinline__ void quantize_vec(const uint4& raw, float s, uint8_t* dst) {
+__device__ __forceinline__ void quantize_vec(const uint4& raw, const KnownDivisor& d,
+                                             uint8_t* dst) {
   constexpr int VEC = Vec16<TIN>::N;
   float x[VEC];
   Vec16<TIN>::load(&raw, x);
   if constexpr (INT8_CODES)
-    quantize_store_int8<VEC>(x, s, dst);
+    quantize_store_int8<TIN, VEC>(x, d, dst);
   else
-    quantize_store<VEC>(x, s, dst);
+    quantize_store<TIN, VEC>(x, d, dst);
 }
 
 // FP8 / INT8 append: each 16-byte vector of fp32/bf16 input is quantised with its head's scale
@@ -144,7 +194,7 @@ __global__ void kv_append_fp8_kernel(const AppendArgs a) {
   const int n = a.num_tokens, step = gridDim.x;
   for (int t = threadIdx.x; t < per_tok; t += blockDim.x) {
     const int h = t / vpr, v = t - h * vpr;
-    const float ks = a.k_scales[h], vs = a.v_scales[h];
+    const KnownDivisor ks = known_divisor(a.k_scales[h]), vs = known_divisor(a.v_scales[h]);
     const int64_t src0 = (int64_t)h * a.head_dim + v * VEC;
     const int64_t dst0 = (int64_t)h * kPageSize * a.head_dim + v * VEC;
     for (int i = blockIdx.x; i < n; i += 2 * step) {
