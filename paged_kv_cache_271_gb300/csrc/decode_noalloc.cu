@@ -12,11 +12,15 @@
 // The scratch is kScratchBytes (16 MiB). It lives in device memory on every GPU where the
 // library's device code has been loaded and stays there until the process exits. Its device
 // address is looked up once per device, on the first call made with that device current; make
-// that first call before starting any stream capture on that device. All calls on a device share
+// that first call before starting any stream capture on that device. The address belongs to
+// the device's context: after a cudaDeviceReset the next call finds a new context and looks
+// the address up again. All calls on a device share
 // the one array and it keeps whatever the last call left in it. Each call zeroes the small
 // region of per-group chunk counters that must start at zero; the partial results are written
 // before they are read. Two calls whose kernels can overlap on the GPU (different streams without ordering
 // between them) race on the array and produce wrong results; calls on one stream are safe.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "pkv.h"
@@ -36,22 +40,47 @@ constexpr int kMaxDevices = 64;
 
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};  // the context each address was looked up in
+
+using CtxGetCurrent = CUresult (*)(CUcontext*);
+
+// The driver's current context (cuCtxGetCurrent, through the runtime's entry-point lookup so
+// the library needs no link against the driver library), or nullptr if unavailable.
+CUcontext current_context() {
+  static CtxGetCurrent fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<CtxGetCurrent>(f);
+  }();
+  CUcontext c = nullptr;
+  if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
 
 // Device address of the scratch on the current device. The array's name is only a host-side
-// stand-in in host code, so the address must come from cudaGetSymbolAddress, once per device.
+// stand-in in host code, so the address must come from cudaGetSymbolAddress: once per device,
+// and again only if the device's context has changed since (a cudaDeviceReset).
 int scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return set_error(PKV_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return set_error(PKV_ECUDA, "device index %d", dev);
+  // (no context yet on this thread: the lookup below creates the device's primary context,
+  // and the next call, finding that context, looks the address up once more)
+  const CUcontext ctx = current_context();
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (!g_scratch_ptr[dev] || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_decode_scratch);
     if (e != cudaSuccess)
       return set_error(PKV_ECUDA, "cudaGetSymbolAddress(decode scratch): %s",
                        cudaGetErrorString(e));
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_ptr[dev];
   return PKV_OK;

@@ -41,7 +41,12 @@ def _noalloc(sc, q, out):
     assert st == 0, pkv.lib().pkv_last_error().decode()
 
 
-def test_noalloc_matches_workspace_entry_point_on_two_calls():
+@pytest.mark.parametrize("merge", ["combine kernel", "merge in place"])
+def test_noalloc_matches_workspace_entry_point_on_two_calls(merge):
+    # split partials merged by the combine kernel, or by the last CTA of each (request, KV
+    # head) through the chunk counters: both uses of the scratch
+    import dataclasses
+    from gpu_harness import oracle_expected
     w = workloads.llama3_8b_batch64(batch=8)
     sc = Scenario(w)
     sc.append()
@@ -49,15 +54,27 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
                                      sc.block_tables.shape[1])
     assert 0 < need <= pkv.lib().pkv_decode_noalloc_scratch_bytes()  # the split scratch is used
     q2 = (sc.q.float() * -0.7).to(torch.bfloat16)
-    for q in (sc.q, q2):  # the second call must not see the first call's leftovers
-        ref = pkv.paged_decode_attention(q, sc.cache.k, sc.cache.v, sc.block_tables,
-                                         sc.context_lens, w.scale, workspace=sc.workspace).clone()
-        out = torch.full_like(q, float("nan"))
-        _noalloc(sc, q, out)
-        torch.cuda.synchronize()
-        assert pkv.device_error() == 0
-        err = float((out.float() - ref.float()).abs().max())
-        assert err <= 1e-2, err
+    pkv.decode_set_chunk_pages(8)  # several chunks per request
+    pkv.decode_set_merge_in_place(64 if merge == "merge in place" else 0)
+    try:
+        need = pkv.decode_workspace_size(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                         sc.block_tables.shape[1])
+        assert need <= pkv.lib().pkv_decode_noalloc_scratch_bytes()
+        ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+        for q in (sc.q, q2):  # the second call must not see the first call's leftovers
+            ref = pkv.paged_decode_attention(q, sc.cache.k, sc.cache.v, sc.block_tables,
+                                             sc.context_lens, w.scale, workspace=ws).clone()
+            out = torch.full_like(q, float("nan"))
+            _noalloc(sc, q, out)
+            torch.cuda.synchronize()
+            assert pkv.device_error() == 0
+            assert torch.equal(out, ref)  # same kernels, same split: the same bits
+            exp = oracle_expected(dataclasses.replace(w, q=q.cpu()))
+            err = float((out.double().cpu() - torch.from_numpy(exp)).abs().max())
+            assert err <= 1e-2, err
+    finally:
+        pkv.decode_set_chunk_pages(0)
+        pkv.decode_set_merge_in_place(0)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
