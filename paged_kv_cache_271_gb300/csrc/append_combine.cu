@@ -76,16 +76,18 @@ __global__ void kv_append_copy_kernel(const AppendArgs a) {
 }
 
 // x / s, correctly rounded to fp32, for a divisor known in advance (the head's scale): with
-// r = RN(1/s) computed once, q0 = RN(x r) and one FMA correction q = RN(q0 + r RN(x - q0 s))
+// r = RN(1/s) computed once, q0 = RN(x r) and one FMA correction q = RN(q0 - r RN(q0 s - x))
 // (Markstein's correction step; Brisebarre, Muller and Raina, "Accelerating correctly rounded
 // floating-point division when the divisor is known in advance", IEEE Trans. Computers 53(8),
 // 2004, study exactly this case). For x with at most 8 significant bits -- every bf16 value --
 // and any fp32 s, q equals the IEEE quotient: checked exhaustively over the 2^7 bf16
 // significands and the 2^23 fp32 significands of s, which covers every exponent as long as
 // no intermediate is subnormal or overflows. That holds for s in [2^-80, 2^80] whenever the
-// quotient matters (|q| >= 2^-13; smaller quotients give the code 0 either way). The sign is
-// copied from x (so -0 / s = -0). Anything else -- s outside that range, an infinite or NaN x
-// or an overflow, which all leave a NaN in q -- takes the IEEE division for the whole vector.
+// quotient matters (|q| >= 2^-13; smaller quotients give the code 0 either way). The remainder
+// is taken as q0 s - x and subtracted, which equals adding x - q0 s exactly (rounding to
+// nearest is symmetric) and keeps the sign of a zero quotient: -0 / s gives -0. Anything else
+// -- s outside that range, an infinite or NaN x or an overflow, which all leave a NaN in q --
+// takes the IEEE division for the whole vector.
 // fp32 inputs (24-bit significands) always take the IEEE division.
 struct KnownDivisor {
   float s, r;
@@ -108,9 +110,8 @@ __device__ __forceinline__ void divide_vec(const float (&x)[N], const KnownDivis
 #pragma unroll
     for (int k = 0; k < N; ++k) {
       const float q0 = __fmul_rn(x[k], d.r);
-      const float qq = __fmaf_rn(__fmaf_rn(-q0, d.s, x[k]), d.r, q0);
-      slow |= qq != qq;  // NaN: infinite or NaN x, or an overflow
-      q[k] = copysignf(qq, x[k]);
+      q[k] = __fmaf_rn(-__fmaf_rn(q0, d.s, -x[k]), d.r, q0);
+      slow |= q[k] != q[k];  // NaN: infinite or NaN x, or an overflow
     }
   }
   if (slow) {

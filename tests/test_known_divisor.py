@@ -36,7 +36,8 @@ def test_reciprocal_and_one_correction_equal_ieee_division(tmp_path):
     except subprocess.CalledProcessError:
         subprocess.run(["gcc"] + _flags() + [src, "-o", exe, "-lm"], check=True)
     out = subprocess.run([exe], check=True, capture_output=True, text=True, timeout=600).stdout
-    n, wrong, wrong_uncorrected = (int(v) for v in out.split())
+    n, wrong, wrong_uncorrected, zero_signs = (int(v) for v in out.split())
     assert n == 128 * 2 ** 23
     assert wrong == 0
+    assert zero_signs == 0  # +0 / s = +0 and -0 / s = -0
     assert wrong_uncorrected > n // 10  # without the correction the check does fail
