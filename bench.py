@@ -78,7 +78,12 @@ def config_of(w):
             "kv_dtype": w.kv_dtype, "context_lens": "sum %d" % int(np.sum(w.context_lens)),
             "pool_pages": w.num_pages,
             "l2": "flushed with a 256 MiB write before every timed step",
-            "step": "slot mapping (host) + paged_decode_step (append + attention, one launch)"}
+            "step": DEVICE_STEP}
+
+
+# What the timed region of a step holds (the host slot mapping runs before it, timed apart).
+DEVICE_STEP = ("device: paged_decode_step (append + attention, one launch) + combine, replayed "
+               "from a CUDA graph; the host slot mapping is timed apart (host_slot_mapping_us)")
 
 
 class StepState:
@@ -110,7 +115,8 @@ class StepState:
             self.config = {"workload": wname + "_state_after_1_step", "batch": tr.batch,
                            "num_q_heads": tr.num_q_heads, "num_kv_heads": tr.num_kv_heads,
                            "head_dim": 128, "page_size": 16, "kv_dtype": coded,
-                           "context_lens": "U[128,8192] seeded, sum %d" % self.ctx_sum}
+                           "context_lens": "U[128,8192] seeded, sum %d" % self.ctx_sum,
+                           "step": DEVICE_STEP}
             self.cache = run.cache
             self.slots = run.last_slots
         else:
@@ -149,8 +155,10 @@ class StepState:
             self.groups = pkv.cascade_groups(self.bt.cpu().numpy(), self.cl.cpu().numpy())
             self.groups.to(dev)
             g = self.groups
-            self.config["step"] = ("slot mapping (host) + cascade_decode_step (shared-prefix "
-                                   "kernel, append + own-page attention, combine)")
+            self.config["step"] = ("device: cascade_decode_step (shared-prefix kernel, append + "
+                                   "own-page attention, combine), replayed from a CUDA graph; "
+                                   "the host slot mapping and grouping are timed apart "
+                                   "(host_slot_mapping_us)")
             self.config["cascade"] = "%d group(s), %s shared pages, %d members max" % (
                 g.n_groups, "/".join(str(int(x)) for x in g.prefix_pages), g.max_members)
             need = pkv.cascade_workspace_size(self.batch, self.h_q, self.h_kv, self.d,
@@ -584,6 +592,7 @@ def run_ours(args):
                 v[1] / (launches[k][1] / max(launches[k][0], 1) * 1e-3) / (1e9 if v[0] == "hbm" else 1e12), 2)}
         for k, v in work.items() if k != top and launches[k][0]}
 
+    roofline["sm_mhz"] = clk.get("sm_mhz")  # median SM clock sampled during the timed steps
     e2e = run_e2e(sc, args, dev, stream, flush, n_sets)
     max_e2e = max_over_ranks(e2e["ms_per_step"], dev)
     e2e_value = aggregate(per_step_bytes, max_e2e, ws)
@@ -612,7 +621,8 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
                     "ms_per_step": round(max_e2e, 5),
-                    "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+                    "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                    "phases_us": e2e["phases_us"]},
             "gpu_launches": int(round(per_step_launches * args.steps)),
             "graph": "the step's launches captured once as a CUDA graph, replayed per step",
             "host_slot_mapping_us": round(1e6 * host_s / max(args.steps, 1), 1),
@@ -851,7 +861,34 @@ def run_e2e(sc, args, dev, stream, flush, n_sets=1):
         ends[i].synchronize()  # the result is on the host before the next step starts
     barrier()
     ms = float(np.mean([s.elapsed_time(e) for s, e in zip(starts, ends)]))
-    return {"ms_per_step": ms, "h2d": hs.h2d_bytes, "d2h": hs.d2h_bytes}
+
+    # Where an e2e step's time goes, from the same steps run again: host time inside the
+    # library call (argument marshalling, grouping for the cascade, enqueueing the copies and
+    # launches) and waiting for the output; device time of each copy and kernel (the library's
+    # event tracing); the rest of the step's device-side span is time the GPU sat idle
+    # between them (waiting for the host to enqueue, copy and launch latencies).
+    t_call = t_wait = 0.0
+    pkv.trace_reset()
+    pkv.trace_enable(True)
+    for i in range(n):
+        flush.zero_()
+        t0 = time.perf_counter()
+        one(i)
+        t1 = time.perf_counter()
+        torch.cuda.current_stream().synchronize()
+        t_call += t1 - t0
+        t_wait += time.perf_counter() - t1
+    pkv.trace_enable(False)
+    phases = {"host_call": round(1e6 * t_call / n, 2), "host_wait": round(1e6 * t_wait / n, 2)}
+    busy = 0.0
+    for k in ("h2d_copy", "cascade_prefix", "paged_decode", "decode_combine", "d2h_copy"):
+        cnt, tot = pkv.trace_read(k)
+        if cnt:
+            phases[k] = round(1e3 * tot / n, 2)
+            busy += 1e3 * tot / n
+    pkv.trace_reset()
+    phases["gpu_idle"] = round(1e3 * ms - busy, 2)
+    return {"ms_per_step": ms, "h2d": hs.h2d_bytes, "d2h": hs.d2h_bytes, "phases_us": phases}
 
 
 def trace_joins(tr):

@@ -209,6 +209,8 @@ int pkv_paged_decode_step_window(const void* q, int32_t dtype_q, int32_t batch,
  *    pkv_decode_noalloc_scratch_bytes()) are rejected with PKV_EINVAL before anything runs.
  *  - Calls no cudaMalloc or cudaFree. The first call on a device looks up the scratch's device
  *    address for that device (with it current); make that call before any stream capture.
+ *    The address is kept per device and context: after a cudaDeviceReset the next call looks
+ *    it up again.
  *  - All calls on a device share the scratch and it keeps the last call's contents; each call
  *    zeroes the small part that must start at zero. Calls whose kernels may overlap on the GPU,
  *    e.g. on two streams without ordering between them, race on it; calls on one stream are
@@ -435,8 +437,9 @@ int pkv_packed_step_layout(int32_t batch, int32_t num_q_heads, int32_t num_kv_he
  * pkv_paged_decode_step_window with its inputs and output in host memory (window = 0, sinks 0:
  * pkv_paged_decode_step): one copy of the packed inputs (host_in, pinned, laid out as
  * pkv_packed_step_layout says) into dev_in (device, the same size), the fused append + decode
- * on the device copies, and one copy of the output (out_dev, device) into out_host (pinned),
- * all on `stream` (the caller synchronises before reading out_host or rewriting host_in).
+ * on the device copies, and one copy of the output (out_dev, device) into out_host (pinned
+ * for an asynchronous copy; any host memory works), all on `stream` (the caller synchronises
+ * before reading out_host or rewriting host_in).
  */
 int pkv_paged_decode_step_packed(const void* host_in, void* dev_in, int32_t batch,
                                  int32_t num_q_heads, int32_t dtype_q, int32_t dtype_new,
@@ -623,10 +626,11 @@ int32_t pkv_prefix_size(const pkv_prefix_cache* c);
 
 /* ---- tracing --------------------------------------------------------------------------------- */
 
-/* When on, every kernel the library launches is bracketed by a pair of CUDA events on its
- * stream. pkv_trace_read() synchronises those events and reports, for the kernel family
- * named ("paged_decode", "decode_combine", "cascade_prefix", "kv_append", "kv_absmax"), the
- * number of launches and their summed device time in milliseconds since the last reset.
+/* When on, every kernel the library launches, and each copy of the packed host steps, is
+ * bracketed by a pair of CUDA events on its stream. pkv_trace_read() synchronises those events
+ * and reports, for the family named ("paged_decode", "decode_combine", "cascade_prefix",
+ * "kv_append", "kv_absmax", "copy_pages", and the packed steps' "h2d_copy" and "d2h_copy"),
+ * the number of launches and their summed device time in milliseconds since the last reset.
  * pkv_trace_reset() drops all records. */
 int pkv_trace_enable(int on);
 int pkv_trace_reset(void);

@@ -74,6 +74,15 @@ cudaError_t traced(const char* name, cudaStream_t s, F&& launch) {
   return e;
 }
 
+}  // namespace
+
+cudaError_t traced_copy(const char* name, void* dst, const void* src, size_t bytes,
+                        cudaMemcpyKind kind, cudaStream_t s) {
+  return traced(name, s, [&] { return cudaMemcpyAsync(dst, src, bytes, kind, s); });
+}
+
+namespace {
+
 int cuda_status(cudaError_t e, const char* what) {
   if (e == cudaSuccess) return PKV_OK;
   return set_error(PKV_ECUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -637,7 +646,7 @@ int pkv_paged_decode_step_packed(const void* host_in, void* dev_in, int32_t batc
   if (st != PKV_OK) return st;
   if (batch == 0) return PKV_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(dev_in, host_in, total, cudaMemcpyHostToDevice, s);
+  cudaError_t e = traced_copy("h2d_copy", dev_in, host_in, total, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_status(e, "packed step inputs copy");
   char* d = static_cast<char*>(dev_in);
   st = decode_impl(who, d + off[0], dtype_q, batch, num_q_heads, k_cache, v_cache, desc,
@@ -648,7 +657,7 @@ int pkv_paged_decode_step_packed(const void* host_in, void* dev_in, int32_t batc
   if (st != PKV_OK) return st;
   const size_t out_bytes =
       (size_t)batch * num_q_heads * desc->head_dim * (dtype_q == PKV_F32 ? 4 : 2);
-  e = cudaMemcpyAsync(out_host, out_dev, out_bytes, cudaMemcpyDeviceToHost, s);
+  e = traced_copy("d2h_copy", out_host, out_dev, out_bytes, cudaMemcpyDeviceToHost, s);
   return cuda_status(e, "packed step output copy");
 }
 

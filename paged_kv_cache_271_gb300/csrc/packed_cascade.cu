@@ -2,14 +2,15 @@
 // (as for pkv_paged_decode_step_packed) plus room for the batch's groups, which this call finds
 // on the host from the packed page tables ("KV cache and PagedAttention", section 6: requests
 // with a common prompt share its pages). One host-to-device copy of the block, the cascade
-// step on the device copies, one device-to-host copy of the output. Built only from the
-// library's C entry points (grouping, workspace size, cascade step).
+// step on the device copies, one device-to-host copy of the output. Built from the library's
+// C entry points (grouping, workspace size, cascade step) and its traced copy.
 #include <cuda_runtime.h>
 
 #include <cstring>
 
 #include "pkv.h"
 #include "pkv_host.h"
+#include "pkv_internal.h"
 
 namespace {
 
@@ -85,7 +86,7 @@ int pkv_cascade_decode_step_packed(void* host_in, void* dev_in, int32_t batch,
     return pkv::set_error(PKV_EINVAL, "%s: workspace of %zu bytes needed, %zu given", who, need,
                           workspace_bytes);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(dev_in, host_in, total, cudaMemcpyHostToDevice, s);
+  cudaError_t e = pkv::traced_copy("h2d_copy", dev_in, host_in, total, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess)
     return pkv::set_error(PKV_ECUDA, "%s: input copy: %s", who, cudaGetErrorString(e));
   st = pkv_cascade_decode_step(d + off[0], dtype_q, batch, num_q_heads, d + off[1], d + off[2],
@@ -94,7 +95,7 @@ int pkv_cascade_decode_step_packed(void* host_in, void* dev_in, int32_t batch,
   if (st != PKV_OK) return st;
   const size_t out_bytes =
       (size_t)batch * num_q_heads * desc->head_dim * (dtype_q == PKV_F32 ? 4 : 2);
-  e = cudaMemcpyAsync(out_host, out_dev, out_bytes, cudaMemcpyDeviceToHost, s);
+  e = pkv::traced_copy("d2h_copy", out_host, out_dev, out_bytes, cudaMemcpyDeviceToHost, s);
   if (e != cudaSuccess)
     return pkv::set_error(PKV_ECUDA, "%s: output copy: %s", who, cudaGetErrorString(e));
   return PKV_OK;

@@ -103,6 +103,9 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, int kv_dtype, int q_dtype, in
 cudaError_t launch_decode_combine(const DecodeArgs& a, int q_dtype, int head_dim,
                                   cudaStream_t s);
 cudaError_t launch_kv_append(const AppendArgs& a, int in_dtype, int cache_dtype, cudaStream_t s);
+// cudaMemcpyAsync on stream s, traced under `name` when launch tracing is on (capi.cu).
+cudaError_t traced_copy(const char* name, void* dst, const void* src, size_t bytes,
+                        cudaMemcpyKind kind, cudaStream_t s);
 cudaError_t launch_copy_pages(void* k, void* v, const int32_t* src, const int32_t* dst, int n,
                               int64_t page_bytes, int num_pages, int* err, cudaStream_t s);
 cudaError_t launch_kv_absmax(const void* x, int dtype, int64_t n_tokens, int h_kv, int head_dim,

@@ -409,6 +409,39 @@ def test_host_step_equals_device_step(kv):
     assert hs.h2d_bytes >= (b.q.numel() + 2 * b.k_new.numel()) * 2
 
 
+def test_host_step_output_into_pageable_memory():
+    # the packed step's output copy lands in pageable host memory as well as in pinned memory:
+    # the same bytes
+    import ctypes
+    w = workloads.custom("hoststep_pageable", 7302, 5, 8, 2, 128, "bf16", "bf16",
+                         [40, 3, 200, 17, 64])
+    b = Scenario(w)
+    hs = pkv.HostStep(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                      b.block_tables.shape[1])
+    hs.q_host.copy_(b.q.cpu())
+    hs.k_new_host.copy_(b.k_new.cpu())
+    hs.v_new_host.copy_(b.v_new.cpu())
+    hs.block_tables_host.copy_(b.block_tables.cpu())
+    hs.context_lens_host.copy_(b.context_lens.cpu())
+    pinned = hs.step(b.cache.k, b.cache.v, w.scale, workspace=b.workspace).clone()
+    torch.cuda.synchronize()
+    pageable = np.full(pinned.numel(), 0x7fc0, dtype=np.uint16)  # NaN until written
+    out_dev = torch.full_like(b.q, float("nan"))
+    desc = pkv.cache_desc(b.cache.k)
+    st = pkv.lib().pkv_paged_decode_step_packed(
+        ctypes.c_void_p(hs.host.data_ptr()), ctypes.c_void_p(hs.dev.data_ptr()), w.batch,
+        w.num_q_heads, pkv.BF16, pkv.BF16, ctypes.c_void_p(b.cache.k.data_ptr()),
+        ctypes.c_void_p(b.cache.v.data_ptr()), ctypes.byref(desc), b.block_tables.shape[1],
+        ctypes.c_float(w.scale), None, None, 0, 0, ctypes.c_void_p(out_dev.data_ptr()),
+        ctypes.c_void_p(pageable.ctypes.data), ctypes.c_void_p(b.workspace.data_ptr()),
+        b.workspace.numel(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, pkv.lib().pkv_last_error().decode()
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    assert np.array_equal(pageable, pinned.view(torch.int16).numpy().view(np.uint16).ravel())
+    assert torch.equal(out_dev.cpu(), pinned)
+
+
 def test_host_step_graph_replays_each_steps_inputs():
     # the captured host step re-reads the pinned inputs on every replay: new queries each
     # step give the same bytes as the step made call by call, and differ between steps
