@@ -480,6 +480,11 @@ typedef struct {
   const int32_t* own_start;      /* [batch] or NULL: prefix_pages[group_of[b]] (0 outside a
                                     group), read directly by the decode of the members' own
                                     pages instead of through group_of (one read fewer) */
+  const int32_t* prefix_page_ids; /* [n_groups][max_prefix_pages] or NULL: group g's shared
+                                    page ids (its members' first table entries), so that the
+                                    prefix pass reads them directly instead of through
+                                    group_members and the first member's table row
+                                    (pkv_cascade_prefix_page_ids fills it) */
 } pkv_cascade_desc;
 
 /*
@@ -498,6 +503,14 @@ int pkv_cascade_groups(const int32_t* block_tables, const int32_t* context_lens,
                        int32_t* group_of, int32_t* prefix_pages, int32_t* group_offsets,
                        int32_t* group_members, int32_t* n_groups, int32_t* max_members,
                        int32_t* max_prefix_pages, int32_t* max_own_pages, int32_t* own_start);
+
+/* The shared page ids of each group, [n_groups][max_prefix_pages] (row g: the first
+ * prefix_pages[g] entries of its first member's table row, the rest -1), from the host arrays
+ * pkv_cascade_groups wrote; ids_out is host memory of n_groups * max_prefix_pages int32. */
+int pkv_cascade_prefix_page_ids(const int32_t* block_tables, int32_t max_pages_per_seq,
+                                const int32_t* prefix_pages, const int32_t* group_offsets,
+                                const int32_t* group_members, int32_t n_groups,
+                                int32_t max_prefix_pages, int32_t* ids_out);
 
 /* Workspace bytes of a cascade decode (its partials: the prefix chunks, then the members' own
  * chunks, for every request); pkv_decode_workspace_size when groups has no group. Zero-fill it
@@ -538,9 +551,11 @@ int pkv_cascade_decode_step(const void* q, int32_t dtype_q, int32_t batch, int32
 /*
  * The cascade decode step from host memory. Layout of the block (host_in, pinned, and its
  * device twin dev_in, the same size): the five regions of pkv_packed_step_layout (offsets[0..4])
- * filled by the caller, then five int32 regions this call fills (offsets[5..9]): group_of
+ * filled by the caller, then six int32 regions this call fills (offsets[5..10]): group_of
  * [batch], prefix_pages [batch], group_offsets [batch + 1], group_members [batch], own_start
- * [batch], each 256-byte aligned; *total_bytes is the size of the block.
+ * [batch] and, last, the groups' shared page ids [batch / 2][max_pages_per_seq] (at most
+ * batch / 2 groups), each 256-byte aligned; *total_bytes is the size of the block. A step
+ * copies the block up to the end of the page ids its groups use.
  */
 int pkv_packed_cascade_layout(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                               int32_t head_dim, int32_t max_pages_per_seq, int32_t dtype_q,

@@ -52,7 +52,7 @@ class _CascadeDesc(ctypes.Structure):
                 ("group_offsets", ctypes.c_void_p), ("group_members", ctypes.c_void_p),
                 ("n_groups", ctypes.c_int32), ("max_members", ctypes.c_int32),
                 ("max_prefix_pages", ctypes.c_int32), ("max_own_pages", ctypes.c_int32),
-                ("own_start", ctypes.c_void_p)]
+                ("own_start", ctypes.c_void_p), ("prefix_page_ids", ctypes.c_void_p)]
 
 
 def lib():
@@ -148,6 +148,7 @@ def lib():
                                               ctypes.POINTER(i32), ctypes.POINTER(i32),
                                               ctypes.POINTER(i32), ctypes.POINTER(i32), vp]),
         "pkv_cascade_workspace_size": (sz, [i32, i32, i32, i32, i32, C]),
+        "pkv_cascade_prefix_page_ids": (ctypes.c_int, [vp, i32, vp, vp, vp, i32, i32, vp]),
         "pkv_cascade_prefix_chunk_pages": (i32, [i32, i32, C]),
         "pkv_cascade_decode_attention": (ctypes.c_int, [vp, i32, i32, i32, vp, vp, D, vp, i32,
                                                         vp, f32, C, vp, vp, sz, vp]),
@@ -322,7 +323,7 @@ class CascadeGroups:
     ``to(device)`` once to place them for the cascade decode."""
 
     def __init__(self, group_of, prefix_pages, group_offsets, group_members, max_members,
-                 max_prefix_pages, max_own_pages=0, own_start=None):
+                 max_prefix_pages, max_own_pages=0, own_start=None, prefix_page_ids=None):
         self.group_of = group_of
         self.prefix_pages = prefix_pages
         self.group_offsets = group_offsets
@@ -334,12 +335,18 @@ class CascadeGroups:
         if own_start is None:  # prefix_pages[group_of[b]], 0 outside a group
             own_start = np.where(group_of >= 0, np.append(prefix_pages, 0)[group_of], 0)
         self.own_start = np.asarray(own_start, dtype=np.int32)
+        # [n_groups][max_prefix_pages] shared page ids (pkv_cascade_prefix_page_ids), or None
+        self.prefix_page_ids = (None if prefix_page_ids is None else
+                                np.asarray(prefix_page_ids, dtype=np.int32).reshape(-1))
         self._dev = None
 
     def packed(self) -> np.ndarray:
-        """The four arrays back to back (int32), as ``to`` places them."""
-        return np.concatenate([self.group_of, self.prefix_pages, self.group_offsets,
-                               self.group_members, self.own_start]).astype(np.int32)
+        """The arrays back to back (int32), as ``to`` places them."""
+        parts = [self.group_of, self.prefix_pages, self.group_offsets, self.group_members,
+                 self.own_start]
+        if self.prefix_page_ids is not None:
+            parts.append(self.prefix_page_ids)
+        return np.concatenate(parts).astype(np.int32)
 
     def to(self, device, buffer=None, staging=None):
         """Place the arrays on the device in one copy: into a new tensor, or into ``buffer``
@@ -358,6 +365,8 @@ class CascadeGroups:
         base = buffer.data_ptr()
         self._ptrs = [base, base + 4 * B, base + 4 * (B + ng), base + 4 * (B + 2 * ng + 1),
                       base + 4 * (B + 2 * ng + 1 + nm)]
+        self._ids_ptr = (None if self.prefix_page_ids is None else
+                         base + 4 * (2 * B + 2 * ng + 1 + nm))
         return self
 
     def desc(self) -> _CascadeDesc:
@@ -367,7 +376,7 @@ class CascadeGroups:
             raise PkvError(-1, "CascadeGroups.to(device) has not been called")
         g, p, o, m, st = self._ptrs
         return _CascadeDesc(g, p, o, m, self.n_groups, self.max_members, self.max_prefix_pages,
-                            self.max_own_pages, st)
+                            self.max_own_pages, st, self._ids_ptr)
 
 
 def cascade_groups(block_tables, context_lens, min_members=2, min_prefix_pages=1) -> CascadeGroups:
@@ -389,8 +398,14 @@ def cascade_groups(block_tables, context_lens, min_members=2, min_prefix_pages=1
                                     members.ctypes.data, ctypes.byref(n), ctypes.byref(mm),
                                     ctypes.byref(mp), ctypes.byref(mo), start.ctypes.data))
     ng = n.value
+    ids = np.empty(max(ng * mp.value, 1), np.int32)
+    if ng:
+        _check(lib().pkv_cascade_prefix_page_ids(bt.ctypes.data, W, prefix.ctypes.data,
+                                                 offs.ctypes.data, members.ctypes.data, ng,
+                                                 mp.value, ids.ctypes.data))
     return CascadeGroups(group_of, prefix[:ng].copy(), offs[:ng + 1].copy(),
-                         members[:offs[ng]].copy(), mm.value, mp.value, mo.value, start[:B].copy())
+                         members[:offs[ng]].copy(), mm.value, mp.value, mo.value, start[:B].copy(),
+                         ids[:ng * mp.value].copy() if ng else None)
 
 
 def cascade_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_pages_per_seq,
@@ -493,7 +508,7 @@ class HostStep:
         self._graphs = {}
         self.batch, self.h_q, self.max_pages = batch, num_q_heads, max_pages
         self.q_code, self.new_code = self._CODE[q_dtype], self._CODE[new_dtype]
-        offs = (ctypes.c_size_t * 10)()
+        offs = (ctypes.c_size_t * 11)()
         total = ctypes.c_size_t(0)
         layout = lib().pkv_packed_cascade_layout if cascade else lib().pkv_packed_step_layout
         _check(layout(batch, num_q_heads, num_kv_heads, head_dim, max_pages, self.q_code,

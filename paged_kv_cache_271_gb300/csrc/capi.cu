@@ -224,16 +224,17 @@ std::atomic<int> g_prefix_chunk_override{0};
 std::atomic<int> g_prefix_kernel{0};  // 0 automatic (tcgen05), 1 mma.sync, 2 tcgen05
 bool prefix_on_tcgen05() { return g_prefix_kernel.load() != 1; }
 
-// Pages per CTA of the cascade prefix kernel: the shared pages of each (group, KV head, row
-// tile) are cut into as many chunks as keep the launch within one wave of resident CTAs
-// (tcgen05: 128 rows per CTA, one CTA per SM, chunks of at least one 4-page tile; mma.sync:
-// 64 rows, three CTAs per SM, at least 2 pages); a chunk of at most the whole prefix.
+// Pages per CTA of the cascade prefix kernel: the shared pages of each (group, KV head, rows
+// of a CTA) are cut into as many chunks as keep the launch within one wave of resident CTAs
+// (tcgen05: 128 or 256 rows per CTA, one CTA per SM, chunks of at least one 4-page tile;
+// mma.sync: 64 rows, three CTAs per SM, at least 2 pages); a chunk of at most the whole prefix.
 int prefix_chunk_pages_for(int n_groups, int h_kv, int group, int max_members, int max_prefix) {
   const int ov = g_prefix_chunk_override.load();
   if (ov > 0) return ov;
   if (max_prefix < 1) return 1;
   const bool tc = prefix_on_tcgen05();
-  const int rows = tc ? kCascadeTcRows : kCascadeRows;
+  const int rows =
+      tc ? kCascadeTcRows * cascade_tc_row_tiles(max_members * group) : kCascadeRows;
   // with the fold left to the combine, the tcgen05 prefix kernel takes about half the SMs and
   // the own-page decode runs on the rest meanwhile (prefix sharing, batch 128: two chunks,
   // 38.1 us a step, against 41.1 us with the prefix kernel on every SM)
@@ -458,6 +459,8 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
     ca.group_offsets = groups->group_offsets;
     ca.group_members = groups->group_members;
     ca.max_members = groups->max_members;
+    ca.prefix_ids = groups->prefix_page_ids;
+    ca.ids_stride = groups->max_prefix_pages;
   }
   if (a.n_chunk_slots > 65535) return set_error(PKV_ESHAPE, "%s: too many chunks", who);
   if (a.n_chunk_slots > 1) {

@@ -101,3 +101,24 @@ extern "C" int pkv_cascade_groups(const int32_t* block_tables, const int32_t* co
   *max_own_pages = mo;
   return PKV_OK;
 }
+
+extern "C" int pkv_cascade_prefix_page_ids(const int32_t* block_tables, int32_t max_pages_per_seq,
+                                           const int32_t* prefix_pages,
+                                           const int32_t* group_offsets,
+                                           const int32_t* group_members, int32_t n_groups,
+                                           int32_t max_prefix_pages, int32_t* ids_out) {
+  if (n_groups < 0 || max_prefix_pages < 0 || max_prefix_pages > max_pages_per_seq ||
+      (n_groups > 0 && (!block_tables || !prefix_pages || !group_offsets || !group_members ||
+                        !ids_out)))
+    return pkv::set_error(PKV_EINVAL, "pkv_cascade_prefix_page_ids: bad argument");
+  for (int32_t g = 0; g < n_groups; ++g) {
+    const int32_t pp = prefix_pages[g];
+    if (pp < 0 || pp > max_prefix_pages || group_offsets[g] >= group_offsets[g + 1])
+      return pkv::set_error(PKV_EINVAL, "pkv_cascade_prefix_page_ids: group %d is malformed", g);
+    const int32_t* row = block_tables + (size_t)group_members[group_offsets[g]] * max_pages_per_seq;
+    int32_t* out = ids_out + (size_t)g * max_prefix_pages;
+    std::memcpy(out, row, (size_t)pp * sizeof(int32_t));
+    for (int32_t i = pp; i < max_prefix_pages; ++i) out[i] = -1;
+  }
+  return PKV_OK;
+}

@@ -79,10 +79,18 @@ __global__ void __launch_bounds__(32 * kCpWarps, 3) cascade_prefix_kernel(
   const int per_chunk = (pp + n_chunks - 1) / n_chunks;
   const int page0 = c * per_chunk;
   const int n_pages = max(0, min(per_chunk, pp - page0));
-  const int b_first = ca.group_members[o0];
-  if (b_first < 0 || b_first >= a.batch) {
-    if (reporter) atomicOr(a.err, PKV_DEVERR_BAD_GROUP);
-    return;
+  // the group's shared pages: from the groups' id array, else as listed by its first member's
+  // table row
+  const int32_t* btrow;
+  if (ca.prefix_ids != nullptr) {
+    btrow = ca.prefix_ids + (size_t)g * ca.ids_stride;
+  } else {
+    const int b_first = ca.group_members[o0];
+    if (b_first < 0 || b_first >= a.batch) {
+      if (reporter) atomicOr(a.err, PKV_DEVERR_BAD_GROUP);
+      return;
+    }
+    btrow = a.block_tables + (size_t)b_first * a.max_pages;
   }
 
   extern __shared__ uint8_t smem_raw[];
@@ -98,8 +106,6 @@ __global__ void __launch_bounds__(32 * kCpWarps, 3) cascade_prefix_kernel(
   }
   __syncthreads();
 
-  // the group's shared pages, as listed by its first member's table row
-  const int32_t* btrow = a.block_tables + (size_t)b_first * a.max_pages;
   const uint64_t pol = l2_evict_last_policy();  // every row tile of the group reads them
   const uint32_t smem_u = smem_u32(smem);
   const int n_steps = (n_pages + 1) / 2;

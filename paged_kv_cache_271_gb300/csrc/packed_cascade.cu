@@ -29,11 +29,12 @@ int pkv_packed_cascade_layout(int32_t batch, int32_t num_q_heads, int32_t num_kv
   int st = pkv_packed_step_layout(batch, num_q_heads, num_kv_heads, head_dim, max_pages_per_seq,
                                   dtype_q, dtype_new, offsets, &base);
   if (st != PKV_OK) return st;
-  // group_of [B], prefix_pages [B], group_offsets [B + 1], group_members [B], own_start [B]
-  const size_t words[5] = {(size_t)batch, (size_t)batch, (size_t)batch + 1, (size_t)batch,
-                           (size_t)batch};
+  // group_of [B], prefix_pages [B], group_offsets [B + 1], group_members [B], own_start [B],
+  // the groups' shared page ids [B / 2][max_pages] (last: a step copies only what it uses)
+  const size_t words[6] = {(size_t)batch, (size_t)batch, (size_t)batch + 1, (size_t)batch,
+                           (size_t)batch, (size_t)(batch / 2) * max_pages_per_seq};
   size_t off = base;
-  for (int i = 0; i < 5; ++i) {
+  for (int i = 0; i < 6; ++i) {
     offsets[5 + i] = off;
     off += align256(words[i] * 4);
   }
@@ -51,7 +52,7 @@ int pkv_cascade_decode_step_packed(void* host_in, void* dev_in, int32_t batch,
   const char* who = "pkv_cascade_decode_step_packed";
   if (!host_in || !dev_in || !out_dev || !out_host || !desc)
     return pkv::set_error(PKV_EINVAL, "%s: null pointer", who);
-  size_t off[10], total = 0;
+  size_t off[11], total = 0;
   int st = pkv_packed_cascade_layout(batch, num_q_heads, desc->num_kv_heads, desc->head_dim,
                                      max_pages_per_seq, dtype_q, dtype_new, off, &total);
   if (st != PKV_OK) return st;
@@ -78,6 +79,10 @@ int pkv_cascade_decode_step_packed(void* host_in, void* dev_in, int32_t batch,
     g.max_members = max_members;
     g.max_prefix_pages = max_prefix;
     g.max_own_pages = max_own;
+    st = pkv_cascade_prefix_page_ids(hp(3), max_pages_per_seq, hp(6), hp(7), hp(8), n_groups,
+                                     max_prefix, hp(10));
+    if (st != PKV_OK) return st;
+    g.prefix_page_ids = dp(10);
   }
   const size_t need = pkv_cascade_workspace_size(batch, num_q_heads, desc->num_kv_heads,
                                                  desc->head_dim, max_pages_per_seq, &g);
@@ -86,7 +91,9 @@ int pkv_cascade_decode_step_packed(void* host_in, void* dev_in, int32_t batch,
     return pkv::set_error(PKV_EINVAL, "%s: workspace of %zu bytes needed, %zu given", who, need,
                           workspace_bytes);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = pkv::traced_copy("h2d_copy", dev_in, host_in, total, cudaMemcpyHostToDevice, s);
+  // the block up to the end of the page ids this step's groups use
+  const size_t used = off[10] + (size_t)n_groups * max_prefix * sizeof(int32_t);
+  cudaError_t e = pkv::traced_copy("h2d_copy", dev_in, host_in, used, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess)
     return pkv::set_error(PKV_ECUDA, "%s: input copy: %s", who, cudaGetErrorString(e));
   st = pkv_cascade_decode_step(d + off[0], dtype_q, batch, num_q_heads, d + off[1], d + off[2],

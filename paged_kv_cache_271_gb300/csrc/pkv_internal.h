@@ -63,15 +63,21 @@ struct DecodeArgs {
 // of it that run at once on a GB300 (152 SMs x 3 resident CTAs).
 constexpr int kCascadeRows = 64;
 constexpr int kCascadeWaveCtas = 152 * 3;
-// The same for the tcgen05 prefix kernel (M = 128 rows per CTA, one CTA per SM).
+// The same for the tcgen05 prefix kernel (M = 128 rows per row tile, one CTA per SM). A CTA
+// takes two row tiles, sharing every K/V copy, when a group has more than one tile of rows.
 constexpr int kCascadeTcRows = 128;
 constexpr int kCascadeTcWaveCtas = 152;
+inline int cascade_tc_row_tiles(int rows_per_group) {
+  return rows_per_group > kCascadeTcRows ? 2 : 1;
+}
 
 // Members of the cascade groups (prefix kernel only).
 struct CascadeArgs {
   const int32_t* group_offsets;  // [n_groups + 1]: members of g are group_members[off[g] .. off[g+1])
   const int32_t* group_members;  // request indices
   int max_members;               // rows per group = members * group size; larger groups are cut
+  const int32_t* prefix_ids;     // [n_groups][ids_stride] shared page ids, or null: read the
+  int ids_stride;                // first member's table row instead
 };
 
 struct AppendArgs {

@@ -371,6 +371,14 @@ def test_cascade_groups_against_model():
         own = [-(-min(max(int(cl[b]), 0), 16 * W) // 16) - pre.get(b, 0) for b in range(B)]
         assert g.max_own_pages == max(own, default=0)
         assert g.own_start.tolist() == [pre.get(b, 0) for b in range(B)]
+        # each group's shared page ids: its members' common first table entries, -1 padded
+        if g.n_groups:
+            ids = g.prefix_page_ids.reshape(g.n_groups, g.max_prefix_pages)
+            for i, (mem, n) in enumerate(ref):
+                assert all(bt[b, :n].tolist() == ids[i, :n].tolist() for b in mem)
+                assert (ids[i, n:] == -1).all()
+        else:
+            assert g.prefix_page_ids is None
 
 
 def test_cascade_argument_errors_are_caught_on_the_host():
@@ -424,13 +432,14 @@ def test_packed_step_layout():
 
 def test_packed_cascade_layout_and_argument_errors():
     L = pkv.lib()
-    offs = (ctypes.c_size_t * 10)()
+    offs = (ctypes.c_size_t * 11)()
     total = ctypes.c_size_t(0)
     B = 100
     assert L.pkv_packed_cascade_layout(B, 32, 8, 128, 256, pkv.BF16, pkv.BF16, offs,
                                        ctypes.byref(total)) == 0
     sizes = [B * 32 * 128 * 2, B * 8 * 128 * 2, B * 8 * 128 * 2, B * 256 * 4, B * 4,
-             B * 4, B * 4, (B + 1) * 4, B * 4, B * 4]  # the step's inputs, then the groups
+             B * 4, B * 4, (B + 1) * 4, B * 4, B * 4,
+             (B // 2) * 256 * 4]  # the step's inputs, then the groups and their page ids
     expect, o = [], 0
     for n in sizes:
         expect.append(o)
