@@ -226,15 +226,14 @@ bool prefix_on_tcgen05() { return g_prefix_kernel.load() != 1; }
 
 // Pages per CTA of the cascade prefix kernel: the shared pages of each (group, KV head, rows
 // of a CTA) are cut into as many chunks as keep the launch within one wave of resident CTAs
-// (tcgen05: 128 or 256 rows per CTA, one CTA per SM, chunks of at least one 4-page tile;
+// (tcgen05: 128 rows per CTA, one CTA per SM, chunks of at least one 4-page tile;
 // mma.sync: 64 rows, three CTAs per SM, at least 2 pages); a chunk of at most the whole prefix.
 int prefix_chunk_pages_for(int n_groups, int h_kv, int group, int max_members, int max_prefix) {
   const int ov = g_prefix_chunk_override.load();
   if (ov > 0) return ov;
   if (max_prefix < 1) return 1;
   const bool tc = prefix_on_tcgen05();
-  const int rows =
-      tc ? kCascadeTcRows * cascade_tc_row_tiles(max_members * group) : kCascadeRows;
+  const int rows = tc ? kCascadeTcRows : kCascadeRows;
   // with the fold left to the combine, the tcgen05 prefix kernel takes about half the SMs and
   // the own-page decode runs on the rest meanwhile (prefix sharing, batch 128: two chunks,
   // 38.1 us a step, against 41.1 us with the prefix kernel on every SM)

@@ -1,35 +1,33 @@
 // Shared-prefix pass of the cascade decode on the fifth-generation tensor cores (tcgen05).
 //
-// Same result as the mma.sync prefix kernel (cascade_prefix.cu): for the query rows -- the
+// Same result as the mma.sync prefix kernel (cascade_prefix.cu): for 128 query rows -- the
 // (member, query head) pairs of one KV head of one group -- and a chunk of the group's shared
 // pages ("KV cache and PagedAttention", section 6), the partial (max, sum, weighted values) of
-// softmax attention over those pages. Here the two contractions run as tcgen05 MMAs with the
-// accumulators in tensor memory. A CTA takes one row tile of 128 rows, or two (256 rows) when
-// the group has more than 128 rows: both row tiles use every K/V tile the CTA copies, which
-// halves the copies per row (the TMA copies, ~80 ns each whatever their size, set the pace).
+// softmax attention over those pages. Here the two contractions run as tcgen05 MMAs whose A
+// operands and accumulators live in tensor memory, so that the tensor core fetches only K and
+// V from shared memory (with Q and P in shared memory too, ncu showed the tcgen05 pipe ~80 %
+// busy on operand fetches while its math ran ~45 % of the time):
 //
-//  * a copy warp (lane 0) streams 64-token tiles (4 pages) of K and V into a ring (5 stages
-//    with one row tile, 3 with two) with TMA copies (128-byte swizzle), refilling a stage as
-//    soon as the P V of its tile is done; an MMA warp (lane 0) issues the MMAs, for each row
-//    tile:
+//  * a copy warp (lane 0) streams 64-token tiles (4 pages) of K and V into a 6-stage ring with
+//    TMA copies (128-byte swizzle), refilling a stage as soon as the P V of its tile is done;
+//    an MMA warp (lane 0) issues the MMAs:
 //      S = Q K^T   M = 128 rows, N = 64 tokens, K = 128 dims  (8 MMAs of K = 16), S in TMEM;
 //      O += P V    M = 128 rows, N = 128 dims, K = 16 tokens (a page): 4 MMAs, O in TMEM;
-//    K arrives as two swizzled [64 rows][64 dims] blocks (2-D boxes, two per page), V as one
-//    4 KB block per page (a 3-D box);
-//    Q, K and P are K-major operands and V an MN-major one, all in the canonical 128-byte
-//    swizzled layout that the TMA copies (and the threads' swizzled stores) produce;
-//  * four softmax warps per row tile, one per TMEM lane quarter, so thread r owns row r: it
-//    zeroes its row of O once, then per tile reads its row of S (tcgen05.ld), applies the
-//    scale (log2 domain), writes P = exp2(s - m) as bf16 into a shared-memory buffer for the
-//    P V MMA and keeps the row sum in a register;
-//  * each row tile has three (two, with two row tiles) S buffers in TMEM and two P buffers in
-//    shared memory: the MMA warp keeps S that many tiles ahead of the softmax, and the P V of
-//    tile t overlaps the softmax of tile t+1;
+//    Q (A of S) and P (A of P V) are read from TMEM; K arrives as two swizzled
+//    [64 rows][64 dims] blocks (2-D boxes, two per page), K-major; V as one 4 KB block per page
+//    (a 3-D box), an MN-major operand;
+//  * four softmax warps, one per TMEM lane quarter, so thread r owns row r: it writes its query
+//    row into TMEM and zeroes its row of O once, then per tile reads its row of S
+//    (tcgen05.ld), applies the scale (log2 domain), writes P = exp2(s - m) as bf16 pairs over
+//    the first half of the same TMEM columns and keeps the row sum in a register;
+//  * S (then P) has three TMEM buffers: the MMA warp keeps S up to three tiles ahead of the
+//    softmax, and the P V of tile t overlaps the softmax of tile t+1; S(t+3) is issued only
+//    once the P V of tile t, which reads P(t) from that buffer, has completed;
 //  * the running maximum is updated lazily: O (in TMEM) is rescaled only when a row's maximum
 //    grows by more than 2^8 (until then P <= 2^8), so most tiles never touch O; the final
 //    (max, sum, O) triple is exact whatever maximum it was accumulated against.
 //
-// The query rows are gathered by the row threads while tensor memory is allocated and the first
+// The query rows are read by the row threads while tensor memory is allocated and the first
 // copies start; each row's partial leaves through shared memory and one bulk copy.
 // Every wait is bounded (PKV_DEVERR_TIMEOUT); the TMEM columns are freed on every exit path.
 #include <cuda.h>
@@ -44,41 +42,29 @@ namespace pkv {
 
 namespace {
 
-constexpr int kTcRows = kCascadeTcRows;                  // query rows per row tile (MMA M)
+constexpr int kTcRows = kCascadeTcRows;                  // query rows per CTA (MMA M)
+constexpr int kTcSoftWarps = kTcRows / 32;               // one per TMEM lane quarter
+constexpr int kTcMmaWarp = kTcSoftWarps;                 // issues the MMAs (lane 0)
+constexpr int kTcCopyWarp = kTcSoftWarps + 1;            // issues the TMA copies (lane 0)
+constexpr int kTcThreads = 32 * (kTcSoftWarps + 2);
 constexpr int kTcTok = 64;                               // tokens per tile
 constexpr int kTcPages = kTcTok / kPageSize;             // pages per tile
-constexpr int kTcQBytes = kTcRows * 256;                 // Q of a row tile: 128 rows x 128 bf16
+constexpr int kTcStages = 6;
 constexpr int kTcKV = kTcTok * 256;                      // K (or V) of one tile
 constexpr int kTcStageBytes = 2 * kTcKV;
-constexpr int kTcPBytes = kTcRows * kTcTok * 2;          // P of one tile of one row tile, bf16
+constexpr int kTcOffBar = kTcStages * kTcStageBytes;
+constexpr int kTcSmem = 1024 + kTcOffBar + 256;
+static_assert(kTcSmem <= 227 * 1024, "shared memory of one CTA");
+static_assert(8 * (2 * kTcStages + 3 + 3 + 2) + 4 * kTcStages + 4 <= 256, "barrier area");
+static_assert(kTcRows * 528 <= kTcOffBar, "partial staging over the ring");
+constexpr int kTcSBufs = 3;                              // S (then P) buffers in TMEM
+// tensor memory columns: O [0, 128), Q [128, 192) (bf16 pairs), S buffer b at 192 + 64 b; P
+// (bf16 pairs) overwrites the first 32 columns of its tile's S buffer
+constexpr uint32_t kTcColQ = 128;
+constexpr uint32_t kTcColS = 192;
 constexpr uint32_t kTcTmemCols = 512;
+static_assert(kTcColS + 64 * kTcSBufs <= kTcTmemCols, "tensor memory columns");
 constexpr float kTcLazyLog2 = 8.f;
-
-// Layout of a CTA that takes RT row tiles (RT = 1 or 2): 4 softmax warps per row tile (one per
-// TMEM lane quarter), then the MMA warp and the copy warp. Shared memory: Q of every row tile,
-// the K/V ring, two P buffers per row tile, barriers. Tensor memory: O of row tile rt at column
-// 128 rt, then the S buffers (64 columns each) of every row tile.
-template <int RT>
-struct TcLayout {
-  static constexpr int kRows = RT * kTcRows;
-  static constexpr int kSoftWarps = RT * (kTcRows / 32);
-  static constexpr int kMmaWarp = kSoftWarps;
-  static constexpr int kCopyWarp = kSoftWarps + 1;
-  static constexpr int kThreads = 32 * (kSoftWarps + 2);
-  static constexpr int kStages = RT == 1 ? 5 : 3;   // what the shared memory holds
-  static constexpr int kSBufs = RT == 1 ? 3 : 2;    // S buffers per row tile
-  static constexpr int kOffStage = RT * kTcQBytes;
-  static constexpr int kOffP = kOffStage + kStages * kTcStageBytes;
-  static constexpr int kOffBar = kOffP + RT * 2 * kTcPBytes;
-  static constexpr int kSmem = 1024 + kOffBar + 256;
-  static constexpr uint32_t kSCol0 = 128 * RT;
-  static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
-  static_assert(8 * (2 * kStages + kSBufs + 2 + 2) + 4 * kStages + 4 <= 256, "barrier area");
-  static_assert(kSCol0 + RT * kSBufs * 64 <= kTcTmemCols, "tensor memory columns");
-  // the partials leave through rows of 528 bytes from the start of shared memory, over Q and
-  // the ring (both idle by then)
-  static_assert(kRows * 528 <= kOffP, "partial staging");
-};
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A and B, A K-major,
 // B K-major or MN-major, shape M x N.
@@ -96,12 +82,14 @@ __device__ __forceinline__ uint64_t tc_desc(uint32_t saddr, uint32_t lbo, uint32
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate) {
+// D (+)= A B with the A operand in tensor memory (its 128 lanes are A's rows; its 32-bit columns
+// hold bf16 pairs along K, the lower index in the low half) and B described in shared memory.
+__device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -146,23 +134,16 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// Byte offset of 16-byte chunk ch (0..7) of row r in a K-major 128-byte-swizzled block of
-// 128-byte rows (8-row groups of 1024 bytes).
-__device__ __forceinline__ uint32_t sw128(int r, int ch) {
-  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4));
-}
-
-template <int G, int RT>
-__global__ void __launch_bounds__(TcLayout<RT>::kThreads, 1) cascade_prefix_tc_kernel(
+template <int G>
+__global__ void __launch_bounds__(kTcThreads, 1) cascade_prefix_tc_kernel(
     const DecodeArgs a, const CascadeArgs ca, const __grid_constant__ CUtensorMap tm_k2,
     const __grid_constant__ CUtensorMap tm_v) {
-  using L = TcLayout<RT>;
   constexpr int D = 128;
-  constexpr int NS = L::kStages, SB = L::kSBufs;
-  const int c = blockIdx.x, pair = blockIdx.y;
+  constexpr int NS = kTcStages, SB = kTcSBufs;
+  const int c = blockIdx.x, rt = blockIdx.y;
   const int g = blockIdx.z / a.h_kv, j = blockIdx.z % a.h_kv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool reporter = c == 0 && pair == 0 && threadIdx.x == 0;
+  const bool reporter = c == 0 && rt == 0 && threadIdx.x == 0;
   // the own-page decode (a programmatic dependent launch) may start on the SMs this grid leaves
   // free; it waits for this grid's completion before it reads the partials written here
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -179,7 +160,7 @@ __global__ void __launch_bounds__(TcLayout<RT>::kThreads, 1) cascade_prefix_tc_k
     members = ca.max_members;
   }
   const int n_rows = members * G;
-  if (pair * L::kRows >= n_rows) return;
+  if (rt * kTcRows >= n_rows) return;
   if (a.prefix_pages[g] > a.max_prefix_pages && reporter) atomicOr(a.err, PKV_DEVERR_BAD_GROUP);
   const int pp = cascade_group_pages(a, g);
   const int n_chunks = cascade_prefix_chunks(a, pp);
@@ -206,27 +187,28 @@ __global__ void __launch_bounds__(TcLayout<RT>::kThreads, 1) cascade_prefix_tc_k
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t su = smem_u32(smem);
-  const uint32_t q_u = su, stage_u = su + L::kOffStage, p_u = su + L::kOffP;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);  // [NS]
-  uint64_t* o_done = full + NS;                                      // [NS]: P V of a tile
-  uint64_t* s_done = o_done + NS;                                    // [SB]: S of every row tile
-  uint64_t* p_ready = s_done + SB;                                   // [2]
-  uint64_t* q_ready = p_ready + 2;                                   // [1]
-  uint64_t* mma_idle = q_ready + 1;                                  // [1]
-  int* page_mask = reinterpret_cast<int*>(mma_idle + 1);             // [NS]
+  const uint32_t stage_u = smem_u32(smem);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTcOffBar);  // [NS]
+  uint64_t* o_done = full + NS;                                     // [NS]: P V of a tile
+  uint64_t* s_done = o_done + NS;                                   // [SB]
+  // [SB]: P of a tile written (one per S buffer: the softmax warps can be up to SB - 1 tiles
+  // apart, since S(t + SB) waits for the P V of tile t, so no warp arrives for tile t + SB
+  // before the barrier of tile t has completed)
+  uint64_t* p_ready = s_done + SB;
+  uint64_t* q_ready = p_ready + SB;                                 // [1]
+  uint64_t* mma_idle = q_ready + 1;                                 // [1]
+  int* page_mask = reinterpret_cast<int*>(mma_idle + 1);            // [NS]
   uint32_t* s_taddr = reinterpret_cast<uint32_t*>(page_mask + NS);
 
-  // A softmax thread owns row r of row tile `tile`, in TMEM lane quarter warp % 4. The row
-  // threads gather their query rows (two dependent reads: member id, then the row) while the
-  // MMA warp allocates tensor memory and the copy warp starts the first copies.
-  const int tile = warp >> 2;
-  const int r = (warp & 3) * 32 + lane;
-  const int R = (pair * RT + tile) * kTcRows + r;
+  // The row threads read their query rows (two dependent reads: member id, then the row)
+  // while the MMA warp allocates tensor memory and the copy warp starts the first copies.
+  const int r = threadIdx.x;  // row of a softmax thread
+  const int R = rt * kTcRows + r;
   bool live = false;
   int rb = 0;
   const int rh = j * G + R % G;
-  if (warp < L::kSoftWarps) {
+  uint4 qv[16];
+  if (warp < kTcSoftWarps) {
     live = R < n_rows;
     rb = live ? ca.group_members[o0 + R / G] : 0;
     if (live && (rb < 0 || rb >= a.batch)) {
@@ -236,15 +218,9 @@ __global__ void __launch_bounds__(TcLayout<RT>::kThreads, 1) cascade_prefix_tc_k
     }
     const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
                                                        ((size_t)rb * a.h_q + rh) * D);
-    uint4 qv[16];
 #pragma unroll
     for (int c16 = 0; c16 < 16; ++c16) qv[c16] = live ? qrow[c16] : make_uint4(0, 0, 0, 0);
-    const uint32_t qt = q_u + tile * kTcQBytes;
-#pragma unroll
-    for (int c16 = 0; c16 < 16; ++c16)  // K-major swizzled Q tile (two 64-dim blocks)
-      sts128(qt + (c16 >> 3) * (kTcQBytes / 2) + sw128(r, c16 & 7), qv[c16]);
-    fence_proxy_async_smem();  // generic stores -> the MMA's reads
-  } else if (warp == L::kMmaWarp) {  // the TMEM columns: O of every row tile, the S buffers
+  } else if (warp == kTcMmaWarp) {  // the TMEM columns: O, Q and the S buffers
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(s_taddr)),
                  "r"(kTcTmemCols)
@@ -256,14 +232,14 @@ __global__ void __launch_bounds__(TcLayout<RT>::kThreads, 1) cascade_prefix_tc_k
       mbar_init(&o_done[s], 1);
     }
     for (int s = 0; s < SB; ++s) mbar_init(&s_done[s], 1);
-    for (int s = 0; s < 2; ++s) mbar_init(&p_ready[s], L::kRows);
-    mbar_init(q_ready, L::kRows);
+    for (int s = 0; s < SB; ++s) mbar_init(&p_ready[s], kTcRows);
+    mbar_init(q_ready, kTcRows);
     mbar_init(mma_idle, 1);
     mbar_fence_init();
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k2)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
   }
-  const uint64_t pol = l2_evict_last_policy();  // every CTA of the group reads them
+  const uint64_t pol = l2_evict_last_policy();  // every row tile of the group reads them
   // Copy warp: lane L holds the id of chunk page 32 m + L for the current batch m of 8 tiles,
   // read ahead of the copies so that no copy waits on a table read.
   int ids = -1;
@@ -307,7 +283,7 @@ __global__ void __launch_bounds__(TcLayout<RT>::kThreads, 1) cascade_prefix_tc_k
     }
   };
   int issued = 0;
-  if (warp == L::kCopyWarp) {
+  if (warp == kTcCopyWarp) {
     __syncwarp();  // lane 0 initialised the barriers
     for (; issued < NS && issued < n_tiles; ++issued) issue(issued, issued);
   }
@@ -317,7 +293,7 @@ __global__ void __launch_bounds__(TcLayout<RT>::kThreads, 1) cascade_prefix_tc_k
   const uint32_t tmem = *s_taddr;
   const float sc = a.scale_log2;
 
-  if (warp == L::kCopyWarp) {
+  if (warp == kTcCopyWarp) {
     // ===================== copy warp (lane 0 issues the copies) =====================
     // refill the stage of tile t with tile t + NS once the P V of tile t is done
     for (int t = 0; issued < n_tiles; ++t, ++issued) {
@@ -329,68 +305,73 @@ __global__ void __launch_bounds__(TcLayout<RT>::kThreads, 1) cascade_prefix_tc_k
       for (int t = max(0, issued - NS); t < issued; ++t)
         mbar_wait(&full[t % NS], (t / NS) & 1, a.err);
     }
-  } else if (warp == L::kMmaWarp) {
+  } else if (warp == kTcMmaWarp) {
     // ===================== MMA warp (lane 0) =====================
     if (lane == 0) {
-      bool ok = mbar_wait(q_ready, 0, a.err);  // Q stored and O zeroed
+      bool ok = mbar_wait(q_ready, 0, a.err);  // Q stored in TMEM and O zeroed
       tc_fence_after();
-      auto pv = [&](int u) {  // O(rt) += P(rt, u) V(u) for every row tile
-        if (!mbar_wait(&p_ready[u & 1], (u >> 1) & 1, a.err)) return false;
+      auto pv = [&](int u) {  // O += P(u) V(u), P read from its tile's S buffer in TMEM
+        if (!mbar_wait(&p_ready[u % SB], (u / SB) & 1, a.err)) return false;
         tc_fence_after();
         const int st = u % NS;
         const uint32_t vb = stage_u + st * kTcStageBytes + kTcKV;
+        const uint32_t p_tmem = tmem + kTcColS + 64 * (u % SB);
         if (page_mask[st] != 0) {  // O starts at zero (stored by the row threads)
 #pragma unroll
-          for (int rt = 0; rt < RT; ++rt) {
-            const uint32_t pb = p_u + (rt * 2 + (u & 1)) * kTcPBytes;
-#pragma unroll
-            for (int kk = 0; kk < kTcTok / 16; ++kk)
-              tc_mma(tmem + 128 * rt, tc_desc(pb + kk * 32, 16, 1024),
-                     tc_desc(vb + kk * 4096, 2048, 1024), kIdescPV, 1u);
-          }
+          for (int kk = 0; kk < kTcTok / 16; ++kk)
+            tc_mma_ta(tmem, p_tmem + 8 * kk, tc_desc(vb + kk * 4096, 2048, 1024), kIdescPV, 1u);
         }
         tc_commit(&o_done[st]);
         return true;
       };
-      auto s_mma = [&](int t) {  // S(rt, t) = Q(rt) K(t)^T into S buffer t % SB of each row tile
+      auto s_mma = [&](int t) {  // S(t) = Q K(t)^T into S buffer t % SB, Q read from TMEM
         const int st = t % NS;
         if (!mbar_wait(&full[st], (t / NS) & 1, a.err)) return false;
         tc_fence_after();
         const uint32_t kb = stage_u + st * kTcStageBytes;
+        const uint32_t s_tmem = tmem + kTcColS + 64 * (t % SB);
 #pragma unroll
-        for (int rt = 0; rt < RT; ++rt) {
-          const uint32_t s_tmem = tmem + L::kSCol0 + 64 * (rt * SB + t % SB);
-          const uint32_t qt = q_u + rt * kTcQBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            tc_mma(s_tmem, tc_desc(qt + (kk >> 2) * (kTcQBytes / 2) + (kk & 3) * 32, 16, 1024),
-                   tc_desc(kb + (kk >> 2) * (kTcKV / 2) + (kk & 3) * 32, 16, 1024), kIdescS,
-                   kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma_ta(s_tmem, tmem + kTcColQ + 8 * kk,
+                    tc_desc(kb + (kk >> 2) * (kTcKV / 2) + (kk & 3) * 32, 16, 1024), kIdescS,
+                    kk > 0 ? 1u : 0u);
         tc_commit(&s_done[t % SB]);
         return true;
       };
-      // S runs up to SB tiles ahead of P V: S(u + SB) reuses the buffers of S(u), free once
-      // the rows have read them (p_ready(u), waited in pv(u))
+      // S runs up to SB tiles ahead of P V. S(u + SB) overwrites the buffer that P(u) lives in,
+      // so it is issued only once the P V of tile u has completed.
       for (int t = 0; ok && t < SB && t < n_tiles; ++t) ok = s_mma(t);
       for (int u = 0; ok && u < n_tiles; ++u) {
         ok = pv(u);
-        if (ok && u + SB < n_tiles) ok = s_mma(u + SB);
+        if (ok && u + SB < n_tiles) {
+          ok = mbar_wait(&o_done[u % NS], (u / NS) & 1, a.err);
+          if (ok) ok = s_mma(u + SB);
+        }
       }
       // before leaving, every MMA issued is complete (on every path)
       tc_commit(mma_idle);
       mbar_wait(mma_idle, 0, a.err);
     }
   } else {
-    // ============ softmax warps: thread r of row tile `tile` owns row r ============
-    const uint32_t lane_t = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t o_col = 128 * tile;
-    {  // O = 0, so that every P V accumulates
-      uint32_t z[32];
+    // ===================== softmax warps: thread r owns row r =====================
+    const uint32_t lane_t = tmem + ((uint32_t)(warp * 32) << 16);
+    {  // Q into its TMEM columns (bf16 pairs along the head dimension), O = 0
+      uint32_t w[32];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) z[k] = 0u;
+      for (int h = 0; h < 2; ++h) {
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) tmem_st32(lane_t + o_col + 32 * cb, z);
+        for (int k = 0; k < 8; ++k) {
+          w[4 * k] = qv[8 * h + k].x;
+          w[4 * k + 1] = qv[8 * h + k].y;
+          w[4 * k + 2] = qv[8 * h + k].z;
+          w[4 * k + 3] = qv[8 * h + k].w;
+        }
+        tmem_st32(lane_t + kTcColQ + 32 * h, w);
+      }
+#pragma unroll
+      for (int k = 0; k < 32; ++k) w[k] = 0u;
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tmem_st32(lane_t + 32 * cb, w);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(q_ready);
@@ -409,7 +390,7 @@ __global__ void __launch_bounds__(TcLayout<RT>::kThreads, 1) cascade_prefix_tc_k
       const int mask = page_mask[st];
       tc_fence_after();
       uint32_t sr[64];
-      const uint32_t s_col = L::kSCol0 + 64 * (tile * SB + t % SB);
+      const uint32_t s_col = kTcColS + 64 * (t % SB);
       tmem_ld32(lane_t + s_col, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
       tmem_ld32(lane_t + s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_wait_ld();
@@ -443,46 +424,37 @@ __global__ void __launch_bounds__(TcLayout<RT>::kThreads, 1) cascade_prefix_tc_k
 #pragma unroll
           for (int cb = 0; cb < 4; ++cb) {
             uint32_t o[32];
-            tmem_ld32(lane_t + o_col + 32 * cb, o);
+            tmem_ld32(lane_t + 32 * cb, o);
             tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-            tmem_st32(lane_t + o_col + 32 * cb, o);
+            tmem_st32(lane_t + 32 * cb, o);
           }
           tmem_wait_st();
           l *= alpha;
           m_used = m_new;
         }
       }
-      if (t >= 2) {  // P buffer t & 1 was read by the P V of tile t - 2
-        const int u = t - 2;
-        ok = mbar_wait(&o_done[u % NS], (u / NS) & 1, a.err);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-      }
+      // P = 2^(s - m) as bf16 pairs over the first 32 columns of the tile's S buffer (its S
+      // is in registers now); the P V MMA reads it from there
       const float m_use = m_used == -INFINITY ? 0.f : m_used;
-      const uint32_t prow = p_u + (tile * 2 + (t & 1)) * kTcPBytes;
+      uint32_t pw[32];
       float sum8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) sum8[k] = 0.f;
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        float p[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          p[k] = ex2_approx(fmaf(__uint_as_float(sr[8 * cc + k]), sc, -m_use));
-          sum8[k] += p[k];
-        }
-        sts128(prow + sw128(r, cc),
-               make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]), pack_bf16(p[4], p[5]),
-                          pack_bf16(p[6], p[7])));
+      for (int k = 0; k < 32; ++k) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * k]), sc, -m_use));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * k + 1]), sc, -m_use));
+        sum8[(2 * k) & 7] += p0;
+        sum8[(2 * k + 1) & 7] += p1;
+        pw[k] = pack_bf16(p0, p1);
       }
+      tmem_st32(lane_t + s_col, pw);
       l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_ready[t & 1]);
+      mbar_arrive(&p_ready[t % SB]);
     }
     // ---- the row's partial for this chunk ----
     if (ok) {
@@ -490,15 +462,15 @@ __global__ void __launch_bounds__(TcLayout<RT>::kThreads, 1) cascade_prefix_tc_k
       ok = mbar_wait(&o_done[u % NS], (u / NS) & 1, a.err);
     }
     if (__all_sync(0xffffffffu, ok)) {
-      // every MMA and copy of the CTA is complete: the row's O goes through shared memory (rows
-      // 528 bytes apart from the start, over Q and the ring: no bank conflicts), then one bulk
-      // copy of its 512 bytes to the workspace
+      // every MMA and copy of the CTA is complete: the row's O goes through shared memory (the
+      // free ring, rows 528 bytes apart: no bank conflicts), then one bulk copy of its 512
+      // bytes to the workspace
       tc_fence_after();
-      const uint32_t orow = su + (tile * kTcRows + r) * 528;
+      const uint32_t orow = stage_u + r * 528;
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t o[32];
-        tmem_ld32(lane_t + o_col + 32 * cb, o);
+        tmem_ld32(lane_t + 32 * cb, o);
         tmem_wait_ld();
 #pragma unroll
         for (int k = 0; k < 8; ++k)
@@ -523,7 +495,7 @@ __global__ void __launch_bounds__(TcLayout<RT>::kThreads, 1) cascade_prefix_tc_k
 
   tc_fence_before();
   __syncthreads();
-  if (warp == L::kMmaWarp) {
+  if (warp == kTcMmaWarp) {
     __syncwarp();
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -532,32 +504,24 @@ __global__ void __launch_bounds__(TcLayout<RT>::kThreads, 1) cascade_prefix_tc_k
   }
 }
 
-template <int G, int RT>
-cudaError_t launch_tc_rt(const DecodeArgs& a, const CascadeArgs& ca, const CUtensorMap& tk,
-                         const CUtensorMap& tv, cudaStream_t s) {
-  using L = TcLayout<RT>;
-  auto kern = cascade_prefix_tc_kernel<G, RT>;
+template <int G>
+cudaError_t launch_tc_g(const DecodeArgs& a, const CascadeArgs& ca, const CUtensorMap& tk,
+                        const CUtensorMap& tv, cudaStream_t s) {
+  auto kern = cascade_prefix_tc_kernel<G>;
   static unsigned long long attr_done = 0;  // one bit per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !((attr_done >> dev) & 1ull)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_done |= 1ull << dev;
   }
   const int chunks = (a.max_prefix_pages + a.prefix_chunk_pages - 1) / a.prefix_chunk_pages;
-  const int pairs = (ca.max_members * G + L::kRows - 1) / L::kRows;
-  dim3 grid(chunks, pairs, a.n_groups * a.h_kv);
-  kern<<<grid, L::kThreads, L::kSmem, s>>>(a, ca, tk, tv);
+  const int tiles = (ca.max_members * G + kTcRows - 1) / kTcRows;
+  dim3 grid(chunks, tiles, a.n_groups * a.h_kv);
+  kern<<<grid, kTcThreads, kTcSmem, s>>>(a, ca, tk, tv);
   return cudaGetLastError();
-}
-
-template <int G>
-cudaError_t launch_tc_g(const DecodeArgs& a, const CascadeArgs& ca, const CUtensorMap& tk,
-                        const CUtensorMap& tv, cudaStream_t s) {
-  return cascade_tc_row_tiles(ca.max_members * G) == 2 ? launch_tc_rt<G, 2>(a, ca, tk, tv, s)
-                                                       : launch_tc_rt<G, 1>(a, ca, tk, tv, s);
 }
 
 }  // namespace

@@ -63,13 +63,9 @@ struct DecodeArgs {
 // of it that run at once on a GB300 (152 SMs x 3 resident CTAs).
 constexpr int kCascadeRows = 64;
 constexpr int kCascadeWaveCtas = 152 * 3;
-// The same for the tcgen05 prefix kernel (M = 128 rows per row tile, one CTA per SM). A CTA
-// takes two row tiles, sharing every K/V copy, when a group has more than one tile of rows.
+// The same for the tcgen05 prefix kernel (M = 128 rows per CTA, one CTA per SM).
 constexpr int kCascadeTcRows = 128;
 constexpr int kCascadeTcWaveCtas = 152;
-inline int cascade_tc_row_tiles(int rows_per_group) {
-  return rows_per_group > kCascadeTcRows ? 2 : 1;
-}
 
 // Members of the cascade groups (prefix kernel only).
 struct CascadeArgs {
