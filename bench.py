@@ -14,8 +14,10 @@ rotate``, the default), or the L2 is flushed with a 256 MiB write before every t
 
 The default workload is the layer above; the others (``--workload``) are the 70B long-context
 layer, prefix sharing (plain and cascade), FP8 and INT8 continuous batching (one step's state,
-or the whole trace step by step with its frees, replacements and prompt prefills), the sliding
-window with sinks and the copy-on-write fork of parallel sampling, each measured the same way.
+or the whole trace step by step with its frees, replacements and prompt prefills), the prompt
+prefill of replacement requests through the quantising append alone (FP8 or INT8 codes), the
+sliding window with sinks and the copy-on-write fork of parallel sampling, each measured the
+same way.
 
 Prints one JSON line on rank 0. ``value`` is algorithmic HBM bytes per step (K and V of every
 attended token, the queries, the outputs, and the appended rows) over the step time, summed
@@ -60,7 +62,8 @@ def peaks(kind="hbm_gbs"):
 
 WORKLOADS = ("llama3_8b_b64", "llama3_70b_long", "prefix_sharing", "prefix_sharing_cascade",
              "fp8_cb_b256", "fp8_cb_b64", "int8_cb_b256", "llama3_8b_window",
-             "parallel_sampling_fork", "fp8_cb_trace", "int8_cb_trace")
+             "parallel_sampling_fork", "fp8_cb_trace", "int8_cb_trace", "fp8_prompt_append",
+             "int8_prompt_append")
 
 
 def workload(name="llama3_8b_b64"):
@@ -646,6 +649,122 @@ class L2Flush:
             self.buf.zero_()
 
 
+def run_prompt_append(args):
+    """The prompt prefill of replacement requests in the continuous-batching workload through
+    the quantising append alone: 20 prompts of U[128, 2048] tokens (seeded), bf16 K/V rows
+    already on the device (three input sets used in turn, 250 MB: more than the L2), quantised
+    with per-head scales into an FP8 (or INT8) pool at slots the request tables hand out. A
+    step is one kv_append launch; ``value`` is its bytes (bf16 rows read, codes written) over
+    the step time. ``e2e`` adds the copy of the rows and slots from pinned host memory."""
+    import torch
+    import paged_kv_cache_271_gb300 as pkv
+    from paged_kv_cache_271_gb300.cache import PagedKVCache
+    ws, rank, local = rank_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(ws, "nccl")
+    pkv.lib()
+    i8 = args.workload.startswith("int8")
+    h_kv, d = 8, 128
+    rng = np.random.default_rng(271005)
+    lens = rng.integers(128, 2049, 20)
+    n = int(lens.sum())
+    pages = int(sum(pkv.pages_needed(int(x)) for x in lens) * 1.1) + 1
+    g = torch.Generator().manual_seed(271005)
+    sets = [(torch.randn(n, h_kv, d, generator=g).to(torch.bfloat16).to(dev),
+             torch.randn(n, h_kv, d, generator=g).to(torch.bfloat16).to(dev)) for _ in range(3)]
+    ks = pkv.kv_absmax_scales(sets[0][0], int8=i8)
+    vs = pkv.kv_absmax_scales(sets[0][1], int8=i8)
+    cache = PagedKVCache(pages, h_kv, d, torch.int8 if i8 else torch.float8_e4m3fn, dev,
+                         initial_free_order=rng.permutation(pages), k_scales=ks, v_scales=vs)
+    rids = list(range(len(lens)))
+    for r in rids:
+        cache.add_request(r)
+    slots_host = cache.reserve(rids, [int(x) for x in lens])
+    slots = torch.from_numpy(slots_host).to(dev)
+    byts = 2 * n * h_kv * d * (2 + 1)
+
+    def step(i, stream=None):
+        k, v = sets[i % 3]
+        pkv.kv_append(k, v, slots, cache.k, cache.v, ks, vs, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        st[i].record(stream)
+        step(i)
+        en[i].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in zip(st, en)]))
+    assert pkv.device_error() == 0
+    max_ms = max_over_ranks(ms, dev)
+    hbm_peak, peak_kind = peaks()
+    value = aggregate(byts, max_ms, ws)
+
+    # e2e: the step's rows and slots copied from pinned host memory, then the append
+    hk = [torch.empty((n, h_kv, d), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    hk[0].copy_(sets[0][0].cpu())
+    hk[1].copy_(sets[0][1].cpu())
+    hs = torch.from_numpy(slots_host).pin_memory()
+    dk, dv, dsl = torch.empty_like(sets[0][0]), torch.empty_like(sets[0][1]), torch.empty_like(slots)
+    for i in range(3):
+        dk.copy_(hk[0], non_blocking=True)
+        dv.copy_(hk[1], non_blocking=True)
+        dsl.copy_(hs, non_blocking=True)
+        pkv.kv_append(dk, dv, dsl, cache.k, cache.v, ks, vs)
+    torch.cuda.synchronize()
+    e_st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    for i in range(args.steps):
+        e_st[i].record(stream)
+        dk.copy_(hk[0], non_blocking=True)
+        dv.copy_(hk[1], non_blocking=True)
+        dsl.copy_(hs, non_blocking=True)
+        pkv.kv_append(dk, dv, dsl, cache.k, cache.v, ks, vs)
+        e_en[i].record(stream)
+        e_en[i].synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in zip(e_st, e_en)])), dev)
+    assert pkv.device_error() == 0
+    if rank == 0:
+        coded = "int8" if i8 else "fp8_e4m3"
+        print(json.dumps({
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16->" + coded, "data": "synthetic",
+            "config": {"workload": "%s_prompt_append_20_prompts" % coded.split("_")[0],
+                       "prompt_lens": "U[128, 2048] seeded, sum %d" % n, "num_kv_heads": h_kv,
+                       "head_dim": d, "page_size": 16, "kv_dtype": coded, "pool_pages": pages,
+                       "l2": "not flushed: 3 input sets of %.0f MB used in turn" % (
+                           2 * n * h_kv * d * 2 / 1e6),
+                       "step": "device: one quantising kv_append launch (bf16 rows in, codes "
+                               "written at the requests' slots)",
+                       "parallelism": "replicas x%d" % ws},
+            "roofline": {"bound": "hbm", "kernel": "kv_append (bf16 -> %s)" % coded,
+                         "achieved": round(value / ws, 1), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(value / ws / hbm_peak, 4), "peak_kind": peak_kind,
+                         "traffic": None, "algorithmic_bytes_per_launch": byts,
+                         "launch_ms": round(max_ms, 5), "sm_mhz": clk.get("sm_mhz")},
+            "cpu_baseline": None,
+            "e2e": {"value": round(aggregate(byts, e2e_ms, ws), 1), "unit": "GB/s",
+                    "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": 2 * n * h_kv * d * 2 + 8 * n,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": args.steps, "clocks": clk}), flush=True)
+
+
 def run_fork(args):
     """Copy-on-write fork (parallel sampling): per step, fork each of 16 prompts into 4 samples
     (reference counts), reserve each sample's first slot -- the shared, partly filled last page
@@ -1174,6 +1293,8 @@ def main(argv=None):
         run_fork(args)
     elif args.workload in ("fp8_cb_trace", "int8_cb_trace"):
         run_trace(args)
+    elif args.workload in ("fp8_prompt_append", "int8_prompt_append"):
+        run_prompt_append(args)
     else:
         run_ours(args)
 

@@ -340,6 +340,63 @@ def test_int8_quantiser_matches_oracle_on_every_bf16_pattern():
     assert pkv.device_error() == 0
 
 
+@pytest.mark.parametrize("int8", [False, True])
+@pytest.mark.parametrize("n_tok", [2048, 4099, 25001])
+def test_prompt_sized_append_bit_exact(int8, n_tok):
+    # a prompt-sized batch (bf16 rows into an FP8 or INT8 cache): every bf16 pattern, cycled
+    # through the rows, a token count that is not a multiple of the kernel's token pairs, eight
+    # per-head scales that include both ends of the reciprocal division's range and beyond,
+    # padding slots (-1, skipped) and slots in shuffled pages
+    h_kv, d = 8, 128
+    bits = torch.arange(0, 65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+    pats = bits[torch.isfinite(bits)] if int8 else bits[~torch.isnan(bits)]
+    need = n_tok * h_kv * d
+    idx = torch.randperm(need, generator=torch.Generator().manual_seed(n_tok)) % pats.numel()
+    k = pats[idx].reshape(n_tok, h_kv, d).contiguous()
+    v = pats[idx.flip(0)].reshape(n_tok, h_kv, d).contiguous()
+    scales = torch.tensor([1.0, 0.0123, 2.0 ** -80, 2.0 ** 80, 2.0 ** -90, 37.0, 3e-5, 7e4])
+    pages = n_tok // 16 + 8
+    rng = np.random.default_rng(n_tok)
+    slots = (rng.permutation(pages)[:, None] * 16 + np.arange(16)[None, :]).ravel()[:n_tok]
+    slots = slots.astype(np.int64)
+    slots[rng.choice(n_tok, n_tok // 50, replace=False)] = -1
+    dt = torch.int8 if int8 else torch.uint8
+    kc = torch.full((pages, h_kv, 16, d), 0x55, dtype=torch.uint8).view(dt).cuda()
+    vc = kc.clone()
+    sc_k, sc_v = scales.cuda(), scales.flip(0).contiguous().cuda()
+    pkv.kv_append(k.cuda(), v.cuda(), torch.from_numpy(slots).cuda(), kc, vc, sc_k, sc_v)
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    quant = oracle.quantize_int8 if int8 else oracle.quantize_e4m3
+    for pool, x, sc in ((kc, k, scales), (vc, v, scales.flip(0))):
+        got = pool.cpu().numpy().view(np.uint8).copy()
+        ref = np.full_like(got, 0x55)
+        xf = x.float().numpy()
+        codes = np.stack([quant(xf[:, j], float(sc[j])) for j in range(h_kv)], 1).view(np.uint8)
+        ok = slots >= 0
+        ref[slots[ok] // 16, :, slots[ok] % 16, :] = codes[ok]
+        np.testing.assert_array_equal(got, ref)
+
+
+def test_prompt_sized_append_bad_slot():
+    # a prompt-sized append reports a slot past the pool and skips that token only
+    n, h_kv, d = 3000, 8, 128
+    pages = n // 16 + 1
+    x = torch.ones(n, h_kv, d, dtype=torch.bfloat16, device="cuda")
+    slots = torch.arange(n, dtype=torch.int64)
+    slots[1500] = pages * 16 + 5
+    kc = torch.zeros(pages, h_kv, 16, d, dtype=torch.uint8, device="cuda")
+    vc = torch.zeros_like(kc)
+    one = torch.ones(h_kv, device="cuda")
+    pkv.device_error()
+    pkv.kv_append(x, x, slots.cuda(), kc, vc, one, one)
+    assert pkv.device_error() & pkv.DEVERR_BAD_SLOT
+    code = int(oracle.quantize_e4m3(np.ones(1, np.float32), 1.0)[0])
+    flat = kc.permute(0, 2, 1, 3).reshape(pages * 16, h_kv * d).cpu()
+    written = (flat == code).all(1)
+    assert int(written.sum()) == n - 1 and not bool(written[1500])
+
+
 # ---- device error word: bad inputs are skipped, never faulted on ---------------------------------
 
 def test_bad_page_id_sets_error_word():
