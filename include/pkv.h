@@ -506,11 +506,13 @@ int pkv_cascade_groups(const int32_t* block_tables, const int32_t* context_lens,
 
 /* The shared page ids of each group, [n_groups][max_prefix_pages] (row g: the first
  * prefix_pages[g] entries of its first member's table row, the rest -1), from the host arrays
- * pkv_cascade_groups wrote; ids_out is host memory of n_groups * max_prefix_pages int32. */
-int pkv_cascade_prefix_page_ids(const int32_t* block_tables, int32_t max_pages_per_seq,
-                                const int32_t* prefix_pages, const int32_t* group_offsets,
-                                const int32_t* group_members, int32_t n_groups,
-                                int32_t max_prefix_pages, int32_t* ids_out);
+ * pkv_cascade_groups wrote for block_tables [batch][max_pages_per_seq]; ids_out is host memory
+ * of n_groups * max_prefix_pages int32. PKV_EINVAL for a group without members, a member
+ * outside [0, batch) or more shared pages than max_prefix_pages. */
+int pkv_cascade_prefix_page_ids(const int32_t* block_tables, int32_t batch,
+                                int32_t max_pages_per_seq, const int32_t* prefix_pages,
+                                const int32_t* group_offsets, const int32_t* group_members,
+                                int32_t n_groups, int32_t max_prefix_pages, int32_t* ids_out);
 
 /* Workspace bytes of a cascade decode (its partials: the prefix chunks, then the members' own
  * chunks, for every request); pkv_decode_workspace_size when groups has no group. Zero-fill it

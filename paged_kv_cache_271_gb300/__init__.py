@@ -148,7 +148,7 @@ def lib():
                                               ctypes.POINTER(i32), ctypes.POINTER(i32),
                                               ctypes.POINTER(i32), ctypes.POINTER(i32), vp]),
         "pkv_cascade_workspace_size": (sz, [i32, i32, i32, i32, i32, C]),
-        "pkv_cascade_prefix_page_ids": (ctypes.c_int, [vp, i32, vp, vp, vp, i32, i32, vp]),
+        "pkv_cascade_prefix_page_ids": (ctypes.c_int, [vp, i32, i32, vp, vp, vp, i32, i32, vp]),
         "pkv_cascade_prefix_chunk_pages": (i32, [i32, i32, C]),
         "pkv_cascade_decode_attention": (ctypes.c_int, [vp, i32, i32, i32, vp, vp, D, vp, i32,
                                                         vp, f32, C, vp, vp, sz, vp]),
@@ -400,7 +400,7 @@ def cascade_groups(block_tables, context_lens, min_members=2, min_prefix_pages=1
     ng = n.value
     ids = np.empty(max(ng * mp.value, 1), np.int32)
     if ng:
-        _check(lib().pkv_cascade_prefix_page_ids(bt.ctypes.data, W, prefix.ctypes.data,
+        _check(lib().pkv_cascade_prefix_page_ids(bt.ctypes.data, B, W, prefix.ctypes.data,
                                                  offs.ctypes.data, members.ctypes.data, ng,
                                                  mp.value, ids.ctypes.data))
     return CascadeGroups(group_of, prefix[:ng].copy(), offs[:ng + 1].copy(),

@@ -102,20 +102,25 @@ extern "C" int pkv_cascade_groups(const int32_t* block_tables, const int32_t* co
   return PKV_OK;
 }
 
-extern "C" int pkv_cascade_prefix_page_ids(const int32_t* block_tables, int32_t max_pages_per_seq,
+extern "C" int pkv_cascade_prefix_page_ids(const int32_t* block_tables, int32_t batch,
+                                           int32_t max_pages_per_seq,
                                            const int32_t* prefix_pages,
                                            const int32_t* group_offsets,
                                            const int32_t* group_members, int32_t n_groups,
                                            int32_t max_prefix_pages, int32_t* ids_out) {
-  if (n_groups < 0 || max_prefix_pages < 0 || max_prefix_pages > max_pages_per_seq ||
+  if (n_groups < 0 || batch < 0 || max_prefix_pages < 0 ||
+      max_prefix_pages > max_pages_per_seq ||
       (n_groups > 0 && (!block_tables || !prefix_pages || !group_offsets || !group_members ||
                         !ids_out)))
     return pkv::set_error(PKV_EINVAL, "pkv_cascade_prefix_page_ids: bad argument");
   for (int32_t g = 0; g < n_groups; ++g) {
     const int32_t pp = prefix_pages[g];
-    if (pp < 0 || pp > max_prefix_pages || group_offsets[g] >= group_offsets[g + 1])
+    const int32_t first = group_offsets[g] < group_offsets[g + 1] && group_offsets[g] >= 0
+                              ? group_members[group_offsets[g]]
+                              : -1;
+    if (pp < 0 || pp > max_prefix_pages || first < 0 || first >= batch)
       return pkv::set_error(PKV_EINVAL, "pkv_cascade_prefix_page_ids: group %d is malformed", g);
-    const int32_t* row = block_tables + (size_t)group_members[group_offsets[g]] * max_pages_per_seq;
+    const int32_t* row = block_tables + (size_t)first * max_pages_per_seq;
     int32_t* out = ids_out + (size_t)g * max_prefix_pages;
     std::memcpy(out, row, (size_t)pp * sizeof(int32_t));
     for (int32_t i = pp; i < max_prefix_pages; ++i) out[i] = -1;

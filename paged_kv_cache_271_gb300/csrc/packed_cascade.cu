@@ -79,8 +79,8 @@ int pkv_cascade_decode_step_packed(void* host_in, void* dev_in, int32_t batch,
     g.max_members = max_members;
     g.max_prefix_pages = max_prefix;
     g.max_own_pages = max_own;
-    st = pkv_cascade_prefix_page_ids(hp(3), max_pages_per_seq, hp(6), hp(7), hp(8), n_groups,
-                                     max_prefix, hp(10));
+    st = pkv_cascade_prefix_page_ids(hp(3), batch, max_pages_per_seq, hp(6), hp(7), hp(8),
+                                     n_groups, max_prefix, hp(10));
     if (st != PKV_OK) return st;
     g.prefix_page_ids = dp(10);
   }

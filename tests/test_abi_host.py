@@ -379,6 +379,16 @@ def test_cascade_groups_against_model():
                 assert (ids[i, n:] == -1).all()
         else:
             assert g.prefix_page_ids is None
+    # malformed groups are refused before any table row is read
+    L = pkv.lib()
+    bt = np.zeros((2, 4), np.int32)
+    ids = np.zeros(8, np.int32)
+    for members, offs in (([5], [0, 1]), ([0], [0, 0]), ([-1], [0, 1])):
+        m = np.array(members, np.int32)
+        o = np.array(offs, np.int32)
+        pp = np.array([2], np.int32)
+        assert L.pkv_cascade_prefix_page_ids(bt.ctypes.data, 2, 4, pp.ctypes.data, o.ctypes.data,
+                                             m.ctypes.data, 1, 2, ids.ctypes.data) == -1
 
 
 def test_cascade_argument_errors_are_caught_on_the_host():
