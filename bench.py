@@ -171,6 +171,18 @@ class StepState:
                                              self.bt.shape[1])
         self.workspace = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev)
 
+    def split_label(self):
+        """Which split the decode of this step used (autotuning records it on the first call)."""
+        import paged_kv_cache_271_gb300 as pkv
+        if self.groups is not None and self.groups.n_groups > 0:
+            return "cascade (chunks)"
+        kv = self.k.dtype
+        choice = pkv.decode_split_choice(kv, self.q.dtype, self.batch, self.h_q, self.h_kv,
+                                         self.bt.shape[1], getattr(self, "window", 0) or 0,
+                                         getattr(self, "sink", 0) or 0, fused=True)
+        return {1: "balanced (measured faster)", 0: "chunks (measured faster)"}.get(
+            choice, "chunks (no split measured: one pass or chunks only)")
+
     def decode_bytes(self):
         """K and V of every attended token + queries + outputs."""
         return self.ctx_sum * self.h_kv * self.d * self.kv_bytes * 2 + 2 * self.batch * self.h_q * self.d * 2
@@ -416,8 +428,9 @@ def _cpu_model():
 
 # the files the tensor-core decode kernel and its launch are compiled from: the recorded
 # ncu traffic stays valid until one of them changes
-DECODE_KERNEL_SOURCES = ("decode_mma.cu", "paged_decode_mma.cuh", "decode_epilogue.cuh",
-                         "decode_plan.cuh", "pkv_device.cuh", "pkv_internal.h", "capi.cu")
+DECODE_KERNEL_SOURCES = ("decode_mma.cu", "decode_flat.cu", "paged_decode_mma.cuh",
+                         "decode_epilogue.cuh", "decode_plan.cuh", "combine_merge.cuh",
+                         "pkv_device.cuh", "pkv_internal.h", "capi.cu")
 
 
 def source_sha() -> str:
@@ -454,6 +467,8 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     init_dist(ws, "nccl")
     pkv.lib()  # fail loudly if the library is missing
+    # the decode's split (chunks or balanced) is measured on the first call of the shape
+    pkv.decode_set_autotune(True)
 
     sc = StepState(args.workload, dev)
     stream = torch.cuda.current_stream()
@@ -480,6 +495,7 @@ def run_ours(args):
         sc.fused_step(pool=i % n_sets)
     torch.cuda.synchronize()
     assert pkv.device_error() == 0
+    sc.config["split"] = sc.split_label()
 
     # The step's device work (append, decode, combine) is captured once as a CUDA graph (one
     # per pool copy) and replayed every step, as a serving loop would; the host slot mapping
@@ -1058,6 +1074,7 @@ def run_trace(args):
     dev = torch.device("cuda", local)
     init_dist(ws, "nccl")
     pkv.lib()
+    pkv.decode_set_autotune(True)  # as in run_ours
     coded = "int8" if args.workload.startswith("int8") else "fp8_e4m3"
     n_warm, n = max(3, args.warmup), max(1, args.steps)
     tr = workloads.fp8_continuous_batching(steps=n_warm + n)

@@ -92,6 +92,10 @@ def lib():
         "pkv_decode_set_chunk_pages": (ctypes.c_int, [i32]),
         "pkv_decode_chunk_pages": (i32, [i32, i32, i32]),
         "pkv_decode_set_kernel": (ctypes.c_int, [i32]),
+        "pkv_decode_set_split": (ctypes.c_int, [i32]),
+        "pkv_decode_set_autotune": (ctypes.c_int, [i32]),
+        "pkv_decode_autotune_reset": (ctypes.c_int, []),
+        "pkv_decode_split_choice": (ctypes.c_int, [i32, i32, i32, i32, i32, i32, i32, i32, i32]),
         "pkv_decode_set_merge_in_place": (ctypes.c_int, [i32]),
         "pkv_decode_set_warp_per_request": (ctypes.c_int, [i32]),
         "pkv_cascade_set_overlap": (ctypes.c_int, [i32]),
@@ -715,6 +719,31 @@ def decode_set_merge_in_place(max_chunks: int):
 def decode_set_kernel(which: int):
     """0 automatic, 1 CUDA-core decode kernel, 2 tensor-core decode kernel."""
     _check(lib().pkv_decode_set_kernel(int(which)))
+
+
+def decode_set_split(mode: int):
+    """0 automatic (the split autotuning recorded for the call's shape, else chunks), 1 chunks
+    only, 2 the balanced split of the tensor-core decode wherever it applies."""
+    _check(lib().pkv_decode_set_split(int(mode)))
+
+
+def decode_set_autotune(on: bool):
+    """Time both splits on the first call of each shape and keep the faster (pkv.h)."""
+    _check(lib().pkv_decode_set_autotune(1 if on else 0))
+
+
+def decode_autotune_reset():
+    _check(lib().pkv_decode_autotune_reset())
+
+
+def decode_split_choice(kv_dtype, q_dtype, batch, num_q_heads, num_kv_heads, max_pages_per_seq,
+                        window=0, sink_tokens=0, fused=False) -> int:
+    """The recorded split for a shape: 1 balanced, 0 chunks, -1 none. Dtypes as torch dtypes
+    or pkv_dtype codes."""
+    code = lambda d: d if isinstance(d, int) else _dtype_code(torch.empty(0, dtype=d))
+    return int(lib().pkv_decode_split_choice(code(kv_dtype), code(q_dtype), batch, num_q_heads,
+                                             num_kv_heads, max_pages_per_seq, window, sink_tokens,
+                                             1 if fused else 0))
 
 
 def decode_chunk_pages(batch, num_kv_heads, max_pages_per_seq) -> int:

@@ -10,6 +10,7 @@
 #include <algorithm>
 #include <math.h>
 
+#include "combine_merge.cuh"
 #include "decode_plan.cuh"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
@@ -102,22 +103,28 @@ __device__ __forceinline__ KnownDivisor known_divisor(float scale) {
   return d;
 }
 
+// Returns true where the vector took the IEEE division (NaN quotients stay NaN there).
 template <typename TIN, int N>
-__device__ __forceinline__ void divide_vec(const float (&x)[N], const KnownDivisor& d,
+__device__ __forceinline__ bool divide_vec(const float (&x)[N], const KnownDivisor& d,
                                            float (&q)[N]) {
   bool slow = sizeof(TIN) == 4 || !d.fast;
   if (!slow) {
+    float sum = 0.f;
 #pragma unroll
     for (int k = 0; k < N; ++k) {
       const float q0 = __fmul_rn(x[k], d.r);
       q[k] = __fmaf_rn(-__fmaf_rn(q0, d.s, -x[k]), d.r, q0);
-      slow |= q[k] != q[k];  // NaN: infinite or NaN x, or an overflow
+      sum = __fadd_rn(sum, q[k]);
     }
+    // a NaN quotient makes the sum NaN; so can two infinite ones of opposite signs, which the
+    // IEEE division then gives again
+    slow = sum != sum;
   }
   if (slow) {
 #pragma unroll
     for (int k = 0; k < N; ++k) q[k] = __fdiv_rn(x[k], d.s);
   }
+  return slow;
 }
 
 template <typename TIN, int N>
@@ -134,33 +141,46 @@ __device__ __forceinline__ void quantize_store(const float (&x)[N], const KnownD
     uint2 w;
     w.x = (uint32_t)codes[0] | ((uint32_t)codes[1] << 16);
     w.y = (uint32_t)codes[2] | ((uint32_t)codes[3] << 16);
-    *reinterpret_cast<uint2*>(dst) = w;
+    __stcs(reinterpret_cast<uint2*>(dst), w);
   } else {
-    *reinterpret_cast<uint32_t*>(dst) = (uint32_t)codes[0] | ((uint32_t)codes[1] << 16);
+    __stcs(reinterpret_cast<uint32_t*>(dst), (uint32_t)codes[0] | ((uint32_t)codes[1] << 16));
   }
 }
 
-// INT8 codes of N values: fp32(x / s) rounded to nearest even, clamped to [-127, 127].
+// The INT8 code of y -- y rounded to the nearest integer, ties to even, and clamped to
+// [-127, 127] -- in the low byte of the result. Clamping first changes nothing (the bounds are
+// integers); adding 1.5 * 2^23 to a value in [-127, 127] gives a sum in [2^23, 2^24), whose
+// last significand bit has weight 1, so the addition itself rounds to the nearest integer
+// (ties to even: 1.5 * 2^23 is even) and the sum's representation is that of 1.5 * 2^23 plus
+// the integer, two's complement in the low bits.
+__device__ __forceinline__ uint32_t int8_code_bits(float y) {
+  return __float_as_uint(__fadd_rn(fminf(fmaxf(y, -127.f), 127.f), 12582912.f));
+}
+
+// INT8 codes of N values: fp32(x / s) rounded to nearest even, clamped to [-127, 127]
+// (a NaN quotient gives the code 0).
 template <typename TIN, int N>
 __device__ __forceinline__ void quantize_store_int8(const float (&x)[N], const KnownDivisor& d,
                                                     uint8_t* dst) {
   float y[N];
-  divide_vec<TIN, N>(x, d, y);
+  if (divide_vec<TIN, N>(x, d, y)) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) y[k] = y[k] == y[k] ? y[k] : 0.f;
+  }
   uint32_t w[N / 4];
 #pragma unroll
   for (int k = 0; k < N / 4; ++k) {
-    uint32_t acc = 0;
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int c = min(127, max(-127, __float2int_rn(y[4 * k + t])));
-      acc |= ((uint32_t)(c & 0xff)) << (8 * t);
-    }
-    w[k] = acc;
+    // low bytes of four codes into one word: (c0, c1) and (c2, c3), then the two pairs
+    const uint32_t c01 = __byte_perm(int8_code_bits(y[4 * k]), int8_code_bits(y[4 * k + 1]),
+                                     0x0040);
+    const uint32_t c23 = __byte_perm(int8_code_bits(y[4 * k + 2]), int8_code_bits(y[4 * k + 3]),
+                                     0x0040);
+    w[k] = __byte_perm(c01, c23, 0x5410);
   }
   if constexpr (N == 8) {
-    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    __stcs(reinterpret_cast<uint2*>(dst), make_uint2(w[0], w[1]));
   } else {
-    *reinterpret_cast<uint32_t*>(dst) = w[0];
+    __stcs(reinterpret_cast<uint32_t*>(dst), w[0]);
   }
 }
 
@@ -176,14 +196,20 @@ __device__ __forceinline__ void quantize_vec(const uint4& raw, const KnownDiviso
     quantize_store<TIN, VEC>(x, d, dst);
 }
 
+// Tokens a thread of the quantising append has in flight: their K and V loads are all issued
+// before the first store (measured on a 25,032-token prompt batch: 1 and 2 tokens about the
+// same, 4 and 8 slower). Rows are read and codes written with evict-first hints: each byte is
+// touched once here.
+constexpr int kAppendTokens = 2;
+
 // FP8 / INT8 append: each 16-byte vector of fp32/bf16 input is quantised with its head's scale
 // and its codes stored at the token's slot. A thread owns fixed (head, vector) columns of the
 // token rows -- their index arithmetic and scales are set once -- and walks the tokens
-// blockIdx.x, blockIdx.x + gridDim.x, ..., two at a time with both tokens' loads issued before
-// either store.
+// blockIdx.x, blockIdx.x + gridDim.x, ..., kAppendTokens at a time.
 template <typename TIN, bool INT8_CODES>
 __global__ void kv_append_fp8_kernel(const AppendArgs a) {
   constexpr int VEC = Vec16<TIN>::N;
+  constexpr int U = kAppendTokens;
   const int vpr = a.head_dim / VEC;
   const int per_tok = a.h_kv * vpr;
   const int64_t row_elems = (int64_t)a.h_kv * a.head_dim;  // one token's input row
@@ -198,28 +224,29 @@ __global__ void kv_append_fp8_kernel(const AppendArgs a) {
     const KnownDivisor ks = known_divisor(a.k_scales[h]), vs = known_divisor(a.v_scales[h]);
     const int64_t src0 = (int64_t)h * a.head_dim + v * VEC;
     const int64_t dst0 = (int64_t)h * kPageSize * a.head_dim + v * VEC;
-    for (int i = blockIdx.x; i < n; i += 2 * step) {
-      const int i2 = i + step;
-      const bool two = i2 < n;
-      const int64_t s1 = a.slots[i];
-      const int64_t s2 = two ? a.slots[i2] : -1;
-      const uint4 k1 = *reinterpret_cast<const uint4*>(kin + i * row_elems + src0);
-      const uint4 v1 = *reinterpret_cast<const uint4*>(vin + i * row_elems + src0);
-      uint4 k2 = make_uint4(0, 0, 0, 0), v2 = k2;
-      if (two) {
-        k2 = *reinterpret_cast<const uint4*>(kin + i2 * row_elems + src0);
-        v2 = *reinterpret_cast<const uint4*>(vin + i2 * row_elems + src0);
+    for (int i = blockIdx.x; i < n; i += U * step) {
+      int64_t slot[U];
+      uint4 kx[U], vx[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int iu = i + u * step;
+        slot[u] = -1;
+        kx[u] = vx[u] = make_uint4(0, 0, 0, 0);
+        if (iu < n) {
+          slot[u] = a.slots[iu];
+          kx[u] = __ldcs(reinterpret_cast<const uint4*>(kin + iu * row_elems + src0));
+          vx[u] = __ldcs(reinterpret_cast<const uint4*>(vin + iu * row_elems + src0));
+        }
       }
-      if (s1 >= a.num_slots || s2 >= a.num_slots) atomicOr(a.err, PKV_DEVERR_BAD_SLOT);
-      if (s1 >= 0 && s1 < a.num_slots) {
-        const int64_t d = (s1 / kPageSize) * page_elems + (s1 % kPageSize) * a.head_dim + dst0;
-        quantize_vec<TIN, INT8_CODES>(k1, ks, kc + d);
-        quantize_vec<TIN, INT8_CODES>(v1, vs, vc + d);
-      }
-      if (s2 >= 0 && s2 < a.num_slots) {
-        const int64_t d = (s2 / kPageSize) * page_elems + (s2 % kPageSize) * a.head_dim + dst0;
-        quantize_vec<TIN, INT8_CODES>(k2, ks, kc + d);
-        quantize_vec<TIN, INT8_CODES>(v2, vs, vc + d);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t sl = slot[u];
+        if (sl >= a.num_slots) atomicOr(a.err, PKV_DEVERR_BAD_SLOT);
+        if (sl >= 0 && sl < a.num_slots) {
+          const int64_t d = (sl / kPageSize) * page_elems + (sl % kPageSize) * a.head_dim + dst0;
+          quantize_vec<TIN, INT8_CODES>(kx[u], ks, kc + d);
+          quantize_vec<TIN, INT8_CODES>(vx[u], vs, vc + d);
+        }
       }
     }
   }
@@ -263,78 +290,14 @@ __global__ void kv_scale_finalize_kernel(float* scales, int h_kv, float code_max
   scales[h] = (amax == 0.f) ? 1.f : __fdiv_rn(amax, code_max);
 }
 
-// Merge of the chunk partials of one (b, h): M = max_c m_c, w_c = 2^(m_c - M),
-// out = sum_c w_c acc_c / sum_c w_c l_c. A warp merges a run of chunks in chunk order: lane L
-// owns dims DL L .. DL L + DL - 1; the (max, sum) pairs of up to 32 chunks come in at once (lane
-// c reads chunk c's), then the values of CB chunks at a time; the maximum and the weights go
-// round by shuffles. Launched as a programmatic dependent of the decode kernel, whose CTAs allow
+// Merge of the chunk partials of one (b, h) in chunk order (merge_run). Launched as a
+// programmatic dependent of the decode kernel, whose CTAs allow
 // it to be scheduled as they start: its CTAs are placed while the decode's last CTAs run and
 // wait for the decode's results before reading them.
 //  * few chunks (SPLIT false): one warp per (h, b), four per CTA, no block barrier;
 //  * many chunks (SPLIT true, a long context cut into up to hundreds of chunks): one CTA per
 //    (h, b) whose four warps each merge a quarter of the chunks (a run of consecutive chunks),
 //    then warp 0 merges the four results in warp order, so fewer loads wait on one another.
-template <int D, int CB>
-__device__ __forceinline__ void merge_run(const float* ml, const float* acc, int lo, int hi,
-                                          int lane, float& M, float& Lw, float (&A)[D / 32]) {
-  constexpr int DL = D / 32;
-  auto load_batch = [&](int c0, int nc, int cb, float (&v)[CB][DL]) {  // values of CB chunks
-#pragma unroll
-    for (int u = 0; u < CB; ++u) {
-      const int c = c0 + cb + u;
-      if (cb + u < nc) {
-        if constexpr (DL == 4) {
-          const float4 x = *reinterpret_cast<const float4*>(acc + (size_t)c * D);
-          v[u][0] = x.x;
-          v[u][1] = x.y;
-          v[u][2] = x.z;
-          v[u][3] = x.w;
-        } else {
-          const float2 x = *reinterpret_cast<const float2*>(acc + (size_t)c * D);
-          v[u][0] = x.x;
-          v[u][1] = x.y;
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < DL; ++k) v[u][k] = 0.f;
-      }
-    }
-  };
-  for (int c0 = lo; c0 < hi; c0 += 32) {  // 32 chunks per round of (max, sum) pairs
-    const int nc = min(32, hi - c0);
-    const float2 p = lane < nc ? *reinterpret_cast<const float2*>(ml + 2 * (c0 + lane))
-                               : make_float2(-INFINITY, 0.f);
-    // the first CB chunks' values do not depend on the pairs: load them together
-    float v[CB][DL];
-    load_batch(c0, nc, 0, v);
-    float mr = p.x;
-#pragma unroll
-    for (int o = 16; o >= 1; o /= 2) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
-    const float Mn = fmaxf(M, mr);
-    if (Mn == -INFINITY) continue;
-    const float rescale = exp2f(M - Mn);  // 0 on the first round with a finite maximum
-    const float w = p.x == -INFINITY ? 0.f : exp2f(p.x - Mn);
-    float lw = w * p.y;
-#pragma unroll
-    for (int o = 16; o >= 1; o /= 2) lw += __shfl_xor_sync(0xffffffffu, lw, o);
-    Lw = fmaf(Lw, rescale, lw);
-#pragma unroll
-    for (int k = 0; k < DL; ++k) A[k] *= rescale;
-    M = Mn;
-    for (int cb = 0; cb < nc; cb += CB) {
-      if (cb > 0) load_batch(c0, nc, cb, v);  // CB chunks' loads in flight together
-#pragma unroll
-      for (int u = 0; u < CB; ++u) {
-        const float wu = __shfl_sync(0xffffffffu, w, (cb + u) & 31);
-        if (cb + u < nc) {
-#pragma unroll
-          for (int k = 0; k < DL; ++k) A[k] = fmaf(wu, v[u][k], A[k]);
-        }
-      }
-    }
-  }
-}
-
 template <typename TQ, int D, bool SPLIT>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeArgs a) {
   constexpr int DL = D / 32;
@@ -445,11 +408,11 @@ cudaError_t launch_kv_append(const AppendArgs& a, int in_dtype, int cache_dtype,
   const int threads = 256;
   if (cache_dtype == PKV_FP8_E4M3 || cache_dtype == PKV_INT8) {
     const bool i8 = cache_dtype == PKV_INT8;
-    // one wave of blocks, each taking a token pair at a time; threads cover a token row's
-    // (head, vector) columns
+    // one wave of blocks, each taking kAppendTokens tokens at a time; threads cover a token
+    // row's (head, vector) columns
     const int per_tok = a.h_kv * (a.head_dim / (in_dtype == PKV_BF16 ? 8 : 4));
     const int qt = per_tok <= 128 ? 128 : 256;
-    const int64_t pairs = ((int64_t)a.num_tokens + 1) / 2;
+    const int64_t groups = ((int64_t)a.num_tokens + kAppendTokens - 1) / kAppendTokens;
     auto go = [&](auto kern, int slot) {
       static int wave[2] = {0, 0};  // resident blocks on the device, per block size
       if (!wave[slot]) {
@@ -459,7 +422,7 @@ cudaError_t launch_kv_append(const AppendArgs& a, int in_dtype, int cache_dtype,
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         wave[slot] = std::max(1, per_sm) * std::max(1, sms);
       }
-      const int blocks = (int)std::min<int64_t>(pairs, wave[slot]);
+      const int blocks = (int)std::min<int64_t>(groups, wave[slot]);
       kern<<<blocks, qt, 0, s>>>(a);
     };
     const int slot = qt == 128 ? 0 : 1;

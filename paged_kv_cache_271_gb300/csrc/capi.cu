@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -99,6 +100,26 @@ std::atomic<int> g_kernel_choice{0};  // 0 automatic, 1 CUDA cores, 2 tensor cor
 // folds its partials in; 2: overlaps it and leaves the fold to the combine kernel
 std::atomic<int> g_cascade_overlap{2};
 std::atomic<int> g_warp_units{1};     // 1: one warp per request for short single-chunk runs
+// 0: automatic -- the measured faster split for the call's shape when one has been recorded
+// (autotuning), else chunks; 1: chunks only; 2: the balanced split (decode_flat.cu) wherever it
+// applies
+std::atomic<int> g_split_mode{0};
+
+// Autotuning of the split: the first call of a shape (while on, and not during stream capture)
+// times both splits and records the faster. Events for the timing are made when it is turned
+// on, on that device, so that decode calls create nothing.
+constexpr int kTuneReps = 3;
+struct SplitKey {
+  int v[11];
+  bool operator<(const SplitKey& o) const {
+    return std::lexicographical_compare(v, v + 11, o.v, o.v + 11);
+  }
+};
+std::mutex g_tune_mu;
+std::map<SplitKey, bool> g_tuned;  // true: the balanced split measured faster
+std::atomic<int> g_autotune{0};
+int g_tune_dev = -1;
+cudaEvent_t g_tune_ev[2 * kTuneReps][2];
 
 // ---- TMA tensor maps of the pools (for the tensor-core decode) -------------------------------
 
@@ -314,6 +335,65 @@ int pkv_decode_set_warp_per_request(int32_t on) {
   return PKV_OK;
 }
 
+int pkv_decode_set_split(int32_t mode) {
+  if (mode < 0 || mode > 2)
+    return set_error(PKV_EINVAL, "pkv_decode_set_split: %d is not 0, 1 or 2", mode);
+  g_split_mode.store(mode);
+  return PKV_OK;
+}
+
+int pkv_decode_set_autotune(int32_t on) {
+  if (on != 0 && on != 1)
+    return set_error(PKV_EINVAL, "pkv_decode_set_autotune: %d is not 0 or 1", on);
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  if (on) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e, "pkv_decode_set_autotune");
+    if (g_tune_dev != dev) {
+      if (g_tune_dev >= 0) {
+        int cur = dev;
+        cudaSetDevice(g_tune_dev);
+        for (auto& pr : g_tune_ev) {
+          cudaEventDestroy(pr[0]);
+          cudaEventDestroy(pr[1]);
+        }
+        cudaSetDevice(cur);
+        g_tune_dev = -1;
+      }
+      for (auto& pr : g_tune_ev) {
+        e = cudaEventCreate(&pr[0]);
+        if (e == cudaSuccess) e = cudaEventCreate(&pr[1]);
+        if (e != cudaSuccess) return cuda_status(e, "pkv_decode_set_autotune: events");
+      }
+      g_tune_dev = dev;
+    }
+  }
+  g_autotune.store(on);
+  return PKV_OK;
+}
+
+int pkv_decode_autotune_reset(void) {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  g_tuned.clear();
+  return PKV_OK;
+}
+
+int pkv_decode_split_choice(int32_t kv_dtype, int32_t q_dtype, int32_t batch, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t max_pages_per_seq, int32_t window,
+                            int32_t sink_tokens, int32_t fused) {
+  // (the key as decode_impl forms it; slots follow from the other fields and the chunk policy)
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  for (const auto& kv : g_tuned) {
+    const int* v = kv.first.v;
+    if (v[0] == kv_dtype && v[1] == q_dtype && v[2] == batch && v[3] == num_q_heads &&
+        v[4] == num_kv_heads && v[5] == max_pages_per_seq && v[6] == window &&
+        v[7] == (window > 0 ? sink_tokens : 0) && v[8] == (fused ? 1 : 0))
+      return kv.second ? 1 : 0;
+  }
+  return -1;
+}
+
 int pkv_cascade_set_overlap(int32_t on) {
   if (on < 0 || on > 2)
     return set_error(PKV_EINVAL, "pkv_cascade_set_overlap: %d is not 0, 1 or 2", on);
@@ -505,6 +585,28 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
   // leave a CTA's four warps with a page or two each)
   // (one chunk column: no request splits, so no merge of chunk partials can arise)
   a.warp_units = use_mma && a.chunk_grid == 1 && a.chunk_pages <= 16 && g_warp_units.load() != 0;
+  // The balanced split (one wave of CTAs, equal shares of the (request, KV head, page) stream
+  // per warp; decode_flat.cu) for a plain call on the tensor-core kernel that needs split
+  // partials merged by the combine kernel, with the automatic chunk size and mode. Its partials
+  // take the chunked layout's slots: [G][cap][D] values and [G][cap][2] (max, sum) with
+  // cap = batch * h_kv * slots, numbered warp + (request, KV head) < warps + batch * h_kv.
+  const int split_mode = g_split_mode.load();
+  const bool flat_applies = use_mma && !cascade && a.n_chunk_slots > 1 && !a.merge_in_place &&
+                            split_mode != 1 && g_chunk_override.load() == 0 &&
+                            batch <= kFlatMaxBatch;
+  int flat_ctas = 0, flat_cap = 0;  // the balanced split's launch, worked out when it may run
+  auto flat_plan = [&]() {
+    const long long rows = (long long)batch * h_kv;
+    const long long cap = rows * a.n_chunk_slots;
+    const long long max_ctas = std::min<long long>(cap - rows, kFlatMaxWarps) / kFlatWarpsPerCta;
+    int wave = 0;
+    if (cap < (1ll << 31) && max_ctas >= 1 &&
+        decode_flat_wave(a, kv, dtype_q, G, &wave) == cudaSuccess) {
+      flat_ctas = (int)std::min<long long>(max_ctas, wave);
+      flat_cap = (int)cap;
+    }
+    return flat_ctas > 0;
+  };
   a.prefix_dep = cascade && use_mma && g_cascade_overlap.load() != 0 ? 1 : 0;
   a.defer_fold = a.prefix_dep && g_cascade_overlap.load() == 2 ? 1 : 0;
   if (a.defer_fold) a.merge_in_place = 0;  // every member's chunks go to the combine
@@ -535,20 +637,70 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
     st = cuda_status(e, "cascade_prefix launch");
     if (st != PKV_OK) return st;
   }
-  e = traced("paged_decode", s, [&] {
-    if (use_mma) return launch_decode_mma(a, kv, dtype_q, G, &tk, &tv, s);
-    if (kv == PKV_F32) return launch_decode_f32(a, dtype_q, D, G, s);
-    if (kv == PKV_BF16) return launch_decode_bf16(a, dtype_q, D, G, s);
-    if (kv == PKV_INT8) return launch_decode_int8(a, dtype_q, D, G, s);
-    return launch_decode_fp8(a, dtype_q, D, G, s);
-  });
-  st = cuda_status(e, "paged_decode launch");
-  if (st != PKV_OK) return st;
-  if (a.n_chunk_slots > 1 && !a.merge_in_place) {
-    e = traced("decode_combine", s, [&] { return launch_decode_combine(a, dtype_q, D, s); });
-    st = cuda_status(e, "decode_combine launch");
+  // the decode (and its combine) with the chunked (flat = false) or the balanced split
+  auto run = [&](bool flat) {
+    cudaError_t err = traced("paged_decode", s, [&] {
+      if (flat) return launch_decode_flat(a, kv, dtype_q, G, flat_ctas, flat_cap, &tk, &tv, s);
+      if (use_mma) return launch_decode_mma(a, kv, dtype_q, G, &tk, &tv, s);
+      if (kv == PKV_F32) return launch_decode_f32(a, dtype_q, D, G, s);
+      if (kv == PKV_BF16) return launch_decode_bf16(a, dtype_q, D, G, s);
+      if (kv == PKV_INT8) return launch_decode_int8(a, dtype_q, D, G, s);
+      return launch_decode_fp8(a, dtype_q, D, G, s);
+    });
+    int rs = cuda_status(err, "paged_decode launch");
+    if (rs != PKV_OK) return rs;
+    if (flat) {
+      err = traced("decode_combine", s, [&] {
+        return launch_decode_flat_combine(a, kv, dtype_q, G, flat_ctas, flat_cap, s);
+      });
+      rs = cuda_status(err, "decode_combine launch");
+    } else if (a.n_chunk_slots > 1 && !a.merge_in_place) {
+      err = traced("decode_combine", s, [&] { return launch_decode_combine(a, dtype_q, D, s); });
+      rs = cuda_status(err, "decode_combine launch");
+    }
+    return rs;
+  };
+  if (!flat_applies) return run(false);
+  if (split_mode == 2) return run(flat_plan());
+  // automatic: the recorded choice for this shape, else (autotuning, not capturing) measure
+  const SplitKey key{{kv, dtype_q, batch, num_q_heads, h_kv, max_pages_per_seq, window, a.sink,
+                      k_new ? 1 : 0, a.n_chunk_slots, 0}};
+  {
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    auto it = g_tuned.find(key);
+    if (it != g_tuned.end()) return run(it->second && flat_plan());
   }
-  return st;
+  int dev = -1;
+  cudaStreamCaptureStatus cap_st = cudaStreamCaptureStatusNone;
+  if (!g_autotune.load() || cudaGetDevice(&dev) != cudaSuccess || dev != g_tune_dev ||
+      cudaStreamIsCapturing(s, &cap_st) != cudaSuccess || cap_st != cudaStreamCaptureStatusNone ||
+      !flat_plan())
+    return run(false);
+  // both splits, alternately, kTuneReps times each; the faster (least time over its runs)
+  // is recorded and gives this call's result (the appended row is written again each run)
+  float best[2] = {1e30f, 1e30f};
+  {
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    for (int rep = 0; rep < kTuneReps && st == PKV_OK; ++rep)
+      for (int f = 0; f < 2 && st == PKV_OK; ++f) {
+        cudaEvent_t* ev = g_tune_ev[2 * rep + f];
+        cudaEventRecord(ev[0], s);
+        st = run(f == 1);
+        cudaEventRecord(ev[1], s);
+      }
+    if (st != PKV_OK) return st;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_status(e, "decode split autotune");
+    for (int rep = 0; rep < kTuneReps; ++rep)
+      for (int f = 0; f < 2; ++f) {
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, g_tune_ev[2 * rep + f][0], g_tune_ev[2 * rep + f][1]) ==
+            cudaSuccess)
+          best[f] = std::min(best[f], ms);
+      }
+    g_tuned[key] = best[1] < best[0];
+  }
+  return run(best[1] < best[0]);
 }
 
 int pkv_paged_decode_attention(const void* q, int32_t dtype_q, int32_t batch,

@@ -233,6 +233,354 @@ __device__ __forceinline__ void widen4_scores(uint32_t w, uint32_t& lo, uint32_t
   }
 }
 
+// ---- pieces shared by the chunked and the balanced tensor-core decodes ---------------------
+
+// Query fragments (MMA B operand of S^T = K Q^T), k order permuted as described above:
+// lane (gid, tig) holds Q[g = 8 nt + gid][32 kp + 8 tig + 0..7] for every kp (bf16 path) or
+// Q[g][16 (4 h + tig) + 0..15] for h = 0, 1 (FP8 path), read with 16-byte loads.
+// FP8 / INT8 path: the MMAs take f16, whose range (max 65504, normal from 2^-14) is far
+// narrower than bf16's or fp32's. Each query row is therefore multiplied by a power of two
+// 2^e_g that puts its largest |q| in [2^14, 2^15) -- exact, so a bf16 q loses nothing -- and
+// 2^-e_g goes into that head's score factor. An fp32 q is split into two f16 parts
+// hi + lo (lo = the f16 rounding of q - hi), each contracted with K: 22 significant bits.
+template <typename KV, typename TQ, int D, int G>
+struct MmaQuery {
+  static constexpr bool F8 = KV::bytes == 1;
+  static constexpr bool QLO = F8 && sizeof(TQ) == 4;
+  static constexpr int NT = (G + 7) / 8, KP = D / 32;
+  uint32_t qf[NT][KP][4];
+  uint32_t qlo[QLO ? NT : 1][QLO ? KP : 1][4];
+  float sc_h[NT][2];  // score factor of heads 8 nt + 2 tig and 8 nt + 2 tig + 1 (log2 units)
+};
+
+// The query fragments of request b, KV head j.
+template <typename KV, typename TQ, int D, int G>
+__device__ __forceinline__ void mma_load_query(const DecodeArgs& a, int b, int j, int lane,
+                                               MmaQuery<KV, TQ, D, G>& Q) {
+  using QT = MmaQuery<KV, TQ, D, G>;
+  constexpr bool F8 = QT::F8, QLO = QT::QLO;
+  constexpr int NT = QT::NT, KP = QT::KP;
+  const int gid = lane >> 2, tig = lane & 3;
+  auto& qf = Q.qf;
+  auto& qlo = Q.qlo;
+  auto& sc_h = Q.sc_h;
+  const float sc = a.scale_log2 * (F8 ? a.k_scales[j] : 1.f);
+  {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int g = nt * 8 + gid;
+      const bool live = g < G;
+      const TQ* qrow = static_cast<const TQ*>(a.q) + ((size_t)b * a.h_q + j * G + (live ? g : 0)) * D;
+      if constexpr (!F8) {
+#pragma unroll
+        for (int kp = 0; kp < KP; ++kp) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (live) v = *reinterpret_cast<const uint4*>(qrow + 32 * kp + 8 * tig);
+          qf[nt][kp][0] = v.x;
+          qf[nt][kp][1] = v.y;
+          qf[nt][kp][2] = v.z;
+          qf[nt][kp][3] = v.w;
+        }
+        sc_h[nt][0] = sc_h[nt][1] = sc;
+      } else {
+        float x[2][16];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const TQ* src = qrow + 16 * (4 * h + tig);
+#pragma unroll
+          for (int k = 0; k < 16; k += (int)(16 / sizeof(TQ))) {
+            if constexpr (sizeof(TQ) == 4) {
+              float4 f = live ? *reinterpret_cast<const float4*>(src + k) : make_float4(0, 0, 0, 0);
+              x[h][k] = f.x;
+              x[h][k + 1] = f.y;
+              x[h][k + 2] = f.z;
+              x[h][k + 3] = f.w;
+            } else {
+              uint4 u = live ? *reinterpret_cast<const uint4*>(src + k) : make_uint4(0, 0, 0, 0);
+              const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                x[h][k + 2 * t] = bf16lo(w[t]);
+                x[h][k + 2 * t + 1] = bf16hi(w[t]);
+              }
+            }
+          }
+        }
+        // largest |q| of head g: this lane's 32 values, then the 4 lanes (tig) sharing g
+        float mx = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int k = 0; k < 16; ++k) mx = fmaxf(mx, fabsf(x[h][k]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const int ex = (__float_as_int(mx) >> 23) & 0xff;  // biased exponent of the maximum
+        // mx * 2^e in [2^14, 2^15) for a normal mx: e = 14 - (ex - 127); none for 0, inf, NaN
+        const int e = (mx > 0.f && ex < 255) ? min(126, max(-126, 141 - ex)) : 0;
+        const float up = __int_as_float((127 + e) << 23);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int k = 0; k < 16; ++k) x[h][k] *= up;
+        // chunk 4h+tig of a K row holds k-steps 4h .. 4h+3, four values each
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const int kp = 2 * h + (ks >> 1), half = ks & 1;
+            const float* v = &x[h][4 * ks];
+            qf[nt][kp][2 * half] = pack_f16(v[0], v[1]);
+            qf[nt][kp][2 * half + 1] = pack_f16(v[2], v[3]);
+            if constexpr (QLO) {
+              const __half2 h01 = *reinterpret_cast<const __half2*>(&qf[nt][kp][2 * half]);
+              const __half2 h23 = *reinterpret_cast<const __half2*>(&qf[nt][kp][2 * half + 1]);
+              qlo[nt][kp][2 * half] = pack_f16(v[0] - __low2float(h01), v[1] - __high2float(h01));
+              qlo[nt][kp][2 * half + 1] =
+                  pack_f16(v[2] - __low2float(h23), v[3] - __high2float(h23));
+            }
+          }
+        // this lane's scores belong to heads 8 nt + 2 tig (+1): their exponents come from the
+        // lanes holding those query rows (gid = 2 tig, 2 tig + 1)
+        const int e0 = __shfl_sync(0xffffffffu, e, (2 * tig) * 4);
+        const int e1 = __shfl_sync(0xffffffffu, e, (2 * tig + 1) * 4);
+        sc_h[nt][0] = sc * __int_as_float((127 - e0) << 23);
+        sc_h[nt][1] = sc * __int_as_float((127 - e1) << 23);
+      }
+    }
+  }
+}
+
+// A warp's running softmax state over the pages it has read: per head the maximum and sum
+// (log2 domain) and the weighted values, in MMA accumulator fragments.
+template <int D, int G>
+struct MmaRun {
+  static constexpr int NT = (G + 7) / 8, MT = D / 16;
+  float m_run[NT][2], l_run[NT][2];
+  float acc[MT][NT][4];
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m_run[nt][0] = m_run[nt][1] = -INFINITY;
+      l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+      for (int mi = 0; mi < MT; ++mi)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[mi][nt][e] = 0.f;
+    }
+  }
+};
+
+// One staged (page, KV head) tile -- K at kt, V at vt (shared-memory addresses), logical page lp
+// of a request of ctx tokens, nvalid rows before the context end -- folded into the warp's
+// running state: scores, online softmax, weighted values.
+template <typename KV, typename TQ, int D, int G>
+__device__ __forceinline__ void mma_attend_page(uint32_t kt, uint32_t vt, int lp, int nvalid,
+                                                int ctx, int sink, int window,
+                                                const MmaQuery<KV, TQ, D, G>& Q,
+                                                MmaRun<D, G>& R, uint16_t* pt, uint32_t pt_u32,
+                                                int lane) {
+  using QT = MmaQuery<KV, TQ, D, G>;
+  constexpr bool F8 = QT::F8, QLO = QT::QLO;
+  constexpr int NT = QT::NT, KP = QT::KP, MT = D / 16;
+  const int gid = lane >> 2, tig = lane & 3;
+  const auto& qf = Q.qf;
+  const auto& qlo = Q.qlo;
+  const auto& sc_h = Q.sc_h;
+  auto& m_run = R.m_run;
+  auto& l_run = R.l_run;
+  auto& acc = R.acc;
+  // ---- scores S^T[16 tokens][8 heads per n-tile] ----
+  float s[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+  if constexpr (!F8) {
+#pragma unroll
+    for (int kp = 0; kp < KP; ++kp) {
+      const uint4 r0 = lds128(kt + swz(gid, 4 * kp + tig));
+      const uint4 r8 = lds128(kt + swz(gid + 8, 4 * kp + tig));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mma16816<false>(s[nt], r0.x, r8.x, r0.y, r8.y, qf[nt][kp][0], qf[nt][kp][1]);
+        mma16816<false>(s[nt], r0.z, r8.z, r0.w, r8.w, qf[nt][kp][2], qf[nt][kp][3]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {  // 16-byte chunk 4h+tig of a row = 4 k-steps x 4 codes
+      const uint4 r0 = lds128(kt + swz(gid, 4 * h + tig));
+      const uint4 r8 = lds128(kt + swz(gid + 8, 4 * h + tig));
+      const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w};
+      const uint32_t w8[4] = {r8.x, r8.y, r8.z, r8.w};
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        widen4_scores<KV>(w0[ks], a0, a2);
+        widen4_scores<KV>(w8[ks], a1, a3);
+        const int kp = 2 * h + (ks >> 1), half = ks & 1;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma16816<true>(s[nt], a0, a1, a2, a3, qf[nt][kp][2 * half],
+                         qf[nt][kp][2 * half + 1]);
+          if constexpr (QLO)
+            mma16816<true>(s[nt], a0, a1, a2, a3, qlo[nt][kp][2 * half],
+                           qlo[nt][kp][2 * half + 1]);
+        }
+      }
+    }
+  }
+
+  // ---- online softmax: lane holds tokens gid, gid+8 of heads 8nt+2tig, 8nt+2tig+1 ----
+  const bool v0 = attended(lp * kPageSize + gid, ctx, sink, window);
+  const bool v8 = attended(lp * kPageSize + gid + 8, ctx, sink, window);
+  float alpha[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    s[nt][0] = v0 ? s[nt][0] * sc_h[nt][0] : -INFINITY;
+    s[nt][1] = v0 ? s[nt][1] * sc_h[nt][1] : -INFINITY;
+    s[nt][2] = v8 ? s[nt][2] * sc_h[nt][0] : -INFINITY;
+    s[nt][3] = v8 ? s[nt][3] * sc_h[nt][1] : -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      float mx = fmaxf(s[nt][k], s[nt][k + 2]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float m_new = fmaxf(m_run[nt][k], mx);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      alpha[nt][k] = exp2f(m_run[nt][k] - m_use);
+      s[nt][k] = exp2f(s[nt][k] - m_use);
+      s[nt][k + 2] = exp2f(s[nt][k + 2] - m_use);
+      l_run[nt][k] = l_run[nt][k] * alpha[nt][k] + s[nt][k] + s[nt][k + 2];
+      m_run[nt][k] = m_new;
+    }
+    // P^T into the warp buffer: pt[g][t], g = 8nt + 2tig (+1), t = gid (+8)
+    uint16_t* row0 = pt + (nt * 8 + 2 * tig) * kPageSize;
+    uint16_t* row1 = row0 + kPageSize;
+    if constexpr (F8) {
+      const __half h0 = __float2half_rn(s[nt][0]), h1 = __float2half_rn(s[nt][1]);
+      const __half h2 = __float2half_rn(s[nt][2]), h3 = __float2half_rn(s[nt][3]);
+      row0[gid] = __half_as_ushort(h0);
+      row1[gid] = __half_as_ushort(h1);
+      row0[gid + 8] = __half_as_ushort(h2);
+      row1[gid + 8] = __half_as_ushort(h3);
+    } else {
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(s[nt][0]);
+      const __nv_bfloat16 h1 = __float2bfloat16_rn(s[nt][1]);
+      const __nv_bfloat16 h2 = __float2bfloat16_rn(s[nt][2]);
+      const __nv_bfloat16 h3 = __float2bfloat16_rn(s[nt][3]);
+      row0[gid] = __bfloat16_as_ushort(h0);
+      row1[gid] = __bfloat16_as_ushort(h1);
+      row0[gid + 8] = __bfloat16_as_ushort(h2);
+      row1[gid + 8] = __bfloat16_as_ushort(h3);
+    }
+#pragma unroll
+    for (int mi = 0; mi < MT; ++mi) {
+      acc[mi][nt][0] *= alpha[nt][0];
+      acc[mi][nt][1] *= alpha[nt][1];
+      acc[mi][nt][2] *= alpha[nt][0];
+      acc[mi][nt][3] *= alpha[nt][1];
+    }
+  }
+
+  // ---- O^T[dims][heads] += V^T P^T ----
+  if constexpr (!F8) {
+    if (nvalid < kPageSize) {
+      // zero the stale rows of the last page (16 chunks of 16 bytes per row)
+      for (int e = lane; e < (kPageSize - nvalid) * 16; e += 32) {
+        const int r = nvalid + (e >> 4), ch = e & 15;
+        sts128(vt + swz(r, ch), make_uint4(0, 0, 0, 0));
+      }
+    }
+  }
+  __syncwarp();
+  uint32_t pb[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const uint32_t rowg = pt_u32 + (nt * 8 + gid) * kPageSize * 2;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(pb[nt][0]) : "r"(rowg + 4 * tig));
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(pb[nt][1]) : "r"(rowg + 16 + 4 * tig));
+  }
+  if constexpr (!F8) {
+    // V^T fragments straight from the swizzled bf16 tile: m-tile mi covers dims 16 mi ..
+    const int q = lane >> 3, rr = lane & 7;
+    const int t = (q >> 1) * 8 + rr;
+#pragma unroll
+    for (int mi = 0; mi < MT; ++mi) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_trans(vt + swz(t, 2 * mi + (q & 1)), a0, a1, a2, a3);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        mma16816<false>(acc[mi][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+    }
+  } else {
+    // V^T fragments built in registers from the FP8 tile. The lane reads 16 codes (dims
+    // 16 gid .. 16 gid + 15) of tokens 2tig, 2tig+1, 2tig+8, 2tig+9; byte permutes pair
+    // each dim's codes of consecutive tokens, which widen exactly to f16. Row gid of m-tile
+    // mi is dim 16 gid + 2 mi and row gid + 8 is dim 16 gid + 2 mi + 1 (undone in the merge).
+    uint4 vr[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int r = 2 * tig + (k & 1) + 8 * (k >> 1);
+      vr[k] = lds128(vt + swz(r, gid));
+      if (r >= nvalid) vr[k] = make_uint4(0, 0, 0, 0);  // stale rows of the last page
+    }
+#pragma unroll
+    for (int mi = 0; mi < MT; ++mi) {
+      const int wi = mi >> 1;
+      const uint32_t sel = (mi & 1) ? 0x7362u : 0x5140u;
+      const uint32_t w0 = wi == 0 ? vr[0].x : wi == 1 ? vr[0].y : wi == 2 ? vr[0].z : vr[0].w;
+      const uint32_t w1 = wi == 0 ? vr[1].x : wi == 1 ? vr[1].y : wi == 2 ? vr[1].z : vr[1].w;
+      const uint32_t w2 = wi == 0 ? vr[2].x : wi == 1 ? vr[2].y : wi == 2 ? vr[2].z : vr[2].w;
+      const uint32_t w3 = wi == 0 ? vr[3].x : wi == 1 ? vr[3].y : wi == 2 ? vr[3].z : vr[3].w;
+      const uint32_t lo = __byte_perm(w0, w1, sel);  // tokens 2tig, 2tig+1
+      const uint32_t hi = __byte_perm(w2, w3, sel);  // tokens 2tig+8, 2tig+9
+      uint32_t a0, a1, a2, a3;
+      widen4<KV>(lo, a0, a1);
+      widen4<KV>(hi, a2, a3);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        mma16816<true>(acc[mi][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+    }
+  }
+}
+
+// A warp's state into its merge area: [G][D] weighted values, [G] maxima, [G] sums.
+template <typename KV, int D, int G>
+__device__ __forceinline__ void mma_run_to_smem(const MmaRun<D, G>& R, float* red_acc,
+                                                float* red_m, float* red_l, int lane) {
+  constexpr bool F8 = KV::bytes == 1;
+  constexpr int NT = MmaRun<D, G>::NT, MT = MmaRun<D, G>::MT;
+  const int gid = lane >> 2, tig = lane & 3;
+  const auto& m_run = R.m_run;
+  const auto& l_run = R.l_run;
+  const auto& acc = R.acc;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      float l = l_run[nt][k];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      const int g = nt * 8 + 2 * tig + k;
+      if (gid == 0 && g < G) {
+        red_m[g] = m_run[nt][k];
+        red_l[g] = l;
+      }
+#pragma unroll
+      for (int mi = 0; mi < MT; ++mi) {
+        if (g < G) {
+          // dims of rows gid and gid+8 of m-tile mi (see the two V^T fragment layouts)
+          const int i0 = F8 ? 16 * gid + 2 * mi : 16 * mi + gid;
+          const int i1 = F8 ? i0 + 1 : i0 + 8;
+          red_acc[g * D + i0] = acc[mi][nt][k];
+          red_acc[g * D + i1] = acc[mi][nt][k + 2];
+        }
+      }
+    }
+  }
+}
+
 // WU (warp per request): every request has a single chunk; warp w of CTA z takes request
 // NW z + w whole (its pages 0, 1, 2, ... through its own two ring stages) and writes its output
 // itself; the warps of a CTA only share the barrier set-up.
@@ -242,9 +590,8 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
     const __grid_constant__ CUtensorMap tm_v) {
   using S = MmaShape<KV, D, G, WU>;
   constexpr bool F8 = S::kFp8;
-  constexpr int NW = S::kWarps, SPW = S::SPW, NT = S::NT, KP = S::KP, MT = S::MT;
+  constexpr int NW = S::kWarps, SPW = S::SPW, NT = S::NT;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gid = lane >> 2, tig = lane & 3;
   const int c = blockIdx.x, j = blockIdx.y;
   const bool warp_live = !WU || (int)blockIdx.z * NW + warp < a.batch;
   const int b = WU ? (warp_live ? (int)blockIdx.z * NW + warp : 0) : (int)blockIdx.z;
@@ -345,114 +692,11 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
     }
   }
 
-  // Query fragments (MMA B operand of S^T = K Q^T), k order permuted as described above:
-  // lane (gid, tig) holds Q[g = 8 nt + gid][32 kp + 8 tig + 0..7] for every kp (bf16 path) or
-  // Q[g][16 (4 h + tig) + 0..15] for h = 0, 1 (FP8 path), read with 16-byte loads.
-  // FP8 / INT8 path: the MMAs take f16, whose range (max 65504, normal from 2^-14) is far
-  // narrower than bf16's or fp32's. Each query row is therefore multiplied by a power of two
-  // 2^e_g that puts its largest |q| in [2^14, 2^15) -- exact, so a bf16 q loses nothing -- and
-  // 2^-e_g goes into that head's score factor. An fp32 q is split into two f16 parts
-  // hi + lo (lo = the f16 rounding of q - hi), each contracted with K: 22 significant bits.
-  constexpr bool QLO = F8 && sizeof(TQ) == 4;
-  uint32_t qf[NT][KP][4];
-  uint32_t qlo[QLO ? NT : 1][QLO ? KP : 1][4];
-  float sc_h[NT][2];  // score factor of heads 8 nt + 2 tig and 8 nt + 2 tig + 1 (log2 units)
-  const float sc = a.scale_log2 * (F8 ? a.k_scales[j] : 1.f);
-  {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int g = nt * 8 + gid;
-      const bool live = g < G;
-      const TQ* qrow = static_cast<const TQ*>(a.q) + ((size_t)b * a.h_q + j * G + (live ? g : 0)) * D;
-      if constexpr (!F8) {
-#pragma unroll
-        for (int kp = 0; kp < KP; ++kp) {
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (live) v = *reinterpret_cast<const uint4*>(qrow + 32 * kp + 8 * tig);
-          qf[nt][kp][0] = v.x;
-          qf[nt][kp][1] = v.y;
-          qf[nt][kp][2] = v.z;
-          qf[nt][kp][3] = v.w;
-        }
-        sc_h[nt][0] = sc_h[nt][1] = sc;
-      } else {
-        float x[2][16];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const TQ* src = qrow + 16 * (4 * h + tig);
-#pragma unroll
-          for (int k = 0; k < 16; k += (int)(16 / sizeof(TQ))) {
-            if constexpr (sizeof(TQ) == 4) {
-              float4 f = live ? *reinterpret_cast<const float4*>(src + k) : make_float4(0, 0, 0, 0);
-              x[h][k] = f.x;
-              x[h][k + 1] = f.y;
-              x[h][k + 2] = f.z;
-              x[h][k + 3] = f.w;
-            } else {
-              uint4 u = live ? *reinterpret_cast<const uint4*>(src + k) : make_uint4(0, 0, 0, 0);
-              const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                x[h][k + 2 * t] = bf16lo(w[t]);
-                x[h][k + 2 * t + 1] = bf16hi(w[t]);
-              }
-            }
-          }
-        }
-        // largest |q| of head g: this lane's 32 values, then the 4 lanes (tig) sharing g
-        float mx = 0.f;
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int k = 0; k < 16; ++k) mx = fmaxf(mx, fabsf(x[h][k]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const int ex = (__float_as_int(mx) >> 23) & 0xff;  // biased exponent of the maximum
-        // mx * 2^e in [2^14, 2^15) for a normal mx: e = 14 - (ex - 127); none for 0, inf, NaN
-        const int e = (mx > 0.f && ex < 255) ? min(126, max(-126, 141 - ex)) : 0;
-        const float up = __int_as_float((127 + e) << 23);
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int k = 0; k < 16; ++k) x[h][k] *= up;
-        // chunk 4h+tig of a K row holds k-steps 4h .. 4h+3, four values each
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const int kp = 2 * h + (ks >> 1), half = ks & 1;
-            const float* v = &x[h][4 * ks];
-            qf[nt][kp][2 * half] = pack_f16(v[0], v[1]);
-            qf[nt][kp][2 * half + 1] = pack_f16(v[2], v[3]);
-            if constexpr (QLO) {
-              const __half2 h01 = *reinterpret_cast<const __half2*>(&qf[nt][kp][2 * half]);
-              const __half2 h23 = *reinterpret_cast<const __half2*>(&qf[nt][kp][2 * half + 1]);
-              qlo[nt][kp][2 * half] = pack_f16(v[0] - __low2float(h01), v[1] - __high2float(h01));
-              qlo[nt][kp][2 * half + 1] =
-                  pack_f16(v[2] - __low2float(h23), v[3] - __high2float(h23));
-            }
-          }
-        // this lane's scores belong to heads 8 nt + 2 tig (+1): their exponents come from the
-        // lanes holding those query rows (gid = 2 tig, 2 tig + 1)
-        const int e0 = __shfl_sync(0xffffffffu, e, (2 * tig) * 4);
-        const int e1 = __shfl_sync(0xffffffffu, e, (2 * tig + 1) * 4);
-        sc_h[nt][0] = sc * __int_as_float((127 - e0) << 23);
-        sc_h[nt][1] = sc * __int_as_float((127 - e1) << 23);
-      }
-    }
-  }
+  MmaQuery<KV, TQ, D, G> Q;
+  mma_load_query<KV, TQ, D, G>(a, b, j, lane, Q);
 
-  float m_run[NT][2], l_run[NT][2];
-  float acc[MT][NT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    m_run[nt][0] = m_run[nt][1] = -INFINITY;
-    l_run[nt][0] = l_run[nt][1] = 0.f;
-#pragma unroll
-    for (int mi = 0; mi < MT; ++mi)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[mi][nt][e] = 0.f;
-  }
+  MmaRun<D, G> R;
+  R.reset();
   const uint32_t pt_u32 = smem_u32(pt);
 
   int m = 0;
@@ -477,159 +721,8 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
         __syncwarp();
       }
 
-      // ---- scores S^T[16 tokens][8 heads per n-tile] ----
-      float s[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-      if constexpr (!F8) {
-#pragma unroll
-        for (int kp = 0; kp < KP; ++kp) {
-          const uint4 r0 = lds128(kt + swz(gid, 4 * kp + tig));
-          const uint4 r8 = lds128(kt + swz(gid + 8, 4 * kp + tig));
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mma16816<false>(s[nt], r0.x, r8.x, r0.y, r8.y, qf[nt][kp][0], qf[nt][kp][1]);
-            mma16816<false>(s[nt], r0.z, r8.z, r0.w, r8.w, qf[nt][kp][2], qf[nt][kp][3]);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {  // 16-byte chunk 4h+tig of a row = 4 k-steps x 4 codes
-          const uint4 r0 = lds128(kt + swz(gid, 4 * h + tig));
-          const uint4 r8 = lds128(kt + swz(gid + 8, 4 * h + tig));
-          const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w};
-          const uint32_t w8[4] = {r8.x, r8.y, r8.z, r8.w};
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            uint32_t a0, a1, a2, a3;
-            widen4_scores<KV>(w0[ks], a0, a2);
-            widen4_scores<KV>(w8[ks], a1, a3);
-            const int kp = 2 * h + (ks >> 1), half = ks & 1;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              mma16816<true>(s[nt], a0, a1, a2, a3, qf[nt][kp][2 * half],
-                             qf[nt][kp][2 * half + 1]);
-              if constexpr (QLO)
-                mma16816<true>(s[nt], a0, a1, a2, a3, qlo[nt][kp][2 * half],
-                               qlo[nt][kp][2 * half + 1]);
-            }
-          }
-        }
-      }
-
-      // ---- online softmax: lane holds tokens gid, gid+8 of heads 8nt+2tig, 8nt+2tig+1 ----
-      const bool v0 = attended(lp * kPageSize + gid, ctx, a.sink, a.window);
-      const bool v8 = attended(lp * kPageSize + gid + 8, ctx, a.sink, a.window);
-      float alpha[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        s[nt][0] = v0 ? s[nt][0] * sc_h[nt][0] : -INFINITY;
-        s[nt][1] = v0 ? s[nt][1] * sc_h[nt][1] : -INFINITY;
-        s[nt][2] = v8 ? s[nt][2] * sc_h[nt][0] : -INFINITY;
-        s[nt][3] = v8 ? s[nt][3] * sc_h[nt][1] : -INFINITY;
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          float mx = fmaxf(s[nt][k], s[nt][k + 2]);
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float m_new = fmaxf(m_run[nt][k], mx);
-          const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-          alpha[nt][k] = exp2f(m_run[nt][k] - m_use);
-          s[nt][k] = exp2f(s[nt][k] - m_use);
-          s[nt][k + 2] = exp2f(s[nt][k + 2] - m_use);
-          l_run[nt][k] = l_run[nt][k] * alpha[nt][k] + s[nt][k] + s[nt][k + 2];
-          m_run[nt][k] = m_new;
-        }
-        // P^T into the warp buffer: pt[g][t], g = 8nt + 2tig (+1), t = gid (+8)
-        uint16_t* row0 = pt + (nt * 8 + 2 * tig) * kPageSize;
-        uint16_t* row1 = row0 + kPageSize;
-        if constexpr (F8) {
-          const __half h0 = __float2half_rn(s[nt][0]), h1 = __float2half_rn(s[nt][1]);
-          const __half h2 = __float2half_rn(s[nt][2]), h3 = __float2half_rn(s[nt][3]);
-          row0[gid] = __half_as_ushort(h0);
-          row1[gid] = __half_as_ushort(h1);
-          row0[gid + 8] = __half_as_ushort(h2);
-          row1[gid + 8] = __half_as_ushort(h3);
-        } else {
-          const __nv_bfloat16 h0 = __float2bfloat16_rn(s[nt][0]);
-          const __nv_bfloat16 h1 = __float2bfloat16_rn(s[nt][1]);
-          const __nv_bfloat16 h2 = __float2bfloat16_rn(s[nt][2]);
-          const __nv_bfloat16 h3 = __float2bfloat16_rn(s[nt][3]);
-          row0[gid] = __bfloat16_as_ushort(h0);
-          row1[gid] = __bfloat16_as_ushort(h1);
-          row0[gid + 8] = __bfloat16_as_ushort(h2);
-          row1[gid + 8] = __bfloat16_as_ushort(h3);
-        }
-#pragma unroll
-        for (int mi = 0; mi < MT; ++mi) {
-          acc[mi][nt][0] *= alpha[nt][0];
-          acc[mi][nt][1] *= alpha[nt][1];
-          acc[mi][nt][2] *= alpha[nt][0];
-          acc[mi][nt][3] *= alpha[nt][1];
-        }
-      }
-
-      // ---- O^T[dims][heads] += V^T P^T ----
-      if constexpr (!F8) {
-        if (nvalid < kPageSize) {
-          // zero the stale rows of the last page (16 chunks of 16 bytes per row)
-          for (int e = lane; e < (kPageSize - nvalid) * 16; e += 32) {
-            const int r = nvalid + (e >> 4), ch = e & 15;
-            sts128(vt + swz(r, ch), make_uint4(0, 0, 0, 0));
-          }
-        }
-      }
-      __syncwarp();
-      uint32_t pb[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const uint32_t rowg = pt_u32 + (nt * 8 + gid) * kPageSize * 2;
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(pb[nt][0]) : "r"(rowg + 4 * tig));
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(pb[nt][1]) : "r"(rowg + 16 + 4 * tig));
-      }
-      if constexpr (!F8) {
-        // V^T fragments straight from the swizzled bf16 tile: m-tile mi covers dims 16 mi ..
-        const int q = lane >> 3, rr = lane & 7;
-        const int t = (q >> 1) * 8 + rr;
-#pragma unroll
-        for (int mi = 0; mi < MT; ++mi) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_trans(vt + swz(t, 2 * mi + (q & 1)), a0, a1, a2, a3);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            mma16816<false>(acc[mi][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
-        }
-      } else {
-        // V^T fragments built in registers from the FP8 tile. The lane reads 16 codes (dims
-        // 16 gid .. 16 gid + 15) of tokens 2tig, 2tig+1, 2tig+8, 2tig+9; byte permutes pair
-        // each dim's codes of consecutive tokens, which widen exactly to f16. Row gid of m-tile
-        // mi is dim 16 gid + 2 mi and row gid + 8 is dim 16 gid + 2 mi + 1 (undone in the merge).
-        uint4 vr[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int r = 2 * tig + (k & 1) + 8 * (k >> 1);
-          vr[k] = lds128(vt + swz(r, gid));
-          if (r >= nvalid) vr[k] = make_uint4(0, 0, 0, 0);  // stale rows of the last page
-        }
-#pragma unroll
-        for (int mi = 0; mi < MT; ++mi) {
-          const int wi = mi >> 1;
-          const uint32_t sel = (mi & 1) ? 0x7362u : 0x5140u;
-          const uint32_t w0 = wi == 0 ? vr[0].x : wi == 1 ? vr[0].y : wi == 2 ? vr[0].z : vr[0].w;
-          const uint32_t w1 = wi == 0 ? vr[1].x : wi == 1 ? vr[1].y : wi == 2 ? vr[1].z : vr[1].w;
-          const uint32_t w2 = wi == 0 ? vr[2].x : wi == 1 ? vr[2].y : wi == 2 ? vr[2].z : vr[2].w;
-          const uint32_t w3 = wi == 0 ? vr[3].x : wi == 1 ? vr[3].y : wi == 2 ? vr[3].z : vr[3].w;
-          const uint32_t lo = __byte_perm(w0, w1, sel);  // tokens 2tig, 2tig+1
-          const uint32_t hi = __byte_perm(w2, w3, sel);  // tokens 2tig+8, 2tig+9
-          uint32_t a0, a1, a2, a3;
-          widen4<KV>(lo, a0, a1);
-          widen4<KV>(hi, a2, a3);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            mma16816<true>(acc[mi][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
-        }
-      }
+      mma_attend_page<KV, TQ, D, G>(kt, vt, lp, nvalid, ctx, a.sink, a.window, Q, R, pt, pt_u32,
+                                    lane);
     }
     __syncwarp();
     if (m + SPW < n_mine) {  // warp-uniform
@@ -655,31 +748,7 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS) paged_decode_mma_kernel(
   float* red_acc = reinterpret_cast<float*>(ring + (WU ? S::RING_BYTES : 0));
   float* red_m = red_acc + NW * G * D;
   float* red_l = red_m + NW * G;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      float l = l_run[nt][k];
-      l += __shfl_xor_sync(0xffffffffu, l, 4);
-      l += __shfl_xor_sync(0xffffffffu, l, 8);
-      l += __shfl_xor_sync(0xffffffffu, l, 16);
-      const int g = nt * 8 + 2 * tig + k;
-      if (gid == 0 && g < G) {
-        red_m[warp * G + g] = m_run[nt][k];
-        red_l[warp * G + g] = l;
-      }
-#pragma unroll
-      for (int mi = 0; mi < MT; ++mi) {
-        if (g < G) {
-          // dims of rows gid and gid+8 of m-tile mi (see the two V^T fragment layouts)
-          const int i0 = F8 ? 16 * gid + 2 * mi : 16 * mi + gid;
-          const int i1 = F8 ? i0 + 1 : i0 + 8;
-          red_acc[(warp * G + g) * D + i0] = acc[mi][nt][k];
-          red_acc[(warp * G + g) * D + i1] = acc[mi][nt][k + 2];
-        }
-      }
-    }
-  }
+  mma_run_to_smem<KV, D, G>(R, red_acc + warp * G * D, red_m + warp * G, red_l + warp * G, lane);
   const float vs = F8 ? a.v_scales[j] : 1.f;
   // a dependent launch of the prefix kernel: its partials are complete and visible past here
   if (a.prefix_dep && !a.defer_fold) asm volatile("griddepcontrol.wait;" ::: "memory");

@@ -104,6 +104,19 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, int kv_dtype, int q_dtype, in
                               const void* tk, const void* tv, cudaStream_t s);
 cudaError_t launch_decode_combine(const DecodeArgs& a, int q_dtype, int head_dim,
                                   cudaStream_t s);
+// Balanced split of the tensor-core decode (decode_flat.cu): the CTAs of kFlatWarpsPerCta warps
+// resident at once for this call (one wave); the decode on `ctas` CTAs with `cap` partial slots
+// per query head; its combine, launched with the same `ctas` and `cap`.
+constexpr int kFlatWarpsPerCta = 4;
+constexpr int kFlatMaxWarps = 1 << 20;  // bounds the warp count (and partial ids) far from int
+constexpr int kFlatMaxBatch = 2048;     // per-request page offsets held in shared memory
+cudaError_t decode_flat_wave(const DecodeArgs& a, int kv_dtype, int q_dtype, int group,
+                             int* ctas);
+cudaError_t launch_decode_flat(const DecodeArgs& a, int kv_dtype, int q_dtype, int group,
+                               int ctas, int cap, const void* tk, const void* tv,
+                               cudaStream_t s);
+cudaError_t launch_decode_flat_combine(const DecodeArgs& a, int kv_dtype, int q_dtype, int group,
+                                       int ctas, int cap, cudaStream_t s);
 cudaError_t launch_kv_append(const AppendArgs& a, int in_dtype, int cache_dtype, cudaStream_t s);
 // cudaMemcpyAsync on stream s, traced under `name` when launch tracing is on (capi.cu).
 cudaError_t traced_copy(const char* name, void* dst, const void* src, size_t bytes,

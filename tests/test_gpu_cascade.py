@@ -300,3 +300,32 @@ def test_cascade_members_with_several_own_chunks(own_chunk, prefix_kernel):
     assert torch.equal(outs[0], outs[1])
     err = np.abs(outs[0].float().cpu().numpy() - oracle_groups_expected(w)).max()
     assert err < TOL, err
+
+
+@pytest.mark.parametrize("chunk", [0, 3], ids=["default_chunks", "chunks_of_3"])
+def test_cascade_without_page_ids_reads_the_first_members_row(chunk, prefix_kernel):
+    # groups given without their shared page ids: the prefix kernel reads the ids from the
+    # first member's table row instead; the same pages, so the same bits as with the ids
+    w = _case(4, h_kv=2, seed=17, groups=((70, 17, 1, 90), (5, 3, 1, 40)),
+              singles=((1, 60),) * 2)
+    sc = GroupScenario(w)
+    sc.append()
+    g = pkv.cascade_groups(sc.bt_host, sc.cl_host)
+    assert g.prefix_page_ids is not None
+    with_ids = g.to(sc.q.device)
+    bare = pkv.CascadeGroups(g.group_of, g.prefix_pages, g.group_offsets, g.group_members,
+                             g.max_members, g.max_prefix_pages, g.max_own_pages,
+                             g.own_start).to(sc.q.device)
+    assert bare.prefix_page_ids is None and bare.desc().prefix_page_ids is None
+    pkv.cascade_set_prefix_chunk_pages(chunk)
+    pkv.device_error()
+    try:
+        a = _cascade(sc, with_ids).clone()
+        b = _cascade(sc, bare).clone()
+        torch.cuda.synchronize()
+    finally:
+        pkv.cascade_set_prefix_chunk_pages(0)
+    _check_no_error()
+    assert torch.equal(a, b)
+    err = np.abs(b.float().cpu().numpy() - oracle_groups_expected(w)).max()
+    assert err < TOL, err
