@@ -442,14 +442,14 @@ def source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
+def recorded_traffic(split):
     """dram bytes per launch of the decode kernel from the committed ncu summary, if it was
-    taken on the current kernel sources; else None."""
+    taken on the current kernel sources and on the split this run used; else None."""
     path = os.path.join(ROOT, "profiles", "paged_decode_llama3_8b_b64.traffic.txt")
     try:
         with open(path) as f:
             rec = dict(tok.split("=", 1) for tok in f.read().split())
-        if rec.get("source_sha") == source_sha():
+        if rec.get("source_sha") == source_sha() and split.startswith(rec.get("split", "?")):
             return float(rec["dram_bytes_per_launch"])
     except (OSError, ValueError, KeyError):
         pass
@@ -585,10 +585,12 @@ def run_ours(args):
     if work[top][0] == "hbm":
         kernel_bytes = work[top][1]
         achieved = kernel_bytes / (top_ms * 1e-3) / 1e9
-        traffic = recorded_traffic() if args.workload == "llama3_8b_b64" else None
+        traffic = (recorded_traffic(sc.config.get("split", ""))
+                   if args.workload == "llama3_8b_b64" else None)
         roofline = {"bound": "hbm",
-                    "kernel": "paged_decode kernel (%s cache, d=%d, G=%d, append fused)"
-                              % (sc.config["kv_dtype"], sc.d, sc.h_q // sc.h_kv),
+                    "kernel": "paged_decode kernel (%s cache, d=%d, G=%d, append fused; "
+                              "split: %s)" % (sc.config["kv_dtype"], sc.d, sc.h_q // sc.h_kv,
+                                              sc.config.get("split", "chunks")),
                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                     "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
                     "frac_of_nominal_8TBs": round(achieved / NOMINAL_HBM_GBS, 4),

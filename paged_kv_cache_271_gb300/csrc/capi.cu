@@ -234,9 +234,34 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Workspace: acc [batch][h_q][slots][d] and (max, sum) [batch][h_q][slots][2] floats, then one
 // counter per (request, KV head) for the in-place merge; 256-byte aligned regions.
-size_t workspace_bytes_for(int batch, int h_q, int h_kv, int head_dim, int slots) {
-  const size_t rows = (size_t)batch * h_q * slots;
+// The balanced split's partials take a region of their own after those (before the counters):
+// [G][cap][head_dim] values and [G][cap][2] (max, sum), cap = batch * h_kv + warps, for at most
+// a wave of four 4-warp CTAs on each of 152 SMs and no more warps than a quarter of the pages
+// the table can hold. It is part of the layout of a plain decode call with an automatic chunk
+// size, more than one chunk slot, batch <= kFlatMaxBatch and room for one CTA.
+constexpr int kFlatBudgetWarps = 152 * 4 * kFlatWarpsPerCta;
+
+int flat_warps_for(int batch, int h_kv, int max_pages) {
+  const long long w = std::min<long long>(kFlatBudgetWarps, (long long)batch * h_kv * max_pages / 4);
+  return (int)(w / kFlatWarpsPerCta * kFlatWarpsPerCta);
+}
+
+bool flat_region_for(int batch, int h_kv, int max_pages, bool cascade, int slots) {
+  return !cascade && slots > 1 && batch <= kFlatMaxBatch && g_chunk_override.load() == 0 &&
+         flat_warps_for(batch, h_kv, max_pages) >= kFlatWarpsPerCta;
+}
+
+size_t flat_cap_for(int batch, int h_kv, int max_pages) {
+  return (size_t)batch * h_kv + flat_warps_for(batch, h_kv, max_pages);
+}
+
+size_t workspace_bytes_for(int batch, int h_q, int h_kv, int head_dim, int slots,
+                           size_t flat_cap = 0) {
+  const size_t rows = (size_t)batch * h_q * slots, frows = flat_cap * (h_q / h_kv);
   return align256(rows * head_dim * sizeof(float)) + align256(rows * 2 * sizeof(float)) +
+         (flat_cap ? align256(frows * head_dim * sizeof(float)) +
+                         align256(frows * 2 * sizeof(float))
+                   : 0) +
          align256((size_t)batch * h_kv * sizeof(int));
 }
 
@@ -412,7 +437,10 @@ size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num
     return 0;
   const int chunk = chunk_pages_for(batch, num_kv_heads, max_pages_per_seq);
   const int slots = (max_pages_per_seq + chunk - 1) / chunk;
-  return slots <= 1 ? 0 : workspace_bytes_for(batch, num_q_heads, num_kv_heads, head_dim, slots);
+  if (slots <= 1) return 0;
+  const bool flat = flat_region_for(batch, num_kv_heads, max_pages_per_seq, false, slots);
+  return workspace_bytes_for(batch, num_q_heads, num_kv_heads, head_dim, slots,
+                             flat ? flat_cap_for(batch, num_kv_heads, max_pages_per_seq) : 0);
 }
 
 int32_t pkv_cascade_prefix_chunk_pages(int32_t num_kv_heads, int32_t num_q_heads,
@@ -542,18 +570,32 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
     ca.ids_stride = groups->max_prefix_pages;
   }
   if (a.n_chunk_slots > 65535) return set_error(PKV_ESHAPE, "%s: too many chunks", who);
+  bool flat_region = false;  // the workspace holds the balanced split's partials too
+  float* flat_acc = nullptr;
+  float* flat_ml = nullptr;
   if (a.n_chunk_slots > 1) {
-    const size_t need = workspace_bytes_for(batch, num_q_heads, h_kv, D, a.n_chunk_slots);
+    flat_region = flat_region_for(batch, h_kv, max_pages_per_seq, cascade, a.n_chunk_slots);
+    const size_t fcap = flat_region ? flat_cap_for(batch, h_kv, max_pages_per_seq) : 0;
+    const size_t need = workspace_bytes_for(batch, num_q_heads, h_kv, D, a.n_chunk_slots, fcap);
     if (!workspace || workspace_bytes < need)
       return set_error(PKV_EINVAL, "%s: workspace of %zu bytes needed, %zu given", who, need,
                        workspace_bytes);
     if (!aligned16(workspace)) return set_error(PKV_EALIGN, "%s: workspace alignment", who);
     const size_t rows = (size_t)batch * num_q_heads * a.n_chunk_slots;
     char* ws = static_cast<char*>(workspace);
+    size_t off = 0;
     a.ws_acc = reinterpret_cast<float*>(ws);
-    a.ws_ml = reinterpret_cast<float*>(ws + align256(rows * D * sizeof(float)));
-    a.counters = reinterpret_cast<int*>(ws + align256(rows * D * sizeof(float)) +
-                                        align256(rows * 2 * sizeof(float)));
+    off += align256(rows * D * sizeof(float));
+    a.ws_ml = reinterpret_cast<float*>(ws + off);
+    off += align256(rows * 2 * sizeof(float));
+    if (flat_region) {
+      const size_t frows = fcap * G;
+      flat_acc = reinterpret_cast<float*>(ws + off);
+      off += align256(frows * D * sizeof(float));
+      flat_ml = reinterpret_cast<float*>(ws + off);
+      off += align256(frows * 2 * sizeof(float));
+    }
+    a.counters = reinterpret_cast<int*>(ws + off);
     // few chunks per sequence: the last CTA of each group merges them (no combine kernel).
     // A cascade decode that folds in the own-page kernel (overlap modes 0 and 1) always merges
     // there: a request's one own chunk folds in its prefix partials, several own chunks merge
@@ -591,18 +633,14 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
   // take the chunked layout's slots: [G][cap][D] values and [G][cap][2] (max, sum) with
   // cap = batch * h_kv * slots, numbered warp + (request, KV head) < warps + batch * h_kv.
   const int split_mode = g_split_mode.load();
-  const bool flat_applies = use_mma && !cascade && a.n_chunk_slots > 1 && !a.merge_in_place &&
-                            split_mode != 1 && g_chunk_override.load() == 0 &&
-                            batch <= kFlatMaxBatch;
+  const bool flat_applies = use_mma && flat_region && !a.merge_in_place && split_mode != 1;
   int flat_ctas = 0, flat_cap = 0;  // the balanced split's launch, worked out when it may run
   auto flat_plan = [&]() {
-    const long long rows = (long long)batch * h_kv;
-    const long long cap = rows * a.n_chunk_slots;
-    const long long max_ctas = std::min<long long>(cap - rows, kFlatMaxWarps) / kFlatWarpsPerCta;
+    const long long cap = (long long)flat_cap_for(batch, h_kv, max_pages_per_seq);
     int wave = 0;
-    if (cap < (1ll << 31) && max_ctas >= 1 &&
-        decode_flat_wave(a, kv, dtype_q, G, &wave) == cudaSuccess) {
-      flat_ctas = (int)std::min<long long>(max_ctas, wave);
+    if (cap < (1ll << 31) && decode_flat_wave(a, kv, dtype_q, G, &wave) == cudaSuccess) {
+      flat_ctas = std::min(flat_warps_for(batch, h_kv, max_pages_per_seq) / kFlatWarpsPerCta,
+                           wave);
       flat_cap = (int)cap;
     }
     return flat_ctas > 0;
@@ -639,8 +677,11 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
   }
   // the decode (and its combine) with the chunked (flat = false) or the balanced split
   auto run = [&](bool flat) {
+    DecodeArgs af = a;  // the balanced split's arguments: partials in their own region
+    af.ws_acc = flat_acc;
+    af.ws_ml = flat_ml;
     cudaError_t err = traced("paged_decode", s, [&] {
-      if (flat) return launch_decode_flat(a, kv, dtype_q, G, flat_ctas, flat_cap, &tk, &tv, s);
+      if (flat) return launch_decode_flat(af, kv, dtype_q, G, flat_ctas, flat_cap, &tk, &tv, s);
       if (use_mma) return launch_decode_mma(a, kv, dtype_q, G, &tk, &tv, s);
       if (kv == PKV_F32) return launch_decode_f32(a, dtype_q, D, G, s);
       if (kv == PKV_BF16) return launch_decode_bf16(a, dtype_q, D, G, s);
@@ -651,7 +692,7 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
     if (rs != PKV_OK) return rs;
     if (flat) {
       err = traced("decode_combine", s, [&] {
-        return launch_decode_flat_combine(a, kv, dtype_q, G, flat_ctas, flat_cap, s);
+        return launch_decode_flat_combine(af, kv, dtype_q, G, flat_ctas, flat_cap, s);
       });
       rs = cuda_status(err, "decode_combine launch");
     } else if (a.n_chunk_slots > 1 && !a.merge_in_place) {

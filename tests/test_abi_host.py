@@ -178,8 +178,18 @@ def test_workspace_size_and_chunk_policy():
     # Llama-3-70B-shaped long contexts (4 x 8 units over 8192 pages): 64-page chunks
     assert pkv.decode_chunk_pages(4, 8, 8192) == 64
     rows = 64 * 32 * 8
-    # partial values, partial (max, sum), then one counter per (request, kv head)
-    assert pkv.decode_workspace_size(64, 32, 8, 128, 256) == rows * 128 * 4 + rows * 2 * 4 + 256 * 8
+    # partial values, partial (max, sum); the balanced split's values and (max, sum) for
+    # 64 * 8 + 2432 partial slots per query head; then one counter per (request, kv head)
+    flat = (64 * 8 + 2432) * 4
+    assert pkv.decode_workspace_size(64, 32, 8, 128, 256) == (rows * 128 * 4 + rows * 2 * 4 +
+                                                              flat * 128 * 4 + flat * 2 * 4 +
+                                                              256 * 8)
+    pkv.decode_set_chunk_pages(32)  # a chosen chunk size: chunks only, no balanced region
+    try:
+        assert pkv.decode_workspace_size(64, 32, 8, 128, 256) == (rows * 128 * 4 + rows * 2 * 4 +
+                                                                  256 * 8)
+    finally:
+        pkv.decode_set_chunk_pages(0)
     # everything fits one chunk: no workspace
     assert pkv.decode_workspace_size(2, 4, 2, 64, 3) == 0
     pkv.decode_set_chunk_pages(2)
@@ -413,7 +423,15 @@ def test_cascade_argument_errors_are_caught_on_the_host():
     g = pkv.CascadeGroups(np.zeros(2, np.int32), np.array([3], np.int32), np.array([0, 2], np.int32),
                           np.array([0, 1], np.int32), 2, 3)
     plain = pkv.decode_workspace_size(2, 8, 4, 128, 600)
-    assert pkv.cascade_workspace_size(2, 8, 4, 128, 600, g) > plain
+    # more partial slots than the plain decode's chunks (whose layout, under a chosen chunk
+    # size, has no balanced-split region)
+    pkv.decode_set_chunk_pages(pkv.decode_chunk_pages(2, 4, 600))
+    try:
+        chunks_only = pkv.decode_workspace_size(2, 8, 4, 128, 600)
+    finally:
+        pkv.decode_set_chunk_pages(0)
+    assert chunks_only < plain
+    assert pkv.cascade_workspace_size(2, 8, 4, 128, 600, g) > chunks_only
     none = pkv.CascadeGroups(np.full(2, -1, np.int32), np.zeros(0, np.int32), np.zeros(1, np.int32),
                              np.zeros(0, np.int32), 0, 0)
     assert pkv.cascade_workspace_size(2, 8, 4, 128, 600, none) == plain

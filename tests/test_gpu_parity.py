@@ -480,8 +480,9 @@ def test_host_step_output_into_pageable_memory():
     hs.v_new_host.copy_(b.v_new.cpu())
     hs.block_tables_host.copy_(b.block_tables.cpu())
     hs.context_lens_host.copy_(b.context_lens.cpu())
-    pinned = hs.step(b.cache.k, b.cache.v, w.scale, workspace=b.workspace).clone()
-    torch.cuda.synchronize()
+    pinned = hs.step(b.cache.k, b.cache.v, w.scale, workspace=b.workspace)
+    torch.cuda.synchronize()  # (out_host holds the output once the stream gets there)
+    pinned = pinned.clone()
     pageable = np.full(pinned.numel(), 0x7fc0, dtype=np.uint16)  # NaN until written
     out_dev = torch.full_like(b.q, float("nan"))
     desc = pkv.cache_desc(b.cache.k)
