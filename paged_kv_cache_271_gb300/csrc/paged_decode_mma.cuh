@@ -27,7 +27,8 @@
 //    from 16-byte loads; V^T fragments by pairing the codes of consecutive tokens with byte
 //    permutes), the query is used in f16, and the MMAs run in f16 with fp32 accumulation; the
 //    K scale multiplies the scores and the V scale the output. The widening is exact, except
-//    that INT8 K codes for the scores carry a bias that the softmax cancels (widen4_scores).
+//    that INT8 codes carry a bias: the softmax cancels it in the scores (widen4_scores), and
+//    in the weighted values it comes off once per head at the end (MmaRun).
 //  * Fused append: the CTA that reads the page holding position ctx-1 writes this step's K/V
 //    row into the pool and into its staged copy of the page first (decode_epilogue.cuh).
 //  * Rows of the last page past the context may hold stale bytes (even NaN): their scores are
@@ -352,16 +353,21 @@ __device__ __forceinline__ void mma_load_query(const DecodeArgs& a, int b, int j
 
 // A warp's running softmax state over the pages it has read: per head the maximum and sum
 // (log2 domain) and the weighted values, in MMA accumulator fragments.
+// INT8 caches: the weighted values are accumulated over the biased codes (code + 1152, see
+// widen4_scores), and p16_run keeps the sum of the f16 P values the MMAs used, so that the
+// bias comes off once at the end: acc - 1152 sum(P) (the P products and their fp32 sums are
+// the same as with unbiased codes, up to the accumulation's rounding of the larger terms).
 template <int D, int G>
 struct MmaRun {
   static constexpr int NT = (G + 7) / 8, MT = D / 16;
-  float m_run[NT][2], l_run[NT][2];
+  float m_run[NT][2], l_run[NT][2], p16_run[NT][2];
   float acc[MT][NT][4];
   __device__ __forceinline__ void reset() {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       m_run[nt][0] = m_run[nt][1] = -INFINITY;
       l_run[nt][0] = l_run[nt][1] = 0.f;
+      p16_run[nt][0] = p16_run[nt][1] = 0.f;
 #pragma unroll
       for (int mi = 0; mi < MT; ++mi)
 #pragma unroll
@@ -381,6 +387,7 @@ __device__ __forceinline__ void mma_attend_page(uint32_t kt, uint32_t vt, int lp
                                                 int lane) {
   using QT = MmaQuery<KV, TQ, D, G>;
   constexpr bool F8 = QT::F8, QLO = QT::QLO;
+  constexpr bool I8 = KV::code == PKV_INT8;
   constexpr int NT = QT::NT, KP = QT::KP, MT = D / 16;
   const int gid = lane >> 2, tig = lane & 3;
   const auto& qf = Q.qf;
@@ -388,6 +395,7 @@ __device__ __forceinline__ void mma_attend_page(uint32_t kt, uint32_t vt, int lp
   const auto& sc_h = Q.sc_h;
   auto& m_run = R.m_run;
   auto& l_run = R.l_run;
+  auto& p16_run = R.p16_run;
   auto& acc = R.acc;
   // ---- scores S^T[16 tokens][8 heads per n-tile] ----
   float s[NT][4];
@@ -459,6 +467,10 @@ __device__ __forceinline__ void mma_attend_page(uint32_t kt, uint32_t vt, int lp
     if constexpr (F8) {
       const __half h0 = __float2half_rn(s[nt][0]), h1 = __float2half_rn(s[nt][1]);
       const __half h2 = __float2half_rn(s[nt][2]), h3 = __float2half_rn(s[nt][3]);
+      if constexpr (I8) {
+        p16_run[nt][0] = p16_run[nt][0] * alpha[nt][0] + __half2float(h0) + __half2float(h2);
+        p16_run[nt][1] = p16_run[nt][1] * alpha[nt][1] + __half2float(h1) + __half2float(h3);
+      }
       row0[gid] = __half_as_ushort(h0);
       row1[gid] = __half_as_ushort(h1);
       row0[gid + 8] = __half_as_ushort(h2);
@@ -535,8 +547,8 @@ __device__ __forceinline__ void mma_attend_page(uint32_t kt, uint32_t vt, int lp
       const uint32_t lo = __byte_perm(w0, w1, sel);  // tokens 2tig, 2tig+1
       const uint32_t hi = __byte_perm(w2, w3, sel);  // tokens 2tig+8, 2tig+9
       uint32_t a0, a1, a2, a3;
-      widen4<KV>(lo, a0, a1);
-      widen4<KV>(hi, a2, a3);
+      widen4_scores<KV>(lo, a0, a1);  // (INT8: biased codes; the bias comes off at the end)
+      widen4_scores<KV>(hi, a2, a3);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
         mma16816<true>(acc[mi][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
@@ -549,6 +561,7 @@ template <typename KV, int D, int G>
 __device__ __forceinline__ void mma_run_to_smem(const MmaRun<D, G>& R, float* red_acc,
                                                 float* red_m, float* red_l, int lane) {
   constexpr bool F8 = KV::bytes == 1;
+  constexpr bool I8 = KV::code == PKV_INT8;
   constexpr int NT = MmaRun<D, G>::NT, MT = MmaRun<D, G>::MT;
   const int gid = lane >> 2, tig = lane & 3;
   const auto& m_run = R.m_run;
@@ -567,14 +580,22 @@ __device__ __forceinline__ void mma_run_to_smem(const MmaRun<D, G>& R, float* re
         red_m[g] = m_run[nt][k];
         red_l[g] = l;
       }
+      float bias = 0.f;  // INT8: 1152 times the head's sum of the P values the MMAs used
+      if constexpr (I8) {
+        float p = R.p16_run[nt][k];
+        p += __shfl_xor_sync(0xffffffffu, p, 4);
+        p += __shfl_xor_sync(0xffffffffu, p, 8);
+        p += __shfl_xor_sync(0xffffffffu, p, 16);
+        bias = 1152.f * p;
+      }
 #pragma unroll
       for (int mi = 0; mi < MT; ++mi) {
         if (g < G) {
           // dims of rows gid and gid+8 of m-tile mi (see the two V^T fragment layouts)
           const int i0 = F8 ? 16 * gid + 2 * mi : 16 * mi + gid;
           const int i1 = F8 ? i0 + 1 : i0 + 8;
-          red_acc[g * D + i0] = acc[mi][nt][k];
-          red_acc[g * D + i1] = acc[mi][nt][k + 2];
+          red_acc[g * D + i0] = acc[mi][nt][k] - bias;
+          red_acc[g * D + i1] = acc[mi][nt][k + 2] - bias;
         }
       }
     }
