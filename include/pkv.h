@@ -294,8 +294,9 @@ int pkv_decode_set_split(int32_t mode);
 
 /* Autotuning of the split (mode 0): while on, the first call of each shape -- cache and query
  * dtypes, batch, head counts, table width, window and sinks, fused append or not -- that the
- * balanced split applies to runs the decode three times with each split, alternately, on its
- * stream, synchronises the stream, records the split with the least time and gives its result.
+ * balanced split applies to runs the decode five times with each split, alternately, on its
+ * stream, synchronises the stream, records the split whose decode kernel took the least time
+ * (the combine is not timed) and gives its result.
  * Later calls of that shape use the recorded split without timing. Calls made while their
  * stream is being captured into a CUDA graph never time (they use the recorded split, else
  * chunks); so do calls on a device other than the one current when autotuning was turned on

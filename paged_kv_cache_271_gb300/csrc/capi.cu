@@ -108,7 +108,7 @@ std::atomic<int> g_split_mode{0};
 // Autotuning of the split: the first call of a shape (while on, and not during stream capture)
 // times both splits and records the faster. Events for the timing are made when it is turned
 // on, on that device, so that decode calls create nothing.
-constexpr int kTuneReps = 3;
+constexpr int kTuneReps = 5;
 struct SplitKey {
   int v[11];
   bool operator<(const SplitKey& o) const {
@@ -676,10 +676,12 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
     if (st != PKV_OK) return st;
   }
   // the decode (and its combine) with the chunked (flat = false) or the balanced split
-  auto run = [&](bool flat) {
+  // (ev: events recorded around the decode kernel, for autotuning)
+  auto run = [&](bool flat, cudaEvent_t* ev = nullptr) {
     DecodeArgs af = a;  // the balanced split's arguments: partials in their own region
     af.ws_acc = flat_acc;
     af.ws_ml = flat_ml;
+    if (ev) cudaEventRecord(ev[0], s);
     cudaError_t err = traced("paged_decode", s, [&] {
       if (flat) return launch_decode_flat(af, kv, dtype_q, G, flat_ctas, flat_cap, &tk, &tv, s);
       if (use_mma) return launch_decode_mma(a, kv, dtype_q, G, &tk, &tv, s);
@@ -688,6 +690,7 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
       if (kv == PKV_INT8) return launch_decode_int8(a, dtype_q, D, G, s);
       return launch_decode_fp8(a, dtype_q, D, G, s);
     });
+    if (ev) cudaEventRecord(ev[1], s);
     int rs = cuda_status(err, "paged_decode launch");
     if (rs != PKV_OK) return rs;
     if (flat) {
@@ -717,18 +720,15 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
       cudaStreamIsCapturing(s, &cap_st) != cudaSuccess || cap_st != cudaStreamCaptureStatusNone ||
       !flat_plan())
     return run(false);
-  // both splits, alternately, kTuneReps times each; the faster (least time over its runs)
-  // is recorded and gives this call's result (the appended row is written again each run)
+  // both splits, alternately, kTuneReps times each; the one whose decode kernel took the
+  // least time over its runs is recorded and gives this call's result (the appended row is
+  // written again each run). The combine is left out of the timing: in a step replayed from
+  // a graph it starts beside the decode's last CTAs, and its own work is small and similar.
   float best[2] = {1e30f, 1e30f};
   {
     std::lock_guard<std::mutex> lk(g_tune_mu);
     for (int rep = 0; rep < kTuneReps && st == PKV_OK; ++rep)
-      for (int f = 0; f < 2 && st == PKV_OK; ++f) {
-        cudaEvent_t* ev = g_tune_ev[2 * rep + f];
-        cudaEventRecord(ev[0], s);
-        st = run(f == 1);
-        cudaEventRecord(ev[1], s);
-      }
+      for (int f = 0; f < 2 && st == PKV_OK; ++f) st = run(f == 1, g_tune_ev[2 * rep + f]);
     if (st != PKV_OK) return st;
     e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_status(e, "decode split autotune");
