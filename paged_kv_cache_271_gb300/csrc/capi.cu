@@ -235,7 +235,8 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // Workspace: acc [batch][h_q][slots][d] and (max, sum) [batch][h_q][slots][2] floats, then one
 // counter per (request, KV head) for the in-place merge; 256-byte aligned regions.
 // The balanced split's partials take a region of their own after those (before the counters):
-// [G][cap][head_dim] values and [G][cap][2] (max, sum), cap = batch * h_kv + warps, for at most
+// [G][cap][head_dim] values, [G][cap][2] (max, sum) and [batch + 1] per-request page offsets,
+// cap = batch * h_kv + warps, for at most
 // a wave of four 4-warp CTAs on each of 152 SMs and no more warps than a quarter of the pages
 // the table can hold. It is part of the layout of a plain decode call with an automatic chunk
 // size, more than one chunk slot, batch <= kFlatMaxBatch and room for one CTA.
@@ -260,7 +261,8 @@ size_t workspace_bytes_for(int batch, int h_q, int h_kv, int head_dim, int slots
   const size_t rows = (size_t)batch * h_q * slots, frows = flat_cap * (h_q / h_kv);
   return align256(rows * head_dim * sizeof(float)) + align256(rows * 2 * sizeof(float)) +
          (flat_cap ? align256(frows * head_dim * sizeof(float)) +
-                         align256(frows * 2 * sizeof(float))
+                         align256(frows * 2 * sizeof(float)) +
+                         align256(((size_t)batch + 1) * sizeof(int))
                    : 0) +
          align256((size_t)batch * h_kv * sizeof(int));
 }
@@ -594,6 +596,8 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
       off += align256(frows * D * sizeof(float));
       flat_ml = reinterpret_cast<float*>(ws + off);
       off += align256(frows * 2 * sizeof(float));
+      a.flat_pre = reinterpret_cast<int*>(ws + off);
+      off += align256(((size_t)batch + 1) * sizeof(int));
     }
     a.counters = reinterpret_cast<int*>(ws + off);
     // few chunks per sequence: the last CTA of each group merges them (no combine kernel).

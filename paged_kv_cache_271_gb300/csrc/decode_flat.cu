@@ -142,6 +142,8 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS, KV::bytes == 1 ? 4 : 3) pa
     }
     if (threadIdx.x == S::kThreads - 1) pre[B] = run;
     __syncthreads();
+    if (blockIdx.x == 0)  // for the combine
+      for (int b = threadIdx.x; b <= B; b += S::kThreads) a.flat_pre[b] = pre[b];
   }
 
   const long long T = (long long)pre[B] * h_kv;  // pages in the stream
@@ -328,31 +330,12 @@ __global__ void __launch_bounds__(32 * PKV_MMA_WARPS, KV::bytes == 1 ? 4 : 3) pa
   }
 }
 
-// The run of partials of (b, j) in the stream, from the context lengths alone (a sum over the
-// block of 128 threads): nb pages per KV head; partial ids first + r .. first + r + count - 1.
+// The run of partials of (b, j) in the stream, from the page offsets the decode's first CTA
+// wrote: nb pages per KV head; partial ids first + r .. first + r + count - 1.
 __device__ __forceinline__ void flat_run(const DecodeArgs& a, int b, int j, int n_warps, int& nb,
                                          long long& first, int& count) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __shared__ int part_before[4], part_all[4];
-  int before = 0, all = 0;
-  for (int bb = threadIdx.x; bb < a.batch; bb += 128) {
-    const int n = seq_pages(flat_ctx(a, bb), a.sink, a.window).n;
-    all += n;
-    if (bb < b) before += n;
-  }
-#pragma unroll
-  for (int o = 16; o >= 1; o /= 2) {
-    before += __shfl_xor_sync(0xffffffffu, before, o);
-    all += __shfl_xor_sync(0xffffffffu, all, o);
-  }
-  if (lane == 0) {
-    part_before[warp] = before;
-    part_all[warp] = all;
-  }
-  __syncthreads();
-  before = part_before[0] + part_before[1] + part_before[2] + part_before[3];
-  all = part_all[0] + part_all[1] + part_all[2] + part_all[3];
-  nb = seq_pages(flat_ctx(a, b), a.sink, a.window).n;
+  const int before = a.flat_pre[b], all = a.flat_pre[a.batch];
+  nb = a.flat_pre[b + 1] - before;
   first = 0;
   count = 0;
   if (nb == 0) return;
@@ -362,9 +345,9 @@ __device__ __forceinline__ void flat_run(const DecodeArgs& a, int b, int j, int 
   count = (int)(flat_owner(P0 + nb - 1, T, N) - first + 1);
 }
 
-// Merges each (b, j)'s partials in stream order, its run worked out before waiting for the
-// decode grid; a (b, j) whose pages lie in one warp's share was written out by the decode (no
-// partials), and one with no pages gets out = 0.
+// Merges each (b, j)'s partials in stream order, once the decode grid is done (its run comes
+// from the decode's page offsets); a (b, j) whose pages lie in one warp's share was written out
+// by the decode (no partials), and one with no pages gets out = 0.
 //  * PER_HEAD false (many (b, j), short runs): one CTA per (b, j); warp w merges heads w, w + 4,
 //    ... one partial run each.
 //  * PER_HEAD true (few (b, j), long runs): one CTA per (b, j, head g); the four warps merge a
@@ -376,13 +359,13 @@ __global__ void __launch_bounds__(128) decode_flat_combine_kernel(const DecodeAr
   constexpr int DL = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.y, b = r / a.h_kv, j = r - b * a.h_kv;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid is done, its writes seen
   int nb, count;
   long long first;
   flat_run(a, b, j, n_warps, nb, first, count);
   if (count == 1) return;  // one warp's share holds the whole (b, j): the decode wrote out
   TQ* out = static_cast<TQ*>(a.out);
   if (!PER_HEAD) {
-    if (count > 0) asm volatile("griddepcontrol.wait;" ::: "memory");  // decode done, seen
     for (int g = warp; g < G; g += 4) {
       const size_t o = ((size_t)b * a.h_q + j * G + g) * D + lane * DL;
       float M = -INFINITY, Lw = 0.f, A[DL];
@@ -406,7 +389,6 @@ __global__ void __launch_bounds__(128) decode_flat_combine_kernel(const DecodeAr
       for (int k = 0; k < DL; ++k) store_from_float(out, o + k, 0.f);
     return;
   }
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // the decode grid is done, its writes seen
   const size_t part = (size_t)g * cap + (size_t)(first + r);
   __shared__ float red_a[4][D];
   __shared__ float red_ml[4][2];

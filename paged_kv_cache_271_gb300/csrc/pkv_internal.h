@@ -57,6 +57,9 @@ struct DecodeArgs {
   // grid's first CTA waits for the prefix grid before it exits, so the decode grid -- which the
   // combine waits for -- cannot complete before the prefix kernel
   int defer_fold;
+  // balanced split (decode_flat.cu): [batch + 1] pages walked per KV head by the requests
+  // before b, written by the decode's first CTA for its combine
+  int* flat_pre;
 };
 
 // Query rows ((member, query head) pairs) per CTA of the cascade prefix kernel, and the CTAs

@@ -181,9 +181,10 @@ def test_workspace_size_and_chunk_policy():
     # partial values, partial (max, sum); the balanced split's values and (max, sum) for
     # 64 * 8 + 2432 partial slots per query head; then one counter per (request, kv head)
     flat = (64 * 8 + 2432) * 4
+    # (and the requests' page offsets, 65 ints in a 256-byte aligned region)
     assert pkv.decode_workspace_size(64, 32, 8, 128, 256) == (rows * 128 * 4 + rows * 2 * 4 +
                                                               flat * 128 * 4 + flat * 2 * 4 +
-                                                              256 * 8)
+                                                              512 + 256 * 8)
     pkv.decode_set_chunk_pages(32)  # a chosen chunk size: chunks only, no balanced region
     try:
         assert pkv.decode_workspace_size(64, 32, 8, 128, 256) == (rows * 128 * 4 + rows * 2 * 4 +

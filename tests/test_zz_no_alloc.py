@@ -41,10 +41,11 @@ def _noalloc(sc, q, out):
     assert st == 0, pkv.lib().pkv_last_error().decode()
 
 
-@pytest.mark.parametrize("merge", ["combine kernel", "merge in place"])
+@pytest.mark.parametrize("merge", ["combine kernel", "merge in place", "balanced split"])
 def test_noalloc_matches_workspace_entry_point_on_two_calls(merge):
     # split partials merged by the combine kernel, or by the last CTA of each (request, KV
-    # head) through the chunk counters: both uses of the scratch
+    # head) through the chunk counters, or the balanced split's partials in their own region:
+    # every use of the scratch
     import dataclasses
     from gpu_harness import oracle_expected
     w = workloads.llama3_8b_batch64(batch=8)
@@ -54,7 +55,10 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(merge):
                                      sc.block_tables.shape[1])
     assert 0 < need <= pkv.lib().pkv_decode_noalloc_scratch_bytes()  # the split scratch is used
     q2 = (sc.q.float() * -0.7).to(torch.bfloat16)
-    pkv.decode_set_chunk_pages(8)  # several chunks per request
+    if merge == "balanced split":
+        pkv.decode_set_split(2)
+    else:
+        pkv.decode_set_chunk_pages(8)  # several chunks per request
     pkv.decode_set_merge_in_place(64 if merge == "merge in place" else 0)
     try:
         need = pkv.decode_workspace_size(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim,
@@ -75,6 +79,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(merge):
     finally:
         pkv.decode_set_chunk_pages(0)
         pkv.decode_set_merge_in_place(0)
+        pkv.decode_set_split(0)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
