@@ -8,6 +8,7 @@
 // coalesced. FP8: code = cvt.rn.satfinite.e4m3(fp32(x / s)) (section 7, "fp8 KV (E4M3)";
 // per-head scale, round-to-nearest-even and saturation are this library's reading).
 #include <algorithm>
+#include <atomic>
 #include <math.h>
 
 #include "combine_merge.cuh"
@@ -414,15 +415,15 @@ cudaError_t launch_kv_append(const AppendArgs& a, int in_dtype, int cache_dtype,
     const int qt = per_tok <= 128 ? 128 : 256;
     const int64_t groups = ((int64_t)a.num_tokens + kAppendTokens - 1) / kAppendTokens;
     auto go = [&](auto kern, int slot) {
-      static int wave[2] = {0, 0};  // resident blocks on the device, per block size
-      if (!wave[slot]) {
+      static std::atomic<int> wave[2];  // resident blocks on the device, per block size
+      if (!wave[slot].load()) {
         int per_sm = 0, dev = 0, sms = 0;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, qt, 0);
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        wave[slot] = std::max(1, per_sm) * std::max(1, sms);
+        wave[slot].store(std::max(1, per_sm) * std::max(1, sms));
       }
-      const int blocks = (int)std::min<int64_t>(groups, wave[slot]);
+      const int blocks = (int)std::min<int64_t>(groups, wave[slot].load());
       kern<<<blocks, qt, 0, s>>>(a);
     };
     const int slot = qt == 128 ? 0 : 1;

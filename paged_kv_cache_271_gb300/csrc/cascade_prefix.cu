@@ -20,6 +20,7 @@
 //  * each CTA writes its rows' partial (max, sum, weighted values) for its chunk of the prefix
 //    to the chunk slots of every member; the members' own pages follow in later slots and the
 //    combine kernel merges them all (the same partial-merge rule as the split decode).
+#include <atomic>
 #include <cuda.h>
 #include <math.h>
 
@@ -285,14 +286,14 @@ template <int G>
 cudaError_t launch_g(const DecodeArgs& a, const CascadeArgs& ca, const CUtensorMap& tk,
                      const CUtensorMap& tv, cudaStream_t s) {
   auto kern = cascade_prefix_kernel<G>;
-  static unsigned long long attr_done = 0;  // one bit per device
+  static std::atomic<unsigned long long> attr_done{0};  // one bit per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !((attr_done >> dev) & 1ull)) {
+  if (dev >= 64 || !((attr_done.load() >> dev) & 1ull)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kCpSmem);
     if (e != cudaSuccess) return e;
-    if (dev < 64) attr_done |= 1ull << dev;
+    if (dev < 64) attr_done.fetch_or(1ull << dev);
   }
   const int chunks = (a.max_prefix_pages + a.prefix_chunk_pages - 1) / a.prefix_chunk_pages;
   const int tiles = (ca.max_members * G + kCpRows - 1) / kCpRows;

@@ -30,6 +30,7 @@
 // The query rows are read by the row threads while tensor memory is allocated and the first
 // copies start; each row's partial leaves through shared memory and one bulk copy.
 // Every wait is bounded (PKV_DEVERR_TIMEOUT); the TMEM columns are freed on every exit path.
+#include <atomic>
 #include <cuda.h>
 #include <math.h>
 
@@ -508,14 +509,14 @@ template <int G>
 cudaError_t launch_tc_g(const DecodeArgs& a, const CascadeArgs& ca, const CUtensorMap& tk,
                         const CUtensorMap& tv, cudaStream_t s) {
   auto kern = cascade_prefix_tc_kernel<G>;
-  static unsigned long long attr_done = 0;  // one bit per device
+  static std::atomic<unsigned long long> attr_done{0};  // one bit per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !((attr_done >> dev) & 1ull)) {
+  if (dev >= 64 || !((attr_done.load() >> dev) & 1ull)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
     if (e != cudaSuccess) return e;
-    if (dev < 64) attr_done |= 1ull << dev;
+    if (dev < 64) attr_done.fetch_or(1ull << dev);
   }
   const int chunks = (a.max_prefix_pages + a.prefix_chunk_pages - 1) / a.prefix_chunk_pages;
   const int tiles = (ca.max_members * G + kTcRows - 1) / kTcRows;

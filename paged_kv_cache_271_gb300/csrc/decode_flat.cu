@@ -17,6 +17,7 @@
 // (b, j) index; distinct for distinct segments): a contiguous run, which the combine finds
 // from the context lengths alone, as the decode does.
 #include <algorithm>
+#include <mutex>
 
 #include "combine_merge.cuh"
 #include "paged_decode_mma.cuh"
@@ -435,13 +436,15 @@ struct FlatLaunch {
     auto kern = paged_decode_flat_kernel<KV, TQ, D, G>;
     const int smem = (int)S::smem_bytes(batch);
     // per device: the largest dynamic shared memory granted so far, and the wave of the last
-    // size asked for
+    // size asked for (under a lock: callers may run on several host threads)
     constexpr int kDevs = 64;
     static int attr_smem[kDevs], occ_smem[kDevs], occ_ctas[kDevs];
+    static std::mutex mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kDevs) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
     if (smem > attr_smem[dev]) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;

@@ -25,6 +25,7 @@
 //    positions, so results do not depend on which physical pages hold the tokens.
 #pragma once
 
+#include <atomic>
 #include <math.h>
 
 #include "pkv_device.cuh"
@@ -355,14 +356,14 @@ template <typename KV, typename TQ, int D, int G>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
   using S = DecodeShape<KV, D, G>;
   auto kern = paged_decode_kernel<KV, TQ, D, G>;
-  static unsigned long long attr_done = 0;  // one bit per device, per instantiation
+  static std::atomic<unsigned long long> attr_done{0};  // one bit per device, per instantiation
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !((attr_done >> dev) & 1ull)) {
+  if (dev >= 64 || !((attr_done.load() >> dev) & 1ull)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (dev < 64) attr_done |= 1ull << dev;
+    if (dev < 64) attr_done.fetch_or(1ull << dev);
   }
   dim3 grid(a.chunk_grid, a.h_kv, a.batch);
   kern<<<grid, S::kThreads, S::SMEM_BYTES, s>>>(a);

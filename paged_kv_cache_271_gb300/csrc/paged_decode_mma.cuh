@@ -35,6 +35,7 @@
 //    set to -inf and their V rows to zero before the P.V product.
 #pragma once
 
+#include <atomic>
 #include <cuda.h>
 #include <math.h>
 
@@ -793,14 +794,14 @@ cudaError_t launch_decode_mma_w(const DecodeArgs& a, const CUtensorMap& tk,
                                 const CUtensorMap& tv, cudaStream_t s) {
   using S = MmaShape<KV, D, G, WU>;
   auto kern = paged_decode_mma_kernel<KV, TQ, D, G, WU>;
-  static unsigned long long attr_done = 0;  // one bit per device, per instantiation
+  static std::atomic<unsigned long long> attr_done{0};  // one bit per device, per instantiation
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !((attr_done >> dev) & 1ull)) {
+  if (dev >= 64 || !((attr_done.load() >> dev) & 1ull)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    if (dev < 64) attr_done |= 1ull << dev;
+    if (dev < 64) attr_done.fetch_or(1ull << dev);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.chunk_grid, a.h_kv, WU ? (a.batch + S::kWarps - 1) / S::kWarps : a.batch);
