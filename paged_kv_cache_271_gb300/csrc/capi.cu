@@ -115,10 +115,11 @@ struct SplitKey {
     return std::lexicographical_compare(v, v + 11, o.v, o.v + 11);
   }
 };
-std::mutex g_tune_mu;
+std::mutex g_tune_mu;      // the recorded choices
+std::mutex g_tune_run_mu;  // the timing runs and their events (one shape timed at a time)
 std::map<SplitKey, bool> g_tuned;  // true: the balanced split measured faster
 std::atomic<int> g_autotune{0};
-int g_tune_dev = -1;
+std::atomic<int> g_tune_dev{-1};
 cudaEvent_t g_tune_ev[2 * kTuneReps][2];
 
 // ---- TMA tensor maps of the pools (for the tensor-core decode) -------------------------------
@@ -372,6 +373,7 @@ int pkv_decode_set_split(int32_t mode) {
 int pkv_decode_set_autotune(int32_t on) {
   if (on != 0 && on != 1)
     return set_error(PKV_EINVAL, "pkv_decode_set_autotune: %d is not 0 or 1", on);
+  std::lock_guard<std::mutex> run_lk(g_tune_run_mu);  // (no timing run uses the events now)
   std::lock_guard<std::mutex> lk(g_tune_mu);
   if (on) {
     int dev = 0;
@@ -380,7 +382,7 @@ int pkv_decode_set_autotune(int32_t on) {
     if (g_tune_dev != dev) {
       if (g_tune_dev >= 0) {
         int cur = dev;
-        cudaSetDevice(g_tune_dev);
+        cudaSetDevice(g_tune_dev.load());
         for (auto& pr : g_tune_ev) {
           cudaEventDestroy(pr[0]);
           cudaEventDestroy(pr[1]);
@@ -730,7 +732,12 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
   // a graph it starts beside the decode's last CTAs, and its own work is small and similar.
   float best[2] = {1e30f, 1e30f};
   {
-    std::lock_guard<std::mutex> lk(g_tune_mu);
+    std::lock_guard<std::mutex> run_lk(g_tune_run_mu);
+    {  // another thread may have timed this shape meanwhile
+      std::lock_guard<std::mutex> lk(g_tune_mu);
+      auto it = g_tuned.find(key);
+      if (it != g_tuned.end()) return run(it->second && flat_plan());
+    }
     for (int rep = 0; rep < kTuneReps && st == PKV_OK; ++rep)
       for (int f = 0; f < 2 && st == PKV_OK; ++f) st = run(f == 1, g_tune_ev[2 * rep + f]);
     if (st != PKV_OK) return st;
@@ -743,6 +750,7 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
             cudaSuccess)
           best[f] = std::min(best[f], ms);
       }
+    std::lock_guard<std::mutex> lk(g_tune_mu);
     g_tuned[key] = best[1] < best[0];
   }
   return run(best[1] < best[0]);

@@ -15,7 +15,7 @@
 // With T pages in the stream and N warps, warp w takes pages [w T / N, (w + 1) T / N), so the
 // warps that share a (b, j) are consecutive and its partials can be numbered w + r (r = the
 // (b, j) index; distinct for distinct segments): a contiguous run, which the combine finds
-// from the context lengths alone, as the decode does.
+// from the requests' stream offsets (written to the workspace by the decode's first CTA).
 #include <algorithm>
 #include <mutex>
 
