@@ -180,7 +180,9 @@ class StepState:
         choice = pkv.decode_split_choice(kv, self.q.dtype, self.batch, self.h_q, self.h_kv,
                                          self.bt.shape[1], getattr(self, "window", 0) or 0,
                                          getattr(self, "sink", 0) or 0, fused=True)
-        return {1: "balanced (measured faster)", 0: "chunks (measured faster)"}.get(
+        return {0: "chunks (measured fastest)", 1: "balanced (measured fastest)",
+                2: "chunks-x1.5 (1.5 times longer chunks, measured fastest)",
+                3: "chunks-x2 (2 times longer chunks, measured fastest)"}.get(
             choice, "chunks (no split measured: one pass or chunks only)")
 
     def decode_bytes(self):
@@ -449,7 +451,7 @@ def recorded_traffic(split):
     try:
         with open(path) as f:
             rec = dict(tok.split("=", 1) for tok in f.read().split())
-        if rec.get("source_sha") == source_sha() and split.startswith(rec.get("split", "?")):
+        if rec.get("source_sha") == source_sha() and split.split(" ")[0] == rec.get("split"):
             return float(rec["dram_bytes_per_launch"])
     except (OSError, ValueError, KeyError):
         pass

@@ -277,9 +277,11 @@ int pkv_decode_set_merge_in_place(int32_t max_chunks);
 int pkv_decode_set_kernel(int32_t which);
 
 /* How the tensor-core decode splits a call that needs split partials (workspace size > 0).
- * Two splits, each merged by a combine kernel in a fixed order:
+ * The splits, each merged by a combine kernel in a fixed order:
  *  - chunks, as described under pkv_paged_decode_attention (a CTA per (request, KV head,
  *    chunk); the hardware hands out CTAs as SMs free up);
+ *  - chunks 1.5 or 2 times the automatic length (fewer CTAs and waves of them; the partials
+ *    fit the same slots), when the chunk size is automatic;
  *  - balanced: the whole call's (request, KV head, attended page) stream is cut into equal
  *    contiguous shares, one per warp of a single wave of CTAs (no more warps than the workspace
  *    has partial slots for), and each (request, KV head)'s partials are merged in stream order.
@@ -288,25 +290,27 @@ int pkv_decode_set_kernel(int32_t which);
  *    request's split (and so its rounding) depends on the whole batch's lengths, not on
  *    physical page placement.
  * mode 0 = automatic (the default): the split recorded for the call's shape by autotuning
- * (pkv_decode_set_autotune), else chunks; 1 = chunks only; 2 = balanced wherever it applies.
+ * (pkv_decode_set_autotune), else chunks; 1 = chunks only; 2 = balanced wherever it applies;
+ * 3, 4 = chunks 1.5 or 2 times longer wherever they apply.
  * Results are deterministic for given inputs and choice. Process-wide. */
 int pkv_decode_set_split(int32_t mode);
 
 /* Autotuning of the split (mode 0): while on, the first call of each shape -- cache and query
- * dtypes, batch, head counts, table width, window and sinks, fused append or not -- that the
- * balanced split applies to runs the decode five times with each split, alternately, on its
- * stream, synchronises the stream, records the split whose decode kernel took the least time
- * (the combine is not timed) and gives its result.
- * Later calls of that shape use the recorded split without timing. Calls made while their
- * stream is being captured into a CUDA graph never time (they use the recorded split, else
- * chunks); so do calls on a device other than the one current when autotuning was turned on
- * (its timing events are made then, so decode calls create nothing). Off by default. */
+ * dtypes, batch, head counts, table width, window and sinks, fused append or not -- for which
+ * more than one split applies runs the decode five times with each split that applies, in
+ * turn, on its stream, synchronises the stream, records the split whose decode kernel took the
+ * least time (the combine is not timed) and gives its result. Later calls of that shape use the
+ * recorded split without timing. Calls made while their stream is being captured into a CUDA
+ * graph never time (they use the recorded split, else chunks); so do calls on a device other
+ * than the one current when autotuning was turned on (its timing events are made then, so
+ * decode calls create nothing). Off by default. */
 int pkv_decode_set_autotune(int32_t on);
 
 /* Forgets every recorded split. */
 int pkv_decode_autotune_reset(void);
 
-/* The split recorded for a shape: 1 balanced, 0 chunks, -1 none recorded. */
+/* The split recorded for a shape: 0 chunks, 1 balanced, 2 and 3 chunks 1.5 and 2 times
+ * longer, -1 none recorded. */
 int pkv_decode_split_choice(int32_t kv_dtype, int32_t q_dtype, int32_t batch, int32_t num_q_heads,
                             int32_t num_kv_heads, int32_t max_pages_per_seq, int32_t window,
                             int32_t sink_tokens, int32_t fused);

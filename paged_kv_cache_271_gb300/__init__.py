@@ -723,7 +723,8 @@ def decode_set_kernel(which: int):
 
 def decode_set_split(mode: int):
     """0 automatic (the split autotuning recorded for the call's shape, else chunks), 1 chunks
-    only, 2 the balanced split of the tensor-core decode wherever it applies."""
+    only, 2 the balanced split of the tensor-core decode wherever it applies, 3 and 4 chunks
+    1.5 and 2 times the automatic length wherever they apply."""
     _check(lib().pkv_decode_set_split(int(mode)))
 
 
@@ -738,8 +739,8 @@ def decode_autotune_reset():
 
 def decode_split_choice(kv_dtype, q_dtype, batch, num_q_heads, num_kv_heads, max_pages_per_seq,
                         window=0, sink_tokens=0, fused=False) -> int:
-    """The recorded split for a shape: 1 balanced, 0 chunks, -1 none. Dtypes as torch dtypes
-    or pkv_dtype codes."""
+    """The recorded split for a shape: 0 chunks, 1 balanced, 2 and 3 chunks 1.5 and 2 times
+    longer, -1 none. Dtypes as torch dtypes or pkv_dtype codes."""
     code = lambda d: d if isinstance(d, int) else _dtype_code(torch.empty(0, dtype=d))
     return int(lib().pkv_decode_split_choice(code(kv_dtype), code(q_dtype), batch, num_q_heads,
                                              num_kv_heads, max_pages_per_seq, window, sink_tokens,

@@ -100,15 +100,16 @@ std::atomic<int> g_kernel_choice{0};  // 0 automatic, 1 CUDA cores, 2 tensor cor
 // folds its partials in; 2: overlaps it and leaves the fold to the combine kernel
 std::atomic<int> g_cascade_overlap{2};
 std::atomic<int> g_warp_units{1};     // 1: one warp per request for short single-chunk runs
-// 0: automatic -- the measured faster split for the call's shape when one has been recorded
+// 0: automatic -- the split measured fastest for the call's shape when one has been recorded
 // (autotuning), else chunks; 1: chunks only; 2: the balanced split (decode_flat.cu) wherever it
-// applies
+// applies; 3, 4: chunks 1.5 or 2 times the automatic length wherever they apply
 std::atomic<int> g_split_mode{0};
 
 // Autotuning of the split: the first call of a shape (while on, and not during stream capture)
 // times both splits and records the faster. Events for the timing are made when it is turned
 // on, on that device, so that decode calls create nothing.
 constexpr int kTuneReps = 5;
+constexpr int kTuneKinds = 4;  // chunks, balanced, chunks 1.5x and 2x longer
 struct SplitKey {
   int v[11];
   bool operator<(const SplitKey& o) const {
@@ -117,10 +118,10 @@ struct SplitKey {
 };
 std::mutex g_tune_mu;      // the recorded choices
 std::mutex g_tune_run_mu;  // the timing runs and their events (one shape timed at a time)
-std::map<SplitKey, bool> g_tuned;  // true: the balanced split measured faster
+std::map<SplitKey, int> g_tuned;  // the kind measured fastest (decode_impl's run)
 std::atomic<int> g_autotune{0};
 std::atomic<int> g_tune_dev{-1};
-cudaEvent_t g_tune_ev[2 * kTuneReps][2];
+cudaEvent_t g_tune_ev[kTuneKinds * kTuneReps][2];
 
 // ---- TMA tensor maps of the pools (for the tensor-core decode) -------------------------------
 
@@ -364,8 +365,8 @@ int pkv_decode_set_warp_per_request(int32_t on) {
 }
 
 int pkv_decode_set_split(int32_t mode) {
-  if (mode < 0 || mode > 2)
-    return set_error(PKV_EINVAL, "pkv_decode_set_split: %d is not 0, 1 or 2", mode);
+  if (mode < 0 || mode > 4)
+    return set_error(PKV_EINVAL, "pkv_decode_set_split: %d is not in 0..4", mode);
   g_split_mode.store(mode);
   return PKV_OK;
 }
@@ -418,7 +419,7 @@ int pkv_decode_split_choice(int32_t kv_dtype, int32_t q_dtype, int32_t batch, in
     if (v[0] == kv_dtype && v[1] == q_dtype && v[2] == batch && v[3] == num_q_heads &&
         v[4] == num_kv_heads && v[5] == max_pages_per_seq && v[6] == window &&
         v[7] == (window > 0 ? sink_tokens : 0) && v[8] == (fused ? 1 : 0))
-      return kv.second ? 1 : 0;
+      return kv.second;
   }
   return -1;
 }
@@ -525,6 +526,7 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
   a.max_pages = max_pages_per_seq;
   a.chunk_pages = chunk_pages_for(batch, h_kv, max_pages_per_seq);
   a.n_chunk_slots = (max_pages_per_seq + a.chunk_pages - 1) / a.chunk_pages;
+  int walk_pages = max_pages_per_seq;  // the most pages a request can walk
   if (window > 0) {
     // a windowed request walks at most its sink pages, the window's pages and one boundary
     // page: the chunks are sized for that run, not for the table width (while the partials
@@ -537,6 +539,7 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
     while ((walk + chunk - 1) / chunk > a.n_chunk_slots) chunk *= 2;
     a.chunk_pages = chunk;
     a.n_chunk_slots = (walk + chunk - 1) / chunk;
+    walk_pages = walk;
   }
   a.chunk_grid = a.n_chunk_slots;
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -633,13 +636,15 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
   // leave a CTA's four warps with a page or two each)
   // (one chunk column: no request splits, so no merge of chunk partials can arise)
   a.warp_units = use_mma && a.chunk_grid == 1 && a.chunk_pages <= 16 && g_warp_units.load() != 0;
-  // The balanced split (one wave of CTAs, equal shares of the (request, KV head, page) stream
-  // per warp; decode_flat.cu) for a plain call on the tensor-core kernel that needs split
-  // partials merged by the combine kernel, with the automatic chunk size and mode. Its partials
-  // take the chunked layout's slots: [G][cap][D] values and [G][cap][2] (max, sum) with
-  // cap = batch * h_kv * slots, numbered warp + (request, KV head) < warps + batch * h_kv.
+  // Splits of a plain call on the tensor-core kernel whose partials go to a combine kernel:
+  // the chunks (kind 0), the balanced split (kind 1: one wave of CTAs, equal shares of the
+  // (request, KV head, page) stream per warp, decode_flat.cu; its partials in the workspace's
+  // region for them), and, when the chunk size is automatic, chunks 1.5 and 2 times longer
+  // (kinds 2 and 3: fewer CTAs and waves; their partials fit the slots of the automatic size).
   const int split_mode = g_split_mode.load();
   const bool flat_applies = use_mma && flat_region && !a.merge_in_place && split_mode != 1;
+  const bool longer_applies = use_mma && !cascade && a.n_chunk_slots > 1 && !a.merge_in_place &&
+                              g_chunk_override.load() == 0 && split_mode != 1 && split_mode != 2;
   int flat_ctas = 0, flat_cap = 0;  // the balanced split's launch, worked out when it may run
   auto flat_plan = [&]() {
     const long long cap = (long long)flat_cap_for(batch, h_kv, max_pages_per_seq);
@@ -681,16 +686,22 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
     st = cuda_status(e, "cascade_prefix launch");
     if (st != PKV_OK) return st;
   }
-  // the decode (and its combine) with the chunked (flat = false) or the balanced split
+  // the decode (and its combine) with split kind 0..3 (above)
   // (ev: events recorded around the decode kernel, for autotuning)
-  auto run = [&](bool flat, cudaEvent_t* ev = nullptr) {
+  auto run = [&](int kind, cudaEvent_t* ev = nullptr) {
     DecodeArgs af = a;  // the balanced split's arguments: partials in their own region
     af.ws_acc = flat_acc;
     af.ws_ml = flat_ml;
+    DecodeArgs ac = a;  // the chunks' arguments (longer chunks: the same partial slots)
+    if (kind >= 2) {
+      ac.chunk_pages = std::min(4096, kind == 2 ? a.chunk_pages * 3 / 2 : a.chunk_pages * 2);
+      ac.chunk_grid = (walk_pages + ac.chunk_pages - 1) / ac.chunk_pages;
+    }
     if (ev) cudaEventRecord(ev[0], s);
     cudaError_t err = traced("paged_decode", s, [&] {
-      if (flat) return launch_decode_flat(af, kv, dtype_q, G, flat_ctas, flat_cap, &tk, &tv, s);
-      if (use_mma) return launch_decode_mma(a, kv, dtype_q, G, &tk, &tv, s);
+      if (kind == 1)
+        return launch_decode_flat(af, kv, dtype_q, G, flat_ctas, flat_cap, &tk, &tv, s);
+      if (use_mma) return launch_decode_mma(ac, kv, dtype_q, G, &tk, &tv, s);
       if (kv == PKV_F32) return launch_decode_f32(a, dtype_q, D, G, s);
       if (kv == PKV_BF16) return launch_decode_bf16(a, dtype_q, D, G, s);
       if (kv == PKV_INT8) return launch_decode_int8(a, dtype_q, D, G, s);
@@ -699,61 +710,78 @@ static int decode_impl(const char* who, const void* q, int32_t dtype_q, int32_t 
     if (ev) cudaEventRecord(ev[1], s);
     int rs = cuda_status(err, "paged_decode launch");
     if (rs != PKV_OK) return rs;
-    if (flat) {
+    if (kind == 1) {
       err = traced("decode_combine", s, [&] {
         return launch_decode_flat_combine(af, kv, dtype_q, G, flat_ctas, flat_cap, s);
       });
       rs = cuda_status(err, "decode_combine launch");
     } else if (a.n_chunk_slots > 1 && !a.merge_in_place) {
-      err = traced("decode_combine", s, [&] { return launch_decode_combine(a, dtype_q, D, s); });
+      err = traced("decode_combine", s, [&] { return launch_decode_combine(ac, dtype_q, D, s); });
       rs = cuda_status(err, "decode_combine launch");
     }
     return rs;
   };
-  if (!flat_applies) return run(false);
-  if (split_mode == 2) return run(flat_plan());
+  if (split_mode == 2) return run(flat_applies && flat_plan() ? 1 : 0);
+  if (split_mode >= 3) return run(longer_applies ? split_mode - 1 : 0);
+  if (!flat_applies && !longer_applies) return run(0);
+  // a recorded kind that still applies (a balanced one needs its launch worked out)
+  auto usable = [&](int kind) {
+    if (kind == 1) return flat_applies && flat_plan() ? 1 : 0;
+    return kind >= 2 && !longer_applies ? 0 : kind;
+  };
   // automatic: the recorded choice for this shape, else (autotuning, not capturing) measure
   const SplitKey key{{kv, dtype_q, batch, num_q_heads, h_kv, max_pages_per_seq, window, a.sink,
                       k_new ? 1 : 0, a.n_chunk_slots, 0}};
   {
     std::lock_guard<std::mutex> lk(g_tune_mu);
     auto it = g_tuned.find(key);
-    if (it != g_tuned.end()) return run(it->second && flat_plan());
+    if (it != g_tuned.end()) return run(usable(it->second));
   }
   int dev = -1;
   cudaStreamCaptureStatus cap_st = cudaStreamCaptureStatusNone;
   if (!g_autotune.load() || cudaGetDevice(&dev) != cudaSuccess || dev != g_tune_dev ||
-      cudaStreamIsCapturing(s, &cap_st) != cudaSuccess || cap_st != cudaStreamCaptureStatusNone ||
-      !flat_plan())
-    return run(false);
-  // both splits, alternately, kTuneReps times each; the one whose decode kernel took the
-  // least time over its runs is recorded and gives this call's result (the appended row is
-  // written again each run). The combine is left out of the timing: in a step replayed from
-  // a graph it starts beside the decode's last CTAs, and its own work is small and similar.
-  float best[2] = {1e30f, 1e30f};
+      cudaStreamIsCapturing(s, &cap_st) != cudaSuccess || cap_st != cudaStreamCaptureStatusNone)
+    return run(0);
+  // every kind that applies, in turn, kTuneReps times each; the one whose decode kernel took
+  // the least time over its runs is recorded and gives this call's result (the appended row is
+  // written again each run). The combine is left out of the timing: in a step replayed from a
+  // graph it starts beside the decode's last CTAs, and its own work is small and similar.
+  int kinds[kTuneKinds], n_kinds = 0;
+  kinds[n_kinds++] = 0;
+  if (flat_applies && flat_plan()) kinds[n_kinds++] = 1;
+  if (longer_applies) {
+    kinds[n_kinds++] = 2;
+    kinds[n_kinds++] = 3;
+  }
+  if (n_kinds == 1) return run(0);
+  float best[kTuneKinds];
+  int pick = 0;
   {
     std::lock_guard<std::mutex> run_lk(g_tune_run_mu);
     {  // another thread may have timed this shape meanwhile
       std::lock_guard<std::mutex> lk(g_tune_mu);
       auto it = g_tuned.find(key);
-      if (it != g_tuned.end()) return run(it->second && flat_plan());
+      if (it != g_tuned.end()) return run(usable(it->second));
     }
     for (int rep = 0; rep < kTuneReps && st == PKV_OK; ++rep)
-      for (int f = 0; f < 2 && st == PKV_OK; ++f) st = run(f == 1, g_tune_ev[2 * rep + f]);
+      for (int f = 0; f < n_kinds && st == PKV_OK; ++f)
+        st = run(kinds[f], g_tune_ev[kTuneKinds * rep + f]);
     if (st != PKV_OK) return st;
     e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_status(e, "decode split autotune");
-    for (int rep = 0; rep < kTuneReps; ++rep)
-      for (int f = 0; f < 2; ++f) {
+    for (int f = 0; f < n_kinds; ++f) {
+      best[f] = 1e30f;
+      for (int rep = 0; rep < kTuneReps; ++rep) {
         float ms = 0.f;
-        if (cudaEventElapsedTime(&ms, g_tune_ev[2 * rep + f][0], g_tune_ev[2 * rep + f][1]) ==
-            cudaSuccess)
-          best[f] = std::min(best[f], ms);
+        cudaEvent_t* ev = g_tune_ev[kTuneKinds * rep + f];
+        if (cudaEventElapsedTime(&ms, ev[0], ev[1]) == cudaSuccess) best[f] = std::min(best[f], ms);
       }
+      if (best[f] < best[pick]) pick = f;
+    }
     std::lock_guard<std::mutex> lk(g_tune_mu);
-    g_tuned[key] = best[1] < best[0];
+    g_tuned[key] = kinds[pick];
   }
-  return run(best[1] < best[0]);
+  return run(kinds[pick]);
 }
 
 int pkv_paged_decode_attention(const void* q, int32_t dtype_q, int32_t batch,

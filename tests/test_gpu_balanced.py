@@ -166,7 +166,7 @@ def test_balanced_flags_bad_pages_and_cut_contexts():
     assert _err(out, oracle_expected(w)) <= 1e-2
 
 
-def test_autotuned_split_is_one_of_the_two_and_is_kept():
+def test_autotuned_split_is_one_of_the_candidates_and_is_kept():
     pkv.decode_set_split(0)
     pkv.decode_autotune_reset()
     lens = [3000, 40, 1800, 700, 2500, 90, 1200, 4000]
@@ -180,11 +180,11 @@ def test_autotuned_split_is_one_of_the_two_and_is_kept():
         pkv.decode_set_autotune(True)
         tuned = sc.decode().clone()
         choice = pkv.decode_split_choice(*key)
-        assert choice in (0, 1)
+        assert choice in (0, 1, 2, 3)
         again = sc.decode().clone()  # the recorded split, no timing
     finally:
         pkv.decode_set_autotune(False)
-    pkv.decode_set_split(2 if choice == 1 else 1)
+    pkv.decode_set_split({0: 1, 1: 2, 2: 3, 3: 4}[choice])  # the same split, forced
     fixed = sc.decode().clone()
     torch.cuda.synchronize()
     assert pkv.device_error() == 0
@@ -223,3 +223,40 @@ def test_autotune_does_not_time_inside_graph_capture():
     torch.cuda.synchronize()
     assert pkv.device_error() == 0
     assert torch.equal(captured, chunked)
+
+
+@pytest.mark.parametrize("mode", [3, 4], ids=["chunks_x1.5", "chunks_x2"])
+@pytest.mark.parametrize("kv,qd,h_q,h_kv,lens", [
+    ("bf16", "bf16", 32, 8, [1, 16, 17, 31, 32, 33, 511, 512, 513, 1000, 3000]),
+    ("fp8_e4m3", "bf16", 32, 8, [40, 700, 1, 2000, 5000]),
+    ("int8", "f32", 32, 4, [77, 260, 1600]),
+    ("bf16", "bf16", 64, 8, [300, 2049, 17]),
+])
+def test_longer_chunks_match_oracle_and_fused_step(mode, kv, qd, h_q, h_kv, lens):
+    # chunks 1.5 or 2 times the automatic length, in the same partial slots
+    w = workloads.custom("longer_chunks", 15900 + h_q + len(lens), len(lens), h_q, h_kv, 128, kv,
+                         qd, lens)
+    pkv.decode_set_split(mode)
+    a = Scenario(w)
+    out_a = a.step().clone()
+    b = Scenario(w)
+    out_b = b.fused_step().clone()
+    again = b.decode().clone()
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    assert torch.equal(out_a, out_b) and torch.equal(out_b, again)
+    assert torch.equal(a.cache.k.view(torch.uint8), b.cache.k.view(torch.uint8))
+    assert _err(out_b, oracle_expected(w)) <= tolerance(w)
+
+
+@pytest.mark.parametrize("mode", [3, 4])
+def test_longer_chunks_window(mode):
+    lens = [3000, 1100, 50, 2500, 1024, 4000]
+    w = workloads.custom("longer_window", 15950 + mode, len(lens), 32, 8, 128, "bf16", "bf16",
+                         lens)
+    pkv.decode_set_split(mode)
+    sc = Scenario(w)
+    out = sc.fused_step(window=1024, sink_tokens=4).clone()
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    assert _err(out, oracle_expected(w, sink=4, window=1024)) <= 1e-2
