@@ -458,6 +458,15 @@ def recorded_traffic(split):
     return None
 
 
+def set_split(pkv, args):
+    """auto: the decode's split (chunks, longer chunks or balanced) is measured on the first
+    call of the shape (autotuning); otherwise the one named."""
+    if args.split == "auto":
+        pkv.decode_set_autotune(True)
+    else:
+        pkv.decode_set_split({"chunks": 1, "balanced": 2, "chunks-x1.5": 3, "chunks-x2": 4}[args.split])
+
+
 def run_ours(args):
     import torch
     import paged_kv_cache_271_gb300 as pkv
@@ -469,8 +478,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     init_dist(ws, "nccl")
     pkv.lib()  # fail loudly if the library is missing
-    # the decode's split (chunks or balanced) is measured on the first call of the shape
-    pkv.decode_set_autotune(True)
+    set_split(pkv, args)
 
     sc = StepState(args.workload, dev)
     stream = torch.cuda.current_stream()
@@ -497,7 +505,8 @@ def run_ours(args):
         sc.fused_step(pool=i % n_sets)
     torch.cuda.synchronize()
     assert pkv.device_error() == 0
-    sc.config["split"] = sc.split_label()
+    sc.config["split"] = (sc.split_label() if args.split == "auto"
+                          else args.split + " (fixed by --split)")
 
     # The step's device work (append, decode, combine) is captured once as a CUDA graph (one
     # per pool copy) and replayed every step, as a serving loop would; the host slot mapping
@@ -1078,7 +1087,7 @@ def run_trace(args):
     dev = torch.device("cuda", local)
     init_dist(ws, "nccl")
     pkv.lib()
-    pkv.decode_set_autotune(True)  # as in run_ours
+    set_split(pkv, args)
     coded = "int8" if args.workload.startswith("int8") else "fp8_e4m3"
     n_warm, n = max(3, args.warmup), max(1, args.steps)
     tr = workloads.fp8_continuous_batching(steps=n_warm + n)
@@ -1303,6 +1312,8 @@ def main(argv=None):
                     help="rotate: copies of the pools used in turn (at least 3 x L2 of other "
                          "copies between two reads of one); flush: write 256 MiB before every "
                          "timed step")
+    ap.add_argument("--split", choices=["auto", "chunks", "balanced", "chunks-x1.5", "chunks-x2"],
+                    default="auto", help="the decode's split: measured per shape (auto) or fixed")
     ap.add_argument("--workload", choices=WORKLOADS, default="llama3_8b_b64",
                     help="the default is the headline layer; the others are for measurement")
     args = ap.parse_args(argv)
