@@ -191,6 +191,18 @@ def test_workspace_size_and_chunk_policy():
                                                                   256 * 8)
     finally:
         pkv.decode_set_chunk_pages(0)
+    # the balanced split keeps the requests' page offsets in shared memory, for at most 2048
+    # requests: a larger batch has no balanced region (the size of the same 64-page chunks
+    # chosen by hand), a batch of 2048 still has one
+    assert pkv.decode_chunk_pages(2049, 8, 69) == 64
+    auto_2049 = pkv.decode_workspace_size(2049, 32, 8, 128, 69)
+    auto_2048 = pkv.decode_workspace_size(2048, 32, 8, 128, 69)
+    pkv.decode_set_chunk_pages(64)
+    try:
+        assert auto_2049 == pkv.decode_workspace_size(2049, 32, 8, 128, 69)
+        assert auto_2048 > pkv.decode_workspace_size(2048, 32, 8, 128, 69)
+    finally:
+        pkv.decode_set_chunk_pages(0)
     # everything fits one chunk: no workspace
     assert pkv.decode_workspace_size(2, 4, 2, 64, 3) == 0
     pkv.decode_set_chunk_pages(2)

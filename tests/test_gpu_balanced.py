@@ -105,6 +105,27 @@ def test_balanced_split_with_empty_requests():
     assert float(np.abs(got - ref).max()) <= 1e-2
 
 
+def test_balanced_split_above_its_batch_limit_takes_the_chunks():
+    # the balanced split keeps the requests' page offsets in shared memory, for at most 2048
+    # requests; a larger batch with the balanced split forced runs the chunks, bit for bit
+    rng = np.random.default_rng(15600)
+    lens = [int(x) for x in rng.integers(1, 48, size=2049)]
+    lens[7] = 1100  # a table 69 pages wide: two chunk slots
+    w = workloads.custom("balanced_big_batch", 15600, len(lens), 32, 8, 128, "bf16", "bf16", lens)
+    sc = Scenario(w)
+    sc.append()
+    out = sc.decode().clone()
+    pkv.decode_set_split(1)
+    chunked = sc.decode().clone()
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    assert torch.equal(out, chunked)
+    pairs = [(7, h) for h in range(32)] + [(b, (5 * b) % 32) for b in range(0, 2049, 41)]
+    ref = oracle_expected(w, pairs=pairs)
+    got = out.float().cpu().numpy()[[b for b, _ in pairs], [h for _, h in pairs]]
+    assert float(np.abs(got - ref).max()) <= tolerance(w)
+
+
 @pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3", "int8"])
 def test_balanced_fused_step_equals_append_then_decode(kv):
     lens = [1, 2000, 33, 700, 16, 1500, 900, 64]
