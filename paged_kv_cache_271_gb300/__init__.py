@@ -729,7 +729,8 @@ def decode_set_split(mode: int):
 
 
 def decode_set_autotune(on: bool):
-    """Time both splits on the first call of each shape and keep the faster (pkv.h)."""
+    """Time every split that applies on the first call of each shape and keep the fastest
+    (pkv.h)."""
     _check(lib().pkv_decode_set_autotune(1 if on else 0))
 
 
