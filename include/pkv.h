@@ -23,6 +23,11 @@
  *  - stream is a cudaStream_t (NULL = the legacy default stream). GPU work is enqueued
  *    asynchronously on it; argument errors are detected on the host before anything is
  *    launched and nothing is launched then.
+ *  - The GPU entry points may be called from several host threads at once (their launch
+ *    caches and the split autotuner's records are locked). A call works on the device current
+ *    in its thread and, if that thread has no CUDA context yet, makes the device's primary
+ *    context current there (cudaSetDevice); a context already current is left as it is. The
+ *    host-side objects (allocator, request tables, prefix cache) are not thread-safe.
  *  - Device-side faults of the data (a page id or slot outside the pool) never trap: the
  *    kernel skips the access and sets a bit in the device error word of the current device,
  *    which pkv_device_error() reads and clears.

@@ -77,6 +77,33 @@ cudaError_t traced(const char* name, cudaStream_t s, F&& launch) {
 
 }  // namespace
 
+void* current_context() {
+  using CtxGetCurrent = CUresult (*)(CUcontext*);
+  static const CtxGetCurrent fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<CtxGetCurrent>(f);
+  }();
+  CUcontext c = nullptr;
+  if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
+
+int bind_context(const char* who) {
+  if (current_context()) return PKV_OK;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaSetDevice(dev);  // initialises the primary context, current
+  if (e != cudaSuccess)
+    return set_error(PKV_ECUDA, "%s: no context for device %d: %s", who, dev,
+                     cudaGetErrorString(e));
+  return PKV_OK;
+}
+
 cudaError_t traced_copy(const char* name, void* dst, const void* src, size_t bytes,
                         cudaMemcpyKind kind, cudaStream_t s) {
   return traced(name, s, [&] { return cudaMemcpyAsync(dst, src, bytes, kind, s); });
@@ -177,6 +204,9 @@ int pool_tensor_map(const void* base, const pkv_cache_desc* d, CUtensorMap* out,
       return set_error(PKV_ECUDA, "cuTensorMapEncodeTiled is not available");
     g_encode = reinterpret_cast<EncodeTiledFn>(fn);
   }
+  // (the encoder needs a current context; a new host thread may not have one yet)
+  const int bst = bind_context("pool tensor map");
+  if (bst != PKV_OK) return bst;
   MapEntry e{};
   e.dev = dev;
   e.base = base;

@@ -40,26 +40,7 @@ constexpr int kMaxDevices = 64;
 
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
-CUcontext g_scratch_ctx[kMaxDevices] = {};  // the context each address was looked up in
-
-using CtxGetCurrent = CUresult (*)(CUcontext*);
-
-// The driver's current context (cuCtxGetCurrent, through the runtime's entry-point lookup so
-// the library needs no link against the driver library), or nullptr if unavailable.
-CUcontext current_context() {
-  static CtxGetCurrent fn = [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      f = nullptr;
-    return reinterpret_cast<CtxGetCurrent>(f);
-  }();
-  CUcontext c = nullptr;
-  if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
-  return c;
-}
+void* g_scratch_ctx[kMaxDevices] = {};  // the context each address was looked up in
 
 // Device address of the scratch on the current device. The array's name is only a host-side
 // stand-in in host code, so the address must come from cudaGetSymbolAddress: once per device,
@@ -71,7 +52,7 @@ int scratch_address(void** out) {
   if (dev < 0 || dev >= kMaxDevices) return set_error(PKV_ECUDA, "device index %d", dev);
   // (no context yet on this thread: the lookup below creates the device's primary context,
   // and the next call, finding that context, looks the address up once more)
-  const CUcontext ctx = current_context();
+  void* const ctx = current_context();
   std::lock_guard<std::mutex> lk(g_scratch_mu);
   if (!g_scratch_ptr[dev] || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
