@@ -38,10 +38,11 @@ def _widen(sc, width):
 @pytest.mark.parametrize("split", [1, 2, 3, 4], ids=["chunks", "balanced", "chunks_x1.5",
                                                      "chunks_x2"])
 @pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
-def test_graph_replayed_steps_follow_the_tables_and_lengths(kv, split):
+@pytest.mark.parametrize("sink,window", [(0, 0), (4, 256)], ids=["full", "window"])
+def test_graph_replayed_steps_follow_the_tables_and_lengths(kv, split, sink, window):
     lens = [15, 16, 31, 700, 1000, 2047, 2048, 33]
-    w = workloads.custom("graph_steps", 16500 + split + 10 * len(kv), len(lens), 32, 8, 128, kv,
-                         "bf16", lens)
+    w = workloads.custom("graph_steps", 16500 + split + 10 * len(kv) + window, len(lens), 32, 8,
+                         128, kv, "bf16", lens)
     pkv.decode_set_split(split)
     a, b = Scenario(w), Scenario(w)
     width = a.block_tables.shape[1] + 2  # room for the pages the steps below add
@@ -52,7 +53,7 @@ def test_graph_replayed_steps_follow_the_tables_and_lengths(kv, split):
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=side):
-        b.fused_step(stream=side)
+        b.fused_step(stream=side, window=window, sink_tokens=sink)
     gen = torch.Generator(device="cuda")
     gen.manual_seed(16500 + split)
     B, h_kv, d = w.batch, w.num_kv_heads, w.head_dim
@@ -74,7 +75,7 @@ def test_graph_replayed_steps_follow_the_tables_and_lengths(kv, split):
             b.block_tables.copy_(bt)
             b.context_lens.copy_(cl)
             torch.cuda.synchronize()
-        eager = a.fused_step().clone()
+        eager = a.fused_step(window=window, sink_tokens=sink).clone()
         g.replay()
         torch.cuda.synchronize()
         assert pkv.device_error() == 0
