@@ -24,6 +24,7 @@ def _modes():
     pkv.device_error()
     yield
     pkv.decode_set_split(0)
+    pkv.decode_set_kernel(0)
 
 
 def _err(out, ref):
@@ -113,3 +114,42 @@ def test_misaligned_rows_pools_and_workspace_are_refused_before_any_launch():
     torch.cuda.synchronize()
     assert pkv.device_error() == 0
     assert torch.equal(sc.cache.k.view(torch.uint8), before_k)  # the refused step wrote nothing
+
+
+@pytest.mark.parametrize("split", [1, 2, 3, 4])
+@pytest.mark.parametrize("kernel", [1, 2], ids=["cuda_cores", "tensor_cores"])
+def test_every_context_empty(kernel, split):
+    # a table wide enough to split, but no request has a token: zero outputs, nothing appended
+    lens = [1200, 30, 2100, 5]
+    w = workloads.custom("all_empty", 16600 + split, len(lens), 32, 8, 128, "bf16", "bf16", lens)
+    pkv.decode_set_kernel(kernel)
+    pkv.decode_set_split(split)
+    sc = Scenario(w)
+    zero = torch.zeros_like(sc.context_lens)
+    k_before = sc.cache.k.view(torch.uint8).clone()
+    out = torch.full_like(sc.q, 7.0)
+    pkv.paged_decode_attention(sc.q, sc.cache.k, sc.cache.v, sc.block_tables, zero, w.scale,
+                               out=out, workspace=sc.workspace)
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    assert int(torch.count_nonzero(out)) == 0
+    out.fill_(7.0)
+    pkv.paged_decode_step(sc.q, sc.k_new, sc.v_new, sc.cache.k, sc.cache.v, sc.block_tables,
+                          zero, w.scale, out=out, workspace=sc.workspace)
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    assert int(torch.count_nonzero(out)) == 0
+    assert torch.equal(sc.cache.k.view(torch.uint8), k_before)
+
+
+def test_empty_batch_launches_nothing():
+    w = workloads.custom("empty_batch", 16700, 2, 32, 8, 128, "bf16", "bf16", [300, 40])
+    sc = Scenario(w)
+    q = sc.q[:0]
+    out = pkv.paged_decode_attention(q, sc.cache.k, sc.cache.v, sc.block_tables[:0],
+                                     sc.context_lens[:0], w.scale)
+    assert out.shape == q.shape
+    out = pkv.paged_decode_step(q, sc.k_new[:0], sc.v_new[:0], sc.cache.k, sc.cache.v,
+                                sc.block_tables[:0], sc.context_lens[:0], w.scale)
+    torch.cuda.synchronize()
+    assert out.shape == q.shape and pkv.device_error() == 0
