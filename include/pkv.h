@@ -20,6 +20,8 @@
  *  - "device" pointers are CUDA device (or managed) memory owned by the caller; "host"
  *    pointers are ordinary host memory owned by the caller. The library never keeps a
  *    pointer after a call returns and never allocates device memory.
+ *  - A call with nothing to do (a batch or token count of 0) returns PKV_OK at once and
+ *    launches nothing; its buffer pointers may then be NULL (empty tensors have no storage).
  *  - stream is a cudaStream_t (NULL = the legacy default stream). GPU work is enqueued
  *    asynchronously on it; argument errors are detected on the host before anything is
  *    launched and nothing is launched then.

@@ -847,7 +847,8 @@ int pkv_paged_decode_step(const void* q, int32_t dtype_q, int32_t batch, int32_t
                           const int32_t* context_lens, float scale, const float* k_scales,
                           const float* v_scales, void* out, void* workspace,
                           size_t workspace_bytes, void* stream) {
-  if (!k_new) return set_error(PKV_EINVAL, "pkv_paged_decode_step: k_new is NULL");
+  if (!k_new && batch != 0)  // (an empty batch may pass null pointers)
+    return set_error(PKV_EINVAL, "pkv_paged_decode_step: k_new is NULL");
   return decode_impl("pkv_paged_decode_step", q, dtype_q, batch, num_q_heads, k_cache, v_cache,
                      desc, block_tables, max_pages_per_seq, context_lens, scale, k_scales,
                      v_scales, out, workspace, workspace_bytes, k_new, v_new, dtype_new, 0, 0,
@@ -862,7 +863,8 @@ int pkv_paged_decode_step_window(const void* q, int32_t dtype_q, int32_t batch,
                                  float scale, const float* k_scales, const float* v_scales,
                                  int32_t sink_tokens, int32_t window, void* out, void* workspace,
                                  size_t workspace_bytes, void* stream) {
-  if (!k_new) return set_error(PKV_EINVAL, "pkv_paged_decode_step_window: k_new is NULL");
+  if (!k_new && batch != 0)
+    return set_error(PKV_EINVAL, "pkv_paged_decode_step_window: k_new is NULL");
   return decode_impl("pkv_paged_decode_step_window", q, dtype_q, batch, num_q_heads, k_cache,
                      v_cache, desc, block_tables, max_pages_per_seq, context_lens, scale,
                      k_scales, v_scales, out, workspace, workspace_bytes, k_new, v_new,
@@ -945,7 +947,8 @@ int pkv_cascade_decode_step(const void* q, int32_t dtype_q, int32_t batch, int32
                             const int32_t* context_lens, float scale,
                             const pkv_cascade_desc* groups, void* out, void* workspace,
                             size_t workspace_bytes, void* stream) {
-  if (!k_new) return set_error(PKV_EINVAL, "pkv_cascade_decode_step: k_new is NULL");
+  if (!k_new && batch != 0)
+    return set_error(PKV_EINVAL, "pkv_cascade_decode_step: k_new is NULL");
   return decode_impl("pkv_cascade_decode_step", q, dtype_q, batch, num_q_heads, k_cache,
                      v_cache, desc, block_tables, max_pages_per_seq, context_lens, scale, nullptr,
                      nullptr, out, workspace, workspace_bytes, k_new, v_new, dtype_new, 0, 0,
