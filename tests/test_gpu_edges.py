@@ -153,3 +153,18 @@ def test_empty_batch_launches_nothing():
                                 sc.block_tables[:0], sc.context_lens[:0], w.scale)
     torch.cuda.synchronize()
     assert out.shape == q.shape and pkv.device_error() == 0
+
+
+@pytest.mark.parametrize("kernel,split", [(1, 1), (2, 1), (2, 2), (2, 3), (2, 4)])
+def test_contexts_around_8192_tokens(kernel, split):
+    # a partial last page (8191), exactly full pages (8192), one token onto a new page (8193)
+    lens = [8191, 8192, 8193, 1, 15]
+    w = workloads.custom("ctx8k", 16800 + 10 * kernel + split, len(lens), 32, 8, 128, "bf16",
+                         "bf16", lens)
+    pkv.decode_set_kernel(kernel)
+    pkv.decode_set_split(split)
+    sc = Scenario(w)
+    out = sc.fused_step().clone()
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    assert _err(out, oracle_expected(w)) <= tolerance(w)
