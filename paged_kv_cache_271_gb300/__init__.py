@@ -202,6 +202,11 @@ def _dtype_code(t: torch.Tensor) -> int:
 def _dev(t: torch.Tensor, name: str):
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise PkvError(-1, "%s must be a CUDA tensor" % name)
+    if t.device.index != torch.cuda.current_device():
+        # the library launches on the current device, whose kernels cannot read another GPU's
+        # memory without peer access
+        raise PkvError(-1, "%s is on %s but the current device is cuda:%d" %
+                       (name, t.device, torch.cuda.current_device()))
     if not t.is_contiguous():
         raise PkvError(-1, "%s must be contiguous" % name)
     return ctypes.c_void_p(t.data_ptr())
