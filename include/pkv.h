@@ -17,8 +17,9 @@
  * Conventions for every entry point
  *  - Return value: PKV_OK (0) or a negative pkv_status. No exception or abort crosses the
  *    ABI. pkv_last_error() gives a message for the calling thread's last failure.
- *  - "device" pointers are CUDA device (or managed) memory owned by the caller; "host"
- *    pointers are ordinary host memory owned by the caller. The library never keeps a
+ *  - "device" pointers are CUDA device (or managed) memory of the current device, owned by
+ *    the caller (kernels are launched on the current device); "host" pointers are ordinary
+ *    host memory owned by the caller. The library never keeps a
  *    pointer after a call returns and never allocates device memory.
  *  - A call with nothing to do (a batch or token count of 0) returns PKV_OK at once and
  *    launches nothing; its buffer pointers may then be NULL (empty tensors have no storage).
