@@ -19,10 +19,10 @@
  *    ABI. pkv_last_error() gives a message for the calling thread's last failure.
  *  - "device" pointers are CUDA device (or managed) memory of the current device, owned by
  *    the caller (kernels are launched on the current device); "host" pointers are ordinary
- *    host memory owned by the caller. No pointer is used after the call that received it
- *    returns (the TMA descriptors of a pool are cached by its address and shape, and a new
- *    pool at the same address with the same shape reuses them correctly); the library never
- *    allocates device memory.
+ *    host memory owned by the caller. A pointer is used only by the call that received it
+ *    and by the GPU work that call enqueues (the TMA descriptors of a pool are cached by its
+ *    address and shape; a new pool at the same address with the same shape reuses them
+ *    correctly). The library never allocates device memory.
  *  - A call with nothing to do (a batch or token count of 0) returns PKV_OK at once and
  *    launches nothing; its buffer pointers may then be NULL (empty tensors have no storage).
  *  - stream is a cudaStream_t (NULL = the legacy default stream). GPU work is enqueued
