@@ -105,6 +105,25 @@ def test_balanced_split_with_empty_requests():
     assert float(np.abs(got - ref).max()) <= 1e-2
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_balanced_split_at_its_batch_limit(kv):
+    # 2048 requests: the most page offsets the balanced split holds in shared memory
+    rng = np.random.default_rng(15650)
+    lens = [int(x) for x in rng.integers(1, 200, size=2048)]
+    lens[100] = 1500
+    lens[2047] = 1100
+    w = workloads.custom("balanced_2048", 15650 + len(kv), len(lens), 32, 8, 128, kv, "bf16", lens)
+    sc = Scenario(w)
+    out = sc.fused_step().clone()
+    torch.cuda.synchronize()
+    assert pkv.device_error() == 0
+    pairs = ([(100, h) for h in range(32)] + [(2047, h) for h in range(32)] +
+             [(b, (3 * b) % 32) for b in range(0, 2048, 37)])
+    ref = oracle_expected(w, pairs=pairs)
+    got = out.float().cpu().numpy()[[b for b, _ in pairs], [h for _, h in pairs]]
+    assert float(np.abs(got - ref).max()) <= tolerance(w)
+
+
 def test_balanced_split_above_its_batch_limit_takes_the_chunks():
     # the balanced split keeps the requests' page offsets in shared memory, for at most 2048
     # requests; a larger batch with the balanced split forced runs the chunks, bit for bit
