@@ -905,13 +905,13 @@ int pkv_paged_decode_step_packed(const void* host_in, void* dev_in, int32_t batc
   const char* who = "pkv_paged_decode_step_packed";
   int st = check_desc(desc, who);
   if (st != PKV_OK) return st;
-  if (!host_in || !dev_in || !out_dev || !out_host)
-    return set_error(PKV_EINVAL, "%s: null pointer", who);
   size_t off[5], total = 0;
   st = pkv_packed_step_layout(batch, num_q_heads, desc->num_kv_heads, desc->head_dim,
                               max_pages_per_seq, dtype_q, dtype_new, off, &total);
   if (st != PKV_OK) return st;
-  if (batch == 0) return PKV_OK;
+  if (batch == 0) return PKV_OK;  // (an empty batch may pass null buffers)
+  if (!host_in || !dev_in || !out_dev || !out_host)
+    return set_error(PKV_EINVAL, "%s: null pointer", who);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = traced_copy("h2d_copy", dev_in, host_in, total, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_status(e, "packed step inputs copy");

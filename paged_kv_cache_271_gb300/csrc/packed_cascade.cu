@@ -50,13 +50,14 @@ int pkv_cascade_decode_step_packed(void* host_in, void* dev_in, int32_t batch,
                                    size_t* workspace_needed, int32_t* n_groups_out,
                                    void* stream) {
   const char* who = "pkv_cascade_decode_step_packed";
-  if (!host_in || !dev_in || !out_dev || !out_host || !desc)
-    return pkv::set_error(PKV_EINVAL, "%s: null pointer", who);
+  if (!desc) return pkv::set_error(PKV_EINVAL, "%s: desc is NULL", who);
   size_t off[11], total = 0;
   int st = pkv_packed_cascade_layout(batch, num_q_heads, desc->num_kv_heads, desc->head_dim,
                                      max_pages_per_seq, dtype_q, dtype_new, off, &total);
   if (st != PKV_OK) return st;
-  if (batch == 0) return PKV_OK;
+  if (batch == 0) return PKV_OK;  // (an empty batch may pass null buffers)
+  if (!host_in || !dev_in || !out_dev || !out_host)
+    return pkv::set_error(PKV_EINVAL, "%s: null pointer", who);
   char* h = static_cast<char*>(host_in);
   char* d = static_cast<char*>(dev_in);
   auto hp = [&](int i) { return reinterpret_cast<int32_t*>(h + off[i]); };

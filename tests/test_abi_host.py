@@ -496,3 +496,25 @@ def test_packed_cascade_layout_and_argument_errors():
     assert L.pkv_cascade_decode_step_packed(None, fake, 2, 8, pkv.BF16, pkv.BF16, fake, fake,
                                             ctypes.byref(d), 4, 0.1, fake, fake, None, 0, None,
                                             None, None) == -1  # null host block
+
+
+def test_empty_batches_need_no_buffers():
+    # nothing to do: PKV_OK before any buffer (all NULL here) is looked at or anything launched
+    L = pkv.lib()
+    d = _desc(cache_dtype=pkv.BF16, head_dim=128)
+    assert L.pkv_paged_decode_attention(None, pkv.BF16, 0, 4, None, None, ctypes.byref(d), None,
+                                        16, None, 0.125, None, None, None, None, 0, None) == 0
+    assert L.pkv_paged_decode_step(None, pkv.BF16, 0, 4, None, None, pkv.BF16, None, None,
+                                   ctypes.byref(d), None, 16, None, 0.125, None, None, None,
+                                   None, 0, None) == 0
+    assert L.pkv_paged_decode_step_packed(None, None, 0, 4, pkv.BF16, pkv.BF16, None, None,
+                                          ctypes.byref(d), 16, 0.125, None, None, 0, 0, None,
+                                          None, None, 0, None) == 0
+    n = ctypes.c_int32(-1)
+    assert L.pkv_cascade_decode_step_packed(None, None, 0, 4, pkv.BF16, pkv.BF16, None, None,
+                                            ctypes.byref(d), 16, 0.125, None, None, None, 0,
+                                            None, ctypes.byref(n), None) == 0
+    # a batch with work still needs its buffers
+    assert L.pkv_paged_decode_step_packed(None, None, 1, 4, pkv.BF16, pkv.BF16, None, None,
+                                          ctypes.byref(d), 16, 0.125, None, None, 0, 0, None,
+                                          None, None, 0, None) == -1
