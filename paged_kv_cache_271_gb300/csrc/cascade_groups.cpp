@@ -9,11 +9,26 @@
 // min_prefix_pages pages is dropped. Members keep batch order inside their group.
 #include <algorithm>
 #include <cstring>
-#include <unordered_map>
 #include <vector>
 
 #include "pkv.h"
 #include "pkv_host.h"
+
+namespace {
+
+// Per-thread scratch of the grouping, kept across calls so that a call allocates nothing once
+// the batch size has been seen: an open-addressing table from first page id to bucket (a slot
+// is live when its stamp equals the call's epoch, so the table is never cleared), and the
+// bucket arrays.
+struct GroupScratch {
+  std::vector<int32_t> key, val;
+  std::vector<uint32_t> stamp;
+  uint32_t epoch = 0;
+  std::vector<int32_t> bucket, count, start, flat, fill;
+};
+thread_local GroupScratch t_scratch;
+
+}  // namespace
 
 extern "C" int pkv_cascade_groups(const int32_t* block_tables, const int32_t* context_lens,
                                   int32_t batch, int32_t max_pages_per_seq, int32_t min_members,
@@ -37,27 +52,48 @@ extern "C" int pkv_cascade_groups(const int32_t* block_tables, const int32_t* co
   };
   // bucket of each request (by first page id, buckets numbered in order of first appearance),
   // then the members of every bucket in batch order, in one flat array (a counting pass)
-  std::unordered_map<int32_t, int32_t> bucket_of;  // first page id -> bucket
-  bucket_of.reserve((size_t)batch * 2);
-  std::vector<int32_t> bucket(batch, -1), count, start;
+  GroupScratch& w = t_scratch;
+  size_t slots = 16;
+  while (slots < (size_t)batch * 2) slots *= 2;
+  if (w.key.size() < slots) {
+    w.key.assign(slots, 0);
+    w.val.assign(slots, 0);
+    w.stamp.assign(slots, 0);
+    w.epoch = 0;
+  }
+  if (++w.epoch == 0) {  // the stamps wrapped: forget them all once
+    std::fill(w.stamp.begin(), w.stamp.end(), 0u);
+    w.epoch = 1;
+  }
+  const size_t mask = slots - 1;
+  w.bucket.assign(batch, -1);
+  w.count.clear();
   for (int32_t b = 0; b < batch; ++b) {
     group_of[b] = -1;
     if (cap(b) < min_prefix_pages) continue;
     const int32_t first = block_tables[(size_t)b * max_pages_per_seq];
-    auto ins = bucket_of.emplace(first, (int32_t)count.size());
-    if (ins.second) count.push_back(0);
-    bucket[b] = ins.first->second;
-    ++count[bucket[b]];
+    size_t i = ((uint32_t)first * 2654435761u) & mask;  // multiplicative hash, linear probing
+    while (w.stamp[i] == w.epoch && w.key[i] != first) i = (i + 1) & mask;
+    if (w.stamp[i] != w.epoch) {  // a new first page: the next bucket
+      w.stamp[i] = w.epoch;
+      w.key[i] = first;
+      w.val[i] = (int32_t)w.count.size();
+      w.count.push_back(0);
+    }
+    w.bucket[b] = w.val[i];
+    ++w.count[w.bucket[b]];
   }
+  const std::vector<int32_t>& bucket = w.bucket;
+  const std::vector<int32_t>& count = w.count;
   const int32_t nb = (int32_t)count.size();
+  std::vector<int32_t>& start = w.start;
   start.assign(nb + 1, 0);
   for (int32_t k = 0; k < nb; ++k) start[k + 1] = start[k] + count[k];
-  std::vector<int32_t> flat(start[nb]);
-  {
-    std::vector<int32_t> fill(start.begin(), start.end() - 1);
-    for (int32_t b = 0; b < batch; ++b)
-      if (bucket[b] >= 0) flat[fill[bucket[b]]++] = b;
-  }
+  std::vector<int32_t>& flat = w.flat;
+  flat.resize(start[nb]);
+  w.fill.assign(start.begin(), start.end() - 1);
+  for (int32_t b = 0; b < batch; ++b)
+    if (bucket[b] >= 0) flat[w.fill[bucket[b]]++] = b;
   int32_t ng = 0, nm = 0, mm = 0, mp = 0;
   group_offsets[0] = 0;
   for (int32_t k = 0; k < nb; ++k) {
