@@ -545,7 +545,9 @@ typedef struct {
  * [batch], prefix_pages [batch], group_offsets [batch + 1], group_members [batch], own_start
  * [batch] (may be NULL), and the
  * counts and bounds of a pkv_cascade_desc (*n_groups may be 0; *max_own_pages counts the pages
- * of a context cut to the table width).
+ * of a context cut to the table width). Its working arrays are kept per host thread between
+ * calls (a call allocates nothing once a batch of that size has been seen); calls from
+ * different threads do not share them.
  */
 int pkv_cascade_groups(const int32_t* block_tables, const int32_t* context_lens, int32_t batch,
                        int32_t max_pages_per_seq, int32_t min_members, int32_t min_prefix_pages,
