@@ -25,10 +25,12 @@ def _gpu():
 def _defaults():
     pkv.decode_set_chunk_pages(0)
     pkv.decode_set_kernel(0)
+    pkv.decode_set_split(0)
     pkv.device_error()
     yield
     pkv.decode_set_chunk_pages(0)
     pkv.decode_set_kernel(0)
+    pkv.decode_set_split(0)
 
 
 CASES = [
@@ -57,11 +59,13 @@ def test_window_decode_parity(kv, qd, h_q, h_kv, d, lens, sink, window, kernel, 
     assert err <= tolerance(w), err
 
 
-@pytest.mark.parametrize("kernel", [1, 2])
-def test_released_pages_are_never_read(kernel):
+# (split: 1 chunks, 2 balanced, 3 and 4 chunks 1.5 and 2 times longer)
+@pytest.mark.parametrize("kernel,split", [(1, 1), (2, 1), (2, 2), (2, 3), (2, 4)])
+def test_released_pages_are_never_read(kernel, split):
     w = workloads.custom("winrel", 5101, 6, 32, 8, 128, "bf16", "bf16",
                          [40, 700, 1000, 2049, 1, 513])
     pkv.decode_set_kernel(kernel)
+    pkv.decode_set_split(split)
     sink, window = 4, 100
     sc = Scenario(w)
     full = sc.fused_step(window=window, sink_tokens=sink).clone()
