@@ -44,13 +44,15 @@ WINDOWS = [(0, 1), (0, 16), (4, 64), (16, 100), (3, 500), (0, 4096)]
 
 @pytest.mark.parametrize("kv,qd,h_q,h_kv,d,lens", CASES)
 @pytest.mark.parametrize("sink,window", WINDOWS)
-@pytest.mark.parametrize("kernel,chunk", [(1, 0), (2, 0), (2, 3)])
-def test_window_decode_parity(kv, qd, h_q, h_kv, d, lens, sink, window, kernel, chunk):
+@pytest.mark.parametrize("kernel,chunk,split", [(1, 0, 0), (2, 0, 0), (2, 3, 0), (2, 0, 2)],
+                         ids=["cuda_cores", "tensor_cores", "tensor_cores_chunk3", "balanced"])
+def test_window_decode_parity(kv, qd, h_q, h_kv, d, lens, sink, window, kernel, chunk, split):
     if kernel == 2 and (kv == "f32" or d != 128):
         pytest.skip("the tensor-core decode serves bf16/FP8 caches with head_dim 128")
     w = workloads.custom("win", 5000 + h_q + len(lens), len(lens), h_q, h_kv, d, kv, qd, lens)
     pkv.decode_set_kernel(kernel)
     pkv.decode_set_chunk_pages(chunk)
+    pkv.decode_set_split(split)
     sc = Scenario(w)
     out = sc.fused_step(window=window, sink_tokens=sink).clone()
     assert pkv.device_error() == 0
