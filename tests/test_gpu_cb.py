@@ -98,3 +98,25 @@ def test_int8_continuous_batching_small_full_check():
 def test_int8_continuous_batching_full_size_sampled():
     tr = workloads.fp8_continuous_batching(steps=6)
     assert _run(tr, 6, full_check=False, cache_dtype="int8") > 0
+
+
+@pytest.mark.parametrize("split", [2, 3, 4], ids=["balanced", "chunks_x1.5", "chunks_x2"])
+def test_fp8_continuous_batching_small_full_check_other_splits(split):
+    pkv.decode_set_split(split)
+    try:
+        tr = workloads.fp8_continuous_batching(batch=16, steps=8, lo=128, hi=512, rep_lo=16,
+                                               rep_hi=400, p_finish=0.3)
+        assert _run(tr, 0, full_check=True) > 0
+    finally:
+        pkv.decode_set_split(0)
+
+
+@pytest.mark.parametrize("cache_dtype", ["fp8_e4m3", "int8"])
+def test_continuous_batching_batch64_balanced_sampled(cache_dtype):
+    # the batch-64 trace, where the balanced split is the measured choice
+    pkv.decode_set_split(2)
+    try:
+        tr = workloads.fp8_continuous_batching(batch=64, steps=6)
+        assert _run(tr, 6, full_check=False, cache_dtype=cache_dtype) > 0
+    finally:
+        pkv.decode_set_split(0)
