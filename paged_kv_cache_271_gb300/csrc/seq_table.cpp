@@ -53,6 +53,8 @@ struct pkv_seq_table {
   std::vector<int32_t> scratch;  // page lists of the current call
   std::vector<int32_t> ones;     // per-request counts of 1 (pkv_seq_step)
   std::vector<int64_t> slots;    // slots nobody asked for (pkv_seq_step)
+  std::vector<Seq*> live_seqs;   // the live requests' entries, looked up once (pkv_seq_step)
+  std::vector<Seq*> new_seqs;    // the new requests' entries (pkv_seq_step)
   // incremental table export (pkv_seq_step): the buffer and width it last wrote, and the
   // request whose row each of its rows holds
   mutable const int32_t* inc_buf = nullptr;  // (pkv_seq_tables into it forgets it)
@@ -65,7 +67,8 @@ extern "C" {
 int pkv_seq_table_create(pkv_allocator* a, int32_t page_size, pkv_seq_table** out) {
   if (!a || !out || page_size <= 0)
     return pkv::set_error(PKV_EINVAL, "pkv_seq_table_create: bad argument");
-  *out = new (std::nothrow) pkv_seq_table{a, page_size, {}, 0, {}, {}, {}, {}, nullptr, -1, {}};
+  *out = new (std::nothrow)
+      pkv_seq_table{a, page_size, {}, 0, {}, {}, {}, {}, {}, {}, nullptr, -1, {}};
   if (!*out) return pkv::set_error(PKV_EINVAL, "pkv_seq_table_create: out of host memory");
   return PKV_OK;
 }
@@ -98,6 +101,90 @@ int seq_add(pkv_seq_table* t, int64_t rid, const int32_t* shared_pages, int32_t 
   s.pages.assign(shared_pages, shared_pages + n_shared);
   s.len = shared_len;
   t->seqs.emplace(rid, std::move(s));
+  return PKV_OK;
+}
+
+// Grows the requests seqs[0 .. n) (distinct, counts >= 0: the caller checked) by counts[i]
+// tokens each: copy-on-write of a shared, partly filled page about to be written, then the new
+// pages and the new tokens' slots; nothing changes unless everything fits (rids: for messages).
+int reserve_seqs(pkv_seq_table* t, Seq* const* seqs, const int64_t* rids, const int32_t* counts,
+                 int32_t n, int64_t* slots_out, int32_t* copy_src, int32_t* copy_dst,
+                 int32_t* n_copies) {
+  const int32_t P = t->page_size;
+  // pass 1: checks, and the pages the batch will take (copies replay the reference counts)
+  std::unordered_map<int32_t, int32_t> dropped;  // shared page -> references given up by copies
+  int64_t total = 0, need_pages = 0;
+  bool any_copy = false;
+  for (int32_t i = 0; i < n; ++i) {
+    Seq& s = *seqs[i];
+    total += counts[i];
+    if (counts[i] > 0) {
+      const int64_t lp = s.len / P;
+      if (lp < (int64_t)s.pages.size()) {
+        const int32_t page = s.pages[lp];
+        if (page < 0)
+          return pkv::set_error(PKV_EINVAL, "pkv_seq_reserve: request %lld writes into a "
+                                "released page", (long long)rids[i]);
+        const int32_t ref = pkv_refcount(t->alloc, page);
+        if (ref <= 0)
+          return pkv::set_error(PKV_EREFCNT, "pkv_seq_reserve: page %d is not allocated", page);
+        if (ref > 1) {  // shared: copied unless every other holder copied it first
+          int32_t& d = dropped[page];
+          if (ref - d > 1) {
+            ++d;
+            ++need_pages;
+            any_copy = true;
+          }
+        }
+      }
+    }
+    const int64_t grow = pages_for(s.len + counts[i], P) - (int64_t)s.pages.size();
+    if (grow > 0) need_pages += grow;
+  }
+  if (total > 0 && !slots_out)
+    return pkv::set_error(PKV_EINVAL, "pkv_seq_reserve: slots_out is NULL");
+  if (any_copy && (!copy_src || !copy_dst))
+    return pkv::set_error(PKV_EINVAL, "pkv_seq_reserve: copy arrays are NULL");
+  if (need_pages > pkv_num_free(t->alloc))
+    return pkv::set_error(PKV_ENOPAGES, "pkv_seq_reserve: %lld pages needed, %d free",
+                          (long long)need_pages, pkv_num_free(t->alloc));
+  // pass 2: copy-on-write, growth and slots (nothing below can fail after pass 1)
+  int32_t nc = 0;
+  int64_t o = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    Seq& s = *seqs[i];
+    const int32_t c = counts[i];
+    if (c > 0) {
+      int32_t src = -1, dst = -1;
+      const int st = pkv_cow_page(t->alloc, s.pages.data(), (int32_t)s.pages.size(), s.len, P,
+                                  &src, &dst);
+      if (st != PKV_OK) return st;
+      if (src >= 0) {
+        copy_src[nc] = src;
+        copy_dst[nc] = dst;
+        ++nc;
+        s.changed(s.len / P);
+      }
+    }
+    const int64_t grow = pages_for(s.len + c, P) - (int64_t)s.pages.size();
+    if (grow > 0) {
+      const size_t old = s.pages.size();
+      s.changed((int64_t)old);
+      s.pages.resize(old + grow);
+      const int st = pkv_alloc(t->alloc, (int32_t)grow, s.pages.data() + old);
+      if (st != PKV_OK) return st;
+    }
+    // slots page by page: page * P + offset, consecutive within a page
+    const int64_t end = s.len + c;
+    for (int64_t pos = s.len; pos < end;) {
+      const int64_t lp = pos / P;
+      const int64_t base = (int64_t)s.pages[lp] * P - lp * P;
+      const int64_t stop = std::min<int64_t>(end, (lp + 1) * P);
+      for (; pos < stop; ++pos) slots_out[o++] = base + pos;
+    }
+    s.len = end;
+  }
+  *n_copies = nc;
   return PKV_OK;
 }
 
@@ -175,91 +262,19 @@ int pkv_seq_reserve(pkv_seq_table* t, const int64_t* rids, const int32_t* counts
                     int64_t* slots_out, int32_t* copy_src, int32_t* copy_dst, int32_t* n_copies) {
   if (!t || n < 0 || (n > 0 && (!rids || !counts)) || !n_copies)
     return pkv::set_error(PKV_EINVAL, "pkv_seq_reserve: bad argument");
-  const int32_t P = t->page_size;
-  // pass 1: checks, and the pages the batch will take (copies replay the reference counts)
   const uint64_t ep = ++t->epoch;
   std::vector<Seq*>& listed = t->listed;
   listed.clear();
-  std::unordered_map<int32_t, int32_t> dropped;  // shared page -> references given up by copies
-  int64_t total = 0, need_pages = 0;
-  bool any_copy = false;
   for (int32_t i = 0; i < n; ++i) {
     auto it = t->seqs.find(rids[i]);
     if (it == t->seqs.end() || it->second.mark == ep || counts[i] < 0)
       return pkv::set_error(PKV_EINVAL, "pkv_seq_reserve: request %lld unknown, listed twice or "
                             "with a negative count", (long long)rids[i]);
-    Seq& s = it->second;
-    s.mark = ep;
-    listed.push_back(&s);
-    total += counts[i];
-    if (counts[i] > 0) {
-      const int64_t lp = s.len / P;
-      if (lp < (int64_t)s.pages.size()) {
-        const int32_t page = s.pages[lp];
-        if (page < 0)
-          return pkv::set_error(PKV_EINVAL, "pkv_seq_reserve: request %lld writes into a "
-                                "released page", (long long)rids[i]);
-        const int32_t ref = pkv_refcount(t->alloc, page);
-        if (ref <= 0)
-          return pkv::set_error(PKV_EREFCNT, "pkv_seq_reserve: page %d is not allocated", page);
-        if (ref > 1) {  // shared: copied unless every other holder copied it first
-          int32_t& d = dropped[page];
-          if (ref - d > 1) {
-            ++d;
-            ++need_pages;
-            any_copy = true;
-          }
-        }
-      }
-    }
-    const int64_t grow = pages_for(s.len + counts[i], P) - (int64_t)s.pages.size();
-    if (grow > 0) need_pages += grow;
+    it->second.mark = ep;
+    listed.push_back(&it->second);
   }
-  if (total > 0 && !slots_out)
-    return pkv::set_error(PKV_EINVAL, "pkv_seq_reserve: slots_out is NULL");
-  if (any_copy && (!copy_src || !copy_dst))
-    return pkv::set_error(PKV_EINVAL, "pkv_seq_reserve: copy arrays are NULL");
-  if (need_pages > pkv_num_free(t->alloc))
-    return pkv::set_error(PKV_ENOPAGES, "pkv_seq_reserve: %lld pages needed, %d free",
-                          (long long)need_pages, pkv_num_free(t->alloc));
-  // pass 2: copy-on-write, growth and slots (nothing below can fail after pass 1)
-  int32_t nc = 0;
-  int64_t o = 0;
-  for (int32_t i = 0; i < n; ++i) {
-    Seq& s = *listed[i];
-    const int32_t c = counts[i];
-    if (c > 0) {
-      int32_t src = -1, dst = -1;
-      const int st = pkv_cow_page(t->alloc, s.pages.data(), (int32_t)s.pages.size(), s.len, P,
-                                  &src, &dst);
-      if (st != PKV_OK) return st;
-      if (src >= 0) {
-        copy_src[nc] = src;
-        copy_dst[nc] = dst;
-        ++nc;
-        s.changed(s.len / P);
-      }
-    }
-    const int64_t grow = pages_for(s.len + c, P) - (int64_t)s.pages.size();
-    if (grow > 0) {
-      const size_t old = s.pages.size();
-      s.changed((int64_t)old);
-      s.pages.resize(old + grow);
-      const int st = pkv_alloc(t->alloc, (int32_t)grow, s.pages.data() + old);
-      if (st != PKV_OK) return st;
-    }
-    // slots page by page: page * P + offset, consecutive within a page
-    const int64_t end = s.len + c;
-    for (int64_t pos = s.len; pos < end;) {
-      const int64_t lp = pos / P;
-      const int64_t base = (int64_t)s.pages[lp] * P - lp * P;
-      const int64_t stop = std::min<int64_t>(end, (lp + 1) * P);
-      for (; pos < stop; ++pos) slots_out[o++] = base + pos;
-    }
-    s.len = end;
-  }
-  *n_copies = nc;
-  return PKV_OK;
+  return reserve_seqs(t, listed.data(), rids, counts, n, slots_out, copy_src, copy_dst,
+                      n_copies);
 }
 
 int pkv_seq_tables(const pkv_seq_table* t, const int64_t* rids, int32_t n, int32_t width,
@@ -326,7 +341,10 @@ int pkv_seq_step(pkv_seq_table* t, const int64_t* free_rids, int32_t n_free,
   if (prompt_total > 0 && !prompt_slots_out)
     return pkv::set_error(PKV_EINVAL, "%s: prompt_slots_out is NULL", who);
   // live requests: distinct, live after the frees and adds, writable, and fitting the table
+  // (each existing one's entry is kept for the reserve and the export below: erasing or adding
+  // other entries of the map leaves it in place)
   const uint64_t ep_live = ++t->epoch;
+  t->live_seqs.assign(n_live, nullptr);
   for (int32_t i = 0; i < n_live; ++i) {
     int64_t len, pages;
     auto f = fresh.find(live_rids[i]);
@@ -344,6 +362,7 @@ int pkv_seq_step(pkv_seq_table* t, const int64_t* free_rids, int32_t n_free,
                               (long long)live_rids[i]);
       Seq& s = it->second;
       s.mark = ep_live;
+      t->live_seqs[i] = &s;
       len = s.len;
       pages = (int64_t)s.pages.size();
       const int64_t lp = len / P;
@@ -375,7 +394,11 @@ int pkv_seq_step(pkv_seq_table* t, const int64_t* free_rids, int32_t n_free,
   if (st != PKV_OK) return st;
   // ---- the new requests and their prompts, then one token for every live request; if the
   // pages run out, the new requests are removed again (their prompt pages go back) ----
-  for (int32_t i = 0; i < n_new; ++i) t->seqs.emplace(new_rids[i], Seq{});
+  t->new_seqs.resize(n_new);
+  for (int32_t i = 0; i < n_new; ++i)
+    t->new_seqs[i] = &t->seqs.emplace(new_rids[i], Seq{}).first->second;
+  for (int32_t i = 0; i < n_live; ++i)  // the new requests among the live ones
+    if (!t->live_seqs[i]) t->live_seqs[i] = &t->seqs.find(live_rids[i])->second;
   auto drop_new = [&]() {
     std::vector<int32_t> live;
     for (int32_t i = 0; i < n_new; ++i) {
@@ -388,8 +411,8 @@ int pkv_seq_step(pkv_seq_table* t, const int64_t* free_rids, int32_t n_free,
     }
   };
   int32_t none = 0;
-  st = pkv_seq_reserve(t, new_rids, prompt_counts, n_new, prompt_slots_out, nullptr, nullptr,
-                       &none);
+  st = reserve_seqs(t, t->new_seqs.data(), new_rids, prompt_counts, n_new, prompt_slots_out,
+                    nullptr, nullptr, &none);
   if (st != PKV_OK) {
     drop_new();
     return st;
@@ -401,8 +424,8 @@ int pkv_seq_step(pkv_seq_table* t, const int64_t* free_rids, int32_t n_free,
       t->slots.resize(n_live);
       slots = t->slots.data();
     }
-    st = pkv_seq_reserve(t, live_rids, t->ones.data(), n_live, slots, copy_src, copy_dst,
-                         n_copies);
+    st = reserve_seqs(t, t->live_seqs.data(), live_rids, t->ones.data(), n_live, slots,
+                      copy_src, copy_dst, n_copies);
     if (st != PKV_OK) {
       drop_new();
       return st;
@@ -421,7 +444,7 @@ int pkv_seq_step(pkv_seq_table* t, const int64_t* free_rids, int32_t n_free,
   }
   if ((int64_t)t->inc_owner.size() < n_live) t->inc_owner.resize(n_live, INT64_MIN);
   for (int32_t i = 0; i < n_live; ++i) {
-    Seq& s = t->seqs.find(live_rids[i])->second;
+    Seq& s = *t->live_seqs[i];
     int32_t* row = block_tables_out + (int64_t)i * width;
     const int64_t np = (int64_t)s.pages.size();
     if (t->inc_owner[i] == live_rids[i] && s.exp_row == i) {
