@@ -111,12 +111,11 @@ def test_fp8_continuous_batching_small_full_check_other_splits(split):
         pkv.decode_set_split(0)
 
 
-@pytest.mark.parametrize("cache_dtype", ["fp8_e4m3", "int8"])
-def test_continuous_batching_batch64_balanced_sampled(cache_dtype):
+def test_fp8_continuous_batching_batch64_balanced_sampled():
     # the batch-64 trace, where the balanced split is the measured choice
     pkv.decode_set_split(2)
     try:
-        tr = workloads.fp8_continuous_batching(batch=64, steps=6)
-        assert _run(tr, 6, full_check=False, cache_dtype=cache_dtype) > 0
+        tr = workloads.fp8_continuous_batching(batch=64, steps=5)
+        assert _run(tr, 6, full_check=False) > 0
     finally:
         pkv.decode_set_split(0)
